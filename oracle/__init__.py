@@ -1,0 +1,268 @@
+"""fp64 CPU oracle for the fused linear selected-token log-prob (test infrastructure).
+
+TEST INFRASTRUCTURE ONLY: the test suite, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg are the only callers.  The product package never
+imports this module, and this module never imports the product package: the
+two share no code.  The arithmetic lives in ``rlk_oracle.c`` (plain loops in
+IEEE double); this file only builds it, converts bf16 inputs to exact doubles
+and marshals arrays through ctypes.
+
+Every parity check in the suite pins the oracle first (closed forms,
+high-precision brute force on tiny vocabularies, central finite differences,
+hand-built audit vectors) before any GPU result is compared with it.
+
+ctypes drops the GIL for the duration of each foreign call, so the helpers
+``*_parallel`` below run independent rows of the (single-threaded) oracle on
+several host threads; the arithmetic of each row is unchanged.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "rlk_oracle.c")
+_LIB = os.path.join(_HERE, "librlk_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_fp = ctypes.POINTER(ctypes.c_float)
+_i64p = ctypes.POINTER(ctypes.c_int64)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+
+
+class AuditResult(ctypes.Structure):
+    _fields_ = [
+        ("active_count", ctypes.c_int64),
+        ("argmax_index", ctypes.c_int64),
+        ("max_abs_dlogp", ctypes.c_double),
+        ("mean_dlogp", ctypes.c_double),
+        ("approx_kl", ctypes.c_double),
+    ]
+
+
+def build(force: bool = False) -> str:
+    """Compile rlk_oracle.c with gcc (no fast-math, no FMA contraction)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".%d.tmp" % os.getpid()
+        cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+               "-std=c11", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            lib.rlk_oracle_linear_logp_fwd.restype = ctypes.c_int64
+            lib.rlk_oracle_linear_logp_fwd.argtypes = [
+                _dp, _dp, _i64p, _u8p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                ctypes.c_double, _dp, _dp]
+            for name in ("rlk_oracle_linear_logp_bwd_dh", "rlk_oracle_linear_logp_bwd_dw"):
+                f = getattr(lib, name)
+                f.restype = None
+                f.argtypes = [_dp, _dp, _i64p, _u8p, _dp, _dp, ctypes.c_int64, ctypes.c_int64,
+                              ctypes.c_int64, ctypes.c_double, ctypes.c_int64, ctypes.c_int64, _dp]
+            lib.rlk_oracle_dlogp_audit.restype = None
+            lib.rlk_oracle_dlogp_audit.argtypes = [_fp, _fp, _u8p, ctypes.c_int64,
+                                                   ctypes.POINTER(AuditResult)]
+            lib.rlk_oracle_grpo_clip_grad.restype = ctypes.c_double
+            lib.rlk_oracle_grpo_clip_grad.argtypes = [_dp, _dp, _dp, _u8p, ctypes.c_int64,
+                                                      ctypes.c_double, _dp]
+            _lib = lib
+    return _lib
+
+
+# ----------------------------------------------------------------------------- conversions
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """Exact conversion of bf16 bit patterns (uint16 array or torch bf16 tensor) to float64."""
+    if hasattr(bits, "view") and hasattr(bits, "dtype") and "bfloat16" in str(bits.dtype):
+        bits = bits.contiguous().view(dtype=__import__("torch").int16).numpy().view(np.uint16)
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(b.shape, dtype=np.float64)
+    flat_in = b.reshape(-1)
+    flat_out = out.reshape(-1)
+    step = 1 << 24
+    for i in range(0, flat_in.size, step):
+        seg = flat_in[i:i + step].astype(np.uint32) << np.uint32(16)
+        flat_out[i:i + step] = seg.view(np.float32)
+    return out
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a
+
+
+def _ptr(a, ctype):
+    return a.ctypes.data_as(ctype) if a is not None else None
+
+
+def _mask_arg(mask, n):
+    if mask is None:
+        return None
+    m = _c(mask, np.uint8)
+    assert m.shape == (n,)
+    return m
+
+
+# ----------------------------------------------------------------------------- forward / backward
+
+def linear_logp_fwd(h, w, y, mask, temperature):
+    """logp[N], lse[N] (float64) for h[N,H], W[V,H] given as exact float64 values."""
+    lib = _load()
+    h = _c(h, np.float64)
+    w = _c(w, np.float64)
+    n, hdim = h.shape
+    vocab = w.shape[0]
+    assert w.shape[1] == hdim
+    y = _c(y, np.int64)
+    m = _mask_arg(mask, n)
+    logp = np.empty(n, np.float64)
+    lse = np.empty(n, np.float64)
+    bad = lib.rlk_oracle_linear_logp_fwd(_ptr(h, _dp), _ptr(w, _dp), _ptr(y, _i64p), _ptr(m, _u8p),
+                                         n, hdim, vocab, float(temperature), _ptr(logp, _dp),
+                                         _ptr(lse, _dp))
+    if bad < 0:
+        raise MemoryError("oracle forward: scratch allocation failed")
+    return logp, lse
+
+
+def linear_logp_fwd_parallel(h, w, y, mask, temperature, threads=None):
+    """Same as linear_logp_fwd, rows split over host threads (each row computed alone)."""
+    h = _c(h, np.float64)
+    w = _c(w, np.float64)
+    n = h.shape[0]
+    y = _c(y, np.int64)
+    m = _mask_arg(mask, n)
+    threads = threads or max(1, len(os.sched_getaffinity(0)))
+    bounds = np.linspace(0, n, min(threads, max(n, 1)) + 1).astype(np.int64)
+    logp = np.empty(n, np.float64)
+    lse = np.empty(n, np.float64)
+
+    def work(i):
+        a, b = int(bounds[i]), int(bounds[i + 1])
+        if a == b:
+            return
+        lp, ls = linear_logp_fwd(h[a:b], w, y[a:b], None if m is None else m[a:b], temperature)
+        logp[a:b] = lp
+        lse[a:b] = ls
+
+    with ThreadPoolExecutor(len(bounds) - 1) as ex:
+        list(ex.map(work, range(len(bounds) - 1)))
+    return logp, lse
+
+
+def linear_logp_bwd_dh(h, w, y, mask, g, lse, temperature, row_begin=0, row_end=None):
+    lib = _load()
+    h = _c(h, np.float64)
+    w = _c(w, np.float64)
+    n, hdim = h.shape
+    vocab = w.shape[0]
+    row_end = n if row_end is None else row_end
+    y = _c(y, np.int64)
+    m = _mask_arg(mask, n)
+    g = _c(g, np.float64)
+    lse = _c(lse, np.float64)
+    out = np.empty((row_end - row_begin, hdim), np.float64)
+    lib.rlk_oracle_linear_logp_bwd_dh(_ptr(h, _dp), _ptr(w, _dp), _ptr(y, _i64p), _ptr(m, _u8p),
+                                      _ptr(g, _dp), _ptr(lse, _dp), n, hdim, vocab,
+                                      float(temperature), row_begin, row_end, _ptr(out, _dp))
+    return out
+
+
+def linear_logp_bwd_dw(h, w, y, mask, g, lse, temperature, v_begin=0, v_end=None):
+    lib = _load()
+    h = _c(h, np.float64)
+    w = _c(w, np.float64)
+    n, hdim = h.shape
+    vocab = w.shape[0]
+    v_end = vocab if v_end is None else v_end
+    y = _c(y, np.int64)
+    m = _mask_arg(mask, n)
+    g = _c(g, np.float64)
+    lse = _c(lse, np.float64)
+    out = np.empty((v_end - v_begin, hdim), np.float64)
+    lib.rlk_oracle_linear_logp_bwd_dw(_ptr(h, _dp), _ptr(w, _dp), _ptr(y, _i64p), _ptr(m, _u8p),
+                                      _ptr(g, _dp), _ptr(lse, _dp), n, hdim, vocab,
+                                      float(temperature), v_begin, v_end, _ptr(out, _dp))
+    return out
+
+
+def _split_parallel(total, fn, threads):
+    threads = threads or max(1, len(os.sched_getaffinity(0)))
+    parts = min(threads, max(total, 1))
+    bounds = np.linspace(0, total, parts + 1).astype(np.int64)
+    with ThreadPoolExecutor(parts) as ex:
+        list(ex.map(lambda i: fn(int(bounds[i]), int(bounds[i + 1])), range(parts)))
+
+
+def linear_logp_bwd_dh_parallel(h, w, y, mask, g, lse, temperature, threads=None):
+    h = _c(h, np.float64)
+    w = _c(w, np.float64)
+    n, hdim = h.shape
+    out = np.empty((n, hdim), np.float64)
+
+    def fn(a, b):
+        if a < b:
+            out[a:b] = linear_logp_bwd_dh(h, w, y, mask, g, lse, temperature, a, b)
+
+    _split_parallel(n, fn, threads)
+    return out
+
+
+def linear_logp_bwd_dw_parallel(h, w, y, mask, g, lse, temperature, v_begin, v_end, threads=None):
+    h = _c(h, np.float64)
+    w = _c(w, np.float64)
+    out = np.empty((v_end - v_begin, h.shape[1]), np.float64)
+
+    def fn(a, b):
+        if a < b:
+            out[a:b] = linear_logp_bwd_dw(h, w, y, mask, g, lse, temperature,
+                                          v_begin + a, v_begin + b)
+
+    _split_parallel(v_end - v_begin, fn, threads)
+    return out
+
+
+# ----------------------------------------------------------------------------- audit / loss
+
+def dlogp_audit(logp_new, logp_old, mask):
+    lib = _load()
+    a = _c(logp_new, np.float32)
+    b = _c(logp_old, np.float32)
+    n = a.shape[0]
+    m = _mask_arg(mask, n)
+    res = AuditResult()
+    lib.rlk_oracle_dlogp_audit(_ptr(a, _fp), _ptr(b, _fp), _ptr(m, _u8p), n, ctypes.byref(res))
+    return {
+        "active_count": res.active_count,
+        "argmax_index": res.argmax_index,
+        "max_abs_dlogp": res.max_abs_dlogp,
+        "mean_dlogp": res.mean_dlogp,
+        "approx_kl": res.approx_kl,
+    }
+
+
+def grpo_clip_grad(logp, old, adv, mask, eps):
+    """(loss, g[N]) of the GRPO clipped-ratio objective, token-mean over active tokens."""
+    lib = _load()
+    lp = _c(logp, np.float64)
+    od = _c(old, np.float64)
+    ad = _c(adv, np.float64)
+    n = lp.shape[0]
+    m = _mask_arg(mask, n)
+    g = np.empty(n, np.float64)
+    loss = lib.rlk_oracle_grpo_clip_grad(_ptr(lp, _dp), _ptr(od, _dp), _ptr(ad, _dp),
+                                         _ptr(m, _u8p), n, float(eps), _ptr(g, _dp))
+    return loss, g

@@ -1,0 +1,234 @@
+/*
+ * rlk_oracle.c -- plain fp64 CPU oracle for the fused linear selected-token
+ * log-prob, its backward, the masked dlogp audit and the GRPO clipped-ratio
+ * upstream gradient.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg do.  It shares no code, header or constant with the CUDA
+ * library.
+ *
+ * Every routine is the plain definition written out with explicit loops in
+ * IEEE double, single-threaded, in ascending index order, with no blocking,
+ * fusion or reordering.  Inputs that are bf16 on the GPU are handed in as
+ * doubles holding the exact bf16 values (the conversion is exact), so every
+ * product h*W below is exact and only the sums round (in fp64).
+ *
+ * Build: gcc -O2 -ffp-contract=off -fPIC -shared (no fast-math), so that the
+ * compiler neither fuses multiply-adds nor reassociates sums.
+ *
+ * Sources (page title, section):
+ *  - "RL-Kernel Roadmap (2026)", P0.2 "Typical Fused Operators": the fused
+ *    linear log-prob that never lands [B,S,V] logits, with a tile-recompute
+ *    backward.
+ *  - "RL-Kernel integration roadmap for vime", Operator Integration Plan,
+ *    "linear_logp / lm_head + logp": inputs (hidden states, target ids,
+ *    active masks, LM-head weight, vocab size, rollout temperature), the
+ *    max / sum-exp / selected-target-logit statistics, full-gradient
+ *    backward from dlogits.
+ *  - "RL-Kernel integration roadmap for vime", Consistency Contract: dlogp =
+ *    recomputed - old; every metric over active tokens only; max_abs_dlogp
+ *    is the primary metric; approx_kl0 = mean(exp(dlogp) - 1 - dlogp);
+ *    active-token count; worst-token location.
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *  - temperature divides the logits before the softmax: z = s / T;
+ *  - inactive rows get logp = 0, lse = 0, dh = 0 and add nothing to dW;
+ *  - an active row whose target lies outside [0, V) gets logp = NaN and is
+ *    counted in the return value;
+ *  - audit ties in max|d| go to the lowest token index; a NaN |d| ranks
+ *    above every number; with no active token: count 0, max 0, index -1,
+ *    mean = kl = NaN (0/0);
+ *  - GRPO loss: L = -(1/Na) * sum_active min(r*A, clip(r, 1-eps, 1+eps)*A),
+ *    r = exp(logp - old), a token-mean over the active tokens.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+/* s = sum_k a[k] * b[k], ascending k, one fp64 accumulator. */
+static double dot(const double* a, const double* b, int64_t n) {
+    double s = 0.0;
+    for (int64_t k = 0; k < n; ++k) s += a[k] * b[k];
+    return s;
+}
+
+static int row_active(const uint8_t* mask, int64_t t) {
+    return mask == NULL || mask[t] != 0;
+}
+
+/*
+ * Forward.  For every active row t:
+ *   z[v]    = (h_t . W_v) / T                       for v in [0, V)
+ *   M       = max_v z[v]
+ *   LSE_t   = M + log( sum_v exp(z[v] - M) )
+ *   logp_t  = z[y_t] - LSE_t
+ * Inactive rows: logp = 0, lse = 0.  lse may be NULL.
+ * Returns the number of active rows whose target is outside [0, V)
+ * (their logp is NaN), or -1 if the scratch row cannot be allocated.
+ */
+int64_t rlk_oracle_linear_logp_fwd(const double* h, const double* w,
+                                   const int64_t* y, const uint8_t* mask,
+                                   int64_t n, int64_t hdim, int64_t vocab,
+                                   double temperature,
+                                   double* logp, double* lse) {
+    double* z = (double*)malloc((size_t)(vocab > 0 ? vocab : 1) * sizeof(double));
+    if (z == NULL) return -1;
+    int64_t bad = 0;
+    for (int64_t t = 0; t < n; ++t) {
+        if (!row_active(mask, t)) {
+            logp[t] = 0.0;
+            if (lse) lse[t] = 0.0;
+            continue;
+        }
+        const double* ht = h + t * hdim;
+        for (int64_t v = 0; v < vocab; ++v) z[v] = dot(ht, w + v * hdim, hdim) / temperature;
+        double m = -INFINITY;
+        for (int64_t v = 0; v < vocab; ++v) if (z[v] > m) m = z[v];
+        double sum = 0.0;
+        for (int64_t v = 0; v < vocab; ++v) sum += exp(z[v] - m);
+        double l = m + log(sum);
+        if (lse) lse[t] = l;
+        if (y[t] < 0 || y[t] >= vocab) {
+            logp[t] = NAN;
+            ++bad;
+        } else {
+            logp[t] = z[y[t]] - l;
+        }
+    }
+    free(z);
+    return bad;
+}
+
+/*
+ * Backward, rows [row_begin, row_end) of dL/dh for L = sum_t g_t * logp_t.
+ * With p[v] = exp(z[v] - LSE_t) (LSE_t from the forward above) and
+ *   G[t][v] = g_t * (delta(v, y_t) - p[v]) / T,
+ *   dh_t    = sum_v G[t][v] * W_v               (ascending v)
+ * Inactive rows and rows with an invalid target get dh_t = 0.
+ * dh points at the first output row (row_begin), row-major [.., H].
+ */
+void rlk_oracle_linear_logp_bwd_dh(const double* h, const double* w,
+                                   const int64_t* y, const uint8_t* mask,
+                                   const double* g, const double* lse,
+                                   int64_t n, int64_t hdim, int64_t vocab,
+                                   double temperature,
+                                   int64_t row_begin, int64_t row_end,
+                                   double* dh) {
+    (void)n;
+    for (int64_t t = row_begin; t < row_end; ++t) {
+        double* out = dh + (t - row_begin) * hdim;
+        for (int64_t k = 0; k < hdim; ++k) out[k] = 0.0;
+        if (!row_active(mask, t) || y[t] < 0 || y[t] >= vocab) continue;
+        const double* ht = h + t * hdim;
+        for (int64_t v = 0; v < vocab; ++v) {
+            double z = dot(ht, w + v * hdim, hdim) / temperature;
+            double p = exp(z - lse[t]);
+            double delta = (v == y[t]) ? 1.0 : 0.0;
+            double G = g[t] * (delta - p) / temperature;
+            const double* wv = w + v * hdim;
+            for (int64_t k = 0; k < hdim; ++k) out[k] += G * wv[k];
+        }
+    }
+}
+
+/*
+ * Backward, rows [v_begin, v_end) of dL/dW:
+ *   dW_v = sum_t G[t][v] * h_t                  (ascending t, active rows)
+ * with G as above.  dw points at the first output row (v_begin).
+ */
+void rlk_oracle_linear_logp_bwd_dw(const double* h, const double* w,
+                                   const int64_t* y, const uint8_t* mask,
+                                   const double* g, const double* lse,
+                                   int64_t n, int64_t hdim, int64_t vocab,
+                                   double temperature,
+                                   int64_t v_begin, int64_t v_end,
+                                   double* dw) {
+    for (int64_t v = v_begin; v < v_end; ++v) {
+        double* out = dw + (v - v_begin) * hdim;
+        for (int64_t k = 0; k < hdim; ++k) out[k] = 0.0;
+        const double* wv = w + v * hdim;
+        for (int64_t t = 0; t < n; ++t) {
+            if (!row_active(mask, t) || y[t] < 0 || y[t] >= vocab) continue;
+            const double* ht = h + t * hdim;
+            double z = dot(ht, wv, hdim) / temperature;
+            double p = exp(z - lse[t]);
+            double delta = (v == y[t]) ? 1.0 : 0.0;
+            double G = g[t] * (delta - p) / temperature;
+            for (int64_t k = 0; k < hdim; ++k) out[k] += G * ht[k];
+        }
+    }
+}
+
+typedef struct {
+    int64_t active_count;
+    int64_t argmax_index;
+    double max_abs_dlogp;
+    double mean_dlogp;
+    double approx_kl;
+} rlk_oracle_audit_t;
+
+/*
+ * Masked dlogp audit over active tokens, ascending t:
+ *   d_t       = logp_new[t] - logp_old[t]         (exact in double)
+ *   count     = #active
+ *   max|d|    and the first index attaining it (NaN ranks highest)
+ *   mean      = sum d / count
+ *   approx_kl = sum (exp(d) - 1 - d) / count, evaluated as expm1(d) - d
+ */
+void rlk_oracle_dlogp_audit(const float* logp_new, const float* logp_old,
+                            const uint8_t* mask, int64_t n,
+                            rlk_oracle_audit_t* out) {
+    int64_t count = 0, arg = -1;
+    double best = 0.0, sum_d = 0.0, sum_kl = 0.0;
+    for (int64_t t = 0; t < n; ++t) {
+        if (!row_active(mask, t)) continue;
+        double d = (double)logp_new[t] - (double)logp_old[t];
+        double a = fabs(d);
+        if (arg < 0) {
+            best = a;
+            arg = t;
+        } else if (isnan(a) ? !isnan(best) : (!isnan(best) && a > best)) {
+            best = a;
+            arg = t;
+        }
+        ++count;
+        sum_d += d;
+        sum_kl += expm1(d) - d;
+    }
+    out->active_count = count;
+    out->argmax_index = arg;
+    out->max_abs_dlogp = count ? best : 0.0;
+    out->mean_dlogp = sum_d / (double)count;
+    out->approx_kl = sum_kl / (double)count;
+}
+
+/*
+ * GRPO / PPO clipped-ratio objective and its per-token gradient.
+ *   r_t   = exp(logp_t - old_t)
+ *   L     = -(1/Na) * sum_active min(r_t * A_t, clip(r_t, 1-eps, 1+eps) * A_t)
+ *   g_t   = dL/dlogp_t = -(A_t * r_t) / Na  where the unclipped term is the
+ *           one selected by the min (always when r_t lies inside the clip
+ *           interval), 0 where the clipped constant is selected, 0 on
+ *           inactive tokens.
+ * Returns L (NaN when no token is active).
+ */
+double rlk_oracle_grpo_clip_grad(const double* logp, const double* old,
+                                 const double* adv, const uint8_t* mask,
+                                 int64_t n, double eps, double* g) {
+    int64_t na = 0;
+    for (int64_t t = 0; t < n; ++t) na += row_active(mask, t) ? 1 : 0;
+    double total = 0.0;
+    for (int64_t t = 0; t < n; ++t) {
+        g[t] = 0.0;
+        if (!row_active(mask, t)) continue;
+        double r = exp(logp[t] - old[t]);
+        double rc = r < 1.0 - eps ? 1.0 - eps : (r > 1.0 + eps ? 1.0 + eps : r);
+        double unclipped = r * adv[t];
+        double clipped = rc * adv[t];
+        int take_unclipped = (unclipped <= clipped);
+        total += take_unclipped ? unclipped : clipped;
+        if (take_unclipped) g[t] = -(adv[t] * r) / (double)na;
+    }
+    return -total / (double)na;
+}

@@ -1,0 +1,391 @@
+"""Pins for the fp64 oracle: each check ties it to something other than itself.
+
+Forward: closed forms (W = 0 gives -log V; V = 1 gives 0; V = 2 gives a
+log-sigmoid; h = 0 gives a uniform softmax), normalisation (sum over all
+targets of exp(logp) = 1), temperature scaling, a logit shift, permutation
+equivariance, and high-precision brute force (exact rational dot products,
+50-digit exp/log) on vocabularies of at most 16 entries.
+
+Backward: central finite differences of L = sum_t g_t logp_t on tiny shapes,
+the softmax-gradient invariant (dW column sums vanish), and closed forms for
+h = 0 and W = 0.
+
+Audit and GRPO: hand-built vectors, exact rational means, finite differences
+of the clipped objective, and the clip branches.
+
+The method is the fused linear selected-token log-prob of "RL-Kernel Roadmap
+(2026)" P0.2 and "RL-Kernel integration roadmap for vime" (linear_logp /
+lm_head + logp; Consistency Contract for the audit).
+"""
+import math
+from decimal import Decimal, getcontext
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+
+def _bf16_grid(rng, shape, scale):
+    """random doubles that are exactly representable in bf16."""
+    import torch
+    x = torch.from_numpy(rng.standard_normal(shape).astype(np.float32) * np.float32(scale))
+    return x.to(torch.bfloat16).double().numpy()
+
+
+def _fwd(o, h, w, y, mask=None, T=1.0):
+    return o.linear_logp_fwd(h, w, np.asarray(y, np.int64), mask, T)
+
+
+# ----------------------------------------------------------------------------- forward closed forms
+
+def test_zero_weight_gives_minus_log_v(oracle_lib):
+    rng = np.random.default_rng(1)
+    for vocab in (1, 2, 7, 1000):
+        h = _bf16_grid(rng, (5, 16), 1.0)
+        w = np.zeros((vocab, 16))
+        y = rng.integers(0, vocab, 5)
+        logp, lse = _fwd(oracle_lib, h, w, y, T=0.7)
+        np.testing.assert_allclose(logp, -math.log(vocab), rtol=0, atol=1e-14)
+        np.testing.assert_allclose(lse, math.log(vocab), rtol=0, atol=1e-14)
+
+
+def test_single_entry_vocab_gives_zero(oracle_lib):
+    rng = np.random.default_rng(2)
+    h = _bf16_grid(rng, (4, 8), 3.0)
+    w = _bf16_grid(rng, (1, 8), 3.0)
+    logp, _ = _fwd(oracle_lib, h, w, [0, 0, 0, 0], T=0.3)
+    assert np.all(logp == 0.0)
+
+
+def test_two_entry_vocab_is_log_sigmoid(oracle_lib):
+    rng = np.random.default_rng(3)
+    h = _bf16_grid(rng, (6, 32), 1.0)
+    w = _bf16_grid(rng, (2, 32), 0.3)
+    y = np.array([0, 1, 0, 1, 1, 0])
+    T = 0.7
+    logp, _ = _fwd(oracle_lib, h, w, y, T=T)
+    for t in range(6):
+        s = [sum(Fraction(a) * Fraction(b) for a, b in zip(h[t], w[v])) for v in range(2)]
+        diff = float((s[1 - y[t]] - s[y[t]]) / Fraction(T))
+        expect = -math.log1p(math.exp(diff)) if diff < 30 else -diff - math.log1p(math.exp(-diff))
+        assert abs(logp[t] - expect) < 1e-13
+
+
+def test_hand_worked_three_entry_example(oracle_lib):
+    # h = (1, 0), W rows (1,0), (0,1), (-1,0): logits (1, 0, -1) at T = 1.
+    h = np.array([[1.0, 0.0], [1.0, 0.0], [1.0, 0.0]])
+    w = np.array([[1.0, 0.0], [0.0, 1.0], [-1.0, 0.0]])
+    logp, lse = _fwd(oracle_lib, h, w, [0, 1, 2], T=1.0)
+    z = math.log(math.e + 1.0 + math.exp(-1.0))
+    np.testing.assert_allclose(logp, [1.0 - z, -z, -1.0 - z], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lse, [z, z, z], rtol=0, atol=1e-15)
+    # T = 2 halves every logit
+    logp2, _ = _fwd(oracle_lib, h, w, [0, 1, 2], T=2.0)
+    z2 = math.log(math.exp(0.5) + 1.0 + math.exp(-0.5))
+    np.testing.assert_allclose(logp2, [0.5 - z2, -z2, -0.5 - z2], rtol=0, atol=1e-15)
+
+
+def test_zero_hidden_gives_uniform(oracle_lib):
+    rng = np.random.default_rng(4)
+    w = _bf16_grid(rng, (37, 16), 1.0)
+    logp, _ = _fwd(oracle_lib, np.zeros((3, 16)), w, [0, 5, 36], T=1.3)
+    np.testing.assert_allclose(logp, -math.log(37), rtol=0, atol=1e-14)
+
+
+def test_probabilities_sum_to_one(oracle_lib):
+    rng = np.random.default_rng(5)
+    vocab, hdim = 300, 24
+    h1 = _bf16_grid(rng, (1, hdim), 1.0)
+    w = _bf16_grid(rng, (vocab, hdim), 0.5)
+    h = np.repeat(h1, vocab, axis=0)
+    logp, lse = _fwd(oracle_lib, h, w, np.arange(vocab), T=0.7)
+    assert abs(math.fsum(np.exp(logp)) - 1.0) < 1e-13
+    assert np.all(lse == lse[0])
+
+
+def test_temperature_scaling(oracle_lib):
+    rng = np.random.default_rng(6)
+    h = _bf16_grid(rng, (8, 32), 1.0)
+    w = _bf16_grid(rng, (50, 32), 0.2)
+    y = rng.integers(0, 50, 8)
+    T = 0.7
+    a, _ = _fwd(oracle_lib, h, w, y, T=T)
+    b, _ = _fwd(oracle_lib, h, w / T, y, T=1.0)
+    c, _ = _fwd(oracle_lib, h / T, w, y, T=1.0)
+    np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(a, c, rtol=0, atol=1e-12)
+    # power-of-two temperature: the scalings are exact
+    d, _ = _fwd(oracle_lib, h, w, y, T=4.0)
+    e, _ = _fwd(oracle_lib, h, w * 0.25, y, T=1.0)
+    np.testing.assert_allclose(d, e, rtol=0, atol=1e-14)
+    # T -> infinity flattens the distribution
+    f, _ = _fwd(oracle_lib, h, w, y, T=1e12)
+    np.testing.assert_allclose(f, -math.log(50), rtol=0, atol=1e-9)
+
+
+def test_logit_shift_and_permutation(oracle_lib):
+    rng = np.random.default_rng(7)
+    h = _bf16_grid(rng, (6, 16), 1.0)
+    w = _bf16_grid(rng, (40, 16), 0.3)
+    y = rng.integers(0, 40, 6)
+    a, _ = _fwd(oracle_lib, h, w, y, T=0.9)
+    # an extra feature that adds the same constant 3 to every logit
+    h2 = np.concatenate([h, np.ones((6, 1))], axis=1)
+    w2 = np.concatenate([w, np.full((40, 1), 3.0)], axis=1)
+    b, _ = _fwd(oracle_lib, h2, w2, y, T=0.9)
+    np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)
+    perm = rng.permutation(40)
+    inv = np.argsort(perm)
+    c, _ = _fwd(oracle_lib, h, w[perm], inv[y], T=0.9)
+    np.testing.assert_allclose(a, c, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("vocab", [1, 2, 3, 5, 8, 13, 16])
+def test_brute_force_high_precision(oracle_lib, vocab):
+    getcontext().prec = 60
+    rng = np.random.default_rng(100 + vocab)
+    hdim = 12
+    h = _bf16_grid(rng, (4, hdim), 2.0)
+    w = _bf16_grid(rng, (vocab, hdim), 1.0)
+    y = rng.integers(0, vocab, 4)
+    T = 0.7
+    logp, lse = _fwd(oracle_lib, h, w, y, T=T)
+    for t in range(4):
+        z = []
+        for v in range(vocab):
+            s = sum(Fraction(a) * Fraction(b) for a, b in zip(h[t], w[v]))
+            q = s / Fraction(T)
+            z.append(Decimal(q.numerator) / Decimal(q.denominator))
+        total = sum((zz.exp() for zz in z), Decimal(0))
+        expect = z[y[t]] - total.ln()          # no max subtraction
+        assert abs(float(expect) - logp[t]) < 1e-13 * max(1.0, abs(float(expect)))
+        assert abs(float(total.ln()) - lse[t]) < 1e-13 * max(1.0, abs(float(total.ln())))
+
+
+def test_inactive_and_invalid_rows(oracle_lib):
+    rng = np.random.default_rng(8)
+    h = _bf16_grid(rng, (5, 8), 1.0)
+    h[1, :] = np.nan                                   # NaN padding on an inactive row
+    w = _bf16_grid(rng, (10, 8), 1.0)
+    y = np.array([3, 999, 4, 10, -1])
+    mask = np.array([1, 0, 1, 1, 1], np.uint8)
+    logp, lse = oracle_lib.linear_logp_fwd(h, w, y, mask, 1.0)
+    assert logp[1] == 0.0 and lse[1] == 0.0
+    assert np.isnan(logp[3]) and np.isnan(logp[4])
+    assert np.isfinite(logp[0]) and np.isfinite(logp[2])
+
+
+# ----------------------------------------------------------------------------- backward
+
+def _loss(o, h, w, y, mask, g, T):
+    logp, _ = o.linear_logp_fwd(h, w, y, mask, T)
+    return float(np.dot(g, np.where(np.isfinite(logp), logp, 0.0)))
+
+
+@pytest.mark.parametrize("shape", [(1, 3, 2), (3, 5, 4), (4, 8, 6)])
+def test_backward_finite_differences(oracle_lib, shape):
+    o = oracle_lib
+    n, hdim, vocab = shape
+    rng = np.random.default_rng(200 + n)
+    h = rng.standard_normal((n, hdim))
+    w = rng.standard_normal((vocab, hdim)) * 0.7
+    y = rng.integers(0, vocab, n)
+    mask = np.ones(n, np.uint8)
+    if n > 2:
+        mask[1] = 0
+    g = rng.standard_normal(n)
+    T = 0.7
+    _, lse = o.linear_logp_fwd(h, w, y, mask, T)
+    dh = o.linear_logp_bwd_dh(h, w, y, mask, g, lse, T)
+    dw = o.linear_logp_bwd_dw(h, w, y, mask, g, lse, T)
+    step = 1e-6
+    for arr, grad in ((h, dh), (w, dw)):
+        for idx in np.ndindex(arr.shape):
+            keep = arr[idx]
+            arr[idx] = keep + step
+            up = _loss(o, h, w, y, mask, g, T)
+            arr[idx] = keep - step
+            dn = _loss(o, h, w, y, mask, g, T)
+            arr[idx] = keep
+            fd = (up - dn) / (2 * step)
+            assert abs(fd - grad[idx]) <= 1e-7 * max(1.0, abs(fd)), (idx, fd, grad[idx])
+    if n > 2:
+        assert np.all(dh[1] == 0.0)
+
+
+def test_backward_softmax_invariant(oracle_lib):
+    o = oracle_lib
+    rng = np.random.default_rng(9)
+    h = _bf16_grid(rng, (12, 16), 1.0)
+    w = _bf16_grid(rng, (30, 16), 0.4)
+    y = rng.integers(0, 30, 12)
+    g = rng.standard_normal(12)
+    mask = (rng.random(12) < 0.7).astype(np.uint8)
+    _, lse = o.linear_logp_fwd(h, w, y, mask, 0.7)
+    dw = o.linear_logp_bwd_dw(h, w, y, mask, g, lse, 0.7)
+    # sum_v G[t][v] = 0 for each row, hence sum_v dW_v = 0
+    scale = np.abs(dw).sum(axis=0).max()
+    assert np.abs(dw.sum(axis=0)).max() < 1e-13 * scale
+    # an inactive row's content does not reach dW
+    h2 = h.copy()
+    h2[mask == 0] = 123.0
+    dw2 = o.linear_logp_bwd_dw(h2, w, y, mask, g, lse, 0.7)
+    assert np.array_equal(dw, dw2)
+
+
+def test_backward_closed_forms(oracle_lib):
+    o = oracle_lib
+    rng = np.random.default_rng(10)
+    vocab, hdim, n, T = 9, 6, 4, 0.7
+    w = rng.standard_normal((vocab, hdim))
+    y = np.array([0, 3, 3, 8])
+    g = rng.standard_normal(n)
+    mask = np.ones(n, np.uint8)
+    # h = 0: uniform softmax, dh_t = (g_t/T) (W_y - mean_v W_v), dW = 0
+    h = np.zeros((n, hdim))
+    _, lse = o.linear_logp_fwd(h, w, y, mask, T)
+    dh = o.linear_logp_bwd_dh(h, w, y, mask, g, lse, T)
+    expect = (g / T)[:, None] * (w[y] - w.mean(axis=0))
+    np.testing.assert_allclose(dh, expect, rtol=0, atol=1e-13)
+    assert np.all(o.linear_logp_bwd_dw(h, w, y, mask, g, lse, T) == 0.0)
+    # W = 0: dW_v = sum_t (g_t/T)(delta - 1/V) h_t, dh = 0
+    h = rng.standard_normal((n, hdim))
+    w0 = np.zeros((vocab, hdim))
+    _, lse = o.linear_logp_fwd(h, w0, y, mask, T)
+    dw = o.linear_logp_bwd_dw(h, w0, y, mask, g, lse, T)
+    onehot = np.zeros((n, vocab))
+    onehot[np.arange(n), y] = 1.0
+    expect = ((onehot - 1.0 / vocab) * (g / T)[:, None]).T @ h
+    np.testing.assert_allclose(dw, expect, rtol=0, atol=1e-13)
+    assert np.all(o.linear_logp_bwd_dh(h, w0, y, mask, g, lse, T) == 0.0)
+
+
+def test_backward_row_ranges_agree(oracle_lib):
+    o = oracle_lib
+    rng = np.random.default_rng(11)
+    h = _bf16_grid(rng, (10, 8), 1.0)
+    w = _bf16_grid(rng, (20, 8), 0.5)
+    y = rng.integers(0, 20, 10)
+    g = rng.standard_normal(10)
+    _, lse = o.linear_logp_fwd(h, w, y, None, 1.1)
+    full = o.linear_logp_bwd_dw(h, w, y, None, g, lse, 1.1)
+    part = o.linear_logp_bwd_dw_parallel(h, w, y, None, g, lse, 1.1, 5, 17, threads=3)
+    assert np.array_equal(full[5:17], part)
+    dh = o.linear_logp_bwd_dh(h, w, y, None, g, lse, 1.1)
+    assert np.array_equal(dh, o.linear_logp_bwd_dh_parallel(h, w, y, None, g, lse, 1.1, threads=4))
+    lp, ls = o.linear_logp_fwd(h, w, y, None, 1.1)
+    lp2, ls2 = o.linear_logp_fwd_parallel(h, w, y, None, 1.1, threads=3)
+    assert np.array_equal(lp, lp2) and np.array_equal(ls, ls2)
+
+
+# ----------------------------------------------------------------------------- audit
+
+def _audit(o, new, old, mask):
+    return o.dlogp_audit(np.asarray(new, np.float32), np.asarray(old, np.float32),
+                         None if mask is None else np.asarray(mask, np.uint8))
+
+
+def test_audit_all_masked(oracle_lib):
+    r = _audit(oracle_lib, [1, 2, 3], [0, 0, 0], [0, 0, 0])
+    assert r["active_count"] == 0 and r["argmax_index"] == -1 and r["max_abs_dlogp"] == 0.0
+    assert math.isnan(r["mean_dlogp"]) and math.isnan(r["approx_kl"])
+    r = _audit(oracle_lib, [], [], [])
+    assert r["active_count"] == 0 and r["argmax_index"] == -1
+
+
+def test_audit_single_and_ties(oracle_lib):
+    r = _audit(oracle_lib, [-1.0, -2.5, -3.0], [-1.0, -2.0, -3.0], [0, 1, 0])
+    assert r["active_count"] == 1 and r["argmax_index"] == 1
+    assert r["max_abs_dlogp"] == 0.5 and r["mean_dlogp"] == -0.5
+    assert abs(r["approx_kl"] - (math.expm1(-0.5) + 0.5)) < 1e-16
+    # ties go to the lowest index; masked entries never win
+    r = _audit(oracle_lib, [0.0, 0.25, -0.25, 0.25, 9.0], [0.0, 0.0, 0.0, 0.0, 0.0], [1, 1, 1, 1, 0])
+    assert r["argmax_index"] == 1 and r["max_abs_dlogp"] == 0.25 and r["active_count"] == 4
+    # d = 0 everywhere: zero mean, zero KL
+    r = _audit(oracle_lib, [-1.0, -2.0], [-1.0, -2.0], None)
+    assert r["mean_dlogp"] == 0.0 and r["approx_kl"] == 0.0 and r["argmax_index"] == 0
+    # a NaN ranks above every number
+    r = _audit(oracle_lib, [0.0, 5.0, float("nan"), float("nan")], [0.0] * 4, None)
+    assert r["argmax_index"] == 2 and math.isnan(r["max_abs_dlogp"])
+
+
+def test_audit_exact_rationals(oracle_lib):
+    rng = np.random.default_rng(12)
+    n = 5000
+    old = (-rng.exponential(1.0, n)).astype(np.float32)
+    new = (old + rng.normal(0, 0.01, n)).astype(np.float32)
+    mask = (rng.random(n) < 0.8).astype(np.uint8)
+    r = _audit(oracle_lib, new, old, mask)
+    act = np.nonzero(mask)[0]
+    assert r["active_count"] == int(mask.sum())
+    d = [Fraction(float(new[t])) - Fraction(float(old[t])) for t in act]
+    mean = sum(d, Fraction(0)) / len(d)
+    assert abs(r["mean_dlogp"] - float(mean)) <= 1e-15 * float(sum(abs(x) for x in d) / len(d))
+    absd = [abs(x) for x in d]
+    best = max(absd)
+    assert r["max_abs_dlogp"] == float(best)
+    assert r["argmax_index"] == int(act[absd.index(best)])
+    kl = math.fsum(math.expm1(float(x)) - float(x) for x in d) / len(d)
+    assert abs(r["approx_kl"] - kl) < 1e-12 * kl
+    # second-order expansion: KL ~ mean d^2 / 2 for small d
+    assert abs(r["approx_kl"] - float(np.mean(np.square([float(x) for x in d]))) / 2) < 0.02 * kl
+
+
+# ----------------------------------------------------------------------------- GRPO objective
+
+def test_grpo_ratio_one_and_clip_branches(oracle_lib):
+    o = oracle_lib
+    logp = np.array([-1.0, -2.0, -3.0, -0.5, -0.7, -0.9])
+    adv = np.array([1.0, -2.0, 0.5, 1.0, 1.0, -1.0])
+    mask = np.array([1, 1, 1, 0, 1, 1], np.uint8)
+    loss, g = o.grpo_clip_grad(logp, logp.copy(), adv, mask, 0.2)
+    na = 5
+    np.testing.assert_allclose(g, np.where(mask == 1, -adv / na, 0.0), rtol=0, atol=1e-16)
+    assert abs(loss - (-(adv * mask).sum() / na)) < 1e-15
+    # r = e^{0.5} > 1.2 with A > 0: clipped branch selected -> zero gradient
+    old = logp - np.array([0.5, 0, 0, 0, 0.5, -0.5])
+    _, g = o.grpo_clip_grad(logp, old, adv, mask, 0.2)
+    assert g[0] == 0.0 and g[4] == 0.0
+    # r = e^{-0.5} < 0.8 with A < 0: clipped (constant) selected -> zero gradient
+    assert g[5] == 0.0
+    # r < 1 - eps with A > 0: unclipped is the minimum -> gradient flows
+    old2 = logp + np.array([0.5, 0, 0, 0, 0, 0])
+    _, g2 = o.grpo_clip_grad(logp, old2, adv, mask, 0.2)
+    assert abs(g2[0] - (-adv[0] * math.exp(-0.5) / na)) < 1e-16
+
+
+def test_grpo_finite_differences(oracle_lib):
+    o = oracle_lib
+    rng = np.random.default_rng(13)
+    n = 40
+    logp = -rng.exponential(1.0, n)
+    old = logp + rng.normal(0, 0.15, n)
+    adv = rng.normal(0, 1, n)
+    mask = (rng.random(n) < 0.8).astype(np.uint8)
+    _, g = o.grpo_clip_grad(logp, old, adv, mask, 0.2)
+    step = 1e-7
+    for t in range(n):
+        r = math.exp(logp[t] - old[t])
+        if abs(r - 0.8) < 1e-4 or abs(r - 1.2) < 1e-4:
+            continue                                    # kink of the clip
+        up = logp.copy()
+        up[t] += step
+        dn = logp.copy()
+        dn[t] -= step
+        fd = (o.grpo_clip_grad(up, old, adv, mask, 0.2)[0]
+              - o.grpo_clip_grad(dn, old, adv, mask, 0.2)[0]) / (2 * step)
+        assert abs(fd - g[t]) < 1e-7, (t, fd, g[t])
+
+
+def test_golden_hand_example(oracle_lib):
+    import json
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "hand_example.json")
+    ex = json.load(open(path))
+    for case in ex["cases"]:
+        n = len(case["targets"])
+        h = np.repeat(np.array(ex["hidden"]), n, axis=0)
+        logp, lse = oracle_lib.linear_logp_fwd(h, np.array(ex["weight"]), case["targets"], None,
+                                               case["temperature"])
+        np.testing.assert_allclose(logp, case["logp"], rtol=0, atol=1e-15)
+        np.testing.assert_allclose(lse, case["lse"], rtol=0, atol=1e-15)
