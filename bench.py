@@ -1,0 +1,431 @@
+"""Benchmark: one step = the whole hot path on one batch of synthetic input.
+
+A step runs, on one stream, the fused linear log-prob forward, the masked
+dlogp audit of its result against the rollout-side old logp, and the
+chunked-recompute backward for the GRPO clipped-ratio upstream gradient --
+the rows of the hot path, all in librlk.so kernels.
+
+Workload (default): the Qwen3-8B-shaped LM head, N = 8192 tokens packed from
+8 sequences, H = 4096, V = 151936, T = 0.7, targets sampled from the softmax
+of the logits, all tokens active; old logp = forward logp + N(0, 0.01^2)
+noise, advantages ~ N(0, 1) per sequence, eps = 0.2 (the GRPO gradient is
+formed once, before timing, as input data).  Inputs are synthetic and
+seeded; W (1.245 GB) is larger than L2, so no flush is needed between steps.
+
+Output: one JSON line (rank 0).  ``value`` is whole-job active tokens per
+second with inputs resident in HBM; ``e2e`` is the same metric through the C
+ABI with the per-step inputs copied from pinned host memory and the result
+read back inside the timed region.  ``--impl reference`` times the fp64 CPU
+oracle on a bounded token sample of the same workload instead.
+
+Multi-GPU (torchrun): every rank scores its own batch (seed + rank); there is
+no collective on the data path, only a barrier and a max over ranks of the
+timed region (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+METRIC = "fused linear-logp tokens/s and TFLOP/s (fwd, bwd) on 1 GB300; % of bf16 dense peak"
+GRPO_EPS = 0.2
+
+
+# ----------------------------------------------------------------------------- environment
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workload
+
+def make_batch(seed, n_tokens=wl.QWEN_N):
+    w = wl.qwen_fwd(seed, n_tokens=n_tokens, sample=True)
+    noise, adv = wl.grpo_bwd_extras(w.n, w.seq_lens, seed)
+    return w, noise, adv
+
+
+def grpo_grad_torch(logp, old, adv, mask, eps):
+    """Per-token gradient of the GRPO clipped-ratio loss (input preparation only)."""
+    active = mask > 0
+    na = max(int(active.sum()), 1)
+    r = torch.exp(logp.double() - old.double())
+    unclipped = r * adv
+    clipped = torch.clamp(r, 1 - eps, 1 + eps) * adv
+    take = (unclipped <= clipped) & active
+    return torch.where(take, -adv * r / na, torch.zeros_like(r)).float()
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, world, rank, local):
+    import rl_post_linear_gb300 as rlk
+    from rl_post_linear_gb300 import build as rlk_build
+    if rank == 0:
+        rlk_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    rlk.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+
+    w, noise, adv = make_batch(args.seed + rank, args.tokens)
+    n, h, v, T = w.n, w.h, w.v, w.temperature
+    n_act = w.n_active
+    hid = w.hidden.to(dev)
+    wt = w.weight.to(dev)
+    y = w.targets.to(dev)
+    mask = w.mask.to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    logp = torch.empty(n, dtype=torch.float32, device=dev)
+    lse = torch.empty(n, dtype=torch.float32, device=dev)
+    dh = torch.empty_like(hid)
+    dw = torch.empty_like(wt)
+    ws_f = torch.empty(rlk.rlk_linear_logp_fwd_workspace_bytes(n, h, v), dtype=torch.uint8,
+                       device=dev)
+    ws_b = torch.empty(rlk.rlk_linear_logp_bwd_workspace_bytes(n, h, v), dtype=torch.uint8,
+                       device=dev)
+    ws_a = torch.empty(rlk.rlk_dlogp_audit_workspace_bytes(n), dtype=torch.uint8, device=dev)
+    audit = torch.empty(rlk.AUDIT_RESULT_BYTES, dtype=torch.uint8, device=dev)
+
+    # input preparation: rollout-side old logp and the GRPO upstream gradient
+    rlk.rlk_linear_logp_fwd(hid, wt, y, mask, T, logp, lse, ws_f, err)
+    torch.cuda.synchronize()
+    old = (logp.double() + torch.from_numpy(noise).to(dev)).float()
+    g = grpo_grad_torch(logp, old, torch.from_numpy(adv).to(dev), mask, GRPO_EPS)
+    n_chunks = -(-v // 16384)
+    launches_per_step = 2 + 2 + 1 + 3 * n_chunks
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        rlk.rlk_linear_logp_fwd(hid, wt, y, mask, T, logp, lse, ws_f, err)
+        if ev is not None:
+            ev[1].record(stream)
+        rlk.rlk_dlogp_audit(logp, old, mask, audit, ws_a)
+        if ev is not None:
+            ev[2].record(stream)
+        rlk.rlk_linear_logp_bwd(hid, wt, y, mask, g, lse, T, dh, dw, ws_b, err)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = start.elapsed_time(stop)
+    fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    aud_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
+    bwd_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in evs]))
+    if int(err.item()) != 0:
+        raise RuntimeError("device error word %#x" % int(err.item()))
+
+    # e2e: per-step inputs from pinned host memory through the C ABI, result read back
+    h_host = w.hidden.pin_memory()
+    y_host = w.targets.pin_memory()
+    m_host = w.mask.pin_memory()
+    old_host = old.cpu().pin_memory()
+    g_host = g.cpu().pin_memory()
+    logp_host = torch.empty(n, dtype=torch.float32).pin_memory()
+    audit_host = torch.empty(rlk.AUDIT_RESULT_BYTES, dtype=torch.uint8).pin_memory()
+    old_d, g_d = torch.empty_like(old), torch.empty_like(g)
+
+    def e2e_step():
+        hid.copy_(h_host, non_blocking=True)
+        y.copy_(y_host, non_blocking=True)
+        mask.copy_(m_host, non_blocking=True)
+        old_d.copy_(old_host, non_blocking=True)
+        g_d.copy_(g_host, non_blocking=True)
+        rlk.rlk_linear_logp_fwd(hid, wt, y, mask, T, logp, lse, ws_f, err)
+        rlk.rlk_dlogp_audit(logp, old_d, mask, audit, ws_a)
+        rlk.rlk_linear_logp_bwd(hid, wt, y, mask, g_d, lse, T, dh, dw, ws_b, err)
+        logp_host.copy_(logp, non_blocking=True)
+        audit_host.copy_(audit, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e_stop.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e_start.elapsed_time(e_stop)
+    h2d = (h_host.numel() * 2 + y_host.numel() * 8 + m_host.numel() + old_host.numel() * 4
+           + g_host.numel() * 4)
+    d2h = logp_host.numel() * 4 + audit_host.numel()
+
+    times = torch.tensor([total_ms, e2e_ms, fwd_ms, aud_ms, bwd_ms], dtype=torch.float64,
+                         device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
+    total_ms, e2e_ms, fwd_ms, aud_ms, bwd_ms = times.tolist()
+    if rank != 0:
+        return None
+
+    pk = peaks()
+    ms_step = total_ms / args.steps
+    tok = n_act * world
+    fwd_tflops = 2.0 * n_act * h * v / (fwd_ms * 1e-3) / 1e12
+    bwd_tflops = 4.0 * n_act * h * v / (bwd_ms * 1e-3) / 1e12
+    peak = pk["bf16_tflops_sustained"]
+    audit_gbs = n * 9 / (aud_ms * 1e-3) / 1e9
+    # dominant kernel by share of the step: the backward GEMMs or the forward GEMM
+    dom = "bwd" if bwd_ms >= fwd_ms else "fwd"
+    achieved = bwd_tflops if dom == "bwd" else fwd_tflops
+    traffic = recorded_traffic("fwd_gemm" if dom == "fwd" else "bwd")
+    out = {
+        "metric": METRIC,
+        "value": tok / (ms_step * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; Qwen3-8B-shaped LM head, random-init weights)",
+        "config": {"workload": w.name + " fwd+audit+GRPO bwd", "n_tokens": n,
+                   "n_active": n_act, "hidden": h, "vocab": v, "temperature": T,
+                   "seq_lens": w.seq_lens, "parallelism": "dp%d (independent batches)" % world,
+                   "l2": "inputs larger than L2 (W = %.3f GB), no flush" % (v * h * 2 / 1e9)},
+        "fwd": {"ms": fwd_ms, "tflops": fwd_tflops, "frac_of_peak": fwd_tflops / peak,
+                "flops": 2.0 * n_act * h * v},
+        "bwd": {"ms": bwd_ms, "tflops": bwd_tflops, "frac_of_peak": bwd_tflops / peak,
+                "flops": 4.0 * n_act * h * v,
+                "executed_tflops": 6.0 * n * h * v / (bwd_ms * 1e-3) / 1e12},
+        "audit": {"ms": aud_ms, "gbs": audit_gbs, "frac_of_hbm": audit_gbs / pk["hbm_gbs"]},
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": "%s bf16 sustained (MEASURED_PEAKS.json)" % pk["source"]},
+        "e2e": {"value": tok / (e2e_ms / args.steps * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu_baseline and world == 1:
+        out["cpu_baseline"] = cpu_baseline(w, old.cpu(), g.cpu(), args.cpu_tokens)
+    return out
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current source."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    cur = source_hash()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) == 3 and parts[0] == kernel and parts[2] == cur:
+            return float(parts[1])
+    return None
+
+
+def source_hash():
+    d = os.path.join(ROOT, "rl_post_linear_gb300", "csrc")
+    hsh = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        hsh.update(open(os.path.join(d, f), "rb").read())
+    return hsh.hexdigest()[:16]
+
+
+# ----------------------------------------------------------------------------- CPU oracle legs
+
+def oracle_step_sample(w, old, g, tokens, threads):
+    """One oracle step (fwd, audit, bwd) over the first `tokens` tokens of the batch."""
+    import oracle
+    h64 = oracle.bf16_bits_to_f64(w.hidden[:tokens])
+    w64 = getattr(w, "_w64", None)
+    if w64 is None:
+        w64 = oracle.bf16_bits_to_f64(w.weight)
+        w._w64 = w64
+    y = w.targets[:tokens].numpy()
+    m = w.mask[:tokens].numpy()
+    gg = g[:tokens].double().numpy()
+    t0 = time.perf_counter()
+    lp, lse = oracle.linear_logp_fwd_parallel(h64, w64, y, m, w.temperature, threads)
+    oracle.dlogp_audit(lp.astype(np.float32), old[:tokens].numpy(), m)
+    oracle.linear_logp_bwd_dh_parallel(h64, w64, y, m, gg, lse, w.temperature, threads)
+    oracle.linear_logp_bwd_dw_blocks(h64, w64, y, m, gg, lse, w.temperature, 0, w.v,
+                                     lambda v0, blk: None, threads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_cores():
+    return max(1, len(os.sched_getaffinity(0)))
+
+
+def cpu_baseline(w, old, g, tokens):
+    cores = cpu_cores()
+    tokens = tokens or cores
+    secs = oracle_step_sample(w, old, g, tokens, cores)
+    return {"value": tokens / secs, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": "first %d tokens of the batch, one full oracle step (fwd, audit, bwd with "
+                      "all %d dW rows), fp64, %.1f s" % (tokens, w.v, secs)}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    w, noise, adv = make_batch(args.seed, args.tokens)
+    import oracle
+    tokens = args.cpu_tokens or cpu_cores()
+    h64 = oracle.bf16_bits_to_f64(w.hidden[:tokens])
+    w._w64 = oracle.bf16_bits_to_f64(w.weight)
+    lp, _ = oracle.linear_logp_fwd_parallel(h64, w._w64, w.targets[:tokens].numpy(),
+                                            w.mask[:tokens].numpy(), w.temperature)
+    old = torch.zeros(w.n, dtype=torch.float32)
+    old[:tokens] = torch.from_numpy(lp + noise[:tokens]).float()
+    _, gg = oracle.grpo_clip_grad(lp, old[:tokens].double().numpy(), adv[:tokens],
+                                  w.mask[:tokens].numpy(), GRPO_EPS)
+    g = torch.zeros(w.n, dtype=torch.float32)
+    g[:tokens] = torch.from_numpy(gg).float()
+    for _ in range(args.warmup):
+        pass                     # the oracle has no warm-up state; W is converted once above
+    times = [oracle_step_sample(w, old, g, tokens, cpu_cores()) for _ in range(args.steps)]
+    secs = float(np.mean(times))
+    val = tokens / secs
+    return {
+        "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; Qwen3-8B-shaped LM head)", "impl": "reference",
+        "config": {"workload": w.name + " fwd+audit+GRPO bwd", "n_tokens": w.n,
+                   "hidden": w.h, "vocab": w.v, "temperature": w.temperature},
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cpu_cores(),
+                         "kind": "oracle",
+                         "sample": "first %d tokens per step, full oracle step" % tokens},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--tokens", type=int, default=wl.QWEN_N)
+    ap.add_argument("--cpu-tokens", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_env()
+    if world > 1 and args.impl == "ours":
+        torch.distributed.init_process_group("nccl")
+    try:
+        out = run_reference(args, world, rank) if args.impl == "reference" else \
+            run_ours(args, world, rank, local)
+        if out is not None:
+            print(json.dumps(out))
+    finally:
+        if world > 1 and args.impl == "ours":
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,153 @@
+/*
+ * rlk.h -- C ABI of the GB300 (sm_103a) fused linear selected-token log-prob.
+ *
+ * What it computes.  For hidden states h[N,H] and LM-head weights W[V,H]
+ * (both bf16), target ids y[N], an active mask and a rollout temperature T:
+ *
+ *     s[t,v]  = sum_k h[t,k] * W[v,k]                 (fp32 accumulation)
+ *     logp[t] = s[t,y_t]/T - log( sum_v exp(s[t,v]/T) )   for active t
+ *
+ * without ever storing the [N,V] logits ("RL-Kernel Roadmap (2026)", P0.2
+ * "Typical Fused Operators": fused CE log-prob that never lands [B,S,V]
+ * logits, forward streaming vocab blocks with an online softmax, backward
+ * recomputing tiles), with the explicit max / sum-exp / target-logit merge
+ * and full-gradient backward of "RL-Kernel integration roadmap for vime",
+ * Operator Integration Plan, "linear_logp / lm_head + logp", and the masked
+ * dlogp diagnostics of the same page's "Consistency Contract".
+ *
+ * Conventions shared by every entry point.
+ *  - Ownership: every array argument is a caller-owned DEVICE pointer unless
+ *    stated otherwise.  The library never allocates, frees or synchronises;
+ *    scratch memory is the caller's `workspace`, sized by the matching
+ *    *_workspace_bytes() query.  Work is enqueued on `stream` and is visible
+ *    once the caller synchronises that stream.
+ *  - Layout: contiguous row-major.  bf16 matrices (hidden, weight, dhidden,
+ *    dweight) must start on a 16-byte boundary; workspace on 256 bytes.
+ *  - Mask bytes: nonzero = active.  A NULL mask means every row is active.
+ *    Targets of inactive rows are never read.
+ *  - Shapes: H must be a positive multiple of 64; 1 <= V < 2^31;
+ *    0 <= N < 2^31.  N = 0 returns RLK_OK without launching anything.
+ *  - Errors: argument errors are returned synchronously, before anything is
+ *    enqueued; a failed launch returns RLK_ERR_LAUNCH.  There is no fallback
+ *    path: an unsupported case is an error, never a silent slower route.
+ *    Data errors found on the device (an active row whose target lies
+ *    outside [0, V)) set bits in *device_error_word (if not NULL; the caller
+ *    zeroes it) and give that row logp = NaN.
+ *  - Determinism: tile shapes, vocab-chunk widths and every reduction order
+ *    are compile-time constants, never functions of N, the mask or the SM
+ *    count, and no floating-point atomics are used.  A row's logp, lse and
+ *    dhidden are therefore bitwise identical whatever batch it is scored in;
+ *    dweight is bitwise reproducible for identical inputs.
+ */
+#ifndef RLK_H_
+#define RLK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    RLK_OK = 0,
+    RLK_ERR_INVALID_VALUE = 1,   /* NULL / misaligned pointer, bad size, T not finite > 0 */
+    RLK_ERR_UNSUPPORTED = 2,     /* H % 64 != 0, too large, or the device is not sm_103 */
+    RLK_ERR_WORKSPACE = 3,       /* workspace NULL, misaligned or smaller than the query */
+    RLK_ERR_LAUNCH = 4,          /* a CUDA launch or attribute call failed */
+} rlk_status_t;
+
+/* bits of *device_error_word */
+#define RLK_DEVERR_TARGET_RANGE 0x1u   /* an active row's target id is outside [0, V) */
+#define RLK_DEVERR_WAIT_TIMEOUT 0x2u   /* a pipeline wait gave up (the results are invalid) */
+
+/* Result of rlk_dlogp_audit, written to device memory. */
+typedef struct {
+    int64_t active_count;   /* number of active tokens (exact) */
+    int64_t argmax_index;   /* lowest token index attaining max |d|; -1 if none is active */
+    double mean_dlogp;      /* sum d / count   (NaN when count == 0) */
+    double approx_kl;       /* sum (exp(d) - 1 - d) / count   (NaN when count == 0) */
+    float max_abs_dlogp;    /* max |d| over active tokens (0 when none; NaN ranks highest) */
+    uint32_t error_flags;   /* bit 0: an active d was not finite */
+} rlk_audit_result_t;
+
+/* Scratch bytes each entry point needs for these sizes (pure arithmetic, no CUDA call). */
+size_t rlk_linear_logp_fwd_workspace_bytes(int64_t N, int64_t H, int64_t V);
+size_t rlk_linear_logp_bwd_workspace_bytes(int64_t N, int64_t H, int64_t V);
+size_t rlk_dlogp_audit_workspace_bytes(int64_t N);
+
+/*
+ * Forward.  "RL-Kernel Roadmap (2026)" P0.2; "RL-Kernel integration roadmap
+ * for vime", linear_logp: local max, global max, local sum-exp, global
+ * sum-exp, selected target logit, final downcast point.
+ *
+ *   hidden      [N,H] bf16        weight [V,H] bf16
+ *   targets     [N] int64         active_mask [N] uint8 or NULL
+ *   temperature T > 0, finite; logits are divided by T before the softmax
+ *   logp_out    [N] fp32: logp of active rows, 0 for inactive rows
+ *   lse_out     [N] fp32 or NULL: log(sum_v exp(s[t,v]/T)) of active rows,
+ *               0 for inactive rows; the backward takes it back
+ *   workspace   >= rlk_linear_logp_fwd_workspace_bytes(N, H, V) bytes
+ * Logits stay fp32 and are never rounded; logp and lse are fp32.
+ */
+rlk_status_t rlk_linear_logp_fwd(const void* hidden, const void* weight,
+                                 const int64_t* targets, const uint8_t* active_mask,
+                                 int64_t N, int64_t H, int64_t V, double temperature,
+                                 float* logp_out, float* lse_out,
+                                 void* workspace, size_t workspace_bytes,
+                                 uint32_t* device_error_word, cudaStream_t stream);
+
+/*
+ * Backward by chunked recompute.  "RL-Kernel Roadmap (2026)" P0.2 (the
+ * backward recomputes tiles instead of storing logits); "RL-Kernel
+ * integration roadmap for vime", linear_logp (dlogits kept as operator-owned
+ * workspace, full-gradient training).  With p = softmax(s[t,:]/T) rebuilt
+ * from the forward's lse and grad_logp[t] = g_t = dL/dlogp_t:
+ *
+ *   dhidden[t] = sum_v g_t (delta(v,y_t) - p[t,v]) W_v / T
+ *   dweight[v] = sum_t g_t (delta(v,y_t) - p[t,v]) h_t / T
+ *
+ *   grad_logp  [N] fp32; lse [N] fp32 from rlk_linear_logp_fwd (same inputs)
+ *   dhidden    [N,H] bf16 out (0 on inactive rows)
+ *   dweight    [V,H] bf16 out, overwritten
+ * Accumulation is fp32; dhidden and dweight are rounded to bf16 once (RNE).
+ * Inactive rows add nothing to dweight, but their hidden rows must hold
+ * finite values (a NaN there would reach dweight through 0 * NaN).
+ */
+rlk_status_t rlk_linear_logp_bwd(const void* hidden, const void* weight,
+                                 const int64_t* targets, const uint8_t* active_mask,
+                                 const float* grad_logp, const float* lse,
+                                 int64_t N, int64_t H, int64_t V, double temperature,
+                                 void* dhidden, void* dweight,
+                                 void* workspace, size_t workspace_bytes,
+                                 uint32_t* device_error_word, cudaStream_t stream);
+
+/*
+ * Masked dlogp audit.  "RL-Kernel integration roadmap for vime", Consistency
+ * Contract: dlogp = recomputed - old over active tokens only; max_abs_dlogp
+ * (the primary metric) with the worst-token index; approx_kl0 =
+ * mean(exp(dlogp) - 1 - dlogp); active-token count.
+ *
+ *   logp_new, logp_old [N] fp32; active_mask [N] uint8 or NULL
+ *   result_dev  one rlk_audit_result_t in device memory (overwritten)
+ * Fixed-size blocks and fixed-order trees: the result is bitwise
+ * reproducible for a given N.
+ */
+rlk_status_t rlk_dlogp_audit(const float* logp_new, const float* logp_old,
+                             const uint8_t* active_mask, int64_t N,
+                             rlk_audit_result_t* result_dev,
+                             void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Build fingerprint and the fixed numeric contract (tile shapes, chunk widths,
+ * accumulation and rounding points).  Static string, never NULL. */
+const char* rlk_contract_string(void);
+
+/* Human-readable name of a status code.  Static string, never NULL. */
+const char* rlk_status_string(rlk_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RLK_H_ */

@@ -235,6 +235,24 @@ def linear_logp_bwd_dw_parallel(h, w, y, mask, g, lse, temperature, v_begin, v_e
     return out
 
 
+def linear_logp_bwd_dw_blocks(h, w, y, mask, g, lse, temperature, v_begin, v_end, consume,
+                              rows_per_block=256, threads=None):
+    """dW rows [v_begin, v_end) in blocks of rows_per_block, each handed to
+    consume(v0, block) (called from worker threads) instead of being stored;
+    the rows are computed exactly as by linear_logp_bwd_dw."""
+    h = _c(h, np.float64)
+    w = _c(w, np.float64)
+    starts = list(range(v_begin, v_end, rows_per_block))
+    threads = threads or max(1, len(os.sched_getaffinity(0)))
+
+    def fn(v0):
+        v1 = min(v_end, v0 + rows_per_block)
+        consume(v0, linear_logp_bwd_dw(h, w, y, mask, g, lse, temperature, v0, v1))
+
+    with ThreadPoolExecutor(min(threads, max(1, len(starts)))) as ex:
+        list(ex.map(fn, starts))
+
+
 # ----------------------------------------------------------------------------- audit / loss
 
 def dlogp_audit(logp_new, logp_old, mask):

@@ -1,0 +1,239 @@
+// api.cu -- the C ABI (include/rlk.h): argument validation, TMA tensor maps,
+// and the launch sequence of each entry point.  Every argument error is
+// detected on the host before anything is enqueued, so invalid calls never
+// reach the GPU.  The library allocates nothing and never synchronises.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdio>
+#include <mutex>
+
+#include "rlk_internal.h"
+
+namespace {
+
+using rlk::align_up;
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+struct DeviceInfo {
+    int sms = 0;
+    bool supported = false;
+    bool valid = false;
+};
+
+// SM count and architecture of the current device (queried once per device).
+rlk_status_t current_device(DeviceInfo& out) {
+    static std::mutex mu;
+    static DeviceInfo cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return RLK_ERR_LAUNCH;
+    std::lock_guard<std::mutex> lock(mu);
+    DeviceInfo& d = cache[dev];
+    if (!d.valid) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return RLK_ERR_LAUNCH;
+        d.sms = sms;
+        d.supported = (major == 10 && minor == 3);
+        d.valid = true;
+    }
+    out = d;
+    return out.supported ? RLK_OK : RLK_ERR_UNSUPPORTED;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// 2D bf16 tensor map, 128-byte swizzle, zero fill outside the tensor.
+rlk_status_t make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                      uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (fn == nullptr) return RLK_ERR_LAUNCH;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? RLK_OK : RLK_ERR_LAUNCH;
+}
+
+rlk_status_t check_shape(int64_t N, int64_t H, int64_t V, double temperature) {
+    if (N < 0 || N > kMaxDim || V < 1 || V > kMaxDim || H < 1) return RLK_ERR_INVALID_VALUE;
+    if (!(std::isfinite(temperature) && temperature > 0.0)) return RLK_ERR_INVALID_VALUE;
+    if (H % 64 != 0 || H > (int64_t(1) << 24)) return RLK_ERR_UNSUPPORTED;
+    return RLK_OK;
+}
+
+#define RLK_TRY(expr)                        \
+    do {                                     \
+        rlk_status_t s_ = (expr);            \
+        if (s_ != RLK_OK) return s_;         \
+    } while (0)
+
+#define RLK_CUDA(expr)                                    \
+    do {                                                  \
+        if ((expr) != cudaSuccess) return RLK_ERR_LAUNCH; \
+    } while (0)
+
+}  // namespace
+
+extern "C" {
+
+size_t rlk_linear_logp_fwd_workspace_bytes(int64_t N, int64_t H, int64_t V) {
+    (void)H;
+    if (N < 0 || V < 1) return 0;
+    return rlk::FwdLayout(N, V).total;
+}
+
+size_t rlk_linear_logp_bwd_workspace_bytes(int64_t N, int64_t H, int64_t V) {
+    (void)V;
+    if (N < 0 || H < 0) return 0;
+    return rlk::BwdLayout(N, H).total;
+}
+
+size_t rlk_dlogp_audit_workspace_bytes(int64_t N) {
+    if (N < 0) return 0;
+    return align_up(rlk::audit_blocks(N) * sizeof(rlk::AuditPartial), 256) + 256;
+}
+
+rlk_status_t rlk_linear_logp_fwd(const void* hidden, const void* weight, const int64_t* targets,
+                                 const uint8_t* active_mask, int64_t N, int64_t H, int64_t V,
+                                 double temperature, float* logp_out, float* lse_out,
+                                 void* workspace, size_t workspace_bytes,
+                                 uint32_t* device_error_word, cudaStream_t stream) {
+    RLK_TRY(check_shape(N, H, V, temperature));
+    if (N == 0) return RLK_OK;
+    if (hidden == nullptr || weight == nullptr || targets == nullptr || logp_out == nullptr)
+        return RLK_ERR_INVALID_VALUE;
+    if (!aligned(hidden, 16) || !aligned(weight, 16)) return RLK_ERR_INVALID_VALUE;
+    if (workspace == nullptr || !aligned(workspace, 256) ||
+        workspace_bytes < rlk_linear_logp_fwd_workspace_bytes(N, H, V))
+        return RLK_ERR_WORKSPACE;
+    DeviceInfo dev;
+    RLK_TRY(current_device(dev));
+
+    CUtensorMap map_h, map_w;
+    RLK_TRY(make_map(&map_h, hidden, H, N, H * 2, 64, rlk::kTileM));
+    RLK_TRY(make_map(&map_w, weight, H, V, H * 2, 64, rlk::kTileV));
+    const float k = static_cast<float>(1.4426950408889634074 / temperature);
+    RLK_CUDA(rlk::launch_fwd(map_h, map_w, targets, active_mask, static_cast<int>(N),
+                             static_cast<int>(H), static_cast<int>(V), k, logp_out, lse_out,
+                             workspace, device_error_word, dev.sms, stream));
+    return RLK_OK;
+}
+
+rlk_status_t rlk_linear_logp_bwd(const void* hidden, const void* weight, const int64_t* targets,
+                                 const uint8_t* active_mask, const float* grad_logp,
+                                 const float* lse, int64_t N, int64_t H, int64_t V,
+                                 double temperature, void* dhidden, void* dweight,
+                                 void* workspace, size_t workspace_bytes,
+                                 uint32_t* device_error_word, cudaStream_t stream) {
+    RLK_TRY(check_shape(N, H, V, temperature));
+    if (N == 0) return RLK_OK;
+    if (hidden == nullptr || weight == nullptr || targets == nullptr || grad_logp == nullptr ||
+        lse == nullptr || dhidden == nullptr || dweight == nullptr)
+        return RLK_ERR_INVALID_VALUE;
+    if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(dhidden, 16) ||
+        !aligned(dweight, 16))
+        return RLK_ERR_INVALID_VALUE;
+    if (workspace == nullptr || !aligned(workspace, 256) ||
+        workspace_bytes < rlk_linear_logp_bwd_workspace_bytes(N, H, V))
+        return RLK_ERR_WORKSPACE;
+    DeviceInfo dev;
+    RLK_TRY(current_device(dev));
+
+    const rlk::BwdLayout lay(N, H);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    void* ds = ws + lay.ds_off;
+    float* dh_acc = reinterpret_cast<float*>(ws + lay.dhacc_off);
+    int* sorted_y = reinterpret_cast<int*>(ws + lay.sorted_y_off);
+    int* sorted_t = reinterpret_cast<int*>(ws + lay.sorted_t_off);
+
+    rlk::BwdMaps maps;
+    RLK_TRY(make_map(&maps.h_kmajor, hidden, H, N, H * 2, 64, rlk::kTileM));
+    RLK_TRY(make_map(&maps.w_kmajor, weight, H, V, H * 2, 64, rlk::kTileV));
+    RLK_TRY(make_map(&maps.w_mnmajor, weight, H, V, H * 2, 64, 64));
+    RLK_TRY(make_map(&maps.h_mnmajor, hidden, H, N, H * 2, 64, 64));
+
+    const int n = static_cast<int>(N), h = static_cast<int>(H), v = static_cast<int>(V);
+    const float k = static_cast<float>(1.4426950408889634074 / temperature);
+    const float temp = static_cast<float>(temperature);
+    RLK_CUDA(rlk::launch_target_sort(targets, active_mask, n, v, sorted_y, sorted_t,
+                                     device_error_word, stream));
+    const int num_chunks = static_cast<int>((V + rlk::kBwdChunk - 1) / rlk::kBwdChunk);
+    for (int c = 0; c < num_chunks; ++c) {
+        const int64_t width = std::min<int64_t>(rlk::kBwdChunk, V - int64_t(c) * rlk::kBwdChunk);
+        rlk::ChunkMaps cm;
+        RLK_TRY(make_map(&cm.ds_kmajor, ds, width, N, uint64_t(rlk::kBwdChunk) * 2, 64, rlk::kTileM));
+        RLK_TRY(make_map(&cm.ds_mnmajor, ds, width, N, uint64_t(rlk::kBwdChunk) * 2, 64, 64));
+        RLK_CUDA(rlk::launch_bwd_chunk(maps, cm, targets, active_mask, grad_logp, lse, hidden,
+                                       weight, n, h, v, c, num_chunks, k, temp, ds, dh_acc,
+                                       sorted_y, sorted_t, dhidden, dweight, device_error_word,
+                                       dev.sms, stream));
+    }
+    return RLK_OK;
+}
+
+rlk_status_t rlk_dlogp_audit(const float* logp_new, const float* logp_old,
+                             const uint8_t* active_mask, int64_t N,
+                             rlk_audit_result_t* result_dev, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
+    if (N < 0 || N > (int64_t(1) << 40)) return RLK_ERR_INVALID_VALUE;
+    if (result_dev == nullptr) return RLK_ERR_INVALID_VALUE;
+    if (N > 0 && (logp_new == nullptr || logp_old == nullptr)) return RLK_ERR_INVALID_VALUE;
+    if (workspace == nullptr || !aligned(workspace, 256) ||
+        workspace_bytes < rlk_dlogp_audit_workspace_bytes(N))
+        return RLK_ERR_WORKSPACE;
+    DeviceInfo dev;
+    RLK_TRY(current_device(dev));
+    const bool vec_ok = aligned(logp_new, 16) && aligned(logp_old, 16) &&
+                        (active_mask == nullptr || aligned(active_mask, 4));
+    RLK_CUDA(rlk::launch_audit(logp_new, logp_old, active_mask, N, result_dev, workspace, vec_ok,
+                               stream));
+    return RLK_OK;
+}
+
+#define RLK_STR2(x) #x
+#define RLK_STR(x) RLK_STR2(x)
+
+const char* rlk_contract_string(void) {
+    return "rlk-gb300 linear_logp v1; arch=sm_103a; nvcc=" RLK_STR(__CUDACC_VER_MAJOR__) "." RLK_STR(
+        __CUDACC_VER_MINOR__) "; inputs=bf16; accum=fp32 (tcgen05 kind::f16, TMEM); "
+                              "tile=128x256x64 cta_group::1, no split-K; "
+                              "fwd_vocab_chunk=1024 (merge ascending); bwd_vocab_chunk=16384; "
+                              "exp=ex2.approx.ftz, log=lg2.approx.ftz; k=fp32(log2(e)/T); "
+                              "logits never rounded; logp/lse fp32; dS bf16 (target term fp32); "
+                              "dh/dW rounded once to bf16 (RNE); no float atomics; "
+                              "audit: 4096-element blocks, fixed trees, fp64 partials";
+}
+
+const char* rlk_status_string(rlk_status_t status) {
+    switch (status) {
+        case RLK_OK: return "RLK_OK";
+        case RLK_ERR_INVALID_VALUE: return "RLK_ERR_INVALID_VALUE";
+        case RLK_ERR_UNSUPPORTED: return "RLK_ERR_UNSUPPORTED";
+        case RLK_ERR_WORKSPACE: return "RLK_ERR_WORKSPACE";
+        case RLK_ERR_LAUNCH: return "RLK_ERR_LAUNCH";
+    }
+    return "RLK_ERR_UNKNOWN";
+}
+
+}  // extern "C"

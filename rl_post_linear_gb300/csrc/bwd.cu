@@ -1,0 +1,453 @@
+// bwd.cu -- chunked-recompute backward of the fused linear log-prob.
+//
+// "RL-Kernel Roadmap (2026)", P0.2: the backward recomputes tiles to trade
+// compute for memory instead of storing full logits or probabilities.
+// "RL-Kernel integration roadmap for vime", linear_logp: dlogits live in
+// operator-owned workspace; the operator returns full gradients.
+//
+// With g_t = dL/dlogp_t, k = log2(e)/T and lse2_t = lse_t log2(e):
+//   p[t,v]  = 2^(S[t,v] k - lse2_t)                 (S recomputed, fp32)
+//   dS[t,v] = -(g_t / T) p[t,v]        (bf16, every v including y_t)
+//   dh_t    = bf16( sum_c (dS_c W_c)_t  +  (g_t / T) W[y_t] )
+//   dW_v    = bf16( (dS^T h)_v  +  sum_{t : y_t = v} (g_t / T) h_t )
+// The "+ (g/T)" target terms are added in fp32 in the epilogues instead of
+// going through bf16 dS: they dominate the gradient norm, and rounding their
+// coefficient to bf16 would cost about as much accuracy as the final bf16
+// rounding of the outputs.
+//
+// The vocabulary is walked in fixed chunks of kBwdChunk columns, ascending.
+// For each chunk c three persistent tcgen05 GEMMs run on the stream:
+//   DsPolicy  S_c = h W_c^T (K = H) -> dS_c [N, chunk] bf16 workspace
+//   DhPolicy  dS_c W_c (K = chunk)  -> dh_acc [N, H] fp32 (+= previous chunks;
+//             the last chunk adds the target term and rounds to bf16)
+//   DwPolicy  dS_c^T h (K = N)      -> dW rows of chunk c, plus target terms
+// None of the reductions is split or done with atomics: dh_t depends only on
+// row t's inputs and the fixed chunk boundaries, so it is batch invariant;
+// dW is reproducible bit for bit.
+//
+// The target terms of dW need, for each vocab row v, the tokens with y_t = v
+// in ascending t.  target_rank_kernel builds that list without atomics: each
+// token's rank is the number of (key, index) pairs smaller than its own, the
+// key being y_t for active rows with a valid target and V otherwise.
+#include <cuda_bf16.h>
+
+#include "gemm.cuh"
+
+namespace rlk {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ bool row_live(const int64_t* targets, const uint8_t* mask, int t, int N,
+                                         int V, int64_t& y) {
+    y = 0;
+    if (t >= N) return false;
+    if (mask != nullptr && mask[t] == 0) return false;
+    y = targets[t];
+    return y >= 0 && y < V;
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(uint4 v, float* out) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        out[2 * i] = __uint_as_float(w[i] << 16);
+        out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+// ----------------------------------------------------------------------------- dS_c
+
+struct DsPolicy {
+    static constexpr bool kAMn = false;   // h [N,H]
+    static constexpr bool kBMn = false;   // W [V,H]
+
+    const int64_t* targets;
+    const uint8_t* mask;
+    const float* grad;
+    const float* lse;
+    __nv_bfloat16* ds;    // [N][kBwdChunk]
+    int N, V, c0, num_m, num_n, kblocks;
+    float k, temp;
+
+    __device__ int num_units() const { return num_m * num_n; }
+    __device__ int k_blocks() const { return kblocks; }
+    __device__ int tiles_in_unit(int) const { return 1; }
+    __device__ void coords(int u, int, int& a_mn, int& a_k, int& b_mn, int& b_k) const {
+        const int n = u / num_m;
+        const int m = u - n * num_m;
+        a_mn = m * kTileM;
+        a_k = 0;
+        b_mn = c0 + n * kTileV;
+        b_k = 0;
+    }
+
+    struct EpiState {
+        float coef, lse2;
+        bool live;
+    };
+
+    __device__ void epi_begin(int u, int row, EpiState& st) const {
+        const int n = u / num_m;
+        const int t = (u - n * num_m) * kTileM + row;
+        int64_t y;
+        st.live = row_live(targets, mask, t, N, V, y);
+        st.coef = st.live ? -__fdiv_rn(grad[t], temp) : 0.f;
+        st.lse2 = st.live ? lse[t] * kLog2e : 0.f;
+    }
+
+    __device__ void epi_tile(int u, int, int row, uint32_t taddr, EpiState& st) const {
+        const int n = u / num_m;
+        const int t = (u - n * num_m) * kTileM + row;
+#pragma unroll 1
+        for (int cc = 0; cc < kTileV / 32; ++cc) {
+            uint32_t r[32];
+            tmem_load_32(taddr + cc * 32, r);
+            if (t >= N) continue;
+            const int col = n * kTileV + cc * 32;   // column inside the chunk
+            const int vb = c0 + col;
+            uint32_t packed[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float s0 = __uint_as_float(r[2 * j]);
+                const float s1 = __uint_as_float(r[2 * j + 1]);
+                const float d0 = (st.live && vb + 2 * j < V)
+                                     ? st.coef * ex2_approx(fmaf(s0, k, -st.lse2)) : 0.f;
+                const float d1 = (st.live && vb + 2 * j + 1 < V)
+                                     ? st.coef * ex2_approx(fmaf(s1, k, -st.lse2)) : 0.f;
+                packed[j] = pack_bf16x2(d0, d1);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(ds + static_cast<size_t>(t) * kBwdChunk + col);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                    packed[4 * i + 3]);
+        }
+    }
+
+    __device__ void epi_end(int, int, EpiState&) const {}
+};
+
+// ----------------------------------------------------------------------------- dh
+
+struct DhPolicy {
+    static constexpr bool kAMn = false;   // dS_c [N, width]: K (vocab) contiguous
+    static constexpr bool kBMn = true;    // W_c [width, H]: N (hidden) contiguous
+
+    const int64_t* targets;
+    const uint8_t* mask;
+    const float* grad;
+    const __nv_bfloat16* weight;   // [V][H]
+    float* dh_acc;                 // [N][H]
+    __nv_bfloat16* dh;             // [N][H]
+    int N, V, H, c0, num_m, num_n, kblocks;
+    bool first, last;
+    float temp;
+
+    __device__ int num_units() const { return num_m * num_n; }
+    __device__ int k_blocks() const { return kblocks; }
+    __device__ int tiles_in_unit(int) const { return 1; }
+    __device__ void coords(int u, int, int& a_mn, int& a_k, int& b_mn, int& b_k) const {
+        const int m = u / num_n;
+        const int n = u - m * num_n;
+        a_mn = m * kTileM;
+        a_k = 0;
+        b_mn = n * kTileV;
+        b_k = c0;
+    }
+
+    struct EpiState {
+        float coef;
+        int64_t y;
+        bool live;
+    };
+
+    __device__ void epi_begin(int u, int row, EpiState& st) const {
+        const int m = u / num_n;
+        const int t = m * kTileM + row;
+        st.live = row_live(targets, mask, t, N, V, st.y);
+        st.coef = st.live ? __fdiv_rn(grad[t], temp) : 0.f;
+    }
+
+    __device__ void epi_tile(int u, int, int row, uint32_t taddr, EpiState& st) const {
+        const int m = u / num_n;
+        const int n = u - m * num_n;
+        const int t = m * kTileM + row;
+#pragma unroll 1
+        for (int cc = 0; cc < kTileV / 32; ++cc) {
+            uint32_t r[32];
+            tmem_load_32(taddr + cc * 32, r);
+            const int col = n * kTileV + cc * 32;
+            if (t >= N || col >= H) continue;
+            float x[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
+            float* acc = dh_acc + static_cast<size_t>(t) * H + col;
+            if (!first) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 pv = reinterpret_cast<const float4*>(acc)[i];
+                    x[4 * i] = pv.x + x[4 * i];
+                    x[4 * i + 1] = pv.y + x[4 * i + 1];
+                    x[4 * i + 2] = pv.z + x[4 * i + 2];
+                    x[4 * i + 3] = pv.w + x[4 * i + 3];
+                }
+            }
+            if (!last) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    reinterpret_cast<float4*>(acc)[i] =
+                        make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+                continue;
+            }
+            if (st.live) {
+                const uint4* wr = reinterpret_cast<const uint4*>(
+                    weight + static_cast<size_t>(st.y) * H + col);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float wv[8];
+                    bf16x8_to_f32(wr[i], wv);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) x[8 * i + j] = fmaf(st.coef, wv[j], x[8 * i + j]);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) x[j] = 0.f;
+            }
+            uint4* dst = reinterpret_cast<uint4*>(dh + static_cast<size_t>(t) * H + col);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(pack_bf16x2(x[8 * i], x[8 * i + 1]),
+                                    pack_bf16x2(x[8 * i + 2], x[8 * i + 3]),
+                                    pack_bf16x2(x[8 * i + 4], x[8 * i + 5]),
+                                    pack_bf16x2(x[8 * i + 6], x[8 * i + 7]));
+        }
+    }
+
+    __device__ void epi_end(int, int, EpiState&) const {}
+};
+
+// ----------------------------------------------------------------------------- dW
+
+struct DwPolicy {
+    static constexpr bool kAMn = true;    // dS_c^T: vocab (M) contiguous, tokens along K
+    static constexpr bool kBMn = true;    // h: hidden (N) contiguous, tokens along K
+
+    const float* grad;
+    const __nv_bfloat16* hidden;   // [N][H]
+    __nv_bfloat16* dw;             // [V][H]
+    const int* sorted_y;           // [N] ascending; V marks rows without a target term
+    const int* sorted_t;           // [N]
+    int N, H, c0, width, num_m, num_n, kblocks;
+    float temp;
+
+    __device__ int num_units() const { return num_m * num_n; }
+    __device__ int k_blocks() const { return kblocks; }
+    __device__ int tiles_in_unit(int) const { return 1; }
+    __device__ void coords(int u, int, int& a_mn, int& a_k, int& b_mn, int& b_k) const {
+        const int m = u / num_n;
+        const int n = u - m * num_n;
+        a_mn = m * kTileM;
+        a_k = 0;
+        b_mn = n * kTileV;
+        b_k = 0;
+    }
+
+    struct EpiState {
+        int lo, hi, v;
+        bool valid;
+    };
+
+    __device__ void epi_begin(int u, int row, EpiState& st) const {
+        const int m = u / num_n;
+        const int vl = m * kTileM + row;
+        st.valid = vl < width;
+        st.v = c0 + vl;
+        st.lo = st.hi = 0;
+        if (!st.valid) return;
+        int lo = 0, hi = N;                  // first index with sorted_y >= v
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (sorted_y[mid] < st.v) lo = mid + 1; else hi = mid;
+        }
+        int e = lo;
+        while (e < N && sorted_y[e] == st.v) ++e;
+        st.lo = lo;
+        st.hi = e;
+    }
+
+    __device__ void epi_tile(int u, int, int, uint32_t taddr, EpiState& st) const {
+        const int m = u / num_n;
+        const int n = u - m * num_n;
+        (void)m;
+#pragma unroll 1
+        for (int cc = 0; cc < kTileV / 32; ++cc) {
+            uint32_t r[32];
+            tmem_load_32(taddr + cc * 32, r);
+            const int col = n * kTileV + cc * 32;
+            if (!st.valid || col >= H) continue;
+            float x[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
+            for (int i = st.lo; i < st.hi; ++i) {
+                const int t = sorted_t[i];
+                const float coef = __fdiv_rn(grad[t], temp);
+                const uint4* hr = reinterpret_cast<const uint4*>(
+                    hidden + static_cast<size_t>(t) * H + col);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float hv[8];
+                    bf16x8_to_f32(hr[q], hv);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) x[8 * q + j] = fmaf(coef, hv[j], x[8 * q + j]);
+                }
+            }
+            uint4* dst = reinterpret_cast<uint4*>(dw + static_cast<size_t>(st.v) * H + col);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(pack_bf16x2(x[8 * i], x[8 * i + 1]),
+                                    pack_bf16x2(x[8 * i + 2], x[8 * i + 3]),
+                                    pack_bf16x2(x[8 * i + 4], x[8 * i + 5]),
+                                    pack_bf16x2(x[8 * i + 6], x[8 * i + 7]));
+        }
+    }
+
+    __device__ void epi_end(int, int, EpiState&) const {}
+};
+
+// ----------------------------------------------------------------------------- target list
+
+constexpr int kRankThreads = 256;
+constexpr int kRankTile = 2048;
+
+__device__ __forceinline__ int target_key(const int64_t* targets, const uint8_t* mask, int t, int V) {
+    if (mask != nullptr && mask[t] == 0) return V;
+    const int64_t y = targets[t];
+    return (y >= 0 && y < V) ? static_cast<int>(y) : V;
+}
+
+__global__ void __launch_bounds__(kRankThreads)
+    target_rank_kernel(const int64_t* __restrict__ targets, const uint8_t* __restrict__ mask, int N,
+                       int V, int* __restrict__ sorted_y, int* __restrict__ sorted_t,
+                       uint32_t* err) {
+    __shared__ int keys[kRankTile];
+    const int t = blockIdx.x * kRankThreads + threadIdx.x;
+    int my = V;
+    if (t < N) {
+        my = target_key(targets, mask, t, V);
+        if ((mask == nullptr || mask[t] != 0) && my == V && err != nullptr)
+            atomicOr(err, RLK_DEVERR_TARGET_RANGE);
+    }
+    int rank = 0;
+    for (int base = 0; base < N; base += kRankTile) {
+        const int cnt = min(kRankTile, N - base);
+        __syncthreads();
+        for (int i = threadIdx.x; i < cnt; i += kRankThreads)
+            keys[i] = target_key(targets, mask, base + i, V);
+        __syncthreads();
+        if (t < N) {
+            for (int i = 0; i < cnt; ++i) {
+                const int ku = keys[i];
+                rank += (ku < my || (ku == my && base + i < t)) ? 1 : 0;
+            }
+        }
+    }
+    if (t < N) {
+        sorted_y[rank] = my;
+        sorted_t[rank] = t;
+    }
+}
+
+cudaError_t launch_target_sort(const int64_t* targets, const uint8_t* mask, int N, int V,
+                               int* sorted_y, int* sorted_t, uint32_t* err, cudaStream_t stream) {
+    target_rank_kernel<<<(N + kRankThreads - 1) / kRankThreads, kRankThreads, 0, stream>>>(
+        targets, mask, N, V, sorted_y, sorted_t, err);
+    return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------- launch
+
+template <class P>
+static cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const P& p, int units,
+                               int num_sms, uint32_t* err, cudaStream_t stream) {
+    auto kern = gemm_persistent_kernel<P>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kGemmSmemBytes));
+    if (e != cudaSuccess) return e;
+    const int grid = units < num_sms ? units : num_sms;
+    kern<<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(a, b, p, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_chunk(const BwdMaps& maps, const ChunkMaps& cmaps, const int64_t* targets,
+                             const uint8_t* mask, const float* grad, const float* lse,
+                             const void* hidden, const void* weight, int N, int H, int V,
+                             int chunk, int num_chunks, float k, float temp, void* ds,
+                             float* dh_acc, const int* sorted_y, const int* sorted_t,
+                             void* dhidden, void* dweight, uint32_t* err, int num_sms,
+                             cudaStream_t stream) {
+    const int c0 = chunk * kBwdChunk;
+    const int width = (V - c0) < kBwdChunk ? (V - c0) : kBwdChunk;
+    const int num_m = (N + kTileM - 1) / kTileM;
+
+    DsPolicy ps;
+    ps.targets = targets;
+    ps.mask = mask;
+    ps.grad = grad;
+    ps.lse = lse;
+    ps.ds = static_cast<__nv_bfloat16*>(ds);
+    ps.N = N;
+    ps.V = V;
+    ps.c0 = c0;
+    ps.num_m = num_m;
+    ps.num_n = (width + kTileV - 1) / kTileV;
+    ps.kblocks = H / 64;
+    ps.k = k;
+    ps.temp = temp;
+    cudaError_t e = launch_gemm(maps.h_kmajor, maps.w_kmajor, ps, ps.num_m * ps.num_n, num_sms,
+                                err, stream);
+    if (e != cudaSuccess) return e;
+
+    DhPolicy pd;
+    pd.targets = targets;
+    pd.mask = mask;
+    pd.grad = grad;
+    pd.weight = static_cast<const __nv_bfloat16*>(weight);
+    pd.dh_acc = dh_acc;
+    pd.dh = static_cast<__nv_bfloat16*>(dhidden);
+    pd.N = N;
+    pd.V = V;
+    pd.H = H;
+    pd.c0 = c0;
+    pd.num_m = num_m;
+    pd.num_n = (H + kTileV - 1) / kTileV;
+    pd.kblocks = (width + 63) / 64;
+    pd.first = chunk == 0;
+    pd.last = chunk == num_chunks - 1;
+    pd.temp = temp;
+    e = launch_gemm(cmaps.ds_kmajor, maps.w_mnmajor, pd, pd.num_m * pd.num_n, num_sms, err, stream);
+    if (e != cudaSuccess) return e;
+
+    DwPolicy pw;
+    pw.grad = grad;
+    pw.hidden = static_cast<const __nv_bfloat16*>(hidden);
+    pw.dw = static_cast<__nv_bfloat16*>(dweight);
+    pw.sorted_y = sorted_y;
+    pw.sorted_t = sorted_t;
+    pw.N = N;
+    pw.H = H;
+    pw.c0 = c0;
+    pw.width = width;
+    pw.num_m = (width + kTileM - 1) / kTileM;
+    pw.num_n = (H + kTileV - 1) / kTileV;
+    pw.kblocks = (N + 63) / 64;
+    pw.temp = temp;
+    return launch_gemm(cmaps.ds_mnmajor, maps.h_mnmajor, pw, pw.num_m * pw.num_n, num_sms, err,
+                       stream);
+}
+
+}  // namespace rlk

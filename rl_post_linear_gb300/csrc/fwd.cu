@@ -1,0 +1,202 @@
+// fwd.cu -- forward of the fused linear selected-token log-prob.
+//
+// "RL-Kernel Roadmap (2026)", P0.2 Typical Fused Operators: the forward
+// streams vocab blocks with an online softmax and never lands the [N,V]
+// logits.  "RL-Kernel integration roadmap for vime", linear_logp: the merge
+// is explicit -- local max, global max, local sum-exp, global sum-exp,
+// selected target logit, final downcast point.
+//
+// Kernel 1 (gemm_persistent_kernel<FwdPolicy>): a work unit is one 128-row
+// token tile times one vocab chunk of kFwdTilesPerChunk 256-column tiles.
+// For every tile the tensor cores form S = h W^T in TMEM (fp32, K = H in
+// ascending 16-wide steps); one epilogue thread owns one token row and folds
+// the tile's 256 logits, 32 at a time and in ascending column order, into
+// the row's running (max m, sum s) with
+//     m' = max(m, max_j S_j),  s' = s 2^((m - m') k) + sum_j 2^((S_j - m') k),
+// k = log2(e)/T.  Columns >= V are excluded.  The target logit S[t, y_t] is
+// taken from the same accumulator.  At the end of the unit it writes the
+// chunk's partial (m, s), and the target logit if the chunk holds y_t.
+//
+// Kernel 2 (fwd_merge_kernel): one thread per row merges the partials of the
+// chunks in ascending chunk order:
+//     M = max_c m_c,  sigma = sum_c s_c 2^((m_c - M) k),
+//     lse2 = M k + log2(sigma),  logp = (S_y k - lse2) ln 2,  lse = lse2 ln 2.
+// Inactive rows get logp = lse = 0; an active row with an out-of-range target
+// gets logp = NaN and raises RLK_DEVERR_TARGET_RANGE.
+//
+// Batch invariance: a row's arithmetic is a fixed sequence -- the same K
+// order, the same 32-column slices, the same chunk boundaries (functions of
+// V only) and the same merge order -- whatever the row's tile, lane, batch or
+// the number of SMs.  No atomics touch any float.
+#include <cmath>
+
+#include "gemm.cuh"
+
+namespace rlk {
+
+// x[i] for a runtime i in [0, 32) through a fixed 5-level select tree, so
+// that the 32 values stay in registers.
+__device__ __forceinline__ float select32(const float (&x)[32], int i) {
+    float a[16], b[8], c[4], d[2];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) a[j] = (i & 16) ? x[j + 16] : x[j];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) b[j] = (i & 8) ? a[j + 8] : a[j];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) c[j] = (i & 4) ? b[j + 4] : b[j];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) d[j] = (i & 2) ? c[j + 2] : c[j];
+    return (i & 1) ? d[1] : d[0];
+}
+
+struct FwdPolicy {
+    static constexpr bool kAMn = false;   // h [N,H]: K-major
+    static constexpr bool kBMn = false;   // W [V,H]: K-major
+
+    const int64_t* targets;
+    const uint8_t* mask;
+    float2* partials;     // [num_chunks][N]
+    float* s_target;      // [N]
+    int N, V, num_m, num_vt, num_chunks, kblocks;
+    float k;              // log2(e) / T
+
+    __device__ int num_units() const { return num_m * num_chunks; }
+    __device__ int k_blocks() const { return kblocks; }
+    __device__ int tiles_in_unit(int u) const {
+        const int c = u / num_m;
+        return min(kFwdTilesPerChunk, num_vt - c * kFwdTilesPerChunk);
+    }
+    __device__ void coords(int u, int q, int& a_mn, int& a_k, int& b_mn, int& b_k) const {
+        const int c = u / num_m;
+        const int m = u - c * num_m;
+        a_mn = m * kTileM;
+        a_k = 0;
+        b_mn = (c * kFwdTilesPerChunk + q) * kTileV;
+        b_k = 0;
+    }
+
+    struct EpiState {
+        float m, s, sy;
+        int64_t y;
+        bool found;
+    };
+
+    __device__ void epi_begin(int u, int row, EpiState& st) const {
+        const int c = u / num_m;
+        const int t = (u - c * num_m) * kTileM + row;
+        st.m = -INFINITY;
+        st.s = 0.f;
+        st.sy = 0.f;
+        st.found = false;
+        st.y = -1;
+        if (t < N && (mask == nullptr || mask[t] != 0)) st.y = targets[t];
+    }
+
+    __device__ void epi_tile(int u, int q, int row, uint32_t taddr, EpiState& st) const {
+        const int c = u / num_m;
+        const int v0 = (c * kFwdTilesPerChunk + q) * kTileV;
+#pragma unroll 1
+        for (int cc = 0; cc < kTileV / 32; ++cc) {
+            const int vb = v0 + cc * 32;
+            if (vb >= V) break;                       // same for the whole warp
+            uint32_t r[32];
+            tmem_load_32(taddr + cc * 32, r);
+            float x[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
+            const int nv = V - vb;
+            if (nv < 32) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (j >= nv) x[j] = -INFINITY;
+            }
+            const int64_t dy = st.y - vb;
+            if (dy >= 0 && dy < 32) {
+                st.sy = select32(x, static_cast<int>(dy));
+                st.found = true;
+            }
+            float cm = x[0];
+#pragma unroll
+            for (int j = 1; j < 32; ++j) cm = fmaxf(cm, x[j]);
+            const float nm = fmaxf(st.m, cm);
+            float acc = st.s * ex2_approx((st.m - nm) * k);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc += ex2_approx((x[j] - nm) * k);
+            st.s = acc;
+            st.m = nm;
+        }
+    }
+
+    __device__ void epi_end(int u, int row, EpiState& st) const {
+        const int c = u / num_m;
+        const int t = (u - c * num_m) * kTileM + row;
+        if (t >= N) return;
+        partials[static_cast<size_t>(c) * N + t] = make_float2(st.m, st.s);
+        if (st.found) s_target[t] = st.sy;
+    }
+};
+
+__global__ void fwd_merge_kernel(const float2* __restrict__ partials,
+                                 const float* __restrict__ s_target,
+                                 const int64_t* __restrict__ targets,
+                                 const uint8_t* __restrict__ mask, int N, int V, int num_chunks,
+                                 float k, float* __restrict__ logp, float* __restrict__ lse,
+                                 uint32_t* err) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= N) return;
+    if (mask != nullptr && mask[t] == 0) {
+        logp[t] = 0.f;
+        if (lse != nullptr) lse[t] = 0.f;
+        return;
+    }
+    float m = -INFINITY;
+    for (int c = 0; c < num_chunks; ++c) m = fmaxf(m, partials[static_cast<size_t>(c) * N + t].x);
+    float sigma = 0.f;
+    for (int c = 0; c < num_chunks; ++c) {
+        const float2 pc = partials[static_cast<size_t>(c) * N + t];
+        sigma += pc.y * ex2_approx((pc.x - m) * k);
+    }
+    const float lse2 = m * k + lg2_approx(sigma);
+    constexpr float kLn2 = 0.693147180559945309f;
+    if (lse != nullptr) lse[t] = lse2 * kLn2;
+    const int64_t y = targets[t];
+    if (y < 0 || y >= V) {
+        logp[t] = __int_as_float(0x7fc00000);
+        if (err != nullptr) atomicOr(err, RLK_DEVERR_TARGET_RANGE);
+        return;
+    }
+    logp[t] = (s_target[t] * k - lse2) * kLn2;
+}
+
+cudaError_t launch_fwd(const CUtensorMap& map_h, const CUtensorMap& map_w, const int64_t* targets,
+                       const uint8_t* mask, int N, int H, int V, float k, float* logp, float* lse,
+                       void* workspace, uint32_t* err, int num_sms, cudaStream_t stream) {
+    FwdLayout lay(N, V);
+    FwdPolicy p;
+    p.targets = targets;
+    p.mask = mask;
+    p.partials = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + lay.partial_off);
+    p.s_target = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + lay.target_off);
+    p.N = N;
+    p.V = V;
+    p.num_m = (N + kTileM - 1) / kTileM;
+    p.num_vt = (V + kTileV - 1) / kTileV;
+    p.num_chunks = static_cast<int>(lay.num_chunks);
+    p.kblocks = H / 64;
+    p.k = k;
+
+    auto kern = gemm_persistent_kernel<FwdPolicy>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kGemmSmemBytes));
+    if (e != cudaSuccess) return e;
+    const long long units = static_cast<long long>(p.num_m) * p.num_chunks;
+    const int grid = static_cast<int>(units < num_sms ? units : num_sms);
+    kern<<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(map_h, map_w, p, err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    fwd_merge_kernel<<<(N + 255) / 256, 256, 0, stream>>>(p.partials, p.s_target, targets, mask, N,
+                                                          V, p.num_chunks, k, logp, lse, err);
+    return cudaGetLastError();
+}
+
+}  // namespace rlk

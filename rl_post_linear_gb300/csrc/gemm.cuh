@@ -1,0 +1,260 @@
+// gemm.cuh -- persistent, warp-specialised bf16 GEMM mainloop for sm_103a.
+//
+//   warp 0      : TMA producer (one elected lane) filling a kStages-deep ring
+//                 of shared-memory stages (A 128x64, B 256x64, 128-byte swizzle)
+//   warp 1      : TMEM allocator and MMA issuer (one elected lane):
+//                 tcgen05.mma.cta_group::1.kind::f16, M=128 N=256 K=16,
+//                 fp32 accumulators in TMEM, two 256-column buffers so the
+//                 epilogue of tile i overlaps the MMAs of tile i+1
+//   warps 2..5  : epilogue, one thread per accumulator row (TMEM lane),
+//                 reading 32-column slices with tcgen05.ld
+//
+// The policy P decides the operands' majorness, the work units (a unit is a
+// run of tiles that shares one epilogue state), tile coordinates, the K
+// extent and the epilogue.  Every unit is processed start to finish by one
+// CTA; units are dealt out round-robin (unit = blockIdx.x + i * gridDim.x).
+// Nothing about the arithmetic of a tile depends on the grid: the K loop
+// always runs in ascending 16-wide steps and never splits K.
+//
+// Waits are bounded (wall-clock timeout plus a shared abort flag).  A wait
+// that gives up records RLK_DEVERR_WAIT_TIMEOUT, tells the other roles to
+// stop, waits (bounded) for its own copies and MMAs in flight, and the CTA
+// always frees its TMEM before it exits.
+#pragma once
+
+#include "ptx.cuh"
+#include "rlk_internal.h"
+
+namespace rlk {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr uint32_t kAStageBytes = kBM * kBK * 2;   // 16 KiB
+constexpr uint32_t kBStageBytes = kBN * kBK * 2;   // 32 KiB
+constexpr uint32_t kStageBytes = kAStageBytes + kBStageBytes;
+constexpr uint32_t kTmemCols = 2 * kBN;            // two fp32 accumulators
+constexpr int kGemmThreads = 192;
+constexpr uint32_t kBarrierBytes = 256;
+constexpr uint32_t kGemmSmemBytes = kStages * kStageBytes + kBarrierBytes + 1024;  // + align slack
+constexpr uint64_t kWaitTimeoutNs = 4000000000ull;  // 4 s for one wait: far above any real wait
+constexpr uint64_t kDrainTimeoutNs = 200000000ull;
+
+// One TMA stage of an operand with `ROWS` rows along M (or N) and kBK along K.
+//  K-major  : one box {64 (K), ROWS}; rows are 128 B apart, 8-row groups 1 KiB.
+//  MN-major : ROWS/64 boxes {64 (MN), 64 (K)} of 8 KiB each; within a box the
+//             64 K rows are 128 B apart.
+template <bool MN_MAJOR, int ROWS>
+__device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
+                                             int mn0, int k0) {
+    if constexpr (!MN_MAJOR) {
+        tma_load_2d(dst, map, bar, k0, mn0);
+    } else {
+#pragma unroll
+        for (int i = 0; i < ROWS / 64; ++i) tma_load_2d(dst + i * 8192, map, bar, mn0 + 64 * i, k0);
+    }
+}
+
+// Descriptor of the kk-th 16-wide K slice of a stage.
+//  K-major  : the slice starts 32 B into each 128 B row (SBO = 1 KiB between
+//             8-row groups; LBO unused by the 128 B swizzle).
+//  MN-major : the slice is 16 K rows = two 1 KiB groups further on
+//             (SBO = 1 KiB between 8-row K groups, LBO = 8 KiB between
+//             64-element MN blocks).
+template <bool MN_MAJOR>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t stage_addr, int kk) {
+    if constexpr (!MN_MAJOR) {
+        return smem_desc_sw128(stage_addr + kk * 32, 16, 1024);
+    } else {
+        return smem_desc_sw128(stage_addr + kk * 2048, 8192, 1024);
+    }
+}
+
+__device__ __forceinline__ void report_error(uint32_t* err, uint32_t bits) {
+    if (err != nullptr) atomicOr(err, bits);
+}
+
+template <class P>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_persistent_kernel(const __grid_constant__ CUtensorMap map_a,
+                           const __grid_constant__ CUtensorMap map_b, const P p, uint32_t* err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* a_stages = smem;
+    uint8_t* b_stages = smem + kStages * kAStageBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+    uint64_t* full = bars;                    // [kStages] TMA -> MMA
+    uint64_t* empty = bars + kStages;         // [kStages] MMA -> TMA
+    uint64_t* tmem_full = bars + 2 * kStages; // [2]       MMA -> epilogue
+    uint64_t* tmem_empty = tmem_full + 2;     // [2]       epilogue -> MMA
+    uint64_t* drain = tmem_empty + 2;         // [1]       MMA self-drain
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    volatile int* never = abort_flag + 1;     // stays 0: drain waits ignore the abort flag
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&map_a);
+        prefetch_tensormap(&map_b);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tmem_full[b], 1);
+            mbar_init(&tmem_empty[b], 4);     // one arrival per epilogue warp
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        *never = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    const int units = p.num_units();
+    const int kblocks = p.k_blocks();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_mask = 0, issued_parity = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+                const int nt = p.tiles_in_unit(u);
+                for (int q = 0; ok && q < nt; ++q) {
+                    int a_mn, a_k, b_mn, b_k;
+                    p.coords(u, q, a_mn, a_k, b_mn, b_k);
+                    for (int kb = 0; kb < kblocks; ++kb) {
+                        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, kWaitTimeoutNs)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&full[stage], kStageBytes);
+                        load_operand<P::kAMn, kBM>(a_stages + stage * kAStageBytes, &map_a,
+                                                   &full[stage], a_mn, a_k + kb * kBK);
+                        load_operand<P::kBMn, kBN>(b_stages + stage * kBStageBytes, &map_b,
+                                                   &full[stage], b_mn, b_k + kb * kBK);
+                        issued_mask |= 1u << stage;
+                        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                        if (++stage == kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+            }
+            if (!ok) {
+                report_error(err, RLK_DEVERR_WAIT_TIMEOUT);
+                *abort_flag = 1;
+            }
+            // let every copy this thread started land before the CTA can exit
+            for (int s = 0; s < kStages; ++s)
+                if (issued_mask & (1u << s))
+                    mbar_wait(&full[s], (issued_parity >> s) & 1u, never, kDrainTimeoutNs);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, P::kAMn, P::kBMn);
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t tile_i = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+                const int nt = p.tiles_in_unit(u);
+                for (int q = 0; ok && q < nt; ++q, ++tile_i) {
+                    const uint32_t buf = tile_i & 1u;
+                    const uint32_t use = tile_i >> 1;
+                    if (!mbar_wait(&tmem_empty[buf], (use & 1u) ^ 1u, abort_flag, kWaitTimeoutNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + buf * kBN;
+                    for (int kb = 0; kb < kblocks; ++kb) {
+                        if (!mbar_wait(&full[stage], phase, abort_flag, kWaitTimeoutNs)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a_addr = smem_u32(a_stages + stage * kAStageBytes);
+                        const uint32_t b_addr = smem_u32(b_stages + stage * kBStageBytes);
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk) {
+                            mma_bf16_ss(d_tmem, operand_desc<P::kAMn>(a_addr, kk),
+                                        operand_desc<P::kBMn>(b_addr, kk), idesc,
+                                        (kb > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        mma_commit(&empty[stage]);
+                        if (++stage == kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (ok) mma_commit(&tmem_full[buf]);
+                }
+            }
+            if (!ok) {
+                report_error(err, RLK_DEVERR_WAIT_TIMEOUT);
+                *abort_flag = 1;
+            }
+            // every MMA issued by this thread completes before TMEM is freed
+            mma_commit(drain);
+            mbar_wait(drain, 0, never, kDrainTimeoutNs);
+        }
+    } else {
+        const int quarter = warp & 3;         // TMEM lanes this warp may access
+        const int row = quarter * 32 + lane;
+        const uint32_t taddr_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+        uint32_t tile_i = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+            typename P::EpiState st;
+            p.epi_begin(u, row, st);
+            const int nt = p.tiles_in_unit(u);
+            for (int q = 0; q < nt; ++q, ++tile_i) {
+                const uint32_t buf = tile_i & 1u;
+                const uint32_t use = tile_i >> 1;
+                int got = 1;
+                if (lane == 0) got = mbar_wait(&tmem_full[buf], use & 1u, abort_flag, kWaitTimeoutNs);
+                got = __shfl_sync(0xffffffffu, got, 0);
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                p.epi_tile(u, q, row, taddr_row + buf * kBN, st);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tmem_empty[buf]);
+            }
+            if (!ok) break;
+            p.epi_end(u, row, st);
+        }
+        if (!ok && lane == 0) {
+            report_error(err, RLK_DEVERR_WAIT_TIMEOUT);
+            *abort_flag = 1;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace rlk

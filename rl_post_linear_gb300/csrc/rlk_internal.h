@@ -1,0 +1,101 @@
+// rlk_internal.h -- constants and launcher declarations shared by the
+// translation units of the CUDA library (not part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/rlk.h"
+
+namespace rlk {
+
+// Fixed numeric contract.  None of these may depend on N, the mask or the GPU.
+constexpr int kTileM = 128;                 // tokens per accumulator tile
+constexpr int kTileV = 256;                 // vocab (or hidden) columns per tile
+constexpr int kFwdTilesPerChunk = 4;        // forward vocab chunk = 1024 columns
+constexpr int kFwdChunk = kFwdTilesPerChunk * kTileV;
+constexpr int kBwdChunk = 16384;            // backward vocab chunk (multiple of kTileV)
+constexpr int kAuditThreads = 256;
+constexpr int kAuditPerThread = 16;         // 4 float4 of each input per thread
+constexpr int kAuditBlockElems = kAuditThreads * kAuditPerThread;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Forward workspace: per (vocab chunk, row) partials {max s, sum 2^((s-max)k)},
+// then the target logit per row.
+struct FwdLayout {
+    int64_t num_chunks;
+    size_t partial_off, target_off, total;
+    FwdLayout(int64_t N, int64_t V) {
+        const int64_t vt = (V + kTileV - 1) / kTileV;
+        num_chunks = (vt + kFwdTilesPerChunk - 1) / kFwdTilesPerChunk;
+        partial_off = 0;
+        target_off = align_up(static_cast<size_t>(num_chunks) * N * 8, 256);
+        total = align_up(target_off + static_cast<size_t>(N) * 4, 256);
+    }
+};
+
+// Backward workspace: dS for one vocab chunk [N, kBwdChunk] bf16, the fp32 dh
+// accumulator [N, H], and the (target, token) list sorted by target.
+struct BwdLayout {
+    size_t ds_off, dhacc_off, sorted_y_off, sorted_t_off, total;
+    BwdLayout(int64_t N, int64_t H) {
+        ds_off = 0;
+        dhacc_off = align_up(static_cast<size_t>(N) * kBwdChunk * 2, 256);
+        sorted_y_off = align_up(dhacc_off + static_cast<size_t>(N) * H * 4, 256);
+        sorted_t_off = align_up(sorted_y_off + static_cast<size_t>(N) * 4, 256);
+        total = align_up(sorted_t_off + static_cast<size_t>(N) * 4, 256);
+    }
+};
+
+struct AuditPartial {
+    int64_t count;
+    int64_t arg;
+    double sum_d;
+    double sum_kl;
+    float best;
+    uint32_t flags;
+};
+
+inline size_t audit_blocks(int64_t N) {
+    return static_cast<size_t>((N + kAuditBlockElems - 1) / kAuditBlockElems);
+}
+
+// Launchers (return the first CUDA error, cudaSuccess otherwise).
+cudaError_t launch_fwd(const CUtensorMap& map_h, const CUtensorMap& map_w,
+                       const int64_t* targets, const uint8_t* mask, int N, int H, int V,
+                       float k_log2e_over_t, float* logp, float* lse, void* workspace,
+                       uint32_t* err, int num_sms, cudaStream_t stream);
+
+struct BwdMaps {
+    CUtensorMap h_kmajor;      // hidden [N,H], box {64, 128}: A of the dS recompute
+    CUtensorMap w_kmajor;      // weight [V,H], box {64, 256}: B of the dS recompute
+    CUtensorMap w_mnmajor;     // weight [V,H], box {64, 64}:  B of the dh GEMM
+    CUtensorMap h_mnmajor;     // hidden [N,H], box {64, 64}:  B of the dW GEMM
+};
+
+// Tensor maps over the dS chunk depend on the chunk width; the host builds
+// them per chunk through this callback-free pair.
+struct ChunkMaps {
+    CUtensorMap ds_kmajor;     // dS [N, width], box {64, 128}: A of the dh GEMM
+    CUtensorMap ds_mnmajor;    // dS [N, width], box {64, 64}:  A of the dW GEMM
+};
+
+cudaError_t launch_target_sort(const int64_t* targets, const uint8_t* mask, int N, int V,
+                               int* sorted_y, int* sorted_t, uint32_t* err, cudaStream_t stream);
+
+cudaError_t launch_bwd_chunk(const BwdMaps& maps, const ChunkMaps& cmaps, const int64_t* targets,
+                             const uint8_t* mask, const float* grad, const float* lse,
+                             const void* hidden, const void* weight, int N, int H, int V,
+                             int chunk, int num_chunks, float k_log2e_over_t, float inv_t,
+                             void* ds, float* dh_acc, const int* sorted_y, const int* sorted_t,
+                             void* dhidden, void* dweight, uint32_t* err, int num_sms,
+                             cudaStream_t stream);
+
+cudaError_t launch_audit(const float* logp_new, const float* logp_old, const uint8_t* mask,
+                         int64_t N, rlk_audit_result_t* result, void* workspace, bool vec_ok,
+                         cudaStream_t stream);
+
+}  // namespace rlk

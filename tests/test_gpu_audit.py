@@ -1,0 +1,82 @@
+"""GPU dlogp audit vs the oracle ("RL-Kernel integration roadmap for vime",
+Consistency Contract): exact counts and worst-token index, max|d| equal to the
+fp32 rounding of the oracle's exact difference, mean and approx-KL within
+1e-6 relative (mean: relative to mean |d|), bitwise reproducibility.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rl_post_linear_gb300 as rlk
+import workloads as wl
+from helpers import dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _both(new, old, mask):
+    d = dev()
+    r = rlk.dlogp_audit(new.to(d), old.to(d), None if mask is None else mask.to(d))
+    o = oracle.dlogp_audit(new.numpy(), old.numpy(), None if mask is None else mask.numpy())
+    return r, o
+
+
+def _check(r, o, new, old, mask):
+    assert r["active_count"] == o["active_count"]
+    assert r["argmax_index"] == o["argmax_index"]
+    assert r["max_abs_dlogp"] == np.float32(o["max_abs_dlogp"])
+    if o["active_count"] == 0:
+        assert math.isnan(r["mean_dlogp"]) and math.isnan(r["approx_kl"])
+        return
+    act = np.ones(len(new), bool) if mask is None else mask.numpy() > 0
+    mean_abs = np.mean(np.abs(new.double().numpy() - old.double().numpy())[act])
+    assert abs(r["mean_dlogp"] - o["mean_dlogp"]) <= 1e-6 * mean_abs + 1e-12
+    assert abs(r["approx_kl"] - o["approx_kl"]) <= 1e-6 * abs(o["approx_kl"]) + 1e-15
+
+
+@pytest.mark.parametrize("n", [1, 5, 4095, 4096, 4097, 100003])
+def test_parity_random(n):
+    new, old, mask = wl.audit_inputs(n, n)
+    r, o = _both(new, old, mask)
+    _check(r, o, new, old, mask)
+    r2, _ = _both(new, old, None)
+    o2 = oracle.dlogp_audit(new.numpy(), old.numpy(), None)
+    _check(r2, o2, new, old, None)
+
+
+def test_unaligned_inputs_take_the_scalar_path():
+    new, old, mask = wl.audit_inputs(50001, 3)
+    d = dev()
+    nb, ob, mb = new.to(d), old.to(d), mask.to(d)
+    r = rlk.dlogp_audit(nb[1:], ob[1:], mb[1:])
+    o = oracle.dlogp_audit(new.numpy()[1:], old.numpy()[1:], mask.numpy()[1:])
+    _check(r, o, new[1:], old[1:], mask[1:])
+
+
+def test_degenerate_cases():
+    z = torch.zeros(10)
+    r, o = _both(z, z, torch.zeros(10, dtype=torch.uint8))
+    assert r["active_count"] == 0 and r["argmax_index"] == -1 and r["max_abs_dlogp"] == 0.0
+    assert math.isnan(r["mean_dlogp"])
+    r, o = _both(torch.tensor([0.0, 0.25, -0.25, 0.25]), torch.zeros(4), None)
+    assert r["argmax_index"] == 1 and r["max_abs_dlogp"] == 0.25
+    new = torch.zeros(9000)
+    new[7000] = float("nan")
+    new[8000] = 3.0
+    r, o = _both(new, torch.zeros(9000), None)
+    assert r["argmax_index"] == 7000 and math.isnan(r["max_abs_dlogp"]) and r["error_flags"] & 1
+    r = rlk.dlogp_audit(torch.zeros(0, device=dev()), torch.zeros(0, device=dev()))
+    assert r["active_count"] == 0 and r["argmax_index"] == -1
+
+
+def test_pages_element_count_exact_and_reproducible():
+    n = 9_400_614
+    new, old, mask = wl.audit_inputs(n, 0)
+    r, o = _both(new, old, mask)
+    _check(r, o, new, old, mask)
+    assert r["active_count"] == int(mask.sum())
+    r2, _ = _both(new, old, mask)
+    assert r == r2

@@ -1,0 +1,92 @@
+"""GPU backward vs the fp64 oracle: dh and dW relative L2 <= 2e-3, exact zeros
+on inactive rows, dh batch invariance and dW run-to-run determinism.
+
+Chunked-recompute backward ("RL-Kernel Roadmap (2026)", P0.2;
+"RL-Kernel integration roadmap for vime", linear_logp).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rl_post_linear_gb300 as rlk
+import workloads as wl
+from helpers import GRAD_REL_L2, dev, f64, rel_l2, same_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(n, h, v, seed, std=0.05, active=0.85):
+    hidden = wl.normal_bf16((n, h), seed, wl.S_HIDDEN)
+    weight = wl.normal_bf16((v, h), seed, wl.S_WEIGHT, std=std)
+    targets = wl.uniform_targets(n, v, seed)
+    g = np.random.default_rng(seed)
+    mask = torch.from_numpy((g.random(n) < active).astype(np.uint8))
+    grad = g.standard_normal(n) / max(1, n)
+    grad[mask.numpy() == 0] = 0.0
+    return hidden, weight, targets, mask, grad
+
+
+def _gpu(hidden, weight, targets, mask, grad, T):
+    d = dev()
+    h, w, y = hidden.to(d), weight.to(d), targets.to(d)
+    m = None if mask is None else mask.to(d)
+    err = torch.zeros(1, dtype=torch.int32, device=d)
+    logp, lse = rlk.linear_logp_fwd(h, w, y, m, T, err)
+    g = torch.tensor(grad, dtype=torch.float32, device=d)
+    dh, dw = rlk.linear_logp_bwd(h, w, y, m, g, lse, T, err)
+    torch.cuda.synchronize()
+    return dh.cpu(), dw.cpu(), lse.cpu(), int(err.item())
+
+
+def _oracle(hidden, weight, targets, mask, grad, T):
+    h64, w64 = f64(hidden), f64(weight)
+    m = None if mask is None else mask.numpy()
+    _, lse = oracle.linear_logp_fwd_parallel(h64, w64, targets.numpy(), m, T)
+    dh = oracle.linear_logp_bwd_dh_parallel(h64, w64, targets.numpy(), m, grad, lse, T)
+    dw = oracle.linear_logp_bwd_dw_parallel(h64, w64, targets.numpy(), m, grad, lse, T, 0,
+                                            w64.shape[0])
+    return dh, dw
+
+
+def test_tiny_parity():
+    w = wl.tiny_fwd(0)
+    g = np.random.default_rng(0).standard_normal(w.n) / w.n_active
+    g[w.mask.numpy() == 0] = 0
+    dh, dw, _, err = _gpu(w.hidden, w.weight, w.targets, w.mask, g, w.temperature)
+    assert err == 0
+    dh_o, dw_o = _oracle(w.hidden, w.weight, w.targets, w.mask, g, w.temperature)
+    e_dh, e_dw = rel_l2(dh, dh_o), rel_l2(dw, dw_o)
+    print("bwd parity tiny: rel-L2 dh %.3e dw %.3e" % (e_dh, e_dw))
+    assert e_dh <= GRAD_REL_L2 and e_dw <= GRAD_REL_L2
+    assert torch.all(dh[w.mask == 0] == 0)
+
+
+@pytest.mark.parametrize("n,h,v,T", [(300, 128, 20000, 0.7), (129, 256, 1000, 1.0),
+                                     (70, 64, 16384 + 300, 1.5)])
+def test_multi_chunk_ragged_parity(n, h, v, T):
+    hidden, weight, targets, mask, grad = _case(n, h, v, n + h + v)
+    targets[5] = targets[6] = targets[40] = 17          # a vocab row hit by several tokens
+    mask[5] = mask[6] = mask[40] = 1
+    dh, dw, _, err = _gpu(hidden, weight, targets, mask, grad, T)
+    assert err == 0
+    dh_o, dw_o = _oracle(hidden, weight, targets, mask, grad, T)
+    e_dh, e_dw = rel_l2(dh, dh_o), rel_l2(dw, dw_o)
+    print("bwd parity n=%d h=%d v=%d: rel-L2 dh %.3e dw %.3e" % (n, h, v, e_dh, e_dw))
+    assert e_dh <= GRAD_REL_L2 and e_dw <= GRAD_REL_L2
+    # the row hit by three tokens: every element within one bf16 rounding of the oracle
+    # (a single 128-element row can exceed 2e-3 rel-L2 from the final rounding alone)
+    row, ref = f64(dw[17]), dw_o[17]
+    assert np.all(np.abs(row - ref) <= 2.0 ** -8 * np.abs(ref) * 1.001 + 2.0 ** -16 * np.abs(ref).max())
+    assert torch.all(dh[mask == 0] == 0)
+
+
+def test_dh_batch_invariance_and_dw_determinism():
+    n, h, v = 300, 128, 5000
+    hidden, weight, targets, mask, grad = _case(n, h, v, 11)
+    dh, dw, _, _ = _gpu(hidden, weight, targets, mask, grad, 0.7)
+    dh2, dw2, _, _ = _gpu(hidden, weight, targets, mask, grad, 0.7)
+    assert same_bits(dh, dh2) and same_bits(dw, dw2)
+    for a, b in ((0, 1), (0, 128), (100, 300), (17, 211)):
+        dhp, _, _, _ = _gpu(hidden[a:b], weight, targets[a:b], mask[a:b], grad[a:b], 0.7)
+        assert same_bits(dhp, dh[a:b]), (a, b)
