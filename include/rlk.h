@@ -139,6 +139,31 @@ rlk_status_t rlk_dlogp_audit(const float* logp_new, const float* logp_old,
                              rlk_audit_result_t* result_dev,
                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * Masked dlogp audit that allocates nothing.  The source pages have no
+ * counterpart to this entry point; it exists for callers that cannot call
+ * cudaMalloc.  A rollout engine that reserved nearly all device memory for its
+ * KV cache at start-up, or a framework hook that may only touch the memory
+ * handed to it, can still audit logp without owning a workspace: the scratch
+ * lives in a fixed array inside the library.
+ *
+ * Same inputs, result and arithmetic as rlk_dlogp_audit, minus the workspace.
+ *  - N must not exceed RLK_AUDIT_NOALLOC_MAX_N; larger N returns
+ *    RLK_ERR_UNSUPPORTED before anything is enqueued (use rlk_dlogp_audit).
+ *  - The scratch is a file-scope __device__ array of 1.25 MiB that every GPU
+ *    loading the library holds until the process exits.  Its device address
+ *    is looked up on the first call on each device (with that device current);
+ *    make that first call before any stream capture.
+ *  - Calls share the scratch, which keeps the last call's contents (nothing
+ *    in it needs to start at zero).  Calls that overlap on the GPU -- on
+ *    different streams without ordering -- race and give wrong results.
+ *  - No cudaMalloc, cudaFree or other allocating call is made.
+ */
+#define RLK_AUDIT_NOALLOC_MAX_N ((int64_t)1 << 27)
+rlk_status_t rlk_dlogp_audit_noalloc(const float* logp_new, const float* logp_old,
+                                     const uint8_t* active_mask, int64_t N,
+                                     rlk_audit_result_t* result_dev, cudaStream_t stream);
+
 /* Build fingerprint and the fixed numeric contract (tile shapes, chunk widths,
  * accumulation and rounding points).  Static string, never NULL. */
 const char* rlk_contract_string(void);

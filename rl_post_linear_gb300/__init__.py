@@ -27,6 +27,7 @@ HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "rlk.h")
 RLK_OK, RLK_ERR_INVALID_VALUE, RLK_ERR_UNSUPPORTED, RLK_ERR_WORKSPACE, RLK_ERR_LAUNCH = range(5)
 RLK_DEVERR_TARGET_RANGE = 0x1
 RLK_DEVERR_WAIT_TIMEOUT = 0x2
+RLK_AUDIT_NOALLOC_MAX_N = 1 << 27
 
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -78,6 +79,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                         ctypes.c_double, _vp, _vp, _vp, _sz, _vp, _vp]
     lib.rlk_dlogp_audit.restype = ctypes.c_int
     lib.rlk_dlogp_audit.argtypes = [_vp, _vp, _vp, _i64, _vp, _vp, _sz, _vp]
+    lib.rlk_dlogp_audit_noalloc.restype = ctypes.c_int
+    lib.rlk_dlogp_audit_noalloc.argtypes = [_vp, _vp, _vp, _i64, _vp, _vp]
     lib.rlk_contract_string.restype = ctypes.c_char_p
     lib.rlk_contract_string.argtypes = []
     lib.rlk_status_string.restype = ctypes.c_char_p
@@ -198,6 +201,23 @@ def rlk_dlogp_audit(logp_new, logp_old, active_mask, result, workspace, stream=N
     st = load().rlk_dlogp_audit(_ptr(logp_new), _ptr(logp_old), _ptr(active_mask), n,
                                 _ptr(result), _ptr(workspace), workspace.numel(), _stream(stream))
     _check("rlk_dlogp_audit", st)
+
+
+def rlk_dlogp_audit_noalloc(logp_new, logp_old, active_mask, result, stream=None):
+    """The audit without a workspace, for callers that cannot allocate device memory (a
+    rollout engine that reserved nearly all of it up front, a hook limited to the tensors it
+    is handed).  Scratch is a fixed 1.25 MiB array inside the library, shared by every call:
+    N <= RLK_AUDIT_NOALLOC_MAX_N, and calls must not overlap on the GPU.  The first call on
+    a device looks the array's address up, so make it before any stream capture."""
+    n = logp_new.shape[0]
+    _need(logp_new, torch.float32, "logp_new", (n,))
+    _need(logp_old, torch.float32, "logp_old", (n,))
+    if active_mask is not None:
+        _need(active_mask, torch.uint8, "active_mask", (n,))
+    _need(result, torch.uint8, "result", (AUDIT_RESULT_BYTES,))
+    st = load().rlk_dlogp_audit_noalloc(_ptr(logp_new), _ptr(logp_old), _ptr(active_mask), n,
+                                        _ptr(result), _stream(stream))
+    _check("rlk_dlogp_audit_noalloc", st)
 
 
 # ----------------------------------------------------------------------------- conveniences

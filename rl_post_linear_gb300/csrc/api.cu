@@ -211,6 +211,24 @@ rlk_status_t rlk_dlogp_audit(const float* logp_new, const float* logp_old,
     return RLK_OK;
 }
 
+rlk_status_t rlk_dlogp_audit_noalloc(const float* logp_new, const float* logp_old,
+                                     const uint8_t* active_mask, int64_t N,
+                                     rlk_audit_result_t* result_dev, cudaStream_t stream) {
+    if (N < 0) return RLK_ERR_INVALID_VALUE;
+    if (N > RLK_AUDIT_NOALLOC_MAX_N) return RLK_ERR_UNSUPPORTED;
+    if (result_dev == nullptr) return RLK_ERR_INVALID_VALUE;
+    if (N > 0 && (logp_new == nullptr || logp_old == nullptr)) return RLK_ERR_INVALID_VALUE;
+    DeviceInfo dev;
+    RLK_TRY(current_device(dev));
+    void* scratch = nullptr;
+    RLK_CUDA(rlk::audit_noalloc_scratch(&scratch));
+    const bool vec_ok = aligned(logp_new, 16) && aligned(logp_old, 16) &&
+                        (active_mask == nullptr || aligned(active_mask, 4));
+    RLK_CUDA(rlk::launch_audit(logp_new, logp_old, active_mask, N, result_dev, scratch, vec_ok,
+                               stream));
+    return RLK_OK;
+}
+
 #define RLK_STR2(x) #x
 #define RLK_STR(x) RLK_STR2(x)
 

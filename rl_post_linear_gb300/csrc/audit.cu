@@ -18,6 +18,7 @@
 // through the d^9 term (truncation below 3e-9 relative); elsewhere it is
 // expm1f(d) - d, where no cancellation arises.
 #include <cmath>
+#include <mutex>
 
 #include "rlk_internal.h"
 
@@ -214,6 +215,34 @@ __global__ void __launch_bounds__(kMergeThreads)
 }
 
 }  // namespace
+
+// Scratch of rlk_dlogp_audit_noalloc: one partial per 4096-element block for
+// up to RLK_AUDIT_NOALLOC_MAX_N tokens (32768 x 40 bytes = 1.25 MiB).  It lives
+// in the library image, so every GPU that loads the library holds it until the
+// process exits.  Pass 1 writes every slot that pass 2 reads, so nothing in it
+// has to start at zero; calls that overlap on the GPU share it and race.
+constexpr size_t kNoAllocBlocks = static_cast<size_t>(RLK_AUDIT_NOALLOC_MAX_N) / kAuditBlockElems;
+static __device__ __align__(256) AuditPartial g_audit_noalloc_scratch[kNoAllocBlocks];
+
+cudaError_t audit_noalloc_scratch(void** out) {
+    // Host code cannot use the array's name as a device address: look the
+    // address up once per device, with that device current.
+    static std::mutex mu;
+    static void* addr[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_audit_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return cudaSuccess;
+}
 
 cudaError_t launch_audit(const float* logp_new, const float* logp_old, const uint8_t* mask,
                          int64_t N, rlk_audit_result_t* result, void* workspace, bool vec_ok,

@@ -98,4 +98,7 @@ cudaError_t launch_audit(const float* logp_new, const float* logp_old, const uin
                          int64_t N, rlk_audit_result_t* result, void* workspace, bool vec_ok,
                          cudaStream_t stream);
 
+// Device address (current device) of the library-owned audit scratch.
+cudaError_t audit_noalloc_scratch(void** out);
+
 }  // namespace rlk
