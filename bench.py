@@ -320,9 +320,36 @@ def run_ours(args, world, rank, local):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }
+    out["audit_hbm"] = {str(na): measure_audit(rlk, dev, na, pk["hbm_gbs"])
+                        for na in (9_400_614, 1 << 26)}
     if not args.no_cpu_baseline and world == 1:
         out["cpu_baseline"] = cpu_baseline(w, old.cpu(), g.cpu(), args.cpu_tokens)
     return out
+
+
+def measure_audit(rlk, dev, n, hbm_gbs, reps=10):
+    """The audit alone at N tokens: 9 algorithmic bytes per token (new, old, mask).  L2 is
+    flushed (a 256 MB write) before every timed launch pair, outside the events."""
+    new, old, mask = (t.to(dev) for t in wl.audit_inputs(n, 0))
+    res = torch.empty(rlk.AUDIT_RESULT_BYTES, dtype=torch.uint8, device=dev)
+    ws = torch.empty(rlk.rlk_dlogp_audit_workspace_bytes(n), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        rlk.rlk_dlogp_audit(new, old, mask, res, ws)
+    ms = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        rlk.rlk_dlogp_audit(new, old, mask, res, ws)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    t = float(np.mean(ms))
+    gbs = n * 9 / (t * 1e-3) / 1e9
+    return {"ms": t, "gbs": gbs, "frac_of_hbm": gbs / hbm_gbs, "bytes": n * 9,
+            "l2": "flushed (256 MB write) before each launch pair"}
 
 
 def recorded_traffic(kernel, n, v, h):
@@ -332,7 +359,7 @@ def recorded_traffic(kernel, n, v, h):
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    cur = source_hash()
+    cur = source_hash(kernel)
     for line in open(path):
         parts = line.split()
         if (len(parts) == 6 and parts[0] == kernel and parts[1:4] == [str(n), str(v), str(h)]
@@ -341,10 +368,14 @@ def recorded_traffic(kernel, n, v, h):
     return None
 
 
-def source_hash():
+KERNEL_SOURCES = {"fwd_gemm": ("fwd.cu", "gemm.cuh", "ptx.cuh", "rlk_internal.h")}
+
+
+def source_hash(kernel="fwd_gemm"):
+    """Hash of the source files that define `kernel` (a changed kernel voids old counters)."""
     d = os.path.join(ROOT, "rl_post_linear_gb300", "csrc")
     hsh = hashlib.sha256()
-    for f in sorted(os.listdir(d)):
+    for f in KERNEL_SOURCES[kernel]:
         hsh.update(open(os.path.join(d, f), "rb").read())
     return hsh.hexdigest()[:16]
 

@@ -77,9 +77,13 @@ struct DsPolicy {
     __device__ int num_units() const { return num_m * num_n; }
     __device__ int k_blocks() const { return kblocks; }
     __device__ int tiles_in_unit(int) const { return 1; }
+    // unit -> (token tile m, vocab tile n of the chunk), token tiles grouped
+    __device__ void unit(int u, int& m, int& n) const {
+        grouped_unit(u, num_m, num_n, kRasterTokenTiles, m, n);
+    }
     __device__ void coords(int u, int, int& a_mn, int& a_k, int& b_mn, int& b_k) const {
-        const int n = u / num_m;
-        const int m = u - n * num_m;
+        int m, n;
+        unit(u, m, n);
         a_mn = m * kTileM;
         a_k = 0;
         b_mn = c0 + n * kTileV;
@@ -92,8 +96,9 @@ struct DsPolicy {
     };
 
     __device__ void epi_begin(int u, int row, EpiState& st) const {
-        const int n = u / num_m;
-        const int t = (u - n * num_m) * kTileM + row;
+        int m, n;
+        unit(u, m, n);
+        const int t = m * kTileM + row;
         int64_t y;
         st.live = row_live(targets, mask, t, N, V, y);
         st.coef = st.live ? -__fdiv_rn(grad[t], temp) : 0.f;
@@ -101,8 +106,9 @@ struct DsPolicy {
     }
 
     __device__ void epi_tile(int u, int, int row, uint32_t taddr, EpiState& st) const {
-        const int n = u / num_m;
-        const int t = (u - n * num_m) * kTileM + row;
+        int m, n;
+        unit(u, m, n);
+        const int t = m * kTileM + row;
 #pragma unroll 1
         for (int cc = 0; cc < kTileV / 32; ++cc) {
             uint32_t r[32];
@@ -248,9 +254,13 @@ struct DwPolicy {
     __device__ int num_units() const { return num_m * num_n; }
     __device__ int k_blocks() const { return kblocks; }
     __device__ int tiles_in_unit(int) const { return 1; }
+    // unit -> (vocab tile m of the chunk, hidden tile n), hidden tiles grouped
+    __device__ void unit(int u, int& m, int& n) const {
+        grouped_unit(u, num_n, num_m, kRasterHiddenTiles, n, m);
+    }
     __device__ void coords(int u, int, int& a_mn, int& a_k, int& b_mn, int& b_k) const {
-        const int m = u / num_n;
-        const int n = u - m * num_n;
+        int m, n;
+        unit(u, m, n);
         a_mn = m * kTileM;
         a_k = 0;
         b_mn = n * kTileV;
@@ -263,7 +273,8 @@ struct DwPolicy {
     };
 
     __device__ void epi_begin(int u, int row, EpiState& st) const {
-        const int m = u / num_n;
+        int m, n;
+        unit(u, m, n);
         const int vl = m * kTileM + row;
         st.valid = vl < width;
         st.v = c0 + vl;
@@ -281,9 +292,8 @@ struct DwPolicy {
     }
 
     __device__ void epi_tile(int u, int, int, uint32_t taddr, EpiState& st) const {
-        const int m = u / num_n;
-        const int n = u - m * num_n;
-        (void)m;
+        int m, n;
+        unit(u, m, n);
 #pragma unroll 1
         for (int cc = 0; cc < kTileV / 32; ++cc) {
             uint32_t r[32];

@@ -62,13 +62,18 @@ struct FwdPolicy {
 
     __device__ int num_units() const { return num_m * num_chunks; }
     __device__ int k_blocks() const { return kblocks; }
+    // unit -> (token tile m, vocab chunk c), token tiles grouped by kRasterTokenTiles
+    __device__ void unit(int u, int& m, int& c) const {
+        grouped_unit(u, num_m, num_chunks, kRasterTokenTiles, m, c);
+    }
     __device__ int tiles_in_unit(int u) const {
-        const int c = u / num_m;
+        int m, c;
+        unit(u, m, c);
         return min(kFwdTilesPerChunk, num_vt - c * kFwdTilesPerChunk);
     }
     __device__ void coords(int u, int q, int& a_mn, int& a_k, int& b_mn, int& b_k) const {
-        const int c = u / num_m;
-        const int m = u - c * num_m;
+        int m, c;
+        unit(u, m, c);
         a_mn = m * kTileM;
         a_k = 0;
         b_mn = (c * kFwdTilesPerChunk + q) * kTileV;
@@ -82,8 +87,9 @@ struct FwdPolicy {
     };
 
     __device__ void epi_begin(int u, int row, EpiState& st) const {
-        const int c = u / num_m;
-        const int t = (u - c * num_m) * kTileM + row;
+        int m, c;
+        unit(u, m, c);
+        const int t = m * kTileM + row;
         st.m = -INFINITY;
         st.s = 0.f;
         st.sy = 0.f;
@@ -93,7 +99,8 @@ struct FwdPolicy {
     }
 
     __device__ void epi_tile(int u, int q, int row, uint32_t taddr, EpiState& st) const {
-        const int c = u / num_m;
+        int m, c;
+        unit(u, m, c);
         const int v0 = (c * kFwdTilesPerChunk + q) * kTileV;
 #pragma unroll 1
         for (int cc = 0; cc < kTileV / 32; ++cc) {
@@ -128,8 +135,9 @@ struct FwdPolicy {
     }
 
     __device__ void epi_end(int u, int row, EpiState& st) const {
-        const int c = u / num_m;
-        const int t = (u - c * num_m) * kTileM + row;
+        int m, c;
+        unit(u, m, c);
+        const int t = m * kTileM + row;
         if (t >= N) return;
         partials[static_cast<size_t>(c) * N + t] = make_float2(st.m, st.s);
         if (st.found) s_target[t] = st.sy;

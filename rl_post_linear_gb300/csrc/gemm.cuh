@@ -71,6 +71,29 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t stage_addr, int kk) {
     }
 }
 
+// Grouped raster of a rows x cols grid of work units: units are visited
+// group by group, a group being `group` consecutive rows (the last group may
+// be shorter) times every column, with the row index running fastest inside a
+// group.  Concurrent CTAs then share one group's rows (kept in L2) while the
+// column operand streams.  Only the visiting order changes, never a unit's
+// arithmetic.
+__device__ __forceinline__ void grouped_unit(int u, int rows, int cols, int group, int& r,
+                                             int& c) {
+    const int full = rows / group;
+    const int per_group = group * cols;
+    const int g = u / per_group;
+    if (g < full) {
+        const int l = u - g * per_group;
+        c = l / group;
+        r = g * group + (l - c * group);
+    } else {
+        const int gr = rows - full * group;
+        const int l = u - full * per_group;
+        c = l / gr;
+        r = full * group + (l - c * gr);
+    }
+}
+
 __device__ __forceinline__ void report_error(uint32_t* err, uint32_t bits) {
     if (err != nullptr) atomicOr(err, bits);
 }

@@ -17,6 +17,12 @@ constexpr int kTileV = 256;                 // vocab (or hidden) columns per til
 constexpr int kFwdTilesPerChunk = 4;        // forward vocab chunk = 1024 columns
 constexpr int kFwdChunk = kFwdTilesPerChunk * kTileV;
 constexpr int kBwdChunk = 16384;            // backward vocab chunk (multiple of kTileV)
+// Raster groups (visiting order only; no effect on any result): token tiles per
+// group for the forward and dS GEMMs, hidden tiles per group for the dW GEMM.
+// A group's share of h (32 x 128 rows, or 8 x 256 columns, of H = 4096) is
+// 33.5 MB, which stays resident in L2 while the other operand streams.
+constexpr int kRasterTokenTiles = 32;
+constexpr int kRasterHiddenTiles = 8;
 constexpr int kAuditThreads = 256;
 constexpr int kAuditPerThread = 16;         // 4 float4 of each input per thread
 constexpr int kAuditBlockElems = kAuditThreads * kAuditPerThread;
