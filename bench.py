@@ -1,16 +1,17 @@
 """Benchmark: one step = the whole hot path on one batch of synthetic input.
 
-A step runs, on one stream, the fused linear log-prob forward, the masked
-dlogp audit of its result against the rollout-side old logp, and the
-chunked-recompute backward for the GRPO clipped-ratio upstream gradient --
-the rows of the hot path, all in librlk.so kernels.
+A step runs, on one stream, the fused linear log-prob forward, the GRPO
+clipped-ratio loss fragment (per-token upstream gradient, token-mean over the
+active tokens), the masked dlogp audit of the new logp against the
+rollout-side old logp, and the chunked-recompute backward -- all in
+librlk.so kernels.
 
 Workload (default): the Qwen3-8B-shaped LM head, N = 8192 tokens packed from
 8 sequences, H = 4096, V = 151936, T = 0.7, targets sampled from the softmax
 of the logits, all tokens active; old logp = forward logp + N(0, 0.01^2)
-noise, advantages ~ N(0, 1) per sequence, eps = 0.2 (the GRPO gradient is
-formed once, before timing, as input data).  Inputs are synthetic and
-seeded; W (1.245 GB) is larger than L2, so no flush is needed between steps.
+noise, advantages ~ N(0, 1) per sequence, eps = 0.2.  Inputs are synthetic
+and seeded; W (1.245 GB) is larger than L2, so no flush is needed between
+steps.
 
 Output: one JSON line (rank 0).  ``value`` is whole-job active tokens per
 second with inputs resident in HBM; ``e2e`` is the same metric through the C
@@ -144,17 +145,6 @@ def make_batch(seed, n_tokens=wl.QWEN_N):
     return w, noise, adv
 
 
-def grpo_grad_torch(logp, old, adv, mask, eps):
-    """Per-token gradient of the GRPO clipped-ratio loss (input preparation only)."""
-    active = mask > 0
-    na = max(int(active.sum()), 1)
-    r = torch.exp(logp.double() - old.double())
-    unclipped = r * adv
-    clipped = torch.clamp(r, 1 - eps, 1 + eps) * adv
-    take = (unclipped <= clipped) & active
-    return torch.where(take, -adv * r / na, torch.zeros_like(r)).float()
-
-
 # ----------------------------------------------------------------------------- our arm
 
 def run_ours(args, world, rank, local):
@@ -189,21 +179,27 @@ def run_ours(args, world, rank, local):
     ws_a = torch.empty(rlk.rlk_dlogp_audit_workspace_bytes(n), dtype=torch.uint8, device=dev)
     audit = torch.empty(rlk.AUDIT_RESULT_BYTES, dtype=torch.uint8, device=dev)
 
-    # input preparation: rollout-side old logp and the GRPO upstream gradient
+    # input preparation: the rollout-side old logp (forward logp + noise) and advantages
     rlk.rlk_linear_logp_fwd(hid, wt, y, mask, T, logp, lse, ws_f, err)
     torch.cuda.synchronize()
     old = (logp.double() + torch.from_numpy(noise).to(dev)).float()
-    g = grpo_grad_torch(logp, old, torch.from_numpy(adv).to(dev), mask, GRPO_EPS)
+    advd = torch.from_numpy(adv).float().to(dev)
+    g = torch.empty(n, dtype=torch.float32, device=dev)
+    ws_l = torch.empty(rlk.rlk_grpo_clip_loss_workspace_bytes(n), dtype=torch.uint8, device=dev)
+    loss_res = torch.empty(rlk.GRPO_RESULT_BYTES, dtype=torch.uint8, device=dev)
+    scale = 1.0 / n_act                         # token mean over the batch's active tokens
     n_chunks = -(-v // 16384)
-    launches_per_step = 2 + 2 + 1 + 3 * n_chunks
+    launches_per_step = 2 + 2 + 2 + 1 + 3 * n_chunks
 
-    def step(ev=None):
+    def step(ev=None, old_t=old, adv_t=advd):
         if ev is not None:
             ev[0].record(stream)
         rlk.rlk_linear_logp_fwd(hid, wt, y, mask, T, logp, lse, ws_f, err)
         if ev is not None:
             ev[1].record(stream)
-        rlk.rlk_dlogp_audit(logp, old, mask, audit, ws_a)
+        rlk.rlk_grpo_clip_loss(logp, old_t, adv_t, mask, GRPO_EPS, GRPO_EPS, scale, g, loss_res,
+                               ws_l)
+        rlk.rlk_dlogp_audit(logp, old_t, mask, audit, ws_a)
         if ev is not None:
             ev[2].record(stream)
         rlk.rlk_linear_logp_bwd(hid, wt, y, mask, g, lse, T, dh, dw, ws_b, err)
@@ -228,32 +224,32 @@ def run_ours(args, world, rank, local):
         torch.distributed.barrier()
     total_ms = start.elapsed_time(stop)
     fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
-    aud_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
+    aud_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))   # loss fragment + audit
     bwd_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in evs]))
     if int(err.item()) != 0:
         raise RuntimeError("device error word %#x" % int(err.item()))
 
-    # e2e: per-step inputs from pinned host memory through the C ABI, result read back
+    # e2e: per-step inputs from pinned host memory through the C ABI, results read back
     h_host = w.hidden.pin_memory()
     y_host = w.targets.pin_memory()
     m_host = w.mask.pin_memory()
     old_host = old.cpu().pin_memory()
-    g_host = g.cpu().pin_memory()
+    adv_host = advd.cpu().pin_memory()
     logp_host = torch.empty(n, dtype=torch.float32).pin_memory()
     audit_host = torch.empty(rlk.AUDIT_RESULT_BYTES, dtype=torch.uint8).pin_memory()
-    old_d, g_d = torch.empty_like(old), torch.empty_like(g)
+    loss_host = torch.empty(rlk.GRPO_RESULT_BYTES, dtype=torch.uint8).pin_memory()
+    old_d, adv_d = torch.empty_like(old), torch.empty_like(advd)
 
     def e2e_step():
         hid.copy_(h_host, non_blocking=True)
         y.copy_(y_host, non_blocking=True)
         mask.copy_(m_host, non_blocking=True)
         old_d.copy_(old_host, non_blocking=True)
-        g_d.copy_(g_host, non_blocking=True)
-        rlk.rlk_linear_logp_fwd(hid, wt, y, mask, T, logp, lse, ws_f, err)
-        rlk.rlk_dlogp_audit(logp, old_d, mask, audit, ws_a)
-        rlk.rlk_linear_logp_bwd(hid, wt, y, mask, g_d, lse, T, dh, dw, ws_b, err)
+        adv_d.copy_(adv_host, non_blocking=True)
+        step(None, old_d, adv_d)
         logp_host.copy_(logp, non_blocking=True)
         audit_host.copy_(audit, non_blocking=True)
+        loss_host.copy_(loss_res, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
@@ -266,8 +262,8 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     e2e_ms = e_start.elapsed_time(e_stop)
     h2d = (h_host.numel() * 2 + y_host.numel() * 8 + m_host.numel() + old_host.numel() * 4
-           + g_host.numel() * 4)
-    d2h = logp_host.numel() * 4 + audit_host.numel()
+           + adv_host.numel() * 4)
+    d2h = logp_host.numel() * 4 + audit_host.numel() + loss_host.numel()
 
     total_ms, e2e_ms, fwd_ms, aud_ms, bwd_ms = max_over_ranks(
         [total_ms, e2e_ms, fwd_ms, aud_ms, bwd_ms], world, dev)
@@ -280,7 +276,7 @@ def run_ours(args, world, rank, local):
     fwd_tflops = 2.0 * n_act * h * v / (fwd_ms * 1e-3) / 1e12
     bwd_tflops = 4.0 * n_act * h * v / (bwd_ms * 1e-3) / 1e12
     peak = pk["bf16_tflops_sustained"]
-    audit_gbs = n * 9 / (aud_ms * 1e-3) / 1e9
+    audit_gbs = n * 26 / (aud_ms * 1e-3) / 1e9
     # roofline: the forward GEMM is the largest single launch, and the only GEMM whose entry
     # point holds one GEMM launch (plus a 0.4% merge), so events around it time it directly;
     # the backward group (30 GEMM launches + the target sort) is reported beside it
@@ -297,7 +293,7 @@ def run_ours(args, world, rank, local):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded; Qwen3-8B-shaped LM head, random-init weights)",
-        "config": {"workload": w.name + " fwd+audit+GRPO bwd", "n_tokens": n,
+        "config": {"workload": w.name + " fwd+GRPO loss+audit+bwd", "n_tokens": n,
                    "n_active": n_act, "hidden": h, "vocab": v, "temperature": T,
                    "seq_lens": w.seq_lens, "parallelism": "dp%d (independent batches)" % world,
                    "l2": "inputs larger than L2 (W = %.3f GB), no flush" % (v * h * 2 / 1e9)},
@@ -306,7 +302,8 @@ def run_ours(args, world, rank, local):
         "bwd": {"ms": bwd_ms, "tflops": bwd_tflops, "frac_of_peak": bwd_tflops / peak,
                 "flops": 4.0 * n_act * h * v,
                 "executed_tflops": 6.0 * n * h * v / (bwd_ms * 1e-3) / 1e12},
-        "audit": {"ms": aud_ms, "gbs": audit_gbs, "frac_of_hbm": audit_gbs / pk["hbm_gbs"]},
+        "loss_and_audit": {"ms": aud_ms, "gbs": audit_gbs, "frac_of_hbm": audit_gbs / pk["hbm_gbs"],
+                           "bytes": "N x (4+4+4+1+4 loss, 4+4+1 audit)"},
         "roofline": {"bound": "tensor", "kernel": "gemm_persistent_kernel<FwdPolicy>",
                      "achieved": fwd_tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": fwd_tflops / peak, "traffic": recorded_traffic("fwd_gemm", n, v, h),
@@ -323,23 +320,29 @@ def run_ours(args, world, rank, local):
     out["audit_hbm"] = {str(na): measure_audit(rlk, dev, na, pk["hbm_gbs"])
                         for na in (9_400_614, 1 << 26)}
     if not args.no_cpu_baseline and world == 1:
-        out["cpu_baseline"] = cpu_baseline(w, old.cpu(), g.cpu(), args.cpu_tokens)
+        out["cpu_baseline"] = cpu_baseline(w, noise, adv, args.cpu_tokens)
     return out
 
 
 def measure_audit(rlk, dev, n, hbm_gbs, reps=10):
-    """The audit alone at N tokens: 9 algorithmic bytes per token (new, old, mask).  L2 is
-    flushed (a 256 MB write) before every timed launch pair, outside the events."""
+    """The audit alone at N tokens: 9 algorithmic bytes per token (new, old, mask).  When
+    the inputs fit in L2, L2 is flushed before every timed launch pair (outside the
+    events): a 256 MB write, then a 256 MB read that evicts the dirty lines, so that no
+    write-back lands inside the timed region.  Larger inputs need no flush."""
     new, old, mask = (t.to(dev) for t in wl.audit_inputs(n, 0))
     res = torch.empty(rlk.AUDIT_RESULT_BYTES, dtype=torch.uint8, device=dev)
     ws = torch.empty(rlk.rlk_dlogp_audit_workspace_bytes(n), dtype=torch.uint8, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    fits = n * 9 < 256 << 20
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if fits else None
+    sweep = torch.empty(64 << 20, dtype=torch.float32, device=dev) if fits else None
     stream = torch.cuda.current_stream()
     for _ in range(3):
         rlk.rlk_dlogp_audit(new, old, mask, res, ws)
     ms = []
     for _ in range(reps):
-        flush.zero_()
+        if fits:
+            flush.zero_()
+            sweep.sum()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         rlk.rlk_dlogp_audit(new, old, mask, res, ws)
@@ -349,7 +352,8 @@ def measure_audit(rlk, dev, n, hbm_gbs, reps=10):
     t = float(np.mean(ms))
     gbs = n * 9 / (t * 1e-3) / 1e9
     return {"ms": t, "gbs": gbs, "frac_of_hbm": gbs / hbm_gbs, "bytes": n * 9,
-            "l2": "flushed (256 MB write) before each launch pair"}
+            "l2": ("flushed (256 MB write + 256 MB read) before each launch pair" if fits
+                   else "inputs larger than L2, no flush")}
 
 
 def recorded_traffic(kernel, n, v, h):
@@ -382,8 +386,11 @@ def source_hash(kernel="fwd_gemm"):
 
 # ----------------------------------------------------------------------------- CPU oracle legs
 
-def oracle_step_sample(w, old, g, tokens, threads):
-    """One oracle step (fwd, audit, bwd) over the first `tokens` tokens of the batch."""
+def oracle_step_sample(w, noise, adv, tokens, threads):
+    """One oracle step (fwd, GRPO loss, audit, bwd with all V rows of dW) over the first
+    `tokens` tokens of the batch, timed.  Everything it consumes is the oracle's own: the
+    rollout-side old logp is its forward logp plus the workload's noise, formed before the
+    timed region from an untimed oracle forward."""
     import oracle
     h64 = oracle.bf16_bits_to_f64(w.hidden[:tokens])
     w64 = getattr(w, "_w64", None)
@@ -392,10 +399,16 @@ def oracle_step_sample(w, old, g, tokens, threads):
         w._w64 = w64
     y = w.targets[:tokens].numpy()
     m = w.mask[:tokens].numpy()
-    gg = g[:tokens].double().numpy()
+    old = getattr(w, "_old_sample", None)
+    if old is None or len(old) != tokens:
+        lp0, _ = oracle.linear_logp_fwd_parallel(h64, w64, y, m, w.temperature, threads)
+        old = (lp0 + noise[:tokens]).astype(np.float32).astype(np.float64)
+        w._old_sample = old
+    n_act = max(int(m.sum()), 1)
     t0 = time.perf_counter()
     lp, lse = oracle.linear_logp_fwd_parallel(h64, w64, y, m, w.temperature, threads)
-    oracle.dlogp_audit(lp.astype(np.float32), old[:tokens].numpy(), m)
+    gg, _ = oracle.grpo_clip(lp, old, adv[:tokens], m, GRPO_EPS, GRPO_EPS, 1.0 / n_act)
+    oracle.dlogp_audit(lp.astype(np.float32), old.astype(np.float32), m)
     oracle.linear_logp_bwd_dh_parallel(h64, w64, y, m, gg, lse, w.temperature, threads)
     oracle.linear_logp_bwd_dw_blocks(h64, w64, y, m, gg, lse, w.temperature, 0, w.v,
                                      lambda v0, blk: None, threads=threads)
@@ -406,46 +419,39 @@ def cpu_cores():
     return max(1, len(os.sched_getaffinity(0)))
 
 
-def cpu_baseline(w, old, g, tokens):
+def cpu_baseline(w, noise, adv, tokens):
     cores = cpu_cores()
     tokens = tokens or cores
-    secs = oracle_step_sample(w, old, g, tokens, cores)
+    secs = oracle_step_sample(w, noise, adv, tokens, cores)
     return {"value": tokens / secs, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": "first %d tokens of the batch, one full oracle step (fwd, audit, bwd with "
-                      "all %d dW rows), fp64, %.1f s" % (tokens, w.v, secs)}
+            "sample": "first %d tokens of the batch, one full oracle step (fwd, GRPO loss, "
+                      "audit, bwd with all %d dW rows), fp64, %.1f s" % (tokens, w.v, secs)}
 
 
 def run_reference(args, world, rank):
     if rank != 0:
         return None
     w, noise, adv = make_batch(args.seed, args.tokens)
-    import oracle
     tokens = args.cpu_tokens or cpu_cores()
-    h64 = oracle.bf16_bits_to_f64(w.hidden[:tokens])
-    w._w64 = oracle.bf16_bits_to_f64(w.weight)
-    lp, _ = oracle.linear_logp_fwd_parallel(h64, w._w64, w.targets[:tokens].numpy(),
-                                            w.mask[:tokens].numpy(), w.temperature)
-    old = torch.zeros(w.n, dtype=torch.float32)
-    old[:tokens] = torch.from_numpy(lp + noise[:tokens]).float()
-    _, gg = oracle.grpo_clip_grad(lp, old[:tokens].double().numpy(), adv[:tokens],
-                                  w.mask[:tokens].numpy(), GRPO_EPS)
-    g = torch.zeros(w.n, dtype=torch.float32)
-    g[:tokens] = torch.from_numpy(gg).float()
-    for _ in range(args.warmup):
-        pass                     # the oracle has no warm-up state; W is converted once above
-    times = [oracle_step_sample(w, old, g, tokens, cpu_cores()) for _ in range(args.steps)]
+    oracle_step_sample(w, noise, adv, tokens, cpu_cores())      # warm-up: W conversion, old logp
+    for _ in range(args.warmup - 1):
+        oracle_step_sample(w, noise, adv, tokens, cpu_cores())
+    times = [oracle_step_sample(w, noise, adv, tokens, cpu_cores()) for _ in range(args.steps)]
     secs = float(np.mean(times))
     val = tokens / secs
     return {
         "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded; Qwen3-8B-shaped LM head)", "impl": "reference",
-        "config": {"workload": w.name + " fwd+audit+GRPO bwd", "n_tokens": w.n,
-                   "hidden": w.h, "vocab": w.v, "temperature": w.temperature},
+        "data": "synthetic (seeded; Qwen3-8B-shaped LM head, random-init weights)",
+        "impl": "reference",
+        "config": {"workload": w.name + " fwd+GRPO loss+audit+bwd", "n_tokens": w.n,
+                   "n_active": w.n_active, "hidden": w.h, "vocab": w.v,
+                   "temperature": w.temperature},
         "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cpu_cores(),
                          "kind": "oracle",
-                         "sample": "first %d tokens per step, full oracle step" % tokens},
+                         "sample": "first %d tokens per step, full oracle step (fwd, GRPO loss, "
+                                   "audit, bwd with all %d dW rows)" % (tokens, w.v)},
         "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

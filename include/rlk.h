@@ -61,6 +61,11 @@ typedef enum {
 /* bits of *device_error_word */
 #define RLK_DEVERR_TARGET_RANGE 0x1u   /* an active row's target id is outside [0, V) */
 #define RLK_DEVERR_WAIT_TIMEOUT 0x2u   /* a pipeline wait gave up (the results are invalid) */
+#define RLK_DEVERR_ROW_RANGE 0x4u      /* an entry of a row-index list is outside [0, N) */
+
+/* element type of rlk_logp_from_logits' logits */
+#define RLK_DTYPE_F32 0
+#define RLK_DTYPE_BF16 1
 
 /* Result of rlk_dlogp_audit, written to device memory. */
 typedef struct {
@@ -72,10 +77,20 @@ typedef struct {
     uint32_t error_flags;   /* bit 0: an active d was not finite */
 } rlk_audit_result_t;
 
+/* Result of rlk_grpo_clip_loss, written to device memory. */
+typedef struct {
+    int64_t active_count;   /* number of active tokens */
+    int64_t clipped_count;  /* active tokens where the clipped term is selected (zero gradient) */
+    int64_t outside_count;  /* active tokens with r outside [1 - eps_low, 1 + eps_high] */
+    double loss;            /* -loss_scale * sum_active min(r A, clip(r) A) */
+    double mean_ratio;      /* sum_active r / active_count   (NaN when none is active) */
+} rlk_grpo_result_t;
+
 /* Scratch bytes each entry point needs for these sizes (pure arithmetic, no CUDA call). */
 size_t rlk_linear_logp_fwd_workspace_bytes(int64_t N, int64_t H, int64_t V);
 size_t rlk_linear_logp_bwd_workspace_bytes(int64_t N, int64_t H, int64_t V);
 size_t rlk_dlogp_audit_workspace_bytes(int64_t N);
+size_t rlk_grpo_clip_loss_workspace_bytes(int64_t N);
 
 /*
  * Forward.  "RL-Kernel Roadmap (2026)" P0.2; "RL-Kernel integration roadmap
@@ -124,6 +139,46 @@ rlk_status_t rlk_linear_logp_bwd(const void* hidden, const void* weight,
                                  uint32_t* device_error_word, cudaStream_t stream);
 
 /*
+ * Forward and backward with the softmax entropy as a second output.
+ * "RL-Kernel Roadmap (2026)", backlog: fused entropy / entropy-bonus kernel
+ * (next to the fused linear log-prob); "RL-Kernel integration roadmap for
+ * vime", linear_logp: entropy requests are served explicitly instead of
+ * falling back.  The same tile loop carries one more per-row accumulator,
+ * sum_v 2^((s_v - max) k) s_v, so that for active rows
+ *
+ *   entropy[t] = -sum_v p[t,v] log p[t,v] = lse[t] - E_p[s/T]
+ *
+ * (fp32; 0 on inactive rows).  Arguments otherwise as rlk_linear_logp_fwd; the
+ * workspace query is rlk_linear_logp_fwd_workspace_bytes.  logp and lse equal
+ * rlk_linear_logp_fwd's bit for bit.
+ */
+rlk_status_t rlk_linear_logp_entropy_fwd(const void* hidden, const void* weight,
+                                         const int64_t* targets, const uint8_t* active_mask,
+                                         int64_t N, int64_t H, int64_t V, double temperature,
+                                         float* logp_out, float* lse_out, float* entropy_out,
+                                         void* workspace, size_t workspace_bytes,
+                                         uint32_t* device_error_word, cudaStream_t stream);
+
+/*
+ * Backward of L = sum_t grad_logp[t] logp[t] + sum_t grad_entropy[t] entropy[t],
+ * with dentropy/dz_v = -p_v (z_v - E_p[z]) (z = s/T):
+ *
+ *   dS[t,v] = ( g_t (delta(v,y_t) - p) - gH_t p (z_v - E_p[z]) ) / T
+ *
+ * lse and entropy are the forward's outputs (E_p[z] = lse - entropy).  Same
+ * chunked recompute, workspace, rounding and determinism as
+ * rlk_linear_logp_bwd; grad_entropy = 0 gives rlk_linear_logp_bwd's result.
+ */
+rlk_status_t rlk_linear_logp_entropy_bwd(const void* hidden, const void* weight,
+                                         const int64_t* targets, const uint8_t* active_mask,
+                                         const float* grad_logp, const float* grad_entropy,
+                                         const float* lse, const float* entropy, int64_t N,
+                                         int64_t H, int64_t V, double temperature,
+                                         void* dhidden, void* dweight, void* workspace,
+                                         size_t workspace_bytes, uint32_t* device_error_word,
+                                         cudaStream_t stream);
+
+/*
  * Masked dlogp audit.  "RL-Kernel integration roadmap for vime", Consistency
  * Contract: dlogp = recomputed - old over active tokens only; max_abs_dlogp
  * (the primary metric) with the worst-token index; approx_kl0 =
@@ -138,6 +193,98 @@ rlk_status_t rlk_dlogp_audit(const float* logp_new, const float* logp_old,
                              const uint8_t* active_mask, int64_t N,
                              rlk_audit_result_t* result_dev,
                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Vocab-sharded forward, for tensor-parallel LM heads.  "RL-Kernel
+ * integration roadmap for vime", linear_logp: TP support makes the
+ * vocab-shard merge explicit -- local max, global max, local sum-exp, global
+ * sum-exp, selected target logit, final downcast point; "RL-Kernel Roadmap
+ * (2026)", TP-invariant reductions.
+ *
+ * rlk_linear_logp_fwd_shard scores one contiguous block of vocabulary rows
+ * [vocab_start, vocab_start + V_local) of the LM head:
+ *   weight_shard     [V_local, H] bf16, the block's rows
+ *   partials_out     [rlk_linear_logp_num_partials(V_local)][N] pairs of fp32
+ *                    (max s, sum_v 2^((s_v - max) log2(e)/T)) per 1024-column
+ *                    chunk of the block and row; chunk c of the block is global
+ *                    chunk vocab_start/1024 + c
+ *   target_logit_out [N] fp32: s[t, y_t] for the rows whose target lies in the
+ *                    block; other rows are left untouched
+ * vocab_start must be a multiple of 1024 (RLK_ERR_UNSUPPORTED otherwise).
+ * rlk_linear_logp_merge then reduces the concatenated partials of all blocks
+ * (global chunk order) exactly as rlk_linear_logp_fwd does: when every block
+ * but the last holds a multiple of 1024 rows, logp and lse are bitwise equal to
+ * the unsharded forward, whatever the number of blocks.  Exchanging the
+ * partials between ranks (an all-gather of 8 bytes per row and chunk, plus the
+ * target logit from the rank that owns y_t) is the caller's.
+ */
+int64_t rlk_linear_logp_num_partials(int64_t V_local);
+rlk_status_t rlk_linear_logp_fwd_shard(const void* hidden, const void* weight_shard,
+                                       const int64_t* targets, const uint8_t* active_mask,
+                                       int64_t N, int64_t H, int64_t V_local,
+                                       int64_t vocab_start, double temperature,
+                                       float* partials_out, float* target_logit_out,
+                                       uint32_t* device_error_word, cudaStream_t stream);
+/*   partials      [num_partials][N] pairs from rlk_linear_logp_fwd_shard, in global chunk order
+ *   num_partials  total over all blocks (= rlk_linear_logp_num_partials(V) when unsharded)
+ *   target_logit  [N] fp32, assembled from the owning blocks
+ *   V             global vocabulary size (targets outside [0, V) are flagged)
+ *   logp_out, lse_out as in rlk_linear_logp_fwd */
+rlk_status_t rlk_linear_logp_merge(const float* partials, int64_t num_partials,
+                                   const float* target_logit, const int64_t* targets,
+                                   const uint8_t* active_mask, int64_t N, int64_t V,
+                                   double temperature, float* logp_out, float* lse_out,
+                                   uint32_t* device_error_word, cudaStream_t stream);
+
+/*
+ * Selected-token logp from existing logits.  "RL-Kernel integration roadmap
+ * for vime", logp Reference Scoring: the reference / audit sibling of
+ * linear_logp when logits already exist, with the same mask and temperature
+ * semantics and a deterministic row-local reduction (fixed topology, fixed
+ * launch configuration; dense and indexed rows give identical bits).
+ *
+ *   logits      [N, row_stride] (V <= row_stride used per row), fp32 or bf16
+ *               (dtype = RLK_DTYPE_F32 / RLK_DTYPE_BF16)
+ *   rows        [M] int64 row indices to score, or NULL for all N rows (M = N)
+ *   targets     [N] int64, active_mask [N] uint8 or NULL (indexed by logits row)
+ *   logp_out, lse_out  [M] fp32 (lse_out may be NULL); inactive rows give 0
+ * Same arithmetic contract as the fused path: max over raw logits, fp32
+ * 2^((x - m) log2(e)/T) sums, lse = (m k + log2 sum) ln 2.  An index outside
+ * [0, N) raises RLK_DEVERR_ROW_RANGE and gives NaN for that output.
+ */
+rlk_status_t rlk_logp_from_logits(const void* logits, int32_t dtype, int64_t N, int64_t V,
+                                  int64_t row_stride, const int64_t* rows, int64_t M,
+                                  const int64_t* targets, const uint8_t* active_mask,
+                                  double temperature, float* logp_out, float* lse_out,
+                                  uint32_t* device_error_word, cudaStream_t stream);
+
+/*
+ * Fused GRPO / PPO clipped-ratio loss fragment.  "RL-Kernel integration
+ * roadmap for vime", RL Loss Operators (fused ratio / loss fragments; the
+ * caller owns advantages, clipping range and aggregation); "RL-Kernel Roadmap
+ * (2026)", backlog (fused PPO clip loss, ratio-clip-aggregate primitive).
+ * For active t, r_t = exp(logp_new[t] - logp_old[t]):
+ *
+ *   term_t  = min(r_t A_t, clip(r_t, 1 - eps_low, 1 + eps_high) A_t)
+ *   loss    = -loss_scale * sum_active term_t
+ *   grad[t] = dloss/dlogp_new[t] = -loss_scale A_t r_t where the unclipped
+ *             product is the one selected, else 0; 0 on inactive tokens
+ *
+ *   logp_new, logp_old, advantages [N] fp32; active_mask [N] uint8 or NULL
+ *   eps_low, eps_high  >= 0 and finite (eps_low < 1)
+ *   loss_scale  > 0 and finite: the aggregation weight, e.g. 1 / (number of
+ *               active tokens) for a token mean.  It is the caller's, so each
+ *               grad[t] depends on token t alone (batch invariant).
+ *   grad_out    [N] fp32, the upstream gradient for rlk_linear_logp_bwd
+ *   result_dev  one rlk_grpo_result_t in device memory
+ * r and grad are fp32; the sums are fp32 per thread and fp64 across threads
+ * in fixed trees (bitwise reproducible for a given N).
+ */
+rlk_status_t rlk_grpo_clip_loss(const float* logp_new, const float* logp_old,
+                                const float* advantages, const uint8_t* active_mask, int64_t N,
+                                double eps_low, double eps_high, double loss_scale,
+                                float* grad_out, rlk_grpo_result_t* result_dev,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * Masked dlogp audit that allocates nothing.  The source pages have no

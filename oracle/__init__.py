@@ -37,6 +37,16 @@ _i64p = ctypes.POINTER(ctypes.c_int64)
 _u8p = ctypes.POINTER(ctypes.c_uint8)
 
 
+class GrpoResult(ctypes.Structure):
+    _fields_ = [
+        ("active_count", ctypes.c_int64),
+        ("clipped_count", ctypes.c_int64),
+        ("outside_count", ctypes.c_int64),
+        ("loss", ctypes.c_double),
+        ("mean_ratio", ctypes.c_double),
+    ]
+
+
 class AuditResult(ctypes.Structure):
     _fields_ = [
         ("active_count", ctypes.c_int64),
@@ -75,6 +85,25 @@ def _load():
             lib.rlk_oracle_dlogp_audit.restype = None
             lib.rlk_oracle_dlogp_audit.argtypes = [_fp, _fp, _u8p, ctypes.c_int64,
                                                    ctypes.POINTER(AuditResult)]
+            lib.rlk_oracle_grpo_clip.restype = None
+            lib.rlk_oracle_grpo_clip.argtypes = [_dp, _dp, _dp, _u8p, ctypes.c_int64,
+                                                 ctypes.c_double, ctypes.c_double,
+                                                 ctypes.c_double, _dp, ctypes.POINTER(GrpoResult)]
+            lib.rlk_oracle_logp_from_logits.restype = ctypes.c_int64
+            lib.rlk_oracle_logp_from_logits.argtypes = [_dp, ctypes.c_int64, ctypes.c_int64,
+                                                        _i64p, ctypes.c_int64, _i64p, _u8p,
+                                                        ctypes.c_double, _dp, _dp]
+            lib.rlk_oracle_linear_logp_entropy_fwd.restype = ctypes.c_int64
+            lib.rlk_oracle_linear_logp_entropy_fwd.argtypes = [
+                _dp, _dp, _i64p, _u8p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                ctypes.c_double, _dp, _dp, _dp]
+            for name in ("rlk_oracle_linear_logp_entropy_bwd_dh",
+                         "rlk_oracle_linear_logp_entropy_bwd_dw"):
+                f = getattr(lib, name)
+                f.restype = None
+                f.argtypes = [_dp, _dp, _i64p, _u8p, _dp, _dp, _dp, _dp, ctypes.c_int64,
+                              ctypes.c_int64, ctypes.c_int64, ctypes.c_double, ctypes.c_int64,
+                              ctypes.c_int64, _dp]
             lib.rlk_oracle_grpo_clip_grad.restype = ctypes.c_double
             lib.rlk_oracle_grpo_clip_grad.argtypes = [_dp, _dp, _dp, _u8p, ctypes.c_int64,
                                                       ctypes.c_double, _dp]
@@ -284,3 +313,129 @@ def grpo_clip_grad(logp, old, adv, mask, eps):
     loss = lib.rlk_oracle_grpo_clip_grad(_ptr(lp, _dp), _ptr(od, _dp), _ptr(ad, _dp),
                                          _ptr(m, _u8p), n, float(eps), _ptr(g, _dp))
     return loss, g
+
+
+def grpo_clip(logp, old, adv, mask, eps_low, eps_high, scale):
+    """(g[N], result dict) of the clipped-ratio fragment with explicit range and scale."""
+    lib = _load()
+    lp = _c(logp, np.float64)
+    od = _c(old, np.float64)
+    ad = _c(adv, np.float64)
+    n = lp.shape[0]
+    m = _mask_arg(mask, n)
+    g = np.empty(n, np.float64)
+    res = GrpoResult()
+    lib.rlk_oracle_grpo_clip(_ptr(lp, _dp), _ptr(od, _dp), _ptr(ad, _dp), _ptr(m, _u8p), n,
+                             float(eps_low), float(eps_high), float(scale), _ptr(g, _dp),
+                             ctypes.byref(res))
+    return g, {f: getattr(res, f) for f, _ in GrpoResult._fields_}
+
+
+def logp_from_logits(logits, y, mask, temperature, rows=None):
+    """logp, lse (float64) of the selected rows of logits[N, V] (exact float64 values)."""
+    lib = _load()
+    z = _c(logits, np.float64)
+    n, vocab = z.shape
+    y = _c(y, np.int64)
+    m = _mask_arg(mask, n)
+    r = None if rows is None else _c(rows, np.int64)
+    cnt = n if r is None else r.shape[0]
+    logp = np.empty(cnt, np.float64)
+    lse = np.empty(cnt, np.float64)
+    lib.rlk_oracle_logp_from_logits(_ptr(z, _dp), vocab, vocab, _ptr(r, _i64p), cnt,
+                                    _ptr(y, _i64p), _ptr(m, _u8p), float(temperature),
+                                    _ptr(logp, _dp), _ptr(lse, _dp))
+    return logp, lse
+
+
+def linear_logp_entropy_fwd(h, w, y, mask, temperature):
+    """logp[N], lse[N], entropy[N] (float64)."""
+    lib = _load()
+    h = _c(h, np.float64)
+    w = _c(w, np.float64)
+    n, hdim = h.shape
+    y = _c(y, np.int64)
+    m = _mask_arg(mask, n)
+    logp, lse, ent = (np.empty(n, np.float64) for _ in range(3))
+    if lib.rlk_oracle_linear_logp_entropy_fwd(_ptr(h, _dp), _ptr(w, _dp), _ptr(y, _i64p),
+                                              _ptr(m, _u8p), n, hdim, w.shape[0],
+                                              float(temperature), _ptr(logp, _dp),
+                                              _ptr(lse, _dp), _ptr(ent, _dp)) < 0:
+        raise MemoryError("oracle forward: scratch allocation failed")
+    return logp, lse, ent
+
+
+def linear_logp_entropy_fwd_parallel(h, w, y, mask, temperature, threads=None):
+    h = _c(h, np.float64)
+    w = _c(w, np.float64)
+    n = h.shape[0]
+    y = _c(y, np.int64)
+    m = _mask_arg(mask, n)
+    out = [np.empty(n, np.float64) for _ in range(3)]
+
+    def fn(a, b):
+        if a < b:
+            r = linear_logp_entropy_fwd(h[a:b], w, y[a:b], None if m is None else m[a:b],
+                                        temperature)
+            for o, x in zip(out, r):
+                o[a:b] = x
+
+    _split_parallel(n, fn, threads)
+    return tuple(out)
+
+
+def _entropy_bwd(name, h, w, y, mask, g, gh, lse, ent, temperature, begin, end, rows):
+    lib = _load()
+    h = _c(h, np.float64)
+    w = _c(w, np.float64)
+    n, hdim = h.shape
+    y = _c(y, np.int64)
+    m = _mask_arg(mask, n)
+    g, gh, lse, ent = (_c(x, np.float64) for x in (g, gh, lse, ent))
+    out = np.empty((end - begin, hdim), np.float64)
+    getattr(lib, name)(_ptr(h, _dp), _ptr(w, _dp), _ptr(y, _i64p), _ptr(m, _u8p), _ptr(g, _dp),
+                       _ptr(gh, _dp), _ptr(lse, _dp), _ptr(ent, _dp), n, hdim, w.shape[0],
+                       float(temperature), begin, end, _ptr(out, _dp))
+    return out
+
+
+def linear_logp_entropy_bwd_dh(h, w, y, mask, g, gh, lse, ent, temperature, row_begin=0,
+                               row_end=None):
+    row_end = np.asarray(h).shape[0] if row_end is None else row_end
+    return _entropy_bwd("rlk_oracle_linear_logp_entropy_bwd_dh", h, w, y, mask, g, gh, lse, ent,
+                        temperature, row_begin, row_end, True)
+
+
+def linear_logp_entropy_bwd_dw(h, w, y, mask, g, gh, lse, ent, temperature, v_begin=0,
+                               v_end=None):
+    v_end = np.asarray(w).shape[0] if v_end is None else v_end
+    return _entropy_bwd("rlk_oracle_linear_logp_entropy_bwd_dw", h, w, y, mask, g, gh, lse, ent,
+                        temperature, v_begin, v_end, False)
+
+
+def linear_logp_entropy_bwd_dh_parallel(h, w, y, mask, g, gh, lse, ent, temperature,
+                                        threads=None):
+    h = _c(h, np.float64)
+    out = np.empty(h.shape, np.float64)
+
+    def fn(a, b):
+        if a < b:
+            out[a:b] = linear_logp_entropy_bwd_dh(h, w, y, mask, g, gh, lse, ent, temperature,
+                                                  a, b)
+
+    _split_parallel(h.shape[0], fn, threads)
+    return out
+
+
+def linear_logp_entropy_bwd_dw_parallel(h, w, y, mask, g, gh, lse, ent, temperature,
+                                        threads=None):
+    w = _c(w, np.float64)
+    out = np.empty(w.shape, np.float64)
+
+    def fn(a, b):
+        if a < b:
+            out[a:b] = linear_logp_entropy_bwd_dw(h, w, y, mask, g, gh, lse, ent, temperature,
+                                                  a, b)
+
+    _split_parallel(w.shape[0], fn, threads)
+    return out

@@ -232,3 +232,203 @@ double rlk_oracle_grpo_clip_grad(const double* logp, const double* old,
     }
     return -total / (double)na;
 }
+
+typedef struct {
+    int64_t active_count;
+    int64_t clipped_count;
+    int64_t outside_count;
+    double loss;
+    double mean_ratio;
+} rlk_oracle_grpo_t;
+
+/*
+ * Clipped-ratio policy-gradient fragment with explicit clip range and
+ * aggregation scale ("RL-Kernel integration roadmap for vime", RL Loss
+ * Operators: the caller owns aggregation and clipping range; "RL-Kernel
+ * Roadmap (2026)", backlog: fused PPO clip loss, ratio-clip-aggregate
+ * primitive).  For active t, with r_t = exp(logp_t - old_t):
+ *   term_t  = min(r_t A_t, clip(r_t, 1 - eps_low, 1 + eps_high) A_t)
+ *   L       = -scale * sum_active term_t
+ *   g_t     = -scale * A_t * r_t   where the unclipped product is the one the
+ *             min selects (always inside the clip range), else 0; 0 inactive
+ *   clipped = #active with the clipped constant selected and r_t outside the
+ *             range (zero gradient); outside = #active with r_t outside the range
+ *   mean_ratio = sum_active r_t / #active
+ * With eps_low = eps_high = eps and scale = 1/#active this is
+ * rlk_oracle_grpo_clip_grad.
+ */
+void rlk_oracle_grpo_clip(const double* logp, const double* old, const double* adv,
+                          const uint8_t* mask, int64_t n, double eps_low, double eps_high,
+                          double scale, double* g, rlk_oracle_grpo_t* out) {
+    int64_t na = 0, clipped = 0, outside = 0;
+    double total = 0.0, rsum = 0.0;
+    const double lo = 1.0 - eps_low, hi = 1.0 + eps_high;
+    for (int64_t t = 0; t < n; ++t) {
+        g[t] = 0.0;
+        if (!row_active(mask, t)) continue;
+        double r = exp(logp[t] - old[t]);
+        double rc = r < lo ? lo : (r > hi ? hi : r);
+        double unclipped = r * adv[t];
+        double clippedv = rc * adv[t];
+        int take_unclipped = (unclipped <= clippedv);
+        int out_of_range = (r < lo || r > hi);
+        ++na;
+        rsum += r;
+        total += take_unclipped ? unclipped : clippedv;
+        if (take_unclipped) g[t] = -scale * adv[t] * r;
+        if (out_of_range) ++outside;
+        if (!take_unclipped && out_of_range) ++clipped;
+    }
+    out->active_count = na;
+    out->clipped_count = clipped;
+    out->outside_count = outside;
+    out->loss = -scale * total;
+    out->mean_ratio = rsum / (double)na;
+}
+
+/*
+ * Selected-token logp from given logits ("RL-Kernel integration roadmap for
+ * vime", logp Reference Scoring: log-softmax over existing logits, the same
+ * active mask and temperature as linear_logp, dense or indexed rows).
+ * Output row i scores logits row r_i = rows[i] (or i when rows is NULL):
+ *   z[v]   = logits[r_i][v] / T
+ *   lse_i  = M + log( sum_v exp(z[v] - M) ),  M = max_v z[v]
+ *   logp_i = z[y[r_i]] - lse_i   when row r_i is active, else logp_i = lse_i = 0
+ * logits is [N][stride] (row stride in elements); targets and mask are indexed
+ * by logits row.  Returns the number of active rows with a target outside
+ * [0, V) (their logp is NaN).
+ */
+int64_t rlk_oracle_logp_from_logits(const double* logits, int64_t stride, int64_t vocab,
+                                    const int64_t* rows, int64_t m, const int64_t* y,
+                                    const uint8_t* mask, double temperature,
+                                    double* logp, double* lse) {
+    int64_t bad = 0;
+    for (int64_t i = 0; i < m; ++i) {
+        const int64_t r = rows ? rows[i] : i;
+        if (!row_active(mask, r)) {
+            logp[i] = 0.0;
+            if (lse) lse[i] = 0.0;
+            continue;
+        }
+        const double* z = logits + r * stride;
+        double mx = -INFINITY;
+        for (int64_t v = 0; v < vocab; ++v) if (z[v] / temperature > mx) mx = z[v] / temperature;
+        double sum = 0.0;
+        for (int64_t v = 0; v < vocab; ++v) sum += exp(z[v] / temperature - mx);
+        const double l = mx + log(sum);
+        if (lse) lse[i] = l;
+        if (y[r] < 0 || y[r] >= vocab) {
+            logp[i] = NAN;
+            ++bad;
+        } else {
+            logp[i] = z[y[r]] / temperature - l;
+        }
+    }
+    return bad;
+}
+
+/*
+ * Entropy of the temperature-scaled softmax, next to logp ("RL-Kernel
+ * Roadmap (2026)", backlog: fused entropy / entropy-bonus kernel; "RL-Kernel
+ * integration roadmap for vime", linear_logp: entropy requests).  For every
+ * active row, with z[v] = (h_t . W_v) / T and log p[v] = z[v] - LSE_t:
+ *   entropy_t = - sum_v p[v] * log p[v]
+ * logp and lse as in rlk_oracle_linear_logp_fwd; inactive rows give 0.
+ */
+int64_t rlk_oracle_linear_logp_entropy_fwd(const double* h, const double* w,
+                                           const int64_t* y, const uint8_t* mask,
+                                           int64_t n, int64_t hdim, int64_t vocab,
+                                           double temperature, double* logp, double* lse,
+                                           double* entropy) {
+    double* z = (double*)malloc((size_t)(vocab > 0 ? vocab : 1) * sizeof(double));
+    if (z == NULL) return -1;
+    int64_t bad = 0;
+    for (int64_t t = 0; t < n; ++t) {
+        if (!row_active(mask, t)) {
+            logp[t] = 0.0;
+            lse[t] = 0.0;
+            entropy[t] = 0.0;
+            continue;
+        }
+        const double* ht = h + t * hdim;
+        for (int64_t v = 0; v < vocab; ++v) z[v] = dot(ht, w + v * hdim, hdim) / temperature;
+        double m = -INFINITY;
+        for (int64_t v = 0; v < vocab; ++v) if (z[v] > m) m = z[v];
+        double sum = 0.0;
+        for (int64_t v = 0; v < vocab; ++v) sum += exp(z[v] - m);
+        double l = m + log(sum);
+        lse[t] = l;
+        double ent = 0.0;
+        for (int64_t v = 0; v < vocab; ++v) {
+            double lp = z[v] - l;
+            ent -= exp(lp) * lp;
+        }
+        entropy[t] = ent;
+        if (y[t] < 0 || y[t] >= vocab) {
+            logp[t] = NAN;
+            ++bad;
+        } else {
+            logp[t] = z[y[t]] - l;
+        }
+    }
+    free(z);
+    return bad;
+}
+
+/*
+ * Backward of L = sum_t g_t logp_t + sum_t gH_t entropy_t.  With
+ * log p[v] = z[v] - LSE_t and the forward's entropy_t:
+ *   dlogp_t/dz_v    = delta(v, y_t) - p[v]
+ *   dentropy_t/dz_v = -p[v] * (log p[v] + entropy_t)
+ *   G[t][v] = ( g_t (delta - p[v]) - gH_t p[v] (log p[v] + entropy_t) ) / T
+ * dh rows [row_begin, row_end) and dW rows [v_begin, v_end) as in the logp-only
+ * backward (ascending v for dh, ascending t for dW).
+ */
+static double entropy_coef(double g, double gh, double delta, double lp, double ent,
+                           double temperature) {
+    double p = exp(lp);
+    return (g * (delta - p) - gh * p * (lp + ent)) / temperature;
+}
+
+void rlk_oracle_linear_logp_entropy_bwd_dh(const double* h, const double* w,
+                                           const int64_t* y, const uint8_t* mask,
+                                           const double* g, const double* gh,
+                                           const double* lse, const double* ent,
+                                           int64_t n, int64_t hdim, int64_t vocab,
+                                           double temperature, int64_t row_begin,
+                                           int64_t row_end, double* dh) {
+    (void)n;
+    for (int64_t t = row_begin; t < row_end; ++t) {
+        double* out = dh + (t - row_begin) * hdim;
+        for (int64_t k = 0; k < hdim; ++k) out[k] = 0.0;
+        if (!row_active(mask, t) || y[t] < 0 || y[t] >= vocab) continue;
+        const double* ht = h + t * hdim;
+        for (int64_t v = 0; v < vocab; ++v) {
+            double lp = dot(ht, w + v * hdim, hdim) / temperature - lse[t];
+            double G = entropy_coef(g[t], gh[t], v == y[t] ? 1.0 : 0.0, lp, ent[t], temperature);
+            const double* wv = w + v * hdim;
+            for (int64_t k = 0; k < hdim; ++k) out[k] += G * wv[k];
+        }
+    }
+}
+
+void rlk_oracle_linear_logp_entropy_bwd_dw(const double* h, const double* w,
+                                           const int64_t* y, const uint8_t* mask,
+                                           const double* g, const double* gh,
+                                           const double* lse, const double* ent,
+                                           int64_t n, int64_t hdim, int64_t vocab,
+                                           double temperature, int64_t v_begin,
+                                           int64_t v_end, double* dw) {
+    for (int64_t v = v_begin; v < v_end; ++v) {
+        double* out = dw + (v - v_begin) * hdim;
+        for (int64_t k = 0; k < hdim; ++k) out[k] = 0.0;
+        const double* wv = w + v * hdim;
+        for (int64_t t = 0; t < n; ++t) {
+            if (!row_active(mask, t) || y[t] < 0 || y[t] >= vocab) continue;
+            const double* ht = h + t * hdim;
+            double lp = dot(ht, wv, hdim) / temperature - lse[t];
+            double G = entropy_coef(g[t], gh[t], v == y[t] ? 1.0 : 0.0, lp, ent[t], temperature);
+            for (int64_t k = 0; k < hdim; ++k) out[k] += G * ht[k];
+        }
+    }
+}

@@ -27,6 +27,8 @@ HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "rlk.h")
 RLK_OK, RLK_ERR_INVALID_VALUE, RLK_ERR_UNSUPPORTED, RLK_ERR_WORKSPACE, RLK_ERR_LAUNCH = range(5)
 RLK_DEVERR_TARGET_RANGE = 0x1
 RLK_DEVERR_WAIT_TIMEOUT = 0x2
+RLK_DEVERR_ROW_RANGE = 0x4
+RLK_DTYPE_F32, RLK_DTYPE_BF16 = 0, 1
 RLK_AUDIT_NOALLOC_MAX_N = 1 << 27
 
 _vp = ctypes.c_void_p
@@ -56,6 +58,20 @@ class AuditResult(ctypes.Structure):
 AUDIT_RESULT_BYTES = ctypes.sizeof(AuditResult)
 
 
+class GrpoResult(ctypes.Structure):
+    """Mirror of rlk_grpo_result_t."""
+    _fields_ = [
+        ("active_count", ctypes.c_int64),
+        ("clipped_count", ctypes.c_int64),
+        ("outside_count", ctypes.c_int64),
+        ("loss", ctypes.c_double),
+        ("mean_ratio", ctypes.c_double),
+    ]
+
+
+GRPO_RESULT_BYTES = ctypes.sizeof(GrpoResult)
+
+
 def load(path: str = LIB_PATH) -> ctypes.CDLL:
     """Load librlk.so (built by ``rl_post_linear_gb300.build``); raise if it is missing."""
     global _lib
@@ -77,8 +93,32 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.rlk_linear_logp_bwd.restype = ctypes.c_int
     lib.rlk_linear_logp_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
                                         ctypes.c_double, _vp, _vp, _vp, _sz, _vp, _vp]
+    lib.rlk_linear_logp_entropy_fwd.restype = ctypes.c_int
+    lib.rlk_linear_logp_entropy_fwd.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64,
+                                                ctypes.c_double, _vp, _vp, _vp, _vp, _sz, _vp,
+                                                _vp]
+    lib.rlk_linear_logp_entropy_bwd.restype = ctypes.c_int
+    lib.rlk_linear_logp_entropy_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64,
+                                                _i64, _i64, ctypes.c_double, _vp, _vp, _vp, _sz,
+                                                _vp, _vp]
     lib.rlk_dlogp_audit.restype = ctypes.c_int
     lib.rlk_dlogp_audit.argtypes = [_vp, _vp, _vp, _i64, _vp, _vp, _sz, _vp]
+    lib.rlk_linear_logp_num_partials.restype = _i64
+    lib.rlk_linear_logp_num_partials.argtypes = [_i64]
+    lib.rlk_linear_logp_fwd_shard.restype = ctypes.c_int
+    lib.rlk_linear_logp_fwd_shard.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
+                                              ctypes.c_double, _vp, _vp, _vp, _vp]
+    lib.rlk_linear_logp_merge.restype = ctypes.c_int
+    lib.rlk_linear_logp_merge.argtypes = [_vp, _i64, _vp, _vp, _vp, _i64, _i64, ctypes.c_double,
+                                          _vp, _vp, _vp, _vp]
+    lib.rlk_logp_from_logits.restype = ctypes.c_int
+    lib.rlk_logp_from_logits.argtypes = [_vp, ctypes.c_int32, _i64, _i64, _i64, _vp, _i64, _vp,
+                                         _vp, ctypes.c_double, _vp, _vp, _vp, _vp]
+    lib.rlk_grpo_clip_loss_workspace_bytes.restype = _sz
+    lib.rlk_grpo_clip_loss_workspace_bytes.argtypes = [_i64]
+    lib.rlk_grpo_clip_loss.restype = ctypes.c_int
+    lib.rlk_grpo_clip_loss.argtypes = [_vp, _vp, _vp, _vp, _i64, ctypes.c_double, ctypes.c_double,
+                                       ctypes.c_double, _vp, _vp, _vp, _sz, _vp]
     lib.rlk_dlogp_audit_noalloc.restype = ctypes.c_int
     lib.rlk_dlogp_audit_noalloc.argtypes = [_vp, _vp, _vp, _i64, _vp, _vp]
     lib.rlk_contract_string.restype = ctypes.c_char_p
@@ -114,6 +154,14 @@ def rlk_linear_logp_bwd_workspace_bytes(N: int, H: int, V: int) -> int:
 
 def rlk_dlogp_audit_workspace_bytes(N: int) -> int:
     return int(load().rlk_dlogp_audit_workspace_bytes(N))
+
+
+def rlk_linear_logp_num_partials(V_local: int) -> int:
+    return int(load().rlk_linear_logp_num_partials(V_local))
+
+
+def rlk_grpo_clip_loss_workspace_bytes(N: int) -> int:
+    return int(load().rlk_grpo_clip_loss_workspace_bytes(N))
 
 
 # ----------------------------------------------------------------------------- marshalling
@@ -189,6 +237,56 @@ def rlk_linear_logp_bwd(hidden, weight, targets, active_mask, grad_logp, lse, te
     _check("rlk_linear_logp_bwd", st)
 
 
+def rlk_linear_logp_entropy_fwd(hidden, weight, targets, active_mask, temperature, logp_out,
+                                lse_out, entropy_out, workspace, device_error_word=None,
+                                stream=None):
+    """Forward with the softmax entropy as a second output; see include/rlk.h."""
+    n, h = hidden.shape
+    v = weight.shape[0]
+    _need(hidden, torch.bfloat16, "hidden")
+    _need(weight, torch.bfloat16, "weight", (v, h))
+    _need(targets, torch.int64, "targets", (n,))
+    if active_mask is not None:
+        _need(active_mask, torch.uint8, "active_mask", (n,))
+    for t, name in ((logp_out, "logp_out"), (entropy_out, "entropy_out")):
+        _need(t, torch.float32, name, (n,))
+    if lse_out is not None:
+        _need(lse_out, torch.float32, "lse_out", (n,))
+    _need(workspace, torch.uint8, "workspace")
+    st = load().rlk_linear_logp_entropy_fwd(_ptr(hidden), _ptr(weight), _ptr(targets),
+                                            _ptr(active_mask), n, h, v, float(temperature),
+                                            _ptr(logp_out), _ptr(lse_out), _ptr(entropy_out),
+                                            _ptr(workspace), workspace.numel(),
+                                            _ptr(device_error_word), _stream(stream))
+    _check("rlk_linear_logp_entropy_fwd", st)
+
+
+def rlk_linear_logp_entropy_bwd(hidden, weight, targets, active_mask, grad_logp, grad_entropy,
+                                lse, entropy, temperature, dhidden, dweight, workspace,
+                                device_error_word=None, stream=None):
+    """Backward of sum g logp + sum gH entropy; see include/rlk.h."""
+    n, h = hidden.shape
+    v = weight.shape[0]
+    _need(hidden, torch.bfloat16, "hidden")
+    _need(weight, torch.bfloat16, "weight", (v, h))
+    _need(targets, torch.int64, "targets", (n,))
+    if active_mask is not None:
+        _need(active_mask, torch.uint8, "active_mask", (n,))
+    for t, name in ((grad_logp, "grad_logp"), (grad_entropy, "grad_entropy"), (lse, "lse"),
+                    (entropy, "entropy")):
+        _need(t, torch.float32, name, (n,))
+    _need(dhidden, torch.bfloat16, "dhidden", (n, h))
+    _need(dweight, torch.bfloat16, "dweight", (v, h))
+    _need(workspace, torch.uint8, "workspace")
+    st = load().rlk_linear_logp_entropy_bwd(_ptr(hidden), _ptr(weight), _ptr(targets),
+                                            _ptr(active_mask), _ptr(grad_logp),
+                                            _ptr(grad_entropy), _ptr(lse), _ptr(entropy), n, h,
+                                            v, float(temperature), _ptr(dhidden), _ptr(dweight),
+                                            _ptr(workspace), workspace.numel(),
+                                            _ptr(device_error_word), _stream(stream))
+    _check("rlk_linear_logp_entropy_bwd", st)
+
+
 def rlk_dlogp_audit(logp_new, logp_old, active_mask, result, workspace, stream=None):
     """Enqueue the audit; ``result`` is a uint8 CUDA tensor of AUDIT_RESULT_BYTES bytes."""
     n = logp_new.shape[0]
@@ -218,6 +316,96 @@ def rlk_dlogp_audit_noalloc(logp_new, logp_old, active_mask, result, stream=None
     st = load().rlk_dlogp_audit_noalloc(_ptr(logp_new), _ptr(logp_old), _ptr(active_mask), n,
                                         _ptr(result), _stream(stream))
     _check("rlk_dlogp_audit_noalloc", st)
+
+
+def rlk_linear_logp_fwd_shard(hidden, weight_shard, targets, active_mask, vocab_start,
+                              temperature, partials_out, target_logit_out,
+                              device_error_word=None, stream=None):
+    """Partials of one vocab block; see include/rlk.h.  partials_out: float32
+    [num_partials(V_local), N, 2] (or any contiguous view of it)."""
+    n, h = hidden.shape
+    v_local = weight_shard.shape[0]
+    _need(hidden, torch.bfloat16, "hidden")
+    _need(weight_shard, torch.bfloat16, "weight_shard", (v_local, h))
+    _need(targets, torch.int64, "targets", (n,))
+    if active_mask is not None:
+        _need(active_mask, torch.uint8, "active_mask", (n,))
+    _need(partials_out, torch.float32, "partials_out")
+    if partials_out.numel() < rlk_linear_logp_num_partials(v_local) * n * 2:
+        raise ValueError("partials_out is too small")
+    _need(target_logit_out, torch.float32, "target_logit_out", (n,))
+    st = load().rlk_linear_logp_fwd_shard(_ptr(hidden), _ptr(weight_shard), _ptr(targets),
+                                          _ptr(active_mask), n, h, v_local, int(vocab_start),
+                                          float(temperature), _ptr(partials_out),
+                                          _ptr(target_logit_out), _ptr(device_error_word),
+                                          _stream(stream))
+    _check("rlk_linear_logp_fwd_shard", st)
+
+
+def rlk_linear_logp_merge(partials, num_partials, target_logit, targets, active_mask, vocab_size,
+                          temperature, logp_out, lse_out, device_error_word=None, stream=None):
+    """Fixed-order merge of block partials (global chunk order); see include/rlk.h."""
+    n = targets.shape[0]
+    _need(partials, torch.float32, "partials")
+    if partials.numel() < num_partials * n * 2:
+        raise ValueError("partials is too small")
+    _need(target_logit, torch.float32, "target_logit", (n,))
+    _need(targets, torch.int64, "targets", (n,))
+    if active_mask is not None:
+        _need(active_mask, torch.uint8, "active_mask", (n,))
+    _need(logp_out, torch.float32, "logp_out", (n,))
+    if lse_out is not None:
+        _need(lse_out, torch.float32, "lse_out", (n,))
+    st = load().rlk_linear_logp_merge(_ptr(partials), int(num_partials), _ptr(target_logit),
+                                      _ptr(targets), _ptr(active_mask), n, int(vocab_size),
+                                      float(temperature), _ptr(logp_out), _ptr(lse_out),
+                                      _ptr(device_error_word), _stream(stream))
+    _check("rlk_linear_logp_merge", st)
+
+
+def rlk_logp_from_logits(logits, rows, targets, active_mask, temperature, logp_out, lse_out,
+                         device_error_word=None, stream=None):
+    """Score rows of existing logits [N, V] (fp32 or bf16, rows contiguous, any row stride);
+    rows = None scores all N rows.  See include/rlk.h."""
+    if logits.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("logits must be float32 or bfloat16")
+    if not logits.is_cuda or logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be a 2-D CUDA tensor with contiguous rows")
+    n, v = logits.shape
+    _need(targets, torch.int64, "targets", (n,))
+    if active_mask is not None:
+        _need(active_mask, torch.uint8, "active_mask", (n,))
+    m = n if rows is None else rows.shape[0]
+    if rows is not None:
+        _need(rows, torch.int64, "rows", (m,))
+    _need(logp_out, torch.float32, "logp_out", (m,))
+    if lse_out is not None:
+        _need(lse_out, torch.float32, "lse_out", (m,))
+    dt = RLK_DTYPE_F32 if logits.dtype == torch.float32 else RLK_DTYPE_BF16
+    st = load().rlk_logp_from_logits(_ptr(logits), dt, n, v, logits.stride(0), _ptr(rows), m,
+                                     _ptr(targets), _ptr(active_mask), float(temperature),
+                                     _ptr(logp_out), _ptr(lse_out), _ptr(device_error_word),
+                                     _stream(stream))
+    _check("rlk_logp_from_logits", st)
+
+
+def rlk_grpo_clip_loss(logp_new, logp_old, advantages, active_mask, eps_low, eps_high,
+                       loss_scale, grad_out, result, workspace, stream=None):
+    """Enqueue the clipped-ratio loss fragment; see include/rlk.h."""
+    n = logp_new.shape[0]
+    _need(logp_new, torch.float32, "logp_new", (n,))
+    _need(logp_old, torch.float32, "logp_old", (n,))
+    _need(advantages, torch.float32, "advantages", (n,))
+    if active_mask is not None:
+        _need(active_mask, torch.uint8, "active_mask", (n,))
+    _need(grad_out, torch.float32, "grad_out", (n,))
+    _need(result, torch.uint8, "result", (GRPO_RESULT_BYTES,))
+    _need(workspace, torch.uint8, "workspace")
+    st = load().rlk_grpo_clip_loss(_ptr(logp_new), _ptr(logp_old), _ptr(advantages),
+                                   _ptr(active_mask), n, float(eps_low), float(eps_high),
+                                   float(loss_scale), _ptr(grad_out), _ptr(result),
+                                   _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("rlk_grpo_clip_loss", st)
 
 
 # ----------------------------------------------------------------------------- conveniences
@@ -252,6 +440,31 @@ def linear_logp_bwd(hidden, weight, targets, active_mask, grad_logp, lse, temper
     return dh, dw
 
 
+def linear_logp_entropy_fwd(hidden, weight, targets, active_mask=None, temperature=1.0,
+                            error_word=None):
+    """(logp[N], lse[N], entropy[N]) fp32."""
+    n, h = hidden.shape
+    v = weight.shape[0]
+    logp, lse, ent = (torch.empty(n, dtype=torch.float32, device=hidden.device) for _ in range(3))
+    ws = _workspace(rlk_linear_logp_fwd_workspace_bytes(n, h, v), hidden.device)
+    rlk_linear_logp_entropy_fwd(hidden, weight, targets, active_mask, temperature, logp, lse, ent,
+                                ws, error_word)
+    return logp, lse, ent
+
+
+def linear_logp_entropy_bwd(hidden, weight, targets, active_mask, grad_logp, grad_entropy, lse,
+                            entropy, temperature=1.0, error_word=None):
+    """(dhidden[N,H], dweight[V,H]) bf16."""
+    n, h = hidden.shape
+    v = weight.shape[0]
+    dh = torch.empty_like(hidden)
+    dw = torch.empty_like(weight)
+    ws = _workspace(rlk_linear_logp_bwd_workspace_bytes(n, h, v), hidden.device)
+    rlk_linear_logp_entropy_bwd(hidden, weight, targets, active_mask, grad_logp, grad_entropy,
+                                lse, entropy, temperature, dh, dw, ws, error_word)
+    return dh, dw
+
+
 def audit_result_to_dict(raw: torch.Tensor) -> dict:
     r = AuditResult.from_buffer_copy(bytes(raw.cpu().numpy().tobytes()))
     return {f: getattr(r, f) for f, _ in AuditResult._fields_}
@@ -264,6 +477,28 @@ def dlogp_audit(logp_new, logp_old, active_mask=None):
     ws = _workspace(rlk_dlogp_audit_workspace_bytes(n), logp_new.device)
     rlk_dlogp_audit(logp_new, logp_old, active_mask, res, ws)
     return audit_result_to_dict(res)
+
+
+def grpo_clip_loss(logp_new, logp_old, advantages, active_mask, eps_low, eps_high, loss_scale):
+    """(grad[N] fp32, result dict); synchronises to read the result back."""
+    n = logp_new.shape[0]
+    grad = torch.empty(n, dtype=torch.float32, device=logp_new.device)
+    res = torch.empty(GRPO_RESULT_BYTES, dtype=torch.uint8, device=logp_new.device)
+    ws = _workspace(rlk_grpo_clip_loss_workspace_bytes(n), logp_new.device)
+    rlk_grpo_clip_loss(logp_new, logp_old, advantages, active_mask, eps_low, eps_high, loss_scale,
+                       grad, res, ws)
+    r = GrpoResult.from_buffer_copy(bytes(res.cpu().numpy().tobytes()))
+    return grad, {f: getattr(r, f) for f, _ in GrpoResult._fields_}
+
+
+def logp_from_logits(logits, targets, active_mask=None, temperature=1.0, rows=None,
+                     error_word=None):
+    """(logp[M], lse[M]) fp32 for the selected rows of existing logits."""
+    m = logits.shape[0] if rows is None else rows.shape[0]
+    logp = torch.empty(m, dtype=torch.float32, device=logits.device)
+    lse = torch.empty(m, dtype=torch.float32, device=logits.device)
+    rlk_logp_from_logits(logits, rows, targets, active_mask, temperature, logp, lse, error_word)
+    return logp, lse
 
 
 class LinearLogp(torch.autograd.Function):
@@ -286,3 +521,28 @@ class LinearLogp(torch.autograd.Function):
 
 def linear_logp(hidden, weight, targets, active_mask=None, temperature=1.0):
     return LinearLogp.apply(hidden, weight, targets, active_mask, temperature)
+
+
+class LinearLogpEntropy(torch.autograd.Function):
+    """(logp, entropy) = LinearLogpEntropy.apply(hidden, weight, targets, active_mask, T)."""
+
+    @staticmethod
+    def forward(ctx, hidden, weight, targets, active_mask, temperature):
+        logp, lse, ent = linear_logp_entropy_fwd(hidden, weight, targets, active_mask, temperature)
+        ctx.save_for_backward(hidden, weight, targets, active_mask, lse, ent)
+        ctx.temperature = temperature
+        return logp, ent
+
+    @staticmethod
+    def backward(ctx, grad_logp, grad_entropy):
+        hidden, weight, targets, active_mask, lse, ent = ctx.saved_tensors
+        z = torch.zeros_like(lse)
+        g = z if grad_logp is None else grad_logp.float().contiguous()
+        gh = z if grad_entropy is None else grad_entropy.float().contiguous()
+        dh, dw = linear_logp_entropy_bwd(hidden, weight, targets, active_mask, g, gh, lse, ent,
+                                         ctx.temperature)
+        return dh, dw, None, None, None
+
+
+def linear_logp_entropy(hidden, weight, targets, active_mask=None, temperature=1.0):
+    return LinearLogpEntropy.apply(hidden, weight, targets, active_mask, temperature)

@@ -4,6 +4,7 @@
 // reach the GPU.  The library allocates nothing and never synchronises.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <mutex>
@@ -111,14 +112,14 @@ size_t rlk_linear_logp_bwd_workspace_bytes(int64_t N, int64_t H, int64_t V) {
 
 size_t rlk_dlogp_audit_workspace_bytes(int64_t N) {
     if (N < 0) return 0;
-    return align_up(rlk::audit_blocks(N) * sizeof(rlk::AuditPartial), 256) + 256;
+    return align_up(rlk::audit_v3_blocks(N) * sizeof(rlk::AuditPartial), 256) + 256;
 }
 
-rlk_status_t rlk_linear_logp_fwd(const void* hidden, const void* weight, const int64_t* targets,
-                                 const uint8_t* active_mask, int64_t N, int64_t H, int64_t V,
-                                 double temperature, float* logp_out, float* lse_out,
-                                 void* workspace, size_t workspace_bytes,
-                                 uint32_t* device_error_word, cudaStream_t stream) {
+static rlk_status_t fwd_impl(const void* hidden, const void* weight, const int64_t* targets,
+                             const uint8_t* active_mask, int64_t N, int64_t H, int64_t V,
+                             double temperature, float* logp_out, float* lse_out,
+                             float* entropy_out, void* workspace, size_t workspace_bytes,
+                             uint32_t* device_error_word, cudaStream_t stream) {
     RLK_TRY(check_shape(N, H, V, temperature));
     if (N == 0) return RLK_OK;
     if (hidden == nullptr || weight == nullptr || targets == nullptr || logp_out == nullptr)
@@ -136,16 +137,36 @@ rlk_status_t rlk_linear_logp_fwd(const void* hidden, const void* weight, const i
     const float k = static_cast<float>(1.4426950408889634074 / temperature);
     RLK_CUDA(rlk::launch_fwd(map_h, map_w, targets, active_mask, static_cast<int>(N),
                              static_cast<int>(H), static_cast<int>(V), k, logp_out, lse_out,
-                             workspace, device_error_word, dev.sms, stream));
+                             entropy_out, workspace, device_error_word, dev.sms, stream));
     return RLK_OK;
 }
 
-rlk_status_t rlk_linear_logp_bwd(const void* hidden, const void* weight, const int64_t* targets,
-                                 const uint8_t* active_mask, const float* grad_logp,
-                                 const float* lse, int64_t N, int64_t H, int64_t V,
-                                 double temperature, void* dhidden, void* dweight,
+rlk_status_t rlk_linear_logp_fwd(const void* hidden, const void* weight, const int64_t* targets,
+                                 const uint8_t* active_mask, int64_t N, int64_t H, int64_t V,
+                                 double temperature, float* logp_out, float* lse_out,
                                  void* workspace, size_t workspace_bytes,
                                  uint32_t* device_error_word, cudaStream_t stream) {
+    return fwd_impl(hidden, weight, targets, active_mask, N, H, V, temperature, logp_out, lse_out,
+                    nullptr, workspace, workspace_bytes, device_error_word, stream);
+}
+
+rlk_status_t rlk_linear_logp_entropy_fwd(const void* hidden, const void* weight,
+                                         const int64_t* targets, const uint8_t* active_mask,
+                                         int64_t N, int64_t H, int64_t V, double temperature,
+                                         float* logp_out, float* lse_out, float* entropy_out,
+                                         void* workspace, size_t workspace_bytes,
+                                         uint32_t* device_error_word, cudaStream_t stream) {
+    if (N > 0 && entropy_out == nullptr) return RLK_ERR_INVALID_VALUE;
+    return fwd_impl(hidden, weight, targets, active_mask, N, H, V, temperature, logp_out, lse_out,
+                    entropy_out, workspace, workspace_bytes, device_error_word, stream);
+}
+
+static rlk_status_t bwd_impl(const void* hidden, const void* weight, const int64_t* targets,
+                             const uint8_t* active_mask, const float* grad_logp,
+                             const float* grad_entropy, const float* entropy, const float* lse,
+                             int64_t N, int64_t H, int64_t V, double temperature, void* dhidden,
+                             void* dweight, void* workspace, size_t workspace_bytes,
+                             uint32_t* device_error_word, cudaStream_t stream) {
     RLK_TRY(check_shape(N, H, V, temperature));
     if (N == 0) return RLK_OK;
     if (hidden == nullptr || weight == nullptr || targets == nullptr || grad_logp == nullptr ||
@@ -184,12 +205,37 @@ rlk_status_t rlk_linear_logp_bwd(const void* hidden, const void* weight, const i
         rlk::ChunkMaps cm;
         RLK_TRY(make_map(&cm.ds_kmajor, ds, width, N, uint64_t(rlk::kBwdChunk) * 2, 64, rlk::kTileM));
         RLK_TRY(make_map(&cm.ds_mnmajor, ds, width, N, uint64_t(rlk::kBwdChunk) * 2, 64, 64));
-        RLK_CUDA(rlk::launch_bwd_chunk(maps, cm, targets, active_mask, grad_logp, lse, hidden,
-                                       weight, n, h, v, c, num_chunks, k, temp, ds, dh_acc,
-                                       sorted_y, sorted_t, dhidden, dweight, device_error_word,
-                                       dev.sms, stream));
+        RLK_CUDA(rlk::launch_bwd_chunk(maps, cm, targets, active_mask, grad_logp, grad_entropy,
+                                       entropy, lse, hidden, weight, n, h, v, c, num_chunks, k,
+                                       temp, ds, dh_acc, sorted_y, sorted_t, dhidden, dweight,
+                                       device_error_word, dev.sms, stream));
     }
     return RLK_OK;
+}
+
+rlk_status_t rlk_linear_logp_bwd(const void* hidden, const void* weight, const int64_t* targets,
+                                 const uint8_t* active_mask, const float* grad_logp,
+                                 const float* lse, int64_t N, int64_t H, int64_t V,
+                                 double temperature, void* dhidden, void* dweight,
+                                 void* workspace, size_t workspace_bytes,
+                                 uint32_t* device_error_word, cudaStream_t stream) {
+    return bwd_impl(hidden, weight, targets, active_mask, grad_logp, nullptr, nullptr, lse, N, H,
+                    V, temperature, dhidden, dweight, workspace, workspace_bytes,
+                    device_error_word, stream);
+}
+
+rlk_status_t rlk_linear_logp_entropy_bwd(const void* hidden, const void* weight,
+                                         const int64_t* targets, const uint8_t* active_mask,
+                                         const float* grad_logp, const float* grad_entropy,
+                                         const float* lse, const float* entropy, int64_t N,
+                                         int64_t H, int64_t V, double temperature,
+                                         void* dhidden, void* dweight, void* workspace,
+                                         size_t workspace_bytes, uint32_t* device_error_word,
+                                         cudaStream_t stream) {
+    if (N > 0 && (grad_entropy == nullptr || entropy == nullptr)) return RLK_ERR_INVALID_VALUE;
+    return bwd_impl(hidden, weight, targets, active_mask, grad_logp, grad_entropy, entropy, lse,
+                    N, H, V, temperature, dhidden, dweight, workspace, workspace_bytes,
+                    device_error_word, stream);
 }
 
 rlk_status_t rlk_dlogp_audit(const float* logp_new, const float* logp_old,
@@ -208,6 +254,117 @@ rlk_status_t rlk_dlogp_audit(const float* logp_new, const float* logp_old,
                         (active_mask == nullptr || aligned(active_mask, 4));
     RLK_CUDA(rlk::launch_audit(logp_new, logp_old, active_mask, N, result_dev, workspace, vec_ok,
                                stream));
+    return RLK_OK;
+}
+
+int64_t rlk_linear_logp_num_partials(int64_t V_local) {
+    return V_local < 1 ? 0 : rlk::fwd_num_chunks(V_local);
+}
+
+rlk_status_t rlk_linear_logp_fwd_shard(const void* hidden, const void* weight_shard,
+                                       const int64_t* targets, const uint8_t* active_mask,
+                                       int64_t N, int64_t H, int64_t V_local,
+                                       int64_t vocab_start, double temperature,
+                                       float* partials_out, float* target_logit_out,
+                                       uint32_t* device_error_word, cudaStream_t stream) {
+    RLK_TRY(check_shape(N, H, V_local, temperature));
+    if (vocab_start < 0 || vocab_start + V_local > kMaxDim) return RLK_ERR_INVALID_VALUE;
+    if (vocab_start % rlk::kFwdChunk != 0) return RLK_ERR_UNSUPPORTED;
+    if (N == 0) return RLK_OK;
+    if (hidden == nullptr || weight_shard == nullptr || targets == nullptr ||
+        partials_out == nullptr || target_logit_out == nullptr)
+        return RLK_ERR_INVALID_VALUE;
+    if (!aligned(hidden, 16) || !aligned(weight_shard, 16) || !aligned(partials_out, 8))
+        return RLK_ERR_INVALID_VALUE;
+    DeviceInfo dev;
+    RLK_TRY(current_device(dev));
+    CUtensorMap map_h, map_w;
+    RLK_TRY(make_map(&map_h, hidden, H, N, H * 2, 64, rlk::kTileM));
+    RLK_TRY(make_map(&map_w, weight_shard, H, V_local, H * 2, 64, rlk::kTileV));
+    const float k = static_cast<float>(1.4426950408889634074 / temperature);
+    RLK_CUDA(rlk::launch_fwd_partials(map_h, map_w, targets, active_mask, static_cast<int>(N),
+                                      static_cast<int>(H), static_cast<int>(V_local),
+                                      vocab_start, k, reinterpret_cast<float2*>(partials_out),
+                                      target_logit_out, device_error_word, dev.sms, stream));
+    return RLK_OK;
+}
+
+rlk_status_t rlk_linear_logp_merge(const float* partials, int64_t num_partials,
+                                   const float* target_logit, const int64_t* targets,
+                                   const uint8_t* active_mask, int64_t N, int64_t V,
+                                   double temperature, float* logp_out, float* lse_out,
+                                   uint32_t* device_error_word, cudaStream_t stream) {
+    if (N < 0 || N > kMaxDim || V < 1 || V > kMaxDim) return RLK_ERR_INVALID_VALUE;
+    if (!(std::isfinite(temperature) && temperature > 0.0)) return RLK_ERR_INVALID_VALUE;
+    if (num_partials < 1 || num_partials > (int64_t(1) << 24)) return RLK_ERR_INVALID_VALUE;
+    if (N == 0) return RLK_OK;
+    if (partials == nullptr || target_logit == nullptr || targets == nullptr || logp_out == nullptr)
+        return RLK_ERR_INVALID_VALUE;
+    if (!aligned(partials, 8)) return RLK_ERR_INVALID_VALUE;
+    DeviceInfo dev;
+    RLK_TRY(current_device(dev));
+    const float k = static_cast<float>(1.4426950408889634074 / temperature);
+    RLK_CUDA(rlk::launch_fwd_merge(reinterpret_cast<const float2*>(partials),
+                                   static_cast<int>(num_partials), target_logit, targets,
+                                   active_mask, static_cast<int>(N), static_cast<int>(V), k,
+                                   logp_out, lse_out, device_error_word, stream));
+    return RLK_OK;
+}
+
+rlk_status_t rlk_logp_from_logits(const void* logits, int32_t dtype, int64_t N, int64_t V,
+                                  int64_t row_stride, const int64_t* rows, int64_t M,
+                                  const int64_t* targets, const uint8_t* active_mask,
+                                  double temperature, float* logp_out, float* lse_out,
+                                  uint32_t* device_error_word, cudaStream_t stream) {
+    if (dtype != RLK_DTYPE_F32 && dtype != RLK_DTYPE_BF16) return RLK_ERR_UNSUPPORTED;
+    if (N < 0 || N > kMaxDim || V < 1 || V > kMaxDim || row_stride < V) return RLK_ERR_INVALID_VALUE;
+    if (!(std::isfinite(temperature) && temperature > 0.0)) return RLK_ERR_INVALID_VALUE;
+    if (rows == nullptr) M = N;
+    if (M < 0 || M > kMaxDim) return RLK_ERR_INVALID_VALUE;
+    if (M == 0) return RLK_OK;
+    if (logits == nullptr || targets == nullptr || logp_out == nullptr) return RLK_ERR_INVALID_VALUE;
+    const size_t esize = dtype == RLK_DTYPE_F32 ? 4 : 2;
+    if (!aligned(logits, esize)) return RLK_ERR_INVALID_VALUE;
+    DeviceInfo dev;
+    RLK_TRY(current_device(dev));
+    const bool vec_ok = aligned(logits, 16) && (static_cast<size_t>(row_stride) * esize) % 16 == 0;
+    const float k = static_cast<float>(1.4426950408889634074 / temperature);
+    RLK_CUDA(rlk::launch_logp_from_logits(logits, dtype == RLK_DTYPE_BF16, row_stride, N,
+                                          static_cast<int>(V), rows, static_cast<int>(M),
+                                          targets, active_mask, k, vec_ok, logp_out, lse_out,
+                                          device_error_word, stream));
+    return RLK_OK;
+}
+
+size_t rlk_grpo_clip_loss_workspace_bytes(int64_t N) {
+    if (N < 0) return 0;
+    return align_up(rlk::audit_blocks(N) * sizeof(rlk::LossPartial), 256) + 256;
+}
+
+rlk_status_t rlk_grpo_clip_loss(const float* logp_new, const float* logp_old,
+                                const float* advantages, const uint8_t* active_mask, int64_t N,
+                                double eps_low, double eps_high, double loss_scale,
+                                float* grad_out, rlk_grpo_result_t* result_dev, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream) {
+    if (N < 0 || N > (int64_t(1) << 40)) return RLK_ERR_INVALID_VALUE;
+    if (!(std::isfinite(eps_low) && eps_low >= 0.0 && eps_low < 1.0)) return RLK_ERR_INVALID_VALUE;
+    if (!(std::isfinite(eps_high) && eps_high >= 0.0)) return RLK_ERR_INVALID_VALUE;
+    if (!(std::isfinite(loss_scale) && loss_scale > 0.0)) return RLK_ERR_INVALID_VALUE;
+    if (result_dev == nullptr) return RLK_ERR_INVALID_VALUE;
+    if (N > 0 && (logp_new == nullptr || logp_old == nullptr || advantages == nullptr ||
+                  grad_out == nullptr))
+        return RLK_ERR_INVALID_VALUE;
+    if (workspace == nullptr || !aligned(workspace, 256) ||
+        workspace_bytes < rlk_grpo_clip_loss_workspace_bytes(N))
+        return RLK_ERR_WORKSPACE;
+    DeviceInfo dev;
+    RLK_TRY(current_device(dev));
+    const bool vec_ok = aligned(logp_new, 16) && aligned(logp_old, 16) &&
+                        aligned(advantages, 16) && aligned(grad_out, 16) &&
+                        (active_mask == nullptr || aligned(active_mask, 4));
+    RLK_CUDA(rlk::launch_grpo_loss(logp_new, logp_old, advantages, active_mask, N, eps_low,
+                                   eps_high, loss_scale, grad_out, result_dev, workspace, vec_ok,
+                                   stream));
     return RLK_OK;
 }
 

@@ -6,13 +6,18 @@
 // approx_kl0 = mean(exp(dlogp) - 1 - dlogp); the active-token count.
 //
 // Pass 1: block b owns the fixed slice [b*4096, (b+1)*4096) (a function of N
-// only).  Each thread handles 16 elements in ascending index order:
-// d = new - old in fp32 (a correctly rounded difference), its count, the
-// largest |d| with the first index attaining it, and fp32 sums of d and of
-// kl(d) = exp(d) - 1 - d.  The sums go to fp64 for a fixed shuffle tree
-// (lanes, then warps).  Pass 2: one block merges the per-block partials,
+// only).  Each thread issues all its loads first (4 float4 of each input and 4
+// mask words, streaming cache hint), then handles its 16 elements in ascending
+// index order without branches: d = new - old in fp32 (a correctly rounded
+// difference), its count, the largest |d| as an order-preserving integer key
+// with the first offset attaining it, and fp32 sums of d and of
+// kl(d) = exp(d) - 1 - d.  A fixed shuffle tree combines the 32 lanes (fp32
+// sums, integer counts), and thread 0 folds the eight warp partials in warp
+// order in fp64.  Pass 2: one block merges the per-block partials,
 // each thread a fixed strided subset in ascending order, then the same
-// fixed tree.  No atomics; the result is bitwise reproducible for a given N.
+// fixed tree; it is launched with programmatic dependent launch, so its launch
+// overlaps pass 1 and it waits for pass 1's results in-kernel.  No atomics; the
+// result is bitwise reproducible for a given N.
 //
 // kl(d) for |d| < 1/2 is the Taylor series d^2 (1/2 + d/6 + d^2/24 + ...)
 // through the d^9 term (truncation below 3e-9 relative); elsewhere it is
@@ -117,69 +122,121 @@ __device__ __forceinline__ Acc block_reduce(Acc a) {
     return a;
 }
 
-__device__ __forceinline__ void visit(float nw, float od, uint8_t m, int64_t idx, int64_t& count,
-                                      float& best, int64_t& arg, float& sd, float& skl,
-                                      uint32_t& flags) {
+// Per-thread state of pass 1.  |d| is kept as an order-preserving integer key
+// (non-negative floats order like their bit patterns; NaN maps above every
+// number), the best key's element offset inside the block, and fp32 sums.
+struct ThreadAcc {
+    int count = 0;
+    uint32_t key = 0;          // 0 = nothing seen (every active |d| has key >= 0 ... see below)
+    int arg = -1;              // offset of the best element inside the block
+    float sd = 0.f, skl = 0.f;
+    uint32_t flags = 0;
+};
+
+// key(|d|) + 1, so that 0 means "no active element yet": ties keep the first
+// (strict comparison), NaN ranks above +inf.
+__device__ __forceinline__ uint32_t abs_key(float d) {
+    const uint32_t bits = __float_as_uint(d) & 0x7fffffffu;
+    return (bits > 0x7f800000u ? 0x7fc00000u : bits) + 1u;
+}
+
+__device__ __forceinline__ void visit3(float nw, float od, uint32_t m, int off, ThreadAcc& a) {
     if (m == 0) return;
     const float d = nw - od;
-    const float a = fabsf(d);
-    if (count == 0 || ranks_above(a, idx, best, arg)) {
-        best = a;
-        arg = idx;
-    }
-    ++count;
-    sd += d;
-    skl += kl_term(d);
-    if (!isfinite(d)) flags |= 1u;
+    const uint32_t key = abs_key(d);
+    const bool better = key > a.key;
+    a.key = better ? key : a.key;
+    a.arg = better ? off : a.arg;
+    a.count += 1;
+    a.sd += d;
+    a.skl += kl_term(d);
+    a.flags |= (key > 0x7f800000u) ? 1u : 0u;    // |d| is inf or NaN
 }
 
 template <bool VEC>
 __global__ void __launch_bounds__(kAuditThreads)
     audit_pass1(const float* __restrict__ nw, const float* __restrict__ od,
                 const uint8_t* __restrict__ mask, int64_t N, AuditPartial* __restrict__ out) {
-    const int64_t base = static_cast<int64_t>(blockIdx.x) * kAuditBlockElems;
-    int64_t count = 0, arg = INT64_MAX;
-    float best = -1.0f, sd = 0.f, skl = 0.f;
-    uint32_t flags = 0;
-    const bool full = base + kAuditBlockElems <= N;
+    // let the merge kernel launch now; it waits for this grid before reading
+    asm volatile("griddepcontrol.launch_dependents;");
+    constexpr int kVec = kAuditV3PerThread / 4;
+    constexpr int kBlock = kAuditThreads * kAuditV3PerThread;
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * kBlock;
+    ThreadAcc a;
+    if (VEC && base + kBlock <= N) {
+        float4 x[kVec], y[kVec];
+        uint32_t m[kVec];
 #pragma unroll
-    for (int j = 0; j < kAuditPerThread / 4; ++j) {
-        const int64_t i0 = base + j * (kAuditThreads * 4) + threadIdx.x * 4;
-        if (VEC && full) {
-            const float4 a = *reinterpret_cast<const float4*>(nw + i0);
-            const float4 b = *reinterpret_cast<const float4*>(od + i0);
-            uchar4 m = make_uchar4(1, 1, 1, 1);
-            if (mask != nullptr) m = *reinterpret_cast<const uchar4*>(mask + i0);
-            visit(a.x, b.x, m.x, i0, count, best, arg, sd, skl, flags);
-            visit(a.y, b.y, m.y, i0 + 1, count, best, arg, sd, skl, flags);
-            visit(a.z, b.z, m.z, i0 + 2, count, best, arg, sd, skl, flags);
-            visit(a.w, b.w, m.w, i0 + 3, count, best, arg, sd, skl, flags);
-        } else {
+        for (int j = 0; j < kVec; ++j) {
+            const int64_t i0 = base + j * (kAuditThreads * 4) + threadIdx.x * 4;
+            x[j] = __ldcs(reinterpret_cast<const float4*>(nw + i0));
+            y[j] = __ldcs(reinterpret_cast<const float4*>(od + i0));
+            m[j] = mask == nullptr ? 0x01010101u
+                                   : __ldcs(reinterpret_cast<const unsigned int*>(mask + i0));
+        }
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+            const int o = j * (kAuditThreads * 4) + threadIdx.x * 4;
+            visit3(x[j].x, y[j].x, m[j] & 0xffu, o, a);
+            visit3(x[j].y, y[j].y, (m[j] >> 8) & 0xffu, o + 1, a);
+            visit3(x[j].z, y[j].z, (m[j] >> 16) & 0xffu, o + 2, a);
+            visit3(x[j].w, y[j].w, m[j] >> 24, o + 3, a);
+        }
+    } else {
+#pragma unroll 1
+        for (int j = 0; j < kVec; ++j) {
+            const int o0 = j * (kAuditThreads * 4) + threadIdx.x * 4;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int64_t i = i0 + e;
-                if (i < N)
-                    visit(nw[i], od[i], mask == nullptr ? uint8_t(1) : mask[i], i, count, best, arg,
-                          sd, skl, flags);
+                const int64_t i = base + o0 + e;
+                if (i < N) visit3(nw[i], od[i], mask == nullptr ? 1u : mask[i], o0 + e, a);
             }
         }
     }
-    Acc a;
-    a.count = count;
-    a.arg = arg;
-    a.sum_d = static_cast<double>(sd);
-    a.sum_kl = static_cast<double>(skl);
-    a.best = best;
-    a.flags = flags;
-    a = block_reduce<kAuditThreads>(a);
+    // fixed tree over the warp (fp32 sums, integer counts, key / offset max)
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const int c = __shfl_down_sync(0xffffffffu, a.count, off);
+        const uint32_t k = __shfl_down_sync(0xffffffffu, a.key, off);
+        const int g = __shfl_down_sync(0xffffffffu, a.arg, off);
+        const float sd = __shfl_down_sync(0xffffffffu, a.sd, off);
+        const float skl = __shfl_down_sync(0xffffffffu, a.skl, off);
+        const uint32_t f = __shfl_down_sync(0xffffffffu, a.flags, off);
+        if (lane + off < 32) {
+            const bool take = k > a.key || (k == a.key && k != 0 && g < a.arg);
+            a.key = take ? k : a.key;
+            a.arg = take ? g : a.arg;
+            a.count += c;
+            a.sd += sd;
+            a.skl += skl;
+            a.flags |= f;
+        }
+    }
+    // the eight warp partials, in warp order, in fp64
+    __shared__ Acc warp_acc[kAuditThreads / 32];
+    if (lane == 0) {
+        Acc w;
+        w.count = a.count;
+        w.arg = a.key == 0 ? INT64_MAX : base + a.arg;
+        w.sum_d = static_cast<double>(a.sd);
+        w.sum_kl = static_cast<double>(a.skl);
+        w.best = a.key == 0 ? -1.0f : __uint_as_float(a.key - 1u);
+        w.flags = a.flags;
+        warp_acc[warp] = w;
+    }
+    __syncthreads();
     if (threadIdx.x == 0) {
+        Acc t = warp_acc[0];
+#pragma unroll
+        for (int w = 1; w < kAuditThreads / 32; ++w) merge(t, warp_acc[w]);
         AuditPartial p;
-        p.count = a.count;
-        p.arg = a.arg;
-        p.sum_d = a.sum_d;
-        p.sum_kl = a.sum_kl;
-        p.best = a.best;
-        p.flags = a.flags;
+        p.count = t.count;
+        p.arg = t.arg;
+        p.sum_d = t.sum_d;
+        p.sum_kl = t.sum_kl;
+        p.best = t.best;
+        p.flags = t.flags;
         out[blockIdx.x] = p;
     }
 }
@@ -189,6 +246,9 @@ constexpr int kMergeThreads = 1024;
 __global__ void __launch_bounds__(kMergeThreads)
     audit_pass2(const AuditPartial* __restrict__ parts, int64_t num_parts,
                 rlk_audit_result_t* __restrict__ result) {
+    // launched early (programmatic dependent launch): wait until every block of
+    // pass 1 has finished and its partials are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     Acc a = empty_acc();
     for (int64_t i = threadIdx.x; i < num_parts; i += kMergeThreads) {
         const AuditPartial p = parts[i];
@@ -221,7 +281,8 @@ __global__ void __launch_bounds__(kMergeThreads)
 // in the library image, so every GPU that loads the library holds it until the
 // process exits.  Pass 1 writes every slot that pass 2 reads, so nothing in it
 // has to start at zero; calls that overlap on the GPU share it and race.
-constexpr size_t kNoAllocBlocks = static_cast<size_t>(RLK_AUDIT_NOALLOC_MAX_N) / kAuditBlockElems;
+constexpr size_t kNoAllocBlocks =
+    static_cast<size_t>(RLK_AUDIT_NOALLOC_MAX_N) / (kAuditThreads * kAuditV3PerThread);
 static __device__ __align__(256) AuditPartial g_audit_noalloc_scratch[kNoAllocBlocks];
 
 cudaError_t audit_noalloc_scratch(void** out) {
@@ -247,7 +308,7 @@ cudaError_t audit_noalloc_scratch(void** out) {
 cudaError_t launch_audit(const float* logp_new, const float* logp_old, const uint8_t* mask,
                          int64_t N, rlk_audit_result_t* result, void* workspace, bool vec_ok,
                          cudaStream_t stream) {
-    const size_t blocks = audit_blocks(N);
+    const size_t blocks = audit_v3_blocks(N);
     AuditPartial* parts = static_cast<AuditPartial*>(workspace);
     if (blocks > 0) {
         if (vec_ok)
@@ -259,8 +320,19 @@ cudaError_t launch_audit(const float* logp_new, const float* logp_old, const uin
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    audit_pass2<<<1, kMergeThreads, 0, stream>>>(parts, static_cast<int64_t>(blocks), result);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const AuditPartial* cparts = parts;
+    const int64_t nparts = static_cast<int64_t>(blocks);
+    return cudaLaunchKernelEx(&cfg, audit_pass2, cparts, nparts, result);
 }
 
 }  // namespace rlk

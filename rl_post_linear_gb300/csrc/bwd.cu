@@ -62,13 +62,19 @@ __device__ __forceinline__ void bf16x8_to_f32(uint4 v, float* out) {
 
 // ----------------------------------------------------------------------------- dS_c
 
-struct DsPolicy {
+// ENT adds the entropy gradient: with Ez = lse - entropy (= E_p[z]),
+//   dS = p (c1 + c2 S),  c1 = -(g - gH Ez) / T,  c2 = -gH / T^2,
+// i.e. -(p/T) (g + gH (S/T - Ez)), the entropy's dH/dz = -p (z - E[z]).
+template <bool ENT>
+struct DsPolicyT {
     static constexpr bool kAMn = false;   // h [N,H]
     static constexpr bool kBMn = false;   // W [V,H]
 
     const int64_t* targets;
     const uint8_t* mask;
     const float* grad;
+    const float* grad_ent;   // ENT only
+    const float* ent;        // ENT only
     const float* lse;
     __nv_bfloat16* ds;    // [N][kBwdChunk]
     int N, V, c0, num_m, num_n, kblocks;
@@ -91,7 +97,7 @@ struct DsPolicy {
     }
 
     struct EpiState {
-        float coef, lse2;
+        float coef, c2, lse2;
         bool live;
     };
 
@@ -101,8 +107,16 @@ struct DsPolicy {
         const int t = m * kTileM + row;
         int64_t y;
         st.live = row_live(targets, mask, t, N, V, y);
-        st.coef = st.live ? -__fdiv_rn(grad[t], temp) : 0.f;
         st.lse2 = st.live ? lse[t] * kLog2e : 0.f;
+        if constexpr (ENT) {
+            const float gh = st.live ? grad_ent[t] : 0.f;
+            const float ez = st.live ? lse[t] - ent[t] : 0.f;
+            st.coef = st.live ? -__fdiv_rn(fmaf(-gh, ez, grad[t]), temp) : 0.f;
+            st.c2 = st.live ? -__fdiv_rn(gh, temp * temp) : 0.f;
+        } else {
+            st.coef = st.live ? -__fdiv_rn(grad[t], temp) : 0.f;
+            st.c2 = 0.f;
+        }
     }
 
     __device__ void epi_tile(int u, int, int row, uint32_t taddr, EpiState& st) const {
@@ -121,10 +135,15 @@ struct DsPolicy {
             for (int j = 0; j < 16; ++j) {
                 const float s0 = __uint_as_float(r[2 * j]);
                 const float s1 = __uint_as_float(r[2 * j + 1]);
+                float c0 = st.coef, c1 = st.coef;
+                if constexpr (ENT) {
+                    c0 = fmaf(st.c2, s0, st.coef);
+                    c1 = fmaf(st.c2, s1, st.coef);
+                }
                 const float d0 = (st.live && vb + 2 * j < V)
-                                     ? st.coef * ex2_approx(fmaf(s0, k, -st.lse2)) : 0.f;
+                                     ? c0 * ex2_approx(fmaf(s0, k, -st.lse2)) : 0.f;
                 const float d1 = (st.live && vb + 2 * j + 1 < V)
-                                     ? st.coef * ex2_approx(fmaf(s1, k, -st.lse2)) : 0.f;
+                                     ? c1 * ex2_approx(fmaf(s1, k, -st.lse2)) : 0.f;
                 packed[j] = pack_bf16x2(d0, d1);
             }
             uint4* dst = reinterpret_cast<uint4*>(ds + static_cast<size_t>(t) * kBwdChunk + col);
@@ -393,8 +412,34 @@ static cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const
     return cudaGetLastError();
 }
 
+template <bool ENT>
+static cudaError_t launch_ds(const BwdMaps& maps, const int64_t* targets, const uint8_t* mask,
+                             const float* grad, const float* grad_ent, const float* ent,
+                             const float* lse, int N, int H, int V, int c0, int width, float k,
+                             float temp, void* ds, uint32_t* err, int num_sms,
+                             cudaStream_t stream) {
+    DsPolicyT<ENT> ps;
+    ps.targets = targets;
+    ps.mask = mask;
+    ps.grad = grad;
+    ps.grad_ent = grad_ent;
+    ps.ent = ent;
+    ps.lse = lse;
+    ps.ds = static_cast<__nv_bfloat16*>(ds);
+    ps.N = N;
+    ps.V = V;
+    ps.c0 = c0;
+    ps.num_m = (N + kTileM - 1) / kTileM;
+    ps.num_n = (width + kTileV - 1) / kTileV;
+    ps.kblocks = H / 64;
+    ps.k = k;
+    ps.temp = temp;
+    return launch_gemm(maps.h_kmajor, maps.w_kmajor, ps, ps.num_m * ps.num_n, num_sms, err, stream);
+}
+
 cudaError_t launch_bwd_chunk(const BwdMaps& maps, const ChunkMaps& cmaps, const int64_t* targets,
-                             const uint8_t* mask, const float* grad, const float* lse,
+                             const uint8_t* mask, const float* grad, const float* grad_ent,
+                             const float* ent, const float* lse,
                              const void* hidden, const void* weight, int N, int H, int V,
                              int chunk, int num_chunks, float k, float temp, void* ds,
                              float* dh_acc, const int* sorted_y, const int* sorted_t,
@@ -404,22 +449,11 @@ cudaError_t launch_bwd_chunk(const BwdMaps& maps, const ChunkMaps& cmaps, const 
     const int width = (V - c0) < kBwdChunk ? (V - c0) : kBwdChunk;
     const int num_m = (N + kTileM - 1) / kTileM;
 
-    DsPolicy ps;
-    ps.targets = targets;
-    ps.mask = mask;
-    ps.grad = grad;
-    ps.lse = lse;
-    ps.ds = static_cast<__nv_bfloat16*>(ds);
-    ps.N = N;
-    ps.V = V;
-    ps.c0 = c0;
-    ps.num_m = num_m;
-    ps.num_n = (width + kTileV - 1) / kTileV;
-    ps.kblocks = H / 64;
-    ps.k = k;
-    ps.temp = temp;
-    cudaError_t e = launch_gemm(maps.h_kmajor, maps.w_kmajor, ps, ps.num_m * ps.num_n, num_sms,
-                                err, stream);
+    cudaError_t e = grad_ent != nullptr
+        ? launch_ds<true>(maps, targets, mask, grad, grad_ent, ent, lse, N, H, V, c0, width, k,
+                          temp, ds, err, num_sms, stream)
+        : launch_ds<false>(maps, targets, mask, grad, nullptr, nullptr, lse, N, H, V, c0, width,
+                           k, temp, ds, err, num_sms, stream);
     if (e != cudaSuccess) return e;
 
     DhPolicy pd;

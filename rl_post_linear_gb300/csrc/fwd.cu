@@ -49,15 +49,24 @@ __device__ __forceinline__ float select32(const float (&x)[32], int i) {
     return (i & 1) ? d[1] : d[0];
 }
 
-struct FwdPolicy {
+// Stand-in for the logits of columns past V: far below any logit, so that
+// 2^((x - m) k) underflows to exactly 0, and finite, so that 0 * x stays 0.
+constexpr float kMaskedLogit = -3.0e38f;
+
+// ENT adds the running sum a = sum_j 2^((S_j - m) k) S_j per row, from which
+// the merge forms E[S] = a / s and the entropy lse - E[S]/T.
+template <bool ENT>
+struct FwdPolicyT {
     static constexpr bool kAMn = false;   // h [N,H]: K-major
     static constexpr bool kBMn = false;   // W [V,H]: K-major
 
     const int64_t* targets;
     const uint8_t* mask;
     float2* partials;     // [num_chunks][N]
+    float* partials_a;    // [num_chunks][N] (ENT only)
     float* s_target;      // [N]
-    int N, V, num_m, num_vt, num_chunks, kblocks;
+    int64_t vocab_start;  // global id of this weight block's first row
+    int N, V, num_m, num_vt, num_chunks, kblocks;   // V: rows of this weight block
     float k;              // log2(e) / T
 
     __device__ int num_units() const { return num_m * num_chunks; }
@@ -81,7 +90,7 @@ struct FwdPolicy {
     }
 
     struct EpiState {
-        float m, s, sy;
+        float m, s, a, sy;
         int64_t y;
         bool found;
     };
@@ -92,6 +101,7 @@ struct FwdPolicy {
         const int t = m * kTileM + row;
         st.m = -INFINITY;
         st.s = 0.f;
+        st.a = 0.f;
         st.sy = 0.f;
         st.found = false;
         st.y = -1;
@@ -115,9 +125,9 @@ struct FwdPolicy {
             if (nv < 32) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                    if (j >= nv) x[j] = -INFINITY;
+                    if (j >= nv) x[j] = kMaskedLogit;
             }
-            const int64_t dy = st.y - vb;
+            const int64_t dy = st.y - vocab_start - vb;
             if (dy >= 0 && dy < 32) {
                 st.sy = select32(x, static_cast<int>(dy));
                 st.found = true;
@@ -126,9 +136,21 @@ struct FwdPolicy {
 #pragma unroll
             for (int j = 1; j < 32; ++j) cm = fmaxf(cm, x[j]);
             const float nm = fmaxf(st.m, cm);
-            float acc = st.s * ex2_approx((st.m - nm) * k);
+            const float rescale = ex2_approx((st.m - nm) * k);
+            float acc = st.s * rescale;
+            if constexpr (ENT) {
+                float aa = st.a * rescale;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc += ex2_approx((x[j] - nm) * k);
+                for (int j = 0; j < 32; ++j) {
+                    const float e = ex2_approx((x[j] - nm) * k);
+                    acc += e;
+                    aa = fmaf(e, x[j], aa);
+                }
+                st.a = aa;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) acc += ex2_approx((x[j] - nm) * k);
+            }
             st.s = acc;
             st.m = nm;
         }
@@ -140,33 +162,39 @@ struct FwdPolicy {
         const int t = m * kTileM + row;
         if (t >= N) return;
         partials[static_cast<size_t>(c) * N + t] = make_float2(st.m, st.s);
+        if constexpr (ENT) partials_a[static_cast<size_t>(c) * N + t] = st.a;
         if (st.found) s_target[t] = st.sy;
     }
 };
 
 __global__ void fwd_merge_kernel(const float2* __restrict__ partials,
+                                 const float* __restrict__ partials_a,
                                  const float* __restrict__ s_target,
                                  const int64_t* __restrict__ targets,
                                  const uint8_t* __restrict__ mask, int N, int V, int num_chunks,
                                  float k, float* __restrict__ logp, float* __restrict__ lse,
-                                 uint32_t* err) {
+                                 float* __restrict__ entropy, uint32_t* err) {
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= N) return;
     if (mask != nullptr && mask[t] == 0) {
         logp[t] = 0.f;
         if (lse != nullptr) lse[t] = 0.f;
+        if (entropy != nullptr) entropy[t] = 0.f;
         return;
     }
     float m = -INFINITY;
     for (int c = 0; c < num_chunks; ++c) m = fmaxf(m, partials[static_cast<size_t>(c) * N + t].x);
-    float sigma = 0.f;
+    float sigma = 0.f, a = 0.f;
     for (int c = 0; c < num_chunks; ++c) {
         const float2 pc = partials[static_cast<size_t>(c) * N + t];
-        sigma += pc.y * ex2_approx((pc.x - m) * k);
+        const float wgt = ex2_approx((pc.x - m) * k);
+        sigma += pc.y * wgt;
+        if (entropy != nullptr) a += partials_a[static_cast<size_t>(c) * N + t] * wgt;
     }
     const float lse2 = m * k + lg2_approx(sigma);
     constexpr float kLn2 = 0.693147180559945309f;
     if (lse != nullptr) lse[t] = lse2 * kLn2;
+    if (entropy != nullptr) entropy[t] = (lse2 - (a / sigma) * k) * kLn2;
     const int64_t y = targets[t];
     if (y < 0 || y >= V) {
         logp[t] = __int_as_float(0x7fc00000);
@@ -176,34 +204,71 @@ __global__ void fwd_merge_kernel(const float2* __restrict__ partials,
     logp[t] = (s_target[t] * k - lse2) * kLn2;
 }
 
-cudaError_t launch_fwd(const CUtensorMap& map_h, const CUtensorMap& map_w, const int64_t* targets,
-                       const uint8_t* mask, int N, int H, int V, float k, float* logp, float* lse,
-                       void* workspace, uint32_t* err, int num_sms, cudaStream_t stream) {
-    FwdLayout lay(N, V);
-    FwdPolicy p;
+template <bool ENT>
+static cudaError_t launch_partials_t(const CUtensorMap& map_h, const CUtensorMap& map_w,
+                                     const int64_t* targets, const uint8_t* mask, int N, int H,
+                                     int V_local, int64_t vocab_start, float k, float2* partials,
+                                     float* partials_a, float* s_target, uint32_t* err,
+                                     int num_sms, cudaStream_t stream) {
+    FwdPolicyT<ENT> p;
     p.targets = targets;
     p.mask = mask;
-    p.partials = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + lay.partial_off);
-    p.s_target = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + lay.target_off);
+    p.partials = partials;
+    p.partials_a = partials_a;
+    p.s_target = s_target;
+    p.vocab_start = vocab_start;
     p.N = N;
-    p.V = V;
+    p.V = V_local;
     p.num_m = (N + kTileM - 1) / kTileM;
-    p.num_vt = (V + kTileV - 1) / kTileV;
-    p.num_chunks = static_cast<int>(lay.num_chunks);
+    p.num_vt = (V_local + kTileV - 1) / kTileV;
+    p.num_chunks = (p.num_vt + kFwdTilesPerChunk - 1) / kFwdTilesPerChunk;
     p.kblocks = H / 64;
     p.k = k;
-
-    auto kern = gemm_persistent_kernel<FwdPolicy>;
+    auto kern = gemm_persistent_kernel<FwdPolicyT<ENT>>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kGemmSmemBytes));
     if (e != cudaSuccess) return e;
     const long long units = static_cast<long long>(p.num_m) * p.num_chunks;
     const int grid = static_cast<int>(units < num_sms ? units : num_sms);
     kern<<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(map_h, map_w, p, err);
-    e = cudaGetLastError();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_partials(const CUtensorMap& map_h, const CUtensorMap& map_w,
+                                const int64_t* targets, const uint8_t* mask, int N, int H,
+                                int V_local, int64_t vocab_start, float k, float2* partials,
+                                float* s_target, uint32_t* err, int num_sms, cudaStream_t stream) {
+    return launch_partials_t<false>(map_h, map_w, targets, mask, N, H, V_local, vocab_start, k,
+                                    partials, nullptr, s_target, err, num_sms, stream);
+}
+
+cudaError_t launch_fwd_merge(const float2* partials, int num_chunks, const float* s_target,
+                             const int64_t* targets, const uint8_t* mask, int N, int V, float k,
+                             float* logp, float* lse, uint32_t* err, cudaStream_t stream) {
+    fwd_merge_kernel<<<(N + 255) / 256, 256, 0, stream>>>(partials, nullptr, s_target, targets,
+                                                          mask, N, V, num_chunks, k, logp, lse,
+                                                          nullptr, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(const CUtensorMap& map_h, const CUtensorMap& map_w, const int64_t* targets,
+                       const uint8_t* mask, int N, int H, int V, float k, float* logp, float* lse,
+                       float* entropy, void* workspace, uint32_t* err, int num_sms,
+                       cudaStream_t stream) {
+    FwdLayout lay(N, V);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    float2* partials = reinterpret_cast<float2*>(ws + lay.partial_off);
+    float* partials_a = reinterpret_cast<float*>(ws + lay.partial_a_off);
+    float* s_target = reinterpret_cast<float*>(ws + lay.target_off);
+    cudaError_t e = entropy != nullptr
+        ? launch_partials_t<true>(map_h, map_w, targets, mask, N, H, V, 0, k, partials, partials_a,
+                                  s_target, err, num_sms, stream)
+        : launch_partials_t<false>(map_h, map_w, targets, mask, N, H, V, 0, k, partials, nullptr,
+                                   s_target, err, num_sms, stream);
     if (e != cudaSuccess) return e;
-    fwd_merge_kernel<<<(N + 255) / 256, 256, 0, stream>>>(p.partials, p.s_target, targets, mask, N,
-                                                          V, p.num_chunks, k, logp, lse, err);
+    fwd_merge_kernel<<<(N + 255) / 256, 256, 0, stream>>>(
+        partials, entropy != nullptr ? partials_a : nullptr, s_target, targets, mask, N, V,
+        static_cast<int>(lay.num_chunks), k, logp, lse, entropy, err);
     return cudaGetLastError();
 }
 

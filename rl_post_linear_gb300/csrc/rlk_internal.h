@@ -24,21 +24,24 @@ constexpr int kBwdChunk = 16384;            // backward vocab chunk (multiple of
 constexpr int kRasterTokenTiles = 32;
 constexpr int kRasterHiddenTiles = 8;
 constexpr int kAuditThreads = 256;
-constexpr int kAuditPerThread = 16;         // 4 float4 of each input per thread
+constexpr int kAuditPerThread = 32;         // 8 float4 of each input per thread (loss fragment)
+constexpr int kAuditV3PerThread = 16;       // 4 float4 of each input per thread (audit)
 constexpr int kAuditBlockElems = kAuditThreads * kAuditPerThread;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Forward workspace: per (vocab chunk, row) partials {max s, sum 2^((s-max)k)},
 // then the target logit per row.
+// (With entropy, a third per (chunk, row) partial: sum 2^((s-max)k) s.)
 struct FwdLayout {
     int64_t num_chunks;
-    size_t partial_off, target_off, total;
+    size_t partial_off, partial_a_off, target_off, total;
     FwdLayout(int64_t N, int64_t V) {
         const int64_t vt = (V + kTileV - 1) / kTileV;
         num_chunks = (vt + kFwdTilesPerChunk - 1) / kFwdTilesPerChunk;
         partial_off = 0;
-        target_off = align_up(static_cast<size_t>(num_chunks) * N * 8, 256);
+        partial_a_off = align_up(static_cast<size_t>(num_chunks) * N * 8, 256);
+        target_off = align_up(partial_a_off + static_cast<size_t>(num_chunks) * N * 4, 256);
         total = align_up(target_off + static_cast<size_t>(N) * 4, 256);
     }
 };
@@ -65,15 +68,41 @@ struct AuditPartial {
     uint32_t flags;
 };
 
+struct LossPartial {
+    int64_t count;
+    int64_t clipped;
+    int64_t outside;
+    double sum_term;
+    double sum_r;
+};
+
 inline size_t audit_blocks(int64_t N) {
     return static_cast<size_t>((N + kAuditBlockElems - 1) / kAuditBlockElems);
+}
+
+inline size_t audit_v3_blocks(int64_t N) {
+    const int64_t b = kAuditThreads * kAuditV3PerThread;
+    return static_cast<size_t>((N + b - 1) / b);
 }
 
 // Launchers (return the first CUDA error, cudaSuccess otherwise).
 cudaError_t launch_fwd(const CUtensorMap& map_h, const CUtensorMap& map_w,
                        const int64_t* targets, const uint8_t* mask, int N, int H, int V,
-                       float k_log2e_over_t, float* logp, float* lse, void* workspace,
-                       uint32_t* err, int num_sms, cudaStream_t stream);
+                       float k_log2e_over_t, float* logp, float* lse, float* entropy,
+                       void* workspace, uint32_t* err, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_fwd_partials(const CUtensorMap& map_h, const CUtensorMap& map_w,
+                                const int64_t* targets, const uint8_t* mask, int N, int H,
+                                int V_local, int64_t vocab_start, float k, float2* partials,
+                                float* s_target, uint32_t* err, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_fwd_merge(const float2* partials, int num_chunks, const float* s_target,
+                             const int64_t* targets, const uint8_t* mask, int N, int V, float k,
+                             float* logp, float* lse, uint32_t* err, cudaStream_t stream);
+
+inline int64_t fwd_num_chunks(int64_t V) {
+    return ((V + kTileV - 1) / kTileV + kFwdTilesPerChunk - 1) / kFwdTilesPerChunk;
+}
 
 struct BwdMaps {
     CUtensorMap h_kmajor;      // hidden [N,H], box {64, 128}: A of the dS recompute
@@ -93,7 +122,8 @@ cudaError_t launch_target_sort(const int64_t* targets, const uint8_t* mask, int 
                                int* sorted_y, int* sorted_t, uint32_t* err, cudaStream_t stream);
 
 cudaError_t launch_bwd_chunk(const BwdMaps& maps, const ChunkMaps& cmaps, const int64_t* targets,
-                             const uint8_t* mask, const float* grad, const float* lse,
+                             const uint8_t* mask, const float* grad, const float* grad_ent,
+                             const float* ent, const float* lse,
                              const void* hidden, const void* weight, int N, int H, int V,
                              int chunk, int num_chunks, float k_log2e_over_t, float inv_t,
                              void* ds, float* dh_acc, const int* sorted_y, const int* sorted_t,
@@ -103,6 +133,16 @@ cudaError_t launch_bwd_chunk(const BwdMaps& maps, const ChunkMaps& cmaps, const 
 cudaError_t launch_audit(const float* logp_new, const float* logp_old, const uint8_t* mask,
                          int64_t N, rlk_audit_result_t* result, void* workspace, bool vec_ok,
                          cudaStream_t stream);
+
+cudaError_t launch_grpo_loss(const float* logp_new, const float* logp_old, const float* adv,
+                             const uint8_t* mask, int64_t N, double eps_low, double eps_high,
+                             double scale, float* grad, rlk_grpo_result_t* result,
+                             void* workspace, bool vec_ok, cudaStream_t stream);
+
+cudaError_t launch_logp_from_logits(const void* logits, bool bf16, int64_t stride, int64_t N, int V,
+                                    const int64_t* rows, int M, const int64_t* targets,
+                                    const uint8_t* mask, float k, bool vec_ok, float* logp,
+                                    float* lse, uint32_t* err, cudaStream_t stream);
 
 // Device address (current device) of the library-owned audit scratch.
 cudaError_t audit_noalloc_scratch(void** out);

@@ -40,10 +40,12 @@ def test_contract_and_status_strings(lib):
 
 
 def test_workspace_queries(lib):
-    # forward: 1024-column vocab chunks, (max, sum) float2 per chunk and row, plus a target logit
+    # forward: 1024-column vocab chunks, (max, sum) float2 and the entropy sum per chunk and
+    # row, plus a target logit
     n, v = 8192, 151936
     chunks = -(-(-(-v // 256)) // 4)
-    expect = -(-(chunks * n * 8) // 256) * 256 + -(-(n * 4) // 256) * 256
+    expect = (-(-(chunks * n * 8) // 256) * 256 + -(-(chunks * n * 4) // 256) * 256
+              + -(-(n * 4) // 256) * 256)
     assert rlk.rlk_linear_logp_fwd_workspace_bytes(n, 4096, v) == expect
     # backward: dS chunk [N, 16384] bf16 + fp32 dh accumulator + two int32 lists
     assert rlk.rlk_linear_logp_bwd_workspace_bytes(n, 4096, v) >= n * 16384 * 2 + n * 4096 * 4

@@ -37,7 +37,7 @@ def _check(r, o, new, old, mask):
     assert abs(r["approx_kl"] - o["approx_kl"]) <= 1e-6 * abs(o["approx_kl"]) + 1e-15
 
 
-@pytest.mark.parametrize("n", [1, 5, 4095, 4096, 4097, 100003])
+@pytest.mark.parametrize("n", [1, 5, 4095, 4096, 4097, 8191, 8192, 8193, 100003])
 def test_parity_random(n):
     new, old, mask = wl.audit_inputs(n, n)
     r, o = _both(new, old, mask)

@@ -1,0 +1,96 @@
+"""Entropy fused into the linear log-prob ("RL-Kernel Roadmap (2026)", backlog:
+fused entropy / entropy-bonus kernel; "RL-Kernel integration roadmap for vime",
+linear_logp: entropy requests).  Forward entropy within 1e-3 absolute of the
+oracle, logp / lse unchanged bit for bit by asking for the entropy, the
+backward of sum g logp + sum gH entropy within 2e-3 relative L2, and bitwise
+batch invariance of entropy and dhidden."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rl_post_linear_gb300 as rlk
+import workloads as wl
+from helpers import GRAD_REL_L2, LOGP_ATOL, dev, f64, rel_l2, same_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(n, h, v, seed, std=0.05):
+    hidden = wl.normal_bf16((n, h), seed, wl.S_HIDDEN)
+    weight = wl.normal_bf16((v, h), seed, wl.S_WEIGHT, std=std)
+    targets = wl.uniform_targets(n, v, seed)
+    g = np.random.default_rng(seed)
+    mask = torch.from_numpy((g.random(n) < 0.85).astype(np.uint8))
+    return hidden, weight, targets, mask, g
+
+
+@pytest.mark.parametrize("n,h,v,T,std", [(64, 128, 1000, 1.0, 0.02), (300, 256, 5000, 0.7, 0.2),
+                                         (70, 64, 16384 + 300, 1.5, 0.5)])
+def test_entropy_forward_parity(n, h, v, T, std):
+    hidden, weight, targets, mask, _ = _case(n, h, v, n + v, std)
+    d = dev()
+    hd, wd, yd, md = hidden.to(d), weight.to(d), targets.to(d), mask.to(d)
+    logp, lse, ent = rlk.linear_logp_entropy_fwd(hd, wd, yd, md, T)
+    logp0, lse0 = rlk.linear_logp_fwd(hd, wd, yd, md, T)
+    assert same_bits(logp.cpu(), logp0.cpu()) and same_bits(lse.cpu(), lse0.cpu())
+    lp_o, lse_o, ent_o = oracle.linear_logp_entropy_fwd_parallel(
+        f64(hidden), f64(weight), targets.numpy(), mask.numpy(), T)
+    act = mask.numpy() > 0
+    de = np.abs(ent.cpu().double().numpy() - ent_o)[act]
+    print("entropy fwd n=%d v=%d: max |dH| %.3e (H ~ %.2f)" % (n, v, de.max(), ent_o[act].mean()))
+    assert de.max() <= LOGP_ATOL
+    assert np.all(ent.cpu().numpy()[~act] == 0)
+
+
+@pytest.mark.parametrize("n,h,v,T", [(64, 128, 1000, 1.0), (150, 128, 20000, 0.7)])
+def test_entropy_backward_parity(n, h, v, T):
+    hidden, weight, targets, mask, g = _case(n, h, v, 7 + n, std=0.3)
+    grad = g.standard_normal(n) / n
+    grad_h = g.standard_normal(n) / n
+    grad[mask.numpy() == 0] = 0
+    grad_h[mask.numpy() == 0] = 0
+    d = dev()
+    hd, wd, yd, md = hidden.to(d), weight.to(d), targets.to(d), mask.to(d)
+    _, lse, ent = rlk.linear_logp_entropy_fwd(hd, wd, yd, md, T)
+    gd = torch.tensor(grad, dtype=torch.float32, device=d)
+    ghd = torch.tensor(grad_h, dtype=torch.float32, device=d)
+    dh, dw = rlk.linear_logp_entropy_bwd(hd, wd, yd, md, gd, ghd, lse, ent, T)
+    h64, w64 = f64(hidden), f64(weight)
+    _, lse_o, ent_o = oracle.linear_logp_entropy_fwd_parallel(h64, w64, targets.numpy(),
+                                                              mask.numpy(), T)
+    g32, gh32 = gd.cpu().double().numpy(), ghd.cpu().double().numpy()
+    dh_o = oracle.linear_logp_entropy_bwd_dh_parallel(h64, w64, targets.numpy(), mask.numpy(),
+                                                      g32, gh32, lse_o, ent_o, T)
+    dw_o = oracle.linear_logp_entropy_bwd_dw_parallel(h64, w64, targets.numpy(), mask.numpy(),
+                                                      g32, gh32, lse_o, ent_o, T)
+    e_dh, e_dw = rel_l2(dh.cpu(), dh_o), rel_l2(dw.cpu(), dw_o)
+    print("entropy bwd n=%d v=%d: rel-L2 dh %.3e dw %.3e" % (n, v, e_dh, e_dw))
+    assert e_dh <= GRAD_REL_L2 and e_dw <= GRAD_REL_L2
+    # gH = 0 gives the logp-only backward bit for bit
+    z = torch.zeros_like(ghd)
+    dh0, dw0 = rlk.linear_logp_entropy_bwd(hd, wd, yd, md, gd, z, lse, ent, T)
+    dh1, dw1 = rlk.linear_logp_bwd(hd, wd, yd, md, gd, lse, T)
+    assert same_bits(dh0.cpu(), dh1.cpu()) and same_bits(dw0.cpu(), dw1.cpu())
+
+
+def test_entropy_batch_invariance_and_autograd():
+    hidden, weight, targets, mask, g = _case(260, 256, 3000, 3)
+    d = dev()
+    hd, wd, yd, md = hidden.to(d), weight.to(d), targets.to(d), mask.to(d)
+    gd = torch.tensor(g.standard_normal(260) * 1e-2, dtype=torch.float32, device=d)
+    ghd = torch.tensor(g.standard_normal(260) * 1e-2, dtype=torch.float32, device=d)
+    _, lse, ent = rlk.linear_logp_entropy_fwd(hd, wd, yd, md, 0.7)
+    dh, _ = rlk.linear_logp_entropy_bwd(hd, wd, yd, md, gd, ghd, lse, ent, 0.7)
+    for a, b in ((0, 1), (100, 231), (37, 201)):
+        _, ls, en = rlk.linear_logp_entropy_fwd(hd[a:b], wd, yd[a:b], md[a:b], 0.7)
+        assert same_bits(en.cpu(), ent[a:b].cpu())
+        dhp, _ = rlk.linear_logp_entropy_bwd(hd[a:b], wd, yd[a:b], md[a:b], gd[a:b], ghd[a:b],
+                                             ls, en, 0.7)
+        assert same_bits(dhp.cpu(), dh[a:b].cpu())
+    # autograd wrapper: the gradient of (g . logp + gH . entropy) is the entropy backward's
+    hr = hd.clone().requires_grad_(True)
+    wr = wd.clone().requires_grad_(True)
+    lp, en = rlk.linear_logp_entropy(hr, wr, yd, md, 0.7)
+    ((lp * gd).sum() + (en * ghd).sum()).backward()
+    assert same_bits(hr.grad.cpu(), dh.cpu())

@@ -389,3 +389,182 @@ def test_golden_hand_example(oracle_lib):
                                                case["temperature"])
         np.testing.assert_allclose(logp, case["logp"], rtol=0, atol=1e-15)
         np.testing.assert_allclose(lse, case["lse"], rtol=0, atol=1e-15)
+
+
+def test_grpo_general_reduces_to_symmetric_token_mean(oracle_lib):
+    o = oracle_lib
+    rng = np.random.default_rng(14)
+    n = 300
+    logp = -rng.exponential(1.0, n)
+    old = logp + rng.normal(0, 0.2, n)
+    adv = rng.normal(0, 1, n)
+    mask = (rng.random(n) < 0.7).astype(np.uint8)
+    loss, g = o.grpo_clip_grad(logp, old, adv, mask, 0.2)
+    g2, res = o.grpo_clip(logp, old, adv, mask, 0.2, 0.2, 1.0 / int(mask.sum()))
+    assert np.allclose(g, g2, rtol=1e-15, atol=0) and abs(res["loss"] - loss) < 1e-15
+    # counts by direct enumeration
+    r = np.exp(logp - old)
+    act = mask > 0
+    outside = act & ((r < 0.8) | (r > 1.2))
+    assert res["active_count"] == act.sum() and res["outside_count"] == outside.sum()
+    zero_grad = act & (g2 == 0) & outside
+    assert res["clipped_count"] == zero_grad.sum()
+    assert abs(res["mean_ratio"] - r[act].mean()) < 1e-14
+
+
+def test_grpo_general_asymmetric_finite_differences(oracle_lib):
+    o = oracle_lib
+    rng = np.random.default_rng(15)
+    n = 50
+    logp = -rng.exponential(1.0, n)
+    old = logp + rng.normal(0, 0.2, n)
+    adv = rng.normal(0, 1, n)
+    mask = (rng.random(n) < 0.8).astype(np.uint8)
+    lo, hi, scale = 0.2, 0.28, 0.013
+    g, _ = o.grpo_clip(logp, old, adv, mask, lo, hi, scale)
+    step = 1e-7
+    for t in range(n):
+        r = math.exp(logp[t] - old[t])
+        if abs(r - (1 - lo)) < 1e-4 or abs(r - (1 + hi)) < 1e-4:
+            continue
+        up, dn = logp.copy(), logp.copy()
+        up[t] += step
+        dn[t] -= step
+        fd = (o.grpo_clip(up, old, adv, mask, lo, hi, scale)[1]["loss"]
+              - o.grpo_clip(dn, old, adv, mask, lo, hi, scale)[1]["loss"]) / (2 * step)
+        assert abs(fd - g[t]) < 1e-8, (t, fd, g[t])
+    # an asymmetric range: r = 1.25 is inside [0.8, 1.28] (no clip), outside [0.8, 1.2]
+    one = np.array([math.log(1.25)])
+    g_in, res_in = o.grpo_clip(one, np.zeros(1), np.ones(1), None, 0.2, 0.28, 1.0)
+    g_out, res_out = o.grpo_clip(one, np.zeros(1), np.ones(1), None, 0.2, 0.2, 1.0)
+    assert g_in[0] == -1.25 and res_in["outside_count"] == 0
+    assert g_out[0] == 0.0 and res_out["clipped_count"] == 1 and abs(res_out["loss"] + 1.2) < 1e-15
+
+
+# ----------------------------------------------------------------------------- logp from logits
+
+def test_logits_closed_forms(oracle_lib):
+    o = oracle_lib
+    # equal logits -> -log V; two entries -> log-sigmoid of the gap; the hand example
+    z = np.zeros((3, 37))
+    logp, lse = o.logp_from_logits(z + 5.0, [0, 7, 36], None, 0.7)
+    np.testing.assert_allclose(logp, -math.log(37), rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse, 5.0 / 0.7 + math.log(37), rtol=0, atol=1e-13)
+    z2 = np.array([[0.3, -1.1], [2.0, 2.5]])
+    logp, _ = o.logp_from_logits(z2, [1, 0], None, 0.5)
+    for i, (a, b) in enumerate(z2):
+        mine, other = (b, a) if i == 0 else (a, b)
+        assert abs(logp[i] + math.log1p(math.exp((other - mine) / 0.5))) < 1e-14
+    ex = np.array([[1.0, 0.0, -1.0]])
+    logp, lse = o.logp_from_logits(ex, [0], None, 1.0)
+    assert abs(lse[0] - math.log(math.e + 1 + math.exp(-1))) < 1e-15
+
+
+def test_logits_brute_force_and_normalisation(oracle_lib):
+    getcontext().prec = 60
+    o = oracle_lib
+    rng = np.random.default_rng(20)
+    z = rng.standard_normal((4, 13)) * 3
+    y = rng.integers(0, 13, 4)
+    logp, _ = o.logp_from_logits(z, y, None, 0.7)
+    for t in range(4):
+        d = [Decimal(float(v)) / Decimal(0.7) for v in z[t]]
+        tot = sum((x.exp() for x in d), Decimal(0))
+        assert abs(float(d[y[t]] - tot.ln()) - logp[t]) < 1e-13
+    allv, _ = o.logp_from_logits(np.repeat(z[:1], 13, axis=0), np.arange(13), None, 1.3)
+    assert abs(math.fsum(np.exp(allv)) - 1.0) < 1e-13
+
+
+def test_logits_indexed_rows_and_mask(oracle_lib):
+    o = oracle_lib
+    rng = np.random.default_rng(21)
+    z = rng.standard_normal((10, 50))
+    y = rng.integers(0, 50, 10)
+    mask = np.array([1, 1, 0, 1, 1, 1, 1, 0, 1, 1], np.uint8)
+    dense, dlse = o.logp_from_logits(z, y, mask, 0.9)
+    rows = np.array([9, 2, 4, 4, 0])
+    idx, ilse = o.logp_from_logits(z, y, mask, 0.9, rows=rows)
+    assert np.array_equal(idx, dense[rows]) and np.array_equal(ilse, dlse[rows])
+    assert dense[2] == 0.0 and dense[7] == 0.0
+    y2 = y.copy()
+    y2[3] = 50
+    bad, _ = o.logp_from_logits(z, y2, mask, 0.9)
+    assert math.isnan(bad[3])
+
+
+# ----------------------------------------------------------------------------- entropy
+
+def test_entropy_closed_forms(oracle_lib):
+    o = oracle_lib
+    rng = np.random.default_rng(30)
+    h = _bf16_grid(rng, (4, 16), 1.0)
+    # W = 0: uniform softmax, entropy = log V; V = 1: entropy 0
+    _, _, ent = o.linear_logp_entropy_fwd(h, np.zeros((50, 16)), [0, 1, 2, 3], None, 0.7)
+    np.testing.assert_allclose(ent, math.log(50), rtol=0, atol=1e-13)
+    _, _, ent1 = o.linear_logp_entropy_fwd(h, _bf16_grid(rng, (1, 16), 1.0), [0] * 4, None, 0.7)
+    assert np.all(np.abs(ent1) < 1e-15)
+    # V = 2: binary entropy of sigmoid(gap)
+    w2 = _bf16_grid(rng, (2, 16), 0.4)
+    lp, _, ent2 = o.linear_logp_entropy_fwd(h, w2, [0] * 4, None, 1.3)
+    p0 = np.exp(lp)
+    np.testing.assert_allclose(ent2, -(p0 * np.log(p0) + (1 - p0) * np.log1p(-p0)), rtol=1e-12)
+    # logp and lse agree with the logp-only forward
+    w = _bf16_grid(rng, (40, 16), 0.5)
+    y = rng.integers(0, 40, 4)
+    a, b, _ = o.linear_logp_entropy_fwd(h, w, y, None, 0.9)
+    c, d = o.linear_logp_fwd(h, w, y, None, 0.9)
+    assert np.array_equal(a, c) and np.array_equal(b, d)
+
+
+def test_entropy_brute_force(oracle_lib):
+    getcontext().prec = 60
+    o = oracle_lib
+    rng = np.random.default_rng(31)
+    h = _bf16_grid(rng, (3, 10), 2.0)
+    w = _bf16_grid(rng, (9, 10), 1.0)
+    _, _, ent = o.linear_logp_entropy_fwd(h, w, [0, 1, 2], None, 0.7)
+    for t in range(3):
+        z = []
+        for v in range(9):
+            q = sum(Fraction(a) * Fraction(b) for a, b in zip(h[t], w[v])) / Fraction(0.7)
+            z.append(Decimal(q.numerator) / Decimal(q.denominator))
+        tot = sum((x.exp() for x in z), Decimal(0))
+        expect = -sum(((x.exp() / tot) * (x - tot.ln()) for x in z), Decimal(0))
+        assert abs(float(expect) - ent[t]) < 1e-13
+
+
+@pytest.mark.parametrize("shape", [(2, 3, 4), (3, 6, 5)])
+def test_entropy_backward_finite_differences(oracle_lib, shape):
+    o = oracle_lib
+    n, hdim, vocab = shape
+    rng = np.random.default_rng(40 + n)
+    h = rng.standard_normal((n, hdim))
+    w = rng.standard_normal((vocab, hdim)) * 0.7
+    y = rng.integers(0, vocab, n)
+    mask = np.ones(n, np.uint8)
+    mask[-1] = 0 if n > 2 else 1
+    g, gh = rng.standard_normal(n), rng.standard_normal(n)
+    T = 0.8
+
+    def loss():
+        lp, _, ent = o.linear_logp_entropy_fwd(h, w, y, mask, T)
+        return float(np.dot(g, lp) + np.dot(gh, ent))
+
+    _, lse, ent = o.linear_logp_entropy_fwd(h, w, y, mask, T)
+    dh = o.linear_logp_entropy_bwd_dh(h, w, y, mask, g, gh, lse, ent, T)
+    dw = o.linear_logp_entropy_bwd_dw(h, w, y, mask, g, gh, lse, ent, T)
+    step = 1e-6
+    for arr, grad in ((h, dh), (w, dw)):
+        for idx in np.ndindex(arr.shape):
+            keep = arr[idx]
+            arr[idx] = keep + step
+            up = loss()
+            arr[idx] = keep - step
+            dn = loss()
+            arr[idx] = keep
+            fd = (up - dn) / (2 * step)
+            assert abs(fd - grad[idx]) <= 1e-7 * max(1.0, abs(fd)), (idx, fd, grad[idx])
+    # gH = 0 reduces to the logp-only backward
+    z = np.zeros(n)
+    assert np.allclose(o.linear_logp_entropy_bwd_dw(h, w, y, mask, g, z, lse, ent, T),
+                       o.linear_logp_bwd_dw(h, w, y, mask, g, lse, T), rtol=1e-14, atol=1e-15)
