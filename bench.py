@@ -319,9 +319,42 @@ def run_ours(args, world, rank, local):
     }
     out["audit_hbm"] = {str(na): measure_audit(rlk, dev, na, pk["hbm_gbs"])
                         for na in (9_400_614, 1 << 26)}
+    if not args.no_second_shape:
+        del hid, wt, dh, dw, ws_b
+        torch.cuda.empty_cache()
+        out["deepseek_fwd"] = measure_deepseek_fwd(rlk, dev, peak, args.warmup, args.steps)
     if not args.no_cpu_baseline and world == 1:
         out["cpu_baseline"] = cpu_baseline(w, noise, adv, args.cpu_tokens)
     return out
+
+
+def measure_deepseek_fwd(rlk, dev, peak, warmup, steps):
+    """The second workload of the pages' shapes: the DeepSeek-style LM head forward
+    (N = 16384, H = 7168, V = 129280, 20% of tokens masked, T = 1); W (1.85 GB) exceeds L2.
+    TFLOP/s counts the active tokens' work, 2 N_a H V."""
+    w = wl.deepseek_fwd(0)
+    hid, wt = w.hidden.to(dev), w.weight.to(dev)
+    y, mask = w.targets.to(dev), w.mask.to(dev)
+    logp = torch.empty(w.n, dtype=torch.float32, device=dev)
+    lse = torch.empty_like(logp)
+    ws = torch.empty(rlk.rlk_linear_logp_fwd_workspace_bytes(w.n, w.h, w.v), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        rlk.rlk_linear_logp_fwd(hid, wt, y, mask, w.temperature, logp, lse, ws)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(steps):
+        rlk.rlk_linear_logp_fwd(hid, wt, y, mask, w.temperature, logp, lse, ws)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    act = 2.0 * w.n_active * w.h * w.v / (ms * 1e-3) / 1e12
+    allr = 2.0 * w.n * w.h * w.v / (ms * 1e-3) / 1e12
+    return {"workload": w.name, "n_active": w.n_active, "ms": ms,
+            "tokens_per_s": w.n_active / (ms * 1e-3), "tflops_active": act,
+            "frac_of_peak_active": act / peak, "tflops_all_rows": allr}
 
 
 def measure_audit(rlk, dev, n, hbm_gbs, reps=10):
@@ -467,6 +500,8 @@ def main():
     ap.add_argument("--tokens", type=int, default=wl.QWEN_N)
     ap.add_argument("--cpu-tokens", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-second-shape", action="store_true",
+                    help="leave out the DeepSeek-shaped forward measurement")
     args = ap.parse_args()
     world, rank, local = dist_env()
     if world > 1 and args.impl == "ours":

@@ -86,11 +86,31 @@ typedef struct {
     double mean_ratio;      /* sum_active r / active_count   (NaN when none is active) */
 } rlk_grpo_result_t;
 
+/* Result of rlk_dlogp_audit_ext, written to device memory (all over active tokens). */
+typedef struct {
+    int64_t active_count;
+    int64_t argmax_index;    /* worst token (lowest index on ties); -1 if none is active */
+    int64_t argmax_seq;      /* its sequence per seq_offsets; -1 without offsets */
+    int64_t argmax_pos;      /* its position inside that sequence; -1 without offsets */
+    int64_t clip_count;      /* #{|exp(d) - 1| > clip_eps} */
+    double mean_dlogp;       /* mean d */
+    double mean_abs_dlogp;   /* mean |d| */
+    double mean_ratio;       /* mean ratio0 = mean exp(d) */
+    double approx_kl;        /* mean (exp(d) - 1 - d) */
+    float max_abs_dlogp;     /* max |d| */
+    float p50_abs_dlogp;     /* nearest-rank percentiles of |d|: the value at 1-based rank */
+    float p90_abs_dlogp;     /*   ceil(p * count) of the ascending order; exact (radix select) */
+    float p99_abs_dlogp;
+    float clipfrac;          /* clipfrac0 = clip_count / active_count */
+    uint32_t error_flags;    /* bit 0: an active d was not finite */
+} rlk_audit_ext_t;
+
 /* Scratch bytes each entry point needs for these sizes (pure arithmetic, no CUDA call). */
 size_t rlk_linear_logp_fwd_workspace_bytes(int64_t N, int64_t H, int64_t V);
 size_t rlk_linear_logp_bwd_workspace_bytes(int64_t N, int64_t H, int64_t V);
 size_t rlk_dlogp_audit_workspace_bytes(int64_t N);
 size_t rlk_grpo_clip_loss_workspace_bytes(int64_t N);
+size_t rlk_dlogp_audit_ext_workspace_bytes(int64_t N);
 
 /*
  * Forward.  "RL-Kernel Roadmap (2026)" P0.2; "RL-Kernel integration roadmap
@@ -285,6 +305,27 @@ rlk_status_t rlk_grpo_clip_loss(const float* logp_new, const float* logp_old,
                                 double eps_low, double eps_high, double loss_scale,
                                 float* grad_out, rlk_grpo_result_t* result_dev,
                                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * The consistency contract's minimum diagnostics ("RL-Kernel integration
+ * roadmap for vime", Consistency Contract): abs_dlogp mean, max, p50, p90,
+ * p99; ratio0 = exp(dlogp); clipfrac0; approx_kl0; active token count; and the
+ * worst token's location.  Over active tokens only.
+ *
+ *   seq_offsets  device int64 [num_seqs + 1] (sequence s holds tokens
+ *                [seq_offsets[s], seq_offsets[s+1])), or NULL
+ *   clip_eps     >= 0, finite: the ratio0 clip range of clipfrac0
+ *   result_dev   one rlk_audit_ext_t in device memory
+ * The sums follow rlk_dlogp_audit's fixed blocks and trees; the percentiles
+ * are exact order statistics selected with integer histograms, so the whole
+ * result is bitwise reproducible for a given N.  ratio0 and the clip test
+ * are evaluated in fp32.
+ */
+rlk_status_t rlk_dlogp_audit_ext(const float* logp_new, const float* logp_old,
+                                 const uint8_t* active_mask, int64_t N,
+                                 const int64_t* seq_offsets, int64_t num_seqs, double clip_eps,
+                                 rlk_audit_ext_t* result_dev, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * Masked dlogp audit that allocates nothing.  The source pages have no

@@ -47,6 +47,14 @@ class GrpoResult(ctypes.Structure):
     ]
 
 
+class AuditExtResult(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("active_count", "argmax_index", "argmax_seq",
+                                               "argmax_pos", "clip_count")] + \
+               [(n, ctypes.c_double) for n in ("mean_dlogp", "mean_abs_dlogp", "mean_ratio",
+                                                "approx_kl", "max_abs_dlogp", "p50_abs_dlogp",
+                                                "p90_abs_dlogp", "p99_abs_dlogp", "clipfrac")]
+
+
 class AuditResult(ctypes.Structure):
     _fields_ = [
         ("active_count", ctypes.c_int64),
@@ -104,6 +112,10 @@ def _load():
                 f.argtypes = [_dp, _dp, _i64p, _u8p, _dp, _dp, _dp, _dp, ctypes.c_int64,
                               ctypes.c_int64, ctypes.c_int64, ctypes.c_double, ctypes.c_int64,
                               ctypes.c_int64, _dp]
+            lib.rlk_oracle_dlogp_audit_ext.restype = ctypes.c_int
+            lib.rlk_oracle_dlogp_audit_ext.argtypes = [_fp, _fp, _u8p, ctypes.c_int64, _i64p,
+                                                       ctypes.c_int64, ctypes.c_double,
+                                                       ctypes.POINTER(AuditExtResult)]
             lib.rlk_oracle_grpo_clip_grad.restype = ctypes.c_double
             lib.rlk_oracle_grpo_clip_grad.argtypes = [_dp, _dp, _dp, _u8p, ctypes.c_int64,
                                                       ctypes.c_double, _dp]
@@ -439,3 +451,19 @@ def linear_logp_entropy_bwd_dw_parallel(h, w, y, mask, g, gh, lse, ent, temperat
 
     _split_parallel(w.shape[0], fn, threads)
     return out
+
+
+def dlogp_audit_ext(logp_new, logp_old, mask, seq_offsets=None, eps=0.2):
+    """The minimum diagnostics of the consistency contract (dict)."""
+    lib = _load()
+    a = _c(logp_new, np.float32)
+    b = _c(logp_old, np.float32)
+    n = a.shape[0]
+    m = _mask_arg(mask, n)
+    off = None if seq_offsets is None else _c(seq_offsets, np.int64)
+    res = AuditExtResult()
+    if lib.rlk_oracle_dlogp_audit_ext(_ptr(a, _fp), _ptr(b, _fp), _ptr(m, _u8p), n,
+                                      _ptr(off, _i64p), 0 if off is None else off.shape[0] - 1,
+                                      float(eps), ctypes.byref(res)) != 0:
+        raise MemoryError("oracle audit: scratch allocation failed")
+    return {f: getattr(res, f) for f, _ in AuditExtResult._fields_}

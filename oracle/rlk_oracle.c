@@ -432,3 +432,92 @@ void rlk_oracle_linear_logp_entropy_bwd_dw(const double* h, const double* w,
         }
     }
 }
+
+typedef struct {
+    int64_t active_count;
+    int64_t argmax_index;
+    int64_t argmax_seq;
+    int64_t argmax_pos;
+    int64_t clip_count;
+    double mean_dlogp;
+    double mean_abs_dlogp;
+    double mean_ratio;
+    double approx_kl;
+    double max_abs_dlogp;
+    double p50_abs_dlogp;
+    double p90_abs_dlogp;
+    double p99_abs_dlogp;
+    double clipfrac;
+} rlk_oracle_audit_ext_t;
+
+static int cmp_abs(const void* a, const void* b) {
+    double x = *(const double*)a, y = *(const double*)b;
+    int nx = isnan(x), ny = isnan(y);
+    if (nx || ny) return nx - ny;          /* NaN sorts above every number */
+    return (x > y) - (x < y);
+}
+
+/* nearest rank: the value at 1-based rank ceil(p * count) of the ascending order */
+static double nearest_rank(const double* sorted, int64_t count, int64_t num, int64_t den) {
+    if (count == 0) return NAN;
+    int64_t rank = (num * count + den - 1) / den;
+    if (rank < 1) rank = 1;
+    return sorted[rank - 1];
+}
+
+/*
+ * The Consistency Contract's minimum diagnostics ("RL-Kernel integration
+ * roadmap for vime"): over active tokens, with d = new - old,
+ *   mean d, mean |d|, max |d| (first index), p50 / p90 / p99 of |d| (nearest
+ *   rank), mean ratio0 = mean exp(d), approx_kl0 = mean(exp(d) - 1 - d),
+ *   clip count = #{|exp(d) - 1| > eps} and clipfrac0 = clip count / count,
+ *   and the worst token's sequence and position, from seq_offsets[0..num_seqs]
+ *   (sequence s holds tokens [seq_offsets[s], seq_offsets[s+1])) when given.
+ * Ties and NaN as in rlk_oracle_dlogp_audit.  Returns -1 if the scratch array
+ * cannot be allocated.
+ */
+int rlk_oracle_dlogp_audit_ext(const float* logp_new, const float* logp_old, const uint8_t* mask,
+                               int64_t n, const int64_t* seq_offsets, int64_t num_seqs,
+                               double eps, rlk_oracle_audit_ext_t* out) {
+    double* absd = (double*)malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
+    if (absd == NULL) return -1;
+    rlk_oracle_audit_t base;
+    rlk_oracle_dlogp_audit(logp_new, logp_old, mask, n, &base);
+    int64_t count = 0, clip = 0;
+    double sum_abs = 0.0, sum_ratio = 0.0;
+    for (int64_t t = 0; t < n; ++t) {
+        if (!row_active(mask, t)) continue;
+        double d = (double)logp_new[t] - (double)logp_old[t];
+        double r = exp(d);
+        absd[count++] = fabs(d);
+        sum_abs += fabs(d);
+        sum_ratio += r;
+        if (fabs(r - 1.0) > eps) ++clip;
+    }
+    qsort(absd, (size_t)count, sizeof(double), cmp_abs);
+    out->active_count = count;
+    out->argmax_index = base.argmax_index;
+    out->argmax_seq = -1;
+    out->argmax_pos = -1;
+    if (seq_offsets != NULL && base.argmax_index >= 0) {
+        for (int64_t s = 0; s < num_seqs; ++s) {
+            if (base.argmax_index >= seq_offsets[s] && base.argmax_index < seq_offsets[s + 1]) {
+                out->argmax_seq = s;
+                out->argmax_pos = base.argmax_index - seq_offsets[s];
+                break;
+            }
+        }
+    }
+    out->clip_count = clip;
+    out->mean_dlogp = base.mean_dlogp;
+    out->mean_abs_dlogp = sum_abs / (double)count;
+    out->mean_ratio = sum_ratio / (double)count;
+    out->approx_kl = base.approx_kl;
+    out->max_abs_dlogp = base.max_abs_dlogp;
+    out->p50_abs_dlogp = nearest_rank(absd, count, 50, 100);
+    out->p90_abs_dlogp = nearest_rank(absd, count, 90, 100);
+    out->p99_abs_dlogp = nearest_rank(absd, count, 99, 100);
+    out->clipfrac = (double)clip / (double)count;
+    free(absd);
+    return 0;
+}

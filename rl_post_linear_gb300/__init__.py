@@ -58,6 +58,20 @@ class AuditResult(ctypes.Structure):
 AUDIT_RESULT_BYTES = ctypes.sizeof(AuditResult)
 
 
+class AuditExtResult(ctypes.Structure):
+    """Mirror of rlk_audit_ext_t."""
+    _fields_ = [(n, ctypes.c_int64) for n in ("active_count", "argmax_index", "argmax_seq",
+                                               "argmax_pos", "clip_count")] + \
+               [(n, ctypes.c_double) for n in ("mean_dlogp", "mean_abs_dlogp", "mean_ratio",
+                                                "approx_kl")] + \
+               [(n, ctypes.c_float) for n in ("max_abs_dlogp", "p50_abs_dlogp", "p90_abs_dlogp",
+                                               "p99_abs_dlogp", "clipfrac")] + \
+               [("error_flags", ctypes.c_uint32)]
+
+
+AUDIT_EXT_RESULT_BYTES = ctypes.sizeof(AuditExtResult)
+
+
 class GrpoResult(ctypes.Structure):
     """Mirror of rlk_grpo_result_t."""
     _fields_ = [
@@ -119,6 +133,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.rlk_grpo_clip_loss.restype = ctypes.c_int
     lib.rlk_grpo_clip_loss.argtypes = [_vp, _vp, _vp, _vp, _i64, ctypes.c_double, ctypes.c_double,
                                        ctypes.c_double, _vp, _vp, _vp, _sz, _vp]
+    lib.rlk_dlogp_audit_ext_workspace_bytes.restype = _sz
+    lib.rlk_dlogp_audit_ext_workspace_bytes.argtypes = [_i64]
+    lib.rlk_dlogp_audit_ext.restype = ctypes.c_int
+    lib.rlk_dlogp_audit_ext.argtypes = [_vp, _vp, _vp, _i64, _vp, _i64, ctypes.c_double, _vp,
+                                        _vp, _sz, _vp]
     lib.rlk_dlogp_audit_noalloc.restype = ctypes.c_int
     lib.rlk_dlogp_audit_noalloc.argtypes = [_vp, _vp, _vp, _i64, _vp, _vp]
     lib.rlk_contract_string.restype = ctypes.c_char_p
@@ -158,6 +177,10 @@ def rlk_dlogp_audit_workspace_bytes(N: int) -> int:
 
 def rlk_linear_logp_num_partials(V_local: int) -> int:
     return int(load().rlk_linear_logp_num_partials(V_local))
+
+
+def rlk_dlogp_audit_ext_workspace_bytes(N: int) -> int:
+    return int(load().rlk_dlogp_audit_ext_workspace_bytes(N))
 
 
 def rlk_grpo_clip_loss_workspace_bytes(N: int) -> int:
@@ -299,6 +322,27 @@ def rlk_dlogp_audit(logp_new, logp_old, active_mask, result, workspace, stream=N
     st = load().rlk_dlogp_audit(_ptr(logp_new), _ptr(logp_old), _ptr(active_mask), n,
                                 _ptr(result), _ptr(workspace), workspace.numel(), _stream(stream))
     _check("rlk_dlogp_audit", st)
+
+
+def rlk_dlogp_audit_ext(logp_new, logp_old, active_mask, seq_offsets, clip_eps, result,
+                        workspace, stream=None):
+    """Extended diagnostics; ``result`` is a uint8 CUDA tensor of AUDIT_EXT_RESULT_BYTES bytes,
+    ``seq_offsets`` an int64 CUDA tensor [num_seqs + 1] or None.  See include/rlk.h."""
+    n = logp_new.shape[0]
+    _need(logp_new, torch.float32, "logp_new", (n,))
+    _need(logp_old, torch.float32, "logp_old", (n,))
+    if active_mask is not None:
+        _need(active_mask, torch.uint8, "active_mask", (n,))
+    num_seqs = 0
+    if seq_offsets is not None:
+        _need(seq_offsets, torch.int64, "seq_offsets")
+        num_seqs = seq_offsets.numel() - 1
+    _need(result, torch.uint8, "result", (AUDIT_EXT_RESULT_BYTES,))
+    _need(workspace, torch.uint8, "workspace")
+    st = load().rlk_dlogp_audit_ext(_ptr(logp_new), _ptr(logp_old), _ptr(active_mask), n,
+                                    _ptr(seq_offsets), num_seqs, float(clip_eps), _ptr(result),
+                                    _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("rlk_dlogp_audit_ext", st)
 
 
 def rlk_dlogp_audit_noalloc(logp_new, logp_old, active_mask, result, stream=None):
@@ -499,6 +543,16 @@ def logp_from_logits(logits, targets, active_mask=None, temperature=1.0, rows=No
     lse = torch.empty(m, dtype=torch.float32, device=logits.device)
     rlk_logp_from_logits(logits, rows, targets, active_mask, temperature, logp, lse, error_word)
     return logp, lse
+
+
+def dlogp_audit_ext(logp_new, logp_old, active_mask=None, seq_offsets=None, clip_eps=0.2):
+    """Extended diagnostics dict (synchronises to read the result back)."""
+    n = logp_new.shape[0]
+    res = torch.empty(AUDIT_EXT_RESULT_BYTES, dtype=torch.uint8, device=logp_new.device)
+    ws = _workspace(rlk_dlogp_audit_ext_workspace_bytes(n), logp_new.device)
+    rlk_dlogp_audit_ext(logp_new, logp_old, active_mask, seq_offsets, clip_eps, res, ws)
+    r = AuditExtResult.from_buffer_copy(bytes(res.cpu().numpy().tobytes()))
+    return {f: getattr(r, f) for f, _ in AuditExtResult._fields_}
 
 
 class LinearLogp(torch.autograd.Function):

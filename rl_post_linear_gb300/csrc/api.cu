@@ -368,6 +368,35 @@ rlk_status_t rlk_grpo_clip_loss(const float* logp_new, const float* logp_old,
     return RLK_OK;
 }
 
+size_t rlk_dlogp_audit_ext_workspace_bytes(int64_t N) {
+    if (N < 0) return 0;
+    return rlk::audit_ext_workspace(N);
+}
+
+rlk_status_t rlk_dlogp_audit_ext(const float* logp_new, const float* logp_old,
+                                 const uint8_t* active_mask, int64_t N,
+                                 const int64_t* seq_offsets, int64_t num_seqs, double clip_eps,
+                                 rlk_audit_ext_t* result_dev, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t stream) {
+    if (N < 0 || N > (int64_t(1) << 40)) return RLK_ERR_INVALID_VALUE;
+    if (result_dev == nullptr) return RLK_ERR_INVALID_VALUE;
+    if (N > 0 && (logp_new == nullptr || logp_old == nullptr)) return RLK_ERR_INVALID_VALUE;
+    if (!(std::isfinite(clip_eps) && clip_eps >= 0.0)) return RLK_ERR_INVALID_VALUE;
+    if (seq_offsets != nullptr && num_seqs < 1) return RLK_ERR_INVALID_VALUE;
+    if (workspace == nullptr || !aligned(workspace, 256) ||
+        workspace_bytes < rlk_dlogp_audit_ext_workspace_bytes(N))
+        return RLK_ERR_WORKSPACE;
+    DeviceInfo dev;
+    RLK_TRY(current_device(dev));
+    const bool vec_ok = aligned(logp_new, 16) && aligned(logp_old, 16) &&
+                        (active_mask == nullptr || aligned(active_mask, 4));
+    RLK_CUDA(rlk::launch_audit_ext(logp_new, logp_old, active_mask, N, seq_offsets,
+                                   seq_offsets == nullptr ? 0 : num_seqs,
+                                   static_cast<float>(clip_eps), result_dev, workspace, vec_ok,
+                                   stream));
+    return RLK_OK;
+}
+
 rlk_status_t rlk_dlogp_audit_noalloc(const float* logp_new, const float* logp_old,
                                      const uint8_t* active_mask, int64_t N,
                                      rlk_audit_result_t* result_dev, cudaStream_t stream) {

@@ -274,6 +274,307 @@ __global__ void __launch_bounds__(kMergeThreads)
     }
 }
 
+// ----------------------------------------------------------------------------- extended audit
+//
+// The consistency contract's minimum diagnostics beyond the base audit: mean
+// |d|, mean ratio0 = exp(d), clipfrac0 = #{|exp(d) - 1| > eps} / count, the
+// p50 / p90 / p99 of |d| by the nearest-rank rule (1-based rank
+// ceil(p * count) of the ascending order), and the worst token's sequence and
+// position.  Pass 1 is the base pass plus three more per-thread sums; the
+// percentiles are selected exactly by a three-pass radix select over the
+// order-preserving 32-bit key of |d| (digits of 11, 11 and 10 bits), with
+// integer histograms: the counts, hence the selected values, are exact and
+// reproducible however the atomics interleave.
+
+struct ExtPartial {
+    AuditPartial base;
+    double sum_abs, sum_ratio;
+    int64_t clip;
+};
+
+struct SelectState {
+    uint32_t prefix[3];
+    uint32_t pad;
+    int64_t rank[3];
+};
+
+constexpr int kHistBins = 2048;
+
+template <bool VEC>
+__global__ void __launch_bounds__(kAuditThreads)
+    audit_ext_pass1(const float* __restrict__ nw, const float* __restrict__ od,
+                    const uint8_t* __restrict__ mask, int64_t N, float eps,
+                    ExtPartial* __restrict__ out) {
+    constexpr int kBlock = kAuditThreads * kAuditV3PerThread;
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * kBlock;
+    ThreadAcc a;
+    float sabs = 0.f, sratio = 0.f;
+    int clip = 0;
+#pragma unroll 1
+    for (int j = 0; j < kAuditV3PerThread / 4; ++j) {
+        const int o0 = j * (kAuditThreads * 4) + threadIdx.x * 4;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
+        uint32_t m = 0x01010101u;
+        const bool full = VEC && base + o0 + 4 <= N;
+        if (full) {
+            x = __ldcs(reinterpret_cast<const float4*>(nw + base + o0));
+            y = __ldcs(reinterpret_cast<const float4*>(od + base + o0));
+            if (mask != nullptr)
+                m = __ldcs(reinterpret_cast<const unsigned int*>(mask + base + o0));
+        }
+        const float xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int64_t i = base + o0 + e;
+            float nv, ov;
+            uint32_t mv;
+            if (full) {
+                nv = xs[e];
+                ov = ys[e];
+                mv = (m >> (8 * e)) & 0xffu;
+            } else {
+                if (i >= N) continue;
+                nv = nw[i];
+                ov = od[i];
+                mv = mask == nullptr ? 1u : mask[i];
+            }
+            if (mv == 0) continue;
+            visit3(nv, ov, 1u, o0 + e, a);
+            const float d = nv - ov;
+            const float r = expf(d);
+            sabs += fabsf(d);
+            sratio += r;
+            clip += fabsf(r - 1.0f) > eps ? 1 : 0;
+        }
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const int c = __shfl_down_sync(0xffffffffu, a.count, off);
+        const uint32_t k = __shfl_down_sync(0xffffffffu, a.key, off);
+        const int g = __shfl_down_sync(0xffffffffu, a.arg, off);
+        const float sd = __shfl_down_sync(0xffffffffu, a.sd, off);
+        const float skl = __shfl_down_sync(0xffffffffu, a.skl, off);
+        const uint32_t f = __shfl_down_sync(0xffffffffu, a.flags, off);
+        const float sa = __shfl_down_sync(0xffffffffu, sabs, off);
+        const float sr = __shfl_down_sync(0xffffffffu, sratio, off);
+        const int cl = __shfl_down_sync(0xffffffffu, clip, off);
+        if (lane + off < 32) {
+            const bool take = k > a.key || (k == a.key && k != 0 && g < a.arg);
+            a.key = take ? k : a.key;
+            a.arg = take ? g : a.arg;
+            a.count += c;
+            a.sd += sd;
+            a.skl += skl;
+            a.flags |= f;
+            sabs += sa;
+            sratio += sr;
+            clip += cl;
+        }
+    }
+    __shared__ Acc warp_acc[kAuditThreads / 32];
+    __shared__ double warp_abs[kAuditThreads / 32], warp_ratio[kAuditThreads / 32];
+    __shared__ int warp_clip[kAuditThreads / 32];
+    if (lane == 0) {
+        Acc w;
+        w.count = a.count;
+        w.arg = a.key == 0 ? INT64_MAX : base + a.arg;
+        w.sum_d = static_cast<double>(a.sd);
+        w.sum_kl = static_cast<double>(a.skl);
+        w.best = a.key == 0 ? -1.0f : __uint_as_float(a.key - 1u);
+        w.flags = a.flags;
+        warp_acc[warp] = w;
+        warp_abs[warp] = static_cast<double>(sabs);
+        warp_ratio[warp] = static_cast<double>(sratio);
+        warp_clip[warp] = clip;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        Acc t = warp_acc[0];
+        double sa = warp_abs[0], sr = warp_ratio[0];
+        int64_t cl = warp_clip[0];
+#pragma unroll
+        for (int w = 1; w < kAuditThreads / 32; ++w) {
+            merge(t, warp_acc[w]);
+            sa += warp_abs[w];
+            sr += warp_ratio[w];
+            cl += warp_clip[w];
+        }
+        ExtPartial p;
+        p.base.count = t.count;
+        p.base.arg = t.arg;
+        p.base.sum_d = t.sum_d;
+        p.base.sum_kl = t.sum_kl;
+        p.base.best = t.best;
+        p.base.flags = t.flags;
+        p.sum_abs = sa;
+        p.sum_ratio = sr;
+        p.clip = cl;
+        out[blockIdx.x] = p;
+    }
+}
+
+// One block: fixed-order merge of the partials; writes the sums into the
+// result, the nearest ranks into the select state, clears the histograms.
+__global__ void __launch_bounds__(kMergeThreads)
+    audit_ext_merge(const ExtPartial* __restrict__ parts, int64_t num_parts,
+                    const int64_t* __restrict__ seq_offsets, int64_t num_seqs,
+                    rlk_audit_ext_t* __restrict__ result, SelectState* __restrict__ sel,
+                    uint32_t* __restrict__ hist) {
+    Acc a = empty_acc();
+    double sa = 0.0, sr = 0.0;
+    int64_t cl = 0;
+    for (int64_t i = threadIdx.x; i < num_parts; i += kMergeThreads) {
+        const ExtPartial p = parts[i];
+        Acc b;
+        b.count = p.base.count;
+        b.arg = p.base.arg;
+        b.sum_d = p.base.sum_d;
+        b.sum_kl = p.base.sum_kl;
+        b.best = p.base.best;
+        b.flags = p.base.flags;
+        merge(a, b);
+        sa += p.sum_abs;
+        sr += p.sum_ratio;
+        cl += p.clip;
+    }
+    for (int i = threadIdx.x; i < 3 * kHistBins; i += kMergeThreads) hist[i] = 0u;
+    a = block_reduce<kMergeThreads>(a);
+    __shared__ double s_abs[kMergeThreads / 32], s_ratio[kMergeThreads / 32];
+    __shared__ long long s_clip[kMergeThreads / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // the same fixed tree for the three extra sums
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const double x = __shfl_down_sync(0xffffffffu, sa, off);
+        const double y = __shfl_down_sync(0xffffffffu, sr, off);
+        const long long z = __shfl_down_sync(0xffffffffu, static_cast<long long>(cl), off);
+        if (lane + off < 32) {
+            sa += x;
+            sr += y;
+            cl += z;
+        }
+    }
+    if (lane == 0) {
+        s_abs[warp] = sa;
+        s_ratio[warp] = sr;
+        s_clip[warp] = cl;
+    }
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+    for (int w = 1; w < kMergeThreads / 32; ++w) {
+        s_abs[0] += s_abs[w];
+        s_ratio[0] += s_ratio[w];
+        s_clip[0] += s_clip[w];
+    }
+    rlk_audit_ext_t r;
+    r.active_count = a.count;
+    r.argmax_index = a.count > 0 ? a.arg : -1;
+    r.argmax_seq = -1;
+    r.argmax_pos = -1;
+    if (seq_offsets != nullptr && num_seqs > 0 && a.count > 0) {
+        int64_t lo = 0, hi = num_seqs;      // last s < num_seqs with seq_offsets[s] <= arg
+        while (hi - lo > 1) {
+            const int64_t mid = (lo + hi) >> 1;
+            if (seq_offsets[mid] <= a.arg) lo = mid; else hi = mid;
+        }
+        if (a.arg >= seq_offsets[lo] && a.arg < seq_offsets[lo + 1]) {
+            r.argmax_seq = lo;
+            r.argmax_pos = a.arg - seq_offsets[lo];
+        }
+    }
+    r.clip_count = s_clip[0];
+    const double cnt = static_cast<double>(a.count);
+    r.mean_dlogp = a.sum_d / cnt;
+    r.mean_abs_dlogp = s_abs[0] / cnt;
+    r.mean_ratio = s_ratio[0] / cnt;
+    r.approx_kl = a.sum_kl / cnt;
+    r.max_abs_dlogp = a.count > 0 ? a.best : 0.0f;
+    r.p50_abs_dlogp = r.p90_abs_dlogp = r.p99_abs_dlogp = __int_as_float(0x7fc00000);
+    r.clipfrac = static_cast<float>(static_cast<double>(s_clip[0]) / cnt);
+    r.error_flags = a.flags;
+    *result = r;
+    const int pct[3] = {50, 90, 99};
+    for (int q = 0; q < 3; ++q) {
+        sel->prefix[q] = 0u;
+        sel->rank[q] = (pct[q] * a.count + 99) / 100;   // nearest rank, 1-based (0 if none)
+    }
+}
+
+// Histogram of one digit of the |d| keys of the active elements that match
+// each percentile's prefix so far.
+template <int PASS>
+__global__ void __launch_bounds__(kAuditThreads)
+    audit_ext_hist(const float* __restrict__ nw, const float* __restrict__ od,
+                   const uint8_t* __restrict__ mask, int64_t N,
+                   const SelectState* __restrict__ sel, uint32_t* __restrict__ hist) {
+    constexpr int kShift = PASS == 0 ? 21 : (PASS == 1 ? 10 : 0);
+    constexpr uint32_t kDigitMask = PASS == 2 ? 0x3ffu : 0x7ffu;
+    constexpr int kPrefixShift = PASS == 1 ? 21 : 10;
+    __shared__ uint32_t h[3 * kHistBins];
+    for (int i = threadIdx.x; i < 3 * kHistBins; i += kAuditThreads) h[i] = 0u;
+    uint32_t pre[3];
+    bool want[3];
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+        pre[q] = sel->prefix[q];
+        want[q] = sel->rank[q] > 0;
+    }
+    __syncthreads();
+    constexpr int kBlock = kAuditThreads * kAuditV3PerThread;
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * kBlock;
+    for (int e = threadIdx.x; e < kBlock; e += kAuditThreads) {
+        const int64_t i = base + e;
+        if (i >= N) break;
+        if (mask != nullptr && mask[i] == 0) continue;
+        const uint32_t key = abs_key(nw[i] - od[i]);
+        const uint32_t digit = (key >> kShift) & kDigitMask;
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+            const bool match = PASS == 0 ? true : ((key >> kPrefixShift) == pre[q]);
+            if (want[q] && match) atomicAdd(&h[q * kHistBins + digit], 1u);
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 3 * kHistBins; i += kAuditThreads) {
+        const uint32_t c = h[i];
+        if (c != 0u) atomicAdd(&hist[i], c);
+    }
+}
+
+// Picks, for each percentile, the bin holding its rank; extends the prefix by
+// that digit and clears the histogram for the next pass.  After the last pass
+// the prefix is the selected key, written to the result.
+template <int PASS>
+__global__ void audit_ext_select(SelectState* __restrict__ sel, uint32_t* __restrict__ hist,
+                                 rlk_audit_ext_t* __restrict__ result) {
+    constexpr int kBits = PASS == 2 ? 10 : 11;
+    const int q = threadIdx.x;
+    if (q < 3 && sel->rank[q] > 0) {
+        const int64_t rank = sel->rank[q];
+        const uint32_t* hq = hist + q * kHistBins;
+        int64_t cum = 0;
+        uint32_t bin = 0;
+        for (int b = 0; b < (1 << kBits); ++b) {
+            if (cum + hq[b] >= rank) {
+                bin = b;
+                break;
+            }
+            cum += hq[b];
+        }
+        sel->rank[q] = rank - cum;
+        sel->prefix[q] = (sel->prefix[q] << kBits) | bin;
+        if (PASS == 2) {
+            const float v = __uint_as_float(sel->prefix[q] - 1u);
+            if (q == 0) result->p50_abs_dlogp = v;
+            if (q == 1) result->p90_abs_dlogp = v;
+            if (q == 2) result->p99_abs_dlogp = v;
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 3 * kHistBins; i += blockDim.x) hist[i] = 0u;
+}
+
 }  // namespace
 
 // Scratch of rlk_dlogp_audit_noalloc: one partial per 4096-element block for
@@ -333,6 +634,45 @@ cudaError_t launch_audit(const float* logp_new, const float* logp_old, const uin
     const AuditPartial* cparts = parts;
     const int64_t nparts = static_cast<int64_t>(blocks);
     return cudaLaunchKernelEx(&cfg, audit_pass2, cparts, nparts, result);
+}
+
+size_t audit_ext_workspace(int64_t N) {
+    return align_up(audit_v3_blocks(N) * sizeof(ExtPartial), 256) + 3 * kHistBins * 4 +
+           sizeof(SelectState) + 256;
+}
+
+cudaError_t launch_audit_ext(const float* logp_new, const float* logp_old, const uint8_t* mask,
+                             int64_t N, const int64_t* seq_offsets, int64_t num_seqs, float eps,
+                             rlk_audit_ext_t* result, void* workspace, bool vec_ok,
+                             cudaStream_t stream) {
+    const size_t blocks = audit_v3_blocks(N);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    ExtPartial* parts = reinterpret_cast<ExtPartial*>(ws);
+    uint32_t* hist = reinterpret_cast<uint32_t*>(ws + align_up(blocks * sizeof(ExtPartial), 256));
+    SelectState* sel = reinterpret_cast<SelectState*>(hist + 3 * kHistBins);
+    const unsigned grid = static_cast<unsigned>(blocks);
+    if (blocks > 0) {
+        if (vec_ok)
+            audit_ext_pass1<true><<<grid, kAuditThreads, 0, stream>>>(logp_new, logp_old, mask, N,
+                                                                      eps, parts);
+        else
+            audit_ext_pass1<false><<<grid, kAuditThreads, 0, stream>>>(logp_new, logp_old, mask,
+                                                                       N, eps, parts);
+    }
+    audit_ext_merge<<<1, kMergeThreads, 0, stream>>>(parts, static_cast<int64_t>(blocks),
+                                                     seq_offsets, num_seqs, result, sel, hist);
+    if (blocks > 0) {
+        audit_ext_hist<0><<<grid, kAuditThreads, 0, stream>>>(logp_new, logp_old, mask, N, sel,
+                                                               hist);
+        audit_ext_select<0><<<1, 32, 0, stream>>>(sel, hist, result);
+        audit_ext_hist<1><<<grid, kAuditThreads, 0, stream>>>(logp_new, logp_old, mask, N, sel,
+                                                               hist);
+        audit_ext_select<1><<<1, 32, 0, stream>>>(sel, hist, result);
+        audit_ext_hist<2><<<grid, kAuditThreads, 0, stream>>>(logp_new, logp_old, mask, N, sel,
+                                                               hist);
+        audit_ext_select<2><<<1, 32, 0, stream>>>(sel, hist, result);
+    }
+    return cudaGetLastError();
 }
 
 }  // namespace rlk

@@ -144,6 +144,12 @@ cudaError_t launch_logp_from_logits(const void* logits, bool bf16, int64_t strid
                                     const uint8_t* mask, float k, bool vec_ok, float* logp,
                                     float* lse, uint32_t* err, cudaStream_t stream);
 
+size_t audit_ext_workspace(int64_t N);
+cudaError_t launch_audit_ext(const float* logp_new, const float* logp_old, const uint8_t* mask,
+                             int64_t N, const int64_t* seq_offsets, int64_t num_seqs, float eps,
+                             rlk_audit_ext_t* result, void* workspace, bool vec_ok,
+                             cudaStream_t stream);
+
 // Device address (current device) of the library-owned audit scratch.
 cudaError_t audit_noalloc_scratch(void** out);
 

@@ -568,3 +568,47 @@ def test_entropy_backward_finite_differences(oracle_lib, shape):
     z = np.zeros(n)
     assert np.allclose(o.linear_logp_entropy_bwd_dw(h, w, y, mask, g, z, lse, ent, T),
                        o.linear_logp_bwd_dw(h, w, y, mask, g, lse, T), rtol=1e-14, atol=1e-15)
+
+
+# ----------------------------------------------------------------------------- extended audit
+
+def test_audit_ext_hand_built(oracle_lib):
+    o = oracle_lib
+    # |d| = 1..100 (a permutation), all active: nearest-rank p50 = 50, p90 = 90, p99 = 99
+    perm = np.random.default_rng(0).permutation(100)
+    d = (perm + 1).astype(np.float32) * np.float32(0.001)
+    sign = np.where(np.arange(100) % 2 == 0, 1, -1).astype(np.float32)
+    r = o.dlogp_audit_ext(d * sign, np.zeros(100, np.float32), None, None, 0.05)
+    srt = np.sort(d.astype(np.float64))
+    assert r["p50_abs_dlogp"] == srt[49] and r["p90_abs_dlogp"] == srt[89]
+    assert r["p99_abs_dlogp"] == srt[98] and r["max_abs_dlogp"] == srt[99]
+    assert abs(r["mean_abs_dlogp"] - float(np.mean(d.astype(np.float64)))) < 1e-15
+    # clip: |exp(d) - 1| > 0.05 <=> d > log(1.05) = 0.04879 or d < log(0.95) = -0.05129
+    dd = (d * sign).astype(np.float64)
+    assert r["clip_count"] == int(np.sum(np.abs(np.exp(dd) - 1) > 0.05))
+    assert abs(r["clipfrac"] - r["clip_count"] / 100) < 1e-15
+    assert abs(r["mean_ratio"] - float(np.mean(np.exp(dd)))) < 1e-15
+    # worst token's sequence and position
+    offs = np.array([0, 30, 31, 100], np.int64)
+    r = o.dlogp_audit_ext(d * sign, np.zeros(100, np.float32), None, offs, 0.05)
+    w = int(np.argmax(d))
+    s = int(np.searchsorted(offs, w, side="right") - 1)
+    assert r["argmax_index"] == w and r["argmax_seq"] == s and r["argmax_pos"] == w - offs[s]
+
+
+def test_audit_ext_small_counts_and_masked(oracle_lib):
+    o = oracle_lib
+    # one active token: every percentile is that token
+    r = o.dlogp_audit_ext(np.array([0.5, 0.25, 7.0], np.float32), np.zeros(3, np.float32),
+                          np.array([0, 1, 0], np.uint8))
+    assert r["p50_abs_dlogp"] == r["p99_abs_dlogp"] == r["max_abs_dlogp"] == 0.25
+    # two tokens: p50 is the smaller (rank 1), p90 / p99 the larger (rank 2)
+    r = o.dlogp_audit_ext(np.array([-0.3, 0.1], np.float32), np.zeros(2, np.float32), None)
+    assert r["p50_abs_dlogp"] == float(np.float32(0.1)) and r["p90_abs_dlogp"] == float(np.float32(0.3))
+    # none active
+    r = o.dlogp_audit_ext(np.zeros(4, np.float32), np.zeros(4, np.float32), np.zeros(4, np.uint8))
+    assert r["active_count"] == 0 and math.isnan(r["p50_abs_dlogp"]) and r["argmax_seq"] == -1
+    # a NaN ranks above every number, so it is the p99 / max of a short list
+    r = o.dlogp_audit_ext(np.array([0.1, float("nan"), 0.2], np.float32), np.zeros(3, np.float32),
+                          None)
+    assert math.isnan(r["p99_abs_dlogp"]) and r["p50_abs_dlogp"] == float(np.float32(0.2))
