@@ -99,9 +99,8 @@ rlk_status_t check_shape(int64_t N, int64_t H, int64_t V, double temperature) {
 extern "C" {
 
 size_t rlk_linear_logp_fwd_workspace_bytes(int64_t N, int64_t H, int64_t V) {
-    (void)H;
-    if (N < 0 || V < 1) return 0;
-    return rlk::FwdLayout(N, V).total;
+    if (N < 0 || V < 1 || H < 0) return 0;
+    return rlk::FwdLayout(N, H, V).total;
 }
 
 size_t rlk_linear_logp_bwd_workspace_bytes(int64_t N, int64_t H, int64_t V) {
@@ -131,13 +130,31 @@ static rlk_status_t fwd_impl(const void* hidden, const void* weight, const int64
     DeviceInfo dev;
     RLK_TRY(current_device(dev));
 
+    // a masked batch is compacted to its active rows first (ascending token order)
+    const rlk::FwdLayout lay(N, H, V);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int* rows = nullptr;
+    int* pos_of = nullptr;
+    int* n_rows = nullptr;
+    const void* gemm_rows = hidden;
+    if (active_mask != nullptr) {
+        rows = reinterpret_cast<int*>(ws + lay.rows_off);
+        pos_of = reinterpret_cast<int*>(ws + lay.pos_off);
+        n_rows = reinterpret_cast<int*>(ws + lay.count_off);
+        void* hc = ws + lay.hc_off;
+        RLK_CUDA(rlk::launch_compact(active_mask, static_cast<int>(N), static_cast<int>(H), hidden,
+                                     hc, reinterpret_cast<int*>(ws + lay.blk_off), rows, pos_of,
+                                     n_rows, stream));
+        gemm_rows = hc;
+    }
     CUtensorMap map_h, map_w;
-    RLK_TRY(make_map(&map_h, hidden, H, N, H * 2, 64, rlk::kTileM));
+    RLK_TRY(make_map(&map_h, gemm_rows, H, N, H * 2, 64, rlk::kTileM));
     RLK_TRY(make_map(&map_w, weight, H, V, H * 2, 64, rlk::kTileV));
     const float k = static_cast<float>(1.4426950408889634074 / temperature);
     RLK_CUDA(rlk::launch_fwd(map_h, map_w, targets, active_mask, static_cast<int>(N),
                              static_cast<int>(H), static_cast<int>(V), k, logp_out, lse_out,
-                             entropy_out, workspace, device_error_word, dev.sms, stream));
+                             entropy_out, workspace, rows, n_rows, pos_of, device_error_word,
+                             dev.sms, stream));
     return RLK_OK;
 }
 
@@ -183,32 +200,53 @@ static rlk_status_t bwd_impl(const void* hidden, const void* weight, const int64
 
     const rlk::BwdLayout lay(N, H);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    void* ds = ws + lay.ds_off;
     float* dh_acc = reinterpret_cast<float*>(ws + lay.dhacc_off);
     int* sorted_y = reinterpret_cast<int*>(ws + lay.sorted_y_off);
     int* sorted_t = reinterpret_cast<int*>(ws + lay.sorted_t_off);
 
-    rlk::BwdMaps maps;
+    rlk::BwdStepMaps maps;
     RLK_TRY(make_map(&maps.h_kmajor, hidden, H, N, H * 2, 64, rlk::kTileM));
     RLK_TRY(make_map(&maps.w_kmajor, weight, H, V, H * 2, 64, rlk::kTileV));
     RLK_TRY(make_map(&maps.w_mnmajor, weight, H, V, H * 2, 64, 64));
     RLK_TRY(make_map(&maps.h_mnmajor, hidden, H, N, H * 2, 64, 64));
 
     const int n = static_cast<int>(N), h = static_cast<int>(H), v = static_cast<int>(V);
-    const float k = static_cast<float>(1.4426950408889634074 / temperature);
-    const float temp = static_cast<float>(temperature);
     RLK_CUDA(rlk::launch_target_sort(targets, active_mask, n, v, sorted_y, sorted_t,
                                      device_error_word, stream));
     const int num_chunks = static_cast<int>((V + rlk::kBwdChunk - 1) / rlk::kBwdChunk);
+    rlk::BwdStep st;
+    st.targets = targets;
+    st.mask = active_mask;
+    st.grad = grad_logp;
+    st.grad_ent = grad_entropy;
+    st.ent = entropy;
+    st.lse = lse;
+    st.hidden = hidden;
+    st.weight = weight;
+    st.N = n;
+    st.H = h;
+    st.V = v;
+    st.num_chunks = num_chunks;
+    st.k = static_cast<float>(1.4426950408889634074 / temperature);
+    st.temp = static_cast<float>(temperature);
+    st.dh_acc = dh_acc;
+    st.sorted_y = sorted_y;
+    st.sorted_t = sorted_t;
+    st.dhidden = dhidden;
+    st.dweight = dweight;
+    void* ds = ws + lay.ds_off;
     for (int c = 0; c < num_chunks; ++c) {
+        // one launch per role: the three roles of a chunk share L2 best when each has the GPU
         const int64_t width = std::min<int64_t>(rlk::kBwdChunk, V - int64_t(c) * rlk::kBwdChunk);
-        rlk::ChunkMaps cm;
-        RLK_TRY(make_map(&cm.ds_kmajor, ds, width, N, uint64_t(rlk::kBwdChunk) * 2, 64, rlk::kTileM));
-        RLK_TRY(make_map(&cm.ds_mnmajor, ds, width, N, uint64_t(rlk::kBwdChunk) * 2, 64, 64));
-        RLK_CUDA(rlk::launch_bwd_chunk(maps, cm, targets, active_mask, grad_logp, grad_entropy,
-                                       entropy, lse, hidden, weight, n, h, v, c, num_chunks, k,
-                                       temp, ds, dh_acc, sorted_y, sorted_t, dhidden, dweight,
-                                       device_error_word, dev.sms, stream));
+        RLK_TRY(make_map(&maps.ds_kmajor, ds, width, N, uint64_t(rlk::kBwdChunk) * 2, 64,
+                         rlk::kTileM));
+        RLK_TRY(make_map(&maps.ds_mnmajor, ds, width, N, uint64_t(rlk::kBwdChunk) * 2, 64, 64));
+        st.ds = ds;
+        st.chunk = c;
+        for (int role : {rlk::kRoleDs, rlk::kRoleDh, rlk::kRoleDw}) {
+            st.role = role;
+            RLK_CUDA(rlk::launch_bwd_step(maps, st, dev.sms, device_error_word, stream));
+        }
     }
     return RLK_OK;
 }
@@ -422,7 +460,7 @@ const char* rlk_contract_string(void) {
     return "rlk-gb300 linear_logp v1; arch=sm_103a; nvcc=" RLK_STR(__CUDACC_VER_MAJOR__) "." RLK_STR(
         __CUDACC_VER_MINOR__) "; inputs=bf16; accum=fp32 (tcgen05 kind::f16, TMEM); "
                               "tile=128x256x64 cta_group::1, no split-K; "
-                              "fwd_vocab_chunk=1024 (merge ascending); bwd_vocab_chunk=16384; "
+                              "fwd_vocab_chunk=1024 (merge ascending); bwd_vocab_chunk=16384; masked batches: active rows compacted (ascending) before the GEMM; "
                               "exp=ex2.approx.ftz, log=lg2.approx.ftz; k=fp32(log2(e)/T); "
                               "logits never rounded; logp/lse fp32; dS bf16 (target term fp32); "
                               "dh/dW rounded once to bf16 (RNE); no float atomics; "

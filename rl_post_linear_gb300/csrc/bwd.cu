@@ -16,11 +16,14 @@
 // rounding of the outputs.
 //
 // The vocabulary is walked in fixed chunks of kBwdChunk columns, ascending.
-// For each chunk c three persistent tcgen05 GEMMs run on the stream:
+// For each chunk c three tcgen05 GEMM roles run:
 //   DsPolicy  S_c = h W_c^T (K = H) -> dS_c [N, chunk] bf16 workspace
 //   DhPolicy  dS_c W_c (K = chunk)  -> dh_acc [N, H] fp32 (+= previous chunks;
 //             the last chunk adds the target term and rounds to bf16)
 //   DwPolicy  dS_c^T h (K = N)      -> dW rows of chunk c, plus target terms
+// one persistent launch per role and chunk, in that order (measured faster
+// than putting roles of neighbouring chunks side by side in one launch: alone,
+// each role keeps its L2 working set).
 // None of the reductions is split or done with atomics: dh_t depends only on
 // row t's inputs and the fixed chunk boundaries, so it is batch invariant;
 // dW is reproducible bit for bit.
@@ -66,9 +69,7 @@ __device__ __forceinline__ void bf16x8_to_f32(uint4 v, float* out) {
 //   dS = p (c1 + c2 S),  c1 = -(g - gH Ez) / T,  c2 = -gH / T^2,
 // i.e. -(p/T) (g + gH (S/T - Ez)), the entropy's dH/dz = -p (z - E[z]).
 template <bool ENT>
-struct DsPolicyT {
-    static constexpr bool kAMn = false;   // h [N,H]
-    static constexpr bool kBMn = false;   // W [V,H]
+struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
 
     const int64_t* targets;
     const uint8_t* mask;
@@ -81,7 +82,7 @@ struct DsPolicyT {
     float k, temp;
 
     __device__ int num_units() const { return num_m * num_n; }
-    __device__ int k_blocks() const { return kblocks; }
+    __device__ int k_blocks(int) const { return kblocks; }
     __device__ int tiles_in_unit(int) const { return 1; }
     // unit -> (token tile m, vocab tile n of the chunk), token tiles grouped
     __device__ void unit(int u, int& m, int& n) const {
@@ -159,9 +160,8 @@ struct DsPolicyT {
 
 // ----------------------------------------------------------------------------- dh
 
-struct DhPolicy {
-    static constexpr bool kAMn = false;   // dS_c [N, width]: K (vocab) contiguous
-    static constexpr bool kBMn = true;    // W_c [width, H]: N (hidden) contiguous
+// dS_c [N, width]: K (vocab) contiguous; W_c [width, H]: N (hidden) contiguous
+struct DhPolicy : SingleRole<false, true> {
 
     const int64_t* targets;
     const uint8_t* mask;
@@ -174,7 +174,7 @@ struct DhPolicy {
     float temp;
 
     __device__ int num_units() const { return num_m * num_n; }
-    __device__ int k_blocks() const { return kblocks; }
+    __device__ int k_blocks(int) const { return kblocks; }
     __device__ int tiles_in_unit(int) const { return 1; }
     __device__ void coords(int u, int, int& a_mn, int& a_k, int& b_mn, int& b_k) const {
         const int m = u / num_n;
@@ -258,9 +258,8 @@ struct DhPolicy {
 
 // ----------------------------------------------------------------------------- dW
 
-struct DwPolicy {
-    static constexpr bool kAMn = true;    // dS_c^T: vocab (M) contiguous, tokens along K
-    static constexpr bool kBMn = true;    // h: hidden (N) contiguous, tokens along K
+// dS_c^T: vocab (M) contiguous, tokens along K; h: hidden (N) contiguous
+struct DwPolicy : SingleRole<true, true> {
 
     const float* grad;
     const __nv_bfloat16* hidden;   // [N][H]
@@ -271,7 +270,7 @@ struct DwPolicy {
     float temp;
 
     __device__ int num_units() const { return num_m * num_n; }
-    __device__ int k_blocks() const { return kblocks; }
+    __device__ int k_blocks(int) const { return kblocks; }
     __device__ int tiles_in_unit(int) const { return 1; }
     // unit -> (vocab tile m of the chunk, hidden tile n), hidden tiles grouped
     __device__ void unit(int u, int& m, int& n) const {
@@ -408,80 +407,67 @@ static cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const
                                          static_cast<int>(kGemmSmemBytes));
     if (e != cudaSuccess) return e;
     const int grid = units < num_sms ? units : num_sms;
-    kern<<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(a, b, p, err);
+    kern<<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(TwoMaps{a, b}, p, err);
     return cudaGetLastError();
 }
 
 template <bool ENT>
-static cudaError_t launch_ds(const BwdMaps& maps, const int64_t* targets, const uint8_t* mask,
-                             const float* grad, const float* grad_ent, const float* ent,
-                             const float* lse, int N, int H, int V, int c0, int width, float k,
-                             float temp, void* ds, uint32_t* err, int num_sms,
-                             cudaStream_t stream) {
+static cudaError_t launch_ds(const BwdStepMaps& maps, const BwdStep& st, int c0, int width,
+                             int num_sms, uint32_t* err, cudaStream_t stream) {
     DsPolicyT<ENT> ps;
-    ps.targets = targets;
-    ps.mask = mask;
-    ps.grad = grad;
-    ps.grad_ent = grad_ent;
-    ps.ent = ent;
-    ps.lse = lse;
-    ps.ds = static_cast<__nv_bfloat16*>(ds);
-    ps.N = N;
-    ps.V = V;
+    ps.targets = st.targets;
+    ps.mask = st.mask;
+    ps.grad = st.grad;
+    ps.grad_ent = st.grad_ent;
+    ps.ent = st.ent;
+    ps.lse = st.lse;
+    ps.ds = static_cast<__nv_bfloat16*>(st.ds);
+    ps.N = st.N;
+    ps.V = st.V;
     ps.c0 = c0;
-    ps.num_m = (N + kTileM - 1) / kTileM;
+    ps.num_m = (st.N + kTileM - 1) / kTileM;
     ps.num_n = (width + kTileV - 1) / kTileV;
-    ps.kblocks = H / 64;
-    ps.k = k;
-    ps.temp = temp;
+    ps.kblocks = st.H / 64;
+    ps.k = st.k;
+    ps.temp = st.temp;
     return launch_gemm(maps.h_kmajor, maps.w_kmajor, ps, ps.num_m * ps.num_n, num_sms, err, stream);
 }
 
-cudaError_t launch_bwd_chunk(const BwdMaps& maps, const ChunkMaps& cmaps, const int64_t* targets,
-                             const uint8_t* mask, const float* grad, const float* grad_ent,
-                             const float* ent, const float* lse,
-                             const void* hidden, const void* weight, int N, int H, int V,
-                             int chunk, int num_chunks, float k, float temp, void* ds,
-                             float* dh_acc, const int* sorted_y, const int* sorted_t,
-                             void* dhidden, void* dweight, uint32_t* err, int num_sms,
-                             cudaStream_t stream) {
-    const int c0 = chunk * kBwdChunk;
+cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_sms, uint32_t* err,
+                            cudaStream_t stream) {
+    const int N = st.N, H = st.H, V = st.V;
+    const int c0 = st.chunk * kBwdChunk;
     const int width = (V - c0) < kBwdChunk ? (V - c0) : kBwdChunk;
-    const int num_m = (N + kTileM - 1) / kTileM;
-
-    cudaError_t e = grad_ent != nullptr
-        ? launch_ds<true>(maps, targets, mask, grad, grad_ent, ent, lse, N, H, V, c0, width, k,
-                          temp, ds, err, num_sms, stream)
-        : launch_ds<false>(maps, targets, mask, grad, nullptr, nullptr, lse, N, H, V, c0, width,
-                           k, temp, ds, err, num_sms, stream);
-    if (e != cudaSuccess) return e;
-
-    DhPolicy pd;
-    pd.targets = targets;
-    pd.mask = mask;
-    pd.grad = grad;
-    pd.weight = static_cast<const __nv_bfloat16*>(weight);
-    pd.dh_acc = dh_acc;
-    pd.dh = static_cast<__nv_bfloat16*>(dhidden);
-    pd.N = N;
-    pd.V = V;
-    pd.H = H;
-    pd.c0 = c0;
-    pd.num_m = num_m;
-    pd.num_n = (H + kTileV - 1) / kTileV;
-    pd.kblocks = (width + 63) / 64;
-    pd.first = chunk == 0;
-    pd.last = chunk == num_chunks - 1;
-    pd.temp = temp;
-    e = launch_gemm(cmaps.ds_kmajor, maps.w_mnmajor, pd, pd.num_m * pd.num_n, num_sms, err, stream);
-    if (e != cudaSuccess) return e;
-
+    if (st.role == kRoleDs)
+        return st.grad_ent != nullptr ? launch_ds<true>(maps, st, c0, width, num_sms, err, stream)
+                                      : launch_ds<false>(maps, st, c0, width, num_sms, err, stream);
+    if (st.role == kRoleDh) {
+        DhPolicy pd;
+        pd.targets = st.targets;
+        pd.mask = st.mask;
+        pd.grad = st.grad;
+        pd.weight = static_cast<const __nv_bfloat16*>(st.weight);
+        pd.dh_acc = st.dh_acc;
+        pd.dh = static_cast<__nv_bfloat16*>(st.dhidden);
+        pd.N = N;
+        pd.V = V;
+        pd.H = H;
+        pd.c0 = c0;
+        pd.num_m = (N + kTileM - 1) / kTileM;
+        pd.num_n = (H + kTileV - 1) / kTileV;
+        pd.kblocks = (width + 63) / 64;
+        pd.first = st.chunk == 0;
+        pd.last = st.chunk == st.num_chunks - 1;
+        pd.temp = st.temp;
+        return launch_gemm(maps.ds_kmajor, maps.w_mnmajor, pd, pd.num_m * pd.num_n, num_sms, err,
+                           stream);
+    }
     DwPolicy pw;
-    pw.grad = grad;
-    pw.hidden = static_cast<const __nv_bfloat16*>(hidden);
-    pw.dw = static_cast<__nv_bfloat16*>(dweight);
-    pw.sorted_y = sorted_y;
-    pw.sorted_t = sorted_t;
+    pw.grad = st.grad;
+    pw.hidden = static_cast<const __nv_bfloat16*>(st.hidden);
+    pw.dw = static_cast<__nv_bfloat16*>(st.dweight);
+    pw.sorted_y = st.sorted_y;
+    pw.sorted_t = st.sorted_t;
     pw.N = N;
     pw.H = H;
     pw.c0 = c0;
@@ -489,8 +475,8 @@ cudaError_t launch_bwd_chunk(const BwdMaps& maps, const ChunkMaps& cmaps, const 
     pw.num_m = (width + kTileM - 1) / kTileM;
     pw.num_n = (H + kTileV - 1) / kTileV;
     pw.kblocks = (N + 63) / 64;
-    pw.temp = temp;
-    return launch_gemm(cmaps.ds_mnmajor, maps.h_mnmajor, pw, pw.num_m * pw.num_n, num_sms, err,
+    pw.temp = st.temp;
+    return launch_gemm(maps.ds_mnmajor, maps.h_mnmajor, pw, pw.num_m * pw.num_n, num_sms, err,
                        stream);
 }
 

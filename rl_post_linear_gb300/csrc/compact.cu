@@ -1,0 +1,108 @@
+// compact.cu -- active-row compaction for masked batches.
+//
+// "RL-Kernel integration roadmap for vime", Consistency Contract: all metrics
+// use active tokens only, and a token's result must not change with padding,
+// packing or active-mask density.  The forward GEMM therefore only needs the
+// active rows: they are gathered, in ascending token order, into a contiguous
+// buffer, so padding and masked-out tokens cost no tensor-core work.  A row's
+// arithmetic does not depend on the tile it lands in, so the result is bitwise
+// the same as without compaction.
+//
+// Deterministic and atomic-free: kernel 1 counts the active rows of each
+// 1024-row block; kernel 2 gives each block its offset as the sum of the counts
+// before it (ascending block order), places the block's active rows by warp
+// ballots (ascending token order), records rows[pos] = t and pos_of[t] = pos
+// (-1 for inactive rows), copies the rows of h, and block 0 stores the active
+// count.
+#include "rlk_internal.h"
+
+namespace rlk {
+
+namespace {
+
+constexpr int kCompactThreads = kCompactBlock;
+
+__global__ void __launch_bounds__(kCompactThreads)
+    compact_count_kernel(const uint8_t* __restrict__ mask, int N, int* __restrict__ blk_count) {
+    const int t = blockIdx.x * kCompactThreads + threadIdx.x;
+    const bool act = t < N && mask[t] != 0;
+    const unsigned ballot = __ballot_sync(0xffffffffu, act);
+    __shared__ int warp_count[kCompactThreads / 32];
+    if ((threadIdx.x & 31) == 0) warp_count[threadIdx.x >> 5] = __popc(ballot);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int c = 0;
+        for (int w = 0; w < kCompactThreads / 32; ++w) c += warp_count[w];
+        blk_count[blockIdx.x] = c;
+    }
+}
+
+__global__ void __launch_bounds__(kCompactThreads)
+    compact_place_kernel(const uint8_t* __restrict__ mask, int N, int H,
+                         const int* __restrict__ blk_count, int num_blocks,
+                         const uint4* __restrict__ hidden, uint4* __restrict__ hidden_c,
+                         int* __restrict__ rows, int* __restrict__ pos_of,
+                         int* __restrict__ n_active) {
+    __shared__ int s_base;
+    __shared__ int warp_count[kCompactThreads / 32];
+    __shared__ int warp_off[kCompactThreads / 32];
+    if (threadIdx.x == 0) {
+        int base = 0;
+        for (int b = 0; b < static_cast<int>(blockIdx.x); ++b) base += blk_count[b];
+        s_base = base;
+        if (blockIdx.x == 0) {
+            int total = 0;
+            for (int b = 0; b < num_blocks; ++b) total += blk_count[b];
+            *n_active = total;
+        }
+    }
+    const int t = blockIdx.x * kCompactThreads + threadIdx.x;
+    const bool act = t < N && mask[t] != 0;
+    const unsigned ballot = __ballot_sync(0xffffffffu, act);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) warp_count[warp] = __popc(ballot);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int off = 0;
+        for (int w = 0; w < kCompactThreads / 32; ++w) {
+            warp_off[w] = off;
+            off += warp_count[w];
+        }
+    }
+    __syncthreads();
+    const int pos = s_base + warp_off[warp] + __popc(ballot & ((1u << lane) - 1u));
+    if (t < N) {
+        pos_of[t] = act ? pos : -1;
+        if (act) rows[pos] = t;
+    }
+    // copy the block's active rows of h: one warp per row, 16 bytes per lane
+    const int vec_per_row = H / 8;
+    __shared__ int s_pos[kCompactThreads];
+    s_pos[threadIdx.x] = act ? pos : -1;
+    __syncthreads();
+    for (int r = warp; r < kCompactThreads; r += kCompactThreads / 32) {
+        const int p = s_pos[r];
+        if (p < 0) continue;
+        const int tr = blockIdx.x * kCompactThreads + r;
+        const uint4* src = hidden + static_cast<size_t>(tr) * vec_per_row;
+        uint4* dst = hidden_c + static_cast<size_t>(p) * vec_per_row;
+        for (int j = lane; j < vec_per_row; j += 32) dst[j] = src[j];
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_compact(const uint8_t* mask, int N, int H, const void* hidden, void* hidden_c,
+                           int* blk_count, int* rows, int* pos_of, int* n_active,
+                           cudaStream_t stream) {
+    const int blocks = (N + kCompactThreads - 1) / kCompactThreads;
+    compact_count_kernel<<<blocks, kCompactThreads, 0, stream>>>(mask, N, blk_count);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    compact_place_kernel<<<blocks, kCompactThreads, 0, stream>>>(
+        mask, N, H, blk_count, blocks, static_cast<const uint4*>(hidden),
+        static_cast<uint4*>(hidden_c), rows, pos_of, n_active);
+    return cudaGetLastError();
+}
+
+}  // namespace rlk

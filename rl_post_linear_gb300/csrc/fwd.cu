@@ -56,24 +56,29 @@ constexpr float kMaskedLogit = -3.0e38f;
 // ENT adds the running sum a = sum_j 2^((S_j - m) k) S_j per row, from which
 // the merge forms E[S] = a / s and the entropy lse - E[S]/T.
 template <bool ENT>
-struct FwdPolicyT {
-    static constexpr bool kAMn = false;   // h [N,H]: K-major
-    static constexpr bool kBMn = false;   // W [V,H]: K-major
+struct FwdPolicyT : SingleRole<false, false> {   // h [N,H] and W [V,H]: K-major
 
     const int64_t* targets;
     const uint8_t* mask;
     float2* partials;     // [num_chunks][N]
     float* partials_a;    // [num_chunks][N] (ENT only)
     float* s_target;      // [N]
+    const int* rows;      // compacted row -> token (nullptr: rows are tokens)
+    const int* n_rows;    // number of compacted rows, on the device (nullptr: N)
     int64_t vocab_start;  // global id of this weight block's first row
     int N, V, num_m, num_vt, num_chunks, kblocks;   // V: rows of this weight block
     float k;              // log2(e) / T
 
-    __device__ int num_units() const { return num_m * num_chunks; }
-    __device__ int k_blocks() const { return kblocks; }
+    __device__ int valid_rows() const { return n_rows != nullptr ? *n_rows : N; }
+    __device__ int token_tiles() const {
+        return n_rows != nullptr ? (*n_rows + kTileM - 1) / kTileM : num_m;
+    }
+
+    __device__ int num_units() const { return token_tiles() * num_chunks; }
+    __device__ int k_blocks(int) const { return kblocks; }
     // unit -> (token tile m, vocab chunk c), token tiles grouped by kRasterTokenTiles
     __device__ void unit(int u, int& m, int& c) const {
-        grouped_unit(u, num_m, num_chunks, kRasterTokenTiles, m, c);
+        grouped_unit(u, token_tiles(), num_chunks, kRasterTokenTiles, m, c);
     }
     __device__ int tiles_in_unit(int u) const {
         int m, c;
@@ -98,14 +103,17 @@ struct FwdPolicyT {
     __device__ void epi_begin(int u, int row, EpiState& st) const {
         int m, c;
         unit(u, m, c);
-        const int t = m * kTileM + row;
+        const int i = m * kTileM + row;
         st.m = -INFINITY;
         st.s = 0.f;
         st.a = 0.f;
         st.sy = 0.f;
         st.found = false;
         st.y = -1;
-        if (t < N && (mask == nullptr || mask[t] != 0)) st.y = targets[t];
+        if (i < valid_rows()) {
+            const int t = rows != nullptr ? rows[i] : i;
+            if (mask == nullptr || mask[t] != 0) st.y = targets[t];
+        }
     }
 
     __device__ void epi_tile(int u, int q, int row, uint32_t taddr, EpiState& st) const {
@@ -159,17 +167,18 @@ struct FwdPolicyT {
     __device__ void epi_end(int u, int row, EpiState& st) const {
         int m, c;
         unit(u, m, c);
-        const int t = m * kTileM + row;
-        if (t >= N) return;
-        partials[static_cast<size_t>(c) * N + t] = make_float2(st.m, st.s);
-        if constexpr (ENT) partials_a[static_cast<size_t>(c) * N + t] = st.a;
-        if (st.found) s_target[t] = st.sy;
+        const int i = m * kTileM + row;          // compacted row (the token when not compacted)
+        if (i >= valid_rows()) return;
+        partials[static_cast<size_t>(c) * N + i] = make_float2(st.m, st.s);
+        if constexpr (ENT) partials_a[static_cast<size_t>(c) * N + i] = st.a;
+        if (st.found) s_target[i] = st.sy;
     }
 };
 
 __global__ void fwd_merge_kernel(const float2* __restrict__ partials,
                                  const float* __restrict__ partials_a,
                                  const float* __restrict__ s_target,
+                                 const int* __restrict__ pos_of,
                                  const int64_t* __restrict__ targets,
                                  const uint8_t* __restrict__ mask, int N, int V, int num_chunks,
                                  float k, float* __restrict__ logp, float* __restrict__ lse,
@@ -182,14 +191,15 @@ __global__ void fwd_merge_kernel(const float2* __restrict__ partials,
         if (entropy != nullptr) entropy[t] = 0.f;
         return;
     }
+    const int i = pos_of != nullptr ? pos_of[t] : t;   // the token's row in the partials
     float m = -INFINITY;
-    for (int c = 0; c < num_chunks; ++c) m = fmaxf(m, partials[static_cast<size_t>(c) * N + t].x);
+    for (int c = 0; c < num_chunks; ++c) m = fmaxf(m, partials[static_cast<size_t>(c) * N + i].x);
     float sigma = 0.f, a = 0.f;
     for (int c = 0; c < num_chunks; ++c) {
-        const float2 pc = partials[static_cast<size_t>(c) * N + t];
+        const float2 pc = partials[static_cast<size_t>(c) * N + i];
         const float wgt = ex2_approx((pc.x - m) * k);
         sigma += pc.y * wgt;
-        if (entropy != nullptr) a += partials_a[static_cast<size_t>(c) * N + t] * wgt;
+        if (entropy != nullptr) a += partials_a[static_cast<size_t>(c) * N + i] * wgt;
     }
     const float lse2 = m * k + lg2_approx(sigma);
     constexpr float kLn2 = 0.693147180559945309f;
@@ -201,21 +211,24 @@ __global__ void fwd_merge_kernel(const float2* __restrict__ partials,
         if (err != nullptr) atomicOr(err, RLK_DEVERR_TARGET_RANGE);
         return;
     }
-    logp[t] = (s_target[t] * k - lse2) * kLn2;
+    logp[t] = (s_target[i] * k - lse2) * kLn2;
 }
 
 template <bool ENT>
 static cudaError_t launch_partials_t(const CUtensorMap& map_h, const CUtensorMap& map_w,
                                      const int64_t* targets, const uint8_t* mask, int N, int H,
                                      int V_local, int64_t vocab_start, float k, float2* partials,
-                                     float* partials_a, float* s_target, uint32_t* err,
-                                     int num_sms, cudaStream_t stream) {
+                                     float* partials_a, float* s_target, const int* rows,
+                                     const int* n_rows, uint32_t* err, int num_sms,
+                                     cudaStream_t stream) {
     FwdPolicyT<ENT> p;
     p.targets = targets;
     p.mask = mask;
     p.partials = partials;
     p.partials_a = partials_a;
     p.s_target = s_target;
+    p.rows = rows;
+    p.n_rows = n_rows;
     p.vocab_start = vocab_start;
     p.N = N;
     p.V = V_local;
@@ -230,7 +243,7 @@ static cudaError_t launch_partials_t(const CUtensorMap& map_h, const CUtensorMap
     if (e != cudaSuccess) return e;
     const long long units = static_cast<long long>(p.num_m) * p.num_chunks;
     const int grid = static_cast<int>(units < num_sms ? units : num_sms);
-    kern<<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(map_h, map_w, p, err);
+    kern<<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(TwoMaps{map_h, map_w}, p, err);
     return cudaGetLastError();
 }
 
@@ -239,35 +252,36 @@ cudaError_t launch_fwd_partials(const CUtensorMap& map_h, const CUtensorMap& map
                                 int V_local, int64_t vocab_start, float k, float2* partials,
                                 float* s_target, uint32_t* err, int num_sms, cudaStream_t stream) {
     return launch_partials_t<false>(map_h, map_w, targets, mask, N, H, V_local, vocab_start, k,
-                                    partials, nullptr, s_target, err, num_sms, stream);
+                                    partials, nullptr, s_target, nullptr, nullptr, err, num_sms,
+                                    stream);
 }
 
 cudaError_t launch_fwd_merge(const float2* partials, int num_chunks, const float* s_target,
                              const int64_t* targets, const uint8_t* mask, int N, int V, float k,
                              float* logp, float* lse, uint32_t* err, cudaStream_t stream) {
-    fwd_merge_kernel<<<(N + 255) / 256, 256, 0, stream>>>(partials, nullptr, s_target, targets,
-                                                          mask, N, V, num_chunks, k, logp, lse,
-                                                          nullptr, err);
+    fwd_merge_kernel<<<(N + 255) / 256, 256, 0, stream>>>(partials, nullptr, s_target, nullptr,
+                                                          targets, mask, N, V, num_chunks, k,
+                                                          logp, lse, nullptr, err);
     return cudaGetLastError();
 }
 
 cudaError_t launch_fwd(const CUtensorMap& map_h, const CUtensorMap& map_w, const int64_t* targets,
                        const uint8_t* mask, int N, int H, int V, float k, float* logp, float* lse,
-                       float* entropy, void* workspace, uint32_t* err, int num_sms,
-                       cudaStream_t stream) {
-    FwdLayout lay(N, V);
+                       float* entropy, void* workspace, const int* rows, const int* n_rows,
+                       const int* pos_of, uint32_t* err, int num_sms, cudaStream_t stream) {
+    FwdLayout lay(N, H, V);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     float2* partials = reinterpret_cast<float2*>(ws + lay.partial_off);
     float* partials_a = reinterpret_cast<float*>(ws + lay.partial_a_off);
     float* s_target = reinterpret_cast<float*>(ws + lay.target_off);
     cudaError_t e = entropy != nullptr
         ? launch_partials_t<true>(map_h, map_w, targets, mask, N, H, V, 0, k, partials, partials_a,
-                                  s_target, err, num_sms, stream)
+                                  s_target, rows, n_rows, err, num_sms, stream)
         : launch_partials_t<false>(map_h, map_w, targets, mask, N, H, V, 0, k, partials, nullptr,
-                                   s_target, err, num_sms, stream);
+                                   s_target, rows, n_rows, err, num_sms, stream);
     if (e != cudaSuccess) return e;
     fwd_merge_kernel<<<(N + 255) / 256, 256, 0, stream>>>(
-        partials, entropy != nullptr ? partials_a : nullptr, s_target, targets, mask, N, V,
+        partials, entropy != nullptr ? partials_a : nullptr, s_target, pos_of, targets, mask, N, V,
         static_cast<int>(lay.num_chunks), k, logp, lse, entropy, err);
     return cudaGetLastError();
 }

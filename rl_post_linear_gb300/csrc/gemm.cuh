@@ -71,6 +71,47 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t stage_addr, int kk) {
     }
 }
 
+// Runtime-majorness variants for policies that mix operand layouts per unit.
+template <int ROWS>
+__device__ __forceinline__ void load_operand_rt(bool mn_major, uint8_t* dst, const CUtensorMap* map,
+                                                uint64_t* bar, int mn0, int k0) {
+    if (mn_major)
+        load_operand<true, ROWS>(dst, map, bar, mn0, k0);
+    else
+        load_operand<false, ROWS>(dst, map, bar, mn0, k0);
+}
+
+__device__ __forceinline__ uint64_t operand_desc_rt(bool mn_major, uint32_t stage_addr, int kk) {
+    return mn_major ? operand_desc<true>(stage_addr, kk) : operand_desc<false>(stage_addr, kk);
+}
+
+// The policy interface the mainloop relies on:
+//   struct Maps                          tensor maps (kernel parameter)
+//   a_map(maps, u), b_map(maps, u)        maps of unit u's operands
+//   a_mn(u), b_mn(u)                      operand majorness of unit u
+//   num_units(), tiles_in_unit(u), k_blocks(u), coords(u, q, ...)
+//   EpiState, epi_begin / epi_tile / epi_end
+// TwoMaps serves the single-role policies.
+struct TwoMaps {
+    CUtensorMap a, b;
+};
+
+// Mixin for policies whose every unit has the same operand layouts and maps.
+template <bool AMN, bool BMN>
+struct SingleRole {
+    using Maps = TwoMaps;
+    static constexpr bool kAMn = AMN;
+    static constexpr bool kBMn = BMN;
+    __device__ static void prefetch(const Maps& m) {
+        prefetch_tensormap(&m.a);
+        prefetch_tensormap(&m.b);
+    }
+    __device__ static const CUtensorMap* a_map(const Maps& m, int) { return &m.a; }
+    __device__ static const CUtensorMap* b_map(const Maps& m, int) { return &m.b; }
+    __device__ static bool a_mn(int) { return AMN; }
+    __device__ static bool b_mn(int) { return BMN; }
+};
+
 // Grouped raster of a rows x cols grid of work units: units are visited
 // group by group, a group being `group` consecutive rows (the last group may
 // be shorter) times every column, with the row index running fastest inside a
@@ -100,8 +141,8 @@ __device__ __forceinline__ void report_error(uint32_t* err, uint32_t bits) {
 
 template <class P>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    gemm_persistent_kernel(const __grid_constant__ CUtensorMap map_a,
-                           const __grid_constant__ CUtensorMap map_b, const P p, uint32_t* err) {
+    gemm_persistent_kernel(const __grid_constant__ typename P::Maps maps, const P p,
+                           uint32_t* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -121,8 +162,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int lane = threadIdx.x & 31;
 
     if (warp == 0 && lane == 0) {
-        prefetch_tensormap(&map_a);
-        prefetch_tensormap(&map_b);
+        P::prefetch(maps);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
@@ -147,7 +187,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t tmem_base = *tmem_holder;
 
     const int units = p.num_units();
-    const int kblocks = p.k_blocks();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -157,6 +196,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             bool ok = true;
             for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
                 const int nt = p.tiles_in_unit(u);
+                const int kblocks = p.k_blocks(u);
+                const bool amn = p.a_mn(u), bmn = p.b_mn(u);
+                const CUtensorMap* ma = p.a_map(maps, u);
+                const CUtensorMap* mb = p.b_map(maps, u);
                 for (int q = 0; ok && q < nt; ++q) {
                     int a_mn, a_k, b_mn, b_k;
                     p.coords(u, q, a_mn, a_k, b_mn, b_k);
@@ -166,10 +209,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             break;
                         }
                         mbar_arrive_expect_tx(&full[stage], kStageBytes);
-                        load_operand<P::kAMn, kBM>(a_stages + stage * kAStageBytes, &map_a,
-                                                   &full[stage], a_mn, a_k + kb * kBK);
-                        load_operand<P::kBMn, kBN>(b_stages + stage * kBStageBytes, &map_b,
-                                                   &full[stage], b_mn, b_k + kb * kBK);
+                        load_operand_rt<kBM>(amn, a_stages + stage * kAStageBytes, ma,
+                                             &full[stage], a_mn, a_k + kb * kBK);
+                        load_operand_rt<kBN>(bmn, b_stages + stage * kBStageBytes, mb,
+                                             &full[stage], b_mn, b_k + kb * kBK);
                         issued_mask |= 1u << stage;
                         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                         if (++stage == kStages) {
@@ -190,13 +233,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, P::kAMn, P::kBMn);
             int stage = 0;
             uint32_t phase = 0;
             uint32_t tile_i = 0;
             bool ok = true;
             for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
                 const int nt = p.tiles_in_unit(u);
+                const int kblocks = p.k_blocks(u);
+                const bool amn = p.a_mn(u), bmn = p.b_mn(u);
+                const uint32_t idesc = idesc_bf16_f32(kBM, kBN, amn, bmn);
                 for (int q = 0; ok && q < nt; ++q, ++tile_i) {
                     const uint32_t buf = tile_i & 1u;
                     const uint32_t use = tile_i >> 1;
@@ -216,8 +261,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         const uint32_t b_addr = smem_u32(b_stages + stage * kBStageBytes);
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; ++kk) {
-                            mma_bf16_ss(d_tmem, operand_desc<P::kAMn>(a_addr, kk),
-                                        operand_desc<P::kBMn>(b_addr, kk), idesc,
+                            mma_bf16_ss(d_tmem, operand_desc_rt(amn, a_addr, kk),
+                                        operand_desc_rt(bmn, b_addr, kk), idesc,
                                         (kb > 0 || kk > 0) ? 1u : 0u);
                         }
                         mma_commit(&empty[stage]);

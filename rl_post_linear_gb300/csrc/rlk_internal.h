@@ -32,17 +32,26 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Forward workspace: per (vocab chunk, row) partials {max s, sum 2^((s-max)k)},
 // then the target logit per row.
-// (With entropy, a third per (chunk, row) partial: sum 2^((s-max)k) s.)
+// (With entropy, a third per (chunk, row) partial: sum 2^((s-max)k) s.)  For a
+// masked batch the active rows are compacted first: the row lists, the active
+// count and the compacted copy of h [N, H] follow.
+constexpr int kCompactBlock = 1024;
 struct FwdLayout {
     int64_t num_chunks;
-    size_t partial_off, partial_a_off, target_off, total;
-    FwdLayout(int64_t N, int64_t V) {
+    size_t partial_off, partial_a_off, target_off, rows_off, pos_off, blk_off, count_off, hc_off,
+        total;
+    FwdLayout(int64_t N, int64_t H, int64_t V) {
         const int64_t vt = (V + kTileV - 1) / kTileV;
         num_chunks = (vt + kFwdTilesPerChunk - 1) / kFwdTilesPerChunk;
         partial_off = 0;
         partial_a_off = align_up(static_cast<size_t>(num_chunks) * N * 8, 256);
         target_off = align_up(partial_a_off + static_cast<size_t>(num_chunks) * N * 4, 256);
-        total = align_up(target_off + static_cast<size_t>(N) * 4, 256);
+        rows_off = align_up(target_off + static_cast<size_t>(N) * 4, 256);
+        pos_off = align_up(rows_off + static_cast<size_t>(N) * 4, 256);
+        blk_off = align_up(pos_off + static_cast<size_t>(N) * 4, 256);
+        count_off = align_up(blk_off + static_cast<size_t>((N + kCompactBlock - 1) / kCompactBlock) * 4, 256);
+        hc_off = align_up(count_off + 4, 256);
+        total = align_up(hc_off + static_cast<size_t>(N) * H * 2, 256);
     }
 };
 
@@ -86,10 +95,17 @@ inline size_t audit_v3_blocks(int64_t N) {
 }
 
 // Launchers (return the first CUDA error, cudaSuccess otherwise).
+// rows / n_rows / pos_of: the compaction of a masked batch (all nullptr when the
+// GEMM runs over the original rows).
 cudaError_t launch_fwd(const CUtensorMap& map_h, const CUtensorMap& map_w,
                        const int64_t* targets, const uint8_t* mask, int N, int H, int V,
                        float k_log2e_over_t, float* logp, float* lse, float* entropy,
-                       void* workspace, uint32_t* err, int num_sms, cudaStream_t stream);
+                       void* workspace, const int* rows, const int* n_rows, const int* pos_of,
+                       uint32_t* err, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_compact(const uint8_t* mask, int N, int H, const void* hidden, void* hidden_c,
+                           int* blk_count, int* rows, int* pos_of, int* n_active,
+                           cudaStream_t stream);
 
 cudaError_t launch_fwd_partials(const CUtensorMap& map_h, const CUtensorMap& map_w,
                                 const int64_t* targets, const uint8_t* mask, int N, int H,
@@ -104,31 +120,45 @@ inline int64_t fwd_num_chunks(int64_t V) {
     return ((V + kTileV - 1) / kTileV + kFwdTilesPerChunk - 1) / kFwdTilesPerChunk;
 }
 
-struct BwdMaps {
+// One backward launch: any of the dS recompute of produce_chunk and the dh / dW
+// GEMMs of consume_chunk (the library launches one role at a time).
+struct BwdStepMaps {
     CUtensorMap h_kmajor;      // hidden [N,H], box {64, 128}: A of the dS recompute
     CUtensorMap w_kmajor;      // weight [V,H], box {64, 256}: B of the dS recompute
     CUtensorMap w_mnmajor;     // weight [V,H], box {64, 64}:  B of the dh GEMM
     CUtensorMap h_mnmajor;     // hidden [N,H], box {64, 64}:  B of the dW GEMM
+    CUtensorMap ds_kmajor;     // consumed dS [N, width], box {64, 128}: A of the dh GEMM
+    CUtensorMap ds_mnmajor;    // consumed dS [N, width], box {64, 64}:  A of the dW GEMM
 };
 
-// Tensor maps over the dS chunk depend on the chunk width; the host builds
-// them per chunk through this callback-free pair.
-struct ChunkMaps {
-    CUtensorMap ds_kmajor;     // dS [N, width], box {64, 128}: A of the dh GEMM
-    CUtensorMap ds_mnmajor;    // dS [N, width], box {64, 64}:  A of the dW GEMM
+// One launch of the backward: a role (the dS recompute, the dh GEMM or the dW
+// GEMM) over one vocabulary chunk.
+constexpr int kRoleDs = 0, kRoleDh = 1, kRoleDw = 2;
+struct BwdStep {
+    const int64_t* targets;
+    const uint8_t* mask;
+    const float* grad;
+    const float* grad_ent;     // entropy gradient, or nullptr
+    const float* ent;          // forward entropy, or nullptr
+    const float* lse;
+    const void* hidden;
+    const void* weight;
+    int N, H, V, num_chunks;
+    int chunk, role;
+    float k, temp;
+    void* ds;                  // dS [N, kBwdChunk] bf16 of the chunk
+    float* dh_acc;
+    const int* sorted_y;
+    const int* sorted_t;
+    void* dhidden;
+    void* dweight;
 };
 
 cudaError_t launch_target_sort(const int64_t* targets, const uint8_t* mask, int N, int V,
                                int* sorted_y, int* sorted_t, uint32_t* err, cudaStream_t stream);
 
-cudaError_t launch_bwd_chunk(const BwdMaps& maps, const ChunkMaps& cmaps, const int64_t* targets,
-                             const uint8_t* mask, const float* grad, const float* grad_ent,
-                             const float* ent, const float* lse,
-                             const void* hidden, const void* weight, int N, int H, int V,
-                             int chunk, int num_chunks, float k_log2e_over_t, float inv_t,
-                             void* ds, float* dh_acc, const int* sorted_y, const int* sorted_t,
-                             void* dhidden, void* dweight, uint32_t* err, int num_sms,
-                             cudaStream_t stream);
+cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& step, int num_sms,
+                            uint32_t* err, cudaStream_t stream);
 
 cudaError_t launch_audit(const float* logp_new, const float* logp_old, const uint8_t* mask,
                          int64_t N, rlk_audit_result_t* result, void* workspace, bool vec_ok,

@@ -41,12 +41,14 @@ def test_contract_and_status_strings(lib):
 
 def test_workspace_queries(lib):
     # forward: 1024-column vocab chunks, (max, sum) float2 and the entropy sum per chunk and
-    # row, plus a target logit
-    n, v = 8192, 151936
+    # row, plus a target logit; then the compaction of a masked batch: two int32 row lists,
+    # per-1024-row block counts, the active count and the compacted bf16 copy of h
+    n, v, h = 8192, 151936, 4096
+    up = lambda x: -(-x // 256) * 256
     chunks = -(-(-(-v // 256)) // 4)
-    expect = (-(-(chunks * n * 8) // 256) * 256 + -(-(chunks * n * 4) // 256) * 256
-              + -(-(n * 4) // 256) * 256)
-    assert rlk.rlk_linear_logp_fwd_workspace_bytes(n, 4096, v) == expect
+    expect = (up(chunks * n * 8) + up(chunks * n * 4) + up(n * 4) + 2 * up(n * 4)
+              + up(-(-n // 1024) * 4) + up(4) + up(n * h * 2))
+    assert rlk.rlk_linear_logp_fwd_workspace_bytes(n, h, v) == expect
     # backward: dS chunk [N, 16384] bf16 + fp32 dh accumulator + two int32 lists
     assert rlk.rlk_linear_logp_bwd_workspace_bytes(n, 4096, v) >= n * 16384 * 2 + n * 4096 * 4
     assert rlk.rlk_dlogp_audit_workspace_bytes(0) >= 256

@@ -106,6 +106,31 @@ def test_duplicate_rows_and_batch_invariance():
     assert same_bits(p, full[perm]) and same_bits(lp, lfull[perm])
 
 
+def test_masked_rows_compacted_without_changing_bits():
+    # A masked batch runs the GEMM over its active rows only, gathered in token order; a
+    # row's result must not depend on that, nor on how many rows are active.
+    n, h, v = 700, 256, 5000
+    hidden = wl.normal_bf16((n, h), 6, wl.S_HIDDEN)
+    weight = wl.normal_bf16((v, h), 6, wl.S_WEIGHT, std=0.05)
+    targets = wl.uniform_targets(n, v, 6)
+    full, lfull, _ = _run(hidden, weight, targets, None, 0.9)
+    ones, lones, err = _run(hidden, weight, targets, torch.ones(n, dtype=torch.uint8), 0.9)
+    assert err == 0 and same_bits(ones, full) and same_bits(lones, lfull)
+    for density in (0.03, 0.5, 0.97):
+        mask = torch.from_numpy((np.random.default_rng(int(density * 100)).random(n) < density)
+                                .astype(np.uint8))
+        part, lpart, err = _run(hidden, weight, targets, mask, 0.9)
+        act = mask > 0
+        assert err == 0 and same_bits(part[act], full[act]) and same_bits(lpart[act], lfull[act])
+        assert torch.all(part[~act] == 0) and torch.all(lpart[~act] == 0)
+    last = torch.zeros(n, dtype=torch.uint8)
+    last[n - 1] = 1
+    one, lone, _ = _run(hidden, weight, targets, last, 0.9)
+    assert same_bits(one[n - 1:], full[n - 1:]) and torch.all(one[:n - 1] == 0)
+    none, lnone, err = _run(hidden, weight, targets, torch.zeros(n, dtype=torch.uint8), 0.9)
+    assert err == 0 and torch.all(none == 0) and torch.all(lnone == 0)
+
+
 def test_invalid_targets_flagged_and_inactive_targets_unread():
     n, h, v = 40, 64, 500
     hidden = wl.normal_bf16((n, h), 4, wl.S_HIDDEN)
