@@ -196,7 +196,7 @@ def run_ours(args, world, rank, local):
     ws_l = torch.empty(rlk.rlk_grpo_clip_loss_workspace_bytes(n), dtype=torch.uint8, device=dev)
     loss_res = torch.empty(rlk.GRPO_RESULT_BYTES, dtype=torch.uint8, device=dev)
     scale = 1.0 / n_act                         # token mean over the batch's active tokens
-    n_chunks = -(-v // 16384)
+    n_chunks = -(-v // 32768)
     # forward: row compaction (2, the step passes a mask) + GEMM + merge; loss 2; audit 2;
     # backward: target sort + one launch per role and vocab chunk
     launches_per_step = 4 + 2 + 2 + 1 + 3 * n_chunks
@@ -289,7 +289,7 @@ def run_ours(args, world, rank, local):
     audit_gbs = n * 26 / (aud_ms * 1e-3) / 1e9
     # roofline: the forward GEMM is the largest single launch, and the only GEMM whose entry
     # point holds one GEMM launch (plus a 0.4% merge), so events around it time it directly;
-    # the backward group (30 GEMM launches + the target sort) is reported beside it
+    # the backward group (15 GEMM launches + the target sort) is reported beside it
     out = {
         "metric": METRIC,
         "value": tok / (ms_step * 1e-3),

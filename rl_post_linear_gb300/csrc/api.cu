@@ -460,7 +460,7 @@ const char* rlk_contract_string(void) {
     return "rlk-gb300 linear_logp v1; arch=sm_103a; nvcc=" RLK_STR(__CUDACC_VER_MAJOR__) "." RLK_STR(
         __CUDACC_VER_MINOR__) "; inputs=bf16; accum=fp32 (tcgen05 kind::f16, TMEM); "
                               "tile=128x256x64 cta_group::1, no split-K; "
-                              "fwd_vocab_chunk=1024 (merge ascending); bwd_vocab_chunk=16384; masked batches: active rows compacted (ascending) before the GEMM; "
+                              "fwd_vocab_chunk=1024 (merge ascending); bwd_vocab_chunk=32768; masked batches: active rows compacted (ascending) before the GEMM; "
                               "exp=ex2.approx.ftz, log=lg2.approx.ftz; k=fp32(log2(e)/T); "
                               "logits never rounded; logp/lse fp32; dS bf16 (target term fp32); "
                               "dh/dW rounded once to bf16 (RNE); no float atomics; "

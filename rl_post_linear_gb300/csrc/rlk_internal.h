@@ -16,7 +16,7 @@ constexpr int kTileM = 128;                 // tokens per accumulator tile
 constexpr int kTileV = 256;                 // vocab (or hidden) columns per tile
 constexpr int kFwdTilesPerChunk = 4;        // forward vocab chunk = 1024 columns
 constexpr int kFwdChunk = kFwdTilesPerChunk * kTileV;
-constexpr int kBwdChunk = 16384;            // backward vocab chunk (multiple of kTileV)
+constexpr int kBwdChunk = 32768;            // backward vocab chunk (multiple of kTileV)
 // Raster groups (visiting order only; no effect on any result): token tiles per
 // group for the forward and dS GEMMs, hidden tiles per group for the dW GEMM.
 // A group's share of h (32 x 128 rows, or 8 x 256 columns, of H = 4096) is

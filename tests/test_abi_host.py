@@ -49,8 +49,8 @@ def test_workspace_queries(lib):
     expect = (up(chunks * n * 8) + up(chunks * n * 4) + up(n * 4) + 2 * up(n * 4)
               + up(-(-n // 1024) * 4) + up(4) + up(n * h * 2))
     assert rlk.rlk_linear_logp_fwd_workspace_bytes(n, h, v) == expect
-    # backward: dS chunk [N, 16384] bf16 + fp32 dh accumulator + two int32 lists
-    assert rlk.rlk_linear_logp_bwd_workspace_bytes(n, 4096, v) >= n * 16384 * 2 + n * 4096 * 4
+    # backward: dS chunk [N, 32768] bf16 + fp32 dh accumulator + two int32 lists
+    assert rlk.rlk_linear_logp_bwd_workspace_bytes(n, 4096, v) >= n * 32768 * 2 + n * 4096 * 4
     assert rlk.rlk_dlogp_audit_workspace_bytes(0) >= 256
     assert rlk.rlk_dlogp_audit_workspace_bytes(9400614) >= 2296 * 40
     assert rlk.rlk_linear_logp_fwd_workspace_bytes(-1, 64, 10) == 0

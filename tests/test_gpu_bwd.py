@@ -62,8 +62,8 @@ def test_tiny_parity():
     assert torch.all(dh[w.mask == 0] == 0)
 
 
-@pytest.mark.parametrize("n,h,v,T", [(300, 128, 20000, 0.7), (129, 256, 1000, 1.0),
-                                     (70, 64, 16384 + 300, 1.5)])
+@pytest.mark.parametrize("n,h,v,T", [(300, 128, 40000, 0.7), (129, 256, 1000, 1.0),
+                                     (70, 64, 2 * 32768 + 300, 1.5)])
 def test_multi_chunk_ragged_parity(n, h, v, T):
     hidden, weight, targets, mask, grad = _case(n, h, v, n + h + v)
     targets[5] = targets[6] = targets[40] = 17          # a vocab row hit by several tokens
