@@ -197,9 +197,9 @@ def run_ours(args, world, rank, local):
     loss_res = torch.empty(rlk.GRPO_RESULT_BYTES, dtype=torch.uint8, device=dev)
     scale = 1.0 / n_act                         # token mean over the batch's active tokens
     n_chunks = -(-v // 32768)
-    # forward: row compaction (2, the step passes a mask) + GEMM + merge; loss 2; audit 2;
-    # backward: target sort + one launch per role and vocab chunk
-    launches_per_step = 4 + 2 + 2 + 1 + 3 * n_chunks
+    # forward: row compaction (3, the step passes a mask) + GEMM + merge; loss 2; audit 2;
+    # backward: target sort (2) + one launch per role and vocab chunk
+    launches_per_step = 5 + 2 + 2 + 2 + 3 * n_chunks
 
     def step(ev=None, old_t=old, adv_t=advd):
         if ev is not None:

@@ -211,8 +211,9 @@ static rlk_status_t bwd_impl(const void* hidden, const void* weight, const int64
     RLK_TRY(make_map(&maps.h_mnmajor, hidden, H, N, H * 2, 64, 64));
 
     const int n = static_cast<int>(N), h = static_cast<int>(H), v = static_cast<int>(V);
-    RLK_CUDA(rlk::launch_target_sort(targets, active_mask, n, v, sorted_y, sorted_t,
-                                     device_error_word, stream));
+    RLK_CUDA(rlk::launch_target_sort(targets, active_mask, n, v,
+                                     reinterpret_cast<uint64_t*>(ws + lay.tiles_off), sorted_y,
+                                     sorted_t, device_error_word, stream));
     const int num_chunks = static_cast<int>((V + rlk::kBwdChunk - 1) / rlk::kBwdChunk);
     rlk::BwdStep st;
     st.targets = targets;

@@ -12,8 +12,8 @@
 // 1024-row block; kernel 2 gives each block its offset as the sum of the counts
 // before it (ascending block order), places the block's active rows by warp
 // ballots (ascending token order), records rows[pos] = t and pos_of[t] = pos
-// (-1 for inactive rows), copies the rows of h, and block 0 stores the active
-// count.
+// (-1 for inactive rows), and block 0 stores the active count; kernel 3 copies
+// the active rows of h, one warp per row over a grid that covers every row.
 #include "rlk_internal.h"
 
 namespace rlk {
@@ -38,9 +38,8 @@ __global__ void __launch_bounds__(kCompactThreads)
 }
 
 __global__ void __launch_bounds__(kCompactThreads)
-    compact_place_kernel(const uint8_t* __restrict__ mask, int N, int H,
+    compact_place_kernel(const uint8_t* __restrict__ mask, int N,
                          const int* __restrict__ blk_count, int num_blocks,
-                         const uint4* __restrict__ hidden, uint4* __restrict__ hidden_c,
                          int* __restrict__ rows, int* __restrict__ pos_of,
                          int* __restrict__ n_active) {
     __shared__ int s_base;
@@ -75,19 +74,22 @@ __global__ void __launch_bounds__(kCompactThreads)
         pos_of[t] = act ? pos : -1;
         if (act) rows[pos] = t;
     }
-    // copy the block's active rows of h: one warp per row, 16 bytes per lane
+}
+
+constexpr int kGatherWarps = 8;             // rows per block of the copy
+
+// hidden_c[i] = hidden[rows[i]] for i < n_active: one warp per row, 16 bytes
+// per lane and access
+__global__ void __launch_bounds__(kGatherWarps * 32)
+    compact_gather_kernel(const int* __restrict__ rows, const int* __restrict__ n_active, int H,
+                          const uint4* __restrict__ hidden, uint4* __restrict__ hidden_c) {
+    const int i = blockIdx.x * kGatherWarps + (threadIdx.x >> 5);
+    if (i >= *n_active) return;
+    const int lane = threadIdx.x & 31;
     const int vec_per_row = H / 8;
-    __shared__ int s_pos[kCompactThreads];
-    s_pos[threadIdx.x] = act ? pos : -1;
-    __syncthreads();
-    for (int r = warp; r < kCompactThreads; r += kCompactThreads / 32) {
-        const int p = s_pos[r];
-        if (p < 0) continue;
-        const int tr = blockIdx.x * kCompactThreads + r;
-        const uint4* src = hidden + static_cast<size_t>(tr) * vec_per_row;
-        uint4* dst = hidden_c + static_cast<size_t>(p) * vec_per_row;
-        for (int j = lane; j < vec_per_row; j += 32) dst[j] = src[j];
-    }
+    const uint4* src = hidden + static_cast<size_t>(rows[i]) * vec_per_row;
+    uint4* dst = hidden_c + static_cast<size_t>(i) * vec_per_row;
+    for (int j = lane; j < vec_per_row; j += 32) dst[j] = src[j];
 }
 
 }  // namespace
@@ -99,9 +101,12 @@ cudaError_t launch_compact(const uint8_t* mask, int N, int H, const void* hidden
     compact_count_kernel<<<blocks, kCompactThreads, 0, stream>>>(mask, N, blk_count);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    compact_place_kernel<<<blocks, kCompactThreads, 0, stream>>>(
-        mask, N, H, blk_count, blocks, static_cast<const uint4*>(hidden),
-        static_cast<uint4*>(hidden_c), rows, pos_of, n_active);
+    compact_place_kernel<<<blocks, kCompactThreads, 0, stream>>>(mask, N, blk_count, blocks, rows,
+                                                                 pos_of, n_active);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    compact_gather_kernel<<<(N + kGatherWarps - 1) / kGatherWarps, kGatherWarps * 32, 0, stream>>>(
+        rows, n_active, H, static_cast<const uint4*>(hidden), static_cast<uint4*>(hidden_c));
     return cudaGetLastError();
 }
 

@@ -56,15 +56,19 @@ struct FwdLayout {
 };
 
 // Backward workspace: dS for one vocab chunk [N, kBwdChunk] bf16, the fp32 dh
-// accumulator [N, H], and the (target, token) list sorted by target.
+// accumulator [N, H], the (target, token) list sorted by target, and the
+// sorted key tiles the list is built from.
+constexpr int kTargetSortTile = 2048;
 struct BwdLayout {
-    size_t ds_off, dhacc_off, sorted_y_off, sorted_t_off, total;
+    size_t ds_off, dhacc_off, sorted_y_off, sorted_t_off, tiles_off, total;
     BwdLayout(int64_t N, int64_t H) {
         ds_off = 0;
         dhacc_off = align_up(static_cast<size_t>(N) * kBwdChunk * 2, 256);
         sorted_y_off = align_up(dhacc_off + static_cast<size_t>(N) * H * 4, 256);
         sorted_t_off = align_up(sorted_y_off + static_cast<size_t>(N) * 4, 256);
-        total = align_up(sorted_t_off + static_cast<size_t>(N) * 4, 256);
+        tiles_off = align_up(sorted_t_off + static_cast<size_t>(N) * 4, 256);
+        const size_t tiles = static_cast<size_t>((N + kTargetSortTile - 1) / kTargetSortTile);
+        total = align_up(tiles_off + tiles * kTargetSortTile * 8, 256);
     }
 };
 
@@ -155,7 +159,8 @@ struct BwdStep {
 };
 
 cudaError_t launch_target_sort(const int64_t* targets, const uint8_t* mask, int N, int V,
-                               int* sorted_y, int* sorted_t, uint32_t* err, cudaStream_t stream);
+                               uint64_t* tiles, int* sorted_y, int* sorted_t, uint32_t* err,
+                               cudaStream_t stream);
 
 cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& step, int num_sms,
                             uint32_t* err, cudaStream_t stream);

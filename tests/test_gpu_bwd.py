@@ -91,3 +91,23 @@ def test_dh_batch_invariance_and_dw_determinism():
     for a, b in ((0, 1), (0, 128), (100, 300), (17, 211)):
         dhp, _, _, _ = _gpu(hidden[a:b], weight, targets[a:b], mask[a:b], grad[a:b], 0.7)
         assert same_bits(dhp, dh[a:b]), (a, b)
+
+
+def test_target_terms_across_sort_tiles():
+    # More tokens than one 2048-key sort tile, a ragged last tile, every vocab row hit by
+    # about a dozen tokens in different tiles, and unread invalid targets on inactive rows.
+    n, h, v = 5000, 64, 300
+    hidden, weight, targets, mask, grad = _case(n, h, v, 21, std=0.2, active=0.8)
+    inactive = np.nonzero(mask.numpy() == 0)[0]
+    targets[torch.from_numpy(inactive[::3])] = -5
+    targets[torch.from_numpy(inactive[1::3])] = v + 7
+    dh, dw, _, err = _gpu(hidden, weight, targets, mask, grad, 0.9)
+    assert err == 0
+    dh_o, dw_o = _oracle(hidden, weight, targets, mask, grad, 0.9)
+    e_dh, e_dw = rel_l2(dh, dh_o), rel_l2(dw, dw_o)
+    print("bwd parity n=%d v=%d (3 sort tiles): rel-L2 dh %.3e dw %.3e" % (n, v, e_dh, e_dw))
+    assert e_dh <= GRAD_REL_L2 and e_dw <= GRAD_REL_L2
+    # dh rows are per token: permuting the tokens permutes dh bit for bit
+    perm = torch.from_numpy(np.random.default_rng(1).permutation(n))
+    dhp, _, _, _ = _gpu(hidden[perm], weight, targets[perm], mask[perm], grad[perm.numpy()], 0.9)
+    assert same_bits(dhp, dh[perm])
