@@ -16,7 +16,8 @@ steps.
 Output: one JSON line (rank 0).  ``value`` is whole-job active tokens per
 second with inputs resident in HBM; ``e2e`` is the same metric through the C
 ABI with the per-step inputs copied from pinned host memory and the result
-read back inside the timed region.  ``--impl reference`` times the fp64 CPU
+read back inside the timed region (step i+1's inputs are copied on a second
+stream while step i computes, into the other of two device input sets).  ``--impl reference`` times the fp64 CPU
 oracle on a bounded token sample of the same workload instead.
 
 Multi-GPU (torchrun): every rank scores its own batch (seed + rank); there is
@@ -201,18 +202,19 @@ def run_ours(args, world, rank, local):
     # backward: target sort (2) + one launch per role and vocab chunk
     launches_per_step = 5 + 2 + 2 + 2 + 3 * n_chunks
 
-    def step(ev=None, old_t=old, adv_t=advd):
+    def step(ev=None, ins=None):
+        h_t, y_t, m_t, old_t, adv_t = ins if ins is not None else (hid, y, mask, old, advd)
         if ev is not None:
             ev[0].record(stream)
-        rlk.rlk_linear_logp_fwd(hid, wt, y, mask, T, logp, lse, ws_f, err)
+        rlk.rlk_linear_logp_fwd(h_t, wt, y_t, m_t, T, logp, lse, ws_f, err)
         if ev is not None:
             ev[1].record(stream)
-        rlk.rlk_grpo_clip_loss(logp, old_t, adv_t, mask, GRPO_EPS, GRPO_EPS, scale, g, loss_res,
+        rlk.rlk_grpo_clip_loss(logp, old_t, adv_t, m_t, GRPO_EPS, GRPO_EPS, scale, g, loss_res,
                                ws_l)
-        rlk.rlk_dlogp_audit(logp, old_t, mask, audit, ws_a)
+        rlk.rlk_dlogp_audit(logp, old_t, m_t, audit, ws_a)
         if ev is not None:
             ev[2].record(stream)
-        rlk.rlk_linear_logp_bwd(hid, wt, y, mask, g, lse, T, dh, dw, ws_b, err)
+        rlk.rlk_linear_logp_bwd(h_t, wt, y_t, m_t, g, lse, T, dh, dw, ws_b, err)
         if ev is not None:
             ev[3].record(stream)
 
@@ -248,26 +250,44 @@ def run_ours(args, world, rank, local):
     logp_host = torch.empty(n, dtype=torch.float32).pin_memory()
     audit_host = torch.empty(rlk.AUDIT_RESULT_BYTES, dtype=torch.uint8).pin_memory()
     loss_host = torch.empty(rlk.GRPO_RESULT_BYTES, dtype=torch.uint8).pin_memory()
-    old_d, adv_d = torch.empty_like(old), torch.empty_like(advd)
+    # Two device input sets: step i+1's inputs are copied on a second stream while step i
+    # computes (a trainer's prefetch); every copy still lies inside the timed region.
+    sets = [(torch.empty_like(hid), torch.empty_like(y), torch.empty_like(mask),
+             torch.empty_like(old), torch.empty_like(advd)) for _ in range(2)]
+    hosts = (h_host, y_host, m_host, old_host, adv_host)
+    copy_stream = torch.cuda.Stream(device=dev)
+    ready = [torch.cuda.Event() for _ in range(2)]
+    free = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        hid.copy_(h_host, non_blocking=True)
-        y.copy_(y_host, non_blocking=True)
-        mask.copy_(m_host, non_blocking=True)
-        old_d.copy_(old_host, non_blocking=True)
-        adv_d.copy_(adv_host, non_blocking=True)
-        step(None, old_d, adv_d)
-        logp_host.copy_(logp, non_blocking=True)
-        audit_host.copy_(audit, non_blocking=True)
-        loss_host.copy_(loss_res, non_blocking=True)
+    def prefetch(i):
+        b = i % 2
+        with torch.cuda.stream(copy_stream):
+            if i >= 2:
+                copy_stream.wait_event(free[b])      # step i-2 is done with this set
+            for dst, src in zip(sets[b], hosts):
+                dst.copy_(src, non_blocking=True)
+            ready[b].record(copy_stream)
 
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
+    def e2e_run(k, begin=None):
+        if begin is not None:
+            copy_stream.wait_event(begin)
+        prefetch(0)
+        for i in range(k):
+            if i + 1 < k:
+                prefetch(i + 1)
+            b = i % 2
+            stream.wait_event(ready[b])
+            step(None, sets[b])
+            free[b].record(stream)
+            logp_host.copy_(logp, non_blocking=True)
+            audit_host.copy_(audit, non_blocking=True)
+            loss_host.copy_(loss_res, non_blocking=True)
+
+    e2e_run(max(1, args.warmup))
     torch.cuda.synchronize()
     e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e_start.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    e2e_run(args.steps, e_start)
     e_stop.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e_start.elapsed_time(e_stop)
@@ -399,6 +419,19 @@ def measure_audit(rlk, dev, n, hbm_gbs, reps=10):
                    else "inputs larger than L2, no flush")}
 
 
+def run_audit_only():
+    """The audit rows of the workload table alone (for profiling the audit kernels)."""
+    import rl_post_linear_gb300 as rlk
+    from rl_post_linear_gb300 import build as rlk_build
+    rlk_build.build()
+    rlk.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pk = peaks()
+    return {"audit_hbm": {str(na): measure_audit(rlk, dev, na, pk["hbm_gbs"])
+                          for na in (9_400_614, 1 << 26)}}
+
+
 def recorded_traffic(kernel, n, v, h):
     """DRAM bytes per launch of `kernel` at this (N, V, H), from the committed ncu summary
     (profiles/traffic.txt: kernel N V H bytes source-hash), or None if the kernel source has
@@ -512,7 +545,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-second-shape", action="store_true",
                     help="leave out the DeepSeek-shaped forward measurement")
+    ap.add_argument("--audit-only", action="store_true",
+                    help="time only the masked audit at N = 9,400,614 and 2^26 (one GPU)")
     args = ap.parse_args()
+    if args.audit_only:
+        print(json.dumps(run_audit_only()))
+        return
     world, rank, local = dist_env()
     if world > 1 and args.impl == "ours":
         torch.distributed.init_process_group("nccl")

@@ -153,6 +153,32 @@ __device__ __forceinline__ void visit3(float nw, float od, uint32_t m, int off, 
     a.flags |= (key > 0x7f800000u) ? 1u : 0u;    // |d| is inf or NaN
 }
 
+// Branch-free visit for the vector path: an inactive element contributes d = 0
+// to the sums (kl_term(0) = 0 exactly) and key 0 to the running max.
+struct GroupAcc {
+    uint32_t key = 0;
+    int arg = -1;
+    float sd = 0.f, skl = 0.f;
+};
+
+__device__ __forceinline__ void visit_group(float nw, float od, bool act, int off, GroupAcc& g,
+                                            uint32_t& flags) {
+    const float d = act ? nw - od : 0.f;
+    const uint32_t key = act ? abs_key(d) : 0u;
+    const bool better = key > g.key;
+    g.key = better ? key : g.key;
+    g.arg = better ? off : g.arg;
+    g.sd += d;
+    g.skl += kl_term(d);
+    flags |= (key > 0x7f800000u) ? 1u : 0u;      // |d| is inf or NaN
+}
+
+// number of nonzero bytes in a word of four mask bytes
+__device__ __forceinline__ int active_bytes(uint32_t m) {
+    const uint32_t hi = ((m & 0x7f7f7f7fu) + 0x7f7f7f7fu) | m;
+    return __popc(hi & 0x80808080u);
+}
+
 template <bool VEC>
 __global__ void __launch_bounds__(kAuditThreads)
     audit_pass1(const float* __restrict__ nw, const float* __restrict__ od,
@@ -174,14 +200,28 @@ __global__ void __launch_bounds__(kAuditThreads)
             m[j] = mask == nullptr ? 0x01010101u
                                    : __ldcs(reinterpret_cast<const unsigned int*>(mask + i0));
         }
+        // One accumulator per float4 group, so that the four groups' dependency chains
+        // (sums, running max) interleave; the groups are then merged in ascending order,
+        // which keeps the first index on ties (group j's offsets precede group j+1's).
+        GroupAcc g[kVec];
 #pragma unroll
         for (int j = 0; j < kVec; ++j) {
             const int o = j * (kAuditThreads * 4) + threadIdx.x * 4;
-            visit3(x[j].x, y[j].x, m[j] & 0xffu, o, a);
-            visit3(x[j].y, y[j].y, (m[j] >> 8) & 0xffu, o + 1, a);
-            visit3(x[j].z, y[j].z, (m[j] >> 16) & 0xffu, o + 2, a);
-            visit3(x[j].w, y[j].w, m[j] >> 24, o + 3, a);
+            a.count += active_bytes(m[j]);
+            visit_group(x[j].x, y[j].x, (m[j] & 0xffu) != 0, o, g[j], a.flags);
+            visit_group(x[j].y, y[j].y, (m[j] & 0xff00u) != 0, o + 1, g[j], a.flags);
+            visit_group(x[j].z, y[j].z, (m[j] & 0xff0000u) != 0, o + 2, g[j], a.flags);
+            visit_group(x[j].w, y[j].w, (m[j] & 0xff000000u) != 0, o + 3, g[j], a.flags);
         }
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+            const bool better = g[j].key > a.key;
+            a.key = better ? g[j].key : a.key;
+            a.arg = better ? g[j].arg : a.arg;
+        }
+        static_assert(kVec == 4, "the fixed summation tree below assumes four groups");
+        a.sd = (g[0].sd + g[1].sd) + (g[2].sd + g[3].sd);
+        a.skl = (g[0].skl + g[1].skl) + (g[2].skl + g[3].skl);
     } else {
 #pragma unroll 1
         for (int j = 0; j < kVec; ++j) {
