@@ -25,8 +25,10 @@
  *    dweight) must start on a 16-byte boundary; workspace on 256 bytes.
  *  - Mask bytes: nonzero = active.  A NULL mask means every row is active.
  *    Targets of inactive rows are never read.
- *  - Shapes: H must be a positive multiple of 64; 1 <= V < 2^31;
- *    0 <= N < 2^31.  N = 0 returns RLK_OK without launching anything.
+ *  - Shapes: H must be a positive multiple of 64; 1 <= V <= 2^31 - 2^16;
+ *    0 <= N <= 2^31 - 2^16 (device indices are 32-bit, with headroom for
+ *    rounding N and V up to whole tiles).  N = 0 returns RLK_OK without
+ *    launching anything.
  *  - Errors: argument errors are returned synchronously, before anything is
  *    enqueued; a failed launch returns RLK_ERR_LAUNCH.  There is no fallback
  *    path: an unsupported case is an error, never a silent slower route.

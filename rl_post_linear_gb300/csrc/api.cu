@@ -15,7 +15,8 @@ namespace {
 
 using rlk::align_up;
 
-constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+// 32-bit device indices, with headroom for rounding N and V up to whole tiles
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - (int64_t(1) << 16);
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static std::once_flag once;

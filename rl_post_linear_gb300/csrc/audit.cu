@@ -32,7 +32,15 @@ namespace rlk {
 namespace {
 
 __device__ __forceinline__ float kl_term(float d) {
-    if (fabsf(d) < 0.5f) {
+    if (fabsf(d) < 0.0625f) {          // Taylor series to d^6: truncation below 4e-10 relative
+        float p = 1.0f / 720.0f;
+        p = fmaf(p, d, 1.0f / 120.0f);
+        p = fmaf(p, d, 1.0f / 24.0f);
+        p = fmaf(p, d, 1.0f / 6.0f);
+        p = fmaf(p, d, 0.5f);
+        return d * d * p;
+    }
+    if (fabsf(d) < 0.5f) {             // to d^9: truncation below 3e-8 relative
         float p = 1.0f / 362880.0f;
         p = fmaf(p, d, 1.0f / 40320.0f);
         p = fmaf(p, d, 1.0f / 5040.0f);
@@ -161,8 +169,7 @@ struct GroupAcc {
     float sd = 0.f, skl = 0.f;
 };
 
-__device__ __forceinline__ void visit_group(float nw, float od, bool act, int off, GroupAcc& g,
-                                            uint32_t& flags) {
+__device__ __forceinline__ void visit_group(float nw, float od, bool act, int off, GroupAcc& g) {
     const float d = act ? nw - od : 0.f;
     const uint32_t key = act ? abs_key(d) : 0u;
     const bool better = key > g.key;
@@ -170,7 +177,6 @@ __device__ __forceinline__ void visit_group(float nw, float od, bool act, int of
     g.arg = better ? off : g.arg;
     g.sd += d;
     g.skl += kl_term(d);
-    flags |= (key > 0x7f800000u) ? 1u : 0u;      // |d| is inf or NaN
 }
 
 // number of nonzero bytes in a word of four mask bytes
@@ -208,10 +214,10 @@ __global__ void __launch_bounds__(kAuditThreads)
         for (int j = 0; j < kVec; ++j) {
             const int o = j * (kAuditThreads * 4) + threadIdx.x * 4;
             a.count += active_bytes(m[j]);
-            visit_group(x[j].x, y[j].x, (m[j] & 0xffu) != 0, o, g[j], a.flags);
-            visit_group(x[j].y, y[j].y, (m[j] & 0xff00u) != 0, o + 1, g[j], a.flags);
-            visit_group(x[j].z, y[j].z, (m[j] & 0xff0000u) != 0, o + 2, g[j], a.flags);
-            visit_group(x[j].w, y[j].w, (m[j] & 0xff000000u) != 0, o + 3, g[j], a.flags);
+            visit_group(x[j].x, y[j].x, (m[j] & 0xffu) != 0, o, g[j]);
+            visit_group(x[j].y, y[j].y, (m[j] & 0xff00u) != 0, o + 1, g[j]);
+            visit_group(x[j].z, y[j].z, (m[j] & 0xff0000u) != 0, o + 2, g[j]);
+            visit_group(x[j].w, y[j].w, (m[j] & 0xff000000u) != 0, o + 3, g[j]);
         }
 #pragma unroll
         for (int j = 0; j < kVec; ++j) {
@@ -219,6 +225,9 @@ __global__ void __launch_bounds__(kAuditThreads)
             a.key = better ? g[j].key : a.key;
             a.arg = better ? g[j].arg : a.arg;
         }
+        // an inf or NaN |d| exists exactly when the largest key is above the key of the
+        // largest finite float (NaN and inf rank above every finite |d|)
+        a.flags = a.key > 0x7f800000u ? 1u : 0u;
         static_assert(kVec == 4, "the fixed summation tree below assumes four groups");
         a.sd = (g[0].sd + g[1].sd) + (g[2].sd + g[3].sd);
         a.skl = (g[0].skl + g[1].skl) + (g[2].skl + g[3].skl);

@@ -78,6 +78,8 @@ def test_forward_argument_errors(lib):
     assert _fwd(lib, V=0) == rlk.RLK_ERR_INVALID_VALUE
     assert _fwd(lib, N=-1) == rlk.RLK_ERR_INVALID_VALUE
     assert _fwd(lib, N=1 << 31) == rlk.RLK_ERR_INVALID_VALUE
+    assert _fwd(lib, N=(1 << 31) - (1 << 16) + 1) == rlk.RLK_ERR_INVALID_VALUE
+    assert _fwd(lib, V=(1 << 31) - (1 << 16) + 1) == rlk.RLK_ERR_INVALID_VALUE
     assert _fwd(lib, hidden=None) == rlk.RLK_ERR_INVALID_VALUE
     assert _fwd(lib, targets=None) == rlk.RLK_ERR_INVALID_VALUE
     assert _fwd(lib, logp=None) == rlk.RLK_ERR_INVALID_VALUE
