@@ -349,6 +349,10 @@ def run_ours(args, world, rank, local):
     }
     out["audit_hbm"] = {str(na): measure_audit(rlk, dev, na, pk["hbm_gbs"])
                         for na in (9_400_614, 1 << 26)}
+    if not args.no_next_rows:
+        out["next_rows"] = measure_next_rows(rlk, dev, pk, args.warmup, args.steps,
+                                             (hid, wt, y, mask, T, n_act, logp, g, dh, dw, ws_f,
+                                              ws_b))
     if not args.no_second_shape:
         del hid, wt, dh, dw, ws_b
         torch.cuda.empty_cache()
@@ -356,6 +360,119 @@ def run_ours(args, world, rank, local):
     if not args.no_cpu_baseline and world == 1:
         out["cpu_baseline"] = cpu_baseline(w, noise, adv, args.cpu_tokens)
     return out
+
+
+def _time_calls(fn, warmup, steps, stream):
+    """Mean device time of one call of fn (CUDA events on the launching stream)."""
+    for _ in range(max(3, warmup)):
+        fn()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(steps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def measure_next_rows(rlk, dev, pk, warmup, steps, state):
+    """The rows built after the hot path, each timed alone on the Qwen-shaped batch (or at
+    N = 2^26 for the per-token fragments), against the roofline that bounds it:
+    the vocab-sharded forward (TP = 4 emulated on one GPU: four block launches and the
+    fixed-order merge, checked bitwise against the unsharded logp), the entropy forward and
+    backward, logp from existing fp32 / bf16 logits [8192, 151936], the extended audit and
+    the clipped-ratio loss fragment."""
+    from rl_post_linear_gb300 import tp
+    hid, wt, y, mask, T, n_act, logp_ref, g, dh, dw, ws_f, ws_b = state
+    n, h = hid.shape
+    v = wt.shape[0]
+    stream = torch.cuda.current_stream()
+    peak, hbm = pk["bf16_tflops_sustained"], pk["hbm_gbs"]
+    fwd_flops, bwd_flops = 2.0 * n_act * h * v, 4.0 * n_act * h * v
+    res = {}
+
+    # NEXT-1: TP = 4 emulated
+    shards = tp.vocab_shards(v, 4)
+    total = rlk.rlk_linear_logp_num_partials(v)
+    partials = torch.empty(total, n, 2, dtype=torch.float32, device=dev)
+    tl = torch.zeros(n, dtype=torch.float32, device=dev)
+    lp4, lse4 = torch.empty_like(logp_ref), torch.empty_like(logp_ref)
+
+    def tp_fwd():
+        for start, size in shards:
+            if size == 0:
+                continue
+            c0 = start // tp.CHUNK
+            cnt = rlk.rlk_linear_logp_num_partials(size)
+            rlk.rlk_linear_logp_fwd_shard(hid, wt[start:start + size], y, mask, start, T,
+                                          partials[c0:c0 + cnt], tl)
+        rlk.rlk_linear_logp_merge(partials, total, tl, y, mask, v, T, lp4, lse4)
+
+    ms = _time_calls(tp_fwd, warmup, steps, stream)
+    rlk.rlk_linear_logp_fwd(hid, wt, y, mask, T, logp_ref, None, ws_f)
+    torch.cuda.synchronize()
+    res["tp4_emulated_fwd"] = {
+        "ms": ms, "tflops": fwd_flops / (ms * 1e-3) / 1e12,
+        "frac_of_peak": fwd_flops / (ms * 1e-3) / 1e12 / peak,
+        "bitwise_equal_to_unsharded": bool(torch.equal(lp4.view(torch.int32),
+                                                       logp_ref.view(torch.int32))),
+        "launches": len(shards) + 1}
+    del partials
+
+    # NEXT-3: entropy forward and backward
+    ent = torch.empty_like(logp_ref)
+    lse_e = torch.empty_like(logp_ref)
+    ms_f = _time_calls(lambda: rlk.rlk_linear_logp_entropy_fwd(hid, wt, y, mask, T, lp4, lse_e,
+                                                               ent, ws_f),
+                       warmup, steps, stream)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    g_ent = torch.randn(n, device=dev, generator=gen) / n
+    ms_b = _time_calls(lambda: rlk.rlk_linear_logp_entropy_bwd(hid, wt, y, mask, g, g_ent, lse_e,
+                                                               ent, T, dh, dw, ws_b),
+                       warmup, steps, stream)
+    res["entropy_fwd"] = {"ms": ms_f, "tflops": fwd_flops / (ms_f * 1e-3) / 1e12,
+                          "frac_of_peak": fwd_flops / (ms_f * 1e-3) / 1e12 / peak}
+    res["entropy_bwd"] = {"ms": ms_b, "tflops": bwd_flops / (ms_b * 1e-3) / 1e12,
+                          "frac_of_peak": bwd_flops / (ms_b * 1e-3) / 1e12 / peak}
+
+    # NEXT-4: logp from existing logits, dense rows; bytes = the logits + targets, mask, out
+    for name, dt, es in (("logits_fp32", torch.float32, 4), ("logits_bf16", torch.bfloat16, 2)):
+        logits = (torch.randn(n, v, device=dev, generator=gen) * 2.0).to(dt)
+        nbytes = n * v * es + n * (8 + 1 + 4 + 4)
+        ms = _time_calls(lambda: rlk.rlk_logp_from_logits(logits, None, y, mask, T, lp4, lse4),
+                         warmup, steps, stream)
+        res["logp_from_" + name] = {"ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9,
+                                    "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm,
+                                    "bytes": nbytes, "shape": [n, v]}
+        del logits
+    torch.cuda.empty_cache()
+
+    # NEXT-4 extended audit and NEXT-2 loss fragment at N = 2^26 (inputs larger than L2)
+    na = 1 << 26
+    new, old, m = (t.to(dev) for t in wl.audit_inputs(na, 0))
+    r_ext = torch.empty(rlk.AUDIT_EXT_RESULT_BYTES, dtype=torch.uint8, device=dev)
+    ws_e = torch.empty(rlk.rlk_dlogp_audit_ext_workspace_bytes(na), dtype=torch.uint8,
+                       device=dev)
+    ms = _time_calls(lambda: rlk.rlk_dlogp_audit_ext(new, old, m, None, GRPO_EPS, r_ext, ws_e),
+                     warmup, steps, stream)
+    res["audit_ext_2p26"] = {"ms": ms, "gbs": na * 9 / (ms * 1e-3) / 1e9,
+                             "frac_of_hbm": na * 9 / (ms * 1e-3) / 1e9 / hbm,
+                             "bytes": na * 9,
+                             "note": "algorithmic 9 B/token; the exact percentiles re-read the "
+                                     "inputs in three radix-select passes"}
+    adv = torch.randn(na, device=dev, generator=gen)
+    grad = torch.empty(na, dtype=torch.float32, device=dev)
+    r_loss = torch.empty(rlk.GRPO_RESULT_BYTES, dtype=torch.uint8, device=dev)
+    ws_l = torch.empty(rlk.rlk_grpo_clip_loss_workspace_bytes(na), dtype=torch.uint8, device=dev)
+    ms = _time_calls(lambda: rlk.rlk_grpo_clip_loss(new, old, adv, m, GRPO_EPS, GRPO_EPS,
+                                                    1.0 / na, grad, r_loss, ws_l),
+                     warmup, steps, stream)
+    res["grpo_loss_2p26"] = {"ms": ms, "gbs": na * 17 / (ms * 1e-3) / 1e9,
+                             "frac_of_hbm": na * 17 / (ms * 1e-3) / 1e9 / hbm,
+                             "bytes": na * 17, "note": "13 B read + 4 B gradient written per token"}
+    return res
 
 
 def measure_deepseek_fwd(rlk, dev, peak, warmup, steps):
@@ -545,6 +662,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-second-shape", action="store_true",
                     help="leave out the DeepSeek-shaped forward measurement")
+    ap.add_argument("--no-next-rows", action="store_true",
+                    help="leave out the TP-emulated, entropy, logits, extended-audit and loss "
+                         "measurements")
     ap.add_argument("--audit-only", action="store_true",
                     help="time only the masked audit at N = 9,400,614 and 2^26 (one GPU)")
     args = ap.parse_args()

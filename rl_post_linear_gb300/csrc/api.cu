@@ -378,7 +378,7 @@ rlk_status_t rlk_logp_from_logits(const void* logits, int32_t dtype, int64_t N, 
 
 size_t rlk_grpo_clip_loss_workspace_bytes(int64_t N) {
     if (N < 0) return 0;
-    return align_up(rlk::audit_blocks(N) * sizeof(rlk::LossPartial), 256) + 256;
+    return align_up(rlk::loss_blocks(N) * sizeof(rlk::LossPartial), 256) + 256;
 }
 
 rlk_status_t rlk_grpo_clip_loss(const float* logp_new, const float* logp_old,

@@ -353,7 +353,7 @@ template <bool VEC>
 __global__ void __launch_bounds__(kAuditThreads)
     audit_ext_pass1(const float* __restrict__ nw, const float* __restrict__ od,
                     const uint8_t* __restrict__ mask, int64_t N, float eps,
-                    ExtPartial* __restrict__ out) {
+                    ExtPartial* __restrict__ out, uint32_t* __restrict__ keys) {
     constexpr int kBlock = kAuditThreads * kAuditV3PerThread;
     const int64_t base = static_cast<int64_t>(blockIdx.x) * kBlock;
     ThreadAcc a;
@@ -372,6 +372,7 @@ __global__ void __launch_bounds__(kAuditThreads)
                 m = __ldcs(reinterpret_cast<const unsigned int*>(mask + base + o0));
         }
         const float xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+        uint32_t k4[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int64_t i = base + o0 + e;
@@ -390,10 +391,19 @@ __global__ void __launch_bounds__(kAuditThreads)
             if (mv == 0) continue;
             visit3(nv, ov, 1u, o0 + e, a);
             const float d = nv - ov;
+            k4[e] = abs_key(d);
             const float r = expf(d);
             sabs += fabsf(d);
             sratio += r;
             clip += fabsf(r - 1.0f) > eps ? 1 : 0;
+        }
+        // |d| keys for the percentile passes (0 for inactive tokens)
+        if (full) {
+            *reinterpret_cast<uint4*>(keys + base + o0) = make_uint4(k4[0], k4[1], k4[2], k4[3]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (base + o0 + e < N) keys[base + o0 + e] = k4[e];
         }
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -552,16 +562,21 @@ __global__ void __launch_bounds__(kMergeThreads)
 
 // Histogram of one digit of the |d| keys of the active elements that match
 // each percentile's prefix so far.
+// One radix-select pass over the |d| keys written by pass 1 (0 = inactive).
+// Pass 0 (top 11 bits) is the same for the three percentiles, so it builds a
+// single histogram; lanes of a warp that hit the same bin add their count with
+// one shared-memory atomic (|d| concentrates in few bins).  Passes 1 and 2
+// count, per percentile, the keys whose higher digits match its prefix.
 template <int PASS>
 __global__ void __launch_bounds__(kAuditThreads)
-    audit_ext_hist(const float* __restrict__ nw, const float* __restrict__ od,
-                   const uint8_t* __restrict__ mask, int64_t N,
+    audit_ext_hist(const uint32_t* __restrict__ keys, int64_t N,
                    const SelectState* __restrict__ sel, uint32_t* __restrict__ hist) {
     constexpr int kShift = PASS == 0 ? 21 : (PASS == 1 ? 10 : 0);
     constexpr uint32_t kDigitMask = PASS == 2 ? 0x3ffu : 0x7ffu;
     constexpr int kPrefixShift = PASS == 1 ? 21 : 10;
-    __shared__ uint32_t h[3 * kHistBins];
-    for (int i = threadIdx.x; i < 3 * kHistBins; i += kAuditThreads) h[i] = 0u;
+    constexpr int kHists = PASS == 0 ? 1 : 3;
+    __shared__ uint32_t h[kHists * kHistBins];
+    for (int i = threadIdx.x; i < kHists * kHistBins; i += kAuditThreads) h[i] = 0u;
     uint32_t pre[3];
     bool want[3];
 #pragma unroll
@@ -570,22 +585,52 @@ __global__ void __launch_bounds__(kAuditThreads)
         want[q] = sel->rank[q] > 0;
     }
     __syncthreads();
-    constexpr int kBlock = kAuditThreads * kAuditV3PerThread;
-    const int64_t base = static_cast<int64_t>(blockIdx.x) * kBlock;
-    for (int e = threadIdx.x; e < kBlock; e += kAuditThreads) {
-        const int64_t i = base + e;
-        if (i >= N) break;
-        if (mask != nullptr && mask[i] == 0) continue;
-        const uint32_t key = abs_key(nw[i] - od[i]);
-        const uint32_t digit = (key >> kShift) & kDigitMask;
+    if (PASS > 0 || want[0] || want[1] || want[2]) {
+        constexpr int kBlock = kAuditThreads * kAuditV3PerThread;
+        const int64_t base = static_cast<int64_t>(blockIdx.x) * kBlock;
+        const int lane = threadIdx.x & 31;
+        constexpr int kVec = kAuditV3PerThread / 4;
+        uint32_t k[kVec][4];
+        // every load first, then the counting (the atomics would otherwise keep the
+        // compiler from moving later loads ahead)
 #pragma unroll
-        for (int q = 0; q < 3; ++q) {
-            const bool match = PASS == 0 ? true : ((key >> kPrefixShift) == pre[q]);
-            if (want[q] && match) atomicAdd(&h[q * kHistBins + digit], 1u);
+        for (int j = 0; j < kVec; ++j) {
+            const int64_t i0 = base + j * (kAuditThreads * 4) + threadIdx.x * 4;
+            if (i0 + 4 <= N) {
+                const uint4 v = __ldcs(reinterpret_cast<const uint4*>(keys + i0));
+                k[j][0] = v.x;
+                k[j][1] = v.y;
+                k[j][2] = v.z;
+                k[j][3] = v.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) k[j][e] = i0 + e < N ? keys[i0 + e] : 0u;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t key = k[j][e];
+                const uint32_t digit = (key >> kShift) & kDigitMask;
+                if (PASS == 0) {
+                    // every lane reaches this point: aggregate equal bins across the warp
+                    const unsigned valid = __ballot_sync(0xffffffffu, key != 0u);
+                    if (key != 0u) {
+                        const unsigned peers = __match_any_sync(valid, digit);
+                        if (lane == __ffs(peers) - 1) atomicAdd(&h[digit], __popc(peers));
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 3; ++q)
+                        if (key != 0u && want[q] && (key >> kPrefixShift) == pre[q])
+                            atomicAdd(&h[q * kHistBins + digit], 1u);
+                }
+            }
         }
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < 3 * kHistBins; i += kAuditThreads) {
+    for (int i = threadIdx.x; i < kHists * kHistBins; i += kAuditThreads) {
         const uint32_t c = h[i];
         if (c != 0u) atomicAdd(&hist[i], c);
     }
@@ -601,7 +646,7 @@ __global__ void audit_ext_select(SelectState* __restrict__ sel, uint32_t* __rest
     const int q = threadIdx.x;
     if (q < 3 && sel->rank[q] > 0) {
         const int64_t rank = sel->rank[q];
-        const uint32_t* hq = hist + q * kHistBins;
+        const uint32_t* hq = hist + (PASS == 0 ? 0 : q * kHistBins);   // pass 0: one shared histogram
         int64_t cum = 0;
         uint32_t bin = 0;
         for (int b = 0; b < (1 << kBits); ++b) {
@@ -685,9 +730,14 @@ cudaError_t launch_audit(const float* logp_new, const float* logp_old, const uin
     return cudaLaunchKernelEx(&cfg, audit_pass2, cparts, nparts, result);
 }
 
+// partials | 3 histograms | select state | |d| keys [N] (uint32)
+static size_t ext_keys_off(int64_t N) {
+    return align_up(align_up(audit_v3_blocks(N) * sizeof(ExtPartial), 256) + 3 * kHistBins * 4 +
+                    sizeof(SelectState), 256);
+}
+
 size_t audit_ext_workspace(int64_t N) {
-    return align_up(audit_v3_blocks(N) * sizeof(ExtPartial), 256) + 3 * kHistBins * 4 +
-           sizeof(SelectState) + 256;
+    return ext_keys_off(N) + align_up(static_cast<size_t>(N) * 4, 256) + 256;
 }
 
 cudaError_t launch_audit_ext(const float* logp_new, const float* logp_old, const uint8_t* mask,
@@ -699,26 +749,24 @@ cudaError_t launch_audit_ext(const float* logp_new, const float* logp_old, const
     ExtPartial* parts = reinterpret_cast<ExtPartial*>(ws);
     uint32_t* hist = reinterpret_cast<uint32_t*>(ws + align_up(blocks * sizeof(ExtPartial), 256));
     SelectState* sel = reinterpret_cast<SelectState*>(hist + 3 * kHistBins);
+    uint32_t* keys = reinterpret_cast<uint32_t*>(ws + ext_keys_off(N));
     const unsigned grid = static_cast<unsigned>(blocks);
     if (blocks > 0) {
         if (vec_ok)
             audit_ext_pass1<true><<<grid, kAuditThreads, 0, stream>>>(logp_new, logp_old, mask, N,
-                                                                      eps, parts);
+                                                                      eps, parts, keys);
         else
             audit_ext_pass1<false><<<grid, kAuditThreads, 0, stream>>>(logp_new, logp_old, mask,
-                                                                       N, eps, parts);
+                                                                       N, eps, parts, keys);
     }
     audit_ext_merge<<<1, kMergeThreads, 0, stream>>>(parts, static_cast<int64_t>(blocks),
                                                      seq_offsets, num_seqs, result, sel, hist);
     if (blocks > 0) {
-        audit_ext_hist<0><<<grid, kAuditThreads, 0, stream>>>(logp_new, logp_old, mask, N, sel,
-                                                               hist);
+        audit_ext_hist<0><<<grid, kAuditThreads, 0, stream>>>(keys, N, sel, hist);
         audit_ext_select<0><<<1, 32, 0, stream>>>(sel, hist, result);
-        audit_ext_hist<1><<<grid, kAuditThreads, 0, stream>>>(logp_new, logp_old, mask, N, sel,
-                                                               hist);
+        audit_ext_hist<1><<<grid, kAuditThreads, 0, stream>>>(keys, N, sel, hist);
         audit_ext_select<1><<<1, 32, 0, stream>>>(sel, hist, result);
-        audit_ext_hist<2><<<grid, kAuditThreads, 0, stream>>>(logp_new, logp_old, mask, N, sel,
-                                                               hist);
+        audit_ext_hist<2><<<grid, kAuditThreads, 0, stream>>>(keys, N, sel, hist);
         audit_ext_select<2><<<1, 32, 0, stream>>>(sel, hist, result);
     }
     return cudaGetLastError();

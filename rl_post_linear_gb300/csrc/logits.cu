@@ -82,7 +82,27 @@ __global__ void __launch_bounds__(kLogitsThreads)
     const T* row = logits + r * stride;
     MS st{-INFINITY, 0.f};
     const int groups = (V + VEC - 1) / VEC;
-    for (int g = threadIdx.x; g < groups; g += kLogitsThreads) {
+    int g = threadIdx.x;
+    if (vec_ok) {
+        // four of the thread's groups per step, all loads first (more bytes in flight);
+        // they are folded in the same ascending order as one at a time
+        const int full = V / VEC;                // groups with VEC valid columns
+        for (; g + 3 * kLogitsThreads < full; g += 4 * kLogitsThreads) {
+            uint4 raw[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                raw[q] = __ldcs(reinterpret_cast<const uint4*>(row + (g + q * kLogitsThreads) * VEC));
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const T* v = reinterpret_cast<const T*>(&raw[q]);
+                float x[VEC];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) x[e] = to_f32(v[e]);
+                fold<VEC>(x, VEC, k, st);
+            }
+        }
+    }
+    for (; g < groups; g += kLogitsThreads) {
         const int c0 = g * VEC;
         const int valid = min(VEC, V - c0);
         float x[VEC];

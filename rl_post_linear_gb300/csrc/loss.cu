@@ -13,7 +13,7 @@
 //   loss   = -scale * sum_active term_t
 // plus the active count, the zero-gradient clipped count, the out-of-range
 // count and the mean ratio.  g_t depends on token t alone (and on the
-// caller's scale), so it is batch invariant.  Reductions: fixed 8192-element
+// caller's scale), so it is batch invariant.  Reductions: fixed 4096-element
 // blocks, fp32 per-thread sums in ascending index order, fp64 fixed shuffle
 // trees, and a single-block merge launched with programmatic dependent launch.
 #include <cmath>
@@ -70,7 +70,7 @@ __device__ __forceinline__ LossAcc block_sum(LossAcc a) {
 }
 
 struct ThreadSums {
-    int64_t count = 0, clipped = 0, outside = 0;
+    int count = 0, clipped = 0, outside = 0;     // at most kLossPerThread each
     float term = 0.f, r = 0.f;
 };
 
@@ -98,10 +98,10 @@ __global__ void __launch_bounds__(kAuditThreads)
                float lo, float hi, float scale, float* __restrict__ grad,
                LossPartial* __restrict__ out) {
     asm volatile("griddepcontrol.launch_dependents;");
-    constexpr int kVec = kAuditPerThread / 4;
-    const int64_t base = static_cast<int64_t>(blockIdx.x) * kAuditBlockElems;
+    constexpr int kVec = kLossPerThread / 4;
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * kLossBlockElems;
     ThreadSums s;
-    if (VEC && base + kAuditBlockElems <= N) {
+    if (VEC && base + kLossBlockElems <= N) {
         float4 a[kVec], b[kVec], c[kVec];
         uint32_t m[kVec];
 #pragma unroll
@@ -179,7 +179,7 @@ cudaError_t launch_grpo_loss(const float* logp_new, const float* logp_old, const
                              const uint8_t* mask, int64_t N, double eps_low, double eps_high,
                              double scale, float* grad, rlk_grpo_result_t* result,
                              void* workspace, bool vec_ok, cudaStream_t stream) {
-    const size_t blocks = audit_blocks(N);
+    const size_t blocks = loss_blocks(N);
     LossPartial* parts = static_cast<LossPartial*>(workspace);
     const float lo = static_cast<float>(1.0 - eps_low);
     const float hi = static_cast<float>(1.0 + eps_high);

@@ -24,9 +24,9 @@ constexpr int kBwdChunk = 32768;            // backward vocab chunk (multiple of
 constexpr int kRasterTokenTiles = 32;
 constexpr int kRasterHiddenTiles = 8;
 constexpr int kAuditThreads = 256;
-constexpr int kAuditPerThread = 32;         // 8 float4 of each input per thread (loss fragment)
+constexpr int kLossPerThread = 16;          // 4 float4 of each input per thread (loss fragment)
 constexpr int kAuditV3PerThread = 16;       // 4 float4 of each input per thread (audit)
-constexpr int kAuditBlockElems = kAuditThreads * kAuditPerThread;
+constexpr int kLossBlockElems = kAuditThreads * kLossPerThread;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -89,8 +89,8 @@ struct LossPartial {
     double sum_r;
 };
 
-inline size_t audit_blocks(int64_t N) {
-    return static_cast<size_t>((N + kAuditBlockElems - 1) / kAuditBlockElems);
+inline size_t loss_blocks(int64_t N) {
+    return static_cast<size_t>((N + kLossBlockElems - 1) / kLossBlockElems);
 }
 
 inline size_t audit_v3_blocks(int64_t N) {
