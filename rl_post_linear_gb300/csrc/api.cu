@@ -234,6 +234,7 @@ static rlk_status_t bwd_impl(const void* hidden, const void* weight, const int64
     st.dh_acc = dh_acc;
     st.sorted_y = sorted_y;
     st.sorted_t = sorted_t;
+    st.ycoef = reinterpret_cast<float*>(ws + lay.ycoef_off);
     st.dhidden = dhidden;
     st.dweight = dweight;
     void* ds = ws + lay.ds_off;

@@ -43,6 +43,7 @@
 namespace rlk {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.69314718055994531f;
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -82,6 +83,7 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
     const float* ent;        // ENT only
     const float* lse;
     __nv_bfloat16* ds;    // [N][kBwdChunk]
+    float* ycoef;         // [N]: 1 - p_y of each live row, written by the tile holding y
     int N, V, c0, num_m, num_n, kblocks;
     float k, temp;
 
@@ -103,6 +105,8 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
 
     struct EpiState {
         float coef, c2, lse2;
+        float coef_y;         // ENT: the target entry's coefficient without the -g/T part
+        int64_t ycol;         // target column relative to the chunk
         bool live;
     };
 
@@ -113,11 +117,14 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
         int64_t y;
         st.live = row_live(targets, mask, t, N, V, y);
         st.lse2 = st.live ? lse[t] * kLog2e : 0.f;
+        st.ycol = y - c0;
+        st.coef_y = 0.f;
         if constexpr (ENT) {
             const float gh = st.live ? grad_ent[t] : 0.f;
             const float ez = st.live ? lse[t] - ent[t] : 0.f;
             st.coef = st.live ? -__fdiv_rn(fmaf(-gh, ez, grad[t]), temp) : 0.f;
             st.c2 = st.live ? -__fdiv_rn(gh, temp * temp) : 0.f;
+            st.coef_y = st.live ? __fdiv_rn(gh * ez, temp) : 0.f;
         } else {
             st.coef = st.live ? -__fdiv_rn(grad[t], temp) : 0.f;
             st.c2 = 0.f;
@@ -135,6 +142,24 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
             if (t >= N) continue;
             const int col = n * kTileV + cc * 32;   // column inside the chunk
             const int vb = c0 + col;
+            // The target entry: its -g p_y / T part stays out of dS, and the dh / dW
+            // epilogues add g (1 - p_y) / T in fp32 instead of g / T.  1 - p_y comes from
+            // expm1 of log p_y, so a dominant target (p_y -> 1) keeps its small gradient
+            // g (1 - p_y) / T to fp32 accuracy rather than as a difference of two bf16-sized
+            // terms.  (ENT keeps the entropy part of the entry in dS.)
+            const int64_t yc = st.ycol - col;
+            int yi = 32;                              // no target in this slice
+            float dy = 0.f;
+            if (st.live && yc >= 0 && yc < 32) {
+                float x[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
+                yi = static_cast<int>(yc);
+                const float sy = select32(x, yi);
+                const float l2 = fmaf(sy, k, -st.lse2);          // log2 p_y
+                ycoef[t] = -expm1f(l2 * kLn2);
+                if constexpr (ENT) dy = fmaf(st.c2, sy, st.coef_y) * ex2_approx(l2);
+            }
             uint32_t packed[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -145,10 +170,12 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
                     c0 = fmaf(st.c2, s0, st.coef);
                     c1 = fmaf(st.c2, s1, st.coef);
                 }
-                const float d0 = (st.live && vb + 2 * j < V)
-                                     ? c0 * ex2_approx(fmaf(s0, k, -st.lse2)) : 0.f;
-                const float d1 = (st.live && vb + 2 * j + 1 < V)
-                                     ? c1 * ex2_approx(fmaf(s1, k, -st.lse2)) : 0.f;
+                float d0 = (st.live && vb + 2 * j < V)
+                               ? c0 * ex2_approx(fmaf(s0, k, -st.lse2)) : 0.f;
+                float d1 = (st.live && vb + 2 * j + 1 < V)
+                               ? c1 * ex2_approx(fmaf(s1, k, -st.lse2)) : 0.f;
+                d0 = (yi == 2 * j) ? dy : d0;
+                d1 = (yi == 2 * j + 1) ? dy : d1;
                 packed[j] = pack_bf16x2(d0, d1);
             }
             uint4* dst = reinterpret_cast<uint4*>(ds + static_cast<size_t>(t) * kBwdChunk + col);
@@ -173,6 +200,7 @@ struct DhPolicy : SingleRole<false, true> {
     const __nv_bfloat16* weight;   // [V][H]
     float* dh_acc;                 // [N][H]
     __nv_bfloat16* dh;             // [N][H]
+    const float* ycoef;            // [N] 1 - p_y, from the dS GEMM
     int N, V, H, c0, num_m, num_n, kblocks;
     bool first, last;
     float temp;
@@ -206,7 +234,8 @@ struct DhPolicy : SingleRole<false, true> {
         unit(u, m, n);
         const int t = m * kTileM + row;
         st.live = row_live(targets, mask, t, N, V, st.y);
-        st.coef = st.live ? __fdiv_rn(grad[t], temp) : 0.f;
+        // the target term (g / T)(1 - p_y), added once, in the last chunk's epilogue
+        st.coef = (st.live && last) ? __fdiv_rn(grad[t], temp) * ycoef[t] : 0.f;
     }
 
     __device__ void epi_tile(int u, int, int row, uint32_t taddr, EpiState& st) const {
@@ -277,6 +306,7 @@ struct DwPolicy : SingleRole<true, true> {
     __nv_bfloat16* dw;             // [V][H]
     const int* sorted_y;           // [N] ascending; V marks rows without a target term
     const int* sorted_t;           // [N]
+    const float* ycoef;            // [N] 1 - p_y, from the dS GEMM
     int N, H, c0, width, num_m, num_n, kblocks;
     float temp;
 
@@ -334,7 +364,7 @@ struct DwPolicy : SingleRole<true, true> {
             for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
             for (int i = st.lo; i < st.hi; ++i) {
                 const int t = sorted_t[i];
-                const float coef = __fdiv_rn(grad[t], temp);
+                const float coef = __fdiv_rn(grad[t], temp) * ycoef[t];
                 const uint4* hr = reinterpret_cast<const uint4*>(
                     hidden + static_cast<size_t>(t) * H + col);
 #pragma unroll
@@ -467,6 +497,7 @@ static cudaError_t launch_ds(const BwdStepMaps& maps, const BwdStep& st, int c0,
     ps.ent = st.ent;
     ps.lse = st.lse;
     ps.ds = static_cast<__nv_bfloat16*>(st.ds);
+    ps.ycoef = st.ycoef;
     ps.N = st.N;
     ps.V = st.V;
     ps.c0 = c0;
@@ -494,6 +525,7 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
         pd.weight = static_cast<const __nv_bfloat16*>(st.weight);
         pd.dh_acc = st.dh_acc;
         pd.dh = static_cast<__nv_bfloat16*>(st.dhidden);
+        pd.ycoef = st.ycoef;
         pd.N = N;
         pd.V = V;
         pd.H = H;
@@ -513,6 +545,7 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
     pw.dw = static_cast<__nv_bfloat16*>(st.dweight);
     pw.sorted_y = st.sorted_y;
     pw.sorted_t = st.sorted_t;
+    pw.ycoef = st.ycoef;
     pw.N = N;
     pw.H = H;
     pw.c0 = c0;

@@ -135,6 +135,21 @@ __device__ __forceinline__ void grouped_unit(int u, int rows, int cols, int grou
     }
 }
 
+// x[i] for a runtime i in [0, 32) through a fixed 5-level select tree, so
+// that the 32 values stay in registers.
+__device__ __forceinline__ float select32(const float (&x)[32], int i) {
+    float a[16], b[8], c[4], d[2];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) a[j] = (i & 16) ? x[j + 16] : x[j];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) b[j] = (i & 8) ? a[j + 8] : a[j];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) c[j] = (i & 4) ? b[j + 4] : b[j];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) d[j] = (i & 2) ? c[j + 2] : c[j];
+    return (i & 1) ? d[1] : d[0];
+}
+
 __device__ __forceinline__ void report_error(uint32_t* err, uint32_t bits) {
     if (err != nullptr) atomicOr(err, bits);
 }

@@ -56,17 +56,18 @@ struct FwdLayout {
 };
 
 // Backward workspace: dS for one vocab chunk [N, kBwdChunk] bf16, the fp32 dh
-// accumulator [N, H], the (target, token) list sorted by target, and the
-// sorted key tiles the list is built from.
+// accumulator [N, H], the (target, token) list sorted by target, 1 - p_y per
+// row, and the sorted key tiles the target list is built from.
 constexpr int kTargetSortTile = 2048;
 struct BwdLayout {
-    size_t ds_off, dhacc_off, sorted_y_off, sorted_t_off, tiles_off, total;
+    size_t ds_off, dhacc_off, sorted_y_off, sorted_t_off, ycoef_off, tiles_off, total;
     BwdLayout(int64_t N, int64_t H) {
         ds_off = 0;
         dhacc_off = align_up(static_cast<size_t>(N) * kBwdChunk * 2, 256);
         sorted_y_off = align_up(dhacc_off + static_cast<size_t>(N) * H * 4, 256);
         sorted_t_off = align_up(sorted_y_off + static_cast<size_t>(N) * 4, 256);
-        tiles_off = align_up(sorted_t_off + static_cast<size_t>(N) * 4, 256);
+        ycoef_off = align_up(sorted_t_off + static_cast<size_t>(N) * 4, 256);
+        tiles_off = align_up(ycoef_off + static_cast<size_t>(N) * 4, 256);
         const size_t tiles = static_cast<size_t>((N + kTargetSortTile - 1) / kTargetSortTile);
         total = align_up(tiles_off + tiles * kTargetSortTile * 8, 256);
     }
@@ -154,6 +155,7 @@ struct BwdStep {
     float* dh_acc;
     const int* sorted_y;
     const int* sorted_t;
+    float* ycoef;              // [N] 1 - p_y of each live row
     void* dhidden;
     void* dweight;
 };
