@@ -199,8 +199,9 @@ def run_ours(args, world, rank, local):
     scale = 1.0 / n_act                         # token mean over the batch's active tokens
     n_chunks = -(-v // 32768)
     # forward: row compaction (3, the step passes a mask) + GEMM + merge; loss 2; audit 2;
-    # backward: target sort (2) + one launch per role and vocab chunk
-    launches_per_step = 5 + 2 + 2 + 2 + 3 * n_chunks
+    # backward: target sort (2), then per vocab chunk the three GEMM roles and the sort of
+    # the chunk's dominant non-target classes (2)
+    launches_per_step = 5 + 2 + 2 + 2 + 5 * n_chunks
 
     def step(ev=None, ins=None):
         h_t, y_t, m_t, old_t, adv_t = ins if ins is not None else (hid, y, mask, old, advd)

@@ -212,9 +212,10 @@ static rlk_status_t bwd_impl(const void* hidden, const void* weight, const int64
     RLK_TRY(make_map(&maps.h_mnmajor, hidden, H, N, H * 2, 64, 64));
 
     const int n = static_cast<int>(N), h = static_cast<int>(H), v = static_cast<int>(V);
-    RLK_CUDA(rlk::launch_target_sort(targets, active_mask, n, v,
-                                     reinterpret_cast<uint64_t*>(ws + lay.tiles_off), sorted_y,
-                                     sorted_t, device_error_word, stream));
+    int* dom = reinterpret_cast<int*>(ws + lay.dom_off);
+    uint64_t* tiles = reinterpret_cast<uint64_t*>(ws + lay.tiles_off);
+    RLK_CUDA(rlk::launch_target_sort(targets, active_mask, n, v, tiles, sorted_y, sorted_t, dom,
+                                     device_error_word, stream));
     const int num_chunks = static_cast<int>((V + rlk::kBwdChunk - 1) / rlk::kBwdChunk);
     rlk::BwdStep st;
     st.targets = targets;
@@ -235,6 +236,10 @@ static rlk_status_t bwd_impl(const void* hidden, const void* weight, const int64
     st.sorted_y = sorted_y;
     st.sorted_t = sorted_t;
     st.ycoef = reinterpret_cast<float*>(ws + lay.ycoef_off);
+    st.dom = dom;
+    st.sorted_dy = reinterpret_cast<int*>(ws + lay.sorted_dy_off);
+    st.sorted_dt = reinterpret_cast<int*>(ws + lay.sorted_dt_off);
+    st.tiles = tiles;
     st.dhidden = dhidden;
     st.dweight = dweight;
     void* ds = ws + lay.ds_off;

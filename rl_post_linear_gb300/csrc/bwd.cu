@@ -5,15 +5,20 @@
 // "RL-Kernel integration roadmap for vime", linear_logp: dlogits live in
 // operator-owned workspace; the operator returns full gradients.
 //
-// With g_t = dL/dlogp_t, k = log2(e)/T and lse2_t = lse_t log2(e):
-//   p[t,v]  = 2^(S[t,v] k - lse2_t)                 (S recomputed, fp32)
-//   dS[t,v] = -(g_t / T) p[t,v]        (bf16, every v including y_t)
-//   dh_t    = bf16( sum_c (dS_c W_c)_t  +  (g_t / T) W[y_t] )
-//   dW_v    = bf16( (dS^T h)_v  +  sum_{t : y_t = v} (g_t / T) h_t )
-// The "+ (g/T)" target terms are added in fp32 in the epilogues instead of
-// going through bf16 dS: they dominate the gradient norm, and rounding their
-// coefficient to bf16 would cost about as much accuracy as the final bf16
-// rounding of the outputs.
+// With g_t = dL/dlogp_t, k = log2(e)/T and lse2_t = lse_t log2(e), the
+// gradient of the logits is G[t,v] = (g_t / T)(delta_{v,y_t} - p[t,v]),
+// p[t,v] = 2^(S[t,v] k - lse2_t) (S recomputed, fp32).  It is applied as
+//   dS[t,v] = -(g_t / T) p[t,v]                       (bf16, v not y_t, a_t)
+//   dS[t,y] = 0,  dS[t,a] = (g_t / T)(1 - p[t,a])     (bf16)
+//   dh_t    = bf16( sum_c (dS_c W_c)_t + (g_t / T)(1 - p_y) W[y_t] - (g_t / T) W[a_t] )
+//   dW_v    = bf16( (dS^T h)_v + sum_{y_t = v} (g_t / T)(1 - p_y) h_t
+//                               - sum_{a_t = v} (g_t / T) h_t )
+// where a_t is the row's dominant non-target class (p > 1/2), if any.  The
+// large parts of the two entries that can dominate a row are added in fp32 in
+// the epilogues, with 1 - p = -expm1(log p): in bf16 dS the target's g/T part
+// (flat softmax) would cost as much accuracy as the final rounding of the
+// outputs, and g (1 - p) / T written as a difference (a confident policy,
+// p -> 1) would lose its leading digits.
 //
 // The vocabulary is walked in fixed chunks of kBwdChunk columns, ascending.
 // For each chunk c three tcgen05 GEMM roles run:
@@ -84,6 +89,7 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
     const float* lse;
     __nv_bfloat16* ds;    // [N][kBwdChunk]
     float* ycoef;         // [N]: 1 - p_y of each live row, written by the tile holding y
+    int* dom;             // [N]: the row's dominant non-target class (p > 1/2), else -1
     int N, V, c0, num_m, num_n, kblocks;
     float k, temp;
 
@@ -106,6 +112,7 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
     struct EpiState {
         float coef, c2, lse2;
         float coef_y;         // ENT: the target entry's coefficient without the -g/T part
+        float gt;             // g / T
         int64_t ycol;         // target column relative to the chunk
         bool live;
     };
@@ -119,6 +126,7 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
         st.lse2 = st.live ? lse[t] * kLog2e : 0.f;
         st.ycol = y - c0;
         st.coef_y = 0.f;
+        st.gt = st.live ? __fdiv_rn(grad[t], temp) : 0.f;
         if constexpr (ENT) {
             const float gh = st.live ? grad_ent[t] : 0.f;
             const float ez = st.live ? lse[t] - ent[t] : 0.f;
@@ -150,21 +158,45 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
             const int64_t yc = st.ycol - col;
             int yi = 32;                              // no target in this slice
             float dy = 0.f;
-            if (st.live && yc >= 0 && yc < 32) {
-                float x[32];
+            float x[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
+            for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
+            if (st.live && yc >= 0 && yc < 32) {
                 yi = static_cast<int>(yc);
                 const float sy = select32(x, yi);
                 const float l2 = fmaf(sy, k, -st.lse2);          // log2 p_y
                 ycoef[t] = -expm1f(l2 * kLn2);
                 if constexpr (ENT) dy = fmaf(st.c2, sy, st.coef_y) * ex2_approx(l2);
             }
+            // A dominant non-target entry is split the same way: G_a = -g/T + (g/T)(1 - p_a)
+            // (+ its entropy part); dS keeps the small second part, and the dh / dW
+            // epilogues add -g/T in fp32 for the class recorded in dom.  "Dominant" is
+            // p_a > 2^-0.99 = 0.5035: two entries of a row cannot both pass, even with the
+            // fp32 error of p, so dom has one writer.
+            int ai = 32;                              // no dominant entry in this slice
+            float da = 0.f;
+            if (st.live) {
+                float cm = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) cm = (vb + j < V) ? fmaxf(cm, x[j]) : cm;
+                const float l2 = fmaf(cm, k, -st.lse2);          // log2 of the slice's top p
+                if (l2 > -0.99f) {
+                    int idx = 31;
+#pragma unroll
+                    for (int j = 31; j >= 0; --j) idx = (x[j] == cm && vb + j < V) ? j : idx;
+                    if (idx != yi) {
+                        ai = idx;
+                        dom[t] = vb + idx;
+                        da = st.gt * -expm1f(l2 * kLn2);
+                        if constexpr (ENT) da = fmaf(fmaf(st.c2, cm, st.coef_y), ex2_approx(l2), da);
+                    }
+                }
+            }
             uint32_t packed[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                const float s0 = __uint_as_float(r[2 * j]);
-                const float s1 = __uint_as_float(r[2 * j + 1]);
+                const float s0 = x[2 * j];
+                const float s1 = x[2 * j + 1];
                 float c0 = st.coef, c1 = st.coef;
                 if constexpr (ENT) {
                     c0 = fmaf(st.c2, s0, st.coef);
@@ -174,8 +206,8 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
                                ? c0 * ex2_approx(fmaf(s0, k, -st.lse2)) : 0.f;
                 float d1 = (st.live && vb + 2 * j + 1 < V)
                                ? c1 * ex2_approx(fmaf(s1, k, -st.lse2)) : 0.f;
-                d0 = (yi == 2 * j) ? dy : d0;
-                d1 = (yi == 2 * j + 1) ? dy : d1;
+                d0 = (yi == 2 * j) ? dy : ((ai == 2 * j) ? da : d0);
+                d1 = (yi == 2 * j + 1) ? dy : ((ai == 2 * j + 1) ? da : d1);
                 packed[j] = pack_bf16x2(d0, d1);
             }
             uint4* dst = reinterpret_cast<uint4*>(ds + static_cast<size_t>(t) * kBwdChunk + col);
@@ -201,6 +233,7 @@ struct DhPolicy : SingleRole<false, true> {
     float* dh_acc;                 // [N][H]
     __nv_bfloat16* dh;             // [N][H]
     const float* ycoef;            // [N] 1 - p_y, from the dS GEMM
+    const int* dom;                // [N] dominant non-target class or -1, from the dS GEMM
     int N, V, H, c0, num_m, num_n, kblocks;
     bool first, last;
     float temp;
@@ -224,8 +257,9 @@ struct DhPolicy : SingleRole<false, true> {
     }
 
     struct EpiState {
-        float coef;
+        float coef, coef_dom;
         int64_t y;
+        int dom;
         bool live;
     };
 
@@ -234,8 +268,12 @@ struct DhPolicy : SingleRole<false, true> {
         unit(u, m, n);
         const int t = m * kTileM + row;
         st.live = row_live(targets, mask, t, N, V, st.y);
-        // the target term (g / T)(1 - p_y), added once, in the last chunk's epilogue
-        st.coef = (st.live && last) ? __fdiv_rn(grad[t], temp) * ycoef[t] : 0.f;
+        // the fp32 terms, added once, in the last chunk's epilogue: (g / T)(1 - p_y) W[y]
+        // and, for a dominant non-target class a, -(g / T) W[a]
+        const float gt = (st.live && last) ? __fdiv_rn(grad[t], temp) : 0.f;
+        st.coef = (st.live && last) ? gt * ycoef[t] : 0.f;
+        st.dom = (st.live && last) ? dom[t] : -1;
+        st.coef_dom = -gt;
     }
 
     __device__ void epi_tile(int u, int, int row, uint32_t taddr, EpiState& st) const {
@@ -279,6 +317,18 @@ struct DhPolicy : SingleRole<false, true> {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) x[8 * i + j] = fmaf(st.coef, wv[j], x[8 * i + j]);
                 }
+                if (st.dom >= 0) {
+                    const uint4* wa = reinterpret_cast<const uint4*>(
+                        weight + static_cast<size_t>(st.dom) * H + col);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        float wv[8];
+                        bf16x8_to_f32(wa[i], wv);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            x[8 * i + j] = fmaf(st.coef_dom, wv[j], x[8 * i + j]);
+                    }
+                }
             } else {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) x[j] = 0.f;
@@ -307,6 +357,8 @@ struct DwPolicy : SingleRole<true, true> {
     const int* sorted_y;           // [N] ascending; V marks rows without a target term
     const int* sorted_t;           // [N]
     const float* ycoef;            // [N] 1 - p_y, from the dS GEMM
+    const int* sorted_dy;          // [N] dominant class of this chunk ascending, V elsewhere
+    const int* sorted_dt;          // [N]
     int N, H, c0, width, num_m, num_n, kblocks;
     float temp;
 
@@ -327,9 +379,22 @@ struct DwPolicy : SingleRole<true, true> {
     }
 
     struct EpiState {
-        int lo, hi, v;
+        int lo, hi, dlo, dhi, v;
         bool valid;
     };
+
+    // [lo, hi): the entries of an ascending list equal to v
+    __device__ static void equal_range(const int* keys, int n, int v, int& lo, int& hi) {
+        int a = 0, b = n;
+        while (a < b) {
+            const int mid = (a + b) >> 1;
+            if (keys[mid] < v) a = mid + 1; else b = mid;
+        }
+        int e = a;
+        while (e < n && keys[e] == v) ++e;
+        lo = a;
+        hi = e;
+    }
 
     __device__ void epi_begin(int u, int row, EpiState& st) const {
         int m, n;
@@ -337,17 +402,10 @@ struct DwPolicy : SingleRole<true, true> {
         const int vl = m * kTileM + row;
         st.valid = vl < width;
         st.v = c0 + vl;
-        st.lo = st.hi = 0;
+        st.lo = st.hi = st.dlo = st.dhi = 0;
         if (!st.valid) return;
-        int lo = 0, hi = N;                  // first index with sorted_y >= v
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (sorted_y[mid] < st.v) lo = mid + 1; else hi = mid;
-        }
-        int e = lo;
-        while (e < N && sorted_y[e] == st.v) ++e;
-        st.lo = lo;
-        st.hi = e;
+        equal_range(sorted_y, N, st.v, st.lo, st.hi);
+        equal_range(sorted_dy, N, st.v, st.dlo, st.dhi);
     }
 
     __device__ void epi_tile(int u, int, int, uint32_t taddr, EpiState& st) const {
@@ -365,6 +423,20 @@ struct DwPolicy : SingleRole<true, true> {
             for (int i = st.lo; i < st.hi; ++i) {
                 const int t = sorted_t[i];
                 const float coef = __fdiv_rn(grad[t], temp) * ycoef[t];
+                const uint4* hr = reinterpret_cast<const uint4*>(
+                    hidden + static_cast<size_t>(t) * H + col);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float hv[8];
+                    bf16x8_to_f32(hr[q], hv);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) x[8 * q + j] = fmaf(coef, hv[j], x[8 * q + j]);
+                }
+            }
+            // tokens whose dominant non-target class is v: -(g_t / T) h_t, ascending t
+            for (int i = st.dlo; i < st.dhi; ++i) {
+                const int t = sorted_dt[i];
+                const float coef = -__fdiv_rn(grad[t], temp);
                 const uint4* hr = reinterpret_cast<const uint4*>(
                     hidden + static_cast<size_t>(t) * H + col);
 #pragma unroll
@@ -395,27 +467,9 @@ constexpr int kSortThreads = 1024;
 constexpr int kPlaceThreads = 256;
 constexpr uint64_t kPadKey = ~0ull;         // above every real key
 
-__global__ void __launch_bounds__(kSortThreads)
-    target_tile_sort_kernel(const int64_t* __restrict__ targets, const uint8_t* __restrict__ mask,
-                            int N, int V, uint64_t* __restrict__ tiles, uint32_t* err) {
-    __shared__ uint64_t key[kSortTile];
-    const int base = blockIdx.x * kSortTile;
-    for (int i = threadIdx.x; i < kSortTile; i += kSortThreads) {
-        const int t = base + i;
-        uint64_t k = kPadKey;
-        if (t < N) {
-            int y = V;
-            if (mask == nullptr || mask[t] != 0) {
-                const int64_t yt = targets[t];
-                if (yt >= 0 && yt < V) y = static_cast<int>(yt);
-                else if (err != nullptr) atomicOr(err, RLK_DEVERR_TARGET_RANGE);
-            }
-            k = (static_cast<uint64_t>(y) << 32) | static_cast<uint32_t>(t);
-        }
-        key[i] = k;
-    }
-    __syncthreads();
-    // bitonic network: merge sorted runs of `size`, comparing at distance `d`
+// Batcher's bitonic network over the block's tile of keys in shared memory:
+// merge sorted runs of `size`, comparing at distance `d`.
+__device__ __forceinline__ void bitonic_sort_tile(uint64_t* key) {
     for (int size = 2; size <= kSortTile; size <<= 1) {
         for (int d = size >> 1; d > 0; d >>= 1) {
             for (int i = threadIdx.x; i < kSortTile; i += kSortThreads) {
@@ -432,6 +486,54 @@ __global__ void __launch_bounds__(kSortThreads)
             __syncthreads();
         }
     }
+}
+
+// Keys (target, token) of the dW target terms; also resets dom[] to "no dominant class".
+__global__ void __launch_bounds__(kSortThreads)
+    target_tile_sort_kernel(const int64_t* __restrict__ targets, const uint8_t* __restrict__ mask,
+                            int N, int V, uint64_t* __restrict__ tiles, int* __restrict__ dom,
+                            uint32_t* err) {
+    __shared__ uint64_t key[kSortTile];
+    const int base = blockIdx.x * kSortTile;
+    for (int i = threadIdx.x; i < kSortTile; i += kSortThreads) {
+        const int t = base + i;
+        uint64_t k = kPadKey;
+        if (t < N) {
+            int y = V;
+            if (mask == nullptr || mask[t] != 0) {
+                const int64_t yt = targets[t];
+                if (yt >= 0 && yt < V) y = static_cast<int>(yt);
+                else if (err != nullptr) atomicOr(err, RLK_DEVERR_TARGET_RANGE);
+            }
+            k = (static_cast<uint64_t>(y) << 32) | static_cast<uint32_t>(t);
+            dom[t] = -1;
+        }
+        key[i] = k;
+    }
+    __syncthreads();
+    bitonic_sort_tile(key);
+    for (int i = threadIdx.x; i < kSortTile; i += kSortThreads) tiles[base + i] = key[i];
+}
+
+// Keys (dominant class, token) of the tokens whose dominant non-target class lies in
+// [lo, hi) (one vocab chunk); V for every other token.
+__global__ void __launch_bounds__(kSortThreads)
+    dom_tile_sort_kernel(const int* __restrict__ dom, int N, int V, int lo, int hi,
+                         uint64_t* __restrict__ tiles) {
+    __shared__ uint64_t key[kSortTile];
+    const int base = blockIdx.x * kSortTile;
+    for (int i = threadIdx.x; i < kSortTile; i += kSortThreads) {
+        const int t = base + i;
+        uint64_t k = kPadKey;
+        if (t < N) {
+            const int a = dom[t];
+            const int c = (a >= lo && a < hi) ? a : V;
+            k = (static_cast<uint64_t>(c) << 32) | static_cast<uint32_t>(t);
+        }
+        key[i] = k;
+    }
+    __syncthreads();
+    bitonic_sort_tile(key);
     for (int i = threadIdx.x; i < kSortTile; i += kSortThreads) tiles[base + i] = key[i];
 }
 
@@ -458,18 +560,33 @@ __global__ void __launch_bounds__(kPlaceThreads)
     sorted_t[rank] = static_cast<int>(k & 0xffffffffu);
 }
 
-cudaError_t launch_target_sort(const int64_t* targets, const uint8_t* mask, int N, int V,
-                               uint64_t* tiles, int* sorted_y, int* sorted_t, uint32_t* err,
-                               cudaStream_t stream) {
+static cudaError_t place_sorted(const uint64_t* tiles, int N, int* sorted_key, int* sorted_t,
+                                cudaStream_t stream) {
     const int num_tiles = (N + kSortTile - 1) / kSortTile;
-    target_tile_sort_kernel<<<num_tiles, kSortThreads, 0, stream>>>(targets, mask, N, V, tiles,
-                                                                     err);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
     const int total = num_tiles * kSortTile;
     target_place_kernel<<<(total + kPlaceThreads - 1) / kPlaceThreads, kPlaceThreads, 0, stream>>>(
-        tiles, num_tiles, sorted_y, sorted_t);
+        tiles, num_tiles, sorted_key, sorted_t);
     return cudaGetLastError();
+}
+
+cudaError_t launch_target_sort(const int64_t* targets, const uint8_t* mask, int N, int V,
+                               uint64_t* tiles, int* sorted_y, int* sorted_t, int* dom,
+                               uint32_t* err, cudaStream_t stream) {
+    const int num_tiles = (N + kSortTile - 1) / kSortTile;
+    target_tile_sort_kernel<<<num_tiles, kSortThreads, 0, stream>>>(targets, mask, N, V, tiles,
+                                                                     dom, err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return place_sorted(tiles, N, sorted_y, sorted_t, stream);
+}
+
+static cudaError_t launch_dom_sort(const int* dom, int N, int V, int lo, int hi, uint64_t* tiles,
+                                   int* sorted_dy, int* sorted_dt, cudaStream_t stream) {
+    const int num_tiles = (N + kSortTile - 1) / kSortTile;
+    dom_tile_sort_kernel<<<num_tiles, kSortThreads, 0, stream>>>(dom, N, V, lo, hi, tiles);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return place_sorted(tiles, N, sorted_dy, sorted_dt, stream);
 }
 
 // ----------------------------------------------------------------------------- launch
@@ -498,6 +615,7 @@ static cudaError_t launch_ds(const BwdStepMaps& maps, const BwdStep& st, int c0,
     ps.lse = st.lse;
     ps.ds = static_cast<__nv_bfloat16*>(st.ds);
     ps.ycoef = st.ycoef;
+    ps.dom = st.dom;
     ps.N = st.N;
     ps.V = st.V;
     ps.c0 = c0;
@@ -514,9 +632,15 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
     const int N = st.N, H = st.H, V = st.V;
     const int c0 = st.chunk * kBwdChunk;
     const int width = (V - c0) < kBwdChunk ? (V - c0) : kBwdChunk;
-    if (st.role == kRoleDs)
-        return st.grad_ent != nullptr ? launch_ds<true>(maps, st, c0, width, num_sms, err, stream)
-                                      : launch_ds<false>(maps, st, c0, width, num_sms, err, stream);
+    if (st.role == kRoleDs) {
+        const cudaError_t e =
+            st.grad_ent != nullptr ? launch_ds<true>(maps, st, c0, width, num_sms, err, stream)
+                                   : launch_ds<false>(maps, st, c0, width, num_sms, err, stream);
+        if (e != cudaSuccess) return e;
+        // the tokens whose dominant non-target class the dS GEMM found in this chunk
+        return launch_dom_sort(st.dom, N, V, c0, c0 + width, st.tiles, st.sorted_dy,
+                               st.sorted_dt, stream);
+    }
     if (st.role == kRoleDh) {
         DhPolicy pd;
         pd.targets = st.targets;
@@ -526,6 +650,7 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
         pd.dh_acc = st.dh_acc;
         pd.dh = static_cast<__nv_bfloat16*>(st.dhidden);
         pd.ycoef = st.ycoef;
+        pd.dom = st.dom;
         pd.N = N;
         pd.V = V;
         pd.H = H;
@@ -546,6 +671,8 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
     pw.sorted_y = st.sorted_y;
     pw.sorted_t = st.sorted_t;
     pw.ycoef = st.ycoef;
+    pw.sorted_dy = st.sorted_dy;
+    pw.sorted_dt = st.sorted_dt;
     pw.N = N;
     pw.H = H;
     pw.c0 = c0;

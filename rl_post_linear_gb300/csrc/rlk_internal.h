@@ -57,17 +57,22 @@ struct FwdLayout {
 
 // Backward workspace: dS for one vocab chunk [N, kBwdChunk] bf16, the fp32 dh
 // accumulator [N, H], the (target, token) list sorted by target, 1 - p_y per
-// row, and the sorted key tiles the target list is built from.
+// row, each row's dominant non-target class and the chunk's (class, token) list
+// sorted by class, and the sorted key tiles the lists are built from.
 constexpr int kTargetSortTile = 2048;
 struct BwdLayout {
-    size_t ds_off, dhacc_off, sorted_y_off, sorted_t_off, ycoef_off, tiles_off, total;
+    size_t ds_off, dhacc_off, sorted_y_off, sorted_t_off, ycoef_off, dom_off, sorted_dy_off,
+        sorted_dt_off, tiles_off, total;
     BwdLayout(int64_t N, int64_t H) {
         ds_off = 0;
         dhacc_off = align_up(static_cast<size_t>(N) * kBwdChunk * 2, 256);
         sorted_y_off = align_up(dhacc_off + static_cast<size_t>(N) * H * 4, 256);
         sorted_t_off = align_up(sorted_y_off + static_cast<size_t>(N) * 4, 256);
         ycoef_off = align_up(sorted_t_off + static_cast<size_t>(N) * 4, 256);
-        tiles_off = align_up(ycoef_off + static_cast<size_t>(N) * 4, 256);
+        dom_off = align_up(ycoef_off + static_cast<size_t>(N) * 4, 256);
+        sorted_dy_off = align_up(dom_off + static_cast<size_t>(N) * 4, 256);
+        sorted_dt_off = align_up(sorted_dy_off + static_cast<size_t>(N) * 4, 256);
+        tiles_off = align_up(sorted_dt_off + static_cast<size_t>(N) * 4, 256);
         const size_t tiles = static_cast<size_t>((N + kTargetSortTile - 1) / kTargetSortTile);
         total = align_up(tiles_off + tiles * kTargetSortTile * 8, 256);
     }
@@ -156,13 +161,17 @@ struct BwdStep {
     const int* sorted_y;
     const int* sorted_t;
     float* ycoef;              // [N] 1 - p_y of each live row
+    int* dom;                  // [N] dominant non-target class (p > 1/2) or -1
+    int* sorted_dy;            // [N] this chunk's dominant classes, ascending (V: none)
+    int* sorted_dt;            // [N]
+    uint64_t* tiles;           // sort scratch
     void* dhidden;
     void* dweight;
 };
 
 cudaError_t launch_target_sort(const int64_t* targets, const uint8_t* mask, int N, int V,
-                               uint64_t* tiles, int* sorted_y, int* sorted_t, uint32_t* err,
-                               cudaStream_t stream);
+                               uint64_t* tiles, int* sorted_y, int* sorted_t, int* dom,
+                               uint32_t* err, cudaStream_t stream);
 
 cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& step, int num_sms,
                             uint32_t* err, cudaStream_t stream);
