@@ -116,6 +116,16 @@ def _load():
             lib.rlk_oracle_dlogp_audit_ext.argtypes = [_fp, _fp, _u8p, ctypes.c_int64, _i64p,
                                                        ctypes.c_int64, ctypes.c_double,
                                                        ctypes.POINTER(AuditExtResult)]
+            lib.rlk_oracle_linear_kl_fwd.restype = ctypes.c_int64
+            lib.rlk_oracle_linear_kl_fwd.argtypes = [
+                _dp, _dp, _dp, _dp, _u8p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                ctypes.c_int64, ctypes.c_double, ctypes.c_double, _dp, _dp, _dp, _dp]
+            for name in ("rlk_oracle_linear_kl_bwd_dh", "rlk_oracle_linear_kl_bwd_dw"):
+                f = getattr(lib, name)
+                f.restype = None
+                f.argtypes = [_dp, _dp, _dp, _dp, _u8p, _dp, _dp, _dp, _dp, _dp, ctypes.c_int64,
+                              ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_double,
+                              ctypes.c_double, ctypes.c_int64, ctypes.c_int64, _dp]
             lib.rlk_oracle_grpo_clip_grad.restype = ctypes.c_double
             lib.rlk_oracle_grpo_clip_grad.argtypes = [_dp, _dp, _dp, _u8p, ctypes.c_int64,
                                                       ctypes.c_double, _dp]
@@ -448,6 +458,98 @@ def linear_logp_entropy_bwd_dw_parallel(h, w, y, mask, g, gh, lse, ent, temperat
         if a < b:
             out[a:b] = linear_logp_entropy_bwd_dw(h, w, y, mask, g, gh, lse, ent, temperature,
                                                   a, b)
+
+    _split_parallel(w.shape[0], fn, threads)
+    return out
+
+
+def linear_kl_fwd(h, w, hr, wr, mask, temperature, temperature_ref):
+    """Full-vocabulary KL of the policy head (h, W, T) against a reference head
+    (hr, Wr, Tr): kl = KL(p || q), kl_rev = KL(q || p), lse, lse_ref (float64 [N])."""
+    lib = _load()
+    h, w, hr, wr = (_c(x, np.float64) for x in (h, w, hr, wr))
+    n, hdim = h.shape
+    m = _mask_arg(mask, n)
+    out = [np.empty(n, np.float64) for _ in range(4)]
+    if lib.rlk_oracle_linear_kl_fwd(_ptr(h, _dp), _ptr(w, _dp), _ptr(hr, _dp), _ptr(wr, _dp),
+                                    _ptr(m, _u8p), n, hdim, hr.shape[1], w.shape[0],
+                                    float(temperature), float(temperature_ref),
+                                    *(_ptr(o, _dp) for o in out)) < 0:
+        raise MemoryError("oracle KL forward: scratch allocation failed")
+    return tuple(out)
+
+
+def linear_kl_fwd_parallel(h, w, hr, wr, mask, temperature, temperature_ref, threads=None):
+    h, w, hr, wr = (_c(x, np.float64) for x in (h, w, hr, wr))
+    n = h.shape[0]
+    m = _mask_arg(mask, n)
+    out = [np.empty(n, np.float64) for _ in range(4)]
+
+    def fn(a, b):
+        if a < b:
+            r = linear_kl_fwd(h[a:b], w, hr[a:b], wr, None if m is None else m[a:b],
+                              temperature, temperature_ref)
+            for o, x in zip(out, r):
+                o[a:b] = x
+
+    _split_parallel(n, fn, threads)
+    return tuple(out)
+
+
+def _kl_bwd(name, h, w, hr, wr, mask, g, gr, lse, lse_ref, kl, temperature, temperature_ref,
+            begin, end, width):
+    lib = _load()
+    h, w, hr, wr = (_c(x, np.float64) for x in (h, w, hr, wr))
+    n, hdim = h.shape
+    m = _mask_arg(mask, n)
+    g, gr, lse, lse_ref, kl = (_c(x, np.float64) for x in (g, gr, lse, lse_ref, kl))
+    out = np.empty((end - begin, width), np.float64)
+    getattr(lib, name)(_ptr(h, _dp), _ptr(w, _dp), _ptr(hr, _dp), _ptr(wr, _dp), _ptr(m, _u8p),
+                       _ptr(g, _dp), _ptr(gr, _dp), _ptr(lse, _dp), _ptr(lse_ref, _dp),
+                       _ptr(kl, _dp), n, hdim, hr.shape[1], w.shape[0], float(temperature),
+                       float(temperature_ref), begin, end, _ptr(out, _dp))
+    return out
+
+
+def linear_kl_bwd_dh(h, w, hr, wr, mask, g, gr, lse, lse_ref, kl, temperature, temperature_ref,
+                     row_begin=0, row_end=None):
+    """Rows [row_begin, row_end) of dL/dh for L = sum g kl + sum gr kl_rev."""
+    row_end = np.asarray(h).shape[0] if row_end is None else row_end
+    return _kl_bwd("rlk_oracle_linear_kl_bwd_dh", h, w, hr, wr, mask, g, gr, lse, lse_ref, kl,
+                   temperature, temperature_ref, row_begin, row_end, np.asarray(h).shape[1])
+
+
+def linear_kl_bwd_dw(h, w, hr, wr, mask, g, gr, lse, lse_ref, kl, temperature, temperature_ref,
+                     v_begin=0, v_end=None):
+    """Rows [v_begin, v_end) of dL/dW for L = sum g kl + sum gr kl_rev."""
+    v_end = np.asarray(w).shape[0] if v_end is None else v_end
+    return _kl_bwd("rlk_oracle_linear_kl_bwd_dw", h, w, hr, wr, mask, g, gr, lse, lse_ref, kl,
+                   temperature, temperature_ref, v_begin, v_end, np.asarray(h).shape[1])
+
+
+def linear_kl_bwd_dh_parallel(h, w, hr, wr, mask, g, gr, lse, lse_ref, kl, temperature,
+                              temperature_ref, threads=None):
+    h = _c(h, np.float64)
+    out = np.empty(h.shape, np.float64)
+
+    def fn(a, b):
+        if a < b:
+            out[a:b] = linear_kl_bwd_dh(h, w, hr, wr, mask, g, gr, lse, lse_ref, kl, temperature,
+                                        temperature_ref, a, b)
+
+    _split_parallel(h.shape[0], fn, threads)
+    return out
+
+
+def linear_kl_bwd_dw_parallel(h, w, hr, wr, mask, g, gr, lse, lse_ref, kl, temperature,
+                              temperature_ref, threads=None):
+    w = _c(w, np.float64)
+    out = np.empty((w.shape[0], np.asarray(h).shape[1]), np.float64)
+
+    def fn(a, b):
+        if a < b:
+            out[a:b] = linear_kl_bwd_dw(h, w, hr, wr, mask, g, gr, lse, lse_ref, kl, temperature,
+                                        temperature_ref, a, b)
 
     _split_parallel(w.shape[0], fn, threads)
     return out

@@ -26,6 +26,9 @@
  *    active masks, LM-head weight, vocab size, rollout temperature), the
  *    max / sum-exp / selected-target-logit statistics, full-gradient
  *    backward from dlogits.
+ *  - "RL-Kernel Roadmap (2026)", backlog: fused entropy, and chunked
+ *    full-vocab / distillation KL fused with lm_head (forward and reverse KL
+ *    over the whole distribution).
  *  - "RL-Kernel integration roadmap for vime", Consistency Contract: dlogp =
  *    recomputed - old; every metric over active tokens only; max_abs_dlogp
  *    is the primary metric; approx_kl0 = mean(exp(dlogp) - 1 - dlogp);
@@ -520,4 +523,120 @@ int rlk_oracle_dlogp_audit_ext(const float* logp_new, const float* logp_old, con
     out->clipfrac = (double)clip / (double)count;
     free(absd);
     return 0;
+}
+
+/*
+ * Full-vocabulary KL between the policy head and a reference head ("RL-Kernel
+ * Roadmap (2026)", backlog: chunked full-vocab KL / distillation KL fused with
+ * lm_head, forward and reverse KL beyond the sampled token).  For every
+ * active row t, with the policy logits z[v] = (h_t . W_v) / T and the
+ * reference logits r[v] = (hr_t . Wr_v) / Tr over the same vocabulary:
+ *   log p[v] = z[v] - LSE(z),  log q[v] = r[v] - LSE(r)
+ *   kl_t     = sum_v p[v] (log p[v] - log q[v])         KL(p || q)
+ *   kl_rev_t = sum_v q[v] (log q[v] - log p[v])         KL(q || p)
+ * Inactive rows: every output 0.  The reference hidden size may differ.
+ */
+static double logsumexp(const double* z, int64_t vocab) {
+    double m = -INFINITY;
+    for (int64_t v = 0; v < vocab; ++v) if (z[v] > m) m = z[v];
+    double sum = 0.0;
+    for (int64_t v = 0; v < vocab; ++v) sum += exp(z[v] - m);
+    return m + log(sum);
+}
+
+int64_t rlk_oracle_linear_kl_fwd(const double* h, const double* w, const double* hr,
+                                 const double* wr, const uint8_t* mask, int64_t n, int64_t hdim,
+                                 int64_t hrdim, int64_t vocab, double temperature,
+                                 double temperature_ref, double* kl, double* kl_rev, double* lse,
+                                 double* lse_ref) {
+    double* z = (double*)malloc((size_t)(vocab > 0 ? vocab : 1) * sizeof(double));
+    double* r = (double*)malloc((size_t)(vocab > 0 ? vocab : 1) * sizeof(double));
+    if (z == NULL || r == NULL) {
+        free(z);
+        free(r);
+        return -1;
+    }
+    for (int64_t t = 0; t < n; ++t) {
+        if (!row_active(mask, t)) {
+            kl[t] = kl_rev[t] = lse[t] = lse_ref[t] = 0.0;
+            continue;
+        }
+        for (int64_t v = 0; v < vocab; ++v) {
+            z[v] = dot(h + t * hdim, w + v * hdim, hdim) / temperature;
+            r[v] = dot(hr + t * hrdim, wr + v * hrdim, hrdim) / temperature_ref;
+        }
+        const double lz = logsumexp(z, vocab), lr = logsumexp(r, vocab);
+        double f = 0.0, b = 0.0;
+        for (int64_t v = 0; v < vocab; ++v) {
+            const double lp = z[v] - lz, lq = r[v] - lr;
+            f += exp(lp) * (lp - lq);
+            b += exp(lq) * (lq - lp);
+        }
+        kl[t] = f;
+        kl_rev[t] = b;
+        lse[t] = lz;
+        lse_ref[t] = lr;
+    }
+    free(z);
+    free(r);
+    return 0;
+}
+
+/*
+ * Backward of L = sum_t (g_t kl_t + gr_t kl_rev_t) with respect to the policy
+ * head only (the reference is fixed).  With l[v] = log p[v] - log q[v]:
+ *   dkl_t/dz_v     = p[v] (l[v] - kl_t)
+ *   dkl_rev_t/dz_v = p[v] - q[v]
+ *   G[t][v] = ( g_t p[v] (l[v] - kl_t) + gr_t (p[v] - q[v]) ) / T
+ *   dh_t = sum_v G[t][v] W_v (ascending v),  dW_v = sum_t G[t][v] h_t
+ * (ascending t).  lse, lse_ref and kl are the forward's outputs.
+ */
+static double kl_coef(const double* h, const double* w, const double* hr, const double* wr,
+                      int64_t t, int64_t v, int64_t hdim, int64_t hrdim, double temperature,
+                      double temperature_ref, double g, double gr, double lse, double lse_ref,
+                      double kl) {
+    const double lp = dot(h + t * hdim, w + v * hdim, hdim) / temperature - lse;
+    const double lq = dot(hr + t * hrdim, wr + v * hrdim, hrdim) / temperature_ref - lse_ref;
+    const double p = exp(lp), q = exp(lq);
+    return (g * p * ((lp - lq) - kl) + gr * (p - q)) / temperature;
+}
+
+void rlk_oracle_linear_kl_bwd_dh(const double* h, const double* w, const double* hr,
+                                 const double* wr, const uint8_t* mask, const double* g,
+                                 const double* gr, const double* lse, const double* lse_ref,
+                                 const double* kl, int64_t n, int64_t hdim, int64_t hrdim,
+                                 int64_t vocab, double temperature, double temperature_ref,
+                                 int64_t row_begin, int64_t row_end, double* dh) {
+    (void)n;
+    for (int64_t t = row_begin; t < row_end; ++t) {
+        double* out = dh + (t - row_begin) * hdim;
+        for (int64_t k = 0; k < hdim; ++k) out[k] = 0.0;
+        if (!row_active(mask, t)) continue;
+        for (int64_t v = 0; v < vocab; ++v) {
+            const double G = kl_coef(h, w, hr, wr, t, v, hdim, hrdim, temperature,
+                                     temperature_ref, g[t], gr[t], lse[t], lse_ref[t], kl[t]);
+            const double* wv = w + v * hdim;
+            for (int64_t k = 0; k < hdim; ++k) out[k] += G * wv[k];
+        }
+    }
+}
+
+void rlk_oracle_linear_kl_bwd_dw(const double* h, const double* w, const double* hr,
+                                 const double* wr, const uint8_t* mask, const double* g,
+                                 const double* gr, const double* lse, const double* lse_ref,
+                                 const double* kl, int64_t n, int64_t hdim, int64_t hrdim,
+                                 int64_t vocab, double temperature, double temperature_ref,
+                                 int64_t v_begin, int64_t v_end, double* dw) {
+    (void)vocab;
+    for (int64_t v = v_begin; v < v_end; ++v) {
+        double* out = dw + (v - v_begin) * hdim;
+        for (int64_t k = 0; k < hdim; ++k) out[k] = 0.0;
+        for (int64_t t = 0; t < n; ++t) {
+            if (!row_active(mask, t)) continue;
+            const double G = kl_coef(h, w, hr, wr, t, v, hdim, hrdim, temperature,
+                                     temperature_ref, g[t], gr[t], lse[t], lse_ref[t], kl[t]);
+            const double* ht = h + t * hdim;
+            for (int64_t k = 0; k < hdim; ++k) out[k] += G * ht[k];
+        }
+    }
 }

@@ -13,6 +13,11 @@ h = 0 and W = 0.
 Audit and GRPO: hand-built vectors, exact rational means, finite differences
 of the clipped objective, and the clip branches.
 
+Full-vocabulary KL against a reference head: identical heads give exactly 0,
+swapping the heads swaps the two directions, V = 2 gives the Bernoulli KL of
+two log-sigmoids, 60-digit brute force on an 11-entry vocabulary, and central
+finite differences of sum g kl + sum gr kl_rev for the backward.
+
 The method is the fused linear selected-token log-prob of "RL-Kernel Roadmap
 (2026)" P0.2 and "RL-Kernel integration roadmap for vime" (linear_logp /
 lm_head + logp; Consistency Contract for the audit).
@@ -612,3 +617,107 @@ def test_audit_ext_small_counts_and_masked(oracle_lib):
     r = o.dlogp_audit_ext(np.array([0.1, float("nan"), 0.2], np.float32), np.zeros(3, np.float32),
                           None)
     assert math.isnan(r["p99_abs_dlogp"]) and r["p50_abs_dlogp"] == float(np.float32(0.2))
+
+
+# ----------------------------------------------------------------------------- full-vocabulary KL
+
+def test_kl_identical_heads_and_swap(oracle_lib):
+    o = oracle_lib
+    rng = np.random.default_rng(50)
+    h, hr = _bf16_grid(rng, (4, 12), 1.0), _bf16_grid(rng, (4, 6), 1.0)
+    w, wr = _bf16_grid(rng, (30, 12), 0.5), _bf16_grid(rng, (30, 6), 0.5)
+    # the same head on both sides: both divergences vanish exactly, the lse is the logp-only one
+    kl, kr, lse, lse_r = o.linear_kl_fwd(h, w, h, w, None, 0.8, 0.8)
+    assert np.all(kl == 0) and np.all(kr == 0) and np.array_equal(lse, lse_r)
+    _, lse0 = o.linear_logp_fwd(h, w, np.zeros(4, np.int64), None, 0.8)
+    assert np.array_equal(lse, lse0)
+    # swapping the heads swaps the two directions; both are non-negative
+    a = o.linear_kl_fwd(h, w, hr, wr, None, 0.8, 1.4)
+    b = o.linear_kl_fwd(hr, wr, h, w, None, 1.4, 0.8)
+    assert np.array_equal(a[0], b[1]) and np.array_equal(a[1], b[0])
+    assert np.all(a[0] > 0) and np.all(a[1] > 0)
+    # masked rows are all zero
+    m = np.array([1, 0, 1, 0], np.uint8)
+    c = o.linear_kl_fwd(h, w, hr, wr, m, 0.8, 1.4)
+    assert all(np.all(x[m == 0] == 0) for x in c)
+    assert all(np.array_equal(x[m == 1], y[m == 1]) for x, y in zip(c, a))
+
+
+def test_kl_two_entry_vocab_is_bernoulli_kl(oracle_lib):
+    o = oracle_lib
+    rng = np.random.default_rng(51)
+    h, hr = _bf16_grid(rng, (5, 8), 1.0), _bf16_grid(rng, (5, 8), 1.0)
+    w, wr = _bf16_grid(rng, (2, 8), 0.6), _bf16_grid(rng, (2, 8), 0.6)
+    T, Tr = 0.9, 1.2
+    kl, kr, _, _ = o.linear_kl_fwd(h, w, hr, wr, None, T, Tr)
+    for t in range(5):
+        a = (h[t] @ (w[1] - w[0])) / T                  # logit gap of the policy
+        b = (hr[t] @ (wr[1] - wr[0])) / Tr              # and of the reference
+        p1, q1 = 1 / (1 + math.exp(-a)), 1 / (1 + math.exp(-b))
+        ls = lambda x: -math.log1p(math.exp(-x))        # log sigmoid
+        lp1, lp0, lq1, lq0 = ls(a), ls(-a), ls(b), ls(-b)
+        f = p1 * (lp1 - lq1) + (1 - p1) * (lp0 - lq0)
+        r = q1 * (lq1 - lp1) + (1 - q1) * (lq0 - lp0)
+        assert abs(kl[t] - f) <= 1e-13 and abs(kr[t] - r) <= 1e-13
+
+
+def test_kl_brute_force_high_precision(oracle_lib):
+    getcontext().prec = 60
+    o = oracle_lib
+    rng = np.random.default_rng(52)
+    h, hr = _bf16_grid(rng, (3, 10), 2.0), _bf16_grid(rng, (3, 7), 2.0)
+    w, wr = _bf16_grid(rng, (11, 10), 0.7), _bf16_grid(rng, (11, 7), 0.7)
+    T, Tr = 0.7, 1.1
+    kl, kr, lse, lse_r = o.linear_kl_fwd(h, w, hr, wr, None, T, Tr)
+
+    def logits(x, m, temp):
+        out = []
+        for v in range(m.shape[0]):
+            q = sum(Fraction(a) * Fraction(b) for a, b in zip(x, m[v])) / Fraction(temp)
+            out.append(Decimal(q.numerator) / Decimal(q.denominator))
+        return out
+
+    for t in range(3):
+        z, r = logits(h[t], w, T), logits(hr[t], wr, Tr)
+        zs = sum((x.exp() for x in z), Decimal(0))
+        rs = sum((x.exp() for x in r), Decimal(0))
+        lp = [x - zs.ln() for x in z]
+        lq = [x - rs.ln() for x in r]
+        f = sum((a.exp() * (a - b) for a, b in zip(lp, lq)), Decimal(0))
+        b_ = sum((b.exp() * (b - a) for a, b in zip(lp, lq)), Decimal(0))
+        assert abs(float(f) - kl[t]) < 1e-13 and abs(float(b_) - kr[t]) < 1e-13
+        assert abs(float(zs.ln()) - lse[t]) < 1e-13 and abs(float(rs.ln()) - lse_r[t]) < 1e-13
+
+
+@pytest.mark.parametrize("shape", [(2, 3, 4, 2), (3, 5, 6, 4)])
+def test_kl_backward_finite_differences(oracle_lib, shape):
+    o = oracle_lib
+    n, hdim, vocab, hrdim = shape
+    rng = np.random.default_rng(60 + n)
+    h, hr = rng.standard_normal((n, hdim)), rng.standard_normal((n, hrdim))
+    w, wr = rng.standard_normal((vocab, hdim)) * 0.7, rng.standard_normal((vocab, hrdim))
+    mask = np.ones(n, np.uint8)
+    mask[0] = 0 if n > 2 else 1
+    g, gr = rng.standard_normal(n), rng.standard_normal(n)
+    T, Tr = 0.8, 1.3
+
+    def loss():
+        kl, kr, _, _ = o.linear_kl_fwd(h, w, hr, wr, mask, T, Tr)
+        return float(np.dot(g, kl) + np.dot(gr, kr))
+
+    kl, _, lse, lse_r = o.linear_kl_fwd(h, w, hr, wr, mask, T, Tr)
+    dh = o.linear_kl_bwd_dh(h, w, hr, wr, mask, g, gr, lse, lse_r, kl, T, Tr)
+    dw = o.linear_kl_bwd_dw(h, w, hr, wr, mask, g, gr, lse, lse_r, kl, T, Tr)
+    step = 1e-6
+    for arr, grad in ((h, dh), (w, dw)):
+        for idx in np.ndindex(arr.shape):
+            keep = arr[idx]
+            arr[idx] = keep + step
+            up = loss()
+            arr[idx] = keep - step
+            dn = loss()
+            arr[idx] = keep
+            fd = (up - dn) / (2 * step)
+            assert abs(fd - grad[idx]) <= 1e-7 * max(1.0, abs(fd)), (idx, fd, grad[idx])
+    # the reference head gets no gradient, and every row of G sums to zero, so the dW columns do
+    assert np.abs(dw.sum(axis=0)).max() <= 1e-12 * max(1.0, np.abs(dw).max())
