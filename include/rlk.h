@@ -201,6 +201,43 @@ rlk_status_t rlk_linear_logp_entropy_bwd(const void* hidden, const void* weight,
                                          cudaStream_t stream);
 
 /*
+ * Full-vocabulary KL between the policy head and a reference head (a frozen
+ * reference policy, or a teacher for distillation).  "RL-Kernel Roadmap
+ * (2026)", backlog: chunked full-vocab KL / distillation KL fused with
+ * lm_head, forward and reverse KL over the whole distribution.  For active
+ * rows, with p = softmax(hidden W^T / T) and q = softmax(hidden_ref Wr^T / Tr):
+ *
+ *   kl[t]      = sum_v p[t,v] (log p[t,v] - log q[t,v])        KL(p || q)
+ *   kl_rev[t]  = sum_v q[t,v] (log q[t,v] - log p[t,v])        KL(q || p)
+ *   lse[t], lse_ref[t]   the two log-partition functions (natural log)
+ *   logp[t]    = log p[t, y_t] when targets are given (lse and logp agree with
+ *                rlk_linear_logp_fwd's to fp32 rounding)
+ *
+ * Neither [N,V] logit tensor is materialised: each vocab tile is computed for
+ * both heads into the two tensor-memory accumulators and folded into online
+ * statistics, merged across 1024-column chunks in ascending order (fixed for
+ * a given V: batch invariant).  Inactive rows get 0 everywhere.
+ *
+ *   hidden [N,H], weight [V,H]; hidden_ref [N,H_ref], weight_ref [V,H_ref]:
+ *       bf16, row-major, 16-byte aligned; H and H_ref multiples of 64
+ *   targets  [N] int64 or NULL (then logp_out must be NULL)
+ *   kl_out   [N] fp32, required; kl_rev_out, lse_out, lse_ref_out, logp_out:
+ *       [N] fp32 or NULL
+ *   workspace  rlk_linear_kl_fwd_workspace_bytes(N, V) bytes, 256-aligned
+ * Errors as rlk_linear_logp_fwd; an active out-of-range target gives logp NaN
+ * and RLK_DEVERR_TARGET_RANGE.
+ */
+size_t rlk_linear_kl_fwd_workspace_bytes(int64_t N, int64_t V);
+rlk_status_t rlk_linear_kl_fwd(const void* hidden, const void* weight, const void* hidden_ref,
+                               const void* weight_ref, const int64_t* targets,
+                               const uint8_t* active_mask, int64_t N, int64_t H, int64_t H_ref,
+                               int64_t V, double temperature, double temperature_ref,
+                               float* kl_out, float* kl_rev_out, float* lse_out,
+                               float* lse_ref_out, float* logp_out, void* workspace,
+                               size_t workspace_bytes, uint32_t* device_error_word,
+                               cudaStream_t stream);
+
+/*
  * Masked dlogp audit.  "RL-Kernel integration roadmap for vime", Consistency
  * Contract: dlogp = recomputed - old over active tokens only; max_abs_dlogp
  * (the primary metric) with the worst-token index; approx_kl0 =

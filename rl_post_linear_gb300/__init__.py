@@ -111,6 +111,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.rlk_linear_logp_entropy_fwd.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64,
                                                 ctypes.c_double, _vp, _vp, _vp, _vp, _sz, _vp,
                                                 _vp]
+    lib.rlk_linear_kl_fwd_workspace_bytes.restype = _sz
+    lib.rlk_linear_kl_fwd_workspace_bytes.argtypes = [_i64, _i64]
+    lib.rlk_linear_kl_fwd.restype = ctypes.c_int
+    lib.rlk_linear_kl_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
+                                      ctypes.c_double, ctypes.c_double, _vp, _vp, _vp, _vp, _vp,
+                                      _vp, _sz, _vp, _vp]
     lib.rlk_linear_logp_entropy_bwd.restype = ctypes.c_int
     lib.rlk_linear_logp_entropy_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64,
                                                 _i64, _i64, ctypes.c_double, _vp, _vp, _vp, _sz,
@@ -310,6 +316,40 @@ def rlk_linear_logp_entropy_bwd(hidden, weight, targets, active_mask, grad_logp,
     _check("rlk_linear_logp_entropy_bwd", st)
 
 
+def rlk_linear_kl_fwd_workspace_bytes(N: int, V: int) -> int:
+    return int(load().rlk_linear_kl_fwd_workspace_bytes(N, V))
+
+
+def rlk_linear_kl_fwd(hidden, weight, hidden_ref, weight_ref, targets, active_mask, temperature,
+                      temperature_ref, kl_out, kl_rev_out, lse_out, lse_ref_out, logp_out,
+                      workspace, device_error_word=None, stream=None):
+    """Full-vocabulary KL of the policy head against a reference head; see include/rlk.h."""
+    n, h = hidden.shape
+    v = weight.shape[0]
+    hr = hidden_ref.shape[1]
+    _need(hidden, torch.bfloat16, "hidden")
+    _need(weight, torch.bfloat16, "weight", (v, h))
+    _need(hidden_ref, torch.bfloat16, "hidden_ref", (n, hr))
+    _need(weight_ref, torch.bfloat16, "weight_ref", (v, hr))
+    if targets is not None:
+        _need(targets, torch.int64, "targets", (n,))
+    if active_mask is not None:
+        _need(active_mask, torch.uint8, "active_mask", (n,))
+    _need(kl_out, torch.float32, "kl_out", (n,))
+    for t, name in ((kl_rev_out, "kl_rev_out"), (lse_out, "lse_out"),
+                    (lse_ref_out, "lse_ref_out"), (logp_out, "logp_out")):
+        if t is not None:
+            _need(t, torch.float32, name, (n,))
+    _need(workspace, torch.uint8, "workspace")
+    st = load().rlk_linear_kl_fwd(_ptr(hidden), _ptr(weight), _ptr(hidden_ref), _ptr(weight_ref),
+                                  _ptr(targets), _ptr(active_mask), n, h, hr, v,
+                                  float(temperature), float(temperature_ref), _ptr(kl_out),
+                                  _ptr(kl_rev_out), _ptr(lse_out), _ptr(lse_ref_out),
+                                  _ptr(logp_out), _ptr(workspace), workspace.numel(),
+                                  _ptr(device_error_word), _stream(stream))
+    _check("rlk_linear_kl_fwd", st)
+
+
 def rlk_dlogp_audit(logp_new, logp_old, active_mask, result, workspace, stream=None):
     """Enqueue the audit; ``result`` is a uint8 CUDA tensor of AUDIT_RESULT_BYTES bytes."""
     n = logp_new.shape[0]
@@ -507,6 +547,21 @@ def linear_logp_entropy_bwd(hidden, weight, targets, active_mask, grad_logp, gra
     rlk_linear_logp_entropy_bwd(hidden, weight, targets, active_mask, grad_logp, grad_entropy,
                                 lse, entropy, temperature, dh, dw, ws, error_word)
     return dh, dw
+
+
+def linear_kl_fwd(hidden, weight, hidden_ref, weight_ref, active_mask=None, temperature=1.0,
+                  temperature_ref=None, targets=None, error_word=None):
+    """(kl, kl_rev, lse, lse_ref, logp or None), each fp32 [N]: KL(p || q) and KL(q || p)
+    between the policy head (hidden, weight, temperature) and the reference head."""
+    n = hidden.shape[0]
+    v = weight.shape[0]
+    temperature_ref = temperature if temperature_ref is None else temperature_ref
+    outs = [torch.empty(n, dtype=torch.float32, device=hidden.device) for _ in range(4)]
+    logp = None if targets is None else torch.empty(n, dtype=torch.float32, device=hidden.device)
+    ws = _workspace(rlk_linear_kl_fwd_workspace_bytes(n, v), hidden.device)
+    rlk_linear_kl_fwd(hidden, weight, hidden_ref, weight_ref, targets, active_mask, temperature,
+                      temperature_ref, *outs, logp, ws, error_word)
+    return (*outs, logp)
 
 
 def audit_result_to_dict(raw: torch.Tensor) -> dict:

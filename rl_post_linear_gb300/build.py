@@ -17,7 +17,8 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "librlk.so")
-SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "audit.cu", "loss.cu", "logits.cu", "compact.cu"]
+SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "audit.cu", "loss.cu", "logits.cu", "compact.cu",
+           "kl.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -168,6 +168,49 @@ rlk_status_t rlk_linear_logp_fwd(const void* hidden, const void* weight, const i
                     nullptr, workspace, workspace_bytes, device_error_word, stream);
 }
 
+size_t rlk_linear_kl_fwd_workspace_bytes(int64_t N, int64_t V) {
+    if (N < 0 || V < 1) return 0;
+    return rlk::KlFwdLayout(N, V).total;
+}
+
+rlk_status_t rlk_linear_kl_fwd(const void* hidden, const void* weight, const void* hidden_ref,
+                               const void* weight_ref, const int64_t* targets,
+                               const uint8_t* active_mask, int64_t N, int64_t H, int64_t H_ref,
+                               int64_t V, double temperature, double temperature_ref,
+                               float* kl_out, float* kl_rev_out, float* lse_out,
+                               float* lse_ref_out, float* logp_out, void* workspace,
+                               size_t workspace_bytes, uint32_t* device_error_word,
+                               cudaStream_t stream) {
+    RLK_TRY(check_shape(N, H, V, temperature));
+    RLK_TRY(check_shape(N, H_ref, V, temperature_ref));
+    if (N == 0) return RLK_OK;
+    if (hidden == nullptr || weight == nullptr || hidden_ref == nullptr ||
+        weight_ref == nullptr || kl_out == nullptr)
+        return RLK_ERR_INVALID_VALUE;
+    if (logp_out != nullptr && targets == nullptr) return RLK_ERR_INVALID_VALUE;
+    if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(hidden_ref, 16) ||
+        !aligned(weight_ref, 16))
+        return RLK_ERR_INVALID_VALUE;
+    if (workspace == nullptr || !aligned(workspace, 256) ||
+        workspace_bytes < rlk_linear_kl_fwd_workspace_bytes(N, V))
+        return RLK_ERR_WORKSPACE;
+    DeviceInfo dev;
+    RLK_TRY(current_device(dev));
+    CUtensorMap map_h, map_w, map_hr, map_wr;
+    RLK_TRY(make_map(&map_h, hidden, H, N, H * 2, 64, rlk::kTileM));
+    RLK_TRY(make_map(&map_w, weight, H, V, H * 2, 64, rlk::kTileV));
+    RLK_TRY(make_map(&map_hr, hidden_ref, H_ref, N, H_ref * 2, 64, rlk::kTileM));
+    RLK_TRY(make_map(&map_wr, weight_ref, H_ref, V, H_ref * 2, 64, rlk::kTileV));
+    const float k = static_cast<float>(1.4426950408889634074 / temperature);
+    const float kr = static_cast<float>(1.4426950408889634074 / temperature_ref);
+    RLK_CUDA(rlk::launch_kl_fwd(map_h, map_w, map_hr, map_wr, targets, active_mask,
+                                static_cast<int>(N), static_cast<int>(H),
+                                static_cast<int>(H_ref), static_cast<int>(V), k, kr, kl_out,
+                                kl_rev_out, lse_out, lse_ref_out, logp_out, workspace,
+                                device_error_word, dev.sms, stream));
+    return RLK_OK;
+}
+
 rlk_status_t rlk_linear_logp_entropy_fwd(const void* hidden, const void* weight,
                                          const int64_t* targets, const uint8_t* active_mask,
                                          int64_t N, int64_t H, int64_t V, double temperature,

@@ -91,6 +91,12 @@ __device__ __forceinline__ uint64_t operand_desc_rt(bool mn_major, uint32_t stag
 //   a_mn(u), b_mn(u)                      operand majorness of unit u
 //   num_units(), tiles_in_unit(u), k_blocks(u), coords(u, q, ...)
 //   EpiState, epi_begin / epi_tile / epi_end
+//   kPairTiles                            false: one epilogue call per tile
+// With kPairTiles the tiles of a unit come in pairs (2i, 2i+1) that may use
+// different operands (tile_a_map / tile_b_map / tile_k_blocks(u, q)); the
+// epilogue sees both accumulators at once (epi_pair, after the odd tile) and
+// releases the two TMEM buffers together.  Units then hold an even number of
+// tiles, so a pair always occupies buffers 0 and 1.
 // TwoMaps serves the single-role policies.
 struct TwoMaps {
     CUtensorMap a, b;
@@ -100,6 +106,7 @@ struct TwoMaps {
 template <bool AMN, bool BMN>
 struct SingleRole {
     using Maps = TwoMaps;
+    static constexpr bool kPairTiles = false;
     static constexpr bool kAMn = AMN;
     static constexpr bool kBMn = BMN;
     __device__ static void prefetch(const Maps& m) {
@@ -218,15 +225,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 for (int q = 0; ok && q < nt; ++q) {
                     int a_mn, a_k, b_mn, b_k;
                     p.coords(u, q, a_mn, a_k, b_mn, b_k);
-                    for (int kb = 0; kb < kblocks; ++kb) {
+                    const CUtensorMap* qa = ma;
+                    const CUtensorMap* qb = mb;
+                    int qk = kblocks;
+                    if constexpr (P::kPairTiles) {
+                        qa = p.tile_a_map(maps, u, q);
+                        qb = p.tile_b_map(maps, u, q);
+                        qk = p.tile_k_blocks(u, q);
+                    }
+                    for (int kb = 0; kb < qk; ++kb) {
                         if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, kWaitTimeoutNs)) {
                             ok = false;
                             break;
                         }
                         mbar_arrive_expect_tx(&full[stage], kStageBytes);
-                        load_operand_rt<kBM>(amn, a_stages + stage * kAStageBytes, ma,
+                        load_operand_rt<kBM>(amn, a_stages + stage * kAStageBytes, qa,
                                              &full[stage], a_mn, a_k + kb * kBK);
-                        load_operand_rt<kBN>(bmn, b_stages + stage * kBStageBytes, mb,
+                        load_operand_rt<kBN>(bmn, b_stages + stage * kBStageBytes, qb,
                                              &full[stage], b_mn, b_k + kb * kBK);
                         issued_mask |= 1u << stage;
                         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -266,7 +281,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * kBN;
-                    for (int kb = 0; kb < kblocks; ++kb) {
+                    int qk = kblocks;
+                    if constexpr (P::kPairTiles) qk = p.tile_k_blocks(u, q);
+                    for (int kb = 0; kb < qk; ++kb) {
                         if (!mbar_wait(&full[stage], phase, abort_flag, kWaitTimeoutNs)) {
                             ok = false;
                             break;
@@ -317,11 +334,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                p.epi_tile(u, q, row, taddr_row + buf * kBN, st);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tmem_empty[buf]);
+                if constexpr (P::kPairTiles) {
+                    if ((q & 1) == 0) continue;       // hold the even tile's buffer
+                    tc_fence_after();
+                    p.epi_pair(u, q, row, taddr_row + (buf ^ 1u) * kBN, taddr_row + buf * kBN, st);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&tmem_empty[buf ^ 1u]);
+                        mbar_arrive(&tmem_empty[buf]);
+                    }
+                } else {
+                    tc_fence_after();
+                    p.epi_tile(u, q, row, taddr_row + buf * kBN, st);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tmem_empty[buf]);
+                }
             }
             if (!ok) break;
             p.epi_end(u, row, st);

@@ -105,6 +105,32 @@ inline size_t audit_v3_blocks(int64_t N) {
 }
 
 // Launchers (return the first CUDA error, cudaSuccess otherwise).
+// Full-vocabulary KL forward workspace: per (1024-column chunk, row) the
+// policy's (max, sum) float2 and sum of weighted log-ratios, the same for the
+// reference, and the policy's target logit per row.
+struct KlFwdLayout {
+    int64_t num_chunks;
+    size_t part_p_off, part_a_off, part_r_off, part_b_off, target_off, total;
+    KlFwdLayout(int64_t N, int64_t V) {
+        const int64_t vt = (V + kTileV - 1) / kTileV;
+        num_chunks = (vt + kFwdTilesPerChunk - 1) / kFwdTilesPerChunk;
+        const size_t cn = static_cast<size_t>(num_chunks) * N;
+        part_p_off = 0;
+        part_a_off = align_up(cn * 8, 256);
+        part_r_off = align_up(part_a_off + cn * 4, 256);
+        part_b_off = align_up(part_r_off + cn * 8, 256);
+        target_off = align_up(part_b_off + cn * 4, 256);
+        total = align_up(target_off + static_cast<size_t>(N) * 4, 256);
+    }
+};
+
+cudaError_t launch_kl_fwd(const CUtensorMap& map_h, const CUtensorMap& map_w,
+                          const CUtensorMap& map_hr, const CUtensorMap& map_wr,
+                          const int64_t* targets, const uint8_t* mask, int N, int H, int Hr, int V,
+                          float k, float kr, float* kl, float* kl_rev, float* lse, float* lse_ref,
+                          float* logp, void* workspace, uint32_t* err, int num_sms,
+                          cudaStream_t stream);
+
 // rows / n_rows / pos_of: the compaction of a masked batch (all nullptr when the
 // GEMM runs over the original rows).
 cudaError_t launch_fwd(const CUtensorMap& map_h, const CUtensorMap& map_w,

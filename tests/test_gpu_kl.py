@@ -1,0 +1,110 @@
+"""Full-vocabulary KL of the policy head against a reference head ("RL-Kernel
+Roadmap (2026)", backlog: chunked full-vocab KL / distillation KL fused with
+lm_head, forward and reverse KL), against the fp64 oracle.
+
+Forward KL, reverse KL and both log-partition functions within 1e-3 absolute
+(the log-domain tolerance of logp); exact identities: identical heads give 0,
+swapping the heads swaps the two directions bit for bit; the policy's lse and
+logp agree with rlk_linear_logp_fwd's to fp32 rounding (the two kernels fold
+the same terms in the same order, but the compiler may fuse the rescale and
+the first addition differently); and batch invariance."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rl_post_linear_gb300 as rlk
+import workloads as wl
+from helpers import LOGP_ATOL, dev, f64, same_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _heads(n, h, hr, v, seed, std=0.05, std_r=0.05, active=0.85):
+    hidden = wl.normal_bf16((n, h), seed, wl.S_HIDDEN)
+    weight = wl.normal_bf16((v, h), seed, wl.S_WEIGHT, std=std)
+    hidden_r = wl.normal_bf16((n, hr), seed + 1, wl.S_HIDDEN)
+    weight_r = wl.normal_bf16((v, hr), seed + 1, wl.S_WEIGHT, std=std_r)
+    targets = wl.uniform_targets(n, v, seed)
+    rng = np.random.default_rng(seed)
+    mask = torch.from_numpy((rng.random(n) < active).astype(np.uint8))
+    return hidden, weight, hidden_r, weight_r, targets, mask
+
+
+def _gpu(hidden, weight, hidden_r, weight_r, mask, T, Tr, targets=None):
+    d = dev()
+    err = torch.zeros(1, dtype=torch.int32, device=d)
+    out = rlk.linear_kl_fwd(hidden.to(d), weight.to(d), hidden_r.to(d), weight_r.to(d),
+                            None if mask is None else mask.to(d), T, Tr,
+                            None if targets is None else targets.to(d), err)
+    torch.cuda.synchronize()
+    return [None if x is None else x.cpu() for x in out], int(err.item())
+
+
+@pytest.mark.parametrize("n,h,hr,v,T,Tr,std", [(64, 128, 64, 1000, 1.0, 1.0, 0.05),
+                                               (300, 256, 128, 5000, 0.7, 1.3, 0.1),
+                                               (129, 64, 192, 4097, 1.0, 0.5, 0.2),
+                                               (40, 128, 128, 20000, 0.9, 0.9, 0.5)])
+def test_parity(n, h, hr, v, T, Tr, std):
+    hidden, weight, hidden_r, weight_r, targets, mask = _heads(n, h, hr, v, n + v, std, std)
+    hidden[mask == 0] = float("nan")               # NaN padding never leaks into active rows
+    (kl, kr, lse, lse_r, _), err = _gpu(hidden, weight, hidden_r, weight_r, mask, T, Tr)
+    assert err == 0
+    o = oracle.linear_kl_fwd_parallel(f64(hidden), f64(weight), f64(hidden_r), f64(weight_r),
+                                      mask.numpy(), T, Tr)
+    act = mask.numpy() > 0
+    errs = [np.abs(g.double().numpy() - e)[act].max() for g, e in zip((kl, kr, lse, lse_r), o)]
+    print("kl n=%d h=%d hr=%d v=%d: KL in [%.3g, %.3g]; max |d| kl %.2e rev %.2e lse %.2e %.2e"
+          % (n, h, hr, v, o[0][act].min(), o[0][act].max(), *errs))
+    assert max(errs) <= LOGP_ATOL
+    for x in (kl, kr, lse, lse_r):
+        assert torch.all(x[~torch.from_numpy(act)] == 0)
+
+
+def test_identities_bitwise():
+    n, h, hr, v = 200, 256, 128, 3000
+    hidden, weight, hidden_r, weight_r, targets, mask = _heads(n, h, hr, v, 5, 0.1, 0.1)
+    # the same head on both sides: exactly zero divergence, equal log-partition functions
+    (kl, kr, lse, lse_r, _), _ = _gpu(hidden, weight, hidden, weight, mask, 0.8, 0.8)
+    assert torch.all(kl == 0) and torch.all(kr == 0) and same_bits(lse, lse_r)
+    # swapping the heads swaps the two directions bit for bit
+    (a, b, la, lb, _), _ = _gpu(hidden, weight, hidden_r, weight_r, mask, 0.8, 1.2)
+    (c, d, lc, ld, _), _ = _gpu(hidden_r, weight_r, hidden, weight, mask, 1.2, 0.8)
+    assert same_bits(a, d) and same_bits(b, c) and same_bits(la, ld) and same_bits(lb, lc)
+    # the policy's lse and selected logp are those of the logp-only forward
+    (_, _, lse2, _, logp), err = _gpu(hidden, weight, hidden_r, weight_r, mask, 0.8, 1.2, targets)
+    assert err == 0
+    d_ = dev()
+    lp0, lse0 = rlk.linear_logp_fwd(hidden.to(d_), weight.to(d_), targets.to(d_), mask.to(d_), 0.8)
+    act = mask > 0
+    assert float((lse2 - lse0.cpu())[act].abs().max()) <= 4e-6
+    assert float((logp - lp0.cpu())[act].abs().max()) <= 4e-6
+
+
+def test_batch_invariance_and_target_errors():
+    n, h, hr, v = 260, 128, 64, 2500
+    hidden, weight, hidden_r, weight_r, targets, mask = _heads(n, h, hr, v, 9, 0.1, 0.2)
+    (kl, kr, lse, lse_r, logp), _ = _gpu(hidden, weight, hidden_r, weight_r, mask, 0.7, 1.0,
+                                         targets)
+    for a, b in ((0, 1), (100, 231), (37, 260)):
+        (k2, r2, l2, lr2, p2), _ = _gpu(hidden[a:b], weight, hidden_r[a:b], weight_r, mask[a:b],
+                                        0.7, 1.0, targets[a:b])
+        for x, y in ((kl, k2), (kr, r2), (lse, l2), (lse_r, lr2), (logp, p2)):
+            assert same_bits(x[a:b], y)
+    t2 = targets.clone()
+    first_active = int(np.nonzero(mask.numpy())[0][0])
+    t2[first_active] = v + 5
+    (_, _, _, _, lp), err = _gpu(hidden, weight, hidden_r, weight_r, mask, 0.7, 1.0, t2)
+    assert err & rlk.RLK_DEVERR_TARGET_RANGE and torch.isnan(lp[first_active]).item()
+
+
+def test_argument_errors():
+    d = dev()
+    z = torch.zeros(4, 64, dtype=torch.bfloat16, device=d)
+    w = torch.zeros(10, 64, dtype=torch.bfloat16, device=d)
+    wr96 = torch.zeros(10, 96, dtype=torch.bfloat16, device=d)
+    with pytest.raises(rlk.RlkError) as e:
+        rlk.linear_kl_fwd(z, w, torch.zeros(4, 96, dtype=torch.bfloat16, device=d), wr96)
+    assert e.value.status == rlk.RLK_ERR_UNSUPPORTED
+    with pytest.raises(rlk.RlkError):
+        rlk.linear_kl_fwd(z, w, z, w, None, 1.0, -1.0)
