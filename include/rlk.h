@@ -238,6 +238,30 @@ rlk_status_t rlk_linear_kl_fwd(const void* hidden, const void* weight, const voi
                                cudaStream_t stream);
 
 /*
+ * Backward of L = sum_t grad_kl[t] kl[t] + sum_t grad_kl_rev[t] kl_rev[t] with
+ * respect to the policy head (the reference head is held fixed):
+ *
+ *   dS[t,v] = ( g_t p_v (log p_v - log q_v - kl_t) + gr_t (p_v - q_v) ) / T
+ *
+ * recomputing both heads' logits per tile (chunked like rlk_linear_logp_bwd:
+ * dS of one vocab chunk in workspace, fp32 dh accumulation across chunks, no
+ * split reductions, no atomics; dh rows batch invariant, dW reproducible bit
+ * for bit).  lse, lse_ref and kl are rlk_linear_kl_fwd's outputs; grad_kl or
+ * grad_kl_rev may be NULL (not both; kl is needed only with grad_kl).
+ * Outputs dhidden [N,H] and dweight [V,H] bf16 (overwritten); inactive rows
+ * get dhidden = 0.  workspace: rlk_linear_kl_bwd_workspace_bytes(N, H, V).
+ */
+size_t rlk_linear_kl_bwd_workspace_bytes(int64_t N, int64_t H, int64_t V);
+rlk_status_t rlk_linear_kl_bwd(const void* hidden, const void* weight, const void* hidden_ref,
+                               const void* weight_ref, const uint8_t* active_mask,
+                               const float* grad_kl, const float* grad_kl_rev, const float* lse,
+                               const float* lse_ref, const float* kl, int64_t N, int64_t H,
+                               int64_t H_ref, int64_t V, double temperature,
+                               double temperature_ref, void* dhidden, void* dweight,
+                               void* workspace, size_t workspace_bytes,
+                               uint32_t* device_error_word, cudaStream_t stream);
+
+/*
  * Masked dlogp audit.  "RL-Kernel integration roadmap for vime", Consistency
  * Contract: dlogp = recomputed - old over active tokens only; max_abs_dlogp
  * (the primary metric) with the worst-token index; approx_kl0 =

@@ -117,6 +117,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.rlk_linear_kl_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
                                       ctypes.c_double, ctypes.c_double, _vp, _vp, _vp, _vp, _vp,
                                       _vp, _sz, _vp, _vp]
+    lib.rlk_linear_kl_bwd_workspace_bytes.restype = _sz
+    lib.rlk_linear_kl_bwd_workspace_bytes.argtypes = [_i64, _i64, _i64]
+    lib.rlk_linear_kl_bwd.restype = ctypes.c_int
+    lib.rlk_linear_kl_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64,
+                                      _i64, _i64, _i64, ctypes.c_double, ctypes.c_double, _vp,
+                                      _vp, _vp, _sz, _vp, _vp]
     lib.rlk_linear_logp_entropy_bwd.restype = ctypes.c_int
     lib.rlk_linear_logp_entropy_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64,
                                                 _i64, _i64, ctypes.c_double, _vp, _vp, _vp, _sz,
@@ -350,6 +356,40 @@ def rlk_linear_kl_fwd(hidden, weight, hidden_ref, weight_ref, targets, active_ma
     _check("rlk_linear_kl_fwd", st)
 
 
+def rlk_linear_kl_bwd_workspace_bytes(N: int, H: int, V: int) -> int:
+    return int(load().rlk_linear_kl_bwd_workspace_bytes(N, H, V))
+
+
+def rlk_linear_kl_bwd(hidden, weight, hidden_ref, weight_ref, active_mask, grad_kl, grad_kl_rev,
+                      lse, lse_ref, kl, temperature, temperature_ref, dhidden, dweight,
+                      workspace, device_error_word=None, stream=None):
+    """Backward of sum g kl + sum gr kl_rev for the policy head; see include/rlk.h."""
+    n, h = hidden.shape
+    v = weight.shape[0]
+    hr = hidden_ref.shape[1]
+    _need(hidden, torch.bfloat16, "hidden")
+    _need(weight, torch.bfloat16, "weight", (v, h))
+    _need(hidden_ref, torch.bfloat16, "hidden_ref", (n, hr))
+    _need(weight_ref, torch.bfloat16, "weight_ref", (v, hr))
+    if active_mask is not None:
+        _need(active_mask, torch.uint8, "active_mask", (n,))
+    for t, name in ((grad_kl, "grad_kl"), (grad_kl_rev, "grad_kl_rev"), (kl, "kl")):
+        if t is not None:
+            _need(t, torch.float32, name, (n,))
+    _need(lse, torch.float32, "lse", (n,))
+    _need(lse_ref, torch.float32, "lse_ref", (n,))
+    _need(dhidden, torch.bfloat16, "dhidden", (n, h))
+    _need(dweight, torch.bfloat16, "dweight", (v, h))
+    _need(workspace, torch.uint8, "workspace")
+    st = load().rlk_linear_kl_bwd(_ptr(hidden), _ptr(weight), _ptr(hidden_ref), _ptr(weight_ref),
+                                  _ptr(active_mask), _ptr(grad_kl), _ptr(grad_kl_rev), _ptr(lse),
+                                  _ptr(lse_ref), _ptr(kl), n, h, hr, v, float(temperature),
+                                  float(temperature_ref), _ptr(dhidden), _ptr(dweight),
+                                  _ptr(workspace), workspace.numel(), _ptr(device_error_word),
+                                  _stream(stream))
+    _check("rlk_linear_kl_bwd", st)
+
+
 def rlk_dlogp_audit(logp_new, logp_old, active_mask, result, workspace, stream=None):
     """Enqueue the audit; ``result`` is a uint8 CUDA tensor of AUDIT_RESULT_BYTES bytes."""
     n = logp_new.shape[0]
@@ -564,6 +604,20 @@ def linear_kl_fwd(hidden, weight, hidden_ref, weight_ref, active_mask=None, temp
     return (*outs, logp)
 
 
+def linear_kl_bwd(hidden, weight, hidden_ref, weight_ref, active_mask, grad_kl, grad_kl_rev,
+                  lse, lse_ref, kl, temperature=1.0, temperature_ref=None, error_word=None):
+    """(dhidden[N,H], dweight[V,H]) bf16 of sum g kl + sum gr kl_rev (policy head only)."""
+    n, h = hidden.shape
+    v = weight.shape[0]
+    temperature_ref = temperature if temperature_ref is None else temperature_ref
+    dh = torch.empty_like(hidden)
+    dw = torch.empty_like(weight)
+    ws = _workspace(rlk_linear_kl_bwd_workspace_bytes(n, h, v), hidden.device)
+    rlk_linear_kl_bwd(hidden, weight, hidden_ref, weight_ref, active_mask, grad_kl, grad_kl_rev,
+                      lse, lse_ref, kl, temperature, temperature_ref, dh, dw, ws, error_word)
+    return dh, dw
+
+
 def audit_result_to_dict(raw: torch.Tensor) -> dict:
     r = AuditResult.from_buffer_copy(bytes(raw.cpu().numpy().tobytes()))
     return {f: getattr(r, f) for f, _ in AuditResult._fields_}
@@ -655,3 +709,37 @@ class LinearLogpEntropy(torch.autograd.Function):
 
 def linear_logp_entropy(hidden, weight, targets, active_mask=None, temperature=1.0):
     return LinearLogpEntropy.apply(hidden, weight, targets, active_mask, temperature)
+
+
+class LinearKl(torch.autograd.Function):
+    """(kl, kl_rev) = LinearKl.apply(hidden, weight, hidden_ref, weight_ref, active_mask, T, Tr);
+    gradients flow to the policy head (hidden, weight) only."""
+
+    @staticmethod
+    def forward(ctx, hidden, weight, hidden_ref, weight_ref, active_mask, temperature,
+                temperature_ref):
+        kl, kl_rev, lse, lse_ref, _ = linear_kl_fwd(hidden, weight, hidden_ref, weight_ref,
+                                                    active_mask, temperature, temperature_ref)
+        ctx.save_for_backward(hidden, weight, hidden_ref, weight_ref, active_mask, lse, lse_ref,
+                              kl)
+        ctx.temperatures = (temperature, temperature_ref)
+        return kl, kl_rev
+
+    @staticmethod
+    def backward(ctx, grad_kl, grad_kl_rev):
+        hidden, weight, hidden_ref, weight_ref, active_mask, lse, lse_ref, kl = ctx.saved_tensors
+        g = None if grad_kl is None else grad_kl.float().contiguous()
+        gr = None if grad_kl_rev is None else grad_kl_rev.float().contiguous()
+        if g is None and gr is None:
+            return None, None, None, None, None, None, None
+        dh, dw = linear_kl_bwd(hidden, weight, hidden_ref, weight_ref, active_mask, g, gr, lse,
+                               lse_ref, kl, *ctx.temperatures)
+        return dh, dw, None, None, None, None, None
+
+
+def linear_kl(hidden, weight, hidden_ref, weight_ref, active_mask=None, temperature=1.0,
+              temperature_ref=None):
+    """Differentiable (kl, kl_rev) of the policy head against a fixed reference head."""
+    temperature_ref = temperature if temperature_ref is None else temperature_ref
+    return LinearKl.apply(hidden, weight, hidden_ref.detach(), weight_ref.detach(), active_mask,
+                          temperature, temperature_ref)

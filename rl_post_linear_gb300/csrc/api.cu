@@ -115,6 +115,27 @@ size_t rlk_dlogp_audit_workspace_bytes(int64_t N) {
     return align_up(rlk::audit_v3_blocks(N) * sizeof(rlk::AuditPartial), 256) + 256;
 }
 
+// The vocabulary in ascending kBwdChunk-column chunks; per chunk the dS
+// recompute, then the dh and the dW GEMMs, one launch per role (the roles of a
+// chunk share L2 best when each has the GPU to itself).
+static rlk_status_t bwd_chunks(rlk::BwdStepMaps& maps, rlk::BwdStep& st, void* ds, int64_t N,
+                               int64_t V, int sms, uint32_t* device_error_word,
+                               cudaStream_t stream) {
+    for (int c = 0; c < st.num_chunks; ++c) {
+        const int64_t width = std::min<int64_t>(rlk::kBwdChunk, V - int64_t(c) * rlk::kBwdChunk);
+        RLK_TRY(make_map(&maps.ds_kmajor, ds, width, N, uint64_t(rlk::kBwdChunk) * 2, 64,
+                         rlk::kTileM));
+        RLK_TRY(make_map(&maps.ds_mnmajor, ds, width, N, uint64_t(rlk::kBwdChunk) * 2, 64, 64));
+        st.ds = ds;
+        st.chunk = c;
+        for (int role : {rlk::kRoleDs, rlk::kRoleDh, rlk::kRoleDw}) {
+            st.role = role;
+            RLK_CUDA(rlk::launch_bwd_step(maps, st, sms, device_error_word, stream));
+        }
+    }
+    return RLK_OK;
+}
+
 static rlk_status_t fwd_impl(const void* hidden, const void* weight, const int64_t* targets,
                              const uint8_t* active_mask, int64_t N, int64_t H, int64_t V,
                              double temperature, float* logp_out, float* lse_out,
@@ -211,6 +232,75 @@ rlk_status_t rlk_linear_kl_fwd(const void* hidden, const void* weight, const voi
     return RLK_OK;
 }
 
+size_t rlk_linear_kl_bwd_workspace_bytes(int64_t N, int64_t H, int64_t V) {
+    return rlk_linear_logp_bwd_workspace_bytes(N, H, V);
+}
+
+rlk_status_t rlk_linear_kl_bwd(const void* hidden, const void* weight, const void* hidden_ref,
+                               const void* weight_ref, const uint8_t* active_mask,
+                               const float* grad_kl, const float* grad_kl_rev, const float* lse,
+                               const float* lse_ref, const float* kl, int64_t N, int64_t H,
+                               int64_t H_ref, int64_t V, double temperature,
+                               double temperature_ref, void* dhidden, void* dweight,
+                               void* workspace, size_t workspace_bytes,
+                               uint32_t* device_error_word, cudaStream_t stream) {
+    RLK_TRY(check_shape(N, H, V, temperature));
+    RLK_TRY(check_shape(N, H_ref, V, temperature_ref));
+    if (N == 0) return RLK_OK;
+    if (hidden == nullptr || weight == nullptr || hidden_ref == nullptr ||
+        weight_ref == nullptr || lse == nullptr || lse_ref == nullptr || dhidden == nullptr ||
+        dweight == nullptr || (grad_kl == nullptr && grad_kl_rev == nullptr) ||
+        (grad_kl != nullptr && kl == nullptr))
+        return RLK_ERR_INVALID_VALUE;
+    if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(hidden_ref, 16) ||
+        !aligned(weight_ref, 16) || !aligned(dhidden, 16) || !aligned(dweight, 16))
+        return RLK_ERR_INVALID_VALUE;
+    if (workspace == nullptr || !aligned(workspace, 256) ||
+        workspace_bytes < rlk_linear_kl_bwd_workspace_bytes(N, H, V))
+        return RLK_ERR_WORKSPACE;
+    DeviceInfo dev;
+    RLK_TRY(current_device(dev));
+
+    const rlk::BwdLayout lay(N, H);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    rlk::BwdStepMaps maps;
+    RLK_TRY(make_map(&maps.h_kmajor, hidden, H, N, H * 2, 64, rlk::kTileM));
+    RLK_TRY(make_map(&maps.w_kmajor, weight, H, V, H * 2, 64, rlk::kTileV));
+    RLK_TRY(make_map(&maps.w_mnmajor, weight, H, V, H * 2, 64, 64));
+    RLK_TRY(make_map(&maps.h_mnmajor, hidden, H, N, H * 2, 64, 64));
+    RLK_TRY(make_map(&maps.hr_kmajor, hidden_ref, H_ref, N, H_ref * 2, 64, rlk::kTileM));
+    RLK_TRY(make_map(&maps.wr_kmajor, weight_ref, H_ref, V, H_ref * 2, 64, rlk::kTileV));
+    rlk::BwdStep st{};
+    st.mask = active_mask;
+    st.grad = grad_kl;
+    st.lse = lse;
+    st.hidden = hidden;
+    st.weight = weight;
+    st.N = static_cast<int>(N);
+    st.H = static_cast<int>(H);
+    st.V = static_cast<int>(V);
+    st.num_chunks = static_cast<int>((V + rlk::kBwdChunk - 1) / rlk::kBwdChunk);
+    st.k = static_cast<float>(1.4426950408889634074 / temperature);
+    st.temp = static_cast<float>(temperature);
+    st.kl = true;
+    st.H_ref = static_cast<int>(H_ref);
+    st.k_ref = static_cast<float>(1.4426950408889634074 / temperature_ref);
+    st.grad_rev = grad_kl_rev;
+    st.lse_ref = lse_ref;
+    st.kl_val = kl;
+    st.dh_acc = reinterpret_cast<float*>(ws + lay.dhacc_off);
+    st.dom = reinterpret_cast<int*>(ws + lay.dom_off);
+    st.dcoef = reinterpret_cast<float*>(ws + lay.dcoef_off);
+    st.sorted_dy = reinterpret_cast<int*>(ws + lay.sorted_dy_off);
+    st.sorted_dt = reinterpret_cast<int*>(ws + lay.sorted_dt_off);
+    st.tiles = reinterpret_cast<uint64_t*>(ws + lay.tiles_off);
+    st.dhidden = dhidden;
+    st.dweight = dweight;
+    // no dominant class yet (all bits set: -1)
+    RLK_CUDA(cudaMemsetAsync(st.dom, 0xff, static_cast<size_t>(N) * sizeof(int), stream));
+    return bwd_chunks(maps, st, ws + lay.ds_off, N, V, dev.sms, device_error_word, stream);
+}
+
 rlk_status_t rlk_linear_logp_entropy_fwd(const void* hidden, const void* weight,
                                          const int64_t* targets, const uint8_t* active_mask,
                                          int64_t N, int64_t H, int64_t V, double temperature,
@@ -260,7 +350,7 @@ static rlk_status_t bwd_impl(const void* hidden, const void* weight, const int64
     RLK_CUDA(rlk::launch_target_sort(targets, active_mask, n, v, tiles, sorted_y, sorted_t, dom,
                                      device_error_word, stream));
     const int num_chunks = static_cast<int>((V + rlk::kBwdChunk - 1) / rlk::kBwdChunk);
-    rlk::BwdStep st;
+    rlk::BwdStep st{};
     st.targets = targets;
     st.mask = active_mask;
     st.grad = grad_logp;
@@ -280,26 +370,13 @@ static rlk_status_t bwd_impl(const void* hidden, const void* weight, const int64
     st.sorted_t = sorted_t;
     st.ycoef = reinterpret_cast<float*>(ws + lay.ycoef_off);
     st.dom = dom;
+    st.dcoef = reinterpret_cast<float*>(ws + lay.dcoef_off);
     st.sorted_dy = reinterpret_cast<int*>(ws + lay.sorted_dy_off);
     st.sorted_dt = reinterpret_cast<int*>(ws + lay.sorted_dt_off);
     st.tiles = tiles;
     st.dhidden = dhidden;
     st.dweight = dweight;
-    void* ds = ws + lay.ds_off;
-    for (int c = 0; c < num_chunks; ++c) {
-        // one launch per role: the three roles of a chunk share L2 best when each has the GPU
-        const int64_t width = std::min<int64_t>(rlk::kBwdChunk, V - int64_t(c) * rlk::kBwdChunk);
-        RLK_TRY(make_map(&maps.ds_kmajor, ds, width, N, uint64_t(rlk::kBwdChunk) * 2, 64,
-                         rlk::kTileM));
-        RLK_TRY(make_map(&maps.ds_mnmajor, ds, width, N, uint64_t(rlk::kBwdChunk) * 2, 64, 64));
-        st.ds = ds;
-        st.chunk = c;
-        for (int role : {rlk::kRoleDs, rlk::kRoleDh, rlk::kRoleDw}) {
-            st.role = role;
-            RLK_CUDA(rlk::launch_bwd_step(maps, st, dev.sms, device_error_word, stream));
-        }
-    }
-    return RLK_OK;
+    return bwd_chunks(maps, st, ws + lay.ds_off, N, V, dev.sms, device_error_word, stream);
 }
 
 rlk_status_t rlk_linear_logp_bwd(const void* hidden, const void* weight, const int64_t* targets,

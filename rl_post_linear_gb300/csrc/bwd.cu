@@ -90,6 +90,7 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
     __nv_bfloat16* ds;    // [N][kBwdChunk]
     float* ycoef;         // [N]: 1 - p_y of each live row, written by the tile holding y
     int* dom;             // [N]: the row's dominant non-target class (p > 1/2), else -1
+    float* dcoef;         // [N]: that class's fp32 gradient coefficient, -g/T
     int N, V, c0, num_m, num_n, kblocks;
     float k, temp;
 
@@ -187,6 +188,7 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
                     if (idx != yi) {
                         ai = idx;
                         dom[t] = vb + idx;
+                        dcoef[t] = -st.gt;
                         da = st.gt * -expm1f(l2 * kLn2);
                         if constexpr (ENT) da = fmaf(fmaf(st.c2, cm, st.coef_y), ex2_approx(l2), da);
                     }
@@ -221,6 +223,149 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
     __device__ void epi_end(int, int, EpiState&) const {}
 };
 
+// ----------------------------------------------------------------------------- dS_c for KL
+//
+// Backward of L = sum_t g_t KL(p_t || q_t) + gr_t KL(q_t || p_t) with respect to
+// the policy head only.  With l_v = log p_v - log q_v:
+//   dKL(p||q)/dz_v = p_v (l_v - KL),   dKL(q||p)/dz_v = p_v - q_v,
+//   dS[t,v] = ( g_t p_v (l_v - KL_t) + gr_t (p_v - q_v) ) / T          (bf16)
+// Both logit tiles are recomputed (the mainloop's paired-tile mode: policy
+// into one TMEM accumulator, reference into the other).  The entry of a
+// dominant policy class (p > 2^-0.99, at most one per row) usually carries
+// most of the row's gradient; it skips bf16 dS and reaches dh / dW through
+// the same fp32 path as the logp backward's dominant classes (dom, dcoef and
+// the per-chunk sorted list).  The dh and dW roles run without target terms.
+
+struct DsKlMaps {
+    CUtensorMap h, w, hr, wr;     // K-major; boxes {64,128} for h / hr, {64,256} for w / wr
+};
+
+struct DsKlPolicy {
+    using Maps = DsKlMaps;
+    static constexpr bool kPairTiles = true;
+
+    const uint8_t* mask;
+    const float* grad;        // d L / d KL(p||q), or nullptr
+    const float* grad_rev;    // d L / d KL(q||p), or nullptr
+    const float* lse;
+    const float* lse_ref;
+    const float* kl;
+    __nv_bfloat16* ds;        // [N][kBwdChunk]
+    int* dom;                 // [N] dominant policy class or -1
+    float* dcoef;             // [N] its fp32 gradient entry
+    int N, V, c0, num_m, num_n, kblocks, kblocks_r;
+    float k, kr, temp;
+
+    __device__ static void prefetch(const Maps& m) {
+        prefetch_tensormap(&m.h);
+        prefetch_tensormap(&m.w);
+        prefetch_tensormap(&m.hr);
+        prefetch_tensormap(&m.wr);
+    }
+    __device__ static const CUtensorMap* a_map(const Maps& m, int) { return &m.h; }
+    __device__ static const CUtensorMap* b_map(const Maps& m, int) { return &m.w; }
+    __device__ static const CUtensorMap* tile_a_map(const Maps& m, int, int q) {
+        return (q & 1) ? &m.hr : &m.h;
+    }
+    __device__ static const CUtensorMap* tile_b_map(const Maps& m, int, int q) {
+        return (q & 1) ? &m.wr : &m.w;
+    }
+    __device__ static bool a_mn(int) { return false; }
+    __device__ static bool b_mn(int) { return false; }
+    __device__ int k_blocks(int) const { return kblocks; }
+    __device__ int tile_k_blocks(int, int q) const { return (q & 1) ? kblocks_r : kblocks; }
+
+    __device__ int num_units() const { return num_m * num_n; }
+    __device__ int tiles_in_unit(int) const { return 2; }
+    __device__ void unit(int u, int& m, int& n) const {
+        grouped_unit(u, num_m, num_n, kRasterTokenTiles, m, n);
+    }
+    __device__ void coords(int u, int, int& a_mn, int& a_k, int& b_mn, int& b_k) const {
+        int m, n;
+        unit(u, m, n);
+        a_mn = m * kTileM;
+        a_k = 0;
+        b_mn = c0 + n * kTileV;
+        b_k = 0;
+    }
+
+    struct EpiState {
+        float lse2, lse2r, kl, gp, gq;
+        bool live;
+    };
+
+    __device__ void epi_begin(int u, int row, EpiState& st) const {
+        int m, n;
+        unit(u, m, n);
+        const int t = m * kTileM + row;
+        st.live = t < N && (mask == nullptr || mask[t] != 0);
+        st.lse2 = st.live ? lse[t] * kLog2e : 0.f;
+        st.lse2r = st.live ? lse_ref[t] * kLog2e : 0.f;
+        st.kl = (st.live && grad != nullptr) ? kl[t] : 0.f;
+        st.gp = (st.live && grad != nullptr) ? __fdiv_rn(grad[t], temp) : 0.f;
+        st.gq = (st.live && grad_rev != nullptr) ? __fdiv_rn(grad_rev[t], temp) : 0.f;
+    }
+
+    __device__ void epi_pair(int u, int, int row, uint32_t tp, uint32_t tr, EpiState& st) const {
+        int m, n;
+        unit(u, m, n);
+        const int t = m * kTileM + row;
+#pragma unroll 1
+        for (int cc = 0; cc < kTileV / 32; ++cc) {
+            uint32_t rp[32], rr[32];
+            tmem_load_32(tp + cc * 32, rp);
+            tmem_load_32(tr + cc * 32, rr);
+            if (t >= N) continue;
+            const int col = n * kTileV + cc * 32;   // column inside the chunk
+            const int vb = c0 + col;
+            // the slice's top policy entry, if it dominates the row
+            int ai = 32;
+            if (st.live) {
+                float cm = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    cm = (vb + j < V) ? fmaxf(cm, __uint_as_float(rp[j])) : cm;
+                if (fmaf(cm, k, -st.lse2) > -0.99f) {
+                    int idx = 31;
+#pragma unroll
+                    for (int j = 31; j >= 0; --j)
+                        idx = (__uint_as_float(rp[j]) == cm && vb + j < V) ? j : idx;
+                    ai = idx;
+                }
+            }
+            uint32_t packed[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                float d[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float s = __uint_as_float(rp[2 * j + e]);
+                    const float r = __uint_as_float(rr[2 * j + e]);
+                    const float l2p = fmaf(s, k, -st.lse2);     // log2 p
+                    const float l2q = fmaf(r, kr, -st.lse2r);   // log2 q
+                    const float p = ex2_approx(l2p), q = ex2_approx(l2q);
+                    const float ell = (l2p - l2q) * kLn2;
+                    const float g = fmaf(st.gp * p, ell - st.kl, st.gq * (p - q));
+                    d[e] = (st.live && vb + 2 * j + e < V) ? g : 0.f;
+                    if (ai == 2 * j + e) {              // fp32 path for the dominant entry
+                        dom[t] = vb + ai;
+                        dcoef[t] = g;
+                        d[e] = 0.f;
+                    }
+                }
+                packed[j] = pack_bf16x2(d[0], d[1]);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(ds + static_cast<size_t>(t) * kBwdChunk + col);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                    packed[4 * i + 3]);
+        }
+    }
+
+    __device__ void epi_end(int, int, EpiState&) const {}
+};
+
 // ----------------------------------------------------------------------------- dh
 
 // dS_c [N, width]: K (vocab) contiguous; W_c [width, H]: N (hidden) contiguous
@@ -234,8 +379,10 @@ struct DhPolicy : SingleRole<false, true> {
     __nv_bfloat16* dh;             // [N][H]
     const float* ycoef;            // [N] 1 - p_y, from the dS GEMM
     const int* dom;                // [N] dominant non-target class or -1, from the dS GEMM
+    const float* dcoef;            // [N] its fp32 coefficient
     int N, V, H, c0, num_m, num_n, kblocks;
     bool first, last;
+    bool terms;                    // false: no fp32 target terms (no targets)
     float temp;
 
     __device__ int num_units() const { return num_m * num_n; }
@@ -267,13 +414,19 @@ struct DhPolicy : SingleRole<false, true> {
         int m, n;
         unit(u, m, n);
         const int t = m * kTileM + row;
-        st.live = row_live(targets, mask, t, N, V, st.y);
         // the fp32 terms, added once, in the last chunk's epilogue: (g / T)(1 - p_y) W[y]
-        // and, for a dominant non-target class a, -(g / T) W[a]
-        const float gt = (st.live && last) ? __fdiv_rn(grad[t], temp) : 0.f;
-        st.coef = (st.live && last) ? gt * ycoef[t] : 0.f;
+        // and, for a dominant non-target class a, dcoef W[a]
+        if (terms) {
+            st.live = row_live(targets, mask, t, N, V, st.y);
+            const float gt = (st.live && last) ? __fdiv_rn(grad[t], temp) : 0.f;
+            st.coef = (st.live && last) ? gt * ycoef[t] : 0.f;
+        } else {
+            st.live = t < N && (mask == nullptr || mask[t] != 0);
+            st.y = 0;
+            st.coef = 0.f;
+        }
         st.dom = (st.live && last) ? dom[t] : -1;
-        st.coef_dom = -gt;
+        st.coef_dom = st.dom >= 0 ? dcoef[t] : 0.f;
     }
 
     __device__ void epi_tile(int u, int, int row, uint32_t taddr, EpiState& st) const {
@@ -308,14 +461,17 @@ struct DhPolicy : SingleRole<false, true> {
                 continue;
             }
             if (st.live) {
-                const uint4* wr = reinterpret_cast<const uint4*>(
-                    weight + static_cast<size_t>(st.y) * H + col);
+                if (terms) {
+                    const uint4* wr = reinterpret_cast<const uint4*>(
+                        weight + static_cast<size_t>(st.y) * H + col);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    float wv[8];
-                    bf16x8_to_f32(wr[i], wv);
+                    for (int i = 0; i < 4; ++i) {
+                        float wv[8];
+                        bf16x8_to_f32(wr[i], wv);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) x[8 * i + j] = fmaf(st.coef, wv[j], x[8 * i + j]);
+                        for (int j = 0; j < 8; ++j)
+                            x[8 * i + j] = fmaf(st.coef, wv[j], x[8 * i + j]);
+                    }
                 }
                 if (st.dom >= 0) {
                     const uint4* wa = reinterpret_cast<const uint4*>(
@@ -359,8 +515,10 @@ struct DwPolicy : SingleRole<true, true> {
     const float* ycoef;            // [N] 1 - p_y, from the dS GEMM
     const int* sorted_dy;          // [N] dominant class of this chunk ascending, V elsewhere
     const int* sorted_dt;          // [N]
+    const float* dcoef;            // [N] fp32 coefficient of each token's dominant class
     int N, H, c0, width, num_m, num_n, kblocks;
     float temp;
+    bool terms;                    // false: no fp32 target terms (no targets)
 
     __device__ int num_units() const { return num_m * num_n; }
     __device__ int k_blocks(int) const { return kblocks; }
@@ -404,7 +562,7 @@ struct DwPolicy : SingleRole<true, true> {
         st.v = c0 + vl;
         st.lo = st.hi = st.dlo = st.dhi = 0;
         if (!st.valid) return;
-        equal_range(sorted_y, N, st.v, st.lo, st.hi);
+        if (terms) equal_range(sorted_y, N, st.v, st.lo, st.hi);
         equal_range(sorted_dy, N, st.v, st.dlo, st.dhi);
     }
 
@@ -433,10 +591,10 @@ struct DwPolicy : SingleRole<true, true> {
                     for (int j = 0; j < 8; ++j) x[8 * q + j] = fmaf(coef, hv[j], x[8 * q + j]);
                 }
             }
-            // tokens whose dominant non-target class is v: -(g_t / T) h_t, ascending t
+            // tokens whose dominant non-target class is v: dcoef_t h_t, ascending t
             for (int i = st.dlo; i < st.dhi; ++i) {
                 const int t = sorted_dt[i];
-                const float coef = -__fdiv_rn(grad[t], temp);
+                const float coef = dcoef[t];
                 const uint4* hr = reinterpret_cast<const uint4*>(
                     hidden + static_cast<size_t>(t) * H + col);
 #pragma unroll
@@ -616,6 +774,7 @@ static cudaError_t launch_ds(const BwdStepMaps& maps, const BwdStep& st, int c0,
     ps.ds = static_cast<__nv_bfloat16*>(st.ds);
     ps.ycoef = st.ycoef;
     ps.dom = st.dom;
+    ps.dcoef = st.dcoef;
     ps.N = st.N;
     ps.V = st.V;
     ps.c0 = c0;
@@ -632,6 +791,40 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
     const int N = st.N, H = st.H, V = st.V;
     const int c0 = st.chunk * kBwdChunk;
     const int width = (V - c0) < kBwdChunk ? (V - c0) : kBwdChunk;
+    if (st.role == kRoleDs && st.kl) {
+        DsKlPolicy ps;
+        ps.mask = st.mask;
+        ps.grad = st.grad;
+        ps.grad_rev = st.grad_rev;
+        ps.lse = st.lse;
+        ps.lse_ref = st.lse_ref;
+        ps.kl = st.kl_val;
+        ps.ds = static_cast<__nv_bfloat16*>(st.ds);
+        ps.dom = st.dom;
+        ps.dcoef = st.dcoef;
+        ps.N = N;
+        ps.V = V;
+        ps.c0 = c0;
+        ps.num_m = (N + kTileM - 1) / kTileM;
+        ps.num_n = (width + kTileV - 1) / kTileV;
+        ps.kblocks = H / 64;
+        ps.kblocks_r = st.H_ref / 64;
+        ps.k = st.k;
+        ps.kr = st.k_ref;
+        ps.temp = st.temp;
+        auto kern = gemm_persistent_kernel<DsKlPolicy>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kGemmSmemBytes));
+        if (e != cudaSuccess) return e;
+        const int units = ps.num_m * ps.num_n;
+        const int grid = units < num_sms ? units : num_sms;
+        kern<<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(
+            DsKlMaps{maps.h_kmajor, maps.w_kmajor, maps.hr_kmajor, maps.wr_kmajor}, ps, err);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        return launch_dom_sort(st.dom, N, V, c0, c0 + width, st.tiles, st.sorted_dy,
+                               st.sorted_dt, stream);
+    }
     if (st.role == kRoleDs) {
         const cudaError_t e =
             st.grad_ent != nullptr ? launch_ds<true>(maps, st, c0, width, num_sms, err, stream)
@@ -651,6 +844,7 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
         pd.dh = static_cast<__nv_bfloat16*>(st.dhidden);
         pd.ycoef = st.ycoef;
         pd.dom = st.dom;
+        pd.dcoef = st.dcoef;
         pd.N = N;
         pd.V = V;
         pd.H = H;
@@ -661,6 +855,7 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
         pd.first = st.chunk == 0;
         pd.last = st.chunk == st.num_chunks - 1;
         pd.temp = st.temp;
+        pd.terms = !st.kl;
         return launch_gemm(maps.ds_kmajor, maps.w_mnmajor, pd, pd.num_m * pd.num_n, num_sms, err,
                            stream);
     }
@@ -673,6 +868,7 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
     pw.ycoef = st.ycoef;
     pw.sorted_dy = st.sorted_dy;
     pw.sorted_dt = st.sorted_dt;
+    pw.dcoef = st.dcoef;
     pw.N = N;
     pw.H = H;
     pw.c0 = c0;
@@ -681,6 +877,7 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
     pw.num_n = (H + kTileV - 1) / kTileV;
     pw.kblocks = (N + 63) / 64;
     pw.temp = st.temp;
+    pw.terms = !st.kl;
     return launch_gemm(maps.ds_mnmajor, maps.h_mnmajor, pw, pw.num_m * pw.num_n, num_sms, err,
                        stream);
 }

@@ -61,8 +61,8 @@ struct FwdLayout {
 // sorted by class, and the sorted key tiles the lists are built from.
 constexpr int kTargetSortTile = 2048;
 struct BwdLayout {
-    size_t ds_off, dhacc_off, sorted_y_off, sorted_t_off, ycoef_off, dom_off, sorted_dy_off,
-        sorted_dt_off, tiles_off, total;
+    size_t ds_off, dhacc_off, sorted_y_off, sorted_t_off, ycoef_off, dom_off, dcoef_off,
+        sorted_dy_off, sorted_dt_off, tiles_off, total;
     BwdLayout(int64_t N, int64_t H) {
         ds_off = 0;
         dhacc_off = align_up(static_cast<size_t>(N) * kBwdChunk * 2, 256);
@@ -70,7 +70,8 @@ struct BwdLayout {
         sorted_t_off = align_up(sorted_y_off + static_cast<size_t>(N) * 4, 256);
         ycoef_off = align_up(sorted_t_off + static_cast<size_t>(N) * 4, 256);
         dom_off = align_up(ycoef_off + static_cast<size_t>(N) * 4, 256);
-        sorted_dy_off = align_up(dom_off + static_cast<size_t>(N) * 4, 256);
+        dcoef_off = align_up(dom_off + static_cast<size_t>(N) * 4, 256);
+        sorted_dy_off = align_up(dcoef_off + static_cast<size_t>(N) * 4, 256);
         sorted_dt_off = align_up(sorted_dy_off + static_cast<size_t>(N) * 4, 256);
         tiles_off = align_up(sorted_dt_off + static_cast<size_t>(N) * 4, 256);
         const size_t tiles = static_cast<size_t>((N + kTargetSortTile - 1) / kTargetSortTile);
@@ -165,6 +166,8 @@ struct BwdStepMaps {
     CUtensorMap h_mnmajor;     // hidden [N,H], box {64, 64}:  B of the dW GEMM
     CUtensorMap ds_kmajor;     // consumed dS [N, width], box {64, 128}: A of the dh GEMM
     CUtensorMap ds_mnmajor;    // consumed dS [N, width], box {64, 64}:  A of the dW GEMM
+    CUtensorMap hr_kmajor;     // KL only: reference hidden [N,Hr], box {64, 128}
+    CUtensorMap wr_kmajor;     // KL only: reference weight [V,Hr], box {64, 256}
 };
 
 // One launch of the backward: a role (the dS recompute, the dh GEMM or the dW
@@ -182,12 +185,20 @@ struct BwdStep {
     int N, H, V, num_chunks;
     int chunk, role;
     float k, temp;
+    // KL against a reference head (kl = true): dS from both heads, no fp32 target terms
+    bool kl;
+    int H_ref;
+    float k_ref;
+    const float* grad_rev;     // d loss / d KL(q || p), or nullptr
+    const float* lse_ref;
+    const float* kl_val;       // the forward's KL(p || q)
     void* ds;                  // dS [N, kBwdChunk] bf16 of the chunk
     float* dh_acc;
     const int* sorted_y;
     const int* sorted_t;
     float* ycoef;              // [N] 1 - p_y of each live row
     int* dom;                  // [N] dominant non-target class (p > 1/2) or -1
+    float* dcoef;              // [N] its fp32 gradient coefficient
     int* sorted_dy;            // [N] this chunk's dominant classes, ascending (V: none)
     int* sorted_dt;            // [N]
     uint64_t* tiles;           // sort scratch
