@@ -438,6 +438,34 @@ def measure_next_rows(rlk, dev, pk, warmup, steps, state):
     res["entropy_bwd"] = {"ms": ms_b, "tflops": bwd_flops / (ms_b * 1e-3) / 1e12,
                           "frac_of_peak": bwd_flops / (ms_b * 1e-3) / 1e12 / peak}
 
+    # NEXT-3: full-vocabulary KL against a reference head of the same shape (a frozen
+    # reference policy); forward 2 N V (H + Hr) FLOP, backward 4 N H V algorithmic (dh, dW;
+    # the recompute of both heads, 2 N V (H + Hr), is executed on top)
+    hid_r = (hid.float() + torch.randn(hid.shape, device=dev, generator=gen)
+             * 0.1).to(torch.bfloat16)
+    wt_r = (wt.float() + torch.randn(wt.shape, device=dev, generator=gen)
+            * 0.005).to(torch.bfloat16)
+    kl, kl_r, lse_p, lse_q = (torch.empty_like(logp_ref) for _ in range(4))
+    ws_kl = torch.empty(rlk.rlk_linear_kl_fwd_workspace_bytes(n, v), dtype=torch.uint8,
+                        device=dev)
+    ms_f = _time_calls(lambda: rlk.rlk_linear_kl_fwd(hid, wt, hid_r, wt_r, None, mask, T, T, kl,
+                                                     kl_r, lse_p, lse_q, None, ws_kl),
+                       warmup, steps, stream)
+    g_kl = torch.randn(n, device=dev, generator=gen) / n
+    ms_b = _time_calls(lambda: rlk.rlk_linear_kl_bwd(hid, wt, hid_r, wt_r, mask, g_kl, g_kl,
+                                                     lse_p, lse_q, kl, T, T, dh, dw, ws_b),
+                       warmup, steps, stream)
+    kl_fwd_flops = 2.0 * n_act * v * (h + h)
+    res["kl_fwd"] = {"ms": ms_f, "tflops": kl_fwd_flops / (ms_f * 1e-3) / 1e12,
+                     "frac_of_peak": kl_fwd_flops / (ms_f * 1e-3) / 1e12 / peak,
+                     "reference_head": "same shape as the policy head",
+                     "mean_kl": float(kl.float().mean())}
+    res["kl_bwd"] = {"ms": ms_b, "tflops": bwd_flops / (ms_b * 1e-3) / 1e12,
+                     "frac_of_peak": bwd_flops / (ms_b * 1e-3) / 1e12 / peak,
+                     "executed_tflops": (bwd_flops + kl_fwd_flops) / (ms_b * 1e-3) / 1e12}
+    del hid_r, wt_r, ws_kl
+    torch.cuda.empty_cache()
+
     # NEXT-4: logp from existing logits, dense rows; bytes = the logits + targets, mask, out
     for name, dt, es in (("logits_fp32", torch.float32, 4), ("logits_bf16", torch.bfloat16, 2)):
         logits = (torch.randn(n, v, device=dev, generator=gen) * 2.0).to(dt)
