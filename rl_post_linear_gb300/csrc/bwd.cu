@@ -243,6 +243,7 @@ struct DsKlMaps {
 struct DsKlPolicy {
     using Maps = DsKlMaps;
     static constexpr bool kPairTiles = true;
+    static constexpr int kEpiWarps = 8;       // two column halves per row
 
     const uint8_t* mask;
     const float* grad;        // d L / d KL(p||q), or nullptr
@@ -294,7 +295,7 @@ struct DsKlPolicy {
         bool live;
     };
 
-    __device__ void epi_begin(int u, int row, EpiState& st) const {
+    __device__ void epi_begin(int u, int row, int, EpiState& st) const {
         int m, n;
         unit(u, m, n);
         const int t = m * kTileM + row;
@@ -306,12 +307,13 @@ struct DsKlPolicy {
         st.gq = (st.live && grad_rev != nullptr) ? __fdiv_rn(grad_rev[t], temp) : 0.f;
     }
 
-    __device__ void epi_pair(int u, int, int row, uint32_t tp, uint32_t tr, EpiState& st) const {
+    __device__ void epi_pair(int u, int, int row, int half, uint32_t tp, uint32_t tr,
+                             EpiState& st) const {
         int m, n;
         unit(u, m, n);
         const int t = m * kTileM + row;
 #pragma unroll 1
-        for (int cc = 0; cc < kTileV / 32; ++cc) {
+        for (int cc = half * (kTileV / 64); cc < (half + 1) * (kTileV / 64); ++cc) {
             uint32_t rp[32], rr[32];
             tmem_load_32(tp + cc * 32, rp);
             tmem_load_32(tr + cc * 32, rr);
@@ -363,7 +365,7 @@ struct DsKlPolicy {
         }
     }
 
-    __device__ void epi_end(int, int, EpiState&) const {}
+    __device__ void epi_end(int, int, int, EpiState&) const {}
 };
 
 // ----------------------------------------------------------------------------- dh
@@ -818,7 +820,7 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
         if (e != cudaSuccess) return e;
         const int units = ps.num_m * ps.num_n;
         const int grid = units < num_sms ? units : num_sms;
-        kern<<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(
+        kern<<<grid, gemm_threads<DsKlPolicy>(), kGemmSmemBytes, stream>>>(
             DsKlMaps{maps.h_kmajor, maps.w_kmajor, maps.hr_kmajor, maps.wr_kmajor}, ps, err);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;

@@ -96,7 +96,10 @@ __device__ __forceinline__ uint64_t operand_desc_rt(bool mn_major, uint32_t stag
 // different operands (tile_a_map / tile_b_map / tile_k_blocks(u, q)); the
 // epilogue sees both accumulators at once (epi_pair, after the odd tile) and
 // releases the two TMEM buffers together.  Units then hold an even number of
-// tiles, so a pair always occupies buffers 0 and 1.
+// tiles, so a pair always occupies buffers 0 and 1.  Pair policies may set
+// kEpiWarps = 8: two warps per TMEM lane quarter, each given half of the
+// tile's columns (epi_begin / epi_pair / epi_end take the half), so that the
+// epilogue, which the MMA waits for, takes half as long.
 // TwoMaps serves the single-role policies.
 struct TwoMaps {
     CUtensorMap a, b;
@@ -107,6 +110,7 @@ template <bool AMN, bool BMN>
 struct SingleRole {
     using Maps = TwoMaps;
     static constexpr bool kPairTiles = false;
+    static constexpr int kEpiWarps = 4;
     static constexpr bool kAMn = AMN;
     static constexpr bool kBMn = BMN;
     __device__ static void prefetch(const Maps& m) {
@@ -161,8 +165,14 @@ __device__ __forceinline__ void report_error(uint32_t* err, uint32_t bits) {
     if (err != nullptr) atomicOr(err, bits);
 }
 
+// threads of a launch: the TMA warp, the MMA warp and the epilogue warps
 template <class P>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+constexpr int gemm_threads() {
+    return 64 + 32 * P::kEpiWarps;
+}
+
+template <class P>
+__global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1)
     gemm_persistent_kernel(const __grid_constant__ typename P::Maps maps, const P p,
                            uint32_t* err) {
     extern __shared__ uint8_t smem_raw[];
@@ -191,7 +201,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tmem_full[b], 1);
-            mbar_init(&tmem_empty[b], 4);     // one arrival per epilogue warp
+            mbar_init(&tmem_empty[b], P::kEpiWarps);   // one arrival per epilogue warp
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -316,13 +326,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
     } else {
         const int quarter = warp & 3;         // TMEM lanes this warp may access
+        const int half = (warp - 2) >> 2;     // column half (0 unless kEpiWarps = 8)
         const int row = quarter * 32 + lane;
         const uint32_t taddr_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
         uint32_t tile_i = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
             typename P::EpiState st;
-            p.epi_begin(u, row, st);
+            if constexpr (P::kPairTiles)
+                p.epi_begin(u, row, half, st);
+            else
+                p.epi_begin(u, row, st);
             const int nt = p.tiles_in_unit(u);
             for (int q = 0; q < nt; ++q, ++tile_i) {
                 const uint32_t buf = tile_i & 1u;
@@ -337,7 +351,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if constexpr (P::kPairTiles) {
                     if ((q & 1) == 0) continue;       // hold the even tile's buffer
                     tc_fence_after();
-                    p.epi_pair(u, q, row, taddr_row + (buf ^ 1u) * kBN, taddr_row + buf * kBN, st);
+                    p.epi_pair(u, q, row, half, taddr_row + (buf ^ 1u) * kBN,
+                               taddr_row + buf * kBN, st);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) {
@@ -353,7 +368,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
             }
             if (!ok) break;
-            p.epi_end(u, row, st);
+            if constexpr (P::kPairTiles)
+                p.epi_end(u, row, half, st);
+            else
+                p.epi_end(u, row, st);
         }
         if (!ok && lane == 0) {
             report_error(err, RLK_DEVERR_WAIT_TIMEOUT);

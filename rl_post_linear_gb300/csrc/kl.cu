@@ -44,12 +44,14 @@ struct KlMaps {
 struct KlFwdPolicy {
     using Maps = KlMaps;
     static constexpr bool kPairTiles = true;
+    static constexpr int kEpiWarps = 8;       // two column halves per row
 
     const int64_t* targets;   // nullptr: no selected logp
-    float2* part_p;           // [num_chunks][N] (m, s) of the policy
-    float* part_a;            // [num_chunks][N] sum 2^((S - m) k) d
-    float2* part_r;           // [num_chunks][N] (mr, sr) of the reference
-    float* part_b;            // [num_chunks][N] sum 2^((R - mr) kr) (-d)
+    // partials per (chunk, column half, row): [num_chunks][2][N]
+    float2* part_p;           // (m, s) of the policy
+    float* part_a;            // sum 2^((S - m) k) d
+    float2* part_r;           // (mr, sr) of the reference
+    float* part_b;            // sum 2^((R - mr) kr) (-d)
     float* s_target;          // [N]
     int N, V, num_m, num_vt, num_chunks, kblocks, kblocks_r;
     float k, kr;
@@ -97,7 +99,7 @@ struct KlFwdPolicy {
         bool found;
     };
 
-    __device__ void epi_begin(int u, int row, EpiState& st) const {
+    __device__ void epi_begin(int u, int row, int, EpiState& st) const {
         int m, c;
         unit(u, m, c);
         const int t = m * kTileM + row;
@@ -107,12 +109,13 @@ struct KlFwdPolicy {
         st.y = (targets != nullptr && t < N) ? targets[t] : -1;
     }
 
-    __device__ void epi_pair(int u, int q, int, uint32_t tp, uint32_t tr, EpiState& st) const {
+    __device__ void epi_pair(int u, int q, int, int half, uint32_t tp, uint32_t tr,
+                             EpiState& st) const {
         int m, c;
         unit(u, m, c);
         const int v0 = (c * kFwdTilesPerChunk + (q >> 1)) * kTileV;
 #pragma unroll 1
-        for (int cc = 0; cc < kTileV / 32; ++cc) {
+        for (int cc = half * (kTileV / 64); cc < (half + 1) * (kTileV / 64); ++cc) {
             const int vb = v0 + cc * 32;
             if (vb >= V) break;                       // same for the whole warp
             uint32_t rp[32], rr[32];
@@ -163,12 +166,12 @@ struct KlFwdPolicy {
         }
     }
 
-    __device__ void epi_end(int u, int row, EpiState& st) const {
+    __device__ void epi_end(int u, int row, int half, EpiState& st) const {
         int m, c;
         unit(u, m, c);
         const int t = m * kTileM + row;
         if (t >= N) return;
-        const size_t o = static_cast<size_t>(c) * N + t;
+        const size_t o = (static_cast<size_t>(c) * 2 + half) * N + t;
         part_p[o] = make_float2(st.m, st.s);
         part_a[o] = st.a;
         part_r[o] = make_float2(st.mr, st.sr);
@@ -181,7 +184,7 @@ __global__ void kl_merge_kernel(const float2* __restrict__ part_p, const float* 
                                 const float2* __restrict__ part_r, const float* __restrict__ part_b,
                                 const float* __restrict__ s_target,
                                 const int64_t* __restrict__ targets,
-                                const uint8_t* __restrict__ mask, int N, int V, int num_chunks,
+                                const uint8_t* __restrict__ mask, int N, int V, int num_parts,
                                 float k, float kr, float* __restrict__ kl,
                                 float* __restrict__ kl_rev, float* __restrict__ lse,
                                 float* __restrict__ lse_ref, float* __restrict__ logp,
@@ -196,13 +199,14 @@ __global__ void kl_merge_kernel(const float2* __restrict__ part_p, const float* 
         if (logp != nullptr) logp[t] = 0.f;
         return;
     }
+    // parts in ascending (chunk, column half) order
     float m = -INFINITY, mr = -INFINITY;
-    for (int c = 0; c < num_chunks; ++c) {
+    for (int c = 0; c < num_parts; ++c) {
         m = fmaxf(m, part_p[static_cast<size_t>(c) * N + t].x);
         mr = fmaxf(mr, part_r[static_cast<size_t>(c) * N + t].x);
     }
     float s = 0.f, a = 0.f, sr = 0.f, b = 0.f;
-    for (int c = 0; c < num_chunks; ++c) {
+    for (int c = 0; c < num_parts; ++c) {
         const size_t o = static_cast<size_t>(c) * N + t;
         const float2 pp = part_p[o], pr = part_r[o];
         const float w = ex2_approx((pp.x - m) * k), wr = ex2_approx((pr.x - mr) * kr);
@@ -261,13 +265,13 @@ cudaError_t launch_kl_fwd(const CUtensorMap& map_h, const CUtensorMap& map_w,
     if (e != cudaSuccess) return e;
     const long long units = static_cast<long long>(p.num_m) * p.num_chunks;
     const int grid = static_cast<int>(units < num_sms ? units : num_sms);
-    kern<<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(KlMaps{map_h, map_w, map_hr, map_wr}, p,
-                                                         err);
+    kern<<<grid, gemm_threads<KlFwdPolicy>(), kGemmSmemBytes, stream>>>(
+        KlMaps{map_h, map_w, map_hr, map_wr}, p, err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     kl_merge_kernel<<<(N + 255) / 256, 256, 0, stream>>>(
-        p.part_p, p.part_a, p.part_r, p.part_b, p.s_target, targets, mask, N, V, p.num_chunks, k,
-        kr, kl, kl_rev, lse, lse_ref, logp, err);
+        p.part_p, p.part_a, p.part_r, p.part_b, p.s_target, targets, mask, N, V,
+        2 * p.num_chunks, k, kr, kl, kl_rev, lse, lse_ref, logp, err);
     return cudaGetLastError();
 }
 

@@ -106,16 +106,16 @@ inline size_t audit_v3_blocks(int64_t N) {
 }
 
 // Launchers (return the first CUDA error, cudaSuccess otherwise).
-// Full-vocabulary KL forward workspace: per (1024-column chunk, row) the
-// policy's (max, sum) float2 and sum of weighted log-ratios, the same for the
-// reference, and the policy's target logit per row.
+// Full-vocabulary KL forward workspace: per (1024-column chunk, column half of
+// its tiles, row) the policy's (max, sum) float2 and sum of weighted
+// log-ratios, the same for the reference, and the policy's target logit per row.
 struct KlFwdLayout {
     int64_t num_chunks;
     size_t part_p_off, part_a_off, part_r_off, part_b_off, target_off, total;
     KlFwdLayout(int64_t N, int64_t V) {
         const int64_t vt = (V + kTileV - 1) / kTileV;
         num_chunks = (vt + kFwdTilesPerChunk - 1) / kFwdTilesPerChunk;
-        const size_t cn = static_cast<size_t>(num_chunks) * N;
+        const size_t cn = static_cast<size_t>(num_chunks) * 2 * N;
         part_p_off = 0;
         part_a_off = align_up(cn * 8, 256);
         part_r_off = align_up(part_a_off + cn * 4, 256);
