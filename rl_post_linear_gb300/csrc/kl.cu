@@ -133,37 +133,49 @@ struct KlFwdPolicy {
                 st.sy = select32(x, static_cast<int>(dy));
                 st.found = true;
             }
-            float cm = -INFINITY, cmr = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                if (j < nv) {
-                    cm = fmaxf(cm, x[j]);
-                    cmr = fmaxf(cmr, xr[j]);
-                }
-            }
-            const float nm = fmaxf(st.m, cm), nmr = fmaxf(st.mr, cmr);
-            const float sc = ex2_approx((st.m - nm) * k), scr = ex2_approx((st.mr - nmr) * kr);
-            float s = st.s * sc, a = st.a * sc, sr = st.sr * scr, b = st.b * scr;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                if (j < nv) {
-                    // two rounded products, so that identical heads give d = 0 exactly
-                    const float d = __fmul_rn(x[j], k) - __fmul_rn(xr[j], kr);
-                    const float e = ex2_approx((x[j] - nm) * k);
-                    const float er = ex2_approx((xr[j] - nmr) * kr);
-                    s += e;
-                    a = fmaf(e, d, a);
-                    sr += er;
-                    b = fmaf(er, -d, b);
-                }
-            }
-            st.m = nm;
-            st.s = s;
-            st.a = a;
-            st.mr = nmr;
-            st.sr = sr;
-            st.b = b;
+            if (nv >= 32)
+                fold<true>(x, xr, 32, st);
+            else
+                fold<false>(x, xr, nv, st);
         }
+    }
+
+    // One 32-column slice of both heads into the row's running statistics; FULL
+    // (all 32 columns inside the vocabulary, a warp-uniform case) drops the
+    // per-column checks.
+    template <bool FULL>
+    __device__ __forceinline__ void fold(const float (&x)[32], const float (&xr)[32], int nv,
+                                         EpiState& st) const {
+        float cm = -INFINITY, cmr = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (FULL || j < nv) {
+                cm = fmaxf(cm, x[j]);
+                cmr = fmaxf(cmr, xr[j]);
+            }
+        }
+        const float nm = fmaxf(st.m, cm), nmr = fmaxf(st.mr, cmr);
+        const float sc = ex2_approx((st.m - nm) * k), scr = ex2_approx((st.mr - nmr) * kr);
+        float s = st.s * sc, a = st.a * sc, sr = st.sr * scr, b = st.b * scr;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (FULL || j < nv) {
+                // two rounded products, so that identical heads give d = 0 exactly
+                const float d = __fmul_rn(x[j], k) - __fmul_rn(xr[j], kr);
+                const float e = ex2_approx((x[j] - nm) * k);
+                const float er = ex2_approx((xr[j] - nmr) * kr);
+                s += e;
+                a = fmaf(e, d, a);
+                sr += er;
+                b = fmaf(er, -d, b);
+            }
+        }
+        st.m = nm;
+        st.s = s;
+        st.a = a;
+        st.mr = nmr;
+        st.sr = sr;
+        st.b = b;
     }
 
     __device__ void epi_end(int u, int row, int half, EpiState& st) const {
