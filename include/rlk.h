@@ -320,6 +320,35 @@ rlk_status_t rlk_linear_logp_merge(const float* partials, int64_t num_partials,
                                    uint32_t* device_error_word, cudaStream_t stream);
 
 /*
+ * Backward of a vocab-sharded head.  Each block of weight rows [vocab_start,
+ * vocab_start + V_local) of a vocab_size-row head contributes
+ *
+ *   dhidden_partial = sum_{v in block} G[t,v] W_v      (fp32 [N,H], unrounded)
+ *   dweight_shard   = rows of dW for the block           (bf16 [V_local,H])
+ *
+ * with G the logp gradient of rlk_linear_logp_bwd (its fp32 target and
+ * dominant-class terms go to the block holding the class).  lse is the
+ * merged forward's (rlk_linear_logp_merge); targets are global ids.
+ * dweight_shard is bit for bit the matching rows of the unsharded dW (a row's
+ * arithmetic does not depend on the blocking).  rlk_linear_logp_dh_merge then
+ * sums the partials of all blocks in ascending block order in fp32 and rounds
+ * once: dhidden = bf16( sum_r partials[r] ), partial r at dh_partials + r*N*H.
+ * Workspace: rlk_linear_logp_bwd_workspace_bytes(N, H, V_local).  The
+ * exchange of partials between ranks is the caller's (an all-gather, then the
+ * merge in rank order, keeps the result independent of the transport).
+ */
+rlk_status_t rlk_linear_logp_bwd_shard(const void* hidden, const void* weight_shard,
+                                       const int64_t* targets, const uint8_t* active_mask,
+                                       const float* grad_logp, const float* lse, int64_t N,
+                                       int64_t H, int64_t V_local, int64_t vocab_start,
+                                       int64_t vocab_size, double temperature,
+                                       float* dhidden_partial, void* dweight_shard,
+                                       void* workspace, size_t workspace_bytes,
+                                       uint32_t* device_error_word, cudaStream_t stream);
+rlk_status_t rlk_linear_logp_dh_merge(const float* dh_partials, int64_t num_partials, int64_t N,
+                                      int64_t H, void* dhidden, cudaStream_t stream);
+
+/*
  * Selected-token logp from existing logits.  "RL-Kernel integration roadmap
  * for vime", logp Reference Scoring: the reference / audit sibling of
  * linear_logp when logits already exist, with the same mask and temperature

@@ -123,6 +123,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.rlk_linear_kl_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64,
                                       _i64, _i64, _i64, ctypes.c_double, ctypes.c_double, _vp,
                                       _vp, _vp, _sz, _vp, _vp]
+    lib.rlk_linear_logp_bwd_shard.restype = ctypes.c_int
+    lib.rlk_linear_logp_bwd_shard.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
+                                              _i64, _i64, ctypes.c_double, _vp, _vp, _vp, _sz,
+                                              _vp, _vp]
+    lib.rlk_linear_logp_dh_merge.restype = ctypes.c_int
+    lib.rlk_linear_logp_dh_merge.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp]
     lib.rlk_linear_logp_entropy_bwd.restype = ctypes.c_int
     lib.rlk_linear_logp_entropy_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64,
                                                 _i64, _i64, ctypes.c_double, _vp, _vp, _vp, _sz,
@@ -388,6 +394,41 @@ def rlk_linear_kl_bwd(hidden, weight, hidden_ref, weight_ref, active_mask, grad_
                                   _ptr(workspace), workspace.numel(), _ptr(device_error_word),
                                   _stream(stream))
     _check("rlk_linear_kl_bwd", st)
+
+
+def rlk_linear_logp_bwd_shard(hidden, weight_shard, targets, active_mask, grad_logp, lse,
+                              vocab_start, vocab_size, temperature, dhidden_partial,
+                              dweight_shard, workspace, device_error_word=None, stream=None):
+    """One vocab block's fp32 dh partial and dW rows; see include/rlk.h."""
+    n, h = hidden.shape
+    v_local = weight_shard.shape[0]
+    _need(hidden, torch.bfloat16, "hidden")
+    _need(weight_shard, torch.bfloat16, "weight_shard", (v_local, h))
+    _need(targets, torch.int64, "targets", (n,))
+    if active_mask is not None:
+        _need(active_mask, torch.uint8, "active_mask", (n,))
+    _need(grad_logp, torch.float32, "grad_logp", (n,))
+    _need(lse, torch.float32, "lse", (n,))
+    _need(dhidden_partial, torch.float32, "dhidden_partial", (n, h))
+    _need(dweight_shard, torch.bfloat16, "dweight_shard", (v_local, h))
+    _need(workspace, torch.uint8, "workspace")
+    st = load().rlk_linear_logp_bwd_shard(_ptr(hidden), _ptr(weight_shard), _ptr(targets),
+                                          _ptr(active_mask), _ptr(grad_logp), _ptr(lse), n, h,
+                                          v_local, int(vocab_start), int(vocab_size),
+                                          float(temperature), _ptr(dhidden_partial),
+                                          _ptr(dweight_shard), _ptr(workspace), workspace.numel(),
+                                          _ptr(device_error_word), _stream(stream))
+    _check("rlk_linear_logp_bwd_shard", st)
+
+
+def rlk_linear_logp_dh_merge(dh_partials, dhidden, stream=None):
+    """dhidden = bf16(sum over the leading axis of dh_partials [k, N, H] fp32), ascending."""
+    k, n, h = dh_partials.shape
+    _need(dh_partials, torch.float32, "dh_partials")
+    _need(dhidden, torch.bfloat16, "dhidden", (n, h))
+    st = load().rlk_linear_logp_dh_merge(_ptr(dh_partials), k, n, h, _ptr(dhidden),
+                                         _stream(stream))
+    _check("rlk_linear_logp_dh_merge", st)
 
 
 def rlk_dlogp_audit(logp_new, logp_old, active_mask, result, workspace, stream=None):

@@ -283,6 +283,9 @@ rlk_status_t rlk_linear_kl_bwd(const void* hidden, const void* weight, const voi
     st.k = static_cast<float>(1.4426950408889634074 / temperature);
     st.temp = static_cast<float>(temperature);
     st.kl = true;
+    st.y_off = 0;
+    st.V_global = static_cast<int>(V);
+    st.round_last = true;
     st.H_ref = static_cast<int>(H_ref);
     st.k_ref = static_cast<float>(1.4426950408889634074 / temperature_ref);
     st.grad_rev = grad_kl_rev;
@@ -312,18 +315,27 @@ rlk_status_t rlk_linear_logp_entropy_fwd(const void* hidden, const void* weight,
                     entropy_out, workspace, workspace_bytes, device_error_word, stream);
 }
 
+// The logp (and entropy) backward.  dh_partial == nullptr: the whole vocabulary,
+// dh rounded to bf16 into dhidden.  Otherwise weight holds the rows
+// [vocab_start, vocab_start + V) of a vocab_size-row head, and that block's fp32
+// contribution to dh is written to dh_partial (dhidden unused).
 static rlk_status_t bwd_impl(const void* hidden, const void* weight, const int64_t* targets,
                              const uint8_t* active_mask, const float* grad_logp,
                              const float* grad_entropy, const float* entropy, const float* lse,
-                             int64_t N, int64_t H, int64_t V, double temperature, void* dhidden,
-                             void* dweight, void* workspace, size_t workspace_bytes,
-                             uint32_t* device_error_word, cudaStream_t stream) {
+                             int64_t N, int64_t H, int64_t V, int64_t vocab_start,
+                             int64_t vocab_size, double temperature, void* dhidden,
+                             float* dh_partial, void* dweight, void* workspace,
+                             size_t workspace_bytes, uint32_t* device_error_word,
+                             cudaStream_t stream) {
     RLK_TRY(check_shape(N, H, V, temperature));
-    if (N == 0) return RLK_OK;
-    if (hidden == nullptr || weight == nullptr || targets == nullptr || grad_logp == nullptr ||
-        lse == nullptr || dhidden == nullptr || dweight == nullptr)
+    if (vocab_start < 0 || vocab_size > kMaxDim || vocab_start + V > vocab_size)
         return RLK_ERR_INVALID_VALUE;
-    if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(dhidden, 16) ||
+    if (N == 0) return RLK_OK;
+    void* dh_out = dh_partial != nullptr ? static_cast<void*>(dh_partial) : dhidden;
+    if (hidden == nullptr || weight == nullptr || targets == nullptr || grad_logp == nullptr ||
+        lse == nullptr || dh_out == nullptr || dweight == nullptr)
+        return RLK_ERR_INVALID_VALUE;
+    if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(dh_out, 16) ||
         !aligned(dweight, 16))
         return RLK_ERR_INVALID_VALUE;
     if (workspace == nullptr || !aligned(workspace, 256) ||
@@ -345,10 +357,11 @@ static rlk_status_t bwd_impl(const void* hidden, const void* weight, const int64
     RLK_TRY(make_map(&maps.h_mnmajor, hidden, H, N, H * 2, 64, 64));
 
     const int n = static_cast<int>(N), h = static_cast<int>(H), v = static_cast<int>(V);
+    const int v_global = static_cast<int>(vocab_size);
     int* dom = reinterpret_cast<int*>(ws + lay.dom_off);
     uint64_t* tiles = reinterpret_cast<uint64_t*>(ws + lay.tiles_off);
-    RLK_CUDA(rlk::launch_target_sort(targets, active_mask, n, v, tiles, sorted_y, sorted_t, dom,
-                                     device_error_word, stream));
+    RLK_CUDA(rlk::launch_target_sort(targets, active_mask, n, v, vocab_start, v_global, tiles,
+                                     sorted_y, sorted_t, dom, device_error_word, stream));
     const int num_chunks = static_cast<int>((V + rlk::kBwdChunk - 1) / rlk::kBwdChunk);
     rlk::BwdStep st{};
     st.targets = targets;
@@ -365,7 +378,10 @@ static rlk_status_t bwd_impl(const void* hidden, const void* weight, const int64
     st.num_chunks = num_chunks;
     st.k = static_cast<float>(1.4426950408889634074 / temperature);
     st.temp = static_cast<float>(temperature);
-    st.dh_acc = dh_acc;
+    st.y_off = vocab_start;
+    st.V_global = v_global;
+    st.round_last = dh_partial == nullptr;
+    st.dh_acc = dh_partial != nullptr ? dh_partial : dh_acc;
     st.sorted_y = sorted_y;
     st.sorted_t = sorted_t;
     st.ycoef = reinterpret_cast<float*>(ws + lay.ycoef_off);
@@ -386,8 +402,36 @@ rlk_status_t rlk_linear_logp_bwd(const void* hidden, const void* weight, const i
                                  void* workspace, size_t workspace_bytes,
                                  uint32_t* device_error_word, cudaStream_t stream) {
     return bwd_impl(hidden, weight, targets, active_mask, grad_logp, nullptr, nullptr, lse, N, H,
-                    V, temperature, dhidden, dweight, workspace, workspace_bytes,
+                    V, 0, V, temperature, dhidden, nullptr, dweight, workspace, workspace_bytes,
                     device_error_word, stream);
+}
+
+rlk_status_t rlk_linear_logp_bwd_shard(const void* hidden, const void* weight_shard,
+                                       const int64_t* targets, const uint8_t* active_mask,
+                                       const float* grad_logp, const float* lse, int64_t N,
+                                       int64_t H, int64_t V_local, int64_t vocab_start,
+                                       int64_t vocab_size, double temperature,
+                                       float* dhidden_partial, void* dweight_shard,
+                                       void* workspace, size_t workspace_bytes,
+                                       uint32_t* device_error_word, cudaStream_t stream) {
+    if (N > 0 && dhidden_partial == nullptr) return RLK_ERR_INVALID_VALUE;
+    return bwd_impl(hidden, weight_shard, targets, active_mask, grad_logp, nullptr, nullptr, lse,
+                    N, H, V_local, vocab_start, vocab_size, temperature, nullptr,
+                    dhidden_partial, dweight_shard, workspace, workspace_bytes,
+                    device_error_word, stream);
+}
+
+rlk_status_t rlk_linear_logp_dh_merge(const float* dh_partials, int64_t num_partials, int64_t N,
+                                      int64_t H, void* dhidden, cudaStream_t stream) {
+    if (num_partials < 1 || N < 0 || N > kMaxDim || H < 1 || H % 64 != 0)
+        return num_partials < 1 || N < 0 || N > kMaxDim || H < 1 ? RLK_ERR_INVALID_VALUE
+                                                                 : RLK_ERR_UNSUPPORTED;
+    if (N == 0) return RLK_OK;
+    if (dh_partials == nullptr || dhidden == nullptr || !aligned(dh_partials, 16) ||
+        !aligned(dhidden, 16))
+        return RLK_ERR_INVALID_VALUE;
+    RLK_CUDA(rlk::launch_dh_merge(dh_partials, num_partials, N, H, dhidden, stream));
+    return RLK_OK;
 }
 
 rlk_status_t rlk_linear_logp_entropy_bwd(const void* hidden, const void* weight,
@@ -400,8 +444,8 @@ rlk_status_t rlk_linear_logp_entropy_bwd(const void* hidden, const void* weight,
                                          cudaStream_t stream) {
     if (N > 0 && (grad_entropy == nullptr || entropy == nullptr)) return RLK_ERR_INVALID_VALUE;
     return bwd_impl(hidden, weight, targets, active_mask, grad_logp, grad_entropy, entropy, lse,
-                    N, H, V, temperature, dhidden, dweight, workspace, workspace_bytes,
-                    device_error_word, stream);
+                    N, H, V, 0, V, temperature, dhidden, nullptr, dweight, workspace,
+                    workspace_bytes, device_error_word, stream);
 }
 
 rlk_status_t rlk_dlogp_audit(const float* logp_new, const float* logp_old,

@@ -91,7 +91,9 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
     float* ycoef;         // [N]: 1 - p_y of each live row, written by the tile holding y
     int* dom;             // [N]: the row's dominant non-target class (p > 1/2), else -1
     float* dcoef;         // [N]: that class's fp32 gradient coefficient, -g/T
-    int N, V, c0, num_m, num_n, kblocks;
+    int64_t y_off;        // global id of this weight block's first row (0 unsharded)
+    int V_global;         // vocabulary size (target validity)
+    int N, V, c0, num_m, num_n, kblocks;   // V: rows of this weight block
     float k, temp;
 
     __device__ int num_units() const { return num_m * num_n; }
@@ -123,9 +125,9 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
         unit(u, m, n);
         const int t = m * kTileM + row;
         int64_t y;
-        st.live = row_live(targets, mask, t, N, V, y);
+        st.live = row_live(targets, mask, t, N, V_global, y);
         st.lse2 = st.live ? lse[t] * kLog2e : 0.f;
-        st.ycol = y - c0;
+        st.ycol = y - y_off - c0;       // outside [0, 32 * 8) unless y is in this chunk
         st.coef_y = 0.f;
         st.gt = st.live ? __fdiv_rn(grad[t], temp) : 0.f;
         if constexpr (ENT) {
@@ -382,8 +384,11 @@ struct DhPolicy : SingleRole<false, true> {
     const float* ycoef;            // [N] 1 - p_y, from the dS GEMM
     const int* dom;                // [N] dominant non-target class or -1, from the dS GEMM
     const float* dcoef;            // [N] its fp32 coefficient
+    int64_t y_off;                 // global id of this weight block's first row
+    int V_global;                  // vocabulary size (target validity)
     int N, V, H, c0, num_m, num_n, kblocks;
     bool first, last;
+    bool round_last;               // false: the last chunk leaves dh_acc in fp32 (a partial)
     bool terms;                    // false: no fp32 target terms (no targets)
     float temp;
 
@@ -407,9 +412,9 @@ struct DhPolicy : SingleRole<false, true> {
 
     struct EpiState {
         float coef, coef_dom;
-        int64_t y;
+        int64_t y;                 // target row inside this weight block
         int dom;
-        bool live;
+        bool live, tgt;            // tgt: the row's target term belongs to this block
     };
 
     __device__ void epi_begin(int u, int row, EpiState& st) const {
@@ -419,12 +424,15 @@ struct DhPolicy : SingleRole<false, true> {
         // the fp32 terms, added once, in the last chunk's epilogue: (g / T)(1 - p_y) W[y]
         // and, for a dominant non-target class a, dcoef W[a]
         if (terms) {
-            st.live = row_live(targets, mask, t, N, V, st.y);
+            st.live = row_live(targets, mask, t, N, V_global, st.y);
+            st.y -= y_off;
+            st.tgt = st.live && last && st.y >= 0 && st.y < V;
             const float gt = (st.live && last) ? __fdiv_rn(grad[t], temp) : 0.f;
-            st.coef = (st.live && last) ? gt * ycoef[t] : 0.f;
+            st.coef = st.tgt ? gt * ycoef[t] : 0.f;
         } else {
             st.live = t < N && (mask == nullptr || mask[t] != 0);
             st.y = 0;
+            st.tgt = false;
             st.coef = 0.f;
         }
         st.dom = (st.live && last) ? dom[t] : -1;
@@ -463,7 +471,7 @@ struct DhPolicy : SingleRole<false, true> {
                 continue;
             }
             if (st.live) {
-                if (terms) {
+                if (st.tgt) {
                     const uint4* wr = reinterpret_cast<const uint4*>(
                         weight + static_cast<size_t>(st.y) * H + col);
 #pragma unroll
@@ -490,6 +498,13 @@ struct DhPolicy : SingleRole<false, true> {
             } else {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) x[j] = 0.f;
+            }
+            if (!round_last) {             // a vocab block's fp32 partial of dh
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    reinterpret_cast<float4*>(acc)[i] =
+                        make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+                continue;
             }
             uint4* dst = reinterpret_cast<uint4*>(dh + static_cast<size_t>(t) * H + col);
 #pragma unroll
@@ -651,19 +666,23 @@ __device__ __forceinline__ void bitonic_sort_tile(uint64_t* key) {
 // Keys (target, token) of the dW target terms; also resets dom[] to "no dominant class".
 __global__ void __launch_bounds__(kSortThreads)
     target_tile_sort_kernel(const int64_t* __restrict__ targets, const uint8_t* __restrict__ mask,
-                            int N, int V, uint64_t* __restrict__ tiles, int* __restrict__ dom,
-                            uint32_t* err) {
+                            int N, int V, int64_t y_off, int V_global,
+                            uint64_t* __restrict__ tiles, int* __restrict__ dom, uint32_t* err) {
     __shared__ uint64_t key[kSortTile];
     const int base = blockIdx.x * kSortTile;
     for (int i = threadIdx.x; i < kSortTile; i += kSortThreads) {
         const int t = base + i;
         uint64_t k = kPadKey;
         if (t < N) {
-            int y = V;
+            int y = V;                          // V: no target term in this block
             if (mask == nullptr || mask[t] != 0) {
                 const int64_t yt = targets[t];
-                if (yt >= 0 && yt < V) y = static_cast<int>(yt);
-                else if (err != nullptr) atomicOr(err, RLK_DEVERR_TARGET_RANGE);
+                if (yt >= 0 && yt < V_global) {
+                    const int64_t yl = yt - y_off;
+                    if (yl >= 0 && yl < V) y = static_cast<int>(yl);
+                } else if (err != nullptr) {
+                    atomicOr(err, RLK_DEVERR_TARGET_RANGE);
+                }
             }
             k = (static_cast<uint64_t>(y) << 32) | static_cast<uint32_t>(t);
             dom[t] = -1;
@@ -730,11 +749,11 @@ static cudaError_t place_sorted(const uint64_t* tiles, int N, int* sorted_key, i
 }
 
 cudaError_t launch_target_sort(const int64_t* targets, const uint8_t* mask, int N, int V,
-                               uint64_t* tiles, int* sorted_y, int* sorted_t, int* dom,
-                               uint32_t* err, cudaStream_t stream) {
+                               int64_t y_off, int V_global, uint64_t* tiles, int* sorted_y,
+                               int* sorted_t, int* dom, uint32_t* err, cudaStream_t stream) {
     const int num_tiles = (N + kSortTile - 1) / kSortTile;
-    target_tile_sort_kernel<<<num_tiles, kSortThreads, 0, stream>>>(targets, mask, N, V, tiles,
-                                                                     dom, err);
+    target_tile_sort_kernel<<<num_tiles, kSortThreads, 0, stream>>>(targets, mask, N, V, y_off,
+                                                                     V_global, tiles, dom, err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return place_sorted(tiles, N, sorted_y, sorted_t, stream);
@@ -777,6 +796,8 @@ static cudaError_t launch_ds(const BwdStepMaps& maps, const BwdStep& st, int c0,
     ps.ycoef = st.ycoef;
     ps.dom = st.dom;
     ps.dcoef = st.dcoef;
+    ps.y_off = st.y_off;
+    ps.V_global = st.V_global;
     ps.N = st.N;
     ps.V = st.V;
     ps.c0 = c0;
@@ -847,6 +868,9 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
         pd.ycoef = st.ycoef;
         pd.dom = st.dom;
         pd.dcoef = st.dcoef;
+        pd.y_off = st.y_off;
+        pd.V_global = st.V_global;
+        pd.round_last = st.round_last;
         pd.N = N;
         pd.V = V;
         pd.H = H;
@@ -882,6 +906,33 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
     pw.terms = !st.kl;
     return launch_gemm(maps.ds_mnmajor, maps.h_mnmajor, pw, pw.num_m * pw.num_n, num_sms, err,
                        stream);
+}
+
+// ----------------------------------------------------------------------------- dh merge
+
+// dh = bf16( sum_r partials[r] ), r ascending, fp32 sums; four elements a thread.
+__global__ void dh_merge_kernel(const float4* __restrict__ partials, int64_t num_parts,
+                                int64_t n4, uint2* __restrict__ dh) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= n4) return;
+    float4 a = partials[i];
+    for (int64_t r = 1; r < num_parts; ++r) {
+        const float4 b = partials[r * n4 + i];
+        a.x += b.x;
+        a.y += b.y;
+        a.z += b.z;
+        a.w += b.w;
+    }
+    dh[i] = make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
+}
+
+cudaError_t launch_dh_merge(const float* partials, int64_t num_parts, int64_t N, int64_t H,
+                            void* dhidden, cudaStream_t stream) {
+    const int64_t n4 = N * H / 4;                  // H is a multiple of 64
+    if (n4 == 0) return cudaSuccess;
+    dh_merge_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, stream>>>(
+        reinterpret_cast<const float4*>(partials), num_parts, n4, static_cast<uint2*>(dhidden));
+    return cudaGetLastError();
 }
 
 }  // namespace rlk

@@ -182,9 +182,12 @@ struct BwdStep {
     const float* lse;
     const void* hidden;
     const void* weight;
-    int N, H, V, num_chunks;
+    int N, H, V, num_chunks;       // V: rows of the weight (block) being differentiated
     int chunk, role;
     float k, temp;
+    int64_t y_off;             // global id of the weight block's first row (0 unsharded)
+    int V_global;              // vocabulary size
+    bool round_last;           // false: dh_acc is the caller's fp32 partial, left unrounded
     // KL against a reference head (kl = true): dS from both heads, no fp32 target terms
     bool kl;
     int H_ref;
@@ -207,8 +210,11 @@ struct BwdStep {
 };
 
 cudaError_t launch_target_sort(const int64_t* targets, const uint8_t* mask, int N, int V,
-                               uint64_t* tiles, int* sorted_y, int* sorted_t, int* dom,
-                               uint32_t* err, cudaStream_t stream);
+                               int64_t y_off, int V_global, uint64_t* tiles, int* sorted_y,
+                               int* sorted_t, int* dom, uint32_t* err, cudaStream_t stream);
+
+cudaError_t launch_dh_merge(const float* partials, int64_t num_parts, int64_t N, int64_t H,
+                            void* dhidden, cudaStream_t stream);
 
 cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& step, int num_sms,
                             uint32_t* err, cudaStream_t stream);

@@ -1,4 +1,5 @@
-"""Tensor-parallel (vocab-sharded) forward on top of the shard / merge entry points.
+"""Tensor-parallel (vocab-sharded) forward and backward on top of the shard / merge
+entry points.
 
 "RL-Kernel integration roadmap for vime", linear_logp: TP support makes the
 vocab-shard merge explicit (local max, global max, local sum-exp, global
@@ -11,7 +12,13 @@ global chunk order), and of the target-logit rows, each row taken from the
 rank whose block holds its target.  ``rlk_linear_logp_merge`` then gives logp
 and lse bitwise equal to the unsharded forward.
 
-The exchange is the only collective; every arithmetic step runs in the
+The backward needs one more exchange: every rank computes its block's fp32
+contribution to dh with ``rlk_linear_logp_bwd_shard`` (and its own rows of dW);
+``gather_dh_partials`` all-gathers the partials in rank order and
+``rlk_linear_logp_dh_merge`` sums them in that order and rounds once, so every
+rank gets the same dh whatever the transport.
+
+The exchanges are the only collectives; every arithmetic step runs in the
 library's kernels.
 """
 from __future__ import annotations
@@ -77,3 +84,13 @@ def exchange(local_partials, local_target_logit, owner, group=None):
     tl = [torch.empty_like(local_target_logit) for _ in range(world)]
     dist.all_gather(tl, local_target_logit.contiguous(), group=group)
     return assemble(gathered, tl, owner)
+
+
+def gather_dh_partials(local_partial, group=None):
+    """All-gather every rank's fp32 dh partial [N, H]; returns [world, N, H] in rank order
+    (the order rlk_linear_logp_dh_merge sums in).  Pure data movement."""
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    gathered = [torch.empty_like(local_partial) for _ in range(world)]
+    dist.all_gather(gathered, local_partial.contiguous(), group=group)
+    return torch.stack(gathered, dim=0)

@@ -73,3 +73,63 @@ def test_tp_flags_out_of_range_targets_and_rejects_unaligned_blocks():
     with pytest.raises(rlk.RlkError) as ex:
         rlk.rlk_linear_logp_fwd_shard(hid, w[100:1100], y, None, 100, 1.0, part, tl)
     assert ex.value.status == rlk.RLK_ERR_UNSUPPORTED
+
+
+def _sharded_bwd(h, w, y, m, g, lse, T, bounds):
+    """Backward over the vocab blocks [bounds[i], bounds[i+1]), then the dh merge."""
+    d = h.device
+    n, hdim = h.shape
+    vocab = w.shape[0]
+    parts = len(bounds) - 1
+    partials = torch.empty(parts, n, hdim, dtype=torch.float32, device=d)
+    dw = torch.empty_like(w)
+    err = torch.zeros(1, dtype=torch.int32, device=d)
+    for r in range(parts):
+        a, b = bounds[r], bounds[r + 1]
+        ws = torch.empty(max(256, rlk.rlk_linear_logp_bwd_workspace_bytes(n, hdim, b - a)),
+                         dtype=torch.uint8, device=d)
+        rlk.rlk_linear_logp_bwd_shard(h, w[a:b], y, m, g, lse, a, vocab, T, partials[r],
+                                      dw[a:b], ws, err)
+    dh = torch.empty_like(h)
+    rlk.rlk_linear_logp_dh_merge(partials, dh)
+    torch.cuda.synchronize()
+    return dh, dw, int(err.item())
+
+
+@pytest.mark.parametrize("n,h,vocab,T,std", [(200, 256, 70000, 0.8, 0.05),
+                                             (150, 128, 9000, 0.3, 0.5)])
+def test_tp_backward(n, h, vocab, T, std):
+    # dW blocks are bitwise the rows of the unsharded dW (a row's arithmetic does not depend
+    # on the blocking); one block reproduces the unsharded dh bit for bit; more blocks change
+    # only the fp32 order in which dh's vocabulary sum is taken.
+    d = dev()
+    seed = n + vocab
+    hid = wl.normal_bf16((n, h), seed, wl.S_HIDDEN).to(d)
+    w = wl.normal_bf16((vocab, h), seed, wl.S_WEIGHT, std=std).to(d)
+    y = wl.uniform_targets(n, vocab, seed).to(d)
+    m = torch.from_numpy((np.random.default_rng(seed).random(n) < 0.9).astype(np.uint8)).to(d)
+    g = torch.tensor(np.random.default_rng(seed + 1).standard_normal(n) / n, dtype=torch.float32,
+                     device=d)
+    _, lse = rlk.linear_logp_fwd(hid, w, y, m, T)
+    dh_ref, dw_ref = rlk.linear_logp_bwd(hid, w, y, m, g, lse, T)
+    dh1, dw1, e = _sharded_bwd(hid, w, y, m, g, lse, T, [0, vocab])
+    assert e == 0 and same_bits(dh1.cpu(), dh_ref.cpu()) and same_bits(dw1.cpu(), dw_ref.cpu())
+    import oracle
+    from helpers import GRAD_REL_L2, f64, rel_l2
+    h64, w64 = f64(hid.cpu()), f64(w.cpu())
+    _, lse_o = oracle.linear_logp_fwd_parallel(h64, w64, y.cpu().numpy(), m.cpu().numpy(), T)
+    g64 = g.cpu().double().numpy()
+    dh_o = oracle.linear_logp_bwd_dh_parallel(h64, w64, y.cpu().numpy(), m.cpu().numpy(), g64,
+                                              lse_o, T)
+    for parts in (2, 4, 8):
+        bounds = [a for a, _ in tp.vocab_shards(vocab, parts)] + [vocab]
+        bounds = sorted(set(bounds))
+        dhp, dwp, e = _sharded_bwd(hid, w, y, m, g, lse, T, bounds)
+        assert e == 0 and same_bits(dwp.cpu(), dw_ref.cpu()), parts
+        err = rel_l2(dhp.cpu(), dh_o)
+        print("tp bwd parts=%d: dh rel-L2 %.3e (unsharded %.3e)" % (parts, err,
+                                                                   rel_l2(dh_ref.cpu(), dh_o)))
+        assert err <= GRAD_REL_L2
+    # block boundaries need no alignment for the backward
+    dhq, dwq, _ = _sharded_bwd(hid, w, y, m, g, lse, T, [0, 1000, vocab // 2 + 7, vocab])
+    assert same_bits(dwq.cpu(), dw_ref.cpu()) and rel_l2(dhq.cpu(), dh_o) <= GRAD_REL_L2

@@ -89,3 +89,29 @@ def test_two_rank_exchange_gloo():
     assert out[0] == out[1]
     assert chunks == [0.0, 1.0, 2.0, 3.0, 4.0]          # global chunk order
     assert tl == [float(o) for o in owner]               # from the owning rank
+
+
+def _dh_worker(rank, world, port, out):
+    import torch.distributed as dist
+    dist.init_process_group("gloo", init_method="tcp://127.0.0.1:%d" % port, rank=rank,
+                            world_size=world)
+    try:
+        local = torch.full((3, 4), float(rank + 1))
+        g = tp.gather_dh_partials(local)
+        out[rank] = g[:, 0, 0].tolist()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_dh_partials_gloo():
+    # every rank receives the partials stacked in rank order
+    ctx = mp.get_context("spawn")
+    out = ctx.Manager().dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_dh_worker, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    assert out[0] == out[1] == [1.0, 2.0]
