@@ -175,3 +175,28 @@ def test_audit_two_to_the_26():
     assert r["argmax_index"] == o["argmax_index"]
     assert r["max_abs_dlogp"] == np.float32(o["max_abs_dlogp"])
     assert abs(r["approx_kl"] - o["approx_kl"]) <= 1e-6 * o["approx_kl"]
+
+
+def test_qwen_entropy_and_kl_sampled(qwen):
+    # the next rows at the shape the benchmark times them: entropy of the policy, and the
+    # full-vocabulary KL against a reference head of the same shape, on sampled tokens
+    w, w64 = qwen
+    d = dev()
+    hd, wd, yd, md = w.hidden.to(d), w.weight.to(d), w.targets.to(d), w.mask.to(d)
+    _, _, ent = rlk.linear_logp_entropy_fwd(hd, wd, yd, md, w.temperature)
+    rows = _sample_rows(w, 24, 7)
+    _, _, ent_o = oracle.linear_logp_entropy_fwd_parallel(f64(w.hidden[rows]), w64,
+                                                          w.targets[rows].numpy(), None,
+                                                          w.temperature)
+    de = np.abs(ent.cpu().double().numpy()[rows] - ent_o)
+    hr = wl.normal_bf16((w.n, w.h), 1, wl.S_HIDDEN)
+    wr = wl.normal_bf16((w.v, w.h), 1, wl.S_WEIGHT, std=0.02)
+    kl, kr, lse, lse_r, _ = rlk.linear_kl_fwd(hd, wd, hr.to(d), wr.to(d), md, w.temperature,
+                                              1.0)
+    rows = rows[:12]
+    o = oracle.linear_kl_fwd_parallel(f64(w.hidden[rows]), w64, f64(hr[rows]),
+                                      oracle.bf16_bits_to_f64(wr), None, w.temperature, 1.0)
+    dk = [np.abs(x.cpu().double().numpy()[rows] - e).max() for x, e in zip((kl, kr, lse, lse_r), o)]
+    print("qwen entropy: max |dH| %.3e (H ~ %.2f); KL ~ %.3f: max |d| kl %.2e rev %.2e lse %.2e "
+          "%.2e" % (de.max(), ent_o.mean(), o[0].mean(), *dk))
+    assert de.max() <= LOGP_ATOL and max(dk) <= LOGP_ATOL
