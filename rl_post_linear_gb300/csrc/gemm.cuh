@@ -6,7 +6,8 @@
 //                 tcgen05.mma.cta_group::1.kind::f16, M=128 N=256 K=16,
 //                 fp32 accumulators in TMEM, two 256-column buffers so the
 //                 epilogue of tile i overlaps the MMAs of tile i+1
-//   warps 2..5  : epilogue, one thread per accumulator row (TMEM lane),
+//   warps 2..   : epilogue (4 warps, or 8 for paired-tile policies), one
+//                 thread per accumulator row (TMEM lane) and column half,
 //                 reading 32-column slices with tcgen05.ld
 //
 // The policy P decides the operands' majorness, the work units (a unit is a

@@ -157,8 +157,7 @@ inline int64_t fwd_num_chunks(int64_t V) {
     return ((V + kTileV - 1) / kTileV + kFwdTilesPerChunk - 1) / kFwdTilesPerChunk;
 }
 
-// One backward launch: any of the dS recompute of produce_chunk and the dh / dW
-// GEMMs of consume_chunk (the library launches one role at a time).
+// Tensor maps of the backward launches (one role per launch).
 struct BwdStepMaps {
     CUtensorMap h_kmajor;      // hidden [N,H], box {64, 128}: A of the dS recompute
     CUtensorMap w_kmajor;      // weight [V,H], box {64, 256}: B of the dS recompute
