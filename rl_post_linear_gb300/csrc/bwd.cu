@@ -338,6 +338,7 @@ struct DsKlPolicy {
                 }
             }
             uint32_t packed[16];
+            float gdom = 0.f;                           // the dominant entry's gradient
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 float d[2];
@@ -350,14 +351,15 @@ struct DsKlPolicy {
                     const float p = ex2_approx(l2p), q = ex2_approx(l2q);
                     const float ell = (l2p - l2q) * kLn2;
                     const float g = fmaf(st.gp * p, ell - st.kl, st.gq * (p - q));
-                    d[e] = (st.live && vb + 2 * j + e < V) ? g : 0.f;
-                    if (ai == 2 * j + e) {              // fp32 path for the dominant entry
-                        dom[t] = vb + ai;
-                        dcoef[t] = g;
-                        d[e] = 0.f;
-                    }
+                    const bool is_dom = ai == 2 * j + e;        // fp32 path, not dS
+                    gdom = is_dom ? g : gdom;
+                    d[e] = (st.live && vb + 2 * j + e < V && !is_dom) ? g : 0.f;
                 }
                 packed[j] = pack_bf16x2(d[0], d[1]);
+            }
+            if (ai < 32) {
+                dom[t] = vb + ai;
+                dcoef[t] = gdom;
             }
             uint4* dst = reinterpret_cast<uint4*>(ds + static_cast<size_t>(t) * kBwdChunk + col);
 #pragma unroll
