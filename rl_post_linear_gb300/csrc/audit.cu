@@ -7,13 +7,15 @@
 //
 // Pass 1: block b owns the fixed slice [b*4096, (b+1)*4096) (a function of N
 // only).  Each thread issues all its loads first (4 float4 of each input and 4
-// mask words, streaming cache hint), then handles its 16 elements in ascending
-// index order without branches: d = new - old in fp32 (a correctly rounded
-// difference), its count, the largest |d| as an order-preserving integer key
-// with the first offset attaining it, and fp32 sums of d and of
-// kl(d) = exp(d) - 1 - d.  A fixed shuffle tree combines the 32 lanes (fp32
-// sums, integer counts), and thread 0 folds the eight warp partials in warp
-// order in fp64.  Pass 2: one block merges the per-block partials,
+// mask words, streaming cache hint), then handles its 16 elements without
+// branches: d = new - old in fp32 (a correctly rounded difference), its
+// count, the largest |d| as an order-preserving integer key with the first
+// offset attaining it, and fp32 sums of d and of kl(d) = exp(d) - 1 - d, in
+// four interleaved chains merged in a fixed order.  A fixed shuffle tree
+// combines the 32 lanes (fp32 sums, integer counts), and thread 0 folds the
+// eight warp partials in warp order into float-pair sums (about 48 bits:
+// two-sum; this GPU's fp64 units are few and slow).  Pass 2: one block merges
+// the per-block partials,
 // each thread a fixed strided subset in ascending order, then the same
 // fixed tree; it is launched with programmatic dependent launch, so its launch
 // overlaps pass 1 and it waits for pass 1's results in-kernel.  No atomics; the
@@ -63,11 +65,26 @@ __device__ __forceinline__ bool ranks_above(float a1, int64_t i1, float a2, int6
     return i1 < i2;
 }
 
+// a + b as a float pair (two-sum, then renormalisation), in a fixed
+// evaluation order: deterministic, and exact to about 2^-44 relative.
+__device__ __forceinline__ DFloat df_add(DFloat a, DFloat b) {
+    const float s = __fadd_rn(a.hi, b.hi);
+    const float bv = __fsub_rn(s, a.hi);
+    const float e = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bv)), __fsub_rn(b.hi, bv));
+    const float lo = __fadd_rn(e, __fadd_rn(a.lo, b.lo));
+    const float hi = __fadd_rn(s, lo);
+    return DFloat{hi, __fsub_rn(lo, __fsub_rn(hi, s))};
+}
+
+__device__ __forceinline__ double df_value(DFloat a) {
+    return static_cast<double>(a.hi) + static_cast<double>(a.lo);
+}
+
 struct Acc {
     int64_t count;
     int64_t arg;
-    double sum_d;
-    double sum_kl;
+    DFloat sum_d;
+    DFloat sum_kl;
     float best;
     uint32_t flags;
 };
@@ -76,8 +93,8 @@ __device__ __forceinline__ Acc empty_acc() {
     Acc a;
     a.count = 0;
     a.arg = INT64_MAX;
-    a.sum_d = 0.0;
-    a.sum_kl = 0.0;
+    a.sum_d = DFloat{0.f, 0.f};
+    a.sum_kl = DFloat{0.f, 0.f};
     a.best = -1.0f;
     a.flags = 0;
     return a;
@@ -86,8 +103,8 @@ __device__ __forceinline__ Acc empty_acc() {
 // a := a (+) b, with a covering lower indices than b
 __device__ __forceinline__ void merge(Acc& a, const Acc& b) {
     a.count += b.count;
-    a.sum_d += b.sum_d;
-    a.sum_kl += b.sum_kl;
+    a.sum_d = df_add(a.sum_d, b.sum_d);
+    a.sum_kl = df_add(a.sum_kl, b.sum_kl);
     a.flags |= b.flags;
     if (b.count > 0 && (a.count == b.count || ranks_above(b.best, b.arg, a.best, a.arg))) {
         a.best = b.best;
@@ -99,8 +116,10 @@ __device__ __forceinline__ Acc shfl_down(const Acc& a, int off) {
     Acc b;
     b.count = __shfl_down_sync(0xffffffffu, a.count, off);
     b.arg = __shfl_down_sync(0xffffffffu, a.arg, off);
-    b.sum_d = __shfl_down_sync(0xffffffffu, a.sum_d, off);
-    b.sum_kl = __shfl_down_sync(0xffffffffu, a.sum_kl, off);
+    b.sum_d.hi = __shfl_down_sync(0xffffffffu, a.sum_d.hi, off);
+    b.sum_d.lo = __shfl_down_sync(0xffffffffu, a.sum_d.lo, off);
+    b.sum_kl.hi = __shfl_down_sync(0xffffffffu, a.sum_kl.hi, off);
+    b.sum_kl.lo = __shfl_down_sync(0xffffffffu, a.sum_kl.lo, off);
     b.best = __shfl_down_sync(0xffffffffu, a.best, off);
     b.flags = __shfl_down_sync(0xffffffffu, a.flags, off);
     return b;
@@ -262,14 +281,14 @@ __global__ void __launch_bounds__(kAuditThreads)
             a.flags |= f;
         }
     }
-    // the eight warp partials, in warp order, in fp64
+    // the eight warp partials, in warp order, in float pairs
     __shared__ Acc warp_acc[kAuditThreads / 32];
     if (lane == 0) {
         Acc w;
         w.count = a.count;
         w.arg = a.key == 0 ? INT64_MAX : base + a.arg;
-        w.sum_d = static_cast<double>(a.sd);
-        w.sum_kl = static_cast<double>(a.skl);
+        w.sum_d = DFloat{a.sd, 0.f};
+        w.sum_kl = DFloat{a.skl, 0.f};
         w.best = a.key == 0 ? -1.0f : __uint_as_float(a.key - 1u);
         w.flags = a.flags;
         warp_acc[warp] = w;
@@ -316,8 +335,8 @@ __global__ void __launch_bounds__(kMergeThreads)
         r.active_count = a.count;
         r.argmax_index = a.count > 0 ? a.arg : -1;
         r.max_abs_dlogp = a.count > 0 ? a.best : 0.0f;
-        r.mean_dlogp = a.sum_d / static_cast<double>(a.count);
-        r.approx_kl = a.sum_kl / static_cast<double>(a.count);
+        r.mean_dlogp = df_value(a.sum_d) / static_cast<double>(a.count);
+        r.approx_kl = df_value(a.sum_kl) / static_cast<double>(a.count);
         r.error_flags = a.flags;
         *result = r;
     }
@@ -438,8 +457,8 @@ __global__ void __launch_bounds__(kAuditThreads)
         Acc w;
         w.count = a.count;
         w.arg = a.key == 0 ? INT64_MAX : base + a.arg;
-        w.sum_d = static_cast<double>(a.sd);
-        w.sum_kl = static_cast<double>(a.skl);
+        w.sum_d = DFloat{a.sd, 0.f};
+        w.sum_kl = DFloat{a.skl, 0.f};
         w.best = a.key == 0 ? -1.0f : __uint_as_float(a.key - 1u);
         w.flags = a.flags;
         warp_acc[warp] = w;
@@ -544,10 +563,10 @@ __global__ void __launch_bounds__(kMergeThreads)
     }
     r.clip_count = s_clip[0];
     const double cnt = static_cast<double>(a.count);
-    r.mean_dlogp = a.sum_d / cnt;
+    r.mean_dlogp = df_value(a.sum_d) / cnt;
     r.mean_abs_dlogp = s_abs[0] / cnt;
     r.mean_ratio = s_ratio[0] / cnt;
-    r.approx_kl = a.sum_kl / cnt;
+    r.approx_kl = df_value(a.sum_kl) / cnt;
     r.max_abs_dlogp = a.count > 0 ? a.best : 0.0f;
     r.p50_abs_dlogp = r.p90_abs_dlogp = r.p99_abs_dlogp = __int_as_float(0x7fc00000);
     r.clipfrac = static_cast<float>(static_cast<double>(s_clip[0]) / cnt);

@@ -79,11 +79,18 @@ struct BwdLayout {
     }
 };
 
+// A sum carried as an unevaluated pair of floats (hi + lo, about 48 significant
+// bits), added with Knuth's two-sum: the audit's cross-block accumulation.  The
+// fp64 units of this GPU are few and slow; pairs of fp32 operations are not.
+struct DFloat {
+    float hi, lo;
+};
+
 struct AuditPartial {
     int64_t count;
     int64_t arg;
-    double sum_d;
-    double sum_kl;
+    DFloat sum_d;
+    DFloat sum_kl;
     float best;
     uint32_t flags;
 };
