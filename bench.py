@@ -199,9 +199,10 @@ def run_ours(args, world, rank, local):
     scale = 1.0 / n_act                         # token mean over the batch's active tokens
     n_chunks = -(-v // 32768)
     # forward: row compaction (3, the step passes a mask) + GEMM + merge; loss 2; audit 2;
-    # backward: target sort (2), then per vocab chunk the three GEMM roles and the sort of
-    # the chunk's dominant non-target classes (2)
-    launches_per_step = 5 + 2 + 2 + 2 + 5 * n_chunks
+    # backward: row compaction (3) and the zeroing of inactive dh rows (1), target sort (2),
+    # then per vocab chunk the three GEMM roles and the sort of the chunk's dominant
+    # non-target classes (2)
+    launches_per_step = 5 + 2 + 2 + 4 + 2 + 5 * n_chunks
 
     def step(ev=None, ins=None):
         h_t, y_t, m_t, old_t, adv_t = ins if ins is not None else (hid, y, mask, old, advd)

@@ -349,14 +349,33 @@ static rlk_status_t bwd_impl(const void* hidden, const void* weight, const int64
     float* dh_acc = reinterpret_cast<float*>(ws + lay.dhacc_off);
     int* sorted_y = reinterpret_cast<int*>(ws + lay.sorted_y_off);
     int* sorted_t = reinterpret_cast<int*>(ws + lay.sorted_t_off);
+    const int n = static_cast<int>(N), h = static_cast<int>(H), v = static_cast<int>(V);
+
+    // A masked batch runs its GEMMs over the active rows only (gathered in ascending
+    // token order, as in the forward); the rows of dh of the inactive tokens are
+    // zeroed here, since no GEMM visits them.
+    int* rows = nullptr;
+    int* n_rows = nullptr;
+    const void* gemm_rows = hidden;
+    if (active_mask != nullptr) {
+        rows = reinterpret_cast<int*>(ws + lay.rows_off);
+        n_rows = reinterpret_cast<int*>(ws + lay.count_off);
+        void* hc = ws + lay.hc_off;
+        RLK_CUDA(rlk::launch_compact(active_mask, n, h, hidden, hc,
+                                     reinterpret_cast<int*>(ws + lay.blk_off), rows,
+                                     reinterpret_cast<int*>(ws + lay.pos_off), n_rows, stream));
+        RLK_CUDA(rlk::launch_zero_inactive_rows(
+            active_mask, n, static_cast<size_t>(H) * (dh_partial != nullptr ? 4 : 2), dh_out,
+            stream));
+        gemm_rows = hc;
+    }
 
     rlk::BwdStepMaps maps;
-    RLK_TRY(make_map(&maps.h_kmajor, hidden, H, N, H * 2, 64, rlk::kTileM));
+    RLK_TRY(make_map(&maps.h_kmajor, gemm_rows, H, N, H * 2, 64, rlk::kTileM));
     RLK_TRY(make_map(&maps.w_kmajor, weight, H, V, H * 2, 64, rlk::kTileV));
     RLK_TRY(make_map(&maps.w_mnmajor, weight, H, V, H * 2, 64, 64));
-    RLK_TRY(make_map(&maps.h_mnmajor, hidden, H, N, H * 2, 64, 64));
+    RLK_TRY(make_map(&maps.h_mnmajor, gemm_rows, H, N, H * 2, 64, 64));
 
-    const int n = static_cast<int>(N), h = static_cast<int>(H), v = static_cast<int>(V);
     const int v_global = static_cast<int>(vocab_size);
     int* dom = reinterpret_cast<int*>(ws + lay.dom_off);
     uint64_t* tiles = reinterpret_cast<uint64_t*>(ws + lay.tiles_off);
@@ -381,7 +400,10 @@ static rlk_status_t bwd_impl(const void* hidden, const void* weight, const int64
     st.y_off = vocab_start;
     st.V_global = v_global;
     st.round_last = dh_partial == nullptr;
-    st.dh_acc = dh_partial != nullptr ? dh_partial : dh_acc;
+    st.dh_acc = dh_acc;
+    st.dh_out32 = dh_partial;
+    st.rows = rows;
+    st.n_rows = n_rows;
     st.sorted_y = sorted_y;
     st.sorted_t = sorted_t;
     st.ycoef = reinterpret_cast<float*>(ws + lay.ycoef_off);

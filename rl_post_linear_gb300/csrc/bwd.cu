@@ -26,6 +26,10 @@
 //   DhPolicy  dS_c W_c (K = chunk)  -> dh_acc [N, H] fp32 (+= previous chunks;
 //             the last chunk adds the target term and rounds to bf16)
 //   DwPolicy  dS_c^T h (K = N)      -> dW rows of chunk c, plus target terms
+// A masked batch is first compacted to its active rows (ascending token order,
+// the forward's gather): h, dS and dh_acc rows are then compacted rows, the K
+// loop of dW runs over ceil(N_active / 64) blocks, and each dh row is written at
+// its token; the inactive tokens' dh rows are zeroed apart.
 // one persistent launch per role and chunk, in that order (measured faster
 // than putting roles of neighbouring chunks side by side in one launch: alone,
 // each role keeps its L2 working set).
@@ -64,6 +68,18 @@ __device__ __forceinline__ bool row_live(const int64_t* targets, const uint8_t* 
     return y >= 0 && y < V;
 }
 
+// Rows of a masked batch compacted to its active tokens (ascending): GEMM row i
+// is token rows[i] for i < *n_rows.  Both nullptr: rows are tokens.
+struct RowMap {
+    const int* rows;
+    const int* n_rows;
+    __device__ int count(int N) const { return n_rows != nullptr ? *n_rows : N; }
+    // at least one tile: with no active row, the dS GEMM still zeroes the rows that
+    // the dW GEMM's (single) K block reads
+    __device__ int tiles(int N) const { return (max(count(N), 1) + kTileM - 1) / kTileM; }
+    __device__ int token(int i) const { return rows != nullptr ? rows[i] : i; }
+};
+
 __device__ __forceinline__ void bf16x8_to_f32(uint4 v, float* out) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -93,15 +109,16 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
     float* dcoef;         // [N]: that class's fp32 gradient coefficient, -g/T
     int64_t y_off;        // global id of this weight block's first row (0 unsharded)
     int V_global;         // vocabulary size (target validity)
+    RowMap rm;            // compaction of a masked batch (dS rows are compacted rows)
     int N, V, c0, num_m, num_n, kblocks;   // V: rows of this weight block
     float k, temp;
 
-    __device__ int num_units() const { return num_m * num_n; }
+    __device__ int num_units() const { return rm.tiles(N) * num_n; }
     __device__ int k_blocks(int) const { return kblocks; }
     __device__ int tiles_in_unit(int) const { return 1; }
-    // unit -> (token tile m, vocab tile n of the chunk), token tiles grouped
+    // unit -> (row tile m, vocab tile n of the chunk), row tiles grouped
     __device__ void unit(int u, int& m, int& n) const {
-        grouped_unit(u, num_m, num_n, kRasterTokenTiles, m, n);
+        grouped_unit(u, rm.tiles(N), num_n, kRasterTokenTiles, m, n);
     }
     __device__ void coords(int u, int, int& a_mn, int& a_k, int& b_mn, int& b_k) const {
         int m, n;
@@ -117,13 +134,16 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
         float coef_y;         // ENT: the target entry's coefficient without the -g/T part
         float gt;             // g / T
         int64_t ycol;         // target column relative to the chunk
+        int t;                // the row's token
         bool live;
     };
 
     __device__ void epi_begin(int u, int row, EpiState& st) const {
         int m, n;
         unit(u, m, n);
-        const int t = m * kTileM + row;
+        const int i = m * kTileM + row;
+        const int t = i < rm.count(N) ? rm.token(i) : N;
+        st.t = t;
         int64_t y;
         st.live = row_live(targets, mask, t, N, V_global, y);
         st.lse2 = st.live ? lse[t] * kLog2e : 0.f;
@@ -145,12 +165,13 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
     __device__ void epi_tile(int u, int, int row, uint32_t taddr, EpiState& st) const {
         int m, n;
         unit(u, m, n);
-        const int t = m * kTileM + row;
+        const int i = m * kTileM + row;          // dS row (compacted row)
+        const int t = st.t;                      // its token
 #pragma unroll 1
         for (int cc = 0; cc < kTileV / 32; ++cc) {
             uint32_t r[32];
             tmem_load_32(taddr + cc * 32, r);
-            if (t >= N) continue;
+            if (i >= N) continue;
             const int col = n * kTileV + cc * 32;   // column inside the chunk
             const int vb = c0 + col;
             // The target entry: its -g p_y / T part stays out of dS, and the dh / dW
@@ -214,7 +235,7 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
                 d1 = (yi == 2 * j + 1) ? dy : ((ai == 2 * j + 1) ? da : d1);
                 packed[j] = pack_bf16x2(d0, d1);
             }
-            uint4* dst = reinterpret_cast<uint4*>(ds + static_cast<size_t>(t) * kBwdChunk + col);
+            uint4* dst = reinterpret_cast<uint4*>(ds + static_cast<size_t>(i) * kBwdChunk + col);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
@@ -388,13 +409,15 @@ struct DhPolicy : SingleRole<false, true> {
     const float* dcoef;            // [N] its fp32 coefficient
     int64_t y_off;                 // global id of this weight block's first row
     int V_global;                  // vocabulary size (target validity)
+    RowMap rm;                     // compaction of a masked batch (dh_acc rows are compacted)
+    float* dh_out32;               // round_last false: fp32 partial of dh by token [N][H]
     int N, V, H, c0, num_m, num_n, kblocks;
     bool first, last;
-    bool round_last;               // false: the last chunk leaves dh_acc in fp32 (a partial)
+    bool round_last;               // false: the last chunk writes dh_out32, unrounded
     bool terms;                    // false: no fp32 target terms (no targets)
     float temp;
 
-    __device__ int num_units() const { return num_m * num_n; }
+    __device__ int num_units() const { return rm.tiles(N) * num_n; }
     __device__ int k_blocks(int) const { return kblocks; }
     __device__ int tiles_in_unit(int) const { return 1; }
     // unit -> (token tile m, hidden tile n) in row order.  (Grouping 8 hidden tiles
@@ -416,13 +439,16 @@ struct DhPolicy : SingleRole<false, true> {
         float coef, coef_dom;
         int64_t y;                 // target row inside this weight block
         int dom;
+        int t;                     // the row's token (N past the compacted rows)
         bool live, tgt;            // tgt: the row's target term belongs to this block
     };
 
     __device__ void epi_begin(int u, int row, EpiState& st) const {
         int m, n;
         unit(u, m, n);
-        const int t = m * kTileM + row;
+        const int i = m * kTileM + row;
+        const int t = i < rm.count(N) ? rm.token(i) : N;
+        st.t = t;
         // the fp32 terms, added once, in the last chunk's epilogue: (g / T)(1 - p_y) W[y]
         // and, for a dominant non-target class a, dcoef W[a]
         if (terms) {
@@ -444,17 +470,18 @@ struct DhPolicy : SingleRole<false, true> {
     __device__ void epi_tile(int u, int, int row, uint32_t taddr, EpiState& st) const {
         int m, n;
         unit(u, m, n);
-        const int t = m * kTileM + row;
+        const int ri = m * kTileM + row;         // dh_acc row (compacted row)
+        const int t = st.t;                      // its token
 #pragma unroll 1
         for (int cc = 0; cc < kTileV / 32; ++cc) {
             uint32_t r[32];
             tmem_load_32(taddr + cc * 32, r);
             const int col = n * kTileV + cc * 32;
-            if (t >= N || col >= H) continue;
+            if (t >= N || col >= H) continue;    // also the rows past the compacted ones
             float x[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
-            float* acc = dh_acc + static_cast<size_t>(t) * H + col;
+            float* acc = dh_acc + static_cast<size_t>(ri) * H + col;
             if (!first) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -502,10 +529,11 @@ struct DhPolicy : SingleRole<false, true> {
                 for (int j = 0; j < 32; ++j) x[j] = 0.f;
             }
             if (!round_last) {             // a vocab block's fp32 partial of dh
+                float* out = dh_out32 + static_cast<size_t>(t) * H + col;
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    reinterpret_cast<float4*>(acc)[i] =
-                        make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+                for (int q = 0; q < 8; ++q)
+                    reinterpret_cast<float4*>(out)[q] =
+                        make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
                 continue;
             }
             uint4* dst = reinterpret_cast<uint4*>(dh + static_cast<size_t>(t) * H + col);
@@ -535,12 +563,15 @@ struct DwPolicy : SingleRole<true, true> {
     const int* sorted_dy;          // [N] dominant class of this chunk ascending, V elsewhere
     const int* sorted_dt;          // [N]
     const float* dcoef;            // [N] fp32 coefficient of each token's dominant class
+    RowMap rm;                     // compaction: K runs over the compacted rows only
     int N, H, c0, width, num_m, num_n, kblocks;
     float temp;
     bool terms;                    // false: no fp32 target terms (no targets)
 
     __device__ int num_units() const { return num_m * num_n; }
-    __device__ int k_blocks(int) const { return kblocks; }
+    __device__ int k_blocks(int) const {
+        return rm.n_rows != nullptr ? (max(*rm.n_rows, 1) + 63) / 64 : kblocks;
+    }
     __device__ int tiles_in_unit(int) const { return 1; }
     // unit -> (vocab tile m of the chunk, hidden tile n), hidden tiles grouped
     __device__ void unit(int u, int& m, int& n) const {
@@ -800,6 +831,7 @@ static cudaError_t launch_ds(const BwdStepMaps& maps, const BwdStep& st, int c0,
     ps.dcoef = st.dcoef;
     ps.y_off = st.y_off;
     ps.V_global = st.V_global;
+    ps.rm = RowMap{st.rows, st.n_rows};
     ps.N = st.N;
     ps.V = st.V;
     ps.c0 = c0;
@@ -873,6 +905,8 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
         pd.y_off = st.y_off;
         pd.V_global = st.V_global;
         pd.round_last = st.round_last;
+        pd.rm = RowMap{st.rows, st.n_rows};
+        pd.dh_out32 = st.dh_out32;
         pd.N = N;
         pd.V = V;
         pd.H = H;
@@ -897,6 +931,7 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
     pw.sorted_dy = st.sorted_dy;
     pw.sorted_dt = st.sorted_dt;
     pw.dcoef = st.dcoef;
+    pw.rm = RowMap{st.rows, st.n_rows};
     pw.N = N;
     pw.H = H;
     pw.c0 = c0;

@@ -13,7 +13,13 @@
 // before it (ascending block order), places the block's active rows by warp
 // ballots (ascending token order), records rows[pos] = t and pos_of[t] = pos
 // (-1 for inactive rows), and block 0 stores the active count; kernel 3 copies
-// the active rows of h, one warp per row over a grid that covers every row.
+// the active rows of h, one warp per row over a grid that covers every row, and
+// zeroes the rows after them up to the end of the last 128-row tile (at least
+// one tile), so a GEMM that reads a whole tile of the compacted rows (or the
+// backward's K loop over them) never meets stale bytes.
+//
+// In the backward the inactive tokens are never visited by a GEMM, so their
+// rows of dh are zeroed by a fourth kernel.
 #include "rlk_internal.h"
 
 namespace rlk {
@@ -78,18 +84,34 @@ __global__ void __launch_bounds__(kCompactThreads)
 
 constexpr int kGatherWarps = 8;             // rows per block of the copy
 
-// hidden_c[i] = hidden[rows[i]] for i < n_active: one warp per row, 16 bytes
-// per lane and access
+// hidden_c[i] = hidden[rows[i]] for i < n_active, zero for the rows after them
+// up to the end of their last tile: one warp per row, 16 bytes per lane and access
 __global__ void __launch_bounds__(kGatherWarps * 32)
-    compact_gather_kernel(const int* __restrict__ rows, const int* __restrict__ n_active, int H,
-                          const uint4* __restrict__ hidden, uint4* __restrict__ hidden_c) {
+    compact_gather_kernel(const int* __restrict__ rows, const int* __restrict__ n_active, int N,
+                          int H, const uint4* __restrict__ hidden, uint4* __restrict__ hidden_c) {
     const int i = blockIdx.x * kGatherWarps + (threadIdx.x >> 5);
-    if (i >= *n_active) return;
+    const int n = *n_active;
+    const int pad_end = min(N, (max(n, 1) + kTileM - 1) / kTileM * kTileM);
+    if (i >= pad_end) return;
     const int lane = threadIdx.x & 31;
     const int vec_per_row = H / 8;
-    const uint4* src = hidden + static_cast<size_t>(rows[i]) * vec_per_row;
     uint4* dst = hidden_c + static_cast<size_t>(i) * vec_per_row;
-    for (int j = lane; j < vec_per_row; j += 32) dst[j] = src[j];
+    if (i < n) {
+        const uint4* src = hidden + static_cast<size_t>(rows[i]) * vec_per_row;
+        for (int j = lane; j < vec_per_row; j += 32) dst[j] = src[j];
+    } else {
+        for (int j = lane; j < vec_per_row; j += 32) dst[j] = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+// out[t] = 0 for every inactive token t: one warp per row, 16-byte stores
+__global__ void __launch_bounds__(kGatherWarps * 32)
+    zero_inactive_rows_kernel(const uint8_t* __restrict__ mask, int N, int vec_per_row,
+                              uint4* __restrict__ out) {
+    const int t = blockIdx.x * kGatherWarps + (threadIdx.x >> 5);
+    if (t >= N || mask[t] != 0) return;
+    uint4* dst = out + static_cast<size_t>(t) * vec_per_row;
+    for (int j = threadIdx.x & 31; j < vec_per_row; j += 32) dst[j] = make_uint4(0u, 0u, 0u, 0u);
 }
 
 }  // namespace
@@ -106,7 +128,15 @@ cudaError_t launch_compact(const uint8_t* mask, int N, int H, const void* hidden
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     compact_gather_kernel<<<(N + kGatherWarps - 1) / kGatherWarps, kGatherWarps * 32, 0, stream>>>(
-        rows, n_active, H, static_cast<const uint4*>(hidden), static_cast<uint4*>(hidden_c));
+        rows, n_active, N, H, static_cast<const uint4*>(hidden), static_cast<uint4*>(hidden_c));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_zero_inactive_rows(const uint8_t* mask, int N, size_t row_bytes, void* out,
+                                      cudaStream_t stream) {
+    zero_inactive_rows_kernel<<<(N + kGatherWarps - 1) / kGatherWarps, kGatherWarps * 32, 0,
+                                stream>>>(mask, N, static_cast<int>(row_bytes / 16),
+                                          static_cast<uint4*>(out));
     return cudaGetLastError();
 }
 

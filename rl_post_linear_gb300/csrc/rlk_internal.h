@@ -62,7 +62,8 @@ struct FwdLayout {
 constexpr int kTargetSortTile = 2048;
 struct BwdLayout {
     size_t ds_off, dhacc_off, sorted_y_off, sorted_t_off, ycoef_off, dom_off, dcoef_off,
-        sorted_dy_off, sorted_dt_off, tiles_off, total;
+        sorted_dy_off, sorted_dt_off, tiles_off, blk_off, rows_off, pos_off, count_off, hc_off,
+        total;
     BwdLayout(int64_t N, int64_t H) {
         ds_off = 0;
         dhacc_off = align_up(static_cast<size_t>(N) * kBwdChunk * 2, 256);
@@ -75,7 +76,14 @@ struct BwdLayout {
         sorted_dt_off = align_up(sorted_dy_off + static_cast<size_t>(N) * 4, 256);
         tiles_off = align_up(sorted_dt_off + static_cast<size_t>(N) * 4, 256);
         const size_t tiles = static_cast<size_t>((N + kTargetSortTile - 1) / kTargetSortTile);
-        total = align_up(tiles_off + tiles * kTargetSortTile * 8, 256);
+        // compaction of a masked batch, as in the forward
+        blk_off = align_up(tiles_off + tiles * kTargetSortTile * 8, 256);
+        rows_off = align_up(blk_off + static_cast<size_t>((N + kCompactBlock - 1) / kCompactBlock) * 4,
+                            256);
+        pos_off = align_up(rows_off + static_cast<size_t>(N) * 4, 256);
+        count_off = align_up(pos_off + static_cast<size_t>(N) * 4, 256);
+        hc_off = align_up(count_off + 4, 256);
+        total = align_up(hc_off + static_cast<size_t>(N) * H * 2, 256);
     }
 };
 
@@ -150,6 +158,9 @@ cudaError_t launch_fwd(const CUtensorMap& map_h, const CUtensorMap& map_w,
 cudaError_t launch_compact(const uint8_t* mask, int N, int H, const void* hidden, void* hidden_c,
                            int* blk_count, int* rows, int* pos_of, int* n_active,
                            cudaStream_t stream);
+// zeroes the rows (row_bytes each, a multiple of 16) of the tokens with mask 0
+cudaError_t launch_zero_inactive_rows(const uint8_t* mask, int N, size_t row_bytes, void* out,
+                                      cudaStream_t stream);
 
 cudaError_t launch_fwd_partials(const CUtensorMap& map_h, const CUtensorMap& map_w,
                                 const int64_t* targets, const uint8_t* mask, int N, int H,
@@ -193,7 +204,10 @@ struct BwdStep {
     float k, temp;
     int64_t y_off;             // global id of the weight block's first row (0 unsharded)
     int V_global;              // vocabulary size
-    bool round_last;           // false: dh_acc is the caller's fp32 partial, left unrounded
+    bool round_last;           // false: the fp32 partial of dh goes to dh_out32, unrounded
+    float* dh_out32;           // [N][H] by token (round_last false)
+    const int* rows;           // compaction of a masked batch: row -> token, or nullptr
+    const int* n_rows;         // number of compacted rows (device), or nullptr
     // KL against a reference head (kl = true): dS from both heads, no fp32 target terms
     bool kl;
     int H_ref;

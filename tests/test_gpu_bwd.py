@@ -111,3 +111,59 @@ def test_target_terms_across_sort_tiles():
     perm = torch.from_numpy(np.random.default_rng(1).permutation(n))
     dhp, _, _, _ = _gpu(hidden[perm], weight, targets[perm], mask[perm], grad[perm.numpy()], 0.9)
     assert same_bits(dhp, dh[perm])
+
+
+def _bwd_raw(hidden, weight, targets, mask, grad, T, fill=0xFF):
+    """The C-ABI backward with outputs and workspace pre-filled with NaN bytes, so that
+    a row or tile nobody writes (or a stale workspace row that gets read) shows."""
+    d = dev()
+    h, w, y = hidden.to(d), weight.to(d), targets.to(d)
+    m = None if mask is None else mask.to(d)
+    err = torch.zeros(1, dtype=torch.int32, device=d)
+    _, lse = rlk.linear_logp_fwd(h, w, y, m, T, err)
+    g = torch.tensor(grad, dtype=torch.float32, device=d)
+    n, hd = hidden.shape
+    dh = torch.empty_like(h).view(torch.uint8).fill_(fill).view(torch.bfloat16)
+    dw = torch.empty_like(w).view(torch.uint8).fill_(fill).view(torch.bfloat16)
+    ws = torch.full((rlk.rlk_linear_logp_bwd_workspace_bytes(n, hd, w.shape[0]),), fill,
+                    dtype=torch.uint8, device=d)
+    rlk.rlk_linear_logp_bwd(h, w, y, m, g, lse, T, dh, dw, ws, err)
+    torch.cuda.synchronize()
+    return dh.cpu(), dw.cpu(), int(err.item())
+
+
+@pytest.mark.parametrize("n,active", [(700, 0.3), (333, 0.9), (2100, 0.05)])
+def test_masked_batch_equals_its_packed_active_rows(n, active):
+    # The backward runs its GEMMs over the active rows only, gathered in ascending token
+    # order: a masked batch gives, bit for bit, the dh rows and the dW of the batch made
+    # of its active rows alone, and zero dh rows for the rest.
+    h, v = 128, 40000                      # two vocabulary chunks, a ragged one last
+    hidden, weight, targets, mask, grad = _case(n, h, v, 31 + n, std=0.1, active=active)
+    dh, dw, err = _bwd_raw(hidden, weight, targets, mask, grad, 0.8)
+    assert err == 0
+    act = torch.from_numpy(np.nonzero(mask.numpy())[0])
+    dhp, dwp, errp = _bwd_raw(hidden[act], weight, targets[act], None, grad[act.numpy()], 0.8)
+    assert errp == 0
+    assert same_bits(dh[act], dhp)
+    assert same_bits(dw, dwp)
+    assert torch.all(dh[mask == 0].float() == 0)
+    dh_o, dw_o = _oracle(hidden, weight, targets, mask, grad, 0.8)
+    assert rel_l2(dh, dh_o) <= GRAD_REL_L2 and rel_l2(dw, dw_o) <= GRAD_REL_L2
+
+
+def test_all_masked_batch_gives_zero_gradients():
+    n, h, v = 300, 128, 5000
+    hidden, weight, targets, mask, grad = _case(n, h, v, 41)
+    mask.zero_()
+    grad[:] = 0.0
+    dh, dw, err = _bwd_raw(hidden, weight, targets, mask, grad, 1.0)
+    assert err == 0
+    assert torch.all(dh.float() == 0) and torch.all(dw.float() == 0)
+    # one active row
+    mask[177] = 1
+    grad[177] = 0.5
+    dh, dw, err = _bwd_raw(hidden, weight, targets, mask, grad, 1.0)
+    assert err == 0
+    assert torch.all(dh[mask == 0].float() == 0)
+    dh_o, dw_o = _oracle(hidden, weight, targets, mask, grad, 1.0)
+    assert rel_l2(dh, dh_o) <= GRAD_REL_L2 and rel_l2(dw, dw_o) <= GRAD_REL_L2
