@@ -358,7 +358,8 @@ def run_ours(args, world, rank, local):
     if not args.no_second_shape:
         del hid, wt, dh, dw, ws_b
         torch.cuda.empty_cache()
-        out["deepseek_fwd"] = measure_deepseek_fwd(rlk, dev, peak, args.warmup, args.steps)
+        out["deepseek_fwd"], out["deepseek_bwd"] = measure_deepseek(rlk, dev, peak, args.warmup,
+                                                                    args.steps)
     if not args.no_cpu_baseline and world == 1:
         out["cpu_baseline"] = cpu_baseline(w, noise, adv, args.cpu_tokens)
     return out
@@ -505,10 +506,11 @@ def measure_next_rows(rlk, dev, pk, warmup, steps, state):
     return res
 
 
-def measure_deepseek_fwd(rlk, dev, peak, warmup, steps):
-    """The second workload of the pages' shapes: the DeepSeek-style LM head forward
-    (N = 16384, H = 7168, V = 129280, 20% of tokens masked, T = 1); W (1.85 GB) exceeds L2.
-    TFLOP/s counts the active tokens' work, 2 N_a H V."""
+def measure_deepseek(rlk, dev, peak, warmup, steps):
+    """The second workload of the pages' shapes: the DeepSeek-style LM head forward and
+    backward (N = 16384, H = 7168, V = 129280, 20% of tokens masked, T = 1); W (1.85 GB)
+    exceeds L2.  TFLOP/s counts the active tokens' work, 2 N_a H V forward and 4 N_a H V
+    backward (upstream gradient N(0, 1) / N_a on the active tokens)."""
     w = wl.deepseek_fwd(0)
     hid, wt = w.hidden.to(dev), w.weight.to(dev)
     y, mask = w.targets.to(dev), w.mask.to(dev)
@@ -528,10 +530,33 @@ def measure_deepseek_fwd(rlk, dev, peak, warmup, steps):
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
     act = 2.0 * w.n_active * w.h * w.v / (ms * 1e-3) / 1e12
-    return {"workload": w.name, "n_active": w.n_active, "ms": ms,
-            "tokens_per_s": w.n_active / (ms * 1e-3), "tflops_active": act,
-            "frac_of_peak_active": act / peak,
-            "note": "masked rows are compacted away before the GEMM (ceil(N_a/128) row tiles)"}
+    fwd = {"workload": w.name, "n_active": w.n_active, "ms": ms,
+           "tokens_per_s": w.n_active / (ms * 1e-3), "tflops_active": act,
+           "frac_of_peak_active": act / peak,
+           "note": "masked rows are compacted away before the GEMM (ceil(N_a/128) row tiles)"}
+
+    g_host = np.random.default_rng(5).standard_normal(w.n).astype(np.float32) / w.n_active
+    g_host[w.mask.numpy() == 0] = 0.0
+    g = torch.from_numpy(g_host).to(dev)
+    dh, dw = torch.empty_like(hid), torch.empty_like(wt)
+    del ws
+    ws_b = torch.empty(rlk.rlk_linear_logp_bwd_workspace_bytes(w.n, w.h, w.v), dtype=torch.uint8,
+                       device=dev)
+    for _ in range(warmup):
+        rlk.rlk_linear_logp_bwd(hid, wt, y, mask, g, lse, w.temperature, dh, dw, ws_b)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(steps):
+        rlk.rlk_linear_logp_bwd(hid, wt, y, mask, g, lse, w.temperature, dh, dw, ws_b)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms_b = a.elapsed_time(b) / steps
+    act_b = 4.0 * w.n_active * w.h * w.v / (ms_b * 1e-3) / 1e12
+    bwd = {"workload": w.name.replace("fwd", "bwd"), "n_active": w.n_active, "ms": ms_b,
+           "tokens_per_s": w.n_active / (ms_b * 1e-3), "tflops_active": act_b,
+           "frac_of_peak_active": act_b / peak,
+           "note": "masked rows are compacted away before the three GEMMs of each chunk"}
+    return fwd, bwd
 
 
 def measure_audit(rlk, dev, n, hbm_gbs, reps=10):

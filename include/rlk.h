@@ -149,8 +149,10 @@ rlk_status_t rlk_linear_logp_fwd(const void* hidden, const void* weight,
  *   dhidden    [N,H] bf16 out (0 on inactive rows)
  *   dweight    [V,H] bf16 out, overwritten
  * Accumulation is fp32; dhidden and dweight are rounded to bf16 once (RNE).
- * Inactive rows add nothing to dweight, but their hidden rows must hold
- * finite values (a NaN there would reach dweight through 0 * NaN).
+ * With an active_mask the GEMMs run over the active rows only (gathered in
+ * ascending token order into the workspace): the hidden rows of inactive
+ * tokens are never read (NaN padding is harmless), and the result is bit for
+ * bit that of the batch made of the active rows alone.
  */
 rlk_status_t rlk_linear_logp_bwd(const void* hidden, const void* weight,
                                  const int64_t* targets, const uint8_t* active_mask,
@@ -249,7 +251,11 @@ rlk_status_t rlk_linear_kl_fwd(const void* hidden, const void* weight, const voi
  * for bit).  lse, lse_ref and kl are rlk_linear_kl_fwd's outputs; grad_kl or
  * grad_kl_rev may be NULL (not both; kl is needed only with grad_kl).
  * Outputs dhidden [N,H] and dweight [V,H] bf16 (overwritten); inactive rows
- * get dhidden = 0.  workspace: rlk_linear_kl_bwd_workspace_bytes(N, H, V).
+ * get dhidden = 0.  Unlike rlk_linear_logp_bwd this backward does not compact
+ * a masked batch: the GEMMs run over all N rows, so the hidden rows of
+ * inactive tokens (both heads) must hold finite values (a NaN there would
+ * reach dweight through 0 * NaN).
+ * workspace: rlk_linear_kl_bwd_workspace_bytes(N, H, V).
  */
 size_t rlk_linear_kl_bwd_workspace_bytes(int64_t N, int64_t H, int64_t V);
 rlk_status_t rlk_linear_kl_bwd(const void* hidden, const void* weight, const void* hidden_ref,

@@ -149,6 +149,11 @@ def test_masked_batch_equals_its_packed_active_rows(n, active):
     assert torch.all(dh[mask == 0].float() == 0)
     dh_o, dw_o = _oracle(hidden, weight, targets, mask, grad, 0.8)
     assert rel_l2(dh, dh_o) <= GRAD_REL_L2 and rel_l2(dw, dw_o) <= GRAD_REL_L2
+    # the inactive rows are never read: NaN padding changes nothing
+    nan_pad = hidden.clone()
+    nan_pad[mask == 0] = float("nan")
+    dhn, dwn, errn = _bwd_raw(nan_pad, weight, targets, mask, grad, 0.8)
+    assert errn == 0 and same_bits(dhn, dh) and same_bits(dwn, dw)
 
 
 def test_all_masked_batch_gives_zero_gradients():
