@@ -625,7 +625,7 @@ rlk_status_t rlk_dlogp_audit_ext(const float* logp_new, const float* logp_old,
     RLK_CUDA(rlk::launch_audit_ext(logp_new, logp_old, active_mask, N, seq_offsets,
                                    seq_offsets == nullptr ? 0 : num_seqs,
                                    static_cast<float>(clip_eps), result_dev, workspace, vec_ok,
-                                   stream));
+                                   dev.sms, stream));
     return RLK_OK;
 }
 

@@ -24,6 +24,7 @@
 // kl(d) for |d| < 1/2 is the Taylor series d^2 (1/2 + d/6 + d^2/24 + ...)
 // through the d^9 term (truncation below 3e-9 relative); elsewhere it is
 // expm1f(d) - d, where no cancellation arises.
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -367,6 +368,7 @@ struct SelectState {
 };
 
 constexpr int kHistBins = 2048;
+constexpr int kHistBlocksPerSm = 8;
 
 template <bool VEC>
 __global__ void __launch_bounds__(kAuditThreads)
@@ -586,9 +588,12 @@ __global__ void __launch_bounds__(kMergeThreads)
 // single histogram; lanes of a warp that hit the same bin add their count with
 // one shared-memory atomic (|d| concentrates in few bins).  Passes 1 and 2
 // count, per percentile, the keys whose higher digits match its prefix.
+// Blocks stride over the 4096-key slices (a grid of a few blocks per SM), so
+// a block adds its shared histogram into the global one once for many slices;
+// the counts are integers, so the totals do not depend on the grid.
 template <int PASS>
 __global__ void __launch_bounds__(kAuditThreads)
-    audit_ext_hist(const uint32_t* __restrict__ keys, int64_t N,
+    audit_ext_hist(const uint32_t* __restrict__ keys, int64_t N, int64_t num_slices,
                    const SelectState* __restrict__ sel, uint32_t* __restrict__ hist) {
     constexpr int kShift = PASS == 0 ? 21 : (PASS == 1 ? 10 : 0);
     constexpr uint32_t kDigitMask = PASS == 2 ? 0x3ffu : 0x7ffu;
@@ -604,9 +609,11 @@ __global__ void __launch_bounds__(kAuditThreads)
         want[q] = sel->rank[q] > 0;
     }
     __syncthreads();
-    if (PASS > 0 || want[0] || want[1] || want[2]) {
+    for (int64_t slice = blockIdx.x; slice < num_slices && (PASS > 0 || want[0] || want[1] ||
+                                                            want[2]);
+         slice += gridDim.x) {
         constexpr int kBlock = kAuditThreads * kAuditV3PerThread;
-        const int64_t base = static_cast<int64_t>(blockIdx.x) * kBlock;
+        const int64_t base = slice * kBlock;
         const int lane = threadIdx.x & 31;
         constexpr int kVec = kAuditV3PerThread / 4;
         uint32_t k[kVec][4];
@@ -657,35 +664,69 @@ __global__ void __launch_bounds__(kAuditThreads)
 
 // Picks, for each percentile, the bin holding its rank; extends the prefix by
 // that digit and clears the histogram for the next pass.  After the last pass
-// the prefix is the selected key, written to the result.
+// the prefix is the selected key, written to the result.  Each of the 256
+// threads owns a run of consecutive bins; an exclusive scan of the runs' counts
+// (integers, so exact) tells the one thread whose run holds the rank, and that
+// thread walks its own run.
+constexpr int kSelectThreads = 256;
+
 template <int PASS>
-__global__ void audit_ext_select(SelectState* __restrict__ sel, uint32_t* __restrict__ hist,
-                                 rlk_audit_ext_t* __restrict__ result) {
+__global__ void __launch_bounds__(kSelectThreads)
+    audit_ext_select(SelectState* __restrict__ sel, uint32_t* __restrict__ hist,
+                     rlk_audit_ext_t* __restrict__ result) {
     constexpr int kBits = PASS == 2 ? 10 : 11;
-    const int q = threadIdx.x;
-    if (q < 3 && sel->rank[q] > 0) {
-        const int64_t rank = sel->rank[q];
-        const uint32_t* hq = hist + (PASS == 0 ? 0 : q * kHistBins);   // pass 0: one shared histogram
-        int64_t cum = 0;
-        uint32_t bin = 0;
-        for (int b = 0; b < (1 << kBits); ++b) {
-            if (cum + hq[b] >= rank) {
-                bin = b;
-                break;
+    constexpr int kRun = (1 << kBits) / kSelectThreads;     // 8 bins (4 in the last pass)
+    __shared__ int64_t warp_sum[kSelectThreads / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int q = 0; q < 3; ++q) {
+        const int64_t rank = sel->rank[q];           // the same for every thread
+        if (rank <= 0) continue;
+        const uint32_t* hq = hist + (PASS == 0 ? 0 : q * kHistBins) + threadIdx.x * kRun;
+        uint32_t c[kRun];
+        int64_t run = 0;
+#pragma unroll
+        for (int j = 0; j < kRun; ++j) {
+            c[j] = hq[j];
+            run += c[j];
+        }
+        // inclusive scan over the block: lanes, then warps in order
+        int64_t incl = run;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int64_t o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        if (lane == 31) warp_sum[warp] = incl;
+        __syncthreads();
+        int64_t before = 0;
+        for (int w = 0; w < warp; ++w) before += warp_sum[w];
+        const int64_t excl = before + incl - run;
+        if (excl < rank && rank <= excl + run) {
+            int64_t cum = excl;                      // count below the selected bin
+            int bin = -1;
+#pragma unroll
+            for (int j = 0; j < kRun; ++j) {
+                if (bin < 0) {
+                    if (rank <= cum + c[j])
+                        bin = j;
+                    else
+                        cum += c[j];
+                }
             }
-            cum += hq[b];
+            const uint32_t digit = static_cast<uint32_t>(threadIdx.x * kRun + bin);
+            sel->rank[q] = rank - cum;
+            sel->prefix[q] = (sel->prefix[q] << kBits) | digit;
+            if (PASS == 2) {
+                const float v = __uint_as_float(sel->prefix[q] - 1u);
+                if (q == 0) result->p50_abs_dlogp = v;
+                if (q == 1) result->p90_abs_dlogp = v;
+                if (q == 2) result->p99_abs_dlogp = v;
+            }
         }
-        sel->rank[q] = rank - cum;
-        sel->prefix[q] = (sel->prefix[q] << kBits) | bin;
-        if (PASS == 2) {
-            const float v = __uint_as_float(sel->prefix[q] - 1u);
-            if (q == 0) result->p50_abs_dlogp = v;
-            if (q == 1) result->p90_abs_dlogp = v;
-            if (q == 2) result->p99_abs_dlogp = v;
-        }
+        __syncthreads();                             // warp_sum is reused for the next q
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < 3 * kHistBins; i += blockDim.x) hist[i] = 0u;
+    for (int i = threadIdx.x; i < 3 * kHistBins; i += kSelectThreads) hist[i] = 0u;
 }
 
 }  // namespace
@@ -761,7 +802,7 @@ size_t audit_ext_workspace(int64_t N) {
 
 cudaError_t launch_audit_ext(const float* logp_new, const float* logp_old, const uint8_t* mask,
                              int64_t N, const int64_t* seq_offsets, int64_t num_seqs, float eps,
-                             rlk_audit_ext_t* result, void* workspace, bool vec_ok,
+                             rlk_audit_ext_t* result, void* workspace, bool vec_ok, int sms,
                              cudaStream_t stream) {
     const size_t blocks = audit_v3_blocks(N);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -770,6 +811,10 @@ cudaError_t launch_audit_ext(const float* logp_new, const float* logp_old, const
     SelectState* sel = reinterpret_cast<SelectState*>(hist + 3 * kHistBins);
     uint32_t* keys = reinterpret_cast<uint32_t*>(ws + ext_keys_off(N));
     const unsigned grid = static_cast<unsigned>(blocks);
+    // the histogram passes: a few resident blocks per SM striding over the slices
+    const unsigned hgrid =
+        static_cast<unsigned>(std::min<size_t>(blocks, static_cast<size_t>(sms) * kHistBlocksPerSm));
+    const int64_t slices = static_cast<int64_t>(blocks);
     if (blocks > 0) {
         if (vec_ok)
             audit_ext_pass1<true><<<grid, kAuditThreads, 0, stream>>>(logp_new, logp_old, mask, N,
@@ -781,12 +826,12 @@ cudaError_t launch_audit_ext(const float* logp_new, const float* logp_old, const
     audit_ext_merge<<<1, kMergeThreads, 0, stream>>>(parts, static_cast<int64_t>(blocks),
                                                      seq_offsets, num_seqs, result, sel, hist);
     if (blocks > 0) {
-        audit_ext_hist<0><<<grid, kAuditThreads, 0, stream>>>(keys, N, sel, hist);
-        audit_ext_select<0><<<1, 32, 0, stream>>>(sel, hist, result);
-        audit_ext_hist<1><<<grid, kAuditThreads, 0, stream>>>(keys, N, sel, hist);
-        audit_ext_select<1><<<1, 32, 0, stream>>>(sel, hist, result);
-        audit_ext_hist<2><<<grid, kAuditThreads, 0, stream>>>(keys, N, sel, hist);
-        audit_ext_select<2><<<1, 32, 0, stream>>>(sel, hist, result);
+        audit_ext_hist<0><<<hgrid, kAuditThreads, 0, stream>>>(keys, N, slices, sel, hist);
+        audit_ext_select<0><<<1, kSelectThreads, 0, stream>>>(sel, hist, result);
+        audit_ext_hist<1><<<hgrid, kAuditThreads, 0, stream>>>(keys, N, slices, sel, hist);
+        audit_ext_select<1><<<1, kSelectThreads, 0, stream>>>(sel, hist, result);
+        audit_ext_hist<2><<<hgrid, kAuditThreads, 0, stream>>>(keys, N, slices, sel, hist);
+        audit_ext_select<2><<<1, kSelectThreads, 0, stream>>>(sel, hist, result);
     }
     return cudaGetLastError();
 }

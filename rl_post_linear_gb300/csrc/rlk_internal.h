@@ -256,7 +256,7 @@ cudaError_t launch_logp_from_logits(const void* logits, bool bf16, int64_t strid
 size_t audit_ext_workspace(int64_t N);
 cudaError_t launch_audit_ext(const float* logp_new, const float* logp_old, const uint8_t* mask,
                              int64_t N, const int64_t* seq_offsets, int64_t num_seqs, float eps,
-                             rlk_audit_ext_t* result, void* workspace, bool vec_ok,
+                             rlk_audit_ext_t* result, void* workspace, bool vec_ok, int sms,
                              cudaStream_t stream);
 
 // Device address (current device) of the library-owned audit scratch.
