@@ -590,7 +590,19 @@ __global__ void __launch_bounds__(kMergeThreads)
 // count, per percentile, the keys whose higher digits match its prefix.
 // Blocks stride over the 4096-key slices (a grid of a few blocks per SM), so
 // a block adds its shared histogram into the global one once for many slices;
-// the counts are integers, so the totals do not depend on the grid.
+// the counts are integers, so the totals do not depend on the grid.  Pass 0
+// gives each warp its own copy of the histogram (the few hot bins would
+// otherwise serialise the warps' atomics) and sums the copies at the end.
+template <int PASS>
+__host__ __device__ constexpr int hist_copies() {
+    return PASS == 0 ? kAuditThreads / 32 : 3;
+}
+
+template <int PASS>
+__host__ __device__ constexpr size_t hist_smem_bytes() {
+    return static_cast<size_t>(hist_copies<PASS>()) * kHistBins * 4;
+}
+
 template <int PASS>
 __global__ void __launch_bounds__(kAuditThreads)
     audit_ext_hist(const uint32_t* __restrict__ keys, int64_t N, int64_t num_slices,
@@ -599,8 +611,10 @@ __global__ void __launch_bounds__(kAuditThreads)
     constexpr uint32_t kDigitMask = PASS == 2 ? 0x3ffu : 0x7ffu;
     constexpr int kPrefixShift = PASS == 1 ? 21 : 10;
     constexpr int kHists = PASS == 0 ? 1 : 3;
-    __shared__ uint32_t h[kHists * kHistBins];
-    for (int i = threadIdx.x; i < kHists * kHistBins; i += kAuditThreads) h[i] = 0u;
+    constexpr int kCopies = hist_copies<PASS>();
+    extern __shared__ uint32_t h[];                 // [kCopies][kHistBins]
+    for (int i = threadIdx.x; i < kCopies * kHistBins; i += kAuditThreads) h[i] = 0u;
+    uint32_t* hw = h + (PASS == 0 ? (threadIdx.x >> 5) * kHistBins : 0);   // this warp's copy
     uint32_t pre[3];
     bool want[3];
 #pragma unroll
@@ -644,7 +658,7 @@ __global__ void __launch_bounds__(kAuditThreads)
                     const unsigned valid = __ballot_sync(0xffffffffu, key != 0u);
                     if (key != 0u) {
                         const unsigned peers = __match_any_sync(valid, digit);
-                        if (lane == __ffs(peers) - 1) atomicAdd(&h[digit], __popc(peers));
+                        if (lane == __ffs(peers) - 1) atomicAdd(&hw[digit], __popc(peers));
                     }
                 } else {
 #pragma unroll
@@ -657,7 +671,11 @@ __global__ void __launch_bounds__(kAuditThreads)
     }
     __syncthreads();
     for (int i = threadIdx.x; i < kHists * kHistBins; i += kAuditThreads) {
-        const uint32_t c = h[i];
+        uint32_t c = h[i];
+        if constexpr (PASS == 0) {
+#pragma unroll
+            for (int w = 1; w < kCopies; ++w) c += h[w * kHistBins + i];
+        }
         if (c != 0u) atomicAdd(&hist[i], c);
     }
 }
@@ -811,10 +829,20 @@ cudaError_t launch_audit_ext(const float* logp_new, const float* logp_old, const
     SelectState* sel = reinterpret_cast<SelectState*>(hist + 3 * kHistBins);
     uint32_t* keys = reinterpret_cast<uint32_t*>(ws + ext_keys_off(N));
     const unsigned grid = static_cast<unsigned>(blocks);
-    // the histogram passes: a few resident blocks per SM striding over the slices
+    // the histogram passes: as many blocks as fit on the SMs, striding over the slices
+    const size_t smem0 = hist_smem_bytes<0>(), smem12 = hist_smem_bytes<1>();
+    const size_t per_sm0 = std::min<size_t>(kHistBlocksPerSm, (200u << 10) / smem0);
+    const unsigned hgrid0 =
+        static_cast<unsigned>(std::min<size_t>(blocks, static_cast<size_t>(sms) * per_sm0));
     const unsigned hgrid =
         static_cast<unsigned>(std::min<size_t>(blocks, static_cast<size_t>(sms) * kHistBlocksPerSm));
     const int64_t slices = static_cast<int64_t>(blocks);
+    if (blocks > 0) {
+        cudaError_t e = cudaFuncSetAttribute(audit_ext_hist<0>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem0));
+        if (e != cudaSuccess) return e;
+    }
     if (blocks > 0) {
         if (vec_ok)
             audit_ext_pass1<true><<<grid, kAuditThreads, 0, stream>>>(logp_new, logp_old, mask, N,
@@ -826,11 +854,11 @@ cudaError_t launch_audit_ext(const float* logp_new, const float* logp_old, const
     audit_ext_merge<<<1, kMergeThreads, 0, stream>>>(parts, static_cast<int64_t>(blocks),
                                                      seq_offsets, num_seqs, result, sel, hist);
     if (blocks > 0) {
-        audit_ext_hist<0><<<hgrid, kAuditThreads, 0, stream>>>(keys, N, slices, sel, hist);
+        audit_ext_hist<0><<<hgrid0, kAuditThreads, smem0, stream>>>(keys, N, slices, sel, hist);
         audit_ext_select<0><<<1, kSelectThreads, 0, stream>>>(sel, hist, result);
-        audit_ext_hist<1><<<hgrid, kAuditThreads, 0, stream>>>(keys, N, slices, sel, hist);
+        audit_ext_hist<1><<<hgrid, kAuditThreads, smem12, stream>>>(keys, N, slices, sel, hist);
         audit_ext_select<1><<<1, kSelectThreads, 0, stream>>>(sel, hist, result);
-        audit_ext_hist<2><<<hgrid, kAuditThreads, 0, stream>>>(keys, N, slices, sel, hist);
+        audit_ext_hist<2><<<hgrid, kAuditThreads, smem12, stream>>>(keys, N, slices, sel, hist);
         audit_ext_select<2><<<1, kSelectThreads, 0, stream>>>(sel, hist, result);
     }
     return cudaGetLastError();
