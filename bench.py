@@ -491,8 +491,8 @@ def measure_next_rows(rlk, dev, pk, warmup, steps, state):
     res["audit_ext_2p26"] = {"ms": ms, "gbs": na * 9 / (ms * 1e-3) / 1e9,
                              "frac_of_hbm": na * 9 / (ms * 1e-3) / 1e9 / hbm,
                              "bytes": na * 9,
-                             "note": "algorithmic 9 B/token; the exact percentiles re-read the "
-                                     "inputs in three radix-select passes"}
+                             "note": "algorithmic 9 B/token; the exact percentiles read the "
+                                     "4-byte |d| keys again in three radix-select passes"}
     adv = torch.randn(na, device=dev, generator=gen)
     grad = torch.empty(na, dtype=torch.float32, device=dev)
     r_loss = torch.empty(rlk.GRPO_RESULT_BYTES, dtype=torch.uint8, device=dev)
@@ -591,8 +591,21 @@ def measure_audit(rlk, dev, n, hbm_gbs, reps=10):
                    else "inputs larger than L2, no flush")}
 
 
+def measure_audit_ext(rlk, dev, n, hbm_gbs, warmup=3, steps=10):
+    """The extended audit (exact percentiles, ratio0, clipfrac0) alone at N tokens, inputs
+    resident, calls back to back."""
+    new, old, m = (t.to(dev) for t in wl.audit_inputs(n, 0))
+    r_ext = torch.empty(rlk.AUDIT_EXT_RESULT_BYTES, dtype=torch.uint8, device=dev)
+    ws_e = torch.empty(rlk.rlk_dlogp_audit_ext_workspace_bytes(n), dtype=torch.uint8, device=dev)
+    ms = _time_calls(lambda: rlk.rlk_dlogp_audit_ext(new, old, m, None, GRPO_EPS, r_ext, ws_e),
+                     warmup, steps, torch.cuda.current_stream())
+    gbs = n * 9 / (ms * 1e-3) / 1e9
+    return {"ms": ms, "gbs": gbs, "frac_of_hbm": gbs / hbm_gbs, "bytes": n * 9}
+
+
 def run_audit_only():
-    """The audit rows of the workload table alone (for profiling the audit kernels)."""
+    """The audit rows of the workload table alone (for profiling the audit kernels): the
+    base audit, then the extended audit, at N = 9,400,614 and 2^26."""
     import rl_post_linear_gb300 as rlk
     from rl_post_linear_gb300 import build as rlk_build
     rlk_build.build()
@@ -600,8 +613,10 @@ def run_audit_only():
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     pk = peaks()
-    return {"audit_hbm": {str(na): measure_audit(rlk, dev, na, pk["hbm_gbs"])
-                          for na in (9_400_614, 1 << 26)}}
+    sizes = (9_400_614, 1 << 26)
+    out = {"audit_hbm": {str(na): measure_audit(rlk, dev, na, pk["hbm_gbs"]) for na in sizes}}
+    out["audit_ext"] = {str(na): measure_audit_ext(rlk, dev, na, pk["hbm_gbs"]) for na in sizes}
+    return out
 
 
 def recorded_traffic(kernel, n, v, h):

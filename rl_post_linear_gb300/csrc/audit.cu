@@ -311,6 +311,18 @@ __global__ void __launch_bounds__(kAuditThreads)
 }
 
 constexpr int kMergeThreads = 1024;
+constexpr int kMergeBatch = 4;   // partials a merge thread loads before it folds them
+
+__device__ __forceinline__ Acc to_acc(const AuditPartial& p) {
+    Acc b;
+    b.count = p.count;
+    b.arg = p.arg;
+    b.sum_d = p.sum_d;
+    b.sum_kl = p.sum_kl;
+    b.best = p.best;
+    b.flags = p.flags;
+    return b;
+}
 
 __global__ void __launch_bounds__(kMergeThreads)
     audit_pass2(const AuditPartial* __restrict__ parts, int64_t num_parts,
@@ -319,17 +331,17 @@ __global__ void __launch_bounds__(kMergeThreads)
     // pass 1 has finished and its partials are visible
     asm volatile("griddepcontrol.wait;" ::: "memory");
     Acc a = empty_acc();
-    for (int64_t i = threadIdx.x; i < num_parts; i += kMergeThreads) {
-        const AuditPartial p = parts[i];
-        Acc b;
-        b.count = p.count;
-        b.arg = p.arg;
-        b.sum_d = p.sum_d;
-        b.sum_kl = p.sum_kl;
-        b.best = p.best;
-        b.flags = p.flags;
-        merge(a, b);
+    // thread t folds partials t, t + 1024, t + 2048, ... in ascending order; they are
+    // loaded kMergeBatch at a time so that the loads overlap (the order is unchanged)
+    int64_t i = threadIdx.x;
+    for (; i + (kMergeBatch - 1) * kMergeThreads < num_parts; i += kMergeBatch * kMergeThreads) {
+        AuditPartial p[kMergeBatch];
+#pragma unroll
+        for (int j = 0; j < kMergeBatch; ++j) p[j] = parts[i + j * kMergeThreads];
+#pragma unroll
+        for (int j = 0; j < kMergeBatch; ++j) merge(a, to_acc(p[j]));
     }
+    for (; i < num_parts; i += kMergeThreads) merge(a, to_acc(parts[i]));
     a = block_reduce<kMergeThreads>(a);
     if (threadIdx.x == 0) {
         rlk_audit_result_t r;
@@ -357,9 +369,23 @@ __global__ void __launch_bounds__(kMergeThreads)
 
 struct ExtPartial {
     AuditPartial base;
-    double sum_abs, sum_ratio;
+    DFloat sum_abs, sum_ratio;
     int64_t clip;
 };
+
+// One active element of the extended pass: the base audit's terms, its |d| key,
+// and the sums of |d|, of the ratio exp(d) and the count of clipped ratios.
+__device__ __forceinline__ uint32_t visit_ext(float nv, float ov, int off, float eps,
+                                              ThreadAcc& a, float& sabs, float& sratio,
+                                              int& clip) {
+    visit3(nv, ov, 1u, off, a);
+    const float d = nv - ov;
+    const float r = expf(d);
+    sabs += fabsf(d);
+    sratio += r;
+    clip += fabsf(r - 1.0f) > eps ? 1 : 0;
+    return abs_key(d);
+}
 
 struct SelectState {
     uint32_t prefix[3];
@@ -380,51 +406,44 @@ __global__ void __launch_bounds__(kAuditThreads)
     ThreadAcc a;
     float sabs = 0.f, sratio = 0.f;
     int clip = 0;
-#pragma unroll 1
-    for (int j = 0; j < kAuditV3PerThread / 4; ++j) {
-        const int o0 = j * (kAuditThreads * 4) + threadIdx.x * 4;
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
-        uint32_t m = 0x01010101u;
-        const bool full = VEC && base + o0 + 4 <= N;
-        if (full) {
-            x = __ldcs(reinterpret_cast<const float4*>(nw + base + o0));
-            y = __ldcs(reinterpret_cast<const float4*>(od + base + o0));
-            if (mask != nullptr)
-                m = __ldcs(reinterpret_cast<const unsigned int*>(mask + base + o0));
-        }
-        const float xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
-        uint32_t k4[4] = {0u, 0u, 0u, 0u};
+    constexpr int kVec = kAuditV3PerThread / 4;
+    if (VEC && base + kBlock <= N) {
+        // every load first (4 float4 of each input, 4 mask words), then the elements
+        float4 x[kVec], y[kVec];
+        uint32_t m[kVec];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int64_t i = base + o0 + e;
-            float nv, ov;
-            uint32_t mv;
-            if (full) {
-                nv = xs[e];
-                ov = ys[e];
-                mv = (m >> (8 * e)) & 0xffu;
-            } else {
-                if (i >= N) continue;
-                nv = nw[i];
-                ov = od[i];
-                mv = mask == nullptr ? 1u : mask[i];
-            }
-            if (mv == 0) continue;
-            visit3(nv, ov, 1u, o0 + e, a);
-            const float d = nv - ov;
-            k4[e] = abs_key(d);
-            const float r = expf(d);
-            sabs += fabsf(d);
-            sratio += r;
-            clip += fabsf(r - 1.0f) > eps ? 1 : 0;
+        for (int j = 0; j < kVec; ++j) {
+            const int64_t i0 = base + j * (kAuditThreads * 4) + threadIdx.x * 4;
+            x[j] = __ldcs(reinterpret_cast<const float4*>(nw + i0));
+            y[j] = __ldcs(reinterpret_cast<const float4*>(od + i0));
+            m[j] = mask == nullptr ? 0x01010101u
+                                   : __ldcs(reinterpret_cast<const unsigned int*>(mask + i0));
         }
-        // |d| keys for the percentile passes (0 for inactive tokens)
-        if (full) {
-            *reinterpret_cast<uint4*>(keys + base + o0) = make_uint4(k4[0], k4[1], k4[2], k4[3]);
-        } else {
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+            const int o0 = j * (kAuditThreads * 4) + threadIdx.x * 4;
+            const float xs[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
+            const float ys[4] = {y[j].x, y[j].y, y[j].z, y[j].w};
+            uint32_t k4[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-                if (base + o0 + e < N) keys[base + o0 + e] = k4[e];
+                k4[e] = ((m[j] >> (8 * e)) & 0xffu) != 0u
+                            ? visit_ext(xs[e], ys[e], o0 + e, eps, a, sabs, sratio, clip)
+                            : 0u;
+            // |d| keys for the percentile passes (0 for inactive tokens)
+            *reinterpret_cast<uint4*>(keys + base + o0) = make_uint4(k4[0], k4[1], k4[2], k4[3]);
+        }
+    } else {
+#pragma unroll 1
+        for (int j = 0; j < kVec; ++j) {
+            const int o0 = j * (kAuditThreads * 4) + threadIdx.x * 4;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int64_t i = base + o0 + e;
+                if (i >= N) continue;
+                const bool act = mask == nullptr || mask[i] != 0;
+                keys[i] = act ? visit_ext(nw[i], od[i], o0 + e, eps, a, sabs, sratio, clip) : 0u;
+            }
         }
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -453,7 +472,7 @@ __global__ void __launch_bounds__(kAuditThreads)
         }
     }
     __shared__ Acc warp_acc[kAuditThreads / 32];
-    __shared__ double warp_abs[kAuditThreads / 32], warp_ratio[kAuditThreads / 32];
+    __shared__ float warp_abs[kAuditThreads / 32], warp_ratio[kAuditThreads / 32];
     __shared__ int warp_clip[kAuditThreads / 32];
     if (lane == 0) {
         Acc w;
@@ -464,20 +483,20 @@ __global__ void __launch_bounds__(kAuditThreads)
         w.best = a.key == 0 ? -1.0f : __uint_as_float(a.key - 1u);
         w.flags = a.flags;
         warp_acc[warp] = w;
-        warp_abs[warp] = static_cast<double>(sabs);
-        warp_ratio[warp] = static_cast<double>(sratio);
+        warp_abs[warp] = sabs;
+        warp_ratio[warp] = sratio;
         warp_clip[warp] = clip;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
         Acc t = warp_acc[0];
-        double sa = warp_abs[0], sr = warp_ratio[0];
+        DFloat sa{warp_abs[0], 0.f}, sr{warp_ratio[0], 0.f};
         int64_t cl = warp_clip[0];
 #pragma unroll
         for (int w = 1; w < kAuditThreads / 32; ++w) {
             merge(t, warp_acc[w]);
-            sa += warp_abs[w];
-            sr += warp_ratio[w];
+            sa = df_add(sa, DFloat{warp_abs[w], 0.f});
+            sr = df_add(sr, DFloat{warp_ratio[w], 0.f});
             cl += warp_clip[w];
         }
         ExtPartial p;
@@ -502,36 +521,41 @@ __global__ void __launch_bounds__(kMergeThreads)
                     rlk_audit_ext_t* __restrict__ result, SelectState* __restrict__ sel,
                     uint32_t* __restrict__ hist) {
     Acc a = empty_acc();
-    double sa = 0.0, sr = 0.0;
+    DFloat sa{0.f, 0.f}, sr{0.f, 0.f};
     int64_t cl = 0;
-    for (int64_t i = threadIdx.x; i < num_parts; i += kMergeThreads) {
-        const ExtPartial p = parts[i];
-        Acc b;
-        b.count = p.base.count;
-        b.arg = p.base.arg;
-        b.sum_d = p.base.sum_d;
-        b.sum_kl = p.base.sum_kl;
-        b.best = p.base.best;
-        b.flags = p.base.flags;
-        merge(a, b);
-        sa += p.sum_abs;
-        sr += p.sum_ratio;
+    // ascending partials per thread, loaded in batches (as in the base audit's merge)
+    auto fold = [&](const ExtPartial& p) {
+        merge(a, to_acc(p.base));
+        sa = df_add(sa, p.sum_abs);
+        sr = df_add(sr, p.sum_ratio);
         cl += p.clip;
+    };
+    int64_t i = threadIdx.x;
+    for (; i + (kMergeBatch - 1) * kMergeThreads < num_parts; i += kMergeBatch * kMergeThreads) {
+        ExtPartial p[kMergeBatch];
+#pragma unroll
+        for (int j = 0; j < kMergeBatch; ++j) p[j] = parts[i + j * kMergeThreads];
+#pragma unroll
+        for (int j = 0; j < kMergeBatch; ++j) fold(p[j]);
     }
+    for (; i < num_parts; i += kMergeThreads) fold(parts[i]);
     for (int i = threadIdx.x; i < 3 * kHistBins; i += kMergeThreads) hist[i] = 0u;
     a = block_reduce<kMergeThreads>(a);
-    __shared__ double s_abs[kMergeThreads / 32], s_ratio[kMergeThreads / 32];
+    __shared__ DFloat s_abs[kMergeThreads / 32], s_ratio[kMergeThreads / 32];
     __shared__ long long s_clip[kMergeThreads / 32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     // the same fixed tree for the three extra sums
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-        const double x = __shfl_down_sync(0xffffffffu, sa, off);
-        const double y = __shfl_down_sync(0xffffffffu, sr, off);
+        DFloat x, y;
+        x.hi = __shfl_down_sync(0xffffffffu, sa.hi, off);
+        x.lo = __shfl_down_sync(0xffffffffu, sa.lo, off);
+        y.hi = __shfl_down_sync(0xffffffffu, sr.hi, off);
+        y.lo = __shfl_down_sync(0xffffffffu, sr.lo, off);
         const long long z = __shfl_down_sync(0xffffffffu, static_cast<long long>(cl), off);
         if (lane + off < 32) {
-            sa += x;
-            sr += y;
+            sa = df_add(sa, x);
+            sr = df_add(sr, y);
             cl += z;
         }
     }
@@ -543,8 +567,8 @@ __global__ void __launch_bounds__(kMergeThreads)
     __syncthreads();
     if (threadIdx.x != 0) return;
     for (int w = 1; w < kMergeThreads / 32; ++w) {
-        s_abs[0] += s_abs[w];
-        s_ratio[0] += s_ratio[w];
+        s_abs[0] = df_add(s_abs[0], s_abs[w]);
+        s_ratio[0] = df_add(s_ratio[0], s_ratio[w]);
         s_clip[0] += s_clip[w];
     }
     rlk_audit_ext_t r;
@@ -566,8 +590,8 @@ __global__ void __launch_bounds__(kMergeThreads)
     r.clip_count = s_clip[0];
     const double cnt = static_cast<double>(a.count);
     r.mean_dlogp = df_value(a.sum_d) / cnt;
-    r.mean_abs_dlogp = s_abs[0] / cnt;
-    r.mean_ratio = s_ratio[0] / cnt;
+    r.mean_abs_dlogp = df_value(s_abs[0]) / cnt;
+    r.mean_ratio = df_value(s_ratio[0]) / cnt;
     r.approx_kl = df_value(a.sum_kl) / cnt;
     r.max_abs_dlogp = a.count > 0 ? a.best : 0.0f;
     r.p50_abs_dlogp = r.p90_abs_dlogp = r.p99_abs_dlogp = __int_as_float(0x7fc00000);

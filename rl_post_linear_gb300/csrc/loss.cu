@@ -157,7 +157,18 @@ __global__ void __launch_bounds__(kLossMergeThreads)
                rlk_grpo_result_t* __restrict__ result) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     LossAcc a{0, 0, 0, 0.0, 0.0};
-    for (int64_t i = threadIdx.x; i < num_parts; i += kLossMergeThreads) {
+    // thread t adds partials t, t + T, t + 2T, ... in ascending order, loading four at a
+    // time so that the loads overlap (the order of the additions is unchanged)
+    int64_t i = threadIdx.x;
+    for (; i + 3 * kLossMergeThreads < num_parts; i += 4 * kLossMergeThreads) {
+        LossPartial p[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) p[j] = parts[i + j * kLossMergeThreads];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            add(a, LossAcc{p[j].count, p[j].clipped, p[j].outside, p[j].sum_term, p[j].sum_r});
+    }
+    for (; i < num_parts; i += kLossMergeThreads) {
         const LossPartial p = parts[i];
         add(a, LossAcc{p.count, p.clipped, p.outside, p.sum_term, p.sum_r});
     }
