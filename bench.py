@@ -454,8 +454,11 @@ def measure_next_rows(rlk, dev, pk, warmup, steps, state):
                                                      kl_r, lse_p, lse_q, None, ws_kl),
                        warmup, steps, stream)
     g_kl = torch.randn(n, device=dev, generator=gen) / n
+    del ws_kl
+    ws_klb = torch.empty(rlk.rlk_linear_kl_bwd_workspace_bytes(n, h, v), dtype=torch.uint8,
+                         device=dev)
     ms_b = _time_calls(lambda: rlk.rlk_linear_kl_bwd(hid, wt, hid_r, wt_r, mask, g_kl, g_kl,
-                                                     lse_p, lse_q, kl, T, T, dh, dw, ws_b),
+                                                     lse_p, lse_q, kl, T, T, dh, dw, ws_klb),
                        warmup, steps, stream)
     kl_fwd_flops = 2.0 * n_act * v * (h + h)
     res["kl_fwd"] = {"ms": ms_f, "tflops": kl_fwd_flops / (ms_f * 1e-3) / 1e12,
@@ -465,7 +468,7 @@ def measure_next_rows(rlk, dev, pk, warmup, steps, state):
     res["kl_bwd"] = {"ms": ms_b, "tflops": bwd_flops / (ms_b * 1e-3) / 1e12,
                      "frac_of_peak": bwd_flops / (ms_b * 1e-3) / 1e12 / peak,
                      "executed_tflops": (bwd_flops + kl_fwd_flops) / (ms_b * 1e-3) / 1e12}
-    del hid_r, wt_r, ws_kl
+    del hid_r, wt_r, ws_klb
     torch.cuda.empty_cache()
 
     # NEXT-4: logp from existing logits, dense rows; bytes = the logits + targets, mask, out

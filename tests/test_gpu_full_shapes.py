@@ -11,6 +11,9 @@ benchmark times.
   column sum must vanish up to the bf16 output rounding).
 * DeepSeek-shaped forward (N = 16384, H = 7168, V = 129280, 20% masked):
   128 sampled tokens.
+* DeepSeek-shaped backward (the same masked batch, compacted to its active
+  rows): 16 sampled active dh rows against the oracle, exact zeros on the
+  inactive rows, and the column sums of dW.
 * Audit at N = 2^26.
 """
 import numpy as np
@@ -163,6 +166,40 @@ def test_deepseek_forward_sampled():
     assert dl.max() <= LOGP_ATOL
     inactive = w.mask.numpy() == 0
     assert np.all(logp.cpu().numpy()[inactive] == 0.0)
+
+
+def test_deepseek_backward_sampled():
+    w = wl.deepseek_fwd(0)
+    d = dev()
+    err = torch.zeros(1, dtype=torch.int32, device=d)
+    hd, wd, yd, md = w.hidden.to(d), w.weight.to(d), w.targets.to(d), w.mask.to(d)
+    act = w.mask.numpy() > 0
+    g = np.random.default_rng(5).standard_normal(w.n) / w.n_active
+    g[~act] = 0.0
+    gd = torch.tensor(g, dtype=torch.float32, device=d)
+    _, lse = rlk.linear_logp_fwd(hd, wd, yd, md, w.temperature, err)
+    dh, dw = rlk.linear_logp_bwd(hd, wd, yd, md, gd, lse, w.temperature, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    rows = _sample_rows(w, 24, 4)
+    rows = rows[act[rows]][:16]
+    w64 = f64(w.weight)
+    h64 = f64(w.hidden[rows])
+    _, lse_o = oracle.linear_logp_fwd_parallel(h64, w64, w.targets[rows].numpy(), None,
+                                               w.temperature)
+    g32 = gd.cpu().double().numpy()
+    dh_o = oracle.linear_logp_bwd_dh_parallel(h64, w64, w.targets[rows].numpy(), None,
+                                              g32[rows], lse_o, w.temperature)
+    dh_c = dh.cpu()
+    e = rel_l2(dh_c[rows], dh_o)
+    assert torch.all(dh_c[torch.from_numpy(~act)].float() == 0)
+    col = dw.double().sum(dim=0)
+    rms = dw.double().pow(2).sum(dim=0).sqrt()
+    worst = float((col.abs() / rms).max())
+    print("deepseek bwd: %d sampled dh rows rel-L2 %.3e; max |col sum| / col norm %.3e"
+          % (len(rows), e, worst))
+    assert e <= GRAD_REL_L2
+    assert worst <= 8 * 2.0 ** -8
 
 
 def test_audit_two_to_the_26():
