@@ -175,7 +175,12 @@ typedef struct {
  * Masked dlogp audit over active tokens, ascending t:
  *   d_t       = logp_new[t] - logp_old[t]         (exact in double)
  *   count     = #active
- *   max|d|    and the first index attaining it (NaN ranks highest)
+ *   max|d|    and the first index attaining it (NaN ranks highest), ranked on
+ *             the fp32 difference of the two fp32 logps (one IEEE subtraction,
+ *             i.e. d_t rounded once to float): the worst token is an index
+ *             decided by floating point, so it is decided in the precision of
+ *             the logps themselves; two tokens whose exact |d| differ below
+ *             fp32 resolution tie, and the first wins
  *   mean      = sum d / count
  *   approx_kl = sum (exp(d) - 1 - d) / count, evaluated as expm1(d) - d
  */
@@ -187,7 +192,8 @@ void rlk_oracle_dlogp_audit(const float* logp_new, const float* logp_old,
     for (int64_t t = 0; t < n; ++t) {
         if (!row_active(mask, t)) continue;
         double d = (double)logp_new[t] - (double)logp_old[t];
-        double a = fabs(d);
+        const float d32 = logp_new[t] - logp_old[t];   /* float operands: an fp32 subtraction */
+        double a = fabs((double)d32);
         if (arg < 0) {
             best = a;
             arg = t;

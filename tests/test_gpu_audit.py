@@ -80,3 +80,27 @@ def test_pages_element_count_exact_and_reproducible():
     assert r["active_count"] == int(mask.sum())
     r2, _ = _both(new, old, mask)
     assert r == r2
+
+
+def test_ties_across_the_slices_of_one_block():
+    # Above 608 x 4096 elements a pass-1 block covers several consecutive 4096-element
+    # slices (N = 5,000,000: three per block).  Equal largest |d| in two slices of one block,
+    # in different float4 groups of the same thread, and in the tail block: the lowest index
+    # must win each time.
+    n = 5_000_000
+    new, old, mask = wl.audit_inputs(n, 9)
+    mask[:] = 1
+    blk = 7 * 3 * 4096                       # first element of block 7
+    cases = [
+        (blk + 4096 + 5, blk + 100),         # slice 1 vs an earlier offset in slice 0
+        (blk + 2 * 4096 + 1024 * 3 + 4 * 17, blk + 4 * 17),   # same thread, group 3 vs 0
+        (n - 3, n - 4096 * 2 - 7),           # the tail block
+    ]
+    for later, earlier in cases:
+        nw, od = new.clone(), old.clone()
+        od[later] = od[earlier] = -1.0           # |d| = 0.75 exactly at both
+        nw[later] = -0.25
+        nw[earlier] = -1.75
+        r, o = _both(nw, od, mask)
+        _check(r, o, nw, od, mask)
+        assert r["argmax_index"] == earlier, (later, earlier)

@@ -312,6 +312,16 @@ def test_audit_single_and_ties(oracle_lib):
     # a NaN ranks above every number
     r = _audit(oracle_lib, [0.0, 5.0, float("nan"), float("nan")], [0.0] * 4, None)
     assert r["argmax_index"] == 2 and math.isnan(r["max_abs_dlogp"])
+    # exact |d| that differ below fp32 resolution tie, and the first index wins: the
+    # second token's exact |d| = 1.5 + 2^-24 is the larger, but it rounds (to even) to the
+    # first token's 1.5
+    old = np.array([-3.0, -1.0], np.float32)
+    new = np.array([np.float32(-1.5), np.float32(0.5) + np.float32(2.0 ** -24)], np.float32)
+    d_exact = [Fraction(float(new[i])) - Fraction(float(old[i])) for i in range(2)]
+    d32 = [np.float32(new[i]) - np.float32(old[i]) for i in range(2)]
+    assert d_exact[1] > d_exact[0] and d32[0] == d32[1] == np.float32(1.5)
+    r = _audit(oracle_lib, new, old, None)
+    assert r["argmax_index"] == 0 and r["max_abs_dlogp"] == 1.5
 
 
 def test_audit_exact_rationals(oracle_lib):
@@ -326,9 +336,10 @@ def test_audit_exact_rationals(oracle_lib):
     d = [Fraction(float(new[t])) - Fraction(float(old[t])) for t in act]
     mean = sum(d, Fraction(0)) / len(d)
     assert abs(r["mean_dlogp"] - float(mean)) <= 1e-15 * float(sum(abs(x) for x in d) / len(d))
-    absd = [abs(x) for x in d]
+    # the worst token is ranked on |d| rounded once to fp32 (the fp32 difference of the logps)
+    absd = [float(np.float32(float(abs(x)))) for x in d]
     best = max(absd)
-    assert r["max_abs_dlogp"] == float(best)
+    assert r["max_abs_dlogp"] == best
     assert r["argmax_index"] == int(act[absd.index(best)])
     kl = math.fsum(math.expm1(float(x)) - float(x) for x in d) / len(d)
     assert abs(r["approx_kl"] - kl) < 1e-12 * kl
