@@ -562,8 +562,9 @@ def measure_deepseek(rlk, dev, peak, warmup, steps):
     return fwd, bwd
 
 
-def measure_audit(rlk, dev, n, hbm_gbs, reps=10):
-    """The audit alone at N tokens: 9 algorithmic bytes per token (new, old, mask).  When
+def measure_audit(rlk, dev, n, hbm_gbs, reps=20):
+    """The audit alone at N tokens: 9 algorithmic bytes per token (new, old, mask); the
+    median of `reps` calls, each timed alone (the mean is reported beside it).  When
     the inputs fit in L2, L2 is flushed before every timed launch pair (outside the
     events): a 256 MB write, then a 256 MB read that evicts the dirty lines, so that no
     write-back lands inside the timed region.  Larger inputs need no flush."""
@@ -587,9 +588,10 @@ def measure_audit(rlk, dev, n, hbm_gbs, reps=10):
         b.record(stream)
         torch.cuda.synchronize()
         ms.append(a.elapsed_time(b))
-    t = float(np.mean(ms))
+    t = float(np.median(ms))
     gbs = n * 9 / (t * 1e-3) / 1e9
-    return {"ms": t, "gbs": gbs, "frac_of_hbm": gbs / hbm_gbs, "bytes": n * 9,
+    return {"ms": t, "ms_mean": float(np.mean(ms)), "reps": reps, "gbs": gbs,
+            "frac_of_hbm": gbs / hbm_gbs, "bytes": n * 9,
             "l2": ("flushed (256 MB write + 256 MB read) before each launch pair" if fits
                    else "inputs larger than L2, no flush")}
 

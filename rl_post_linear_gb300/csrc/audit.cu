@@ -5,16 +5,18 @@
 // max_abs_dlogp is the primary metric, reported with the worst token;
 // approx_kl0 = mean(exp(dlogp) - 1 - dlogp); the active-token count.
 //
-// Pass 1: block b owns the fixed slice [b*4096, (b+1)*4096) (a function of N
-// only).  Each thread issues all its loads first (4 float4 of each input and 4
-// mask words, streaming cache hint), then handles its 16 elements without
-// branches: d = new - old in fp32 (a correctly rounded difference), its
-// count, the largest |d| as an order-preserving integer key with the first
-// offset attaining it, and fp32 sums of d and of kl(d) = exp(d) - 1 - d, in
-// four interleaved chains merged in a fixed order.  A fixed shuffle tree
-// combines the 32 lanes (fp32 sums, integer counts), and thread 0 folds the
-// eight warp partials in warp order into float-pair sums (about 48 bits:
-// two-sum; this GPU's fp64 units are few and slow).  Pass 2: one block merges
+// Pass 1: the elements are cut into 4096-element slices, and block b owns a
+// fixed run of consecutive slices (ceil(slices / 608) of them: a function of N
+// only, so that one wave of blocks covers any N).  For each slice a thread
+// issues all its loads first (4 float4 of each input and 4 mask words,
+// streaming cache hint), then handles its 16 elements without branches:
+// d = new - old in fp32 (a correctly rounded difference), its count, the
+// largest |d| as an order-preserving integer key with the first offset
+// attaining it, and fp32 sums of d and of kl(d) = exp(d) - 1 - d, in four
+// interleaved chains merged in a fixed order; each slice's sums are added to
+// the thread's float-pair sums (about 48 bits: two-sum; this GPU's fp64 units
+// are few and slow).  A fixed shuffle tree combines the 32 lanes, and thread 0
+// folds the eight warp partials in warp order.  Pass 2: one block merges
 // the per-block partials,
 // each thread a fixed strided subset in ascending order, then the same
 // fixed tree; it is launched with programmatic dependent launch, so its launch
@@ -205,93 +207,136 @@ __device__ __forceinline__ int active_bytes(uint32_t m) {
     return __popc(hi & 0x80808080u);
 }
 
+// Pass 1's partition is a function of N only: slices of 4096 elements, and
+// blocks of ceil(slices / kAuditMaxBlocks) consecutive slices, so that one wave
+// of blocks covers any N (608 = 4 resident blocks on each of 152 SMs) and pass 2
+// merges at most kAuditMaxBlocks partials.
+constexpr int64_t kAuditMaxBlocks = 608;
+
+inline int64_t audit_slices_per_block(int64_t N) {
+    const int64_t slices = static_cast<int64_t>(audit_v3_blocks(N));
+    return slices <= kAuditMaxBlocks ? 1 : (slices + kAuditMaxBlocks - 1) / kAuditMaxBlocks;
+}
+
+inline int64_t audit_pass1_blocks(int64_t N) {
+    const int64_t slices = static_cast<int64_t>(audit_v3_blocks(N));
+    const int64_t spb = audit_slices_per_block(N);
+    return (slices + spb - 1) / spb;
+}
+
 template <bool VEC>
 __global__ void __launch_bounds__(kAuditThreads)
     audit_pass1(const float* __restrict__ nw, const float* __restrict__ od,
-                const uint8_t* __restrict__ mask, int64_t N, AuditPartial* __restrict__ out) {
+                const uint8_t* __restrict__ mask, int64_t N, int64_t slices_per_block,
+                AuditPartial* __restrict__ out) {
     // let the merge kernel launch now; it waits for this grid before reading
     asm volatile("griddepcontrol.launch_dependents;");
     constexpr int kVec = kAuditV3PerThread / 4;
     constexpr int kBlock = kAuditThreads * kAuditV3PerThread;
-    const int64_t base = static_cast<int64_t>(blockIdx.x) * kBlock;
-    ThreadAcc a;
-    if (VEC && base + kBlock <= N) {
-        float4 x[kVec], y[kVec];
-        uint32_t m[kVec];
-#pragma unroll
-        for (int j = 0; j < kVec; ++j) {
-            const int64_t i0 = base + j * (kAuditThreads * 4) + threadIdx.x * 4;
-            x[j] = __ldcs(reinterpret_cast<const float4*>(nw + i0));
-            y[j] = __ldcs(reinterpret_cast<const float4*>(od + i0));
-            m[j] = mask == nullptr ? 0x01010101u
-                                   : __ldcs(reinterpret_cast<const unsigned int*>(mask + i0));
-        }
-        // One accumulator per float4 group, so that the four groups' dependency chains
-        // (sums, running max) interleave; the groups are then merged in ascending order,
-        // which keeps the first index on ties (group j's offsets precede group j+1's).
-        GroupAcc g[kVec];
-#pragma unroll
-        for (int j = 0; j < kVec; ++j) {
-            const int o = j * (kAuditThreads * 4) + threadIdx.x * 4;
-            a.count += active_bytes(m[j]);
-            visit_group(x[j].x, y[j].x, (m[j] & 0xffu) != 0, o, g[j]);
-            visit_group(x[j].y, y[j].y, (m[j] & 0xff00u) != 0, o + 1, g[j]);
-            visit_group(x[j].z, y[j].z, (m[j] & 0xff0000u) != 0, o + 2, g[j]);
-            visit_group(x[j].w, y[j].w, (m[j] & 0xff000000u) != 0, o + 3, g[j]);
-        }
-#pragma unroll
-        for (int j = 0; j < kVec; ++j) {
-            const bool better = g[j].key > a.key;
-            a.key = better ? g[j].key : a.key;
-            a.arg = better ? g[j].arg : a.arg;
-        }
-        // an inf or NaN |d| exists exactly when the largest key is above the key of the
-        // largest finite float (NaN and inf rank above every finite |d|)
-        a.flags = a.key > 0x7f800000u ? 1u : 0u;
-        static_assert(kVec == 4, "the fixed summation tree below assumes four groups");
-        a.sd = (g[0].sd + g[1].sd) + (g[2].sd + g[3].sd);
-        a.skl = (g[0].skl + g[1].skl) + (g[2].skl + g[3].skl);
-    } else {
+    const int64_t block_base = static_cast<int64_t>(blockIdx.x) * slices_per_block * kBlock;
+    // running state over the block's slices, visited in ascending order: count, the
+    // best key and its offset in the block (strictly greater replaces, so the first
+    // offset wins ties), float-pair sums of each slice's fp32 sums
+    int count = 0;
+    uint32_t best_key = 0;
+    int64_t best_off = -1;
+    uint32_t flags = 0;
+    DFloat sum_d{0.f, 0.f}, sum_kl{0.f, 0.f};
 #pragma unroll 1
-        for (int j = 0; j < kVec; ++j) {
-            const int o0 = j * (kAuditThreads * 4) + threadIdx.x * 4;
+    for (int64_t sl = 0; sl < slices_per_block; ++sl) {
+        const int64_t base = block_base + sl * kBlock;
+        if (base >= N) break;
+        const int64_t slice_off = sl * kBlock;
+        ThreadAcc a;
+        if (VEC && base + kBlock <= N) {
+            float4 x[kVec], y[kVec];
+            uint32_t m[kVec];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int64_t i = base + o0 + e;
-                if (i < N) visit3(nw[i], od[i], mask == nullptr ? 1u : mask[i], o0 + e, a);
+            for (int j = 0; j < kVec; ++j) {
+                const int64_t i0 = base + j * (kAuditThreads * 4) + threadIdx.x * 4;
+                x[j] = __ldcs(reinterpret_cast<const float4*>(nw + i0));
+                y[j] = __ldcs(reinterpret_cast<const float4*>(od + i0));
+                m[j] = mask == nullptr ? 0x01010101u
+                                       : __ldcs(reinterpret_cast<const unsigned int*>(mask + i0));
+            }
+            // One accumulator per float4 group, so that the four groups' dependency chains
+            // (sums, running max) interleave; the groups are then merged in ascending order,
+            // which keeps the first index on ties (group j's offsets precede group j+1's).
+            GroupAcc g[kVec];
+#pragma unroll
+            for (int j = 0; j < kVec; ++j) {
+                const int o = j * (kAuditThreads * 4) + threadIdx.x * 4;
+                a.count += active_bytes(m[j]);
+                visit_group(x[j].x, y[j].x, (m[j] & 0xffu) != 0, o, g[j]);
+                visit_group(x[j].y, y[j].y, (m[j] & 0xff00u) != 0, o + 1, g[j]);
+                visit_group(x[j].z, y[j].z, (m[j] & 0xff0000u) != 0, o + 2, g[j]);
+                visit_group(x[j].w, y[j].w, (m[j] & 0xff000000u) != 0, o + 3, g[j]);
+            }
+#pragma unroll
+            for (int j = 0; j < kVec; ++j) {
+                const bool better = g[j].key > a.key;
+                a.key = better ? g[j].key : a.key;
+                a.arg = better ? g[j].arg : a.arg;
+            }
+            // an inf or NaN |d| exists exactly when the largest key is above the key of the
+            // largest finite float (NaN and inf rank above every finite |d|)
+            a.flags = a.key > 0x7f800000u ? 1u : 0u;
+            static_assert(kVec == 4, "the fixed summation tree below assumes four groups");
+            a.sd = (g[0].sd + g[1].sd) + (g[2].sd + g[3].sd);
+            a.skl = (g[0].skl + g[1].skl) + (g[2].skl + g[3].skl);
+        } else {
+#pragma unroll 1
+            for (int j = 0; j < kVec; ++j) {
+                const int o0 = j * (kAuditThreads * 4) + threadIdx.x * 4;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int64_t i = base + o0 + e;
+                    if (i < N) visit3(nw[i], od[i], mask == nullptr ? 1u : mask[i], o0 + e, a);
+                }
             }
         }
+        count += a.count;
+        if (a.key > best_key) {
+            best_key = a.key;
+            best_off = slice_off + a.arg;
+        }
+        flags |= a.flags;
+        sum_d = df_add(sum_d, DFloat{a.sd, 0.f});
+        sum_kl = df_add(sum_kl, DFloat{a.skl, 0.f});
     }
-    // fixed tree over the warp (fp32 sums, integer counts, key / offset max)
+    // fixed tree over the warp (float-pair sums, integer counts, key / offset max)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-        const int c = __shfl_down_sync(0xffffffffu, a.count, off);
-        const uint32_t k = __shfl_down_sync(0xffffffffu, a.key, off);
-        const int g = __shfl_down_sync(0xffffffffu, a.arg, off);
-        const float sd = __shfl_down_sync(0xffffffffu, a.sd, off);
-        const float skl = __shfl_down_sync(0xffffffffu, a.skl, off);
-        const uint32_t f = __shfl_down_sync(0xffffffffu, a.flags, off);
+        const int c = __shfl_down_sync(0xffffffffu, count, off);
+        const uint32_t k = __shfl_down_sync(0xffffffffu, best_key, off);
+        const int64_t g = __shfl_down_sync(0xffffffffu, best_off, off);
+        DFloat sd, skl;
+        sd.hi = __shfl_down_sync(0xffffffffu, sum_d.hi, off);
+        sd.lo = __shfl_down_sync(0xffffffffu, sum_d.lo, off);
+        skl.hi = __shfl_down_sync(0xffffffffu, sum_kl.hi, off);
+        skl.lo = __shfl_down_sync(0xffffffffu, sum_kl.lo, off);
+        const uint32_t f = __shfl_down_sync(0xffffffffu, flags, off);
         if (lane + off < 32) {
-            const bool take = k > a.key || (k == a.key && k != 0 && g < a.arg);
-            a.key = take ? k : a.key;
-            a.arg = take ? g : a.arg;
-            a.count += c;
-            a.sd += sd;
-            a.skl += skl;
-            a.flags |= f;
+            const bool take = k > best_key || (k == best_key && k != 0 && g < best_off);
+            best_key = take ? k : best_key;
+            best_off = take ? g : best_off;
+            count += c;
+            sum_d = df_add(sum_d, sd);
+            sum_kl = df_add(sum_kl, skl);
+            flags |= f;
         }
     }
-    // the eight warp partials, in warp order, in float pairs
+    // the eight warp partials, in warp order
     __shared__ Acc warp_acc[kAuditThreads / 32];
     if (lane == 0) {
         Acc w;
-        w.count = a.count;
-        w.arg = a.key == 0 ? INT64_MAX : base + a.arg;
-        w.sum_d = DFloat{a.sd, 0.f};
-        w.sum_kl = DFloat{a.skl, 0.f};
-        w.best = a.key == 0 ? -1.0f : __uint_as_float(a.key - 1u);
-        w.flags = a.flags;
+        w.count = count;
+        w.arg = best_key == 0 ? INT64_MAX : block_base + best_off;
+        w.sum_d = sum_d;
+        w.sum_kl = sum_kl;
+        w.best = best_key == 0 ? -1.0f : __uint_as_float(best_key - 1u);
+        w.flags = flags;
         warp_acc[warp] = w;
     }
     __syncthreads();
@@ -805,15 +850,17 @@ cudaError_t audit_noalloc_scratch(void** out) {
 cudaError_t launch_audit(const float* logp_new, const float* logp_old, const uint8_t* mask,
                          int64_t N, rlk_audit_result_t* result, void* workspace, bool vec_ok,
                          cudaStream_t stream) {
-    const size_t blocks = audit_v3_blocks(N);
+    // at most audit_v3_blocks(N) partials: the workspace is sized for that many
+    const size_t blocks = static_cast<size_t>(audit_pass1_blocks(N));
+    const int64_t spb = audit_slices_per_block(N);
     AuditPartial* parts = static_cast<AuditPartial*>(workspace);
     if (blocks > 0) {
         if (vec_ok)
             audit_pass1<true><<<static_cast<unsigned>(blocks), kAuditThreads, 0, stream>>>(
-                logp_new, logp_old, mask, N, parts);
+                logp_new, logp_old, mask, N, spb, parts);
         else
             audit_pass1<false><<<static_cast<unsigned>(blocks), kAuditThreads, 0, stream>>>(
-                logp_new, logp_old, mask, N, parts);
+                logp_new, logp_old, mask, N, spb, parts);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
