@@ -293,14 +293,17 @@ rlk_status_t rlk_linear_kl_bwd(const void* hidden, const void* weight, const voi
     st.kl_val = kl;
     st.dh_acc = reinterpret_cast<float*>(ws + lay.dhacc_off);
     st.dom = reinterpret_cast<int*>(ws + lay.dom_off);
+    st.dom_flags = reinterpret_cast<int*>(ws + lay.flags_off);
     st.dcoef = reinterpret_cast<float*>(ws + lay.dcoef_off);
     st.sorted_dy = reinterpret_cast<int*>(ws + lay.sorted_dy_off);
     st.sorted_dt = reinterpret_cast<int*>(ws + lay.sorted_dt_off);
     st.tiles = reinterpret_cast<uint64_t*>(ws + lay.tiles_off);
     st.dhidden = dhidden;
     st.dweight = dweight;
-    // no dominant class yet (all bits set: -1)
+    // no dominant class yet (all bits set: -1), and none in any chunk
     RLK_CUDA(cudaMemsetAsync(st.dom, 0xff, static_cast<size_t>(N) * sizeof(int), stream));
+    RLK_CUDA(cudaMemsetAsync(st.dom_flags, 0, static_cast<size_t>(st.num_chunks) * sizeof(int),
+                             stream));
     return bwd_chunks(maps, st, ws + lay.ds_off, N, V, dev.sms, device_error_word, stream);
 }
 
@@ -379,9 +382,11 @@ static rlk_status_t bwd_impl(const void* hidden, const void* weight, const int64
     const int v_global = static_cast<int>(vocab_size);
     int* dom = reinterpret_cast<int*>(ws + lay.dom_off);
     uint64_t* tiles = reinterpret_cast<uint64_t*>(ws + lay.tiles_off);
-    RLK_CUDA(rlk::launch_target_sort(targets, active_mask, n, v, vocab_start, v_global, tiles,
-                                     sorted_y, sorted_t, dom, device_error_word, stream));
     const int num_chunks = static_cast<int>((V + rlk::kBwdChunk - 1) / rlk::kBwdChunk);
+    int* dom_flags = reinterpret_cast<int*>(ws + lay.flags_off);
+    RLK_CUDA(rlk::launch_target_sort(targets, active_mask, n, v, vocab_start, v_global, tiles,
+                                     sorted_y, sorted_t, dom, dom_flags, num_chunks,
+                                     device_error_word, stream));
     rlk::BwdStep st{};
     st.targets = targets;
     st.mask = active_mask;
@@ -408,6 +413,7 @@ static rlk_status_t bwd_impl(const void* hidden, const void* weight, const int64
     st.sorted_t = sorted_t;
     st.ycoef = reinterpret_cast<float*>(ws + lay.ycoef_off);
     st.dom = dom;
+    st.dom_flags = dom_flags;
     st.dcoef = reinterpret_cast<float*>(ws + lay.dcoef_off);
     st.sorted_dy = reinterpret_cast<int*>(ws + lay.sorted_dy_off);
     st.sorted_dt = reinterpret_cast<int*>(ws + lay.sorted_dt_off);

@@ -107,6 +107,7 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
     float* ycoef;         // [N]: 1 - p_y of each live row, written by the tile holding y
     int* dom;             // [N]: the row's dominant non-target class (p > 1/2), else -1
     float* dcoef;         // [N]: that class's fp32 gradient coefficient, -g/T
+    int* dom_flag;        // set to 1 when some row's dominant class lies in this chunk
     int64_t y_off;        // global id of this weight block's first row (0 unsharded)
     int V_global;         // vocabulary size (target validity)
     RowMap rm;            // compaction of a masked batch (dS rows are compacted rows)
@@ -212,6 +213,7 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
                         ai = idx;
                         dom[t] = vb + idx;
                         dcoef[t] = -st.gt;
+                        *dom_flag = 1;
                         da = st.gt * -expm1f(l2 * kLn2);
                         if constexpr (ENT) da = fmaf(fmaf(st.c2, cm, st.coef_y), ex2_approx(l2), da);
                     }
@@ -277,6 +279,7 @@ struct DsKlPolicy {
     __nv_bfloat16* ds;        // [N][kBwdChunk]
     int* dom;                 // [N] dominant policy class or -1
     float* dcoef;             // [N] its fp32 gradient entry
+    int* dom_flag;            // set to 1 when some row's dominant class lies in this chunk
     int N, V, c0, num_m, num_n, kblocks, kblocks_r;
     float k, kr, temp;
 
@@ -381,6 +384,7 @@ struct DsKlPolicy {
             if (ai < 32) {
                 dom[t] = vb + ai;
                 dcoef[t] = gdom;
+                *dom_flag = 1;
             }
             uint4* dst = reinterpret_cast<uint4*>(ds + static_cast<size_t>(t) * kBwdChunk + col);
 #pragma unroll
@@ -562,6 +566,7 @@ struct DwPolicy : SingleRole<true, true> {
     const float* ycoef;            // [N] 1 - p_y, from the dS GEMM
     const int* sorted_dy;          // [N] dominant class of this chunk ascending, V elsewhere
     const int* sorted_dt;          // [N]
+    const int* dom_flag;           // 0: no dominant class in this chunk (the list was not built)
     const float* dcoef;            // [N] fp32 coefficient of each token's dominant class
     RowMap rm;                     // compaction: K runs over the compacted rows only
     int N, H, c0, width, num_m, num_n, kblocks;
@@ -613,7 +618,7 @@ struct DwPolicy : SingleRole<true, true> {
         st.lo = st.hi = st.dlo = st.dhi = 0;
         if (!st.valid) return;
         if (terms) equal_range(sorted_y, N, st.v, st.lo, st.hi);
-        equal_range(sorted_dy, N, st.v, st.dlo, st.dhi);
+        if (*dom_flag != 0) equal_range(sorted_dy, N, st.v, st.dlo, st.dhi);
     }
 
     __device__ void epi_tile(int u, int, int, uint32_t taddr, EpiState& st) const {
@@ -696,13 +701,17 @@ __device__ __forceinline__ void bitonic_sort_tile(uint64_t* key) {
     }
 }
 
-// Keys (target, token) of the dW target terms; also resets dom[] to "no dominant class".
+// Keys (target, token) of the dW target terms; also resets dom[] to "no dominant class"
+// and the chunks' flags to "no dominant class in this chunk".
 __global__ void __launch_bounds__(kSortThreads)
     target_tile_sort_kernel(const int64_t* __restrict__ targets, const uint8_t* __restrict__ mask,
                             int N, int V, int64_t y_off, int V_global,
-                            uint64_t* __restrict__ tiles, int* __restrict__ dom, uint32_t* err) {
+                            uint64_t* __restrict__ tiles, int* __restrict__ dom,
+                            int* __restrict__ dom_flags, int num_chunks, uint32_t* err) {
     __shared__ uint64_t key[kSortTile];
     const int base = blockIdx.x * kSortTile;
+    if (blockIdx.x == 0)
+        for (int c = threadIdx.x; c < num_chunks; c += kSortThreads) dom_flags[c] = 0;
     for (int i = threadIdx.x; i < kSortTile; i += kSortThreads) {
         const int t = base + i;
         uint64_t k = kPadKey;
@@ -728,10 +737,12 @@ __global__ void __launch_bounds__(kSortThreads)
 }
 
 // Keys (dominant class, token) of the tokens whose dominant non-target class lies in
-// [lo, hi) (one vocab chunk); V for every other token.
+// [lo, hi) (one vocab chunk); V for every other token.  Nothing to do when the dS
+// GEMM found no dominant class in the chunk (its flag is 0); dW then reads no list.
 __global__ void __launch_bounds__(kSortThreads)
     dom_tile_sort_kernel(const int* __restrict__ dom, int N, int V, int lo, int hi,
-                         uint64_t* __restrict__ tiles) {
+                         const int* __restrict__ flag, uint64_t* __restrict__ tiles) {
+    if (*flag == 0) return;
     __shared__ uint64_t key[kSortTile];
     const int base = blockIdx.x * kSortTile;
     for (int i = threadIdx.x; i < kSortTile; i += kSortThreads) {
@@ -751,7 +762,9 @@ __global__ void __launch_bounds__(kSortThreads)
 
 __global__ void __launch_bounds__(kPlaceThreads)
     target_place_kernel(const uint64_t* __restrict__ tiles, int num_tiles,
-                        int* __restrict__ sorted_y, int* __restrict__ sorted_t) {
+                        const int* __restrict__ flag, int* __restrict__ sorted_y,
+                        int* __restrict__ sorted_t) {
+    if (flag != nullptr && *flag == 0) return;    // an empty dominant-class list
     const int e = blockIdx.x * kPlaceThreads + threadIdx.x;
     if (e >= num_tiles * kSortTile) return;
     const uint64_t k = tiles[e];
@@ -772,33 +785,35 @@ __global__ void __launch_bounds__(kPlaceThreads)
     sorted_t[rank] = static_cast<int>(k & 0xffffffffu);
 }
 
-static cudaError_t place_sorted(const uint64_t* tiles, int N, int* sorted_key, int* sorted_t,
-                                cudaStream_t stream) {
+static cudaError_t place_sorted(const uint64_t* tiles, int N, const int* flag, int* sorted_key,
+                                int* sorted_t, cudaStream_t stream) {
     const int num_tiles = (N + kSortTile - 1) / kSortTile;
     const int total = num_tiles * kSortTile;
     target_place_kernel<<<(total + kPlaceThreads - 1) / kPlaceThreads, kPlaceThreads, 0, stream>>>(
-        tiles, num_tiles, sorted_key, sorted_t);
+        tiles, num_tiles, flag, sorted_key, sorted_t);
     return cudaGetLastError();
 }
 
 cudaError_t launch_target_sort(const int64_t* targets, const uint8_t* mask, int N, int V,
                                int64_t y_off, int V_global, uint64_t* tiles, int* sorted_y,
-                               int* sorted_t, int* dom, uint32_t* err, cudaStream_t stream) {
+                               int* sorted_t, int* dom, int* dom_flags, int num_chunks,
+                               uint32_t* err, cudaStream_t stream) {
     const int num_tiles = (N + kSortTile - 1) / kSortTile;
-    target_tile_sort_kernel<<<num_tiles, kSortThreads, 0, stream>>>(targets, mask, N, V, y_off,
-                                                                     V_global, tiles, dom, err);
+    target_tile_sort_kernel<<<num_tiles, kSortThreads, 0, stream>>>(
+        targets, mask, N, V, y_off, V_global, tiles, dom, dom_flags, num_chunks, err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return place_sorted(tiles, N, sorted_y, sorted_t, stream);
+    return place_sorted(tiles, N, nullptr, sorted_y, sorted_t, stream);
 }
 
-static cudaError_t launch_dom_sort(const int* dom, int N, int V, int lo, int hi, uint64_t* tiles,
-                                   int* sorted_dy, int* sorted_dt, cudaStream_t stream) {
+static cudaError_t launch_dom_sort(const int* dom, int N, int V, int lo, int hi, const int* flag,
+                                   uint64_t* tiles, int* sorted_dy, int* sorted_dt,
+                                   cudaStream_t stream) {
     const int num_tiles = (N + kSortTile - 1) / kSortTile;
-    dom_tile_sort_kernel<<<num_tiles, kSortThreads, 0, stream>>>(dom, N, V, lo, hi, tiles);
+    dom_tile_sort_kernel<<<num_tiles, kSortThreads, 0, stream>>>(dom, N, V, lo, hi, flag, tiles);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return place_sorted(tiles, N, sorted_dy, sorted_dt, stream);
+    return place_sorted(tiles, N, flag, sorted_dy, sorted_dt, stream);
 }
 
 // ----------------------------------------------------------------------------- launch
@@ -832,6 +847,7 @@ static cudaError_t launch_ds(const BwdStepMaps& maps, const BwdStep& st, int c0,
     ps.y_off = st.y_off;
     ps.V_global = st.V_global;
     ps.rm = RowMap{st.rows, st.n_rows};
+    ps.dom_flag = st.dom_flags + st.chunk;
     ps.N = st.N;
     ps.V = st.V;
     ps.c0 = c0;
@@ -859,6 +875,7 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
         ps.ds = static_cast<__nv_bfloat16*>(st.ds);
         ps.dom = st.dom;
         ps.dcoef = st.dcoef;
+        ps.dom_flag = st.dom_flags + st.chunk;
         ps.N = N;
         ps.V = V;
         ps.c0 = c0;
@@ -879,8 +896,8 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
             DsKlMaps{maps.h_kmajor, maps.w_kmajor, maps.hr_kmajor, maps.wr_kmajor}, ps, err);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        return launch_dom_sort(st.dom, N, V, c0, c0 + width, st.tiles, st.sorted_dy,
-                               st.sorted_dt, stream);
+        return launch_dom_sort(st.dom, N, V, c0, c0 + width, st.dom_flags + st.chunk, st.tiles,
+                               st.sorted_dy, st.sorted_dt, stream);
     }
     if (st.role == kRoleDs) {
         const cudaError_t e =
@@ -888,8 +905,8 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
                                    : launch_ds<false>(maps, st, c0, width, num_sms, err, stream);
         if (e != cudaSuccess) return e;
         // the tokens whose dominant non-target class the dS GEMM found in this chunk
-        return launch_dom_sort(st.dom, N, V, c0, c0 + width, st.tiles, st.sorted_dy,
-                               st.sorted_dt, stream);
+        return launch_dom_sort(st.dom, N, V, c0, c0 + width, st.dom_flags + st.chunk, st.tiles,
+                               st.sorted_dy, st.sorted_dt, stream);
     }
     if (st.role == kRoleDh) {
         DhPolicy pd;
@@ -930,6 +947,7 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
     pw.ycoef = st.ycoef;
     pw.sorted_dy = st.sorted_dy;
     pw.sorted_dt = st.sorted_dt;
+    pw.dom_flag = st.dom_flags + st.chunk;
     pw.dcoef = st.dcoef;
     pw.rm = RowMap{st.rows, st.n_rows};
     pw.N = N;

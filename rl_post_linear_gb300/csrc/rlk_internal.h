@@ -17,6 +17,7 @@ constexpr int kTileV = 256;                 // vocab (or hidden) columns per til
 constexpr int kFwdTilesPerChunk = 4;        // forward vocab chunk = 1024 columns
 constexpr int kFwdChunk = kFwdTilesPerChunk * kTileV;
 constexpr int kBwdChunk = 32768;            // backward vocab chunk (multiple of kTileV)
+constexpr int kMaxBwdChunks = 65536;        // 2^31 / kBwdChunk: chunks of the largest vocabulary
 // Raster groups (visiting order only; no effect on any result): token tiles per
 // group for the forward and dS GEMMs, hidden tiles per group for the dW GEMM.
 // A group's share of h (32 x 128 rows, or 8 x 256 columns, of H = 4096) is
@@ -63,7 +64,7 @@ constexpr int kTargetSortTile = 2048;
 struct BwdLayout {
     size_t ds_off, dhacc_off, sorted_y_off, sorted_t_off, ycoef_off, dom_off, dcoef_off,
         sorted_dy_off, sorted_dt_off, tiles_off, blk_off, rows_off, pos_off, count_off, hc_off,
-        total;
+        flags_off, total;
     BwdLayout(int64_t N, int64_t H) {
         ds_off = 0;
         dhacc_off = align_up(static_cast<size_t>(N) * kBwdChunk * 2, 256);
@@ -83,7 +84,9 @@ struct BwdLayout {
         pos_off = align_up(rows_off + static_cast<size_t>(N) * 4, 256);
         count_off = align_up(pos_off + static_cast<size_t>(N) * 4, 256);
         hc_off = align_up(count_off + 4, 256);
-        total = align_up(hc_off + static_cast<size_t>(N) * H * 2, 256);
+        // one flag per vocab chunk: the chunk holds some token's dominant class
+        flags_off = align_up(hc_off + static_cast<size_t>(N) * H * 2, 256);
+        total = align_up(flags_off + static_cast<size_t>(kMaxBwdChunks) * 4, 256);
     }
 };
 
@@ -221,6 +224,7 @@ struct BwdStep {
     const int* sorted_t;
     float* ycoef;              // [N] 1 - p_y of each live row
     int* dom;                  // [N] dominant non-target class (p > 1/2) or -1
+    int* dom_flags;            // [num_chunks] nonzero: the chunk holds some row's dominant class
     float* dcoef;              // [N] its fp32 gradient coefficient
     int* sorted_dy;            // [N] this chunk's dominant classes, ascending (V: none)
     int* sorted_dt;            // [N]
@@ -231,7 +235,8 @@ struct BwdStep {
 
 cudaError_t launch_target_sort(const int64_t* targets, const uint8_t* mask, int N, int V,
                                int64_t y_off, int V_global, uint64_t* tiles, int* sorted_y,
-                               int* sorted_t, int* dom, uint32_t* err, cudaStream_t stream);
+                               int* sorted_t, int* dom, int* dom_flags, int num_chunks, uint32_t* err,
+                               cudaStream_t stream);
 
 cudaError_t launch_dh_merge(const float* partials, int64_t num_parts, int64_t N, int64_t H,
                             void* dhidden, cudaStream_t stream);

@@ -172,3 +172,56 @@ def test_all_masked_batch_gives_zero_gradients():
     assert torch.all(dh[mask == 0].float() == 0)
     dh_o, dw_o = _oracle(hidden, weight, targets, mask, grad, 1.0)
     assert rel_l2(dh, dh_o) <= GRAD_REL_L2 and rel_l2(dw, dw_o) <= GRAD_REL_L2
+
+
+def _dominant_case(n, h, v, seed, rows_by_chunk):
+    """Random head plus, for the listed rows, one planted class per row in the given chunk
+    whose logit is about 17 (p > 0.9 at T = 1): a dominant non-target class."""
+    hidden, weight, targets, mask, grad = _case(n, h, v, seed, std=0.02, active=1.0)
+    rng = np.random.default_rng(seed + 100)
+    w = weight.float()
+    hf = hidden.float()
+    for chunk, rows in rows_by_chunk.items():
+        lo, hi = chunk * 32768, min(v, (chunk + 1) * 32768)
+        for t in rows:
+            a = int(rng.integers(lo, hi))
+            w[a] += 2.2 * hf[t] / hf[t].norm()
+    return hidden, w.to(torch.bfloat16), targets, mask, grad
+
+
+def test_dominant_classes_in_some_chunks_and_a_reused_workspace():
+    # Three vocabulary chunks: rows 0-39 have a dominant class in chunk 0, rows 40-79 in
+    # chunk 2, none in chunk 1 (whose dominant-class sort is skipped).  Then a head with no
+    # dominant class at all through the same workspace: the lists left by the first call
+    # must not be read.
+    n, h, v, T = 200, 64, 70000, 1.0
+    hidden, weight, targets, mask, grad = _dominant_case(
+        n, h, v, 51, {0: range(0, 40), 2: range(40, 80)})
+    d = dev()
+    ws = torch.empty(rlk.rlk_linear_logp_bwd_workspace_bytes(n, h, v), dtype=torch.uint8,
+                     device=d)
+    err = torch.zeros(1, dtype=torch.int32, device=d)
+
+    def run(hid, wt):
+        hd, wd, yd, md = hid.to(d), wt.to(d), targets.to(d), mask.to(d)
+        _, lse = rlk.linear_logp_fwd(hd, wd, yd, md, T, err)
+        g = torch.tensor(grad, dtype=torch.float32, device=d)
+        dh, dw = torch.empty_like(hd), torch.empty_like(wd)
+        rlk.rlk_linear_logp_bwd(hd, wd, yd, md, g, lse, T, dh, dw, ws, err)
+        torch.cuda.synchronize()
+        return dh.cpu(), dw.cpu(), lse.cpu()
+
+    dh, dw, lse = run(hidden, weight)
+    assert int(err.item()) == 0
+    p_max = float(torch.exp(hidden.float() @ weight.float().t() / T
+                            - lse[:, None]).max(dim=1).values[:80].min())
+    assert p_max > 0.6                                  # the planted classes dominate
+    dh_o, dw_o = _oracle(hidden, weight, targets, mask, grad, T)
+    e_dh, e_dw = rel_l2(dh, dh_o), rel_l2(dw, dw_o)
+    print("dominant classes in chunks 0 and 2: rel-L2 dh %.3e dw %.3e" % (e_dh, e_dw))
+    assert e_dh <= GRAD_REL_L2 and e_dw <= GRAD_REL_L2
+    plain = wl.normal_bf16((v, h), 52, wl.S_WEIGHT, std=0.02)
+    dh2, dw2, _ = run(hidden, plain)
+    assert int(err.item()) == 0
+    dh2_o, dw2_o = _oracle(hidden, plain, targets, mask, grad, T)
+    assert rel_l2(dh2, dh2_o) <= GRAD_REL_L2 and rel_l2(dw2, dw2_o) <= GRAD_REL_L2
