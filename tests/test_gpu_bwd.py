@@ -225,3 +225,33 @@ def test_dominant_classes_in_some_chunks_and_a_reused_workspace():
     assert int(err.item()) == 0
     dh2_o, dw2_o = _oracle(hidden, plain, targets, mask, grad, T)
     assert rel_l2(dh2, dh2_o) <= GRAD_REL_L2 and rel_l2(dw2, dw2_o) <= GRAD_REL_L2
+
+
+def test_single_class_vocabulary_gives_zero_up_to_lse_rounding():
+    # V = 1: p = 1 for every row, so the exact gradient g (delta - p) / T is 0.  The kernels
+    # rebuild log2 p as S k - lse log2(e) from the forward's fp32 lse, which is off by about
+    # one fp32 ulp of lse: the target entry's coefficient (g / T)(1 - p) is then of order
+    # 2^-23 |g| / T instead of 0.  The outputs must stay at that rounding level.
+    T = 0.9
+    for n in (1, 5, 300):
+        hidden, weight, targets, mask, grad = _case(n, 64, 1, 61 + n, std=0.3, active=0.8)
+        dh, dw, err = _bwd_raw(hidden, weight, targets, mask, grad, T)
+        assert err == 0
+        assert torch.all(dh[mask == 0].float() == 0)
+        lse_scale = float((hidden.float() @ weight.float().t()).abs().max()) / T + 1.0
+        g_max = float(np.abs(grad).max()) / T
+        bound_dh = 8 * 2.0 ** -23 * lse_scale * g_max * float(weight.float().abs().max())
+        bound_dw = 8 * 2.0 ** -23 * lse_scale * g_max * float(hidden.float().abs().max()) * n
+        assert float(dh.float().abs().max()) <= bound_dh
+        assert float(dw.float().abs().max()) <= bound_dw
+
+
+@pytest.mark.parametrize("n,h,v", [(1, 64, 3), (40, 64, 2), (3, 192, 7)])
+def test_tiny_vocabulary_and_batch(n, h, v):
+    hidden, weight, targets, mask, grad = _case(n, h, v, 71 + n * v, std=0.2, active=1.0)
+    dh, dw, err = _bwd_raw(hidden, weight, targets, mask, grad, 0.8)
+    assert err == 0
+    dh_o, dw_o = _oracle(hidden, weight, targets, mask, grad, 0.8)
+    e_dh, e_dw = rel_l2(dh, dh_o), rel_l2(dw, dw_o)
+    print("bwd n=%d h=%d v=%d: rel-L2 dh %.3e dw %.3e" % (n, h, v, e_dh, e_dw))
+    assert e_dh <= GRAD_REL_L2 and e_dw <= GRAD_REL_L2
