@@ -660,11 +660,15 @@ const char* rlk_contract_string(void) {
     return "rlk-gb300 linear_logp v1; arch=sm_103a; nvcc=" RLK_STR(__CUDACC_VER_MAJOR__) "." RLK_STR(
         __CUDACC_VER_MINOR__) "; inputs=bf16; accum=fp32 (tcgen05 kind::f16, TMEM); "
                               "tile=128x256x64 cta_group::1, no split-K; "
-                              "fwd_vocab_chunk=1024 (merge ascending); bwd_vocab_chunk=32768; masked batches: active rows compacted (ascending) before the GEMM; "
+                              "fwd_vocab_chunk=1024 (merge ascending); bwd_vocab_chunk=32768; "
+                              "masked batches: active rows compacted (ascending) before the "
+                              "forward and backward GEMMs; "
                               "exp=ex2.approx.ftz, log=lg2.approx.ftz; k=fp32(log2(e)/T); "
-                              "logits never rounded; logp/lse fp32; dS bf16 (target term fp32); "
+                              "logits never rounded; logp/lse fp32; dS bf16 (target and "
+                              "dominant-class terms fp32); "
                               "dh/dW rounded once to bf16 (RNE); no float atomics; "
-                              "audit: 4096-element blocks, fixed trees, fp64 partials";
+                              "audit: 4096-element slices, ceil(slices/608) per block, fixed "
+                              "trees, float-pair (two-sum) partials";
 }
 
 const char* rlk_status_string(rlk_status_t status) {
