@@ -10,7 +10,7 @@
 //
 // Deterministic and atomic-free: kernel 1 counts the active rows of each
 // 1024-row block; kernel 2 gives each block its offset as the sum of the counts
-// before it (ascending block order), places the block's active rows by warp
+// before it (summed by all the block's threads), places the block's active rows by warp
 // ballots (ascending token order), records rows[pos] = t and pos_of[t] = pos
 // (-1 for inactive rows), and block 0 stores the active count; kernel 3 copies
 // the active rows of h, one warp per row over a grid that covers every row, and
@@ -51,14 +51,22 @@ __global__ void __launch_bounds__(kCompactThreads)
     __shared__ int s_base;
     __shared__ int warp_count[kCompactThreads / 32];
     __shared__ int warp_off[kCompactThreads / 32];
-    if (threadIdx.x == 0) {
-        int base = 0;
-        for (int b = 0; b < static_cast<int>(blockIdx.x); ++b) base += blk_count[b];
-        s_base = base;
-        if (blockIdx.x == 0) {
-            int total = 0;
-            for (int b = 0; b < num_blocks; ++b) total += blk_count[b];
-            *n_active = total;
+    __shared__ int s_part[kCompactThreads / 32];
+    // this block's offset: the counts of the blocks before it, summed by all threads
+    // (integers: the order of the additions does not matter); block 0 also sums them all
+    {
+        const int upto = blockIdx.x == 0 ? num_blocks : static_cast<int>(blockIdx.x);
+        int part = 0;
+        for (int b = threadIdx.x; b < upto; b += kCompactThreads) part += blk_count[b];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) part += __shfl_down_sync(0xffffffffu, part, off);
+        if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = part;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int sum = 0;
+            for (int w = 0; w < kCompactThreads / 32; ++w) sum += s_part[w];
+            s_base = blockIdx.x == 0 ? 0 : sum;
+            if (blockIdx.x == 0) *n_active = sum;
         }
     }
     const int t = blockIdx.x * kCompactThreads + threadIdx.x;
