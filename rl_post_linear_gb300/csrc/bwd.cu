@@ -213,7 +213,7 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
                         ai = idx;
                         dom[t] = vb + idx;
                         dcoef[t] = -st.gt;
-                        *dom_flag = 1;
+                        atomicOr(dom_flag, 1);   // set by many rows
                         da = st.gt * -expm1f(l2 * kLn2);
                         if constexpr (ENT) da = fmaf(fmaf(st.c2, cm, st.coef_y), ex2_approx(l2), da);
                     }
@@ -384,7 +384,7 @@ struct DsKlPolicy {
             if (ai < 32) {
                 dom[t] = vb + ai;
                 dcoef[t] = gdom;
-                *dom_flag = 1;
+                atomicOr(dom_flag, 1);   // set by many rows
             }
             uint4* dst = reinterpret_cast<uint4*>(ds + static_cast<size_t>(t) * kBwdChunk + col);
 #pragma unroll
