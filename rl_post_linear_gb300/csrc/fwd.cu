@@ -17,10 +17,11 @@
 // taken from the same accumulator.  At the end of the unit it writes the
 // chunk's partial (m, s), and the target logit if the chunk holds y_t.
 //
-// Kernel 2 (fwd_merge_kernel): one thread per row merges the partials of the
-// chunks in ascending chunk order:
-//     M = max_c m_c,  sigma = sum_c s_c 2^((m_c - M) k),
-//     lse2 = M k + log2(sigma),  logp = (S_y k - lse2) ln 2,  lse = lse2 ln 2.
+// Kernel 2 (fwd_merge_kernel): eight threads per row merge the partials of the
+// chunks, each the chunks c = g (mod 8) in ascending order, then one of them
+// the eight groups in ascending order, each level as
+//     M = max m,  sigma = sum s 2^((m - M) k);
+// then lse2 = M k + log2(sigma),  logp = (S_y k - lse2) ln 2,  lse = lse2 ln 2.
 // Inactive rows get logp = lse = 0; an active row with an out-of-range target
 // gets logp = NaN and raises RLK_DEVERR_TARGET_RANGE.
 //
@@ -161,36 +162,65 @@ struct FwdPolicyT : SingleRole<false, false> {   // h [N,H] and W [V,H]: K-major
     }
 };
 
-__global__ void fwd_merge_kernel(const float2* __restrict__ partials,
-                                 const float* __restrict__ partials_a,
-                                 const float* __restrict__ s_target,
-                                 const int* __restrict__ pos_of,
-                                 const int64_t* __restrict__ targets,
-                                 const uint8_t* __restrict__ mask, int N, int V, int num_chunks,
-                                 float k, float* __restrict__ logp, float* __restrict__ lse,
-                                 float* __restrict__ entropy, uint32_t* err) {
-    const int t = blockIdx.x * blockDim.x + threadIdx.x;
-    if (t >= N) return;
-    if (mask != nullptr && mask[t] == 0) {
+// The merge: kMergeRows rows per block, each row's chunks dealt to kMergeGroups
+// threads (chunk c to group c mod kMergeGroups, so consecutive rows of a group
+// read consecutive addresses).  Each group merges its chunks in ascending order
+// (its max, then the rescaled sums); thread group 0 then merges the groups in
+// ascending order the same way.  A fixed two-level order, a function of the row
+// and of V only: batch invariant, no atomics.
+constexpr int kMergeRows = 32;
+constexpr int kMergeGroups = 8;
+
+__global__ void __launch_bounds__(kMergeRows * kMergeGroups)
+    fwd_merge_kernel(const float2* __restrict__ partials, const float* __restrict__ partials_a,
+                     const float* __restrict__ s_target, const int* __restrict__ pos_of,
+                     const int64_t* __restrict__ targets, const uint8_t* __restrict__ mask,
+                     int N, int V, int num_chunks, float k, float* __restrict__ logp,
+                     float* __restrict__ lse, float* __restrict__ entropy, uint32_t* err) {
+    __shared__ float s_m[kMergeGroups][kMergeRows];
+    __shared__ float s_s[kMergeGroups][kMergeRows];
+    __shared__ float s_a[kMergeGroups][kMergeRows];
+    const int r = threadIdx.x % kMergeRows;
+    const int g = threadIdx.x / kMergeRows;
+    const int t = blockIdx.x * kMergeRows + r;
+    const bool live = t < N && (mask == nullptr || mask[t] != 0);
+    const int i = !live ? 0 : (pos_of != nullptr ? pos_of[t] : t);   // the token's partials row
+    float m = -INFINITY, sigma = 0.f, a = 0.f;
+    if (live) {
+        for (int c = g; c < num_chunks; c += kMergeGroups)
+            m = fmaxf(m, partials[static_cast<size_t>(c) * N + i].x);
+        for (int c = g; c < num_chunks; c += kMergeGroups) {
+            const float2 pc = partials[static_cast<size_t>(c) * N + i];
+            const float wgt = ex2_approx((pc.x - m) * k);
+            sigma += pc.y * wgt;
+            if (entropy != nullptr) a += partials_a[static_cast<size_t>(c) * N + i] * wgt;
+        }
+    }
+    s_m[g][r] = m;
+    s_s[g][r] = sigma;
+    s_a[g][r] = a;
+    __syncthreads();
+    if (g != 0 || t >= N) return;
+    if (!live) {
         logp[t] = 0.f;
         if (lse != nullptr) lse[t] = 0.f;
         if (entropy != nullptr) entropy[t] = 0.f;
         return;
     }
-    const int i = pos_of != nullptr ? pos_of[t] : t;   // the token's row in the partials
-    float m = -INFINITY;
-    for (int c = 0; c < num_chunks; ++c) m = fmaxf(m, partials[static_cast<size_t>(c) * N + i].x);
-    float sigma = 0.f, a = 0.f;
-    for (int c = 0; c < num_chunks; ++c) {
-        const float2 pc = partials[static_cast<size_t>(c) * N + i];
-        const float wgt = ex2_approx((pc.x - m) * k);
-        sigma += pc.y * wgt;
-        if (entropy != nullptr) a += partials_a[static_cast<size_t>(c) * N + i] * wgt;
+    float mm = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < kMergeGroups; ++q) mm = fmaxf(mm, s_m[q][r]);
+    float sg = 0.f, ag = 0.f;
+#pragma unroll
+    for (int q = 0; q < kMergeGroups; ++q) {
+        const float wgt = ex2_approx((s_m[q][r] - mm) * k);   // 0 for a group without chunks
+        sg += s_s[q][r] * wgt;
+        ag += s_a[q][r] * wgt;
     }
-    const float lse2 = m * k + lg2_approx(sigma);
+    const float lse2 = mm * k + lg2_approx(sg);
     constexpr float kLn2 = 0.693147180559945309f;
     if (lse != nullptr) lse[t] = lse2 * kLn2;
-    if (entropy != nullptr) entropy[t] = (lse2 - (a / sigma) * k) * kLn2;
+    if (entropy != nullptr) entropy[t] = (lse2 - (ag / sg) * k) * kLn2;
     const int64_t y = targets[t];
     if (y < 0 || y >= V) {
         logp[t] = __int_as_float(0x7fc00000);
@@ -245,9 +275,9 @@ cudaError_t launch_fwd_partials(const CUtensorMap& map_h, const CUtensorMap& map
 cudaError_t launch_fwd_merge(const float2* partials, int num_chunks, const float* s_target,
                              const int64_t* targets, const uint8_t* mask, int N, int V, float k,
                              float* logp, float* lse, uint32_t* err, cudaStream_t stream) {
-    fwd_merge_kernel<<<(N + 255) / 256, 256, 0, stream>>>(partials, nullptr, s_target, nullptr,
-                                                          targets, mask, N, V, num_chunks, k,
-                                                          logp, lse, nullptr, err);
+    fwd_merge_kernel<<<(N + kMergeRows - 1) / kMergeRows, kMergeRows * kMergeGroups, 0, stream>>>(
+        partials, nullptr, s_target, nullptr, targets, mask, N, V, num_chunks, k, logp, lse,
+        nullptr, err);
     return cudaGetLastError();
 }
 
@@ -266,7 +296,7 @@ cudaError_t launch_fwd(const CUtensorMap& map_h, const CUtensorMap& map_w, const
         : launch_partials_t<false>(map_h, map_w, targets, mask, N, H, V, 0, k, partials, nullptr,
                                    s_target, rows, n_rows, err, num_sms, stream);
     if (e != cudaSuccess) return e;
-    fwd_merge_kernel<<<(N + 255) / 256, 256, 0, stream>>>(
+    fwd_merge_kernel<<<(N + kMergeRows - 1) / kMergeRows, kMergeRows * kMergeGroups, 0, stream>>>(
         partials, entropy != nullptr ? partials_a : nullptr, s_target, pos_of, targets, mask, N, V,
         static_cast<int>(lay.num_chunks), k, logp, lse, entropy, err);
     return cudaGetLastError();
