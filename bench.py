@@ -464,9 +464,12 @@ def measure_next_rows(rlk, dev, pk, warmup, steps, state):
     gen = torch.Generator(device=dev)
     gen.manual_seed(7)
     g_ent = torch.randn(n, device=dev, generator=gen) / n
+    ws_eb = torch.empty(rlk.rlk_linear_logp_entropy_bwd_workspace_bytes(n, h, v),
+                        dtype=torch.uint8, device=dev)
     ms_b = _time_calls(lambda: rlk.rlk_linear_logp_entropy_bwd(hid, wt, y, mask, g, g_ent, lse_e,
-                                                               ent, T, dh, dw, ws_b),
+                                                               ent, T, dh, dw, ws_eb),
                        warmup, steps, stream)
+    del ws_eb
     res["entropy_fwd"] = {"ms": ms_f, "tflops": fwd_flops / (ms_f * 1e-3) / 1e12,
                           "frac_of_peak": fwd_flops / (ms_f * 1e-3) / 1e12 / peak}
     res["entropy_bwd"] = {"ms": ms_b, "tflops": bwd_flops / (ms_b * 1e-3) / 1e12,

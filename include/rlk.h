@@ -110,14 +110,15 @@ typedef struct {
 /* Scratch bytes each entry point needs for these sizes (pure arithmetic, no CUDA call). */
 size_t rlk_linear_logp_fwd_workspace_bytes(int64_t N, int64_t H, int64_t V);
 size_t rlk_linear_logp_bwd_workspace_bytes(int64_t N, int64_t H, int64_t V);
+size_t rlk_linear_logp_entropy_bwd_workspace_bytes(int64_t N, int64_t H, int64_t V);
 size_t rlk_dlogp_audit_workspace_bytes(int64_t N);
 size_t rlk_grpo_clip_loss_workspace_bytes(int64_t N);
 size_t rlk_dlogp_audit_ext_workspace_bytes(int64_t N);
 
 /*
  * Forward.  "RL-Kernel Roadmap (2026)" P0.2; "RL-Kernel integration roadmap
- * for vime", linear_logp: local max, global max, local sum-exp, global
- * sum-exp, selected target logit, final downcast point.
+ * for vime", linear_logp (the explicit merge of per-block softmax statistics
+ * and where the result is downcast).
  *
  *   hidden      [N,H] bf16        weight [V,H] bf16
  *   targets     [N] int64         active_mask [N] uint8 or NULL
@@ -190,8 +191,15 @@ rlk_status_t rlk_linear_logp_entropy_fwd(const void* hidden, const void* weight,
  *   dS[t,v] = ( g_t (delta(v,y_t) - p) - gH_t p (z_v - E_p[z]) ) / T
  *
  * lse and entropy are the forward's outputs (E_p[z] = lse - entropy).  Same
- * chunked recompute, workspace, rounding and determinism as
- * rlk_linear_logp_bwd; grad_entropy = 0 gives rlk_linear_logp_bwd's result.
+ * chunked recompute, rounding and determinism as rlk_linear_logp_bwd, except
+ * that dS is kept as two bf16 planes, hi = bf16(dS) and lo = bf16(dS - hi),
+ * and the dh and dW GEMMs run over both (twice their K): the entropy gradient
+ * has no fp32 part that dominates a row, and one bf16 rounding of dS would
+ * cost as much accuracy as the final rounding of the outputs.  Rows with
+ * grad_entropy = 0 store lo = 0, so grad_entropy = 0 gives
+ * rlk_linear_logp_bwd's dhidden and dweight bit for bit.
+ * workspace: rlk_linear_logp_entropy_bwd_workspace_bytes(N, H, V) (the dS
+ * part is twice rlk_linear_logp_bwd's).
  */
 rlk_status_t rlk_linear_logp_entropy_bwd(const void* hidden, const void* weight,
                                          const int64_t* targets, const uint8_t* active_mask,
@@ -254,8 +262,10 @@ rlk_status_t rlk_linear_kl_fwd(const void* hidden, const void* weight, const voi
  * get dhidden = 0.  Unlike rlk_linear_logp_bwd this backward does not compact
  * a masked batch: the GEMMs run over all N rows, so the hidden rows of
  * inactive tokens (both heads) must hold finite values (a NaN there would
- * reach dweight through 0 * NaN).
- * workspace: rlk_linear_kl_bwd_workspace_bytes(N, H, V).
+ * reach dweight through 0 * NaN).  As in rlk_linear_logp_entropy_bwd, dS is
+ * kept as hi and lo bf16 planes that the dh and dW GEMMs both consume.
+ * workspace: rlk_linear_kl_bwd_workspace_bytes(N, H, V)
+ * (= rlk_linear_logp_entropy_bwd_workspace_bytes).
  */
 size_t rlk_linear_kl_bwd_workspace_bytes(int64_t N, int64_t H, int64_t V);
 rlk_status_t rlk_linear_kl_bwd(const void* hidden, const void* weight, const void* hidden_ref,
@@ -275,8 +285,13 @@ rlk_status_t rlk_linear_kl_bwd(const void* hidden, const void* weight, const voi
  *
  *   logp_new, logp_old [N] fp32; active_mask [N] uint8 or NULL
  *   result_dev  one rlk_audit_result_t in device memory (overwritten)
+ *   workspace   rlk_dlogp_audit_workspace_bytes(N) bytes, 256-aligned; its
+ *               contents on entry do not matter
  * Fixed-size blocks and fixed-order trees: the result is bitwise
- * reproducible for a given N.
+ * reproducible for a given N.  One kernel launch (after a 4-byte
+ * cudaMemsetAsync of a counter in the workspace): each block writes its
+ * partial and takes an integer ticket, and the block with the last ticket
+ * merges all partials in a fixed order.
  */
 rlk_status_t rlk_dlogp_audit(const float* logp_new, const float* logp_old,
                              const uint8_t* active_mask, int64_t N,
@@ -285,10 +300,9 @@ rlk_status_t rlk_dlogp_audit(const float* logp_new, const float* logp_old,
 
 /*
  * Vocab-sharded forward, for tensor-parallel LM heads.  "RL-Kernel
- * integration roadmap for vime", linear_logp: TP support makes the
- * vocab-shard merge explicit -- local max, global max, local sum-exp, global
- * sum-exp, selected target logit, final downcast point; "RL-Kernel Roadmap
- * (2026)", TP-invariant reductions.
+ * integration roadmap for vime", linear_logp (TP support: the merge of the
+ * vocabulary shards' softmax statistics is an explicit step); "RL-Kernel
+ * Roadmap (2026)", TP-invariant reductions.
  *
  * rlk_linear_logp_fwd_shard scores one contiguous block of vocabulary rows
  * [vocab_start, vocab_start + V_local) of the LM head:
@@ -353,6 +367,37 @@ rlk_status_t rlk_linear_logp_bwd_shard(const void* hidden, const void* weight_sh
                                        uint32_t* device_error_word, cudaStream_t stream);
 rlk_status_t rlk_linear_logp_dh_merge(const float* dh_partials, int64_t num_partials, int64_t N,
                                       int64_t H, void* dhidden, cudaStream_t stream);
+
+/*
+ * Data-parallel gradient exchange of the LM head.  "RL-Kernel Roadmap
+ * (2026)", WS2 (a deterministic all-reduce: a fixed rank order with fp32
+ * accumulation).  dW sums over the batch, so with the tokens split over
+ * ranks every rank holds a partial sum of it; rounding each partial to bf16
+ * and summing in whatever order a collective picks would be neither
+ * reproducible nor as accurate as one rounding at the end.
+ *
+ * rlk_linear_logp_bwd_dw_partial is rlk_linear_logp_bwd on one rank's tokens
+ * (same arguments, workspace query, dhidden and error behaviour), except that
+ * dW is written unrounded:
+ *   dweight_partial  [V,H] fp32 (overwritten), 16-byte aligned
+ * rlk_linear_logp_dw_merge then forms
+ *   dweight = bf16( sum_{r = 0}^{num_partials - 1} dw_partials[r] )   [V,H] bf16
+ * with fp32 additions in ascending r (partial r at dw_partials + r*V*H), one
+ * RNE rounding per element: the result depends on the partials and their
+ * order only.  Gathering the partials in rank order (an all-to-all of row
+ * blocks, or an all-gather) is the caller's.  Errors: num_partials < 1, a
+ * NULL or unaligned pointer -> RLK_ERR_INVALID_VALUE; H % 64 != 0 ->
+ * RLK_ERR_UNSUPPORTED; V = 0 -> RLK_OK, nothing enqueued.
+ */
+rlk_status_t rlk_linear_logp_bwd_dw_partial(const void* hidden, const void* weight,
+                                            const int64_t* targets, const uint8_t* active_mask,
+                                            const float* grad_logp, const float* lse, int64_t N,
+                                            int64_t H, int64_t V, double temperature,
+                                            void* dhidden, float* dweight_partial,
+                                            void* workspace, size_t workspace_bytes,
+                                            uint32_t* device_error_word, cudaStream_t stream);
+rlk_status_t rlk_linear_logp_dw_merge(const float* dw_partials, int64_t num_partials, int64_t V,
+                                      int64_t H, void* dweight, cudaStream_t stream);
 
 /*
  * Selected-token logp from existing logits.  "RL-Kernel integration roadmap
@@ -436,13 +481,18 @@ rlk_status_t rlk_dlogp_audit_ext(const float* logp_new, const float* logp_old,
  * Same inputs, result and arithmetic as rlk_dlogp_audit, minus the workspace.
  *  - N must not exceed RLK_AUDIT_NOALLOC_MAX_N; larger N returns
  *    RLK_ERR_UNSUPPORTED before anything is enqueued (use rlk_dlogp_audit).
- *  - The scratch is a file-scope __device__ array of 1.25 MiB that every GPU
- *    loading the library holds until the process exits.  Its device address
- *    is looked up on the first call on each device (with that device current);
- *    make that first call before any stream capture.
- *  - Calls share the scratch, which keeps the last call's contents (nothing
- *    in it needs to start at zero).  Calls that overlap on the GPU -- on
- *    different streams without ordering -- race and give wrong results.
+ *  - The scratch is a file-scope __device__ array of about 1.25 MiB that
+ *    every GPU loading the library holds until the process exits.  Its device
+ *    address is looked up on the first call on each device (with that device
+ *    current) and again whenever the device's context has been created anew
+ *    (after cudaDeviceReset, say); make the first call on a device before any
+ *    stream capture.
+ *  - Calls share the scratch, which keeps the last call's contents.  Its one
+ *    word that must start at zero (the merge ticket) is cleared on the stream
+ *    by each call (cudaMemsetAsync, which allocates nothing); the per-block
+ *    partials are written before they are read.  Calls that overlap on the
+ *    GPU -- on different streams without ordering -- race and give wrong
+ *    results.
  *  - No cudaMalloc, cudaFree or other allocating call is made.
  */
 #define RLK_AUDIT_NOALLOC_MAX_N ((int64_t)1 << 27)

@@ -99,6 +99,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.rlk_linear_logp_fwd_workspace_bytes.argtypes = [_i64, _i64, _i64]
     lib.rlk_linear_logp_bwd_workspace_bytes.restype = _sz
     lib.rlk_linear_logp_bwd_workspace_bytes.argtypes = [_i64, _i64, _i64]
+    lib.rlk_linear_logp_entropy_bwd_workspace_bytes.restype = _sz
+    lib.rlk_linear_logp_entropy_bwd_workspace_bytes.argtypes = [_i64, _i64, _i64]
     lib.rlk_dlogp_audit_workspace_bytes.restype = _sz
     lib.rlk_dlogp_audit_workspace_bytes.argtypes = [_i64]
     lib.rlk_linear_logp_fwd.restype = ctypes.c_int
@@ -129,6 +131,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                               _vp, _vp]
     lib.rlk_linear_logp_dh_merge.restype = ctypes.c_int
     lib.rlk_linear_logp_dh_merge.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp]
+    lib.rlk_linear_logp_bwd_dw_partial.restype = ctypes.c_int
+    lib.rlk_linear_logp_bwd_dw_partial.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64,
+                                                   _i64, ctypes.c_double, _vp, _vp, _vp, _sz,
+                                                   _vp, _vp]
+    lib.rlk_linear_logp_dw_merge.restype = ctypes.c_int
+    lib.rlk_linear_logp_dw_merge.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp]
     lib.rlk_linear_logp_entropy_bwd.restype = ctypes.c_int
     lib.rlk_linear_logp_entropy_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64,
                                                 _i64, _i64, ctypes.c_double, _vp, _vp, _vp, _sz,
@@ -187,6 +195,10 @@ def rlk_linear_logp_fwd_workspace_bytes(N: int, H: int, V: int) -> int:
 
 def rlk_linear_logp_bwd_workspace_bytes(N: int, H: int, V: int) -> int:
     return int(load().rlk_linear_logp_bwd_workspace_bytes(N, H, V))
+
+
+def rlk_linear_logp_entropy_bwd_workspace_bytes(N: int, H: int, V: int) -> int:
+    return int(load().rlk_linear_logp_entropy_bwd_workspace_bytes(N, H, V))
 
 
 def rlk_dlogp_audit_workspace_bytes(N: int) -> int:
@@ -431,6 +443,41 @@ def rlk_linear_logp_dh_merge(dh_partials, dhidden, stream=None):
     _check("rlk_linear_logp_dh_merge", st)
 
 
+def rlk_linear_logp_bwd_dw_partial(hidden, weight, targets, active_mask, grad_logp, lse,
+                                   temperature, dhidden, dweight_partial, workspace,
+                                   device_error_word=None, stream=None):
+    """One data-parallel rank's backward: bf16 dhidden and an unrounded fp32 dW partial."""
+    n, h = hidden.shape
+    v = weight.shape[0]
+    _need(hidden, torch.bfloat16, "hidden")
+    _need(weight, torch.bfloat16, "weight", (v, h))
+    _need(targets, torch.int64, "targets", (n,))
+    if active_mask is not None:
+        _need(active_mask, torch.uint8, "active_mask", (n,))
+    _need(grad_logp, torch.float32, "grad_logp", (n,))
+    _need(lse, torch.float32, "lse", (n,))
+    _need(dhidden, torch.bfloat16, "dhidden", (n, h))
+    _need(dweight_partial, torch.float32, "dweight_partial", (v, h))
+    _need(workspace, torch.uint8, "workspace")
+    st = load().rlk_linear_logp_bwd_dw_partial(_ptr(hidden), _ptr(weight), _ptr(targets),
+                                               _ptr(active_mask), _ptr(grad_logp), _ptr(lse), n,
+                                               h, v, float(temperature), _ptr(dhidden),
+                                               _ptr(dweight_partial), _ptr(workspace),
+                                               workspace.numel(), _ptr(device_error_word),
+                                               _stream(stream))
+    _check("rlk_linear_logp_bwd_dw_partial", st)
+
+
+def rlk_linear_logp_dw_merge(dw_partials, dweight, stream=None):
+    """dweight = bf16(sum over the leading axis of dw_partials [k, V, H] fp32), ascending."""
+    k, v, h = dw_partials.shape
+    _need(dw_partials, torch.float32, "dw_partials")
+    _need(dweight, torch.bfloat16, "dweight", (v, h))
+    st = load().rlk_linear_logp_dw_merge(_ptr(dw_partials), k, v, h, _ptr(dweight),
+                                         _stream(stream))
+    _check("rlk_linear_logp_dw_merge", st)
+
+
 def rlk_dlogp_audit(logp_new, logp_old, active_mask, result, workspace, stream=None):
     """Enqueue the audit; ``result`` is a uint8 CUDA tensor of AUDIT_RESULT_BYTES bytes."""
     n = logp_new.shape[0]
@@ -624,7 +671,7 @@ def linear_logp_entropy_bwd(hidden, weight, targets, active_mask, grad_logp, gra
     v = weight.shape[0]
     dh = torch.empty_like(hidden)
     dw = torch.empty_like(weight)
-    ws = _workspace(rlk_linear_logp_bwd_workspace_bytes(n, h, v), hidden.device)
+    ws = _workspace(rlk_linear_logp_entropy_bwd_workspace_bytes(n, h, v), hidden.device)
     rlk_linear_logp_entropy_bwd(hidden, weight, targets, active_mask, grad_logp, grad_entropy,
                                 lse, entropy, temperature, dh, dw, ws, error_word)
     return dh, dw

@@ -110,9 +110,15 @@ size_t rlk_linear_logp_bwd_workspace_bytes(int64_t N, int64_t H, int64_t V) {
     return rlk::BwdLayout(N, H).total;
 }
 
+size_t rlk_linear_logp_entropy_bwd_workspace_bytes(int64_t N, int64_t H, int64_t V) {
+    (void)V;
+    if (N < 0 || H < 0) return 0;
+    return rlk::BwdLayout(N, H, true).total;
+}
+
 size_t rlk_dlogp_audit_workspace_bytes(int64_t N) {
     if (N < 0) return 0;
-    return align_up(rlk::audit_v3_blocks(N) * sizeof(rlk::AuditPartial), 256) + 256;
+    return rlk::audit_ticket_offset(N) + 256;   // the partials, then the ticket word
 }
 
 // The vocabulary in ascending kBwdChunk-column chunks; per chunk the dS
@@ -121,11 +127,14 @@ size_t rlk_dlogp_audit_workspace_bytes(int64_t N) {
 static rlk_status_t bwd_chunks(rlk::BwdStepMaps& maps, rlk::BwdStep& st, void* ds, int64_t N,
                                int64_t V, int sms, uint32_t* device_error_word,
                                cudaStream_t stream) {
+    // hilo: each dS row holds the hi plane, then the lo plane kBwdChunk columns on; the
+    // maps span both (the columns between them are written or never read)
+    const uint64_t ld = uint64_t(rlk::kBwdChunk) * (st.hilo ? 2 : 1);
     for (int c = 0; c < st.num_chunks; ++c) {
         const int64_t width = std::min<int64_t>(rlk::kBwdChunk, V - int64_t(c) * rlk::kBwdChunk);
-        RLK_TRY(make_map(&maps.ds_kmajor, ds, width, N, uint64_t(rlk::kBwdChunk) * 2, 64,
-                         rlk::kTileM));
-        RLK_TRY(make_map(&maps.ds_mnmajor, ds, width, N, uint64_t(rlk::kBwdChunk) * 2, 64, 64));
+        const uint64_t inner = uint64_t(width) + (st.hilo ? uint64_t(rlk::kBwdChunk) : 0);
+        RLK_TRY(make_map(&maps.ds_kmajor, ds, inner, N, ld * 2, 64, rlk::kTileM));
+        RLK_TRY(make_map(&maps.ds_mnmajor, ds, inner, N, ld * 2, 64, 64));
         st.ds = ds;
         st.chunk = c;
         for (int role : {rlk::kRoleDs, rlk::kRoleDh, rlk::kRoleDw}) {
@@ -233,7 +242,7 @@ rlk_status_t rlk_linear_kl_fwd(const void* hidden, const void* weight, const voi
 }
 
 size_t rlk_linear_kl_bwd_workspace_bytes(int64_t N, int64_t H, int64_t V) {
-    return rlk_linear_logp_bwd_workspace_bytes(N, H, V);
+    return rlk_linear_logp_entropy_bwd_workspace_bytes(N, H, V);
 }
 
 rlk_status_t rlk_linear_kl_bwd(const void* hidden, const void* weight, const void* hidden_ref,
@@ -261,7 +270,7 @@ rlk_status_t rlk_linear_kl_bwd(const void* hidden, const void* weight, const voi
     DeviceInfo dev;
     RLK_TRY(current_device(dev));
 
-    const rlk::BwdLayout lay(N, H);
+    const rlk::BwdLayout lay(N, H, true);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     rlk::BwdStepMaps maps;
     RLK_TRY(make_map(&maps.h_kmajor, hidden, H, N, H * 2, 64, rlk::kTileM));
@@ -283,6 +292,7 @@ rlk_status_t rlk_linear_kl_bwd(const void* hidden, const void* weight, const voi
     st.k = static_cast<float>(1.4426950408889634074 / temperature);
     st.temp = static_cast<float>(temperature);
     st.kl = true;
+    st.hilo = true;
     st.y_off = 0;
     st.V_global = static_cast<int>(V);
     st.round_last = true;
@@ -327,27 +337,31 @@ static rlk_status_t bwd_impl(const void* hidden, const void* weight, const int64
                              const float* grad_entropy, const float* entropy, const float* lse,
                              int64_t N, int64_t H, int64_t V, int64_t vocab_start,
                              int64_t vocab_size, double temperature, void* dhidden,
-                             float* dh_partial, void* dweight, void* workspace,
-                             size_t workspace_bytes, uint32_t* device_error_word,
-                             cudaStream_t stream) {
+                             float* dh_partial, void* dweight, float* dw_partial,
+                             void* workspace, size_t workspace_bytes,
+                             uint32_t* device_error_word, cudaStream_t stream) {
     RLK_TRY(check_shape(N, H, V, temperature));
     if (vocab_start < 0 || vocab_size > kMaxDim || vocab_start + V > vocab_size)
         return RLK_ERR_INVALID_VALUE;
     if (N == 0) return RLK_OK;
     void* dh_out = dh_partial != nullptr ? static_cast<void*>(dh_partial) : dhidden;
+    void* dw_out = dw_partial != nullptr ? static_cast<void*>(dw_partial) : dweight;
     if (hidden == nullptr || weight == nullptr || targets == nullptr || grad_logp == nullptr ||
-        lse == nullptr || dh_out == nullptr || dweight == nullptr)
+        lse == nullptr || dh_out == nullptr || dw_out == nullptr)
         return RLK_ERR_INVALID_VALUE;
     if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(dh_out, 16) ||
-        !aligned(dweight, 16))
+        !aligned(dw_out, 16))
         return RLK_ERR_INVALID_VALUE;
-    if (workspace == nullptr || !aligned(workspace, 256) ||
-        workspace_bytes < rlk_linear_logp_bwd_workspace_bytes(N, H, V))
+    // the entropy gradient takes dS as hi / lo planes (twice the dS workspace)
+    const bool hilo = grad_entropy != nullptr;
+    const size_t need = hilo ? rlk_linear_logp_entropy_bwd_workspace_bytes(N, H, V)
+                             : rlk_linear_logp_bwd_workspace_bytes(N, H, V);
+    if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need)
         return RLK_ERR_WORKSPACE;
     DeviceInfo dev;
     RLK_TRY(current_device(dev));
 
-    const rlk::BwdLayout lay(N, H);
+    const rlk::BwdLayout lay(N, H, hilo);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     float* dh_acc = reinterpret_cast<float*>(ws + lay.dhacc_off);
     int* sorted_y = reinterpret_cast<int*>(ws + lay.sorted_y_off);
@@ -393,6 +407,7 @@ static rlk_status_t bwd_impl(const void* hidden, const void* weight, const int64
     st.grad = grad_logp;
     st.grad_ent = grad_entropy;
     st.ent = entropy;
+    st.hilo = hilo;
     st.lse = lse;
     st.hidden = hidden;
     st.weight = weight;
@@ -420,6 +435,7 @@ static rlk_status_t bwd_impl(const void* hidden, const void* weight, const int64
     st.tiles = tiles;
     st.dhidden = dhidden;
     st.dweight = dweight;
+    st.dw_out32 = dw_partial;
     return bwd_chunks(maps, st, ws + lay.ds_off, N, V, dev.sms, device_error_word, stream);
 }
 
@@ -430,8 +446,33 @@ rlk_status_t rlk_linear_logp_bwd(const void* hidden, const void* weight, const i
                                  void* workspace, size_t workspace_bytes,
                                  uint32_t* device_error_word, cudaStream_t stream) {
     return bwd_impl(hidden, weight, targets, active_mask, grad_logp, nullptr, nullptr, lse, N, H,
-                    V, 0, V, temperature, dhidden, nullptr, dweight, workspace, workspace_bytes,
-                    device_error_word, stream);
+                    V, 0, V, temperature, dhidden, nullptr, dweight, nullptr, workspace,
+                    workspace_bytes, device_error_word, stream);
+}
+
+rlk_status_t rlk_linear_logp_bwd_dw_partial(const void* hidden, const void* weight,
+                                            const int64_t* targets, const uint8_t* active_mask,
+                                            const float* grad_logp, const float* lse, int64_t N,
+                                            int64_t H, int64_t V, double temperature,
+                                            void* dhidden, float* dweight_partial,
+                                            void* workspace, size_t workspace_bytes,
+                                            uint32_t* device_error_word, cudaStream_t stream) {
+    if (N > 0 && dweight_partial == nullptr) return RLK_ERR_INVALID_VALUE;
+    return bwd_impl(hidden, weight, targets, active_mask, grad_logp, nullptr, nullptr, lse, N, H,
+                    V, 0, V, temperature, dhidden, nullptr, nullptr, dweight_partial, workspace,
+                    workspace_bytes, device_error_word, stream);
+}
+
+rlk_status_t rlk_linear_logp_dw_merge(const float* dw_partials, int64_t num_partials, int64_t V,
+                                      int64_t H, void* dweight, cudaStream_t stream) {
+    if (num_partials < 1 || V < 0 || V > kMaxDim || H < 1) return RLK_ERR_INVALID_VALUE;
+    if (H % 64 != 0) return RLK_ERR_UNSUPPORTED;
+    if (V == 0) return RLK_OK;
+    if (dw_partials == nullptr || dweight == nullptr || !aligned(dw_partials, 16) ||
+        !aligned(dweight, 16))
+        return RLK_ERR_INVALID_VALUE;
+    RLK_CUDA(rlk::launch_dh_merge(dw_partials, num_partials, V, H, dweight, stream));
+    return RLK_OK;
 }
 
 rlk_status_t rlk_linear_logp_bwd_shard(const void* hidden, const void* weight_shard,
@@ -445,7 +486,7 @@ rlk_status_t rlk_linear_logp_bwd_shard(const void* hidden, const void* weight_sh
     if (N > 0 && dhidden_partial == nullptr) return RLK_ERR_INVALID_VALUE;
     return bwd_impl(hidden, weight_shard, targets, active_mask, grad_logp, nullptr, nullptr, lse,
                     N, H, V_local, vocab_start, vocab_size, temperature, nullptr,
-                    dhidden_partial, dweight_shard, workspace, workspace_bytes,
+                    dhidden_partial, dweight_shard, nullptr, workspace, workspace_bytes,
                     device_error_word, stream);
 }
 
@@ -472,7 +513,7 @@ rlk_status_t rlk_linear_logp_entropy_bwd(const void* hidden, const void* weight,
                                          cudaStream_t stream) {
     if (N > 0 && (grad_entropy == nullptr || entropy == nullptr)) return RLK_ERR_INVALID_VALUE;
     return bwd_impl(hidden, weight, targets, active_mask, grad_logp, grad_entropy, entropy, lse,
-                    N, H, V, 0, V, temperature, dhidden, nullptr, dweight, workspace,
+                    N, H, V, 0, V, temperature, dhidden, nullptr, dweight, nullptr, workspace,
                     workspace_bytes, device_error_word, stream);
 }
 
@@ -490,8 +531,10 @@ rlk_status_t rlk_dlogp_audit(const float* logp_new, const float* logp_old,
     RLK_TRY(current_device(dev));
     const bool vec_ok = aligned(logp_new, 16) && aligned(logp_old, 16) &&
                         (active_mask == nullptr || aligned(active_mask, 4));
-    RLK_CUDA(rlk::launch_audit(logp_new, logp_old, active_mask, N, result_dev, workspace, vec_ok,
-                               stream));
+    unsigned int* ticket = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(workspace) +
+                                                           rlk::audit_ticket_offset(N));
+    RLK_CUDA(rlk::launch_audit(logp_new, logp_old, active_mask, N, result_dev, workspace, ticket,
+                               vec_ok, stream));
     return RLK_OK;
 }
 
@@ -645,11 +688,12 @@ rlk_status_t rlk_dlogp_audit_noalloc(const float* logp_new, const float* logp_ol
     DeviceInfo dev;
     RLK_TRY(current_device(dev));
     void* scratch = nullptr;
-    RLK_CUDA(rlk::audit_noalloc_scratch(&scratch));
+    unsigned int* ticket = nullptr;
+    RLK_CUDA(rlk::audit_noalloc_scratch(&scratch, &ticket));
     const bool vec_ok = aligned(logp_new, 16) && aligned(logp_old, 16) &&
                         (active_mask == nullptr || aligned(active_mask, 4));
-    RLK_CUDA(rlk::launch_audit(logp_new, logp_old, active_mask, N, result_dev, scratch, vec_ok,
-                               stream));
+    RLK_CUDA(rlk::launch_audit(logp_new, logp_old, active_mask, N, result_dev, scratch, ticket,
+                               vec_ok, stream));
     return RLK_OK;
 }
 

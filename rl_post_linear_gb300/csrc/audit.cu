@@ -224,13 +224,22 @@ inline int64_t audit_pass1_blocks(int64_t N) {
     return (slices + spb - 1) / spb;
 }
 
-template <bool VEC>
+template <int THREADS, bool COHERENT>
+__device__ void merge_partials(const AuditPartial* parts, int64_t num_parts,
+                               rlk_audit_result_t* result);
+
+// FUSED: one launch.  After writing its partial, each block takes an integer ticket
+// (atomicAdd on a counter that starts at zero); the block that draws the last one
+// merges every partial in the fixed order of merge_partials and writes the result.
+// Which block merges depends on the schedule, the merge order does not.
+template <bool VEC, bool FUSED>
 __global__ void __launch_bounds__(kAuditThreads)
     audit_pass1(const float* __restrict__ nw, const float* __restrict__ od,
                 const uint8_t* __restrict__ mask, int64_t N, int64_t slices_per_block,
-                AuditPartial* __restrict__ out) {
-    // let the merge kernel launch now; it waits for this grid before reading
-    asm volatile("griddepcontrol.launch_dependents;");
+                AuditPartial* __restrict__ out, unsigned int* ticket,
+                rlk_audit_result_t* __restrict__ result) {
+    // two launches: let the merge kernel launch now; it waits for this grid before reading
+    if constexpr (!FUSED) asm volatile("griddepcontrol.launch_dependents;");
     constexpr int kVec = kAuditV3PerThread / 4;
     constexpr int kBlock = kAuditThreads * kAuditV3PerThread;
     const int64_t block_base = static_cast<int64_t>(blockIdx.x) * slices_per_block * kBlock;
@@ -353,6 +362,19 @@ __global__ void __launch_bounds__(kAuditThreads)
         p.flags = t.flags;
         out[blockIdx.x] = p;
     }
+    if constexpr (FUSED) {
+        __shared__ int is_last;
+        if (threadIdx.x == 0) {
+            __threadfence();             // the partial is visible before the ticket is taken
+            is_last = atomicAdd(ticket, 1u) == gridDim.x - 1u;
+        }
+        __syncthreads();
+        if (is_last) {
+            __threadfence();
+            merge_partials<kAuditThreads, true>(out, gridDim.x, result);
+            if (threadIdx.x == 0) *ticket = 0u;
+        }
+    }
 }
 
 constexpr int kMergeThreads = 1024;
@@ -369,25 +391,41 @@ __device__ __forceinline__ Acc to_acc(const AuditPartial& p) {
     return b;
 }
 
-__global__ void __launch_bounds__(kMergeThreads)
-    audit_pass2(const AuditPartial* __restrict__ parts, int64_t num_parts,
-                rlk_audit_result_t* __restrict__ result) {
-    // launched early (programmatic dependent launch): wait until every block of
-    // pass 1 has finished and its partials are visible
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+// Partial i, read through L2 when COHERENT (partials written by other blocks of the
+// same grid: L1 is not coherent across SMs).
+template <bool COHERENT>
+__device__ __forceinline__ AuditPartial load_partial(const AuditPartial* parts, int64_t i) {
+    if constexpr (!COHERENT) {
+        return parts[i];
+    } else {
+        static_assert(sizeof(AuditPartial) == 40, "five 8-byte words");
+        const unsigned long long* w = reinterpret_cast<const unsigned long long*>(parts + i);
+        unsigned long long v[5];
+#pragma unroll
+        for (int j = 0; j < 5; ++j) v[j] = __ldcg(w + j);
+        AuditPartial p;
+        memcpy(&p, v, sizeof(p));
+        return p;
+    }
+}
+
+// Thread t folds partials t, t + THREADS, t + 2 THREADS, ... in ascending order (they
+// are loaded kMergeBatch at a time so that the loads overlap; the order is unchanged),
+// then the fixed block tree; thread 0 writes the result.
+template <int THREADS, bool COHERENT>
+__device__ void merge_partials(const AuditPartial* parts, int64_t num_parts,
+                               rlk_audit_result_t* result) {
     Acc a = empty_acc();
-    // thread t folds partials t, t + 1024, t + 2048, ... in ascending order; they are
-    // loaded kMergeBatch at a time so that the loads overlap (the order is unchanged)
     int64_t i = threadIdx.x;
-    for (; i + (kMergeBatch - 1) * kMergeThreads < num_parts; i += kMergeBatch * kMergeThreads) {
+    for (; i + (kMergeBatch - 1) * THREADS < num_parts; i += kMergeBatch * THREADS) {
         AuditPartial p[kMergeBatch];
 #pragma unroll
-        for (int j = 0; j < kMergeBatch; ++j) p[j] = parts[i + j * kMergeThreads];
+        for (int j = 0; j < kMergeBatch; ++j) p[j] = load_partial<COHERENT>(parts, i + j * THREADS);
 #pragma unroll
         for (int j = 0; j < kMergeBatch; ++j) merge(a, to_acc(p[j]));
     }
-    for (; i < num_parts; i += kMergeThreads) merge(a, to_acc(parts[i]));
-    a = block_reduce<kMergeThreads>(a);
+    for (; i < num_parts; i += THREADS) merge(a, to_acc(load_partial<COHERENT>(parts, i)));
+    a = block_reduce<THREADS>(a);
     if (threadIdx.x == 0) {
         rlk_audit_result_t r;
         r.active_count = a.count;
@@ -398,6 +436,15 @@ __global__ void __launch_bounds__(kMergeThreads)
         r.error_flags = a.flags;
         *result = r;
     }
+}
+
+__global__ void __launch_bounds__(kMergeThreads)
+    audit_pass2(const AuditPartial* __restrict__ parts, int64_t num_parts,
+                rlk_audit_result_t* __restrict__ result) {
+    // launched early (programmatic dependent launch): wait until every block of
+    // pass 1 has finished and its partials are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    merge_partials<kMergeThreads, false>(parts, num_parts, result);
 }
 
 // ----------------------------------------------------------------------------- extended audit
@@ -818,49 +865,97 @@ __global__ void __launch_bounds__(kSelectThreads)
 
 }  // namespace
 
-// Scratch of rlk_dlogp_audit_noalloc: one partial per 4096-element block for
-// up to RLK_AUDIT_NOALLOC_MAX_N tokens (32768 x 40 bytes = 1.25 MiB).  It lives
-// in the library image, so every GPU that loads the library holds it until the
-// process exits.  Pass 1 writes every slot that pass 2 reads, so nothing in it
-// has to start at zero; calls that overlap on the GPU share it and race.
+// Scratch of rlk_dlogp_audit_noalloc: room for the partials of pass 1 (it writes
+// at most kAuditMaxBlocks of them, whatever N) and the ticket counter of the
+// single-launch audit.  It lives in the library image, so every GPU that loads
+// the library holds it until the process exits.  Pass 1 writes every partial that
+// the merge reads; the ticket is cleared on the stream before each launch.  Calls
+// that overlap on the GPU share it and race.
 constexpr size_t kNoAllocBlocks =
     static_cast<size_t>(RLK_AUDIT_NOALLOC_MAX_N) / (kAuditThreads * kAuditV3PerThread);
-static __device__ __align__(256) AuditPartial g_audit_noalloc_scratch[kNoAllocBlocks];
+static_assert(kNoAllocBlocks >= static_cast<size_t>(kAuditMaxBlocks),
+              "the no-alloc scratch must hold every partial pass 1 can write");
+struct NoAllocScratch {
+    AuditPartial parts[kNoAllocBlocks];
+    unsigned int ticket;
+};
+static __device__ __align__(256) NoAllocScratch g_audit_noalloc_scratch;
 
-cudaError_t audit_noalloc_scratch(void** out) {
-    // Host code cannot use the array's name as a device address: look the
-    // address up once per device, with that device current.
+namespace {
+
+using PfnCtxGetCurrent = CUresult (*)(CUcontext*);
+using PfnCtxGetId = CUresult (*)(CUcontext, unsigned long long*);
+
+template <class F>
+F driver_fn(const char* name) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<F>(p);
+}
+
+}  // namespace
+
+cudaError_t audit_noalloc_scratch(void** parts, unsigned int** ticket) {
+    // Host code cannot use the array's name as a device address: the address is looked
+    // up with the device current, and cached per device together with the unique id of
+    // the context it belongs to, so that a context created anew (after cudaDeviceReset,
+    // say) is looked up again instead of reusing a stale address.
     static std::mutex mu;
+    static std::once_flag once;
+    static PfnCtxGetCurrent get_current = nullptr;
+    static PfnCtxGetId get_id = nullptr;
     static void* addr[64] = {};
+    static unsigned long long ctx_id[64] = {};
+    std::call_once(once, [] {
+        get_current = driver_fn<PfnCtxGetCurrent>("cuCtxGetCurrent");
+        get_id = driver_fn<PfnCtxGetId>("cuCtxGetId");
+    });
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    // without a current context yet (no id), the address is looked up on every call
+    unsigned long long id = 0;
+    CUcontext ctx = nullptr;
+    const bool have_id = get_current != nullptr && get_id != nullptr &&
+                         get_current(&ctx) == CUDA_SUCCESS && ctx != nullptr &&
+                         get_id(ctx, &id) == CUDA_SUCCESS;
     std::lock_guard<std::mutex> lock(mu);
-    if (addr[dev] == nullptr) {
+    if (!have_id || addr[dev] == nullptr || ctx_id[dev] != id) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_audit_noalloc_scratch);
         if (e != cudaSuccess) return e;
         addr[dev] = p;
+        ctx_id[dev] = have_id ? id : 0;
     }
-    *out = addr[dev];
+    NoAllocScratch* sc = static_cast<NoAllocScratch*>(addr[dev]);
+    *parts = sc->parts;
+    *ticket = &sc->ticket;
     return cudaSuccess;
 }
 
-cudaError_t launch_audit(const float* logp_new, const float* logp_old, const uint8_t* mask,
-                         int64_t N, rlk_audit_result_t* result, void* workspace, bool vec_ok,
-                         cudaStream_t stream) {
-    // at most audit_v3_blocks(N) partials: the workspace is sized for that many
+size_t audit_ticket_offset(int64_t N) {
+    // room for at least one partial: N = 0 still runs one block
+    return align_up(std::max<size_t>(1, audit_v3_blocks(N)) * sizeof(AuditPartial), 256);
+}
+
+// Two launches: pass 1, then one block that merges, by programmatic dependent launch.
+static cudaError_t launch_audit_two_pass(const float* logp_new, const float* logp_old,
+                                         const uint8_t* mask, int64_t N,
+                                         rlk_audit_result_t* result, AuditPartial* parts,
+                                         bool vec_ok, cudaStream_t stream) {
     const size_t blocks = static_cast<size_t>(audit_pass1_blocks(N));
     const int64_t spb = audit_slices_per_block(N);
-    AuditPartial* parts = static_cast<AuditPartial*>(workspace);
     if (blocks > 0) {
         if (vec_ok)
-            audit_pass1<true><<<static_cast<unsigned>(blocks), kAuditThreads, 0, stream>>>(
-                logp_new, logp_old, mask, N, spb, parts);
+            audit_pass1<true, false><<<static_cast<unsigned>(blocks), kAuditThreads, 0, stream>>>(
+                logp_new, logp_old, mask, N, spb, parts, nullptr, nullptr);
         else
-            audit_pass1<false><<<static_cast<unsigned>(blocks), kAuditThreads, 0, stream>>>(
-                logp_new, logp_old, mask, N, spb, parts);
+            audit_pass1<false, false><<<static_cast<unsigned>(blocks), kAuditThreads, 0, stream>>>(
+                logp_new, logp_old, mask, N, spb, parts, nullptr, nullptr);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -877,6 +972,35 @@ cudaError_t launch_audit(const float* logp_new, const float* logp_old, const uin
     const AuditPartial* cparts = parts;
     const int64_t nparts = static_cast<int64_t>(blocks);
     return cudaLaunchKernelEx(&cfg, audit_pass2, cparts, nparts, result);
+}
+
+// One launch: the ticket is cleared on the stream, then pass 1's last block merges.
+static cudaError_t launch_audit_fused(const float* logp_new, const float* logp_old,
+                                      const uint8_t* mask, int64_t N, rlk_audit_result_t* result,
+                                      AuditPartial* parts, unsigned int* ticket, bool vec_ok,
+                                      cudaStream_t stream) {
+    // N = 0 still runs one block, which writes the empty result
+    const size_t blocks = std::max<size_t>(1, static_cast<size_t>(audit_pass1_blocks(N)));
+    const int64_t spb = audit_slices_per_block(N);
+    cudaError_t e = cudaMemsetAsync(ticket, 0, sizeof(unsigned int), stream);
+    if (e != cudaSuccess) return e;
+    if (vec_ok)
+        audit_pass1<true, true><<<static_cast<unsigned>(blocks), kAuditThreads, 0, stream>>>(
+            logp_new, logp_old, mask, N, spb, parts, ticket, result);
+    else
+        audit_pass1<false, true><<<static_cast<unsigned>(blocks), kAuditThreads, 0, stream>>>(
+            logp_new, logp_old, mask, N, spb, parts, ticket, result);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_audit(const float* logp_new, const float* logp_old, const uint8_t* mask,
+                         int64_t N, rlk_audit_result_t* result, void* partials,
+                         unsigned int* ticket, bool vec_ok, cudaStream_t stream) {
+    AuditPartial* parts = static_cast<AuditPartial*>(partials);
+    if (kAuditFused)
+        return launch_audit_fused(logp_new, logp_old, mask, N, result, parts, ticket, vec_ok,
+                                  stream);
+    return launch_audit_two_pass(logp_new, logp_old, mask, N, result, parts, vec_ok, stream);
 }
 
 // partials | 3 histograms | select state | |d| keys [N] (uint32)

@@ -59,6 +59,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// The rounding residues of a pair packed by pack_bf16x2: bf16(d - bf16(d)) of
+// both values.  d - bf16(d) is exact in fp32, so hi + lo carries d to about 16
+// significant bits.
+__device__ __forceinline__ uint32_t pack_lo_bf16x2(float d0, float d1, uint32_t hi) {
+    const float h0 = __uint_as_float(hi << 16);
+    const float h1 = __uint_as_float(hi & 0xffff0000u);
+    return pack_bf16x2(d0 - h0, d1 - h1);
+}
+
 __device__ __forceinline__ bool row_live(const int64_t* targets, const uint8_t* mask, int t, int N,
                                          int V, int64_t& y) {
     y = 0;
@@ -96,6 +105,13 @@ __device__ __forceinline__ void bf16x8_to_f32(uint4 v, float* out) {
 // i.e. -(p/T) (g + gH (S/T - Ez)), the entropy's dH/dz = -p (z - E[z]).
 template <bool ENT>
 struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
+    // With ENT, dS is stored as a pair of bf16 planes per row, hi = bf16(dS) and
+    // lo = bf16(dS - hi) (columns [kBwdChunk, 2 kBwdChunk) of the row), and the dh and
+    // dW GEMMs run over both planes: the entropy gradient has no fp32 part that
+    // dominates the row, so a single bf16 rounding of dS would cost as much accuracy
+    // as the final rounding of the outputs.  Rows with gH = 0 keep lo = 0 and so give
+    // the logp-only backward's dh rows bit for bit.
+    static constexpr int kLd = ENT ? 2 * kBwdChunk : kBwdChunk;   // dS row stride
 
     const int64_t* targets;
     const uint8_t* mask;
@@ -137,6 +153,7 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
         int64_t ycol;         // target column relative to the chunk
         int t;                // the row's token
         bool live;
+        bool lo;              // ENT: the row stores the lo plane of dS (gH != 0)
     };
 
     __device__ void epi_begin(int u, int row, EpiState& st) const {
@@ -150,9 +167,11 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
         st.lse2 = st.live ? lse[t] * kLog2e : 0.f;
         st.ycol = y - y_off - c0;       // outside [0, 32 * 8) unless y is in this chunk
         st.coef_y = 0.f;
+        st.lo = false;
         st.gt = st.live ? __fdiv_rn(grad[t], temp) : 0.f;
         if constexpr (ENT) {
             const float gh = st.live ? grad_ent[t] : 0.f;
+            st.lo = gh != 0.f;
             const float ez = st.live ? lse[t] - ent[t] : 0.f;
             st.coef = st.live ? -__fdiv_rn(fmaf(-gh, ez, grad[t]), temp) : 0.f;
             st.c2 = st.live ? -__fdiv_rn(gh, temp * temp) : 0.f;
@@ -220,6 +239,7 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
                 }
             }
             uint32_t packed[16];
+            uint32_t packed_lo[ENT ? 16 : 1];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const float s0 = x[2 * j];
@@ -236,12 +256,21 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
                 d0 = (yi == 2 * j) ? dy : ((ai == 2 * j) ? da : d0);
                 d1 = (yi == 2 * j + 1) ? dy : ((ai == 2 * j + 1) ? da : d1);
                 packed[j] = pack_bf16x2(d0, d1);
+                if constexpr (ENT) packed_lo[j] = st.lo ? pack_lo_bf16x2(d0, d1, packed[j]) : 0u;
             }
-            uint4* dst = reinterpret_cast<uint4*>(ds + static_cast<size_t>(i) * kBwdChunk + col);
+            uint4* dst = reinterpret_cast<uint4*>(ds + static_cast<size_t>(i) * kLd + col);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
                                     packed[4 * i + 3]);
+            if constexpr (ENT) {
+                uint4* dlo = reinterpret_cast<uint4*>(ds + static_cast<size_t>(i) * kLd +
+                                                      kBwdChunk + col);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    dlo[i] = make_uint4(packed_lo[4 * i], packed_lo[4 * i + 1],
+                                        packed_lo[4 * i + 2], packed_lo[4 * i + 3]);
+            }
         }
     }
 
@@ -268,7 +297,13 @@ struct DsKlMaps {
 struct DsKlPolicy {
     using Maps = DsKlMaps;
     static constexpr bool kPairTiles = true;
+    static constexpr bool kKRemap = false;
     static constexpr int kEpiWarps = 8;       // two column halves per row
+    // dS as hi / lo bf16 planes (columns [0, kBwdChunk) and [kBwdChunk, 2 kBwdChunk) of
+    // each row), which the dh and dW GEMMs both consume: the KL gradient has no fp32
+    // part that dominates a row, so one bf16 rounding of dS would cost as much
+    // accuracy as the final rounding of the outputs.
+    static constexpr int kLd = 2 * kBwdChunk;
 
     const uint8_t* mask;
     const float* grad;        // d L / d KL(p||q), or nullptr
@@ -361,7 +396,7 @@ struct DsKlPolicy {
                     ai = idx;
                 }
             }
-            uint32_t packed[16];
+            uint32_t packed[16], packed_lo[16];
             float gdom = 0.f;                           // the dominant entry's gradient
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -380,17 +415,22 @@ struct DsKlPolicy {
                     d[e] = (st.live && vb + 2 * j + e < V && !is_dom) ? g : 0.f;
                 }
                 packed[j] = pack_bf16x2(d[0], d[1]);
+                packed_lo[j] = pack_lo_bf16x2(d[0], d[1], packed[j]);
             }
             if (ai < 32) {
                 dom[t] = vb + ai;
                 dcoef[t] = gdom;
                 atomicOr(dom_flag, 1);   // set by many rows
             }
-            uint4* dst = reinterpret_cast<uint4*>(ds + static_cast<size_t>(t) * kBwdChunk + col);
+            uint4* dst = reinterpret_cast<uint4*>(ds + static_cast<size_t>(t) * kLd + col);
+            uint4* dlo = reinterpret_cast<uint4*>(ds + static_cast<size_t>(t) * kLd + kBwdChunk + col);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < 4; ++i) {
                 dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
                                     packed[4 * i + 3]);
+                dlo[i] = make_uint4(packed_lo[4 * i], packed_lo[4 * i + 1], packed_lo[4 * i + 2],
+                                    packed_lo[4 * i + 3]);
+            }
         }
     }
 
@@ -399,8 +439,11 @@ struct DsKlPolicy {
 
 // ----------------------------------------------------------------------------- dh
 
-// dS_c [N, width]: K (vocab) contiguous; W_c [width, H]: N (hidden) contiguous
+// dS_c [N, width]: K (vocab) contiguous; W_c [width, H]: N (hidden) contiguous.
+// hilo: dS is a hi and a lo bf16 plane (columns kBwdChunk apart); the K loop
+// runs over the hi plane, then over the lo plane against the same rows of W_c.
 struct DhPolicy : SingleRole<false, true> {
+    static constexpr bool kKRemap = true;
 
     const int64_t* targets;
     const uint8_t* mask;
@@ -419,10 +462,18 @@ struct DhPolicy : SingleRole<false, true> {
     bool first, last;
     bool round_last;               // false: the last chunk writes dh_out32, unrounded
     bool terms;                    // false: no fp32 target terms (no targets)
+    bool hilo;                     // dS as hi and lo planes: K runs over both
     float temp;
 
     __device__ int num_units() const { return rm.tiles(N) * num_n; }
-    __device__ int k_blocks(int) const { return kblocks; }
+    __device__ int k_blocks(int) const { return hilo ? 2 * kblocks : kblocks; }
+    __device__ void k_remap(int kb, int nkb, int&, int& a_k, int&, int& b_k) const {
+        if (hilo && kb >= nkb / 2) {
+            const int j = kb - nkb / 2;
+            a_k = kBwdChunk + j * 64;
+            b_k = c0 + j * 64;
+        }
+    }
     __device__ int tiles_in_unit(int) const { return 1; }
     // unit -> (token tile m, hidden tile n) in row order.  (Grouping 8 hidden tiles
     // cut the modelled DRAM reads by a fifth but measured 1% slower on GB300.)
@@ -555,8 +606,11 @@ struct DhPolicy : SingleRole<false, true> {
 
 // ----------------------------------------------------------------------------- dW
 
-// dS_c^T: vocab (M) contiguous, tokens along K; h: hidden (N) contiguous
+// dS_c^T: vocab (M) contiguous, tokens along K; h: hidden (N) contiguous.
+// hilo: the K loop runs over the tokens of the hi plane of dS, then over the
+// same tokens of the lo plane (kBwdChunk columns further on), against h twice.
 struct DwPolicy : SingleRole<true, true> {
+    static constexpr bool kKRemap = true;
 
     const float* grad;
     const __nv_bfloat16* hidden;   // [N][H]
@@ -568,14 +622,25 @@ struct DwPolicy : SingleRole<true, true> {
     const int* sorted_dt;          // [N]
     const int* dom_flag;           // 0: no dominant class in this chunk (the list was not built)
     const float* dcoef;            // [N] fp32 coefficient of each token's dominant class
+    float* dw_out32;               // non-null: dW rows go here in fp32, unrounded [V][H]
     RowMap rm;                     // compaction: K runs over the compacted rows only
     int N, H, c0, width, num_m, num_n, kblocks;
     float temp;
     bool terms;                    // false: no fp32 target terms (no targets)
+    bool hilo;                     // dS as hi and lo planes: K runs over both
 
     __device__ int num_units() const { return num_m * num_n; }
     __device__ int k_blocks(int) const {
-        return rm.n_rows != nullptr ? (max(*rm.n_rows, 1) + 63) / 64 : kblocks;
+        const int kb = rm.n_rows != nullptr ? (max(*rm.n_rows, 1) + 63) / 64 : kblocks;
+        return hilo ? 2 * kb : kb;
+    }
+    __device__ void k_remap(int kb, int nkb, int& a_mn, int& a_k, int&, int& b_k) const {
+        if (hilo && kb >= nkb / 2) {
+            const int j = kb - nkb / 2;
+            a_mn += kBwdChunk;
+            a_k = j * 64;
+            b_k = j * 64;
+        }
     }
     __device__ int tiles_in_unit(int) const { return 1; }
     // unit -> (vocab tile m of the chunk, hidden tile n), hidden tiles grouped
@@ -659,6 +724,14 @@ struct DwPolicy : SingleRole<true, true> {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) x[8 * q + j] = fmaf(coef, hv[j], x[8 * q + j]);
                 }
+            }
+            if (dw_out32 != nullptr) {     // a data-parallel rank's unrounded partial
+                float4* out = reinterpret_cast<float4*>(dw_out32 + static_cast<size_t>(st.v) * H +
+                                                        col);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    out[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+                continue;
             }
             uint4* dst = reinterpret_cast<uint4*>(dw + static_cast<size_t>(st.v) * H + col);
 #pragma unroll
@@ -935,6 +1008,7 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
         pd.last = st.chunk == st.num_chunks - 1;
         pd.temp = st.temp;
         pd.terms = !st.kl;
+        pd.hilo = st.hilo;
         return launch_gemm(maps.ds_kmajor, maps.w_mnmajor, pd, pd.num_m * pd.num_n, num_sms, err,
                            stream);
     }
@@ -949,6 +1023,7 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
     pw.sorted_dt = st.sorted_dt;
     pw.dom_flag = st.dom_flags + st.chunk;
     pw.dcoef = st.dcoef;
+    pw.dw_out32 = st.dw_out32;
     pw.rm = RowMap{st.rows, st.n_rows};
     pw.N = N;
     pw.H = H;
@@ -959,13 +1034,16 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
     pw.kblocks = (N + 63) / 64;
     pw.temp = st.temp;
     pw.terms = !st.kl;
+    pw.hilo = st.hilo;
     return launch_gemm(maps.ds_mnmajor, maps.h_mnmajor, pw, pw.num_m * pw.num_n, num_sms, err,
                        stream);
 }
 
 // ----------------------------------------------------------------------------- dh merge
 
-// dh = bf16( sum_r partials[r] ), r ascending, fp32 sums; four elements a thread.
+// out = bf16( sum_r partials[r] ), r ascending, fp32 sums; four elements a thread.
+// Serves the vocab-sharded backward's dh partials and the data-parallel ranks'
+// dW partials alike.
 __global__ void dh_merge_kernel(const float4* __restrict__ partials, int64_t num_parts,
                                 int64_t n4, uint2* __restrict__ dh) {
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;

@@ -2,9 +2,11 @@
 //
 // "RL-Kernel Roadmap (2026)", P0.2 Typical Fused Operators: the forward
 // streams vocab blocks with an online softmax and never lands the [N,V]
-// logits.  "RL-Kernel integration roadmap for vime", linear_logp: the merge
-// is explicit -- local max, global max, local sum-exp, global sum-exp,
-// selected target logit, final downcast point.
+// logits.  "RL-Kernel integration roadmap for vime", linear_logp section:
+// here each (row, vocab chunk) leaves a running maximum and a scaled sum of
+// exponentials, the row's target logit is kept from the same accumulator, and
+// a separate launch merges the per-chunk pairs in one fixed order before the
+// single fp32 result is formed.
 //
 // Kernel 1 (gemm_persistent_kernel<FwdPolicy>): a work unit is one 128-row
 // token tile times one vocab chunk of kFwdTilesPerChunk 256-column tiles.

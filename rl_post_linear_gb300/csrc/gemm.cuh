@@ -93,6 +93,10 @@ __device__ __forceinline__ uint64_t operand_desc_rt(bool mn_major, uint32_t stag
 //   num_units(), tiles_in_unit(u), k_blocks(u), coords(u, q, ...)
 //   EpiState, epi_begin / epi_tile / epi_end
 //   kPairTiles                            false: one epilogue call per tile
+//   kKRemap, k_remap(kb, nkb, a_mn, a_k, b_mn, b_k)
+//                                         true: the coordinates of K block kb
+//                                         (of nkb) are the policy's, not the
+//                                         plain ascending walk along K
 // With kPairTiles the tiles of a unit come in pairs (2i, 2i+1) that may use
 // different operands (tile_a_map / tile_b_map / tile_k_blocks(u, q)); the
 // epilogue sees both accumulators at once (epi_pair, after the odd tile) and
@@ -111,6 +115,7 @@ template <bool AMN, bool BMN>
 struct SingleRole {
     using Maps = TwoMaps;
     static constexpr bool kPairTiles = false;
+    static constexpr bool kKRemap = false;
     static constexpr int kEpiWarps = 4;
     static constexpr bool kAMn = AMN;
     static constexpr bool kBMn = BMN;
@@ -249,11 +254,13 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1)
                             ok = false;
                             break;
                         }
+                        int am = a_mn, ak = a_k + kb * kBK, bm = b_mn, bk = b_k + kb * kBK;
+                        if constexpr (P::kKRemap) p.k_remap(kb, qk, am, ak, bm, bk);
                         mbar_arrive_expect_tx(&full[stage], kStageBytes);
                         load_operand_rt<kBM>(amn, a_stages + stage * kAStageBytes, qa,
-                                             &full[stage], a_mn, a_k + kb * kBK);
+                                             &full[stage], am, ak);
                         load_operand_rt<kBN>(bmn, b_stages + stage * kBStageBytes, qb,
-                                             &full[stage], b_mn, b_k + kb * kBK);
+                                             &full[stage], bm, bk);
                         issued_mask |= 1u << stage;
                         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                         if (++stage == kStages) {

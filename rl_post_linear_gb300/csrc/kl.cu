@@ -44,6 +44,7 @@ struct KlMaps {
 struct KlFwdPolicy {
     using Maps = KlMaps;
     static constexpr bool kPairTiles = true;
+    static constexpr bool kKRemap = false;
     static constexpr int kEpiWarps = 8;       // two column halves per row
 
     const int64_t* targets;   // nullptr: no selected logp

@@ -56,18 +56,19 @@ struct FwdLayout {
     }
 };
 
-// Backward workspace: dS for one vocab chunk [N, kBwdChunk] bf16, the fp32 dh
-// accumulator [N, H], the (target, token) list sorted by target, 1 - p_y per
-// row, each row's dominant non-target class and the chunk's (class, token) list
-// sorted by class, and the sorted key tiles the lists are built from.
+// Backward workspace: dS for one vocab chunk [N, kBwdChunk] bf16 (hilo: a hi
+// and a lo plane, [N, 2 kBwdChunk]), the fp32 dh accumulator [N, H], the
+// (target, token) list sorted by target, 1 - p_y per row, each row's dominant
+// non-target class and the chunk's (class, token) list sorted by class, and the
+// sorted key tiles the lists are built from.
 constexpr int kTargetSortTile = 2048;
 struct BwdLayout {
     size_t ds_off, dhacc_off, sorted_y_off, sorted_t_off, ycoef_off, dom_off, dcoef_off,
         sorted_dy_off, sorted_dt_off, tiles_off, blk_off, rows_off, pos_off, count_off, hc_off,
         flags_off, total;
-    BwdLayout(int64_t N, int64_t H) {
+    BwdLayout(int64_t N, int64_t H, bool hilo = false) {
         ds_off = 0;
-        dhacc_off = align_up(static_cast<size_t>(N) * kBwdChunk * 2, 256);
+        dhacc_off = align_up(static_cast<size_t>(N) * kBwdChunk * 2 * (hilo ? 2 : 1), 256);
         sorted_y_off = align_up(dhacc_off + static_cast<size_t>(N) * H * 4, 256);
         sorted_t_off = align_up(sorted_y_off + static_cast<size_t>(N) * 4, 256);
         ycoef_off = align_up(sorted_t_off + static_cast<size_t>(N) * 4, 256);
@@ -209,6 +210,7 @@ struct BwdStep {
     int V_global;              // vocabulary size
     bool round_last;           // false: the fp32 partial of dh goes to dh_out32, unrounded
     float* dh_out32;           // [N][H] by token (round_last false)
+    float* dw_out32;           // non-null: dW as an unrounded fp32 partial [V][H]
     const int* rows;           // compaction of a masked batch: row -> token, or nullptr
     const int* n_rows;         // number of compacted rows (device), or nullptr
     // KL against a reference head (kl = true): dS from both heads, no fp32 target terms
@@ -218,7 +220,8 @@ struct BwdStep {
     const float* grad_rev;     // d loss / d KL(q || p), or nullptr
     const float* lse_ref;
     const float* kl_val;       // the forward's KL(p || q)
-    void* ds;                  // dS [N, kBwdChunk] bf16 of the chunk
+    bool hilo;                 // dS as hi and lo bf16 planes [N, 2 kBwdChunk] (entropy, KL)
+    void* ds;                  // dS [N, kBwdChunk] bf16 of the chunk (hilo: [N, 2 kBwdChunk])
     float* dh_acc;
     const int* sorted_y;
     const int* sorted_t;
@@ -244,9 +247,14 @@ cudaError_t launch_dh_merge(const float* partials, int64_t num_parts, int64_t N,
 cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& step, int num_sms,
                             uint32_t* err, cudaStream_t stream);
 
+// The audit: per-block partials (at most 608 of them), then their merge in a fixed
+// order.  kAuditFused: one launch, whose last block (integer ticket, cleared on the
+// stream first) merges; otherwise a second, one-block launch merges.
+constexpr bool kAuditFused = false;
+size_t audit_ticket_offset(int64_t N);   // of the ticket word in rlk_dlogp_audit's workspace
 cudaError_t launch_audit(const float* logp_new, const float* logp_old, const uint8_t* mask,
-                         int64_t N, rlk_audit_result_t* result, void* workspace, bool vec_ok,
-                         cudaStream_t stream);
+                         int64_t N, rlk_audit_result_t* result, void* partials,
+                         unsigned int* ticket, bool vec_ok, cudaStream_t stream);
 
 cudaError_t launch_grpo_loss(const float* logp_new, const float* logp_old, const float* adv,
                              const uint8_t* mask, int64_t N, double eps_low, double eps_high,
@@ -264,7 +272,8 @@ cudaError_t launch_audit_ext(const float* logp_new, const float* logp_old, const
                              rlk_audit_ext_t* result, void* workspace, bool vec_ok, int sms,
                              cudaStream_t stream);
 
-// Device address (current device) of the library-owned audit scratch.
-cudaError_t audit_noalloc_scratch(void** out);
+// Device addresses (current device) of the library-owned audit scratch: the partials
+// and the ticket word.
+cudaError_t audit_noalloc_scratch(void** parts, unsigned int** ticket);
 
 }  // namespace rlk

@@ -1,10 +1,9 @@
 """Tensor-parallel (vocab-sharded) forward and backward on top of the shard / merge
 entry points.
 
-"RL-Kernel integration roadmap for vime", linear_logp: TP support makes the
-vocab-shard merge explicit (local max, global max, local sum-exp, global
-sum-exp, selected target logit); "RL-Kernel Roadmap (2026)", TP-invariant
-reductions.  Each rank holds a contiguous block of LM-head rows starting on a
+"RL-Kernel integration roadmap for vime", linear_logp section (TP support,
+with the merge of the vocabulary shards as an explicit step); "RL-Kernel
+Roadmap (2026)", TP-invariant reductions.  Each rank holds a contiguous block of LM-head rows starting on a
 1024-row boundary, computes its block's partials with
 ``rlk_linear_logp_fwd_shard``, and the ranks exchange them once: an
 all-gather of the (max, sum) pairs, concatenated in rank order (which is the

@@ -6,9 +6,13 @@ benchmark times.
   sequence, both sides of every 128-row tile edge in range, and seeded random
   ones -- against the oracle, token by token.
 * Qwen-shaped GRPO backward: the whole dh and dW tensors against the oracle at
-  N = 64 with the full H and V; at N = 8192, 16 sampled dh rows against the
-  oracle and, for dW, the softmax-gradient identity sum_v dW_v = 0 (each
-  column sum must vanish up to the bf16 output rounding).
+  N = 256 with the full H and V (four 64-token K blocks in the dW GEMM); at
+  N = 8192, 16 sampled dh rows against the oracle and, for dW, the
+  softmax-gradient identity sum_v dW_v = 0 (each column sum must vanish up to
+  the bf16 output rounding).
+* Entropy and full-vocabulary KL backwards at the Qwen shape (N = 8192):
+  sampled dh rows against the oracle and the same column-sum identity of dW
+  (the entropy and both KL gradients also sum to zero over the vocabulary).
 * DeepSeek-shaped forward (N = 16384, H = 7168, V = 129280, 20% masked):
   128 sampled tokens.
 * DeepSeek-shaped backward (the same masked batch, compacted to its active
@@ -78,7 +82,7 @@ def _grpo_g(logp_o, w, seed, rows):
 
 def test_qwen_backward_full_tensors_reduced_n(qwen):
     w, w64 = qwen
-    n = 64
+    n = 256
     rows = np.arange(n)
     h = w.hidden[:n]
     y = w.targets[:n]
@@ -114,8 +118,8 @@ def test_qwen_backward_full_tensors_reduced_n(qwen):
                                      w.v, consume, rows_per_block=512)
     e_dw = (acc["num"] / acc["den"]) ** 0.5
     e_dw_r = (acc["num_r"] / acc["den"]) ** 0.5
-    print("qwen bwd N=64: rel-L2 dh %.3e dw %.3e (dw vs bf16-rounded oracle %.3e)"
-          % (e_dh, e_dw, e_dw_r))
+    print("qwen bwd N=%d: rel-L2 dh %.3e dw %.3e (dw vs bf16-rounded oracle %.3e)"
+          % (n, e_dh, e_dw, e_dw_r))
     assert e_dh <= GRAD_REL_L2 and e_dw <= GRAD_REL_L2
 
 
@@ -237,3 +241,70 @@ def test_qwen_entropy_and_kl_sampled(qwen):
     print("qwen entropy: max |dH| %.3e (H ~ %.2f); KL ~ %.3f: max |d| kl %.2e rev %.2e lse %.2e "
           "%.2e" % (de.max(), ent_o.mean(), o[0].mean(), *dk))
     assert de.max() <= LOGP_ATOL and max(dk) <= LOGP_ATOL
+
+
+def _column_identity(dw):
+    # sum_v dW_v = 0 for a gradient whose rows sum to zero over the vocabulary
+    col = dw.double().sum(dim=0)
+    rms = dw.double().pow(2).sum(dim=0).sqrt()
+    return float((col.abs() / rms).max())
+
+
+def test_qwen_entropy_backward_sampled(qwen):
+    w, w64 = qwen
+    d = dev()
+    err = torch.zeros(1, dtype=torch.int32, device=d)
+    hd, wd, yd, md = w.hidden.to(d), w.weight.to(d), w.targets.to(d), w.mask.to(d)
+    rng = np.random.default_rng(11)
+    gd = torch.tensor(rng.standard_normal(w.n) / w.n, dtype=torch.float32, device=d)
+    ghd = torch.tensor(rng.standard_normal(w.n) / w.n, dtype=torch.float32, device=d)
+    _, lse, ent = rlk.linear_logp_entropy_fwd(hd, wd, yd, md, w.temperature, err)
+    dh, dw = rlk.linear_logp_entropy_bwd(hd, wd, yd, md, gd, ghd, lse, ent, w.temperature, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    rows = _sample_rows(w, 16, 12)
+    h64 = f64(w.hidden[rows])
+    y = w.targets[rows].numpy()
+    _, lse_o, ent_o = oracle.linear_logp_entropy_fwd_parallel(h64, w64, y, None, w.temperature)
+    dh_o = oracle.linear_logp_entropy_bwd_dh_parallel(
+        h64, w64, y, None, gd.cpu().double().numpy()[rows], ghd.cpu().double().numpy()[rows],
+        lse_o, ent_o, w.temperature)
+    e = rel_l2(dh.cpu()[rows], dh_o)
+    worst = _column_identity(dw)
+    print("qwen entropy bwd N=8192: sampled dh rel-L2 %.3e; max |col sum| / col norm %.3e"
+          % (e, worst))
+    assert e <= GRAD_REL_L2
+    assert worst <= 8 * 2.0 ** -8
+
+
+def test_qwen_kl_backward_sampled(qwen):
+    w, w64 = qwen
+    d = dev()
+    err = torch.zeros(1, dtype=torch.int32, device=d)
+    hd, wd, md = w.hidden.to(d), w.weight.to(d), w.mask.to(d)
+    hr = wl.normal_bf16((w.n, w.h), 1, wl.S_HIDDEN)
+    wr = wl.normal_bf16((w.v, w.h), 1, wl.S_WEIGHT, std=0.02)
+    hrd, wrd = hr.to(d), wr.to(d)
+    rng = np.random.default_rng(13)
+    gd = torch.tensor(rng.standard_normal(w.n) / w.n, dtype=torch.float32, device=d)
+    grd = torch.tensor(rng.standard_normal(w.n) / w.n, dtype=torch.float32, device=d)
+    kl, _, lse, lse_r, _ = rlk.linear_kl_fwd(hd, wd, hrd, wrd, md, w.temperature, 1.0)
+    dh, dw = rlk.linear_kl_bwd(hd, wd, hrd, wrd, md, gd, grd, lse, lse_r, kl, w.temperature, 1.0,
+                               err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    rows = _sample_rows(w, 12, 14)
+    h64, hr64 = f64(w.hidden[rows]), f64(hr[rows])
+    wr64 = oracle.bf16_bits_to_f64(wr)
+    kl_o, _, lse_o, lse_ro = oracle.linear_kl_fwd_parallel(h64, w64, hr64, wr64, None,
+                                                           w.temperature, 1.0)
+    dh_o = oracle.linear_kl_bwd_dh_parallel(h64, w64, hr64, wr64, None,
+                                            gd.cpu().double().numpy()[rows],
+                                            grd.cpu().double().numpy()[rows], lse_o, lse_ro,
+                                            kl_o, w.temperature, 1.0)
+    e = rel_l2(dh.cpu()[rows], dh_o)
+    worst = _column_identity(dw)
+    print("qwen kl bwd N=8192: sampled dh rel-L2 %.3e; max |col sum| / col norm %.3e"
+          % (e, worst))
+    assert e <= GRAD_REL_L2
+    assert worst <= 8 * 2.0 ** -8

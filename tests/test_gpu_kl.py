@@ -1,7 +1,7 @@
 """Full-vocabulary KL of the policy head against a reference head ("RL-Kernel
 Roadmap (2026)", backlog: chunked full-vocab KL / distillation KL fused with
 lm_head, forward and reverse KL), forward and backward, against the fp64
-oracle.  Backward: relative L2 of dh and dW within 2.5e-3 (derived below),
+oracle.  Backward: relative L2 of dh and dW within the 2e-3 gradient contract,
 bitwise run to run, dh rows bitwise batch invariant, and the autograd
 wrapper gives the entry point's result.
 
@@ -18,15 +18,15 @@ import torch
 import oracle
 import rl_post_linear_gb300 as rlk
 import workloads as wl
-from helpers import LOGP_ATOL, dev, f64, same_bits
+from helpers import GRAD_REL_L2, LOGP_ATOL, dev, f64, same_bits
 
 pytestmark = pytest.mark.gpu
 
-# The KL gradient has no exact fp32 part like the logp gradient's target entry: apart from the
-# entry of a dominant policy class (kept in fp32), all of it passes through the bf16 dS and then
-# the bf16 output, two roundings of about 1.66e-3 relative L2 each for these tensors:
-# sqrt(2) * 1.66e-3 = 2.35e-3 (the same derivation as the entropy gradient's).
-KL_GRAD_REL_L2 = 2.5e-3
+# The KL gradient has no exact fp32 part like the logp gradient's target entry.  Apart from the
+# entry of a dominant policy class (kept in fp32), it passes through dS kept as hi and lo bf16
+# planes (about 16 significant bits together), so the final bf16 rounding of the outputs (about
+# 1.66e-3 relative L2) is the only one of size: the gradient contract's 2e-3 applies.
+KL_GRAD_REL_L2 = GRAD_REL_L2
 
 
 def _heads(n, h, hr, v, seed, std=0.05, std_r=0.05, active=0.85):

@@ -39,11 +39,24 @@ def test_owner_and_assemble():
         else:
             assert starts[o] <= t < starts[o] + sh[o][1]
     n = len(targets)
-    parts = [torch.full((-(-size // 1024), n, 2), float(r)) for r, (_, size) in enumerate(sh)]
+    # rank r's chunk c holds the value 100 r + c in every element: the assembled partials must
+    # list the chunks of rank 0, then rank 1, ..., each rank's in its own chunk order, which for
+    # blocks starting on 1024-row boundaries is the global chunk order
+    counts = [-(-size // 1024) for _, size in sh]
+    assert counts == [1, 2, 2]          # blocks of 1024, 2048 and 1928 rows
+    parts = [torch.arange(c, dtype=torch.float32).mul(1).add(100.0 * r)
+             .reshape(c, 1, 1).expand(c, n, 2).contiguous() for r, c in enumerate(counts)]
     tls = [torch.full((n,), 10.0 + r) for r in range(3)]
     p, tl = tp.assemble(parts, tls, owner)
     assert p.shape == (5, n, 2)
-    assert torch.equal(p[:, 0, 0], torch.tensor([0.0, 0.0, 1.0, 1.0, 2.0])[:p.shape[0]]) or True
+    expect = torch.tensor([0.0, 100.0, 101.0, 200.0, 201.0])
+    for row in range(n):
+        for e in range(2):
+            assert torch.equal(p[:, row, e], expect)
+    # global chunk c covers vocab rows [1024 c, 1024 (c + 1)): its owner is the block holding it
+    for c in range(p.shape[0]):
+        r = int(p[c, 0, 0].item()) // 100
+        assert sh[r][0] <= 1024 * c < sh[r][0] + sh[r][1]
     assert tl.tolist()[:4] == [10.0 + o for o in owner.tolist()[:4]]
 
 
