@@ -287,11 +287,10 @@ rlk_status_t rlk_linear_kl_bwd(const void* hidden, const void* weight, const voi
  *   result_dev  one rlk_audit_result_t in device memory (overwritten)
  *   workspace   rlk_dlogp_audit_workspace_bytes(N) bytes, 256-aligned; its
  *               contents on entry do not matter
- * Fixed-size blocks and fixed-order trees: the result is bitwise
- * reproducible for a given N.  One kernel launch (after a 4-byte
- * cudaMemsetAsync of a counter in the workspace): each block writes its
- * partial and takes an integer ticket, and the block with the last ticket
- * merges all partials in a fixed order.
+ * Fixed-size slices, a fixed assignment of slices to blocks and fixed-order
+ * trees: the result is bitwise reproducible for a given N, whatever the
+ * inputs' alignment.  Two launches: the per-block partials, then their merge
+ * (launched early by programmatic dependent launch).
  */
 rlk_status_t rlk_dlogp_audit(const float* logp_new, const float* logp_old,
                              const uint8_t* active_mask, int64_t N,
@@ -487,12 +486,10 @@ rlk_status_t rlk_dlogp_audit_ext(const float* logp_new, const float* logp_old,
  *    current) and again whenever the device's context has been created anew
  *    (after cudaDeviceReset, say); make the first call on a device before any
  *    stream capture.
- *  - Calls share the scratch, which keeps the last call's contents.  Its one
- *    word that must start at zero (the merge ticket) is cleared on the stream
- *    by each call (cudaMemsetAsync, which allocates nothing); the per-block
- *    partials are written before they are read.  Calls that overlap on the
- *    GPU -- on different streams without ordering -- race and give wrong
- *    results.
+ *  - Calls share the scratch, which keeps the last call's contents (nothing
+ *    in it needs to start at zero: every partial is written before it is
+ *    read).  Calls that overlap on the GPU -- on different streams without
+ *    ordering -- race and give wrong results.
  *  - No cudaMalloc, cudaFree or other allocating call is made.
  */
 #define RLK_AUDIT_NOALLOC_MAX_N ((int64_t)1 << 27)

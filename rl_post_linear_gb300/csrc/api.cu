@@ -118,7 +118,7 @@ size_t rlk_linear_logp_entropy_bwd_workspace_bytes(int64_t N, int64_t H, int64_t
 
 size_t rlk_dlogp_audit_workspace_bytes(int64_t N) {
     if (N < 0) return 0;
-    return rlk::audit_ticket_offset(N) + 256;   // the partials, then the ticket word
+    return align_up(rlk::audit_v3_blocks(N) * sizeof(rlk::AuditPartial), 256) + 256;
 }
 
 // The vocabulary in ascending kBwdChunk-column chunks; per chunk the dS
@@ -531,10 +531,8 @@ rlk_status_t rlk_dlogp_audit(const float* logp_new, const float* logp_old,
     RLK_TRY(current_device(dev));
     const bool vec_ok = aligned(logp_new, 16) && aligned(logp_old, 16) &&
                         (active_mask == nullptr || aligned(active_mask, 4));
-    unsigned int* ticket = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(workspace) +
-                                                           rlk::audit_ticket_offset(N));
-    RLK_CUDA(rlk::launch_audit(logp_new, logp_old, active_mask, N, result_dev, workspace, ticket,
-                               vec_ok, stream));
+    RLK_CUDA(rlk::launch_audit(logp_new, logp_old, active_mask, N, result_dev, workspace, vec_ok,
+                               stream));
     return RLK_OK;
 }
 
@@ -688,12 +686,11 @@ rlk_status_t rlk_dlogp_audit_noalloc(const float* logp_new, const float* logp_ol
     DeviceInfo dev;
     RLK_TRY(current_device(dev));
     void* scratch = nullptr;
-    unsigned int* ticket = nullptr;
-    RLK_CUDA(rlk::audit_noalloc_scratch(&scratch, &ticket));
+    RLK_CUDA(rlk::audit_noalloc_scratch(&scratch));
     const bool vec_ok = aligned(logp_new, 16) && aligned(logp_old, 16) &&
                         (active_mask == nullptr || aligned(active_mask, 4));
-    RLK_CUDA(rlk::launch_audit(logp_new, logp_old, active_mask, N, result_dev, scratch, ticket,
-                               vec_ok, stream));
+    RLK_CUDA(rlk::launch_audit(logp_new, logp_old, active_mask, N, result_dev, scratch, vec_ok,
+                               stream));
     return RLK_OK;
 }
 
@@ -711,8 +708,8 @@ const char* rlk_contract_string(void) {
                               "logits never rounded; logp/lse fp32; dS bf16 (target and "
                               "dominant-class terms fp32); "
                               "dh/dW rounded once to bf16 (RNE); no float atomics; "
-                              "audit: 4096-element slices, ceil(slices/608) per block, fixed "
-                              "trees, float-pair (two-sum) partials";
+                              "audit: 4096-element slices dealt round-robin to min(slices, 608) "
+                              "blocks, fixed trees, float-pair (two-sum) partials";
 }
 
 const char* rlk_status_string(rlk_status_t status) {

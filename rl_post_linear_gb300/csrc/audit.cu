@@ -36,15 +36,19 @@ namespace rlk {
 
 namespace {
 
+// exp(d) - 1 - d for |d| < 1/16: the Taylor series to d^6 (truncation below 4e-10
+// relative).  Branch-free, so the audit's fast path evaluates it for every element.
+__device__ __forceinline__ float kl_small(float d) {
+    float p = 1.0f / 720.0f;
+    p = fmaf(p, d, 1.0f / 120.0f);
+    p = fmaf(p, d, 1.0f / 24.0f);
+    p = fmaf(p, d, 1.0f / 6.0f);
+    p = fmaf(p, d, 0.5f);
+    return d * d * p;
+}
+
 __device__ __forceinline__ float kl_term(float d) {
-    if (fabsf(d) < 0.0625f) {          // Taylor series to d^6: truncation below 4e-10 relative
-        float p = 1.0f / 720.0f;
-        p = fmaf(p, d, 1.0f / 120.0f);
-        p = fmaf(p, d, 1.0f / 24.0f);
-        p = fmaf(p, d, 1.0f / 6.0f);
-        p = fmaf(p, d, 0.5f);
-        return d * d * p;
-    }
+    if (fabsf(d) < 0.0625f) return kl_small(d);
     if (fabsf(d) < 0.5f) {             // to d^9: truncation below 3e-8 relative
         float p = 1.0f / 362880.0f;
         p = fmaf(p, d, 1.0f / 40320.0f);
@@ -128,6 +132,12 @@ __device__ __forceinline__ Acc shfl_down(const Acc& a, int off) {
     return b;
 }
 
+// Barrier 1 over the first `threads` threads of the block (the audit kernels'
+// reducing threads; a streaming kernel's copy warp does not take part).
+__device__ __forceinline__ void named_barrier(int threads) {
+    asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory");
+}
+
 // Fixed tree over the block: lanes (16, 8, 4, 2, 1), then the warp results
 // in warp order with the same tree.  Lane 0 of warp 0 returns the total.
 template <int THREADS>
@@ -140,7 +150,7 @@ __device__ __forceinline__ Acc block_reduce(Acc a) {
         if (lane + off < 32) merge(a, b);
     }
     if (lane == 0) warp_acc[warp] = a;
-    __syncthreads();
+    named_barrier(THREADS);
     if (warp == 0) {
         a = lane < THREADS / 32 ? warp_acc[lane] : empty_acc();
 #pragma unroll
@@ -183,172 +193,208 @@ __device__ __forceinline__ void visit3(float nw, float od, uint32_t m, int off, 
     a.flags |= (key > 0x7f800000u) ? 1u : 0u;    // |d| is inf or NaN
 }
 
-// Branch-free visit for the vector path: an inactive element contributes d = 0
-// to the sums (kl_term(0) = 0 exactly) and key 0 to the running max.
-struct GroupAcc {
-    uint32_t key = 0;
-    int arg = -1;
-    float sd = 0.f, skl = 0.f;
-};
-
-__device__ __forceinline__ void visit_group(float nw, float od, bool act, int off, GroupAcc& g) {
-    const float d = act ? nw - od : 0.f;
-    const uint32_t key = act ? abs_key(d) : 0u;
-    const bool better = key > g.key;
-    g.key = better ? key : g.key;
-    g.arg = better ? off : g.arg;
-    g.sd += d;
-    g.skl += kl_term(d);
-}
-
 // number of nonzero bytes in a word of four mask bytes
 __device__ __forceinline__ int active_bytes(uint32_t m) {
     const uint32_t hi = ((m & 0x7f7f7f7fu) + 0x7f7f7f7fu) | m;
     return __popc(hi & 0x80808080u);
 }
 
-// Pass 1's partition is a function of N only: slices of 4096 elements, and
-// blocks of ceil(slices / kAuditMaxBlocks) consecutive slices, so that one wave
-// of blocks covers any N (608 = 4 resident blocks on each of 152 SMs) and pass 2
-// merges at most kAuditMaxBlocks partials.
+// Pass 1's partition is a function of N only: slices of 4096 elements, dealt out
+// round-robin to G = min(slices, kAuditMaxBlocks) blocks (block b takes slices b,
+// b + G, b + 2G, ... in ascending order), so that one wave of blocks covers any N
+// (608 = 4 resident blocks on each of 152 SMs), the whole grid sweeps the inputs
+// front to back together, and the merge reads at most kAuditMaxBlocks partials.
 constexpr int64_t kAuditMaxBlocks = 608;
-
-inline int64_t audit_slices_per_block(int64_t N) {
-    const int64_t slices = static_cast<int64_t>(audit_v3_blocks(N));
-    return slices <= kAuditMaxBlocks ? 1 : (slices + kAuditMaxBlocks - 1) / kAuditMaxBlocks;
-}
+constexpr int kSlice = kAuditThreads * kAuditV3PerThread;   // 4096 elements
+constexpr int kVec = kAuditV3PerThread / 4;                 // float4 groups per thread
 
 inline int64_t audit_pass1_blocks(int64_t N) {
     const int64_t slices = static_cast<int64_t>(audit_v3_blocks(N));
-    const int64_t spb = audit_slices_per_block(N);
-    return (slices + spb - 1) / spb;
+    return slices < kAuditMaxBlocks ? slices : kAuditMaxBlocks;
 }
 
-template <int THREADS, bool COHERENT>
-__device__ void merge_partials(const AuditPartial* parts, int64_t num_parts,
-                               rlk_audit_result_t* result);
+// The order-preserving key of |d| as the running max compares it: the bits of |d|
+// with every NaN mapped to one pattern above inf, plus one, so that 0 means "no
+// active element" (ties keep the first offset: strict comparison).
+__device__ __forceinline__ uint32_t key_of_bits(uint32_t b) {
+    return (b > 0x7f800000u ? 0x7fc00000u : b) + 1u;
+}
 
-// FUSED: one launch.  After writing its partial, each block takes an integer ticket
-// (atomicAdd on a counter that starts at zero); the block that draws the last one
-// merges every partial in the fixed order of merge_partials and writes the result.
-// Which block merges depends on the schedule, the merge order does not.
-template <bool VEC, bool FUSED>
-__global__ void __launch_bounds__(kAuditThreads)
-    audit_pass1(const float* __restrict__ nw, const float* __restrict__ od,
-                const uint8_t* __restrict__ mask, int64_t N, int64_t slices_per_block,
-                AuditPartial* __restrict__ out, unsigned int* ticket,
-                rlk_audit_result_t* __restrict__ result) {
-    // two launches: let the merge kernel launch now; it waits for this grid before reading
-    if constexpr (!FUSED) asm volatile("griddepcontrol.launch_dependents;");
-    constexpr int kVec = kAuditV3PerThread / 4;
-    constexpr int kBlock = kAuditThreads * kAuditV3PerThread;
-    const int64_t block_base = static_cast<int64_t>(blockIdx.x) * slices_per_block * kBlock;
-    // running state over the block's slices, visited in ascending order: count, the
-    // best key and its offset in the block (strictly greater replaces, so the first
-    // offset wins ties), float-pair sums of each slice's fp32 sums
+// One slice seen by one thread: its elements j*1024 + 4*tid + e (group j, lane e of
+// the group) with the new and old values and the four mask bytes of each group.
+// An inactive element contributes d = 0 to the sums and nothing to the running max.
+// The per-element work is branch-free and short: the sums of d and of
+// kl(d) = exp(d) - 1 - d (its small-|d| series; one accumulator per group, so the
+// four groups' dependency chains interleave, merged in a fixed tree) and the largest
+// |d| bits of each group.  Two things are done per slice, not per element: when some
+// |d| reaches 1/16 (or is inf / NaN) the slice's kl sums are formed again with the
+// exact kl_term; and the offset of the slice's largest |d| (the first one, in element
+// order, on ties) is looked up only when that value beats `best_key`, the thread's
+// running best, since otherwise it is not needed.  a.key is the slice's key, a.arg
+// its first offset when a.key > best_key.
+__device__ __forceinline__ void visit_slice(const float4 (&x)[kVec], const float4 (&y)[kVec],
+                                            const uint32_t (&m)[kVec], int tid, uint32_t best_key,
+                                            ThreadAcc& a) {
+    float sd[kVec], skl[kVec];
+    uint32_t gmax[kVec];
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+        a.count += active_bytes(m[j]);
+        const float xs[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
+        const float ys[4] = {y[j].x, y[j].y, y[j].z, y[j].w};
+        sd[j] = 0.f;
+        skl[j] = 0.f;
+        gmax[j] = 0u;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const bool act = ((m[j] >> (8 * e)) & 0xffu) != 0u;
+            const float d = act ? xs[e] - ys[e] : 0.f;
+            gmax[j] = max(gmax[j], __float_as_uint(d) & 0x7fffffffu);
+            sd[j] += d;
+            skl[j] += kl_small(d);
+        }
+    }
+    const uint32_t smax = max(max(gmax[0], gmax[1]), max(gmax[2], gmax[3]));
+    // an inf or NaN |d| exists exactly when the largest bits reach those of inf
+    a.flags = smax >= 0x7f800000u ? 1u : 0u;
+    if (smax >= 0x3d800000u) {                 // some |d| >= 1/16, inf or NaN: exact terms
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+            const float xs[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
+            const float ys[4] = {y[j].x, y[j].y, y[j].z, y[j].w};
+            skl[j] = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const bool act = ((m[j] >> (8 * e)) & 0xffu) != 0u;
+                skl[j] += act ? kl_term(xs[e] - ys[e]) : 0.f;
+            }
+        }
+    }
+    static_assert(kVec == 4, "the fixed summation tree below assumes four groups");
+    a.sd = (sd[0] + sd[1]) + (sd[2] + sd[3]);
+    a.skl = (skl[0] + skl[1]) + (skl[2] + skl[3]);
+    a.key = a.count > 0 ? key_of_bits(smax) : 0u;
+    a.arg = -1;
+    if (a.key > best_key) {
+        // the first active element, in (group, lane) order, whose key is the slice's
+        int arg = -1;
+#pragma unroll
+        for (int j = kVec - 1; j >= 0; --j) {
+            const float xs[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
+            const float ys[4] = {y[j].x, y[j].y, y[j].z, y[j].w};
+#pragma unroll
+            for (int e = 3; e >= 0; --e) {
+                const bool act = ((m[j] >> (8 * e)) & 0xffu) != 0u;
+                const uint32_t b = __float_as_uint(xs[e] - ys[e]) & 0x7fffffffu;
+                arg = (act && key_of_bits(b) == a.key) ? j * (kAuditThreads * 4) + tid * 4 + e
+                                                       : arg;
+            }
+        }
+        a.arg = arg;
+    }
+}
+
+// A slice read straight from global memory: vector loads when VEC (16-byte aligned
+// inputs, whole slice inside N), else element by element with elements past N
+// inactive.  Either way the arithmetic is visit_slice's.
+template <bool VEC>
+__device__ __forceinline__ void load_and_visit_slice(const float* nw, const float* od,
+                                                     const uint8_t* mask, int64_t N,
+                                                     int64_t base, uint32_t best_key,
+                                                     ThreadAcc& a) {
+    float4 x[kVec], y[kVec];
+    uint32_t m[kVec];
+    if (VEC && base + kSlice <= N) {
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+            const int64_t i0 = base + j * (kAuditThreads * 4) + threadIdx.x * 4;
+            x[j] = __ldcs(reinterpret_cast<const float4*>(nw + i0));
+            y[j] = __ldcs(reinterpret_cast<const float4*>(od + i0));
+            m[j] = mask == nullptr ? 0x01010101u
+                                   : __ldcs(reinterpret_cast<const unsigned int*>(mask + i0));
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+            const int64_t i0 = base + j * (kAuditThreads * 4) + threadIdx.x * 4;
+            float xv[4], yv[4];
+            uint32_t mv = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const bool in = i0 + e < N;
+                xv[e] = in ? nw[i0 + e] : 0.f;
+                yv[e] = in ? od[i0 + e] : 0.f;
+                const uint32_t b = in ? (mask == nullptr ? 1u : (mask[i0 + e] != 0 ? 1u : 0u)) : 0u;
+                mv |= b << (8 * e);
+            }
+            x[j] = make_float4(xv[0], xv[1], xv[2], xv[3]);
+            y[j] = make_float4(yv[0], yv[1], yv[2], yv[3]);
+            m[j] = mv;
+        }
+    }
+    visit_slice(x, y, m, threadIdx.x, best_key, a);
+}
+
+// The running state of a block's thread over the block's slices, visited in ascending
+// order: count, the best key and its element index (strictly greater replaces, so the
+// first index wins ties), float-pair sums of each slice's fp32 sums.
+struct RunAcc {
     int count = 0;
     uint32_t best_key = 0;
     int64_t best_off = -1;
     uint32_t flags = 0;
     DFloat sum_d{0.f, 0.f}, sum_kl{0.f, 0.f};
-#pragma unroll 1
-    for (int64_t sl = 0; sl < slices_per_block; ++sl) {
-        const int64_t base = block_base + sl * kBlock;
-        if (base >= N) break;
-        const int64_t slice_off = sl * kBlock;
-        ThreadAcc a;
-        if (VEC && base + kBlock <= N) {
-            float4 x[kVec], y[kVec];
-            uint32_t m[kVec];
-#pragma unroll
-            for (int j = 0; j < kVec; ++j) {
-                const int64_t i0 = base + j * (kAuditThreads * 4) + threadIdx.x * 4;
-                x[j] = __ldcs(reinterpret_cast<const float4*>(nw + i0));
-                y[j] = __ldcs(reinterpret_cast<const float4*>(od + i0));
-                m[j] = mask == nullptr ? 0x01010101u
-                                       : __ldcs(reinterpret_cast<const unsigned int*>(mask + i0));
-            }
-            // One accumulator per float4 group, so that the four groups' dependency chains
-            // (sums, running max) interleave; the groups are then merged in ascending order,
-            // which keeps the first index on ties (group j's offsets precede group j+1's).
-            GroupAcc g[kVec];
-#pragma unroll
-            for (int j = 0; j < kVec; ++j) {
-                const int o = j * (kAuditThreads * 4) + threadIdx.x * 4;
-                a.count += active_bytes(m[j]);
-                visit_group(x[j].x, y[j].x, (m[j] & 0xffu) != 0, o, g[j]);
-                visit_group(x[j].y, y[j].y, (m[j] & 0xff00u) != 0, o + 1, g[j]);
-                visit_group(x[j].z, y[j].z, (m[j] & 0xff0000u) != 0, o + 2, g[j]);
-                visit_group(x[j].w, y[j].w, (m[j] & 0xff000000u) != 0, o + 3, g[j]);
-            }
-#pragma unroll
-            for (int j = 0; j < kVec; ++j) {
-                const bool better = g[j].key > a.key;
-                a.key = better ? g[j].key : a.key;
-                a.arg = better ? g[j].arg : a.arg;
-            }
-            // an inf or NaN |d| exists exactly when the largest key is above the key of the
-            // largest finite float (NaN and inf rank above every finite |d|)
-            a.flags = a.key > 0x7f800000u ? 1u : 0u;
-            static_assert(kVec == 4, "the fixed summation tree below assumes four groups");
-            a.sd = (g[0].sd + g[1].sd) + (g[2].sd + g[3].sd);
-            a.skl = (g[0].skl + g[1].skl) + (g[2].skl + g[3].skl);
-        } else {
-#pragma unroll 1
-            for (int j = 0; j < kVec; ++j) {
-                const int o0 = j * (kAuditThreads * 4) + threadIdx.x * 4;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int64_t i = base + o0 + e;
-                    if (i < N) visit3(nw[i], od[i], mask == nullptr ? 1u : mask[i], o0 + e, a);
-                }
-            }
-        }
+
+    __device__ __forceinline__ void add_slice(const ThreadAcc& a, int64_t slice_base) {
         count += a.count;
         if (a.key > best_key) {
             best_key = a.key;
-            best_off = slice_off + a.arg;
+            best_off = slice_base + a.arg;
         }
         flags |= a.flags;
         sum_d = df_add(sum_d, DFloat{a.sd, 0.f});
         sum_kl = df_add(sum_kl, DFloat{a.skl, 0.f});
     }
-    // fixed tree over the warp (float-pair sums, integer counts, key / offset max)
+};
+
+// The block's partial from its kAuditThreads threads: a fixed tree over each
+// warp (float-pair sums, integer counts, key / index max), then the eight warp
+// partials in warp order, written by thread 0.
+__device__ __forceinline__ void finish_block(RunAcc r, AuditPartial* out) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-        const int c = __shfl_down_sync(0xffffffffu, count, off);
-        const uint32_t k = __shfl_down_sync(0xffffffffu, best_key, off);
-        const int64_t g = __shfl_down_sync(0xffffffffu, best_off, off);
+        const int c = __shfl_down_sync(0xffffffffu, r.count, off);
+        const uint32_t k = __shfl_down_sync(0xffffffffu, r.best_key, off);
+        const int64_t g = __shfl_down_sync(0xffffffffu, r.best_off, off);
         DFloat sd, skl;
-        sd.hi = __shfl_down_sync(0xffffffffu, sum_d.hi, off);
-        sd.lo = __shfl_down_sync(0xffffffffu, sum_d.lo, off);
-        skl.hi = __shfl_down_sync(0xffffffffu, sum_kl.hi, off);
-        skl.lo = __shfl_down_sync(0xffffffffu, sum_kl.lo, off);
-        const uint32_t f = __shfl_down_sync(0xffffffffu, flags, off);
+        sd.hi = __shfl_down_sync(0xffffffffu, r.sum_d.hi, off);
+        sd.lo = __shfl_down_sync(0xffffffffu, r.sum_d.lo, off);
+        skl.hi = __shfl_down_sync(0xffffffffu, r.sum_kl.hi, off);
+        skl.lo = __shfl_down_sync(0xffffffffu, r.sum_kl.lo, off);
+        const uint32_t f = __shfl_down_sync(0xffffffffu, r.flags, off);
         if (lane + off < 32) {
-            const bool take = k > best_key || (k == best_key && k != 0 && g < best_off);
-            best_key = take ? k : best_key;
-            best_off = take ? g : best_off;
-            count += c;
-            sum_d = df_add(sum_d, sd);
-            sum_kl = df_add(sum_kl, skl);
-            flags |= f;
+            const bool take = k > r.best_key || (k == r.best_key && k != 0 && g < r.best_off);
+            r.best_key = take ? k : r.best_key;
+            r.best_off = take ? g : r.best_off;
+            r.count += c;
+            r.sum_d = df_add(r.sum_d, sd);
+            r.sum_kl = df_add(r.sum_kl, skl);
+            r.flags |= f;
         }
     }
-    // the eight warp partials, in warp order
     __shared__ Acc warp_acc[kAuditThreads / 32];
     if (lane == 0) {
         Acc w;
-        w.count = count;
-        w.arg = best_key == 0 ? INT64_MAX : block_base + best_off;
-        w.sum_d = sum_d;
-        w.sum_kl = sum_kl;
-        w.best = best_key == 0 ? -1.0f : __uint_as_float(best_key - 1u);
-        w.flags = flags;
+        w.count = r.count;
+        w.arg = r.best_key == 0 ? INT64_MAX : r.best_off;
+        w.sum_d = r.sum_d;
+        w.sum_kl = r.sum_kl;
+        w.best = r.best_key == 0 ? -1.0f : __uint_as_float(r.best_key - 1u);
+        w.flags = r.flags;
         warp_acc[warp] = w;
     }
-    __syncthreads();
+    named_barrier(kAuditThreads);
     if (threadIdx.x == 0) {
         Acc t = warp_acc[0];
 #pragma unroll
@@ -362,19 +408,24 @@ __global__ void __launch_bounds__(kAuditThreads)
         p.flags = t.flags;
         out[blockIdx.x] = p;
     }
-    if constexpr (FUSED) {
-        __shared__ int is_last;
-        if (threadIdx.x == 0) {
-            __threadfence();             // the partial is visible before the ticket is taken
-            is_last = atomicAdd(ticket, 1u) == gridDim.x - 1u;
-        }
-        __syncthreads();
-        if (is_last) {
-            __threadfence();
-            merge_partials<kAuditThreads, true>(out, gridDim.x, result);
-            if (threadIdx.x == 0) *ticket = 0u;
-        }
+}
+
+// Pass 1 (any alignment; vector loads when VEC); a second launch merges.
+template <bool VEC>
+__global__ void __launch_bounds__(kAuditThreads)
+    audit_pass1(const float* __restrict__ nw, const float* __restrict__ od,
+                const uint8_t* __restrict__ mask, int64_t N, AuditPartial* __restrict__ out) {
+    // let the merge kernel launch now; it waits for this grid before reading
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int64_t slices = (N + kSlice - 1) / kSlice;
+    RunAcc r;
+#pragma unroll 1
+    for (int64_t sl = blockIdx.x; sl < slices; sl += gridDim.x) {
+        ThreadAcc a;
+        load_and_visit_slice<VEC>(nw, od, mask, N, sl * kSlice, r.best_key, a);
+        r.add_slice(a, sl * kSlice);
     }
+    finish_block(r, out);
 }
 
 constexpr int kMergeThreads = 1024;
@@ -391,28 +442,10 @@ __device__ __forceinline__ Acc to_acc(const AuditPartial& p) {
     return b;
 }
 
-// Partial i, read through L2 when COHERENT (partials written by other blocks of the
-// same grid: L1 is not coherent across SMs).
-template <bool COHERENT>
-__device__ __forceinline__ AuditPartial load_partial(const AuditPartial* parts, int64_t i) {
-    if constexpr (!COHERENT) {
-        return parts[i];
-    } else {
-        static_assert(sizeof(AuditPartial) == 40, "five 8-byte words");
-        const unsigned long long* w = reinterpret_cast<const unsigned long long*>(parts + i);
-        unsigned long long v[5];
-#pragma unroll
-        for (int j = 0; j < 5; ++j) v[j] = __ldcg(w + j);
-        AuditPartial p;
-        memcpy(&p, v, sizeof(p));
-        return p;
-    }
-}
-
 // Thread t folds partials t, t + THREADS, t + 2 THREADS, ... in ascending order (they
 // are loaded kMergeBatch at a time so that the loads overlap; the order is unchanged),
 // then the fixed block tree; thread 0 writes the result.
-template <int THREADS, bool COHERENT>
+template <int THREADS>
 __device__ void merge_partials(const AuditPartial* parts, int64_t num_parts,
                                rlk_audit_result_t* result) {
     Acc a = empty_acc();
@@ -420,11 +453,11 @@ __device__ void merge_partials(const AuditPartial* parts, int64_t num_parts,
     for (; i + (kMergeBatch - 1) * THREADS < num_parts; i += kMergeBatch * THREADS) {
         AuditPartial p[kMergeBatch];
 #pragma unroll
-        for (int j = 0; j < kMergeBatch; ++j) p[j] = load_partial<COHERENT>(parts, i + j * THREADS);
+        for (int j = 0; j < kMergeBatch; ++j) p[j] = parts[i + j * THREADS];
 #pragma unroll
         for (int j = 0; j < kMergeBatch; ++j) merge(a, to_acc(p[j]));
     }
-    for (; i < num_parts; i += THREADS) merge(a, to_acc(load_partial<COHERENT>(parts, i)));
+    for (; i < num_parts; i += THREADS) merge(a, to_acc(parts[i]));
     a = block_reduce<THREADS>(a);
     if (threadIdx.x == 0) {
         rlk_audit_result_t r;
@@ -444,7 +477,7 @@ __global__ void __launch_bounds__(kMergeThreads)
     // launched early (programmatic dependent launch): wait until every block of
     // pass 1 has finished and its partials are visible
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    merge_partials<kMergeThreads, false>(parts, num_parts, result);
+    merge_partials<kMergeThreads>(parts, num_parts, result);
 }
 
 // ----------------------------------------------------------------------------- extended audit
@@ -866,20 +899,15 @@ __global__ void __launch_bounds__(kSelectThreads)
 }  // namespace
 
 // Scratch of rlk_dlogp_audit_noalloc: room for the partials of pass 1 (it writes
-// at most kAuditMaxBlocks of them, whatever N) and the ticket counter of the
-// single-launch audit.  It lives in the library image, so every GPU that loads
-// the library holds it until the process exits.  Pass 1 writes every partial that
-// the merge reads; the ticket is cleared on the stream before each launch.  Calls
+// at most kAuditMaxBlocks of them, whatever N).  It lives in the library image, so
+// every GPU that loads the library holds it until the process exits.  Pass 1 writes
+// every partial that the merge reads, so nothing in it has to start at zero; calls
 // that overlap on the GPU share it and race.
 constexpr size_t kNoAllocBlocks =
     static_cast<size_t>(RLK_AUDIT_NOALLOC_MAX_N) / (kAuditThreads * kAuditV3PerThread);
 static_assert(kNoAllocBlocks >= static_cast<size_t>(kAuditMaxBlocks),
               "the no-alloc scratch must hold every partial pass 1 can write");
-struct NoAllocScratch {
-    AuditPartial parts[kNoAllocBlocks];
-    unsigned int ticket;
-};
-static __device__ __align__(256) NoAllocScratch g_audit_noalloc_scratch;
+static __device__ __align__(256) AuditPartial g_audit_noalloc_scratch[kNoAllocBlocks];
 
 namespace {
 
@@ -898,7 +926,7 @@ F driver_fn(const char* name) {
 
 }  // namespace
 
-cudaError_t audit_noalloc_scratch(void** parts, unsigned int** ticket) {
+cudaError_t audit_noalloc_scratch(void** parts) {
     // Host code cannot use the array's name as a device address: the address is looked
     // up with the device current, and cached per device together with the unique id of
     // the context it belongs to, so that a context created anew (after cudaDeviceReset,
@@ -931,31 +959,25 @@ cudaError_t audit_noalloc_scratch(void** parts, unsigned int** ticket) {
         addr[dev] = p;
         ctx_id[dev] = have_id ? id : 0;
     }
-    NoAllocScratch* sc = static_cast<NoAllocScratch*>(addr[dev]);
-    *parts = sc->parts;
-    *ticket = &sc->ticket;
+    *parts = addr[dev];
     return cudaSuccess;
 }
 
-size_t audit_ticket_offset(int64_t N) {
-    // room for at least one partial: N = 0 still runs one block
-    return align_up(std::max<size_t>(1, audit_v3_blocks(N)) * sizeof(AuditPartial), 256);
-}
-
-// Two launches: pass 1, then one block that merges, by programmatic dependent launch.
-static cudaError_t launch_audit_two_pass(const float* logp_new, const float* logp_old,
-                                         const uint8_t* mask, int64_t N,
-                                         rlk_audit_result_t* result, AuditPartial* parts,
-                                         bool vec_ok, cudaStream_t stream) {
-    const size_t blocks = static_cast<size_t>(audit_pass1_blocks(N));
-    const int64_t spb = audit_slices_per_block(N);
+// Pass 1 (vector loads when vec_ok, element loads otherwise: the same arithmetic),
+// then one block that merges, launched by programmatic dependent launch so that its
+// launch overlaps pass 1.
+cudaError_t launch_audit(const float* logp_new, const float* logp_old, const uint8_t* mask,
+                         int64_t N, rlk_audit_result_t* result, void* partials, bool vec_ok,
+                         cudaStream_t stream) {
+    AuditPartial* parts = static_cast<AuditPartial*>(partials);
+    const unsigned blocks = static_cast<unsigned>(audit_pass1_blocks(N));
     if (blocks > 0) {
         if (vec_ok)
-            audit_pass1<true, false><<<static_cast<unsigned>(blocks), kAuditThreads, 0, stream>>>(
-                logp_new, logp_old, mask, N, spb, parts, nullptr, nullptr);
+            audit_pass1<true><<<blocks, kAuditThreads, 0, stream>>>(logp_new, logp_old, mask, N,
+                                                                    parts);
         else
-            audit_pass1<false, false><<<static_cast<unsigned>(blocks), kAuditThreads, 0, stream>>>(
-                logp_new, logp_old, mask, N, spb, parts, nullptr, nullptr);
+            audit_pass1<false><<<blocks, kAuditThreads, 0, stream>>>(logp_new, logp_old, mask, N,
+                                                                     parts);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -972,35 +994,6 @@ static cudaError_t launch_audit_two_pass(const float* logp_new, const float* log
     const AuditPartial* cparts = parts;
     const int64_t nparts = static_cast<int64_t>(blocks);
     return cudaLaunchKernelEx(&cfg, audit_pass2, cparts, nparts, result);
-}
-
-// One launch: the ticket is cleared on the stream, then pass 1's last block merges.
-static cudaError_t launch_audit_fused(const float* logp_new, const float* logp_old,
-                                      const uint8_t* mask, int64_t N, rlk_audit_result_t* result,
-                                      AuditPartial* parts, unsigned int* ticket, bool vec_ok,
-                                      cudaStream_t stream) {
-    // N = 0 still runs one block, which writes the empty result
-    const size_t blocks = std::max<size_t>(1, static_cast<size_t>(audit_pass1_blocks(N)));
-    const int64_t spb = audit_slices_per_block(N);
-    cudaError_t e = cudaMemsetAsync(ticket, 0, sizeof(unsigned int), stream);
-    if (e != cudaSuccess) return e;
-    if (vec_ok)
-        audit_pass1<true, true><<<static_cast<unsigned>(blocks), kAuditThreads, 0, stream>>>(
-            logp_new, logp_old, mask, N, spb, parts, ticket, result);
-    else
-        audit_pass1<false, true><<<static_cast<unsigned>(blocks), kAuditThreads, 0, stream>>>(
-            logp_new, logp_old, mask, N, spb, parts, ticket, result);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_audit(const float* logp_new, const float* logp_old, const uint8_t* mask,
-                         int64_t N, rlk_audit_result_t* result, void* partials,
-                         unsigned int* ticket, bool vec_ok, cudaStream_t stream) {
-    AuditPartial* parts = static_cast<AuditPartial*>(partials);
-    if (kAuditFused)
-        return launch_audit_fused(logp_new, logp_old, mask, N, result, parts, ticket, vec_ok,
-                                  stream);
-    return launch_audit_two_pass(logp_new, logp_old, mask, N, result, parts, vec_ok, stream);
 }
 
 // partials | 3 histograms | select state | |d| keys [N] (uint32)

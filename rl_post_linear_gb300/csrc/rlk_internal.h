@@ -248,13 +248,11 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& step, int nu
                             uint32_t* err, cudaStream_t stream);
 
 // The audit: per-block partials (at most 608 of them), then their merge in a fixed
-// order.  kAuditFused: one launch, whose last block (integer ticket, cleared on the
-// stream first) merges; otherwise a second, one-block launch merges.
-constexpr bool kAuditFused = false;
-size_t audit_ticket_offset(int64_t N);   // of the ticket word in rlk_dlogp_audit's workspace
+// order by a second launch.  vec_ok: new / old 16-byte and the mask 4-byte aligned
+// (vector loads).
 cudaError_t launch_audit(const float* logp_new, const float* logp_old, const uint8_t* mask,
-                         int64_t N, rlk_audit_result_t* result, void* partials,
-                         unsigned int* ticket, bool vec_ok, cudaStream_t stream);
+                         int64_t N, rlk_audit_result_t* result, void* partials, bool vec_ok,
+                         cudaStream_t stream);
 
 cudaError_t launch_grpo_loss(const float* logp_new, const float* logp_old, const float* adv,
                              const uint8_t* mask, int64_t N, double eps_low, double eps_high,
@@ -272,8 +270,7 @@ cudaError_t launch_audit_ext(const float* logp_new, const float* logp_old, const
                              rlk_audit_ext_t* result, void* workspace, bool vec_ok, int sms,
                              cudaStream_t stream);
 
-// Device addresses (current device) of the library-owned audit scratch: the partials
-// and the ticket word.
-cudaError_t audit_noalloc_scratch(void** parts, unsigned int** ticket);
+// Device address (current device and context) of the library-owned audit scratch.
+cudaError_t audit_noalloc_scratch(void** parts);
 
 }  // namespace rlk

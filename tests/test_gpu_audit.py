@@ -82,19 +82,29 @@ def test_pages_element_count_exact_and_reproducible():
     assert r == r2
 
 
+def _block_slices(n, b):
+    # the partition of pass 1: 4096-element slices dealt round-robin to min(slices, 608)
+    # blocks; block b visits its slices in ascending order
+    slices = -(-n // 4096)
+    g = min(slices, 608)
+    return list(range(b, slices, g))
+
+
 def test_ties_across_the_slices_of_one_block():
-    # Above 608 x 4096 elements a pass-1 block covers several consecutive 4096-element
-    # slices (N = 5,000,000: three per block).  Equal largest |d| in two slices of one block,
-    # in different float4 groups of the same thread, and in the tail block: the lowest index
-    # must win each time.
+    # At N = 5,000,000 (1221 slices) block 3 holds slices 3, 611 and 1219.  Equal largest |d|
+    # in two slices of one block, in different float4 groups of the same thread, across two
+    # blocks whose merge order is the opposite of their index order, and in the tail slice:
+    # the lowest index must win each time.
     n = 5_000_000
+    sl = _block_slices(n, 3)
+    assert sl == [3, 611, 1219]
     new, old, mask = wl.audit_inputs(n, 9)
     mask[:] = 1
-    blk = 7 * 3 * 4096                       # first element of block 7
     cases = [
-        (blk + 4096 + 5, blk + 100),         # slice 1 vs an earlier offset in slice 0
-        (blk + 2 * 4096 + 1024 * 3 + 4 * 17, blk + 4 * 17),   # same thread, group 3 vs 0
-        (n - 3, n - 4096 * 2 - 7),           # the tail block
+        (sl[1] * 4096 + 5, sl[0] * 4096 + 100),                      # block 3: slice 611 vs 3
+        (sl[2] * 4096 + 1024 * 3 + 4 * 17, sl[0] * 4096 + 4 * 17),  # one thread: group 3 vs 0
+        (612 * 4096 + 9, 5 * 4096 + 2000),        # block 4 (merged first) vs block 5
+        (n - 3, n - 4096 * 2 - 7),                # the tail slice
     ]
     for later, earlier in cases:
         nw, od = new.clone(), old.clone()
@@ -104,3 +114,26 @@ def test_ties_across_the_slices_of_one_block():
         r, o = _both(nw, od, mask)
         _check(r, o, nw, od, mask)
         assert r["argmax_index"] == earlier, (later, earlier)
+
+
+@pytest.mark.parametrize("n", [5003, 9_400_614])
+def test_alignment_does_not_change_the_bits(n):
+    # The same values placed at three alignments -- vector loads (all 16-byte aligned, or
+    # the mask only 4-byte aligned) and element loads (values 4-byte aligned) -- go
+    # through one arithmetic: the results are equal bit for bit.
+    new, old, mask = wl.audit_inputs(n, 21)
+    d = dev()
+    out = []
+    for off_v, off_m in ((0, 0), (4, 4), (1, 1)):
+        nb = torch.zeros(n + 8, device=d)
+        ob = torch.zeros(n + 8, device=d)
+        mb = torch.zeros(n + 16, dtype=torch.uint8, device=d)
+        nb[off_v:off_v + n] = new.to(d)
+        ob[off_v:off_v + n] = old.to(d)
+        mb[off_m:off_m + n] = mask.to(d)
+        out.append(rlk.dlogp_audit(nb[off_v:off_v + n], ob[off_v:off_v + n], mb[off_m:off_m + n]))
+    o = oracle.dlogp_audit(new.numpy(), old.numpy(), mask.numpy())
+    _check(out[0], o, new, old, mask)
+    for r in out[1:]:
+        assert r == out[0] or all(
+            (r[k] == out[0][k]) or (math.isnan(r[k]) and math.isnan(out[0][k])) for k in r)
