@@ -180,7 +180,7 @@ static rlk_status_t fwd_impl(const void* hidden, const void* weight, const int64
     }
     CUtensorMap map_h, map_w;
     RLK_TRY(make_map(&map_h, gemm_rows, H, N, H * 2, 64, rlk::kTileM));
-    RLK_TRY(make_map(&map_w, weight, H, V, H * 2, 64, rlk::kTileV));
+    RLK_TRY(make_map(&map_w, weight, H, V, H * 2, 64, rlk::kPairBRows));
     const float k = static_cast<float>(1.4426950408889634074 / temperature);
     RLK_CUDA(rlk::launch_fwd(map_h, map_w, targets, active_mask, static_cast<int>(N),
                              static_cast<int>(H), static_cast<int>(V), k, logp_out, lse_out,
@@ -389,7 +389,7 @@ static rlk_status_t bwd_impl(const void* hidden, const void* weight, const int64
 
     rlk::BwdStepMaps maps;
     RLK_TRY(make_map(&maps.h_kmajor, gemm_rows, H, N, H * 2, 64, rlk::kTileM));
-    RLK_TRY(make_map(&maps.w_kmajor, weight, H, V, H * 2, 64, rlk::kTileV));
+    RLK_TRY(make_map(&maps.w_kmajor_pair, weight, H, V, H * 2, 64, rlk::kPairBRows));
     RLK_TRY(make_map(&maps.w_mnmajor, weight, H, V, H * 2, 64, 64));
     RLK_TRY(make_map(&maps.h_mnmajor, gemm_rows, H, N, H * 2, 64, 64));
 
@@ -559,7 +559,7 @@ rlk_status_t rlk_linear_logp_fwd_shard(const void* hidden, const void* weight_sh
     RLK_TRY(current_device(dev));
     CUtensorMap map_h, map_w;
     RLK_TRY(make_map(&map_h, hidden, H, N, H * 2, 64, rlk::kTileM));
-    RLK_TRY(make_map(&map_w, weight_shard, H, V_local, H * 2, 64, rlk::kTileV));
+    RLK_TRY(make_map(&map_w, weight_shard, H, V_local, H * 2, 64, rlk::kPairBRows));
     const float k = static_cast<float>(1.4426950408889634074 / temperature);
     RLK_CUDA(rlk::launch_fwd_partials(map_h, map_w, targets, active_mask, static_cast<int>(N),
                                       static_cast<int>(H), static_cast<int>(V_local),

@@ -85,7 +85,7 @@ struct RowMap {
     __device__ int count(int N) const { return n_rows != nullptr ? *n_rows : N; }
     // at least one tile: with no active row, the dS GEMM still zeroes the rows that
     // the dW GEMM's (single) K block reads
-    __device__ int tiles(int N) const { return (max(count(N), 1) + kTileM - 1) / kTileM; }
+    __device__ int tiles(int N) const { return (max(count(N), 1) + kUnitM - 1) / kUnitM; }
     __device__ int token(int i) const { return rows != nullptr ? rows[i] : i; }
 };
 
@@ -105,6 +105,7 @@ __device__ __forceinline__ void bf16x8_to_f32(uint4 v, float* out) {
 // i.e. -(p/T) (g + gH (S/T - Ez)), the entropy's dH/dz = -p (z - E[z]).
 template <bool ENT>
 struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
+    static constexpr bool kCtaPair = true;       // 256-token tiles on a CTA pair
     // With ENT, dS is stored as a pair of bf16 planes per row, hi = bf16(dS) and
     // lo = bf16(dS - hi) (columns [kBwdChunk, 2 kBwdChunk) of the row), and the dh and
     // dW GEMMs run over both planes: the entropy gradient has no fp32 part that
@@ -135,12 +136,12 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
     __device__ int tiles_in_unit(int) const { return 1; }
     // unit -> (row tile m, vocab tile n of the chunk), row tiles grouped
     __device__ void unit(int u, int& m, int& n) const {
-        grouped_unit(u, rm.tiles(N), num_n, kRasterTokenTiles, m, n);
+        grouped_unit(u, rm.tiles(N), num_n, kRasterTokenRows / kUnitM, m, n);
     }
     __device__ void coords(int u, int, int& a_mn, int& a_k, int& b_mn, int& b_k) const {
         int m, n;
         unit(u, m, n);
-        a_mn = m * kTileM;
+        a_mn = m * kUnitM;
         a_k = 0;
         b_mn = c0 + n * kTileV;
         b_k = 0;
@@ -159,7 +160,7 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
     __device__ void epi_begin(int u, int row, EpiState& st) const {
         int m, n;
         unit(u, m, n);
-        const int i = m * kTileM + row;
+        const int i = m * kUnitM + row;
         const int t = i < rm.count(N) ? rm.token(i) : N;
         st.t = t;
         int64_t y;
@@ -185,7 +186,7 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
     __device__ void epi_tile(int u, int, int row, uint32_t taddr, EpiState& st) const {
         int m, n;
         unit(u, m, n);
-        const int i = m * kTileM + row;          // dS row (compacted row)
+        const int i = m * kUnitM + row;          // dS row (compacted row)
         const int t = st.t;                      // its token
 #pragma unroll 1
         for (int cc = 0; cc < kTileV / 32; ++cc) {
@@ -298,6 +299,7 @@ struct DsKlPolicy {
     using Maps = DsKlMaps;
     static constexpr bool kPairTiles = true;
     static constexpr bool kKRemap = false;
+    static constexpr bool kCtaPair = false;
     static constexpr int kEpiWarps = 8;       // two column halves per row
     // dS as hi / lo bf16 planes (columns [0, kBwdChunk) and [kBwdChunk, 2 kBwdChunk) of
     // each row), which the dh and dW GEMMs both consume: the KL gradient has no fp32
@@ -340,7 +342,7 @@ struct DsKlPolicy {
     __device__ int num_units() const { return num_m * num_n; }
     __device__ int tiles_in_unit(int) const { return 2; }
     __device__ void unit(int u, int& m, int& n) const {
-        grouped_unit(u, num_m, num_n, kRasterTokenTiles, m, n);
+        grouped_unit(u, num_m, num_n, kRasterTokenRows / kTileM, m, n);
     }
     __device__ void coords(int u, int, int& a_mn, int& a_k, int& b_mn, int& b_k) const {
         int m, n;
@@ -444,6 +446,7 @@ struct DsKlPolicy {
 // runs over the hi plane, then over the lo plane against the same rows of W_c.
 struct DhPolicy : SingleRole<false, true> {
     static constexpr bool kKRemap = true;
+    static constexpr bool kCtaPair = true;       // 256-token tiles on a CTA pair
 
     const int64_t* targets;
     const uint8_t* mask;
@@ -484,7 +487,7 @@ struct DhPolicy : SingleRole<false, true> {
     __device__ void coords(int u, int, int& a_mn, int& a_k, int& b_mn, int& b_k) const {
         int m, n;
         unit(u, m, n);
-        a_mn = m * kTileM;
+        a_mn = m * kUnitM;
         a_k = 0;
         b_mn = n * kTileV;
         b_k = c0;
@@ -501,7 +504,7 @@ struct DhPolicy : SingleRole<false, true> {
     __device__ void epi_begin(int u, int row, EpiState& st) const {
         int m, n;
         unit(u, m, n);
-        const int i = m * kTileM + row;
+        const int i = m * kUnitM + row;
         const int t = i < rm.count(N) ? rm.token(i) : N;
         st.t = t;
         // the fp32 terms, added once, in the last chunk's epilogue: (g / T)(1 - p_y) W[y]
@@ -525,7 +528,7 @@ struct DhPolicy : SingleRole<false, true> {
     __device__ void epi_tile(int u, int, int row, uint32_t taddr, EpiState& st) const {
         int m, n;
         unit(u, m, n);
-        const int ri = m * kTileM + row;         // dh_acc row (compacted row)
+        const int ri = m * kUnitM + row;         // dh_acc row (compacted row)
         const int t = st.t;                      // its token
 #pragma unroll 1
         for (int cc = 0; cc < kTileV / 32; ++cc) {
@@ -611,6 +614,7 @@ struct DhPolicy : SingleRole<false, true> {
 // same tokens of the lo plane (kBwdChunk columns further on), against h twice.
 struct DwPolicy : SingleRole<true, true> {
     static constexpr bool kKRemap = true;
+    static constexpr bool kCtaPair = true;       // 256-vocab-row tiles on a CTA pair
 
     const float* grad;
     const __nv_bfloat16* hidden;   // [N][H]
@@ -650,7 +654,7 @@ struct DwPolicy : SingleRole<true, true> {
     __device__ void coords(int u, int, int& a_mn, int& a_k, int& b_mn, int& b_k) const {
         int m, n;
         unit(u, m, n);
-        a_mn = m * kTileM;
+        a_mn = m * kUnitM;
         a_k = 0;
         b_mn = n * kTileV;
         b_k = 0;
@@ -677,7 +681,7 @@ struct DwPolicy : SingleRole<true, true> {
     __device__ void epi_begin(int u, int row, EpiState& st) const {
         int m, n;
         unit(u, m, n);
-        const int vl = m * kTileM + row;
+        const int vl = m * kUnitM + row;
         st.valid = vl < width;
         st.v = c0 + vl;
         st.lo = st.hi = st.dlo = st.dhi = 0;
@@ -894,13 +898,7 @@ static cudaError_t launch_dom_sort(const int* dom, int N, int V, int lo, int hi,
 template <class P>
 static cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const P& p, int units,
                                int num_sms, uint32_t* err, cudaStream_t stream) {
-    auto kern = gemm_persistent_kernel<P>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kGemmSmemBytes));
-    if (e != cudaSuccess) return e;
-    const int grid = units < num_sms ? units : num_sms;
-    kern<<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(TwoMaps{a, b}, p, err);
-    return cudaGetLastError();
+    return launch_persistent(TwoMaps{a, b}, p, units, num_sms, err, stream);
 }
 
 template <bool ENT>
@@ -924,12 +922,13 @@ static cudaError_t launch_ds(const BwdStepMaps& maps, const BwdStep& st, int c0,
     ps.N = st.N;
     ps.V = st.V;
     ps.c0 = c0;
-    ps.num_m = (st.N + kTileM - 1) / kTileM;
+    ps.num_m = (st.N + kUnitM - 1) / kUnitM;
     ps.num_n = (width + kTileV - 1) / kTileV;
     ps.kblocks = st.H / 64;
     ps.k = st.k;
     ps.temp = st.temp;
-    return launch_gemm(maps.h_kmajor, maps.w_kmajor, ps, ps.num_m * ps.num_n, num_sms, err, stream);
+    return launch_gemm(maps.h_kmajor, maps.w_kmajor_pair, ps, ps.num_m * ps.num_n, num_sms, err,
+                       stream);
 }
 
 cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_sms, uint32_t* err,
@@ -1001,7 +1000,7 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
         pd.V = V;
         pd.H = H;
         pd.c0 = c0;
-        pd.num_m = (N + kTileM - 1) / kTileM;
+        pd.num_m = (N + kUnitM - 1) / kUnitM;
         pd.num_n = (H + kTileV - 1) / kTileV;
         pd.kblocks = (width + 63) / 64;
         pd.first = st.chunk == 0;
@@ -1029,7 +1028,7 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
     pw.H = H;
     pw.c0 = c0;
     pw.width = width;
-    pw.num_m = (width + kTileM - 1) / kTileM;
+    pw.num_m = (width + kUnitM - 1) / kUnitM;
     pw.num_n = (H + kTileV - 1) / kTileV;
     pw.kblocks = (N + 63) / 64;
     pw.temp = st.temp;

@@ -46,6 +46,7 @@ constexpr float kMaskedLogit = -3.0e38f;
 // the merge forms E[S] = a / s and the entropy lse - E[S]/T.
 template <bool ENT>
 struct FwdPolicyT : SingleRole<false, false> {   // h [N,H] and W [V,H]: K-major
+    static constexpr bool kCtaPair = true;       // 256-token tiles on a CTA pair
 
     const int64_t* targets;
     const uint8_t* mask;
@@ -60,14 +61,14 @@ struct FwdPolicyT : SingleRole<false, false> {   // h [N,H] and W [V,H]: K-major
 
     __device__ int valid_rows() const { return n_rows != nullptr ? *n_rows : N; }
     __device__ int token_tiles() const {
-        return n_rows != nullptr ? (*n_rows + kTileM - 1) / kTileM : num_m;
+        return n_rows != nullptr ? (*n_rows + kUnitM - 1) / kUnitM : num_m;
     }
 
     __device__ int num_units() const { return token_tiles() * num_chunks; }
     __device__ int k_blocks(int) const { return kblocks; }
-    // unit -> (token tile m, vocab chunk c), token tiles grouped by kRasterTokenTiles
+    // unit -> (token tile m, vocab chunk c), token tiles grouped kRasterTokenRows rows at a time
     __device__ void unit(int u, int& m, int& c) const {
-        grouped_unit(u, token_tiles(), num_chunks, kRasterTokenTiles, m, c);
+        grouped_unit(u, token_tiles(), num_chunks, kRasterTokenRows / kUnitM, m, c);
     }
     __device__ int tiles_in_unit(int u) const {
         int m, c;
@@ -77,7 +78,7 @@ struct FwdPolicyT : SingleRole<false, false> {   // h [N,H] and W [V,H]: K-major
     __device__ void coords(int u, int q, int& a_mn, int& a_k, int& b_mn, int& b_k) const {
         int m, c;
         unit(u, m, c);
-        a_mn = m * kTileM;
+        a_mn = m * kUnitM;
         a_k = 0;
         b_mn = (c * kFwdTilesPerChunk + q) * kTileV;
         b_k = 0;
@@ -92,7 +93,7 @@ struct FwdPolicyT : SingleRole<false, false> {   // h [N,H] and W [V,H]: K-major
     __device__ void epi_begin(int u, int row, EpiState& st) const {
         int m, c;
         unit(u, m, c);
-        const int i = m * kTileM + row;
+        const int i = m * kUnitM + row;
         st.m = -INFINITY;
         st.s = 0.f;
         st.a = 0.f;
@@ -156,7 +157,7 @@ struct FwdPolicyT : SingleRole<false, false> {   // h [N,H] and W [V,H]: K-major
     __device__ void epi_end(int u, int row, EpiState& st) const {
         int m, c;
         unit(u, m, c);
-        const int i = m * kTileM + row;          // compacted row (the token when not compacted)
+        const int i = m * kUnitM + row;          // compacted row (the token when not compacted)
         if (i >= valid_rows()) return;
         partials[static_cast<size_t>(c) * N + i] = make_float2(st.m, st.s);
         if constexpr (ENT) partials_a[static_cast<size_t>(c) * N + i] = st.a;
@@ -250,19 +251,13 @@ static cudaError_t launch_partials_t(const CUtensorMap& map_h, const CUtensorMap
     p.vocab_start = vocab_start;
     p.N = N;
     p.V = V_local;
-    p.num_m = (N + kTileM - 1) / kTileM;
+    p.num_m = (N + kUnitM - 1) / kUnitM;
     p.num_vt = (V_local + kTileV - 1) / kTileV;
     p.num_chunks = (p.num_vt + kFwdTilesPerChunk - 1) / kFwdTilesPerChunk;
     p.kblocks = H / 64;
     p.k = k;
-    auto kern = gemm_persistent_kernel<FwdPolicyT<ENT>>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kGemmSmemBytes));
-    if (e != cudaSuccess) return e;
     const long long units = static_cast<long long>(p.num_m) * p.num_chunks;
-    const int grid = static_cast<int>(units < num_sms ? units : num_sms);
-    kern<<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(TwoMaps{map_h, map_w}, p, err);
-    return cudaGetLastError();
+    return launch_persistent(TwoMaps{map_h, map_w}, p, units, num_sms, err, stream);
 }
 
 cudaError_t launch_fwd_partials(const CUtensorMap& map_h, const CUtensorMap& map_w,

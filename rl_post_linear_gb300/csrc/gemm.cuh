@@ -1,14 +1,28 @@
 // gemm.cuh -- persistent, warp-specialised bf16 GEMM mainloop for sm_103a.
 //
-//   warp 0      : TMA producer (one elected lane) filling a kStages-deep ring
-//                 of shared-memory stages (A 128x64, B 256x64, 128-byte swizzle)
+//   warp 0      : TMA producer (one elected lane) filling a ring of
+//                 shared-memory stages (A 128x64, B 256x64 or, for CTA
+//                 pairs, its 128x64 half; 128-byte swizzle)
 //   warp 1      : TMEM allocator and MMA issuer (one elected lane):
-//                 tcgen05.mma.cta_group::1.kind::f16, M=128 N=256 K=16,
-//                 fp32 accumulators in TMEM, two 256-column buffers so the
-//                 epilogue of tile i overlaps the MMAs of tile i+1
+//                 tcgen05.mma.kind::f16, K=16, fp32 accumulators in TMEM,
+//                 two 256-column buffers so the epilogue of tile i overlaps
+//                 the MMAs of tile i+1
 //   warps 2..   : epilogue (4 warps, or 8 for paired-tile policies), one
 //                 thread per accumulator row (TMEM lane) and column half,
 //                 reading 32-column slices with tcgen05.ld
+//
+// Two MMA shapes.  cta_group::1: one CTA, M=128 N=256.  CTA pairs
+// (policies with kCtaPair): a cluster of two CTAs computes a 256x256 tile
+// with tcgen05.mma.cta_group::2 M=256 N=256 -- each CTA loads 128 rows of A
+// and 128 rows of B into its own ring (at the same offsets), the even CTA
+// issues the MMAs, which read B from both CTAs, and each CTA's TMEM receives
+// its 128 rows of the accumulator.  Per FLOP each SM then moves a third
+// less operand data from L2 into shared memory and reads a third less from
+// it.  Both CTAs' copies complete on the even CTA's "full" barrier, whose
+// producer announces the bytes of both (a local arrive: a cluster-scope
+// release on every stage would fence the producer and starve the MMAs); the
+// even CTA's commits release the stage and signal "TMEM full" in both CTAs;
+// both CTAs' epilogue warps arrive on the even CTA's "TMEM empty" barrier.
 //
 // The policy P decides the operands' majorness, the work units (a unit is a
 // run of tiles that shares one epilogue state), tile coordinates, the K
@@ -31,7 +45,10 @@ namespace rlk {
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
-constexpr int kStages = 4;
+constexpr int kPairM = 2 * kBM;                    // rows of a CTA pair's tile
+static_assert(kPairM == kUnitM, "the pair tile is the policies' unit");
+constexpr int kStages = 4;                         // single CTA: 48 KiB stages
+constexpr int kPairStages = 6;                     // CTA pair: 32 KiB stages
 constexpr uint32_t kAStageBytes = kBM * kBK * 2;   // 16 KiB
 constexpr uint32_t kBStageBytes = kBN * kBK * 2;   // 32 KiB
 constexpr uint32_t kStageBytes = kAStageBytes + kBStageBytes;
@@ -39,6 +56,18 @@ constexpr uint32_t kTmemCols = 2 * kBN;            // two fp32 accumulators
 constexpr int kGemmThreads = 192;
 constexpr uint32_t kBarrierBytes = 256;
 constexpr uint32_t kGemmSmemBytes = kStages * kStageBytes + kBarrierBytes + 1024;  // + align slack
+
+// Ring geometry of a policy: stage count and bytes of each operand per stage.
+template <bool PAIR>
+struct RingShape {
+    static constexpr int stages = PAIR ? kPairStages : kStages;
+    static constexpr int b_rows = PAIR ? kBN / 2 : kBN;
+    static constexpr uint32_t a_bytes = kAStageBytes;
+    static constexpr uint32_t b_bytes = static_cast<uint32_t>(b_rows) * kBK * 2;
+    static constexpr uint32_t stage_bytes = a_bytes + b_bytes;
+    static constexpr uint32_t smem_bytes = stages * stage_bytes + kBarrierBytes + 1024;
+};
+static_assert(RingShape<true>::smem_bytes <= 227 * 1024, "CTA-pair ring exceeds shared memory");
 constexpr uint64_t kWaitTimeoutNs = 4000000000ull;  // 4 s for one wait: far above any real wait
 constexpr uint64_t kDrainTimeoutNs = 200000000ull;
 
@@ -72,6 +101,30 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t stage_addr, int kk) {
     }
 }
 
+// The same for one CTA of a pair: the copies complete on the even CTA's barrier
+// (bar: shared::cluster address).
+template <bool MN_MAJOR, int ROWS>
+__device__ __forceinline__ void load_operand_pair(uint8_t* dst, const CUtensorMap* map,
+                                                  uint32_t bar, int mn0, int k0) {
+    if constexpr (!MN_MAJOR) {
+        tma_load_2d_pair(dst, map, bar, k0, mn0);
+    } else {
+#pragma unroll
+        for (int i = 0; i < ROWS / 64; ++i)
+            tma_load_2d_pair(dst + i * 8192, map, bar, mn0 + 64 * i, k0);
+    }
+}
+
+template <int ROWS>
+__device__ __forceinline__ void load_operand_pair_rt(bool mn_major, uint8_t* dst,
+                                                     const CUtensorMap* map, uint32_t bar,
+                                                     int mn0, int k0) {
+    if (mn_major)
+        load_operand_pair<true, ROWS>(dst, map, bar, mn0, k0);
+    else
+        load_operand_pair<false, ROWS>(dst, map, bar, mn0, k0);
+}
+
 // Runtime-majorness variants for policies that mix operand layouts per unit.
 template <int ROWS>
 __device__ __forceinline__ void load_operand_rt(bool mn_major, uint8_t* dst, const CUtensorMap* map,
@@ -97,6 +150,11 @@ __device__ __forceinline__ uint64_t operand_desc_rt(bool mn_major, uint32_t stag
 //                                         true: the coordinates of K block kb
 //                                         (of nkb) are the policy's, not the
 //                                         plain ascending walk along K
+//   kCtaPair                              true: units are 256-row tiles of a
+//                                         CTA pair; coords() gives the tile's
+//                                         origin, the mainloop adds the CTA's
+//                                         128-row offset to both operands, and
+//                                         the epilogue's row runs over 0..255
 // With kPairTiles the tiles of a unit come in pairs (2i, 2i+1) that may use
 // different operands (tile_a_map / tile_b_map / tile_k_blocks(u, q)); the
 // epilogue sees both accumulators at once (epi_pair, after the odd tile) and
@@ -116,6 +174,7 @@ struct SingleRole {
     using Maps = TwoMaps;
     static constexpr bool kPairTiles = false;
     static constexpr bool kKRemap = false;
+    static constexpr bool kCtaPair = false;
     static constexpr int kEpiWarps = 4;
     static constexpr bool kAMn = AMN;
     static constexpr bool kBMn = BMN;
@@ -178,36 +237,50 @@ constexpr int gemm_threads() {
 }
 
 template <class P>
+constexpr uint32_t gemm_smem_bytes() {
+    return RingShape<P::kCtaPair>::smem_bytes;
+}
+
+template <class P>
 __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1)
     gemm_persistent_kernel(const __grid_constant__ typename P::Maps maps, const P p,
                            uint32_t* err) {
+    constexpr bool PAIR = P::kCtaPair;
+    static_assert(!(PAIR && P::kPairTiles), "paired-tile policies run on single CTAs");
+    using Ring = RingShape<PAIR>;
+    constexpr int S = Ring::stages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* a_stages = smem;
-    uint8_t* b_stages = smem + kStages * kAStageBytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-    uint64_t* full = bars;                    // [kStages] TMA -> MMA
-    uint64_t* empty = bars + kStages;         // [kStages] MMA -> TMA
-    uint64_t* tmem_full = bars + 2 * kStages; // [2]       MMA -> epilogue
-    uint64_t* tmem_empty = tmem_full + 2;     // [2]       epilogue -> MMA
-    uint64_t* drain = tmem_empty + 2;         // [1]       MMA self-drain
+    uint8_t* b_stages = smem + S * Ring::a_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Ring::stage_bytes);
+    uint64_t* full = bars;                    // [S] TMA -> MMA (pair: the even CTA's counts both CTAs' bytes)
+    uint64_t* empty = bars + S;               // [S] MMA -> TMA
+    uint64_t* tmem_full = bars + 2 * S;       // [2] MMA -> epilogue
+    uint64_t* tmem_empty = tmem_full + 2;     // [2] epilogue -> MMA (pair: both CTAs' warps)
+    uint64_t* drain = tmem_empty + 2;         // [1] MMA self-drain
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     volatile int* never = abort_flag + 1;     // stays 0: drain waits ignore the abort flag
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // the unit stream of this CTA (pair: of its cluster) and this CTA's row offset in it
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const int wg = PAIR ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+    const int num_wg = PAIR ? static_cast<int>(num_clusters_x()) : static_cast<int>(gridDim.x);
+    const int half_off = static_cast<int>(rank) * kBM;
 
     if (warp == 0 && lane == 0) {
         P::prefetch(maps);
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tmem_full[b], 1);
-            mbar_init(&tmem_empty[b], P::kEpiWarps);   // one arrival per epilogue warp
+            mbar_init(&tmem_empty[b], (PAIR ? 2 : 1) * P::kEpiWarps);   // one arrival per epilogue warp
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -216,11 +289,17 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1)
         fence_proxy_async_smem();
     }
     if (warp == 1) {
-        tmem_alloc(tmem_holder, kTmemCols);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(tmem_holder, kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_holder, kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();       // the peer's barriers exist before any remote arrival
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
@@ -232,7 +311,7 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1)
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_parity = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+            for (int u = wg; ok && u < units; u += num_wg) {
                 const int nt = p.tiles_in_unit(u);
                 const int kblocks = p.k_blocks(u);
                 const bool amn = p.a_mn(u), bmn = p.b_mn(u);
@@ -250,20 +329,35 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1)
                         qk = p.tile_k_blocks(u, q);
                     }
                     for (int kb = 0; kb < qk; ++kb) {
-                        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, kWaitTimeoutNs)) {
+                        const bool got = PAIR
+                            ? mbar_wait_cluster(&empty[stage], phase ^ 1u, abort_flag, kWaitTimeoutNs)
+                            : mbar_wait(&empty[stage], phase ^ 1u, abort_flag, kWaitTimeoutNs);
+                        if (!got) {
                             ok = false;
                             break;
                         }
                         int am = a_mn, ak = a_k + kb * kBK, bm = b_mn, bk = b_k + kb * kBK;
                         if constexpr (P::kKRemap) p.k_remap(kb, qk, am, ak, bm, bk);
-                        mbar_arrive_expect_tx(&full[stage], kStageBytes);
-                        load_operand_rt<kBM>(amn, a_stages + stage * kAStageBytes, qa,
-                                             &full[stage], am, ak);
-                        load_operand_rt<kBN>(bmn, b_stages + stage * kBStageBytes, qb,
-                                             &full[stage], bm, bk);
+                        if constexpr (PAIR) {
+                            // the even CTA's barrier counts both CTAs' bytes: its producer
+                            // announces them with a local arrive, the odd CTA's copies only
+                            // complete on it (no fence on this path)
+                            const uint32_t lf = mapa_shared(smem_u32(&full[stage]), 0);
+                            if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * Ring::stage_bytes);
+                            load_operand_pair_rt<kBM>(amn, a_stages + stage * Ring::a_bytes, qa, lf,
+                                                      am + half_off, ak);
+                            load_operand_pair_rt<Ring::b_rows>(bmn, b_stages + stage * Ring::b_bytes,
+                                                               qb, lf, bm + half_off, bk);
+                        } else {
+                            mbar_arrive_expect_tx(&full[stage], Ring::stage_bytes);
+                            load_operand_rt<kBM>(amn, a_stages + stage * Ring::a_bytes, qa,
+                                                 &full[stage], am, ak);
+                            load_operand_rt<kBN>(bmn, b_stages + stage * Ring::b_bytes, qb,
+                                                 &full[stage], bm, bk);
+                        }
                         issued_mask |= 1u << stage;
                         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                        if (++stage == kStages) {
+                        if (++stage == S) {
                             stage = 0;
                             phase ^= 1u;
                         }
@@ -274,26 +368,35 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1)
                 report_error(err, RLK_DEVERR_WAIT_TIMEOUT);
                 *abort_flag = 1;
             }
-            // let every copy this thread started land before the CTA can exit
-            for (int s = 0; s < kStages; ++s)
-                if (issued_mask & (1u << s))
-                    mbar_wait(&full[s], (issued_parity >> s) & 1u, never, kDrainTimeoutNs);
+            // let every copy this thread started land before the CTA can exit (pair: the
+            // even CTA's MMAs release a stage only after reading it, so a released stage
+            // has landed)
+            for (int s = 0; s < S; ++s)
+                if (issued_mask & (1u << s)) {
+                    if constexpr (PAIR)
+                        mbar_wait_cluster(&empty[s], (issued_parity >> s) & 1u, never, kDrainTimeoutNs);
+                    else
+                        mbar_wait(&full[s], (issued_parity >> s) & 1u, never, kDrainTimeoutNs);
+                }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && (!PAIR || rank == 0)) {
             int stage = 0;
             uint32_t phase = 0;
             uint32_t tile_i = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+            for (int u = wg; ok && u < units; u += num_wg) {
                 const int nt = p.tiles_in_unit(u);
                 const int kblocks = p.k_blocks(u);
                 const bool amn = p.a_mn(u), bmn = p.b_mn(u);
-                const uint32_t idesc = idesc_bf16_f32(kBM, kBN, amn, bmn);
+                const uint32_t idesc = idesc_bf16_f32(PAIR ? kPairM : kBM, kBN, amn, bmn);
                 for (int q = 0; ok && q < nt; ++q, ++tile_i) {
                     const uint32_t buf = tile_i & 1u;
                     const uint32_t use = tile_i >> 1;
-                    if (!mbar_wait(&tmem_empty[buf], (use & 1u) ^ 1u, abort_flag, kWaitTimeoutNs)) {
+                    const bool got = PAIR
+                        ? mbar_wait_cluster(&tmem_empty[buf], (use & 1u) ^ 1u, abort_flag, kWaitTimeoutNs)
+                        : mbar_wait(&tmem_empty[buf], (use & 1u) ^ 1u, abort_flag, kWaitTimeoutNs);
+                    if (!got) {
                         ok = false;
                         break;
                     }
@@ -302,26 +405,42 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1)
                     int qk = kblocks;
                     if constexpr (P::kPairTiles) qk = p.tile_k_blocks(u, q);
                     for (int kb = 0; kb < qk; ++kb) {
-                        if (!mbar_wait(&full[stage], phase, abort_flag, kWaitTimeoutNs)) {
+                        const bool landed = PAIR
+                            ? mbar_wait_cluster(&full[stage], phase, abort_flag, kWaitTimeoutNs)
+                            : mbar_wait(&full[stage], phase, abort_flag, kWaitTimeoutNs);
+                        if (!landed) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t a_addr = smem_u32(a_stages + stage * kAStageBytes);
-                        const uint32_t b_addr = smem_u32(b_stages + stage * kBStageBytes);
+                        const uint32_t a_addr = smem_u32(a_stages + stage * Ring::a_bytes);
+                        const uint32_t b_addr = smem_u32(b_stages + stage * Ring::b_bytes);
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; ++kk) {
-                            mma_bf16_ss(d_tmem, operand_desc_rt(amn, a_addr, kk),
-                                        operand_desc_rt(bmn, b_addr, kk), idesc,
-                                        (kb > 0 || kk > 0) ? 1u : 0u);
+                            if constexpr (PAIR)
+                                mma_bf16_ss_pair(d_tmem, operand_desc_rt(amn, a_addr, kk),
+                                                 operand_desc_rt(bmn, b_addr, kk), idesc,
+                                                 (kb > 0 || kk > 0) ? 1u : 0u);
+                            else
+                                mma_bf16_ss(d_tmem, operand_desc_rt(amn, a_addr, kk),
+                                            operand_desc_rt(bmn, b_addr, kk), idesc,
+                                            (kb > 0 || kk > 0) ? 1u : 0u);
                         }
-                        mma_commit(&empty[stage]);
-                        if (++stage == kStages) {
+                        if constexpr (PAIR)
+                            mma_commit_pair(&empty[stage], 3);
+                        else
+                            mma_commit(&empty[stage]);
+                        if (++stage == S) {
                             stage = 0;
                             phase ^= 1u;
                         }
                     }
-                    if (ok) mma_commit(&tmem_full[buf]);
+                    if (ok) {
+                        if constexpr (PAIR)
+                            mma_commit_pair(&tmem_full[buf], 3);
+                        else
+                            mma_commit(&tmem_full[buf]);
+                    }
                 }
             }
             if (!ok) {
@@ -329,28 +448,34 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1)
                 *abort_flag = 1;
             }
             // every MMA issued by this thread completes before TMEM is freed
-            mma_commit(drain);
+            if constexpr (PAIR)
+                mma_commit_pair(drain, 1);
+            else
+                mma_commit(drain);
             mbar_wait(drain, 0, never, kDrainTimeoutNs);
         }
     } else {
         const int quarter = warp & 3;         // TMEM lanes this warp may access
         const int half = (warp - 2) >> 2;     // column half (0 unless kEpiWarps = 8)
-        const int row = quarter * 32 + lane;
+        const int row = quarter * 32 + lane;  // this thread's accumulator row in the CTA
+        const int prow = half_off + row;      // ... in the unit's tile (pair: 0..255)
         const uint32_t taddr_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
         uint32_t tile_i = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        for (int u = wg; ok && u < units; u += num_wg) {
             typename P::EpiState st;
             if constexpr (P::kPairTiles)
                 p.epi_begin(u, row, half, st);
             else
-                p.epi_begin(u, row, st);
+                p.epi_begin(u, prow, st);
             const int nt = p.tiles_in_unit(u);
             for (int q = 0; q < nt; ++q, ++tile_i) {
                 const uint32_t buf = tile_i & 1u;
                 const uint32_t use = tile_i >> 1;
                 int got = 1;
-                if (lane == 0) got = mbar_wait(&tmem_full[buf], use & 1u, abort_flag, kWaitTimeoutNs);
+                if (lane == 0)
+                    got = PAIR ? mbar_wait_cluster(&tmem_full[buf], use & 1u, abort_flag, kWaitTimeoutNs)
+                               : mbar_wait(&tmem_full[buf], use & 1u, abort_flag, kWaitTimeoutNs);
                 got = __shfl_sync(0xffffffffu, got, 0);
                 if (!got) {
                     ok = false;
@@ -369,17 +494,22 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1)
                     }
                 } else {
                     tc_fence_after();
-                    p.epi_tile(u, q, row, taddr_row + buf * kBN, st);
+                    p.epi_tile(u, q, prow, taddr_row + buf * kBN, st);
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&tmem_empty[buf]);
+                    if (lane == 0) {
+                        if constexpr (PAIR)
+                            mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty[buf]), 0));
+                        else
+                            mbar_arrive(&tmem_empty[buf]);
+                    }
                 }
             }
             if (!ok) break;
             if constexpr (P::kPairTiles)
                 p.epi_end(u, row, half, st);
             else
-                p.epi_end(u, row, st);
+                p.epi_end(u, prow, st);
         }
         if (!ok && lane == 0) {
             report_error(err, RLK_DEVERR_WAIT_TIMEOUT);
@@ -389,10 +519,41 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1)
 
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();       // the peer is done with this CTA's ring and TMEM
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        if constexpr (PAIR)
+            tmem_dealloc_pair(tmem_base, kTmemCols);
+        else
+            tmem_dealloc(tmem_base, kTmemCols);
     }
+}
+
+// Launch of a persistent GEMM: one CTA (pair: one cluster of two) per SM (pair: per
+// two SMs) up to the number of units.
+template <class P>
+cudaError_t launch_persistent(const typename P::Maps& maps, const P& p, long long units,
+                              int num_sms, uint32_t* err, cudaStream_t stream) {
+    auto kern = gemm_persistent_kernel<P>;
+    constexpr uint32_t smem = gemm_smem_bytes<P>();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const long long slots = P::kCtaPair ? num_sms / 2 : num_sms;
+    const long long groups = units < slots ? units : slots;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((P::kCtaPair ? 2 : 1) * (groups > 0 ? groups : 1)));
+    cfg.blockDim = dim3(gemm_threads<P>());
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = P::kCtaPair ? 2 : 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = P::kCtaPair ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, maps, p, err);
 }
 
 }  // namespace rlk

@@ -45,6 +45,7 @@ struct KlFwdPolicy {
     using Maps = KlMaps;
     static constexpr bool kPairTiles = true;
     static constexpr bool kKRemap = false;
+    static constexpr bool kCtaPair = false;
     static constexpr int kEpiWarps = 8;       // two column halves per row
 
     const int64_t* targets;   // nullptr: no selected logp
@@ -78,7 +79,7 @@ struct KlFwdPolicy {
 
     __device__ int num_units() const { return num_m * num_chunks; }
     __device__ void unit(int u, int& m, int& c) const {
-        grouped_unit(u, num_m, num_chunks, kRasterTokenTiles, m, c);
+        grouped_unit(u, num_m, num_chunks, (kRasterTokenRows / kTileM), m, c);
     }
     __device__ int tiles_in_unit(int u) const {
         int m, c;

@@ -18,12 +18,17 @@ constexpr int kFwdTilesPerChunk = 4;        // forward vocab chunk = 1024 column
 constexpr int kFwdChunk = kFwdTilesPerChunk * kTileV;
 constexpr int kBwdChunk = 32768;            // backward vocab chunk (multiple of kTileV)
 constexpr int kMaxBwdChunks = 65536;        // 2^31 / kBwdChunk: chunks of the largest vocabulary
-// Raster groups (visiting order only; no effect on any result): token tiles per
+// Raster groups (visiting order only; no effect on any result): token rows per
 // group for the forward and dS GEMMs, hidden tiles per group for the dW GEMM.
-// A group's share of h (32 x 128 rows, or 8 x 256 columns, of H = 4096) is
-// 33.5 MB, which stays resident in L2 while the other operand streams.
-constexpr int kRasterTokenTiles = 32;
+// A group's share of h (4096 rows, or 8 x 256 columns, of H = 4096) is 33.5 MB,
+// which stays resident in L2 while the other operand streams.
+constexpr int kRasterTokenRows = 4096;
 constexpr int kRasterHiddenTiles = 8;
+// Rows of the tile a CTA pair computes (the forward, dS, dh and dW GEMMs).  Each
+// CTA of the pair loads half of the tile's B operand: K-major B tensor maps of
+// these GEMMs have boxes of kPairBRows rows (their ring slots hold no more).
+constexpr int kUnitM = 256;
+constexpr int kPairBRows = kTileV / 2;
 constexpr int kAuditThreads = 256;
 constexpr int kLossPerThread = 16;          // 4 float4 of each input per thread (loss fragment)
 constexpr int kAuditV3PerThread = 16;       // 4 float4 of each input per thread (audit)
@@ -182,7 +187,8 @@ inline int64_t fwd_num_chunks(int64_t V) {
 // Tensor maps of the backward launches (one role per launch).
 struct BwdStepMaps {
     CUtensorMap h_kmajor;      // hidden [N,H], box {64, 128}: A of the dS recompute
-    CUtensorMap w_kmajor;      // weight [V,H], box {64, 256}: B of the dS recompute
+    CUtensorMap w_kmajor;      // weight [V,H], box {64, 256}: B of the KL dS recompute
+    CUtensorMap w_kmajor_pair; // weight [V,H], box {64, 128}: B of the dS recompute (CTA pair)
     CUtensorMap w_mnmajor;     // weight [V,H], box {64, 64}:  B of the dh GEMM
     CUtensorMap h_mnmajor;     // hidden [N,H], box {64, 64}:  B of the dW GEMM
     CUtensorMap ds_kmajor;     // consumed dS [N, width], box {64, 128}: A of the dh GEMM
