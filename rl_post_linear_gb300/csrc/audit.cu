@@ -162,36 +162,29 @@ __device__ __forceinline__ Acc block_reduce(Acc a) {
     return a;
 }
 
-// Per-thread state of pass 1.  |d| is kept as an order-preserving integer key
-// (non-negative floats order like their bit patterns; NaN maps above every
-// number), the best key's element offset inside the block, and fp32 sums.
+// Per-thread state of one slice: the active count, the slice's largest |d| as an
+// order-preserving integer key (0: no active element) and the offset of its first
+// occurrence (set only when it beats the thread's running best), and fp32 sums.
 struct ThreadAcc {
     int count = 0;
-    uint32_t key = 0;          // 0 = nothing seen (every active |d| has key >= 0 ... see below)
-    int arg = -1;              // offset of the best element inside the block
+    uint32_t key = 0;
+    int arg = -1;
     float sd = 0.f, skl = 0.f;
     uint32_t flags = 0;
 };
 
-// key(|d|) + 1, so that 0 means "no active element yet": ties keep the first
-// (strict comparison), NaN ranks above +inf.
-__device__ __forceinline__ uint32_t abs_key(float d) {
-    const uint32_t bits = __float_as_uint(d) & 0x7fffffffu;
-    return (bits > 0x7f800000u ? 0x7fc00000u : bits) + 1u;
-}
-
-__device__ __forceinline__ void visit3(float nw, float od, uint32_t m, int off, ThreadAcc& a) {
-    if (m == 0) return;
-    const float d = nw - od;
-    const uint32_t key = abs_key(d);
-    const bool better = key > a.key;
-    a.key = better ? key : a.key;
-    a.arg = better ? off : a.arg;
-    a.count += 1;
-    a.sd += d;
-    a.skl += kl_term(d);
-    a.flags |= (key > 0x7f800000u) ? 1u : 0u;    // |d| is inf or NaN
-}
+// The extended audit's terms of one slice seen by one thread: the sum of |d| and
+// the count of clipped ratios (outputs); where the slice's keys go, the block's
+// coarse histogram, the count of exact zeros and the clip thresholds (inputs).
+struct ExtSlice {
+    float sabs = 0.f;
+    int clip = 0;
+    uint32_t* keys;        // the slice's keys in global memory (element 0 of the slice)
+    int64_t valid;         // elements of the slice inside N
+    uint32_t* hist;        // coarse histogram in shared memory
+    uint32_t n_zero;       // running count of |d| == 0 (kept in a register)
+    float clip_lo, clip_hi;
+};
 
 // number of nonzero bytes in a word of four mask bytes
 __device__ __forceinline__ int active_bytes(uint32_t m) {
@@ -213,6 +206,45 @@ inline int64_t audit_pass1_blocks(int64_t N) {
     return slices < kAuditMaxBlocks ? slices : kAuditMaxBlocks;
 }
 
+constexpr int kCoarseWindowLo = 96;                   // exponent field of 2^-31
+constexpr int kCoarseOctaves = 32;                    // window [2^-31, 2)
+constexpr int kCoarseSub = 128;                       // bins per octave (7 mantissa bits)
+constexpr int kCoarseZero = 0;                        // |d| == 0
+constexpr int kCoarseLow = 1;                         // 0 < |d| < 2^-31
+constexpr int kCoarseFirst = 2;                       // first bin of the window
+constexpr int kCoarseHigh = kCoarseFirst + kCoarseOctaves * kCoarseSub;   // |d| >= 2, inf, NaN
+constexpr int kCoarseBins = kCoarseHigh + 1;          // 4099
+
+// bin = (b >> 16) - kCoarseShift inside the window (b = the |d| bits)
+constexpr int kCoarseShift = (kCoarseWindowLo << 7) - kCoarseFirst;     // 12286
+static_assert(kCoarseSub == 128, "bits 30..16 address the window's bins");
+
+// The keys of coarse bin `bin` are the range [lo, lo + span) (the bins preserve order).
+__device__ __forceinline__ void coarse_bin_keys(int bin, uint32_t& lo, uint32_t& span) {
+    if (bin == kCoarseZero) {
+        lo = 1u;
+        span = 1u;
+    } else if (bin == kCoarseLow) {
+        lo = 2u;
+        span = (static_cast<uint32_t>(kCoarseWindowLo) << 23) - 1u;
+    } else if (bin == kCoarseHigh) {
+        lo = (static_cast<uint32_t>(kCoarseWindowLo + kCoarseOctaves) << 23) + 1u;
+        span = 0x7fc00001u - lo + 1u;
+    } else {
+        lo = (static_cast<uint32_t>(bin + kCoarseShift) << 16) + 1u;
+        span = 0x10000u;
+    }
+}
+
+// Coarse bin of nonzero |d| bits b (the key minus 1).  Bits 30..16 of b are the
+// exponent and the top 7 mantissa bits, so inside the window the bin is
+// (b >> 16) - (96 << 7) + kCoarseFirst; below and above the window the same value
+// clamps to kCoarseLow and kCoarseHigh (any NaN lands there too); b = 0 is
+// kCoarseZero, counted apart.
+__device__ __forceinline__ int coarse_bin_nonzero(uint32_t bits) {
+    return min(max(static_cast<int>(bits >> 16) - kCoarseShift, kCoarseLow), kCoarseHigh);
+}
+
 // The order-preserving key of |d| as the running max compares it: the bits of |d|
 // with every NaN mapped to one pattern above inf, plus one, so that 0 means "no
 // active element" (ties keep the first offset: strict comparison).
@@ -232,11 +264,13 @@ __device__ __forceinline__ uint32_t key_of_bits(uint32_t b) {
 // order, on ties) is looked up only when that value beats `best_key`, the thread's
 // running best, since otherwise it is not needed.  a.key is the slice's key, a.arg
 // its first offset when a.key > best_key.
+template <bool EXT = false>
 __device__ __forceinline__ void visit_slice(const float4 (&x)[kVec], const float4 (&y)[kVec],
                                             const uint32_t (&m)[kVec], int tid, uint32_t best_key,
-                                            ThreadAcc& a) {
-    float sd[kVec], skl[kVec];
+                                            ThreadAcc& a, ExtSlice* ext = nullptr) {
+    float sd[kVec], skl[kVec], sab[kVec];
     uint32_t gmax[kVec];
+    int clip = 0;
 #pragma unroll
     for (int j = 0; j < kVec; ++j) {
         a.count += active_bytes(m[j]);
@@ -244,15 +278,40 @@ __device__ __forceinline__ void visit_slice(const float4 (&x)[kVec], const float
         const float ys[4] = {y[j].x, y[j].y, y[j].z, y[j].w};
         sd[j] = 0.f;
         skl[j] = 0.f;
+        sab[j] = 0.f;
         gmax[j] = 0u;
+        uint32_t k4[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const bool act = ((m[j] >> (8 * e)) & 0xffu) != 0u;
             const float d = act ? xs[e] - ys[e] : 0.f;
-            gmax[j] = max(gmax[j], __float_as_uint(d) & 0x7fffffffu);
+            const uint32_t bits = __float_as_uint(d) & 0x7fffffffu;
+            gmax[j] = max(gmax[j], bits);
             sd[j] += d;
             skl[j] += kl_small(d);
+            if constexpr (EXT) {
+                // |exp(d) - 1| > eps  <=>  d > log1p(eps) or d < log1p(-eps); d = 0 when inactive
+                sab[j] += __uint_as_float(bits);
+                clip += (d > ext->clip_hi || d < ext->clip_lo) ? 1 : 0;
+                k4[e] = act ? key_of_bits(bits) : 0u;
+                ext->n_zero += (act && bits == 0u) ? 1u : 0u;
+                if (act && bits != 0u) atomicAdd(&ext->hist[coarse_bin_nonzero(bits)], 1u);
+            }
         }
+        if constexpr (EXT) {          // the group's keys (0 for inactive elements)
+            const int o = j * (kAuditThreads * 4) + tid * 4;
+            if (o + 4 <= ext->valid) {
+                *reinterpret_cast<uint4*>(ext->keys + o) = make_uint4(k4[0], k4[1], k4[2], k4[3]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (o + e < ext->valid) ext->keys[o + e] = k4[e];
+            }
+        }
+    }
+    if constexpr (EXT) {
+        ext->sabs = (sab[0] + sab[1]) + (sab[2] + sab[3]);
+        ext->clip = clip;
     }
     const uint32_t smax = max(max(gmax[0], gmax[1]), max(gmax[2], gmax[3]));
     // an inf or NaN |d| exists exactly when the largest bits reach those of inf
@@ -297,11 +356,11 @@ __device__ __forceinline__ void visit_slice(const float4 (&x)[kVec], const float
 // A slice read straight from global memory: vector loads when VEC (16-byte aligned
 // inputs, whole slice inside N), else element by element with elements past N
 // inactive.  Either way the arithmetic is visit_slice's.
-template <bool VEC>
+template <bool VEC, bool EXT = false>
 __device__ __forceinline__ void load_and_visit_slice(const float* nw, const float* od,
                                                      const uint8_t* mask, int64_t N,
                                                      int64_t base, uint32_t best_key,
-                                                     ThreadAcc& a) {
+                                                     ThreadAcc& a, ExtSlice* ext = nullptr) {
     float4 x[kVec], y[kVec];
     uint32_t m[kVec];
     if (VEC && base + kSlice <= N) {
@@ -332,7 +391,7 @@ __device__ __forceinline__ void load_and_visit_slice(const float* nw, const floa
             m[j] = mv;
         }
     }
-    visit_slice(x, y, m, threadIdx.x, best_key, a);
+    visit_slice<EXT>(x, y, m, threadIdx.x, best_key, a, ext);
 }
 
 // The running state of a block's thread over the block's slices, visited in ascending
@@ -359,8 +418,8 @@ struct RunAcc {
 
 // The block's partial from its kAuditThreads threads: a fixed tree over each
 // warp (float-pair sums, integer counts, key / index max), then the eight warp
-// partials in warp order, written by thread 0.
-__device__ __forceinline__ void finish_block(RunAcc r, AuditPartial* out) {
+// partials in warp order, returned in thread 0 (unspecified in the others).
+__device__ __forceinline__ AuditPartial block_partial(RunAcc r) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
@@ -395,19 +454,19 @@ __device__ __forceinline__ void finish_block(RunAcc r, AuditPartial* out) {
         warp_acc[warp] = w;
     }
     named_barrier(kAuditThreads);
+    AuditPartial p{};
     if (threadIdx.x == 0) {
         Acc t = warp_acc[0];
 #pragma unroll
         for (int w = 1; w < kAuditThreads / 32; ++w) merge(t, warp_acc[w]);
-        AuditPartial p;
         p.count = t.count;
         p.arg = t.arg;
         p.sum_d = t.sum_d;
         p.sum_kl = t.sum_kl;
         p.best = t.best;
         p.flags = t.flags;
-        out[blockIdx.x] = p;
     }
+    return p;
 }
 
 // Pass 1 (any alignment; vector loads when VEC); a second launch merges.
@@ -425,7 +484,8 @@ __global__ void __launch_bounds__(kAuditThreads)
         load_and_visit_slice<VEC>(nw, od, mask, N, sl * kSlice, r.best_key, a);
         r.add_slice(a, sl * kSlice);
     }
-    finish_block(r, out);
+    const AuditPartial p = block_partial(r);
+    if (threadIdx.x == 0) out[blockIdx.x] = p;
 }
 
 constexpr int kMergeThreads = 1024;
@@ -486,173 +546,161 @@ __global__ void __launch_bounds__(kMergeThreads)
 // |d|, mean ratio0 = exp(d), clipfrac0 = #{|exp(d) - 1| > eps} / count, the
 // p50 / p90 / p99 of |d| by the nearest-rank rule (1-based rank
 // ceil(p * count) of the ascending order), and the worst token's sequence and
-// position.  Pass 1 is the base pass plus three more per-thread sums; the
-// percentiles are selected exactly by a three-pass radix select over the
-// order-preserving 32-bit key of |d| (digits of 11, 11 and 10 bits), with
-// integer histograms: the counts, hence the selected values, are exact and
-// reproducible however the atomics interleave.
+// position.
+//
+//   pass 1   the base audit's slices and blocks, plus per thread the sum of |d|
+//            and the clip count; it writes each element's |d| key (the order-
+//            preserving key of the base audit, 0 for inactive elements) and
+//            counts the keys into a coarse histogram: exact zeros, keys below
+//            2^-31, 128 bins per octave over [2^-31, 2), keys from 2 up (inf
+//            and NaN included) -- per block in shared memory, then added to a
+//            global one with integer atomics.
+//   merge    one block: the fixed-order merge of the partials, and for each
+//            percentile the coarse bin holding its rank, with the number of
+//            keys below that bin (an exact integer).
+//   pass 2   reads the keys once and appends those in each percentile's bin to
+//            that percentile's candidate list (in any order: only the multiset
+//            matters).
+//   select   an exact radix select of the remaining rank among each list's
+//            keys (two 8-bit digits inside a bin of the window, three digits of
+//            11, 11 and 9 bits in the bins outside it), counted with integer
+//            histograms.
+// Mean ratio0 = 1 + mean(d) + mean(exp(d) - 1 - d), from the sums the base audit
+// already forms (exact algebra; no exp per element).  The clip test
+// |exp(d) - 1| > eps is d > log1p(eps) or d < log1p(-eps), the two thresholds
+// rounded to fp32 on the host.  Every count is an integer, so the selected
+// values, like the sums, are bitwise reproducible for a given N.
 
 struct ExtPartial {
     AuditPartial base;
-    DFloat sum_abs, sum_ratio;
+    DFloat sum_abs;
     int64_t clip;
 };
 
-// One active element of the extended pass: the base audit's terms, its |d| key,
-// and the sums of |d|, of the ratio exp(d) and the count of clipped ratios.
-__device__ __forceinline__ uint32_t visit_ext(float nv, float ov, int off, float eps,
-                                              ThreadAcc& a, float& sabs, float& sratio,
-                                              int& clip) {
-    visit3(nv, ov, 1u, off, a);
-    const float d = nv - ov;
-    const float r = expf(d);
-    sabs += fabsf(d);
-    sratio += r;
-    clip += fabsf(r - 1.0f) > eps ? 1 : 0;
-    return abs_key(d);
-}
+constexpr int kSelBins = 2048;
+constexpr int kSelPasses = 3;
 
-struct SelectState {
-    uint32_t prefix[3];
-    uint32_t pad;
-    int64_t rank[3];
+// The selection of one percentile after some radix passes.
+struct SelState {
+    int64_t rank;          // 1-based rank left to select among the matching keys; 0: none
+    uint32_t kmask;        // bits of the |d| bits already fixed ...
+    uint32_t kvalue;       // ... and their values
+    int32_t done;          // 1: the value is kvalue
+    int32_t pad;
 };
 
-constexpr int kHistBins = 2048;
-constexpr int kHistBlocksPerSm = 8;
+// The selection state of the three percentiles (p50, p90, p99).  st[p] is the
+// state before radix pass p (st[0] from the merge); the kernel of pass p writes
+// st[p] from st[p - 1], so no kernel overwrites what its own blocks read.
+struct ExtSelect {
+    unsigned long long cand_count[3];   // candidates appended by pass 2
+    int32_t bin[3];                     // coarse bin of the rank
+    int32_t pad;
+    SelState st[kSelPasses][3];
+};
+
+// the radix digit of pass p for a percentile in coarse bin `bin` (bits == 0: no pass)
+__device__ __forceinline__ void sel_digit(int bin, int p, int& shift, int& bits) {
+    if (bin >= kCoarseFirst && bin < kCoarseHigh) {     // the low 16 bits vary inside a bin
+        shift = p == 0 ? 8 : 0;
+        bits = p < 2 ? 8 : 0;
+    } else {                                              // all 31 bits vary
+        shift = p == 0 ? 20 : (p == 1 ? 9 : 0);
+        bits = p < 2 ? 11 : 9;
+    }
+}
+
+// The extended pass 1 deals the slices to min(slices, kExtMaxBlocks) blocks (a fixed
+// partition of its own: three of its blocks are resident on each of 152 SMs).
+constexpr int64_t kExtMaxBlocks = 456;
 
 template <bool VEC>
-__global__ void __launch_bounds__(kAuditThreads)
+__global__ void __launch_bounds__(kAuditThreads, 3)
     audit_ext_pass1(const float* __restrict__ nw, const float* __restrict__ od,
-                    const uint8_t* __restrict__ mask, int64_t N, float eps,
-                    ExtPartial* __restrict__ out, uint32_t* __restrict__ keys) {
-    constexpr int kBlock = kAuditThreads * kAuditV3PerThread;
-    const int64_t base = static_cast<int64_t>(blockIdx.x) * kBlock;
-    ThreadAcc a;
-    float sabs = 0.f, sratio = 0.f;
+                    const uint8_t* __restrict__ mask, int64_t N, float clip_lo, float clip_hi,
+                    ExtPartial* __restrict__ out, uint32_t* __restrict__ keys,
+                    unsigned long long* __restrict__ coarse) {
+    __shared__ uint32_t h[kCoarseBins];
+    for (int i = threadIdx.x; i < kCoarseBins; i += kAuditThreads) h[i] = 0u;
+    __syncthreads();
+    const int64_t slices = (N + kSlice - 1) / kSlice;
+    RunAcc r;
+    DFloat sabs{0.f, 0.f};
     int clip = 0;
-    constexpr int kVec = kAuditV3PerThread / 4;
-    if (VEC && base + kBlock <= N) {
-        // every load first (4 float4 of each input, 4 mask words), then the elements
-        float4 x[kVec], y[kVec];
-        uint32_t m[kVec];
-#pragma unroll
-        for (int j = 0; j < kVec; ++j) {
-            const int64_t i0 = base + j * (kAuditThreads * 4) + threadIdx.x * 4;
-            x[j] = __ldcs(reinterpret_cast<const float4*>(nw + i0));
-            y[j] = __ldcs(reinterpret_cast<const float4*>(od + i0));
-            m[j] = mask == nullptr ? 0x01010101u
-                                   : __ldcs(reinterpret_cast<const unsigned int*>(mask + i0));
-        }
-#pragma unroll
-        for (int j = 0; j < kVec; ++j) {
-            const int o0 = j * (kAuditThreads * 4) + threadIdx.x * 4;
-            const float xs[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
-            const float ys[4] = {y[j].x, y[j].y, y[j].z, y[j].w};
-            uint32_t k4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                k4[e] = ((m[j] >> (8 * e)) & 0xffu) != 0u
-                            ? visit_ext(xs[e], ys[e], o0 + e, eps, a, sabs, sratio, clip)
-                            : 0u;
-            // |d| keys for the percentile passes (0 for inactive tokens)
-            *reinterpret_cast<uint4*>(keys + base + o0) = make_uint4(k4[0], k4[1], k4[2], k4[3]);
-        }
-    } else {
+    ExtSlice x;
+    x.hist = h;
+    x.n_zero = 0u;
+    x.clip_lo = clip_lo;
+    x.clip_hi = clip_hi;
 #pragma unroll 1
-        for (int j = 0; j < kVec; ++j) {
-            const int o0 = j * (kAuditThreads * 4) + threadIdx.x * 4;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int64_t i = base + o0 + e;
-                if (i >= N) continue;
-                const bool act = mask == nullptr || mask[i] != 0;
-                keys[i] = act ? visit_ext(nw[i], od[i], o0 + e, eps, a, sabs, sratio, clip) : 0u;
-            }
-        }
+    for (int64_t sl = blockIdx.x; sl < slices; sl += gridDim.x) {
+        const int64_t base = sl * kSlice;
+        ThreadAcc a;
+        x.keys = keys + base;
+        x.valid = N - base;
+        load_and_visit_slice<VEC, true>(nw, od, mask, N, base, r.best_key, a, &x);
+        r.add_slice(a, base);
+        sabs = df_add(sabs, DFloat{x.sabs, 0.f});
+        clip += x.clip;
     }
+    uint32_t n_zero = x.n_zero;
+    // the block's partial: the base audit's tree, then the same tree for |d| and the clips
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-        const int c = __shfl_down_sync(0xffffffffu, a.count, off);
-        const uint32_t k = __shfl_down_sync(0xffffffffu, a.key, off);
-        const int g = __shfl_down_sync(0xffffffffu, a.arg, off);
-        const float sd = __shfl_down_sync(0xffffffffu, a.sd, off);
-        const float skl = __shfl_down_sync(0xffffffffu, a.skl, off);
-        const uint32_t f = __shfl_down_sync(0xffffffffu, a.flags, off);
-        const float sa = __shfl_down_sync(0xffffffffu, sabs, off);
-        const float sr = __shfl_down_sync(0xffffffffu, sratio, off);
-        const int cl = __shfl_down_sync(0xffffffffu, clip, off);
+        DFloat y;
+        y.hi = __shfl_down_sync(0xffffffffu, sabs.hi, off);
+        y.lo = __shfl_down_sync(0xffffffffu, sabs.lo, off);
+        const int c = __shfl_down_sync(0xffffffffu, clip, off);
+        const uint32_t z0 = __shfl_down_sync(0xffffffffu, n_zero, off);
         if (lane + off < 32) {
-            const bool take = k > a.key || (k == a.key && k != 0 && g < a.arg);
-            a.key = take ? k : a.key;
-            a.arg = take ? g : a.arg;
-            a.count += c;
-            a.sd += sd;
-            a.skl += skl;
-            a.flags |= f;
-            sabs += sa;
-            sratio += sr;
-            clip += cl;
+            sabs = df_add(sabs, y);
+            clip += c;
+            n_zero += z0;
         }
     }
-    __shared__ Acc warp_acc[kAuditThreads / 32];
-    __shared__ float warp_abs[kAuditThreads / 32], warp_ratio[kAuditThreads / 32];
-    __shared__ int warp_clip[kAuditThreads / 32];
+    __shared__ DFloat w_abs[kAuditThreads / 32];
+    __shared__ int w_clip[kAuditThreads / 32];
     if (lane == 0) {
-        Acc w;
-        w.count = a.count;
-        w.arg = a.key == 0 ? INT64_MAX : base + a.arg;
-        w.sum_d = DFloat{a.sd, 0.f};
-        w.sum_kl = DFloat{a.skl, 0.f};
-        w.best = a.key == 0 ? -1.0f : __uint_as_float(a.key - 1u);
-        w.flags = a.flags;
-        warp_acc[warp] = w;
-        warp_abs[warp] = sabs;
-        warp_ratio[warp] = sratio;
-        warp_clip[warp] = clip;
+        w_abs[warp] = sabs;
+        w_clip[warp] = clip;
+        if (n_zero) atomicAdd(&h[kCoarseZero], n_zero);
     }
-    __syncthreads();
+    const AuditPartial bp = block_partial(r);      // its barrier also orders the writes above
+    for (int i = threadIdx.x; i < kCoarseBins; i += kAuditThreads)
+        if (h[i] != 0u) atomicAdd(&coarse[i], static_cast<unsigned long long>(h[i]));
     if (threadIdx.x == 0) {
-        Acc t = warp_acc[0];
-        DFloat sa{warp_abs[0], 0.f}, sr{warp_ratio[0], 0.f};
-        int64_t cl = warp_clip[0];
+        DFloat sa = w_abs[0];
+        int64_t cl = w_clip[0];
 #pragma unroll
         for (int w = 1; w < kAuditThreads / 32; ++w) {
-            merge(t, warp_acc[w]);
-            sa = df_add(sa, DFloat{warp_abs[w], 0.f});
-            sr = df_add(sr, DFloat{warp_ratio[w], 0.f});
-            cl += warp_clip[w];
+            sa = df_add(sa, w_abs[w]);
+            cl += w_clip[w];
         }
-        ExtPartial p;
-        p.base.count = t.count;
-        p.base.arg = t.arg;
-        p.base.sum_d = t.sum_d;
-        p.base.sum_kl = t.sum_kl;
-        p.base.best = t.best;
-        p.base.flags = t.flags;
-        p.sum_abs = sa;
-        p.sum_ratio = sr;
-        p.clip = cl;
-        out[blockIdx.x] = p;
+        ExtPartial ep;
+        ep.base = bp;
+        ep.sum_abs = sa;
+        ep.clip = cl;
+        out[blockIdx.x] = ep;
     }
 }
 
-// One block: fixed-order merge of the partials; writes the sums into the
-// result, the nearest ranks into the select state, clears the histograms.
+// One block: the fixed-order merge of the partials; writes the sums into the
+// result; for each percentile the coarse bin holding its rank and the rank left
+// inside it; clears the candidate counts and the select histograms.
 __global__ void __launch_bounds__(kMergeThreads)
     audit_ext_merge(const ExtPartial* __restrict__ parts, int64_t num_parts,
                     const int64_t* __restrict__ seq_offsets, int64_t num_seqs,
-                    rlk_audit_ext_t* __restrict__ result, SelectState* __restrict__ sel,
-                    uint32_t* __restrict__ hist) {
+                    const unsigned long long* __restrict__ coarse,
+                    rlk_audit_ext_t* __restrict__ result, ExtSelect* __restrict__ sel,
+                    unsigned long long* __restrict__ sel_hist) {
     Acc a = empty_acc();
-    DFloat sa{0.f, 0.f}, sr{0.f, 0.f};
+    DFloat sa{0.f, 0.f};
     int64_t cl = 0;
     // ascending partials per thread, loaded in batches (as in the base audit's merge)
     auto fold = [&](const ExtPartial& p) {
         merge(a, to_acc(p.base));
         sa = df_add(sa, p.sum_abs);
-        sr = df_add(sr, p.sum_ratio);
         cl += p.clip;
     };
     int64_t i = threadIdx.x;
@@ -664,236 +712,337 @@ __global__ void __launch_bounds__(kMergeThreads)
         for (int j = 0; j < kMergeBatch; ++j) fold(p[j]);
     }
     for (; i < num_parts; i += kMergeThreads) fold(parts[i]);
-    for (int i = threadIdx.x; i < 3 * kHistBins; i += kMergeThreads) hist[i] = 0u;
+    for (int k = threadIdx.x; k < kSelPasses * 3 * kSelBins; k += kMergeThreads) sel_hist[k] = 0ull;
     a = block_reduce<kMergeThreads>(a);
-    __shared__ DFloat s_abs[kMergeThreads / 32], s_ratio[kMergeThreads / 32];
+    __shared__ DFloat s_abs[kMergeThreads / 32];
     __shared__ long long s_clip[kMergeThreads / 32];
+    __shared__ long long s_count;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    // the same fixed tree for the three extra sums
+    // the same fixed tree for the two extra sums
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-        DFloat x, y;
+        DFloat x;
         x.hi = __shfl_down_sync(0xffffffffu, sa.hi, off);
         x.lo = __shfl_down_sync(0xffffffffu, sa.lo, off);
-        y.hi = __shfl_down_sync(0xffffffffu, sr.hi, off);
-        y.lo = __shfl_down_sync(0xffffffffu, sr.lo, off);
         const long long z = __shfl_down_sync(0xffffffffu, static_cast<long long>(cl), off);
         if (lane + off < 32) {
             sa = df_add(sa, x);
-            sr = df_add(sr, y);
             cl += z;
         }
     }
     if (lane == 0) {
         s_abs[warp] = sa;
-        s_ratio[warp] = sr;
         s_clip[warp] = cl;
     }
+    if (threadIdx.x == 0) s_count = a.count;
     __syncthreads();
-    if (threadIdx.x != 0) return;
-    for (int w = 1; w < kMergeThreads / 32; ++w) {
-        s_abs[0] = df_add(s_abs[0], s_abs[w]);
-        s_ratio[0] = df_add(s_ratio[0], s_ratio[w]);
-        s_clip[0] += s_clip[w];
-    }
-    rlk_audit_ext_t r;
-    r.active_count = a.count;
-    r.argmax_index = a.count > 0 ? a.arg : -1;
-    r.argmax_seq = -1;
-    r.argmax_pos = -1;
-    if (seq_offsets != nullptr && num_seqs > 0 && a.count > 0) {
-        int64_t lo = 0, hi = num_seqs;      // last s < num_seqs with seq_offsets[s] <= arg
-        while (hi - lo > 1) {
-            const int64_t mid = (lo + hi) >> 1;
-            if (seq_offsets[mid] <= a.arg) lo = mid; else hi = mid;
+    const int64_t count = s_count;
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < kMergeThreads / 32; ++w) {
+            s_abs[0] = df_add(s_abs[0], s_abs[w]);
+            s_clip[0] += s_clip[w];
         }
-        if (a.arg >= seq_offsets[lo] && a.arg < seq_offsets[lo + 1]) {
-            r.argmax_seq = lo;
-            r.argmax_pos = a.arg - seq_offsets[lo];
+        rlk_audit_ext_t r;
+        r.active_count = a.count;
+        r.argmax_index = a.count > 0 ? a.arg : -1;
+        r.argmax_seq = -1;
+        r.argmax_pos = -1;
+        if (seq_offsets != nullptr && num_seqs > 0 && a.count > 0) {
+            int64_t lo = 0, hi = num_seqs;      // last s < num_seqs with seq_offsets[s] <= arg
+            while (hi - lo > 1) {
+                const int64_t mid = (lo + hi) >> 1;
+                if (seq_offsets[mid] <= a.arg) lo = mid; else hi = mid;
+            }
+            if (a.arg >= seq_offsets[lo] && a.arg < seq_offsets[lo + 1]) {
+                r.argmax_seq = lo;
+                r.argmax_pos = a.arg - seq_offsets[lo];
+            }
         }
+        r.clip_count = s_clip[0];
+        const double cnt = static_cast<double>(a.count);
+        r.mean_dlogp = df_value(a.sum_d) / cnt;
+        r.mean_abs_dlogp = df_value(s_abs[0]) / cnt;
+        r.approx_kl = df_value(a.sum_kl) / cnt;
+        // mean exp(d) = 1 + mean d + mean (exp(d) - 1 - d)
+        r.mean_ratio = (cnt + df_value(a.sum_d) + df_value(a.sum_kl)) / cnt;
+        r.max_abs_dlogp = a.count > 0 ? a.best : 0.0f;
+        r.p50_abs_dlogp = r.p90_abs_dlogp = r.p99_abs_dlogp = __int_as_float(0x7fc00000);
+        r.clipfrac = static_cast<float>(static_cast<double>(s_clip[0]) / cnt);
+        r.error_flags = a.flags;
+        *result = r;
     }
-    r.clip_count = s_clip[0];
-    const double cnt = static_cast<double>(a.count);
-    r.mean_dlogp = df_value(a.sum_d) / cnt;
-    r.mean_abs_dlogp = df_value(s_abs[0]) / cnt;
-    r.mean_ratio = df_value(s_ratio[0]) / cnt;
-    r.approx_kl = df_value(a.sum_kl) / cnt;
-    r.max_abs_dlogp = a.count > 0 ? a.best : 0.0f;
-    r.p50_abs_dlogp = r.p90_abs_dlogp = r.p99_abs_dlogp = __int_as_float(0x7fc00000);
-    r.clipfrac = static_cast<float>(static_cast<double>(s_clip[0]) / cnt);
-    r.error_flags = a.flags;
-    *result = r;
+    // each percentile's coarse bin: an exclusive scan of the bins (integers, so exact),
+    // five consecutive bins per thread; the one thread whose run holds the rank walks it
+    constexpr int kRun = (kCoarseBins + kMergeThreads - 1) / kMergeThreads;   // 5
+    __shared__ unsigned long long warp_sum[kMergeThreads / 32];
+    // defaults (no active token: done, rank 0), overwritten below by the thread that finds
+    // each rank; the barrier of the scan orders the two
+    if (threadIdx.x < 3) {
+        SelState st;
+        st.rank = 0;
+        st.kmask = 0u;
+        st.kvalue = 0u;
+        st.done = 1;
+        st.pad = 0;
+        sel->cand_count[threadIdx.x] = 0ull;
+        sel->bin[threadIdx.x] = -1;
+        sel->st[0][threadIdx.x] = st;
+    }
+    unsigned long long c[kRun];
+    unsigned long long run = 0;
+#pragma unroll
+    for (int j = 0; j < kRun; ++j) {
+        const int b = threadIdx.x * kRun + j;
+        c[j] = b < kCoarseBins ? coarse[b] : 0ull;
+        run += c[j];
+    }
+    unsigned long long incl = run;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const unsigned long long o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    unsigned long long before = 0;
+    for (int w = 0; w < warp; ++w) before += warp_sum[w];
+    const unsigned long long excl = before + incl - run;
     const int pct[3] = {50, 90, 99};
     for (int q = 0; q < 3; ++q) {
-        sel->prefix[q] = 0u;
-        sel->rank[q] = (pct[q] * a.count + 99) / 100;   // nearest rank, 1-based (0 if none)
-    }
-}
-
-// Histogram of one digit of the |d| keys of the active elements that match
-// each percentile's prefix so far.
-// One radix-select pass over the |d| keys written by pass 1 (0 = inactive).
-// Pass 0 (top 11 bits) is the same for the three percentiles, so it builds a
-// single histogram; lanes of a warp that hit the same bin add their count with
-// one shared-memory atomic (|d| concentrates in few bins).  Passes 1 and 2
-// count, per percentile, the keys whose higher digits match its prefix.
-// Blocks stride over the 4096-key slices (a grid of a few blocks per SM), so
-// a block adds its shared histogram into the global one once for many slices;
-// the counts are integers, so the totals do not depend on the grid.  Pass 0
-// gives each warp its own copy of the histogram (the few hot bins would
-// otherwise serialise the warps' atomics) and sums the copies at the end.
-template <int PASS>
-__host__ __device__ constexpr int hist_copies() {
-    return PASS == 0 ? kAuditThreads / 32 : 3;
-}
-
-template <int PASS>
-__host__ __device__ constexpr size_t hist_smem_bytes() {
-    return static_cast<size_t>(hist_copies<PASS>()) * kHistBins * 4;
-}
-
-template <int PASS>
-__global__ void __launch_bounds__(kAuditThreads)
-    audit_ext_hist(const uint32_t* __restrict__ keys, int64_t N, int64_t num_slices,
-                   const SelectState* __restrict__ sel, uint32_t* __restrict__ hist) {
-    constexpr int kShift = PASS == 0 ? 21 : (PASS == 1 ? 10 : 0);
-    constexpr uint32_t kDigitMask = PASS == 2 ? 0x3ffu : 0x7ffu;
-    constexpr int kPrefixShift = PASS == 1 ? 21 : 10;
-    constexpr int kHists = PASS == 0 ? 1 : 3;
-    constexpr int kCopies = hist_copies<PASS>();
-    extern __shared__ uint32_t h[];                 // [kCopies][kHistBins]
-    for (int i = threadIdx.x; i < kCopies * kHistBins; i += kAuditThreads) h[i] = 0u;
-    uint32_t* hw = h + (PASS == 0 ? (threadIdx.x >> 5) * kHistBins : 0);   // this warp's copy
-    uint32_t pre[3];
-    bool want[3];
-#pragma unroll
-    for (int q = 0; q < 3; ++q) {
-        pre[q] = sel->prefix[q];
-        want[q] = sel->rank[q] > 0;
-    }
-    __syncthreads();
-    for (int64_t slice = blockIdx.x; slice < num_slices && (PASS > 0 || want[0] || want[1] ||
-                                                            want[2]);
-         slice += gridDim.x) {
-        constexpr int kBlock = kAuditThreads * kAuditV3PerThread;
-        const int64_t base = slice * kBlock;
-        const int lane = threadIdx.x & 31;
-        constexpr int kVec = kAuditV3PerThread / 4;
-        uint32_t k[kVec][4];
-        // every load first, then the counting (the atomics would otherwise keep the
-        // compiler from moving later loads ahead)
-#pragma unroll
-        for (int j = 0; j < kVec; ++j) {
-            const int64_t i0 = base + j * (kAuditThreads * 4) + threadIdx.x * 4;
-            if (i0 + 4 <= N) {
-                const uint4 v = __ldcs(reinterpret_cast<const uint4*>(keys + i0));
-                k[j][0] = v.x;
-                k[j][1] = v.y;
-                k[j][2] = v.z;
-                k[j][3] = v.w;
-            } else {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) k[j][e] = i0 + e < N ? keys[i0 + e] : 0u;
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < kVec; ++j) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const uint32_t key = k[j][e];
-                const uint32_t digit = (key >> kShift) & kDigitMask;
-                if (PASS == 0) {
-                    // every lane reaches this point: aggregate equal bins across the warp
-                    const unsigned valid = __ballot_sync(0xffffffffu, key != 0u);
-                    if (key != 0u) {
-                        const unsigned peers = __match_any_sync(valid, digit);
-                        if (lane == __ffs(peers) - 1) atomicAdd(&hw[digit], __popc(peers));
-                    }
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 3; ++q)
-                        if (key != 0u && want[q] && (key >> kPrefixShift) == pre[q])
-                            atomicAdd(&h[q * kHistBins + digit], 1u);
-                }
-            }
-        }
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < kHists * kHistBins; i += kAuditThreads) {
-        uint32_t c = h[i];
-        if constexpr (PASS == 0) {
-#pragma unroll
-            for (int w = 1; w < kCopies; ++w) c += h[w * kHistBins + i];
-        }
-        if (c != 0u) atomicAdd(&hist[i], c);
-    }
-}
-
-// Picks, for each percentile, the bin holding its rank; extends the prefix by
-// that digit and clears the histogram for the next pass.  After the last pass
-// the prefix is the selected key, written to the result.  Each of the 256
-// threads owns a run of consecutive bins; an exclusive scan of the runs' counts
-// (integers, so exact) tells the one thread whose run holds the rank, and that
-// thread walks its own run.
-constexpr int kSelectThreads = 256;
-
-template <int PASS>
-__global__ void __launch_bounds__(kSelectThreads)
-    audit_ext_select(SelectState* __restrict__ sel, uint32_t* __restrict__ hist,
-                     rlk_audit_ext_t* __restrict__ result) {
-    constexpr int kBits = PASS == 2 ? 10 : 11;
-    constexpr int kRun = (1 << kBits) / kSelectThreads;     // 8 bins (4 in the last pass)
-    __shared__ int64_t warp_sum[kSelectThreads / 32];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int q = 0; q < 3; ++q) {
-        const int64_t rank = sel->rank[q];           // the same for every thread
-        if (rank <= 0) continue;
-        const uint32_t* hq = hist + (PASS == 0 ? 0 : q * kHistBins) + threadIdx.x * kRun;
-        uint32_t c[kRun];
-        int64_t run = 0;
-#pragma unroll
-        for (int j = 0; j < kRun; ++j) {
-            c[j] = hq[j];
-            run += c[j];
-        }
-        // inclusive scan over the block: lanes, then warps in order
-        int64_t incl = run;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int64_t o = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += o;
-        }
-        if (lane == 31) warp_sum[warp] = incl;
-        __syncthreads();
-        int64_t before = 0;
-        for (int w = 0; w < warp; ++w) before += warp_sum[w];
-        const int64_t excl = before + incl - run;
-        if (excl < rank && rank <= excl + run) {
-            int64_t cum = excl;                      // count below the selected bin
+        const int64_t rank = (pct[q] * count + 99) / 100;   // nearest rank, 1-based (0 if none)
+        if (rank <= 0) continue;                            // st[0][q] says done, rank 0
+        const unsigned long long rk = static_cast<unsigned long long>(rank);
+        if (excl < rk && rk <= excl + run) {               // exactly one thread
+            unsigned long long cum = excl;
             int bin = -1;
 #pragma unroll
             for (int j = 0; j < kRun; ++j) {
                 if (bin < 0) {
-                    if (rank <= cum + c[j])
-                        bin = j;
-                    else
-                        cum += c[j];
+                    if (rk <= cum + c[j]) bin = threadIdx.x * kRun + j;
+                    else cum += c[j];
                 }
             }
-            const uint32_t digit = static_cast<uint32_t>(threadIdx.x * kRun + bin);
-            sel->rank[q] = rank - cum;
-            sel->prefix[q] = (sel->prefix[q] << kBits) | digit;
-            if (PASS == 2) {
-                const float v = __uint_as_float(sel->prefix[q] - 1u);
-                if (q == 0) result->p50_abs_dlogp = v;
-                if (q == 1) result->p90_abs_dlogp = v;
-                if (q == 2) result->p99_abs_dlogp = v;
+            SelState st;
+            st.rank = static_cast<int64_t>(rk - cum);
+            st.kmask = 0u;
+            st.kvalue = 0u;
+            st.done = 0;
+            st.pad = 0;
+            if (bin == kCoarseZero) {                 // every key in the bin is |d| = 0
+                st.done = 1;
+            } else if (bin >= kCoarseFirst && bin < kCoarseHigh) {
+                // the bin fixes the exponent and the top 7 mantissa bits
+                st.kmask = 0x7fff0000u;
+                st.kvalue =
+                    (static_cast<uint32_t>((bin - kCoarseFirst) >> 7) + kCoarseWindowLo) << 23 |
+                    (static_cast<uint32_t>((bin - kCoarseFirst) & 0x7f) << 16);
+            }
+            sel->bin[q] = bin;
+            sel->st[0][q] = st;
+        }
+    }
+}
+
+// Pass 2 puts every key in a percentile's coarse bin in that percentile's candidate
+// list, in any order (only the multiset matters); kCandStage keys per list are
+// staged in shared memory first.
+constexpr int kCandStage = 2048;
+
+__device__ __forceinline__ void collect_key(uint32_t key, const uint32_t (&lo)[3],
+                                            const uint32_t (&span)[3], unsigned* s_n,
+                                            uint32_t (*stage)[kCandStage], ExtSelect* sel,
+                                            uint32_t* cand, int64_t cand_stride) {
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+        if (key - lo[q] < span[q]) {          // inactive keys (0) are below every range
+            const unsigned pos = atomicAdd(&s_n[q], 1u);
+            if (pos < kCandStage) {
+                stage[q][pos] = key;
+            } else {                  // the stage is full: straight to the global list
+                const unsigned long long g = atomicAdd(&sel->cand_count[q], 1ull);
+                cand[q * cand_stride + static_cast<int64_t>(g)] = key;
             }
         }
-        __syncthreads();                             // warp_sum is reused for the next q
+    }
+}
+
+// Pass 2 reads the keys as a plain stream (16 bytes per thread and iteration, the
+// whole grid sweeping them front to back; the candidate multiset does not depend on
+// it).  A block stages its candidates in shared memory (a shared atomic per
+// candidate: they are rare) and, at the end, reserves room in each global list with
+// one atomic; what does not fit in the stage goes to the global list at once.
+__global__ void __launch_bounds__(kAuditThreads)
+    audit_ext_collect(const uint32_t* __restrict__ keys, int64_t N, ExtSelect* __restrict__ sel,
+                      uint32_t* __restrict__ cand, int64_t cand_stride) {
+    __shared__ uint32_t stage[3][kCandStage];
+    __shared__ unsigned s_n[3];
+    __shared__ unsigned long long s_base[3];
+    // each percentile's key range; an empty range (span 0) for one already known
+    uint32_t lo[3], span[3];
+    bool need = false;
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+        lo[q] = 0u;
+        span[q] = 0u;
+        if (!sel->st[0][q].done) {
+            coarse_bin_keys(sel->bin[q], lo[q], span[q]);
+            need = true;
+        }
+    }
+    if (!need) return;
+    if (threadIdx.x < 3) s_n[threadIdx.x] = 0u;
+    __syncthreads();
+    const int64_t n4 = N / 4;
+    const uint4* k4 = reinterpret_cast<const uint4*>(keys);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kAuditThreads;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kAuditThreads + threadIdx.x; i < n4;
+         i += stride) {
+        const uint4 v = __ldcs(k4 + i);
+        collect_key(v.x, lo, span, s_n, stage, sel, cand, cand_stride);
+        collect_key(v.y, lo, span, s_n, stage, sel, cand, cand_stride);
+        collect_key(v.z, lo, span, s_n, stage, sel, cand, cand_stride);
+        collect_key(v.w, lo, span, s_n, stage, sel, cand, cand_stride);
+    }
+    if (blockIdx.x == 0 && threadIdx.x < N - n4 * 4)     // the last N mod 4 keys
+        collect_key(keys[n4 * 4 + threadIdx.x], lo, span, s_n, stage, sel, cand, cand_stride);
+    __syncthreads();
+    if (threadIdx.x < 3) {
+        const unsigned n = min(s_n[threadIdx.x], static_cast<unsigned>(kCandStage));
+        s_base[threadIdx.x] = n > 0u ? atomicAdd(&sel->cand_count[threadIdx.x],
+                                                 static_cast<unsigned long long>(n))
+                                     : 0ull;
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < 3 * kHistBins; i += kSelectThreads) hist[i] = 0u;
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+        const unsigned n = min(s_n[q], static_cast<unsigned>(kCandStage));
+        for (unsigned i = threadIdx.x; i < n; i += kAuditThreads)
+            cand[q * cand_stride + static_cast<int64_t>(s_base[q]) + i] = stage[q][i];
+    }
+}
+
+// The select step after radix pass p of percentile q: the digit whose bin holds
+// the rank (an exclusive scan of the 2^bits counts, exact), appended to the known
+// bits.  Run identically by every block of the next pass and by the final step.
+__device__ void sel_step(int q, int p, int bin, const unsigned long long* __restrict__ sel_hist,
+                         SelState& st) {
+    __shared__ unsigned long long warp_sum[kAuditThreads / 32];
+    __shared__ uint32_t s_digit;
+    __shared__ int64_t s_rank;
+    int shift, bits;
+    sel_digit(bin, p, shift, bits);
+    if (st.done || bits == 0) return;                  // block-uniform
+    if (threadIdx.x == 0) {                            // (always overwritten: the counts are exact)
+        s_digit = 0u;
+        s_rank = 1;
+    }
+    const int nb = 1 << bits;
+    const int runl = nb / kAuditThreads;                 // 8, or 2 for 9 bits
+    const unsigned long long* hq = sel_hist + (static_cast<int64_t>(p) * 3 + q) * kSelBins;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned long long c[8];
+    unsigned long long run = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        c[j] = j < runl ? hq[threadIdx.x * runl + j] : 0ull;
+        run += c[j];
+    }
+    unsigned long long incl = run;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const unsigned long long o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    unsigned long long before = 0;
+    for (int w = 0; w < warp; ++w) before += warp_sum[w];
+    const unsigned long long excl = before + incl - run;
+    const unsigned long long rk = static_cast<unsigned long long>(st.rank);
+    if (excl < rk && rk <= excl + run) {
+        unsigned long long cum = excl;
+        int dg = -1;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (dg < 0 && j < runl) {
+                if (rk <= cum + c[j]) dg = threadIdx.x * runl + j;
+                else cum += c[j];
+            }
+        }
+        s_digit = static_cast<uint32_t>(dg);
+        s_rank = static_cast<int64_t>(rk - cum);
+    }
+    __syncthreads();
+    const uint32_t dmask = static_cast<uint32_t>(nb - 1) << shift;
+    st.kmask |= dmask;
+    st.kvalue = (st.kvalue & ~dmask) | (s_digit << shift);
+    st.rank = s_rank;
+    int s2, b2;
+    sel_digit(bin, p + 1, s2, b2);
+    st.done = (p + 1 >= kSelPasses || b2 == 0) ? 1 : 0;
+    __syncthreads();
+}
+
+// Radix pass p over each percentile's candidates (blockIdx.y = percentile): the
+// histogram of digit p among the candidates that match the bits known so far.
+// For p > 0 every block first repeats the select step of pass p - 1; block 0
+// stores its outcome.
+template <int P>
+__global__ void __launch_bounds__(kAuditThreads)
+    audit_ext_radix(ExtSelect* __restrict__ sel, const uint32_t* __restrict__ cand,
+                    int64_t cand_stride, unsigned long long* __restrict__ sel_hist) {
+    const int q = blockIdx.y;
+    const int bin = sel->bin[q];
+    SelState st = sel->st[P == 0 ? 0 : P - 1][q];
+    if (P > 0) {
+        sel_step(q, P - 1, bin, sel_hist, st);
+        if (blockIdx.x == 0 && threadIdx.x == 0) sel->st[P][q] = st;
+    }
+    if (st.done) return;                                // block-uniform
+    const uint32_t kmask = st.kmask, kvalue = st.kvalue;
+    int shift, bits;
+    sel_digit(bin, P, shift, bits);
+    const uint32_t dmask = (1u << bits) - 1u;
+    __shared__ uint32_t h[kSelBins];
+    for (int i = threadIdx.x; i < kSelBins; i += kAuditThreads) h[i] = 0u;
+    __syncthreads();
+    const int64_t n = static_cast<int64_t>(sel->cand_count[q]);
+    const uint32_t* cq = cand + q * cand_stride;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kAuditThreads + threadIdx.x; i - threadIdx.x < n;
+         i += static_cast<int64_t>(gridDim.x) * kAuditThreads) {
+        const bool in = i < n;
+        const uint32_t b = in ? cq[i] - 1u : 0u;
+        const bool match = in && (b & kmask) == kvalue;
+        const uint32_t digit = (b >> shift) & dmask;
+        // equal digits within the warp add up in one atomic (many equal keys are common)
+        const unsigned act = __ballot_sync(0xffffffffu, match);
+        if (match) {
+            const unsigned peers = __match_any_sync(act, digit);
+            if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&h[digit], __popc(peers));
+        }
+    }
+    __syncthreads();
+    unsigned long long* gh = sel_hist + (static_cast<int64_t>(P) * 3 + q) * kSelBins;
+    for (int i = threadIdx.x; i < (1 << bits); i += kAuditThreads)
+        if (h[i] != 0u) atomicAdd(&gh[i], static_cast<unsigned long long>(h[i]));
+}
+
+// The last select step; the selected |d| bits become p50 / p90 / p99.
+__global__ void __launch_bounds__(kAuditThreads)
+    audit_ext_finish(const ExtSelect* __restrict__ sel,
+                     const unsigned long long* __restrict__ sel_hist,
+                     rlk_audit_ext_t* __restrict__ result) {
+    for (int q = 0; q < 3; ++q) {
+        SelState st = sel->st[kSelPasses - 1][q];
+        if (st.rank <= 0) continue;                      // no active token: NaN stays
+        sel_step(q, kSelPasses - 1, sel->bin[q], sel_hist, st);
+        if (threadIdx.x == 0) {
+            const float v = __uint_as_float(st.kvalue);
+            if (q == 0) result->p50_abs_dlogp = v;
+            if (q == 1) result->p90_abs_dlogp = v;
+            if (q == 2) result->p99_abs_dlogp = v;
+        }
+    }
 }
 
 }  // namespace
@@ -996,58 +1145,66 @@ cudaError_t launch_audit(const float* logp_new, const float* logp_old, const uin
     return cudaLaunchKernelEx(&cfg, audit_pass2, cparts, nparts, result);
 }
 
-// partials | 3 histograms | select state | |d| keys [N] (uint32)
-static size_t ext_keys_off(int64_t N) {
-    return align_up(align_up(audit_v3_blocks(N) * sizeof(ExtPartial), 256) + 3 * kHistBins * 4 +
-                    sizeof(SelectState), 256);
-}
+// extended audit workspace: partials | coarse histogram | select state | select
+// histograms | |d| keys [N] | candidate lists [3][N] (uint32)
+struct ExtLayout {
+    size_t coarse_off, sel_off, hist_off, keys_off, cand_off, total;
+    explicit ExtLayout(int64_t N) {
+        coarse_off = align_up(static_cast<size_t>(kExtMaxBlocks) * sizeof(ExtPartial), 256);
+        sel_off = align_up(coarse_off + kCoarseBins * sizeof(unsigned long long), 256);
+        hist_off = align_up(sel_off + sizeof(ExtSelect), 256);
+        keys_off = align_up(hist_off + kSelPasses * 3 * kSelBins * sizeof(unsigned long long), 256);
+        cand_off = align_up(keys_off + static_cast<size_t>(N) * 4, 256);
+        total = align_up(cand_off + 3 * static_cast<size_t>(N) * 4, 256) + 256;
+    }
+};
 
-size_t audit_ext_workspace(int64_t N) {
-    return ext_keys_off(N) + align_up(static_cast<size_t>(N) * 4, 256) + 256;
-}
+size_t audit_ext_workspace(int64_t N) { return ExtLayout(N).total; }
 
 cudaError_t launch_audit_ext(const float* logp_new, const float* logp_old, const uint8_t* mask,
                              int64_t N, const int64_t* seq_offsets, int64_t num_seqs, float eps,
                              rlk_audit_ext_t* result, void* workspace, bool vec_ok, int sms,
                              cudaStream_t stream) {
-    const size_t blocks = audit_v3_blocks(N);
+    const ExtLayout lay(N);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     ExtPartial* parts = reinterpret_cast<ExtPartial*>(ws);
-    uint32_t* hist = reinterpret_cast<uint32_t*>(ws + align_up(blocks * sizeof(ExtPartial), 256));
-    SelectState* sel = reinterpret_cast<SelectState*>(hist + 3 * kHistBins);
-    uint32_t* keys = reinterpret_cast<uint32_t*>(ws + ext_keys_off(N));
-    const unsigned grid = static_cast<unsigned>(blocks);
-    // the histogram passes: as many blocks as fit on the SMs, striding over the slices
-    const size_t smem0 = hist_smem_bytes<0>(), smem12 = hist_smem_bytes<1>();
-    const size_t per_sm0 = std::min<size_t>(kHistBlocksPerSm, (200u << 10) / smem0);
-    const unsigned hgrid0 =
-        static_cast<unsigned>(std::min<size_t>(blocks, static_cast<size_t>(sms) * per_sm0));
-    const unsigned hgrid =
-        static_cast<unsigned>(std::min<size_t>(blocks, static_cast<size_t>(sms) * kHistBlocksPerSm));
-    const int64_t slices = static_cast<int64_t>(blocks);
-    if (blocks > 0) {
-        cudaError_t e = cudaFuncSetAttribute(audit_ext_hist<0>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem0));
-        if (e != cudaSuccess) return e;
-    }
+    unsigned long long* coarse = reinterpret_cast<unsigned long long*>(ws + lay.coarse_off);
+    ExtSelect* sel = reinterpret_cast<ExtSelect*>(ws + lay.sel_off);
+    unsigned long long* sel_hist = reinterpret_cast<unsigned long long*>(ws + lay.hist_off);
+    uint32_t* keys = reinterpret_cast<uint32_t*>(ws + lay.keys_off);
+    uint32_t* cand = reinterpret_cast<uint32_t*>(ws + lay.cand_off);
+    const int64_t cand_stride = N;
+    // the clip thresholds of |exp(d) - 1| > eps, rounded to fp32 once
+    const double e = static_cast<double>(eps);
+    const float clip_hi = static_cast<float>(std::log1p(e));
+    const float clip_lo = e < 1.0 ? static_cast<float>(std::log1p(-e)) : -INFINITY;
+    const int64_t slices = static_cast<int64_t>(audit_v3_blocks(N));
+    const unsigned blocks = static_cast<unsigned>(std::min<int64_t>(slices, kExtMaxBlocks));
+    cudaError_t err = cudaMemsetAsync(coarse, 0, kCoarseBins * sizeof(unsigned long long), stream);
+    if (err != cudaSuccess) return err;
     if (blocks > 0) {
         if (vec_ok)
-            audit_ext_pass1<true><<<grid, kAuditThreads, 0, stream>>>(logp_new, logp_old, mask, N,
-                                                                      eps, parts, keys);
+            audit_ext_pass1<true><<<blocks, kAuditThreads, 0, stream>>>(
+                logp_new, logp_old, mask, N, clip_lo, clip_hi, parts, keys, coarse);
         else
-            audit_ext_pass1<false><<<grid, kAuditThreads, 0, stream>>>(logp_new, logp_old, mask,
-                                                                       N, eps, parts, keys);
+            audit_ext_pass1<false><<<blocks, kAuditThreads, 0, stream>>>(
+                logp_new, logp_old, mask, N, clip_lo, clip_hi, parts, keys, coarse);
     }
     audit_ext_merge<<<1, kMergeThreads, 0, stream>>>(parts, static_cast<int64_t>(blocks),
-                                                     seq_offsets, num_seqs, result, sel, hist);
+                                                     seq_offsets, num_seqs, coarse, result, sel,
+                                                     sel_hist);
     if (blocks > 0) {
-        audit_ext_hist<0><<<hgrid0, kAuditThreads, smem0, stream>>>(keys, N, slices, sel, hist);
-        audit_ext_select<0><<<1, kSelectThreads, 0, stream>>>(sel, hist, result);
-        audit_ext_hist<1><<<hgrid, kAuditThreads, smem12, stream>>>(keys, N, slices, sel, hist);
-        audit_ext_select<1><<<1, kSelectThreads, 0, stream>>>(sel, hist, result);
-        audit_ext_hist<2><<<hgrid, kAuditThreads, smem12, stream>>>(keys, N, slices, sel, hist);
-        audit_ext_select<2><<<1, kSelectThreads, 0, stream>>>(sel, hist, result);
+        // the candidate scan: eight blocks per SM at most (the candidate lists do not depend
+        // on the grid)
+        const unsigned cgrid = static_cast<unsigned>(std::max<int64_t>(
+            1, std::min<int64_t>((N / 4 + kAuditThreads - 1) / kAuditThreads,
+                                 8 * static_cast<int64_t>(sms > 0 ? sms : 1))));
+        audit_ext_collect<<<cgrid, kAuditThreads, 0, stream>>>(keys, N, sel, cand, cand_stride);
+        const dim3 rg(blocks, 3);
+        audit_ext_radix<0><<<rg, kAuditThreads, 0, stream>>>(sel, cand, cand_stride, sel_hist);
+        audit_ext_radix<1><<<rg, kAuditThreads, 0, stream>>>(sel, cand, cand_stride, sel_hist);
+        audit_ext_radix<2><<<rg, kAuditThreads, 0, stream>>>(sel, cand, cand_stride, sel_hist);
+        audit_ext_finish<<<1, kAuditThreads, 0, stream>>>(sel, sel_hist, result);
     }
     return cudaGetLastError();
 }
