@@ -472,8 +472,13 @@ def measure_next_rows(rlk, dev, pk, warmup, steps, state):
     del ws_eb
     res["entropy_fwd"] = {"ms": ms_f, "tflops": fwd_flops / (ms_f * 1e-3) / 1e12,
                           "frac_of_peak": fwd_flops / (ms_f * 1e-3) / 1e12 / peak}
+    # executed: the dS recompute (2 N H V) and the dh and dW GEMMs over the hi and lo planes
+    # of dS (4 N H V each)
+    ent_exec = 2.5 * bwd_flops
     res["entropy_bwd"] = {"ms": ms_b, "tflops": bwd_flops / (ms_b * 1e-3) / 1e12,
-                          "frac_of_peak": bwd_flops / (ms_b * 1e-3) / 1e12 / peak}
+                          "frac_of_peak": bwd_flops / (ms_b * 1e-3) / 1e12 / peak,
+                          "executed_tflops": ent_exec / (ms_b * 1e-3) / 1e12,
+                          "executed_frac_of_peak": ent_exec / (ms_b * 1e-3) / 1e12 / peak}
 
     # NEXT-3: full-vocabulary KL against a reference head of the same shape (a frozen
     # reference policy); forward 2 N V (H + Hr) FLOP, backward 4 N H V algorithmic (dh, dW;
@@ -500,9 +505,13 @@ def measure_next_rows(rlk, dev, pk, warmup, steps, state):
                      "frac_of_peak": kl_fwd_flops / (ms_f * 1e-3) / 1e12 / peak,
                      "reference_head": "same shape as the policy head",
                      "mean_kl": float(kl.float().mean())}
+    # executed: both heads recomputed (2 N V (H + Hr)) and the dh and dW GEMMs over the hi
+    # and lo planes of dS (4 N H V each)
+    kl_exec = 2.0 * bwd_flops + kl_fwd_flops
     res["kl_bwd"] = {"ms": ms_b, "tflops": bwd_flops / (ms_b * 1e-3) / 1e12,
                      "frac_of_peak": bwd_flops / (ms_b * 1e-3) / 1e12 / peak,
-                     "executed_tflops": (bwd_flops + kl_fwd_flops) / (ms_b * 1e-3) / 1e12}
+                     "executed_tflops": kl_exec / (ms_b * 1e-3) / 1e12,
+                     "executed_frac_of_peak": kl_exec / (ms_b * 1e-3) / 1e12 / peak}
     del hid_r, wt_r, ws_klb
     torch.cuda.empty_cache()
 
@@ -529,8 +538,9 @@ def measure_next_rows(rlk, dev, pk, warmup, steps, state):
     res["audit_ext_2p26"] = {"ms": ms, "gbs": na * 9 / (ms * 1e-3) / 1e9,
                              "frac_of_hbm": na * 9 / (ms * 1e-3) / 1e9 / hbm,
                              "bytes": na * 9,
-                             "note": "algorithmic 9 B/token; the exact percentiles read the "
-                                     "4-byte |d| keys again in three radix-select passes"}
+                             "note": "algorithmic 9 B/token; pass 1 also writes the 4-byte "
+                                     "|d| keys, which one scan reads back to collect the "
+                                     "percentiles' candidates"}
     adv = torch.randn(na, device=dev, generator=gen)
     grad = torch.empty(na, dtype=torch.float32, device=dev)
     r_loss = torch.empty(rlk.GRPO_RESULT_BYTES, dtype=torch.uint8, device=dev)
