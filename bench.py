@@ -581,7 +581,7 @@ def measure_deepseek(rlk, dev, peak, warmup, steps):
     fwd = {"workload": w.name, "n_active": w.n_active, "ms": ms,
            "tokens_per_s": w.n_active / (ms * 1e-3), "tflops_active": act,
            "frac_of_peak_active": act / peak,
-           "note": "masked rows are compacted away before the GEMM (ceil(N_a/128) row tiles)"}
+           "note": "masked rows are compacted away before the GEMM (ceil(N_a/256) row tiles)"}
 
     g_host = np.random.default_rng(5).standard_normal(w.n).astype(np.float32) / w.n_active
     g_host[w.mask.numpy() == 0] = 0.0

@@ -700,16 +700,21 @@ rlk_status_t rlk_dlogp_audit_noalloc(const float* logp_new, const float* logp_ol
 const char* rlk_contract_string(void) {
     return "rlk-gb300 linear_logp v1; arch=sm_103a; nvcc=" RLK_STR(__CUDACC_VER_MAJOR__) "." RLK_STR(
         __CUDACC_VER_MINOR__) "; inputs=bf16; accum=fp32 (tcgen05 kind::f16, TMEM); "
-                              "tile=128x256x64 cta_group::1, no split-K; "
+                              "tiles: 256x256x64 on CTA pairs (cta_group::2) for the logp "
+                              "and entropy GEMMs, 128x256x64 (cta_group::1) for the KL GEMMs; "
+                              "no split-K; "
                               "fwd_vocab_chunk=1024 (merge ascending); bwd_vocab_chunk=32768; "
                               "masked batches: active rows compacted (ascending) before the "
                               "forward and backward GEMMs; "
                               "exp=ex2.approx.ftz, log=lg2.approx.ftz; k=fp32(log2(e)/T); "
                               "logits never rounded; logp/lse fp32; dS bf16 (target and "
-                              "dominant-class terms fp32); "
+                              "dominant-class terms fp32; entropy and KL: hi and lo bf16 "
+                              "planes); "
                               "dh/dW rounded once to bf16 (RNE); no float atomics; "
                               "audit: 4096-element slices dealt round-robin to min(slices, 608) "
-                              "blocks, fixed trees, float-pair (two-sum) partials";
+                              "blocks, fixed trees, float-pair (two-sum) partials; "
+                              "data-parallel dW: fp32 partials merged in rank order, one "
+                              "rounding";
 }
 
 const char* rlk_status_string(rlk_status_t status) {

@@ -30,9 +30,14 @@
 // the forward's gather): h, dS and dh_acc rows are then compacted rows, the K
 // loop of dW runs over ceil(N_active / 64) blocks, and each dh row is written at
 // its token; the inactive tokens' dh rows are zeroed apart.
-// one persistent launch per role and chunk, in that order (measured faster
+// Each role is one persistent launch per chunk, in that order (measured faster
 // than putting roles of neighbouring chunks side by side in one launch: alone,
-// each role keeps its L2 working set).
+// each role keeps its L2 working set), on CTA pairs with 256 x 256 tiles.
+// For the entropy and KL backwards, whose gradients have no fp32 part that
+// dominates a row, dS is stored as two bf16 planes, hi = bf16(dS) and
+// lo = bf16(dS - hi); the dh and dW K loops run over both planes against the
+// same W (or h) blocks, so dS enters the products with about 16 significant
+// bits.
 // None of the reductions is split or done with atomics: dh_t depends only on
 // row t's inputs and the fixed chunk boundaries, so it is batch invariant;
 // dW is reproducible bit for bit.

@@ -14,9 +14,10 @@
 // ballots (ascending token order), records rows[pos] = t and pos_of[t] = pos
 // (-1 for inactive rows), and block 0 stores the active count; kernel 3 copies
 // the active rows of h, one warp per row over a grid that covers every row, and
-// zeroes the rows after them up to the end of the last 128-row tile (at least
-// one tile), so a GEMM that reads a whole tile of the compacted rows (or the
-// backward's K loop over them) never meets stale bytes.
+// zeroes the rows after them up to the end of the last 128-row block (at least
+// one block), so the backward's K loop over the compacted rows (64-row K blocks)
+// never meets stale bytes.  GEMM rows past the active count are dead rows: the
+// epilogues discard them, or write zeros whatever their accumulators hold.
 //
 // In the backward the inactive tokens are never visited by a GEMM, so their
 // rows of dh are zeroed by a fourth kernel.

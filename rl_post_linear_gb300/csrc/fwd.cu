@@ -8,10 +8,11 @@
 // a separate launch merges the per-chunk pairs in one fixed order before the
 // single fp32 result is formed.
 //
-// Kernel 1 (gemm_persistent_kernel<FwdPolicy>): a work unit is one 128-row
-// token tile times one vocab chunk of kFwdTilesPerChunk 256-column tiles.
-// For every tile the tensor cores form S = h W^T in TMEM (fp32, K = H in
-// ascending 16-wide steps); one epilogue thread owns one token row and folds
+// Kernel 1 (gemm_persistent_kernel<FwdPolicy>): a work unit is one 256-row
+// token tile, computed by a CTA pair (128 rows in each CTA's TMEM), times one
+// vocab chunk of kFwdTilesPerChunk 256-column tiles.  For every tile the
+// tensor cores form S = h W^T in TMEM (fp32, K = H in ascending 16-wide
+// steps); one epilogue thread owns one token row and folds
 // the tile's 256 logits, 32 at a time and in ascending column order, into
 // the row's running (max m, sum s) with
 //     m' = max(m, max_j S_j),  s' = s 2^((m - m') k) + sum_j 2^((S_j - m') k),
