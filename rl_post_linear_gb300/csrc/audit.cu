@@ -28,6 +28,7 @@
 // expm1f(d) - d, where no cancellation arises.
 #include <algorithm>
 #include <cmath>
+#include <cstddef>
 #include <mutex>
 
 #include "rlk_internal.h"
@@ -174,16 +175,21 @@ struct ThreadAcc {
 };
 
 // The extended audit's terms of one slice seen by one thread: the sum of |d| and
-// the count of clipped ratios (outputs); where the slice's keys go, the block's
-// coarse histogram, the count of exact zeros and the clip thresholds (inputs).
+// the count of clipped ratios (outputs, per slice); per percentile q the count of
+// active keys below its window (running over the thread's slices).  The keys inside
+// window q are appended to the warp's own range of list q: `cand` + q * `qstride`,
+// `n[q]` keys so far (the same value in every lane).  Given: the windows
+// [lo, lo + span] of keys and the clip thresholds.
 struct ExtSlice {
     float sabs = 0.f;
     int clip = 0;
-    uint32_t* keys;        // the slice's keys in global memory (element 0 of the slice)
-    int64_t valid;         // elements of the slice inside N
-    uint32_t* hist;        // coarse histogram in shared memory
-    uint32_t n_zero;       // running count of |d| == 0 (kept in a register)
+    int below[3] = {0, 0, 0};
+    uint32_t n[3] = {0u, 0u, 0u};
+    uint32_t lo[3], span[3];
     float clip_lo, clip_hi;
+    uint32_t* cand;
+    int64_t qstride;
+    uint32_t (*skeys)[kAuditThreads];     // [16][threads] in shared memory: the slice's keys
 };
 
 // number of nonzero bytes in a word of four mask bytes
@@ -271,6 +277,7 @@ __device__ __forceinline__ void visit_slice(const float4 (&x)[kVec], const float
     float sd[kVec], skl[kVec], sab[kVec];
     uint32_t gmax[kVec];
     int clip = 0;
+    uint32_t inw[3] = {0u, 0u, 0u};       // EXT: elements inside each window (bit 4j + e)
 #pragma unroll
     for (int j = 0; j < kVec; ++j) {
         a.count += active_bytes(m[j]);
@@ -280,7 +287,6 @@ __device__ __forceinline__ void visit_slice(const float4 (&x)[kVec], const float
         skl[j] = 0.f;
         sab[j] = 0.f;
         gmax[j] = 0u;
-        uint32_t k4[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const bool act = ((m[j] >> (8 * e)) & 0xffu) != 0u;
@@ -293,19 +299,37 @@ __device__ __forceinline__ void visit_slice(const float4 (&x)[kVec], const float
                 // |exp(d) - 1| > eps  <=>  d > log1p(eps) or d < log1p(-eps); d = 0 when inactive
                 sab[j] += __uint_as_float(bits);
                 clip += (d > ext->clip_hi || d < ext->clip_lo) ? 1 : 0;
-                k4[e] = act ? key_of_bits(bits) : 0u;
-                ext->n_zero += (act && bits == 0u) ? 1u : 0u;
-                if (act && bits != 0u) atomicAdd(&ext->hist[coarse_bin_nonzero(bits)], 1u);
+                // the key (0 when inactive); u = key - lo wraps, so that an active key is
+                // below window q exactly when u > -lo (key 0 gives u = -lo: never) and
+                // inside it when u <= span.  Elements inside a window are marked (bit 4j + e) and their
+                // keys listed after the loop.
+                const uint32_t key = act ? key_of_bits(bits) : 0u;
+                ext->skeys[4 * j + e][tid] = key;
+#pragma unroll
+                for (int q = 0; q < 3; ++q) {
+                    const uint32_t u = key - ext->lo[q];
+                    ext->below[q] += (u > 0u - ext->lo[q]) ? 1 : 0;
+                    inw[q] |= (u <= ext->span[q]) ? (1u << (4 * j + e)) : 0u;
+                }
             }
         }
-        if constexpr (EXT) {          // the group's keys (0 for inactive elements)
-            const int o = j * (kAuditThreads * 4) + tid * 4;
-            if (o + 4 <= ext->valid) {
-                *reinterpret_cast<uint4*>(ext->keys + o) = make_uint4(k4[0], k4[1], k4[2], k4[3]);
-            } else {
+    }
+    if constexpr (EXT) {
+        // the warp's keys inside window q go to its range of list q in lane order
+        const int lane = tid & 31;
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (o + e < ext->valid) ext->keys[o + e] = k4[e];
+        for (int q = 0; q < 3; ++q) {
+            if (__any_sync(0xffffffffu, inw[q] != 0u)) {            // warp-uniform
+                const int c = __popc(inw[q]);
+                int incl = c;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, incl, off);
+                    if (lane >= off) incl += v;
+                }
+                uint32_t* dst = ext->cand + q * ext->qstride + ext->n[q] + (incl - c);
+                for (uint32_t m = inw[q]; m != 0u; m &= m - 1u) *dst++ = ext->skeys[__ffs(m) - 1][tid];
+                ext->n[q] += static_cast<uint32_t>(__shfl_sync(0xffffffffu, incl, 31));
             }
         }
     }
@@ -355,14 +379,11 @@ __device__ __forceinline__ void visit_slice(const float4 (&x)[kVec], const float
 
 // A slice read straight from global memory: vector loads when VEC (16-byte aligned
 // inputs, whole slice inside N), else element by element with elements past N
-// inactive.  Either way the arithmetic is visit_slice's.
-template <bool VEC, bool EXT = false>
-__device__ __forceinline__ void load_and_visit_slice(const float* nw, const float* od,
-                                                     const uint8_t* mask, int64_t N,
-                                                     int64_t base, uint32_t best_key,
-                                                     ThreadAcc& a, ExtSlice* ext = nullptr) {
-    float4 x[kVec], y[kVec];
-    uint32_t m[kVec];
+// inactive.  Either way the arithmetic that follows is the same.
+template <bool VEC>
+__device__ __forceinline__ void load_slice(const float* nw, const float* od, const uint8_t* mask,
+                                           int64_t N, int64_t base, float4 (&x)[kVec],
+                                           float4 (&y)[kVec], uint32_t (&m)[kVec]) {
     if (VEC && base + kSlice <= N) {
 #pragma unroll
         for (int j = 0; j < kVec; ++j) {
@@ -391,6 +412,16 @@ __device__ __forceinline__ void load_and_visit_slice(const float* nw, const floa
             m[j] = mv;
         }
     }
+}
+
+template <bool VEC, bool EXT = false>
+__device__ __forceinline__ void load_and_visit_slice(const float* nw, const float* od,
+                                                     const uint8_t* mask, int64_t N,
+                                                     int64_t base, uint32_t best_key,
+                                                     ThreadAcc& a, ExtSlice* ext = nullptr) {
+    float4 x[kVec], y[kVec];
+    uint32_t m[kVec];
+    load_slice<VEC>(nw, od, mask, N, base, x, y, m);
     visit_slice<EXT>(x, y, m, threadIdx.x, best_key, a, ext);
 }
 
@@ -546,39 +577,54 @@ __global__ void __launch_bounds__(kMergeThreads)
 // |d|, mean ratio0 = exp(d), clipfrac0 = #{|exp(d) - 1| > eps} / count, the
 // p50 / p90 / p99 of |d| by the nearest-rank rule (1-based rank
 // ceil(p * count) of the ascending order), and the worst token's sequence and
-// position.
+// position.  A percentile is an exact order statistic of the |d| keys (the
+// base audit's order-preserving keys); it is found among a small candidate set
+// that provably holds it, by an exact radix select with integer histograms.
 //
-//   pass 1   the base audit's slices and blocks, plus per thread the sum of |d|
-//            and the clip count; it writes each element's |d| key (the order-
-//            preserving key of the base audit, 0 for inactive elements) and
-//            counts the keys into a coarse histogram: exact zeros, keys below
-//            2^-31, 128 bins per octave over [2^-31, 2), keys from 2 up (inf
-//            and NaN included) -- per block in shared memory, then added to a
-//            global one with integer atomics.
-//   merge    one block: the fixed-order merge of the partials, and for each
-//            percentile the coarse bin holding its rank, with the number of
-//            keys below that bin (an exact integer).
-//   pass 2   reads the keys once and appends those in each percentile's bin to
-//            that percentile's candidate list (in any order: only the multiset
-//            matters).
-//   select   an exact radix select of the remaining rank among each list's
-//            keys (two 8-bit digits inside a bin of the window, three digits of
-//            11, 11 and 9 bits in the bins outside it), counted with integer
-//            histograms.
-// Mean ratio0 = 1 + mean(d) + mean(exp(d) - 1 - d), from the sums the base audit
-// already forms (exact algebra; no exp per element).  The clip test
-// |exp(d) - 1| > eps is d > log1p(eps) or d < log1p(-eps), the two thresholds
-// rounded to fp32 on the host.  Every count is an integer, so the selected
-// values, like the sums, are bitwise reproducible for a given N.
+//   sample   every K-th 4096-element slice (K a function of N, 64 to 127
+//            slices in all) is counted into a coarse histogram of |d|: exact
+//            zeros, |d| below 2^-31, 128 bins per octave over [2^-31, 2), |d|
+//            from 2 up (inf and NaN included).  The last block to finish
+//            (an integer ticket) turns it into one window of keys per
+//            percentile: the bins from sample rank r - w to r + w, where r is
+//            the percentile's rank in the sample and w six standard
+//            deviations of a sample rank plus 16.
+//   main     the base audit's slices and blocks, plus per thread the sum of
+//            |d|, the clip count, and per percentile the count of active keys
+//            below its window; keys inside a window go to that percentile's
+//            candidate list.
+//   merge    one block: the fixed-order merge of the partials into the
+//            result, and the check that each percentile's rank r falls inside
+//            its window (below < r <= below + candidates, exact integers).
+//   fallback only where the check failed (a sample that misrepresents the
+//            whole, which the window makes improbable): an exact coarse
+//            histogram of all keys, then the keys of the bin holding the rank
+//            replace that percentile's candidates.  Launched always; it
+//            returns at once when every check passed.
+//   select   radix passes over the candidates that share the window's common
+//            leading bits: digits of up to 11 bits, from the highest varying
+//            bit down, each pass a histogram of the candidates that match the
+//            digits chosen so far.
+// The result never depends on the sample: it only decides how much work the
+// selection takes.  Mean ratio0 = 1 + mean(d) + mean(exp(d) - 1 - d), from the
+// sums the base audit already forms (exact algebra; no exp per element).  The
+// clip test |exp(d) - 1| > eps is d > log1p(eps) or d < log1p(-eps), the two
+// thresholds rounded to fp32 on the host.  Every count is an integer, so the
+// selected values, like the sums, are bitwise reproducible for a given N.
 
 struct ExtPartial {
     AuditPartial base;
     DFloat sum_abs;
     int64_t clip;
+    int64_t below[3];
 };
 
 constexpr int kSelBins = 2048;
 constexpr int kSelPasses = 3;
+constexpr int kSelDigit = 11;          // bits of a radix digit
+
+// percentile q of (p50, p90, p99)
+__host__ __device__ __forceinline__ int pct_of(int q) { return q == 0 ? 50 : (q == 1 ? 90 : 99); }
 
 // The selection of one percentile after some radix passes.
 struct SelState {
@@ -586,122 +632,340 @@ struct SelState {
     uint32_t kmask;        // bits of the |d| bits already fixed ...
     uint32_t kvalue;       // ... and their values
     int32_t done;          // 1: the value is kvalue
-    int32_t pad;
+    int32_t vbits;         // the low bits that vary inside the window
 };
 
-// The selection state of the three percentiles (p50, p90, p99).  st[p] is the
-// state before radix pass p (st[0] from the merge); the kernel of pass p writes
-// st[p] from st[p - 1], so no kernel overwrites what its own blocks read.
+// The state shared by the extended audit's kernels.  st[p] is the state before
+// radix pass p (st[0] from the merge or the fallback); the kernel of pass p
+// writes st[p] from st[p - 1], so no kernel overwrites what its own blocks read.
 struct ExtSelect {
-    unsigned long long cand_count[3];   // candidates appended by pass 2
-    int32_t bin[3];                     // coarse bin of the rank
-    int32_t pad;
+    int64_t rank[3];                    // each percentile's rank among all active keys
+    uint32_t win_lo[3];                 // each percentile's window of keys [lo, hi]
+    uint32_t win_hi[3];
+    int32_t fallback[3];                // 1: the window missed the rank
+    int32_t need_fallback;
     SelState st[kSelPasses][3];
 };
 
-// the radix digit of pass p for a percentile in coarse bin `bin` (bits == 0: no pass)
-__device__ __forceinline__ void sel_digit(int bin, int p, int& shift, int& bits) {
-    if (bin >= kCoarseFirst && bin < kCoarseHigh) {     // the low 16 bits vary inside a bin
-        shift = p == 0 ? 8 : 0;
-        bits = p < 2 ? 8 : 0;
-    } else {                                              // all 31 bits vary
-        shift = p == 0 ? 20 : (p == 1 ? 9 : 0);
-        bits = p < 2 ? 11 : 9;
+// Candidate lists.  The main pass (and the fallback, with the same blocks and
+// slices) gives each warp a fixed range of every list, room for all the elements
+// it visits: capw = 512 keys per slice of its block.  List q starts at q * qstride;
+// the keys warp w of block b has put there are [(8 b + w) capw, + wn[q][8 b + w]).
+constexpr int kWarps = kAuditThreads / 32;
+constexpr int64_t kExtMaxBlocks = 456;             // three resident on each of 152 SMs
+constexpr int64_t kWnStride = kExtMaxBlocks * kWarps;
+
+struct ExtGeom {
+    int64_t slices, blocks, capw, qstride;
+    __host__ __device__ explicit ExtGeom(int64_t N) {
+        slices = (N + kSlice - 1) / kSlice;
+        blocks = slices < kExtMaxBlocks ? slices : kExtMaxBlocks;
+        const int64_t per_block = blocks > 0 ? (slices + blocks - 1) / blocks : 0;
+        capw = per_block * (kSlice / kWarps);
+        qstride = blocks * kWarps * capw;
     }
+};
+
+// (The GPU tests read the fallback flags at this place in the workspace.)
+static_assert(sizeof(ExtPartial) == 80 && offsetof(ExtSelect, fallback) == 48,
+              "extended-audit workspace layout");
+
+// The keys of coarse bin `bin` are the range [lo, hi] (the bins preserve order).
+__device__ __forceinline__ void coarse_bin_range(int bin, uint32_t& lo, uint32_t& hi) {
+    uint32_t span;
+    coarse_bin_keys(bin, lo, span);
+    hi = lo + span - 1u;
 }
 
-// The extended pass 1 deals the slices to min(slices, kExtMaxBlocks) blocks (a fixed
-// partition of its own: three of its blocks are resident on each of 152 SMs).
-constexpr int64_t kExtMaxBlocks = 456;
+// The digit of radix pass p for a window whose low `vbits` bits vary (bits == 0: no pass).
+__device__ __forceinline__ void sel_digit(int vbits, int p, int& shift, int& bits) {
+    const int top = vbits - kSelDigit * p;
+    shift = top > kSelDigit ? top - kSelDigit : 0;
+    bits = top > 0 ? top - shift : 0;
+}
 
+// The state before the first radix pass for keys in [lo, hi] and the rank left
+// among them: the common leading bits of the window are known.
+__device__ __forceinline__ SelState window_state(uint32_t lo, uint32_t hi, int64_t rank) {
+    const uint32_t a = lo - 1u, b = hi - 1u;          // |d| bits
+    const uint32_t diff = a ^ b;
+    SelState st;
+    st.vbits = diff == 0u ? 0 : 32 - __clz(diff);
+    st.kmask = st.vbits >= 32 ? 0u : (0xffffffffu << st.vbits);
+    st.kvalue = a & st.kmask;
+    st.rank = rank;
+    st.done = st.vbits == 0 ? 1 : 0;
+    return st;
+}
+
+// A coarse histogram (kCoarseBins u64 counts, read through L2) held by the 256
+// threads of a block, kBinRun consecutive bins each, with the exclusive prefix
+// of each thread's run: find(r) locates the bin of 1-based rank r.
+constexpr int kBinRun = (kCoarseBins + kAuditThreads - 1) / kAuditThreads;   // 17
+
+struct BinScan {
+    unsigned long long c[kBinRun];
+    unsigned long long run, excl, total;
+
+    __device__ void load(const unsigned long long* hist) {
+        __shared__ unsigned long long warp_sum[kAuditThreads / 32];
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        run = 0;
+#pragma unroll
+        for (int j = 0; j < kBinRun; ++j) {
+            const int b = threadIdx.x * kBinRun + j;
+            c[j] = b < kCoarseBins ? __ldcg(hist + b) : 0ull;
+            run += c[j];
+        }
+        unsigned long long incl = run;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const unsigned long long o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        if (lane == 31) warp_sum[warp] = incl;
+        __syncthreads();
+        unsigned long long before = 0;
+        total = 0;
+#pragma unroll
+        for (int w = 0; w < kAuditThreads / 32; ++w) {
+            before += w < warp ? warp_sum[w] : 0ull;
+            total += warp_sum[w];
+        }
+        excl = before + incl - run;
+        __syncthreads();
+    }
+
+    // true in exactly the one thread whose run holds rank r (1 <= r <= total): the bin
+    // and the count of keys in the bins before it
+    __device__ bool find(unsigned long long r, int& bin, unsigned long long& below) const {
+        if (!(excl < r && r <= excl + run)) return false;
+        unsigned long long cum = excl;
+        bin = -1;
+#pragma unroll
+        for (int j = 0; j < kBinRun; ++j) {
+            if (bin < 0) {
+                if (r <= cum + c[j]) bin = threadIdx.x * kBinRun + j;
+                else cum += c[j];
+            }
+        }
+        below = cum;
+        return true;
+    }
+};
+
+// The coarse histogram of the active keys of slices first, first + stride, ...
+// below `slices`, visited by block b at b, b + grid, ... (integer counts, so the
+// order does not matter): per block in shared memory, then added to `hist`.
 template <bool VEC>
-__global__ void __launch_bounds__(kAuditThreads, 3)
-    audit_ext_pass1(const float* __restrict__ nw, const float* __restrict__ od,
-                    const uint8_t* __restrict__ mask, int64_t N, float clip_lo, float clip_hi,
-                    ExtPartial* __restrict__ out, uint32_t* __restrict__ keys,
-                    unsigned long long* __restrict__ coarse) {
+__device__ void coarse_histogram(const float* nw, const float* od, const uint8_t* mask, int64_t N,
+                                 int64_t slices, int64_t stride, unsigned long long* hist) {
     __shared__ uint32_t h[kCoarseBins];
     for (int i = threadIdx.x; i < kCoarseBins; i += kAuditThreads) h[i] = 0u;
     __syncthreads();
+    uint32_t n_zero = 0;
+#pragma unroll 1
+    for (int64_t i = blockIdx.x; i * stride < slices; i += gridDim.x) {
+        float4 x[kVec], y[kVec];
+        uint32_t m[kVec];
+        load_slice<VEC>(nw, od, mask, N, i * stride * kSlice, x, y, m);
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+            const float xs[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
+            const float ys[4] = {y[j].x, y[j].y, y[j].z, y[j].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const bool act = ((m[j] >> (8 * e)) & 0xffu) != 0u;
+                const uint32_t bits = __float_as_uint(xs[e] - ys[e]) & 0x7fffffffu;
+                n_zero += (act && bits == 0u) ? 1u : 0u;
+                if (act && bits != 0u) atomicAdd(&h[coarse_bin_nonzero(bits)], 1u);
+            }
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) n_zero += __shfl_down_sync(0xffffffffu, n_zero, off);
+    if ((threadIdx.x & 31) == 0 && n_zero != 0u) atomicAdd(&h[kCoarseZero], n_zero);
+    __syncthreads();
+    for (int i = threadIdx.x; i < kCoarseBins; i += kAuditThreads)
+        if (h[i] != 0u) atomicAdd(&hist[i], static_cast<unsigned long long>(h[i]));
+}
+
+// Sample slices: every K-th, about kSampleSlices of them, one block each.
+constexpr int64_t kSampleSlices = 64;
+constexpr int64_t kSampleMaxBlocks = 128;
+
+inline int64_t ext_sample_stride(int64_t slices) {
+    return slices > kSampleSlices ? slices / kSampleSlices : 1;
+}
+
+// The sample's histogram; the last block to finish sets the windows and clears the
+// candidate counts.
+template <bool VEC>
+__global__ void __launch_bounds__(kAuditThreads)
+    audit_ext_sample(const float* __restrict__ nw, const float* __restrict__ od,
+                     const uint8_t* __restrict__ mask, int64_t N, int64_t stride,
+                     unsigned long long* __restrict__ shist, unsigned* __restrict__ ticket,
+                     ExtSelect* __restrict__ sel) {
+    asm volatile("griddepcontrol.launch_dependents;");
     const int64_t slices = (N + kSlice - 1) / kSlice;
+    coarse_histogram<VEC>(nw, od, mask, N, slices, stride, shist);
+    __shared__ bool s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    BinScan bs;
+    bs.load(shist);
+    const unsigned long long sa = bs.total;           // active keys in the sample
+    // window ends in sample ranks; an end outside [1, sa] opens the window to that side
+    __shared__ int s_bin[3][2];
+    if (threadIdx.x < 3) {
+        s_bin[threadIdx.x][0] = kCoarseZero;
+        s_bin[threadIdx.x][1] = kCoarseHigh;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+        if (sa == 0ull) break;
+        const double pf = pct_of(q) / 100.0;
+        const long long r = static_cast<long long>((pct_of(q) * sa + 99) / 100);
+        const long long w =
+            static_cast<long long>(ceil(6.0 * sqrt(static_cast<double>(sa) * pf * (1.0 - pf)))) + 16;
+        int bin;
+        unsigned long long below;
+        if (r - w >= 1 && bs.find(static_cast<unsigned long long>(r - w), bin, below))
+            s_bin[q][0] = bin;
+        if (r + w <= static_cast<long long>(sa) &&
+            bs.find(static_cast<unsigned long long>(r + w), bin, below))
+            s_bin[q][1] = bin;
+    }
+    __syncthreads();
+    if (threadIdx.x < 3) {
+        const int q = threadIdx.x;
+        uint32_t lo, hi, lo2, hi2;
+        coarse_bin_range(s_bin[q][0], lo, hi);
+        coarse_bin_range(s_bin[q][1], lo2, hi2);
+        sel->win_lo[q] = lo;
+        sel->win_hi[q] = hi2;
+        sel->fallback[q] = 0;
+    }
+    if (threadIdx.x == 0) sel->need_fallback = 0;
+}
+
+// The extended audit's pass over all slices (see above); the partition of the
+// slices is the base audit's with at most kExtMaxBlocks blocks.
+
+template <bool VEC>
+__global__ void __launch_bounds__(kAuditThreads, 3)
+    audit_ext_main(const float* __restrict__ nw, const float* __restrict__ od,
+                   const uint8_t* __restrict__ mask, int64_t N, float clip_lo, float clip_hi,
+                   ExtPartial* __restrict__ out, const ExtSelect* __restrict__ sel,
+                   uint32_t* __restrict__ cand, uint32_t* __restrict__ wn) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");       // the windows
+    asm volatile("griddepcontrol.launch_dependents;");
+    __shared__ uint32_t skeys[kAuditV3PerThread][kAuditThreads];
+    const ExtGeom g(N);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t wr = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+    ExtSlice x;
+    x.skeys = skeys;
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+        x.lo[q] = sel->win_lo[q];
+        x.span[q] = sel->win_hi[q] - x.lo[q];
+    }
+    x.clip_lo = clip_lo;
+    x.clip_hi = clip_hi;
+    x.cand = cand + wr * g.capw;
+    x.qstride = g.qstride;
     RunAcc r;
     DFloat sabs{0.f, 0.f};
     int clip = 0;
-    ExtSlice x;
-    x.hist = h;
-    x.n_zero = 0u;
-    x.clip_lo = clip_lo;
-    x.clip_hi = clip_hi;
 #pragma unroll 1
-    for (int64_t sl = blockIdx.x; sl < slices; sl += gridDim.x) {
+    for (int64_t sl = blockIdx.x; sl < g.slices; sl += gridDim.x) {
         const int64_t base = sl * kSlice;
         ThreadAcc a;
-        x.keys = keys + base;
-        x.valid = N - base;
         load_and_visit_slice<VEC, true>(nw, od, mask, N, base, r.best_key, a, &x);
         r.add_slice(a, base);
         sabs = df_add(sabs, DFloat{x.sabs, 0.f});
         clip += x.clip;
     }
-    uint32_t n_zero = x.n_zero;
-    // the block's partial: the base audit's tree, then the same tree for |d| and the clips
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) {
+#pragma unroll
+        for (int q = 0; q < 3; ++q) wn[q * kWnStride + wr] = x.n[q];
+    }
+    // the block's partial: the base audit's tree, then the same tree for |d|, the clips
+    // and the counts below the windows
+    long long below[3] = {x.below[0], x.below[1], x.below[2]};
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
         DFloat y;
         y.hi = __shfl_down_sync(0xffffffffu, sabs.hi, off);
         y.lo = __shfl_down_sync(0xffffffffu, sabs.lo, off);
         const int c = __shfl_down_sync(0xffffffffu, clip, off);
-        const uint32_t z0 = __shfl_down_sync(0xffffffffu, n_zero, off);
+        long long b[3];
+#pragma unroll
+        for (int q = 0; q < 3; ++q) b[q] = __shfl_down_sync(0xffffffffu, below[q], off);
         if (lane + off < 32) {
             sabs = df_add(sabs, y);
             clip += c;
-            n_zero += z0;
+#pragma unroll
+            for (int q = 0; q < 3; ++q) below[q] += b[q];
         }
     }
-    __shared__ DFloat w_abs[kAuditThreads / 32];
-    __shared__ int w_clip[kAuditThreads / 32];
+    __shared__ DFloat w_abs[kWarps];
+    __shared__ int w_clip[kWarps];
+    __shared__ long long w_below[kWarps][3];
     if (lane == 0) {
         w_abs[warp] = sabs;
         w_clip[warp] = clip;
-        if (n_zero) atomicAdd(&h[kCoarseZero], n_zero);
+#pragma unroll
+        for (int q = 0; q < 3; ++q) w_below[warp][q] = below[q];
     }
     const AuditPartial bp = block_partial(r);      // its barrier also orders the writes above
-    for (int i = threadIdx.x; i < kCoarseBins; i += kAuditThreads)
-        if (h[i] != 0u) atomicAdd(&coarse[i], static_cast<unsigned long long>(h[i]));
     if (threadIdx.x == 0) {
         DFloat sa = w_abs[0];
         int64_t cl = w_clip[0];
+        int64_t bl[3] = {w_below[0][0], w_below[0][1], w_below[0][2]};
 #pragma unroll
-        for (int w = 1; w < kAuditThreads / 32; ++w) {
+        for (int w = 1; w < kWarps; ++w) {
             sa = df_add(sa, w_abs[w]);
             cl += w_clip[w];
+#pragma unroll
+            for (int q = 0; q < 3; ++q) bl[q] += w_below[w][q];
         }
         ExtPartial ep;
         ep.base = bp;
         ep.sum_abs = sa;
         ep.clip = cl;
+#pragma unroll
+        for (int q = 0; q < 3; ++q) ep.below[q] = bl[q];
         out[blockIdx.x] = ep;
     }
 }
 
-// One block: the fixed-order merge of the partials; writes the sums into the
-// result; for each percentile the coarse bin holding its rank and the rank left
-// inside it; clears the candidate counts and the select histograms.
+// One block: the fixed-order merge of the partials into the result; each
+// percentile's rank, checked against its window; clears the select histograms.
 __global__ void __launch_bounds__(kMergeThreads)
     audit_ext_merge(const ExtPartial* __restrict__ parts, int64_t num_parts,
                     const int64_t* __restrict__ seq_offsets, int64_t num_seqs,
-                    const unsigned long long* __restrict__ coarse,
                     rlk_audit_ext_t* __restrict__ result, ExtSelect* __restrict__ sel,
-                    unsigned long long* __restrict__ sel_hist) {
+                    unsigned long long* __restrict__ sel_hist, const uint32_t* __restrict__ wn) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
     Acc a = empty_acc();
     DFloat sa{0.f, 0.f};
     int64_t cl = 0;
+    int64_t bl[3] = {0, 0, 0};
     // ascending partials per thread, loaded in batches (as in the base audit's merge)
     auto fold = [&](const ExtPartial& p) {
         merge(a, to_acc(p.base));
         sa = df_add(sa, p.sum_abs);
         cl += p.clip;
+#pragma unroll
+        for (int q = 0; q < 3; ++q) bl[q] += p.below[q];
     };
     int64_t i = threadIdx.x;
     for (; i + (kMergeBatch - 1) * kMergeThreads < num_parts; i += kMergeBatch * kMergeThreads) {
@@ -712,239 +976,222 @@ __global__ void __launch_bounds__(kMergeThreads)
         for (int j = 0; j < kMergeBatch; ++j) fold(p[j]);
     }
     for (; i < num_parts; i += kMergeThreads) fold(parts[i]);
+    // the candidates of each list: the warps' counts (integers: any order)
+    int64_t nc[3] = {0, 0, 0};
+    for (int64_t k = threadIdx.x; k < num_parts * kWarps; k += kMergeThreads) {
+#pragma unroll
+        for (int q = 0; q < 3; ++q) nc[q] += wn[q * kWnStride + k];
+    }
     for (int k = threadIdx.x; k < kSelPasses * 3 * kSelBins; k += kMergeThreads) sel_hist[k] = 0ull;
     a = block_reduce<kMergeThreads>(a);
     __shared__ DFloat s_abs[kMergeThreads / 32];
     __shared__ long long s_clip[kMergeThreads / 32];
-    __shared__ long long s_count;
+    __shared__ long long s_below[kMergeThreads / 32][3];
+    __shared__ long long s_nc[kMergeThreads / 32][3];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    // the same fixed tree for the two extra sums
+    // the same fixed tree for the extra sums (the counts are integers)
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
         DFloat x;
         x.hi = __shfl_down_sync(0xffffffffu, sa.hi, off);
         x.lo = __shfl_down_sync(0xffffffffu, sa.lo, off);
         const long long z = __shfl_down_sync(0xffffffffu, static_cast<long long>(cl), off);
+        long long b[3], c[3];
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+            b[q] = __shfl_down_sync(0xffffffffu, static_cast<long long>(bl[q]), off);
+            c[q] = __shfl_down_sync(0xffffffffu, static_cast<long long>(nc[q]), off);
+        }
         if (lane + off < 32) {
             sa = df_add(sa, x);
             cl += z;
+#pragma unroll
+            for (int q = 0; q < 3; ++q) {
+                bl[q] += b[q];
+                nc[q] += c[q];
+            }
         }
     }
     if (lane == 0) {
         s_abs[warp] = sa;
         s_clip[warp] = cl;
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+            s_below[warp][q] = bl[q];
+            s_nc[warp][q] = nc[q];
+        }
     }
-    if (threadIdx.x == 0) s_count = a.count;
     __syncthreads();
-    const int64_t count = s_count;
-    if (threadIdx.x == 0) {
-        for (int w = 1; w < kMergeThreads / 32; ++w) {
-            s_abs[0] = df_add(s_abs[0], s_abs[w]);
-            s_clip[0] += s_clip[w];
+    if (threadIdx.x != 0) return;
+    for (int w = 1; w < kMergeThreads / 32; ++w) {
+        s_abs[0] = df_add(s_abs[0], s_abs[w]);
+        s_clip[0] += s_clip[w];
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+            s_below[0][q] += s_below[w][q];
+            s_nc[0][q] += s_nc[w][q];
         }
-        rlk_audit_ext_t r;
-        r.active_count = a.count;
-        r.argmax_index = a.count > 0 ? a.arg : -1;
-        r.argmax_seq = -1;
-        r.argmax_pos = -1;
-        if (seq_offsets != nullptr && num_seqs > 0 && a.count > 0) {
-            int64_t lo = 0, hi = num_seqs;      // last s < num_seqs with seq_offsets[s] <= arg
-            while (hi - lo > 1) {
-                const int64_t mid = (lo + hi) >> 1;
-                if (seq_offsets[mid] <= a.arg) lo = mid; else hi = mid;
-            }
-            if (a.arg >= seq_offsets[lo] && a.arg < seq_offsets[lo + 1]) {
-                r.argmax_seq = lo;
-                r.argmax_pos = a.arg - seq_offsets[lo];
-            }
-        }
-        r.clip_count = s_clip[0];
-        const double cnt = static_cast<double>(a.count);
-        r.mean_dlogp = df_value(a.sum_d) / cnt;
-        r.mean_abs_dlogp = df_value(s_abs[0]) / cnt;
-        r.approx_kl = df_value(a.sum_kl) / cnt;
-        // mean exp(d) = 1 + mean d + mean (exp(d) - 1 - d)
-        r.mean_ratio = (cnt + df_value(a.sum_d) + df_value(a.sum_kl)) / cnt;
-        r.max_abs_dlogp = a.count > 0 ? a.best : 0.0f;
-        r.p50_abs_dlogp = r.p90_abs_dlogp = r.p99_abs_dlogp = __int_as_float(0x7fc00000);
-        r.clipfrac = static_cast<float>(static_cast<double>(s_clip[0]) / cnt);
-        r.error_flags = a.flags;
-        *result = r;
     }
-    // each percentile's coarse bin: an exclusive scan of the bins (integers, so exact),
-    // five consecutive bins per thread; the one thread whose run holds the rank walks it
-    constexpr int kRun = (kCoarseBins + kMergeThreads - 1) / kMergeThreads;   // 5
-    __shared__ unsigned long long warp_sum[kMergeThreads / 32];
-    // defaults (no active token: done, rank 0), overwritten below by the thread that finds
-    // each rank; the barrier of the scan orders the two
-    if (threadIdx.x < 3) {
+    rlk_audit_ext_t r;
+    r.active_count = a.count;
+    r.argmax_index = a.count > 0 ? a.arg : -1;
+    r.argmax_seq = -1;
+    r.argmax_pos = -1;
+    if (seq_offsets != nullptr && num_seqs > 0 && a.count > 0) {
+        int64_t lo = 0, hi = num_seqs;      // last s < num_seqs with seq_offsets[s] <= arg
+        while (hi - lo > 1) {
+            const int64_t mid = (lo + hi) >> 1;
+            if (seq_offsets[mid] <= a.arg) lo = mid; else hi = mid;
+        }
+        if (a.arg >= seq_offsets[lo] && a.arg < seq_offsets[lo + 1]) {
+            r.argmax_seq = lo;
+            r.argmax_pos = a.arg - seq_offsets[lo];
+        }
+    }
+    r.clip_count = s_clip[0];
+    const double cnt = static_cast<double>(a.count);
+    r.mean_dlogp = df_value(a.sum_d) / cnt;
+    r.mean_abs_dlogp = df_value(s_abs[0]) / cnt;
+    r.approx_kl = df_value(a.sum_kl) / cnt;
+    // mean exp(d) = 1 + mean d + mean (exp(d) - 1 - d)
+    r.mean_ratio = (cnt + df_value(a.sum_d) + df_value(a.sum_kl)) / cnt;
+    r.max_abs_dlogp = a.count > 0 ? a.best : 0.0f;
+    r.p50_abs_dlogp = r.p90_abs_dlogp = r.p99_abs_dlogp = __int_as_float(0x7fc00000);
+    r.clipfrac = static_cast<float>(static_cast<double>(s_clip[0]) / cnt);
+    r.error_flags = a.flags;
+    *result = r;
+    int need = 0;
+    for (int q = 0; q < 3; ++q) {
+        const int64_t rank = (pct_of(q) * a.count + 99) / 100;   // nearest rank, 1-based (0: none)
+        const int64_t below = s_below[0][q];
+        const int64_t ncq = s_nc[0][q];
+        sel->rank[q] = rank;
         SelState st;
-        st.rank = 0;
-        st.kmask = 0u;
-        st.kvalue = 0u;
-        st.done = 1;
-        st.pad = 0;
-        sel->cand_count[threadIdx.x] = 0ull;
-        sel->bin[threadIdx.x] = -1;
-        sel->st[0][threadIdx.x] = st;
-    }
-    unsigned long long c[kRun];
-    unsigned long long run = 0;
-#pragma unroll
-    for (int j = 0; j < kRun; ++j) {
-        const int b = threadIdx.x * kRun + j;
-        c[j] = b < kCoarseBins ? coarse[b] : 0ull;
-        run += c[j];
-    }
-    unsigned long long incl = run;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const unsigned long long o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
-    }
-    if (lane == 31) warp_sum[warp] = incl;
-    __syncthreads();
-    unsigned long long before = 0;
-    for (int w = 0; w < warp; ++w) before += warp_sum[w];
-    const unsigned long long excl = before + incl - run;
-    const int pct[3] = {50, 90, 99};
-    for (int q = 0; q < 3; ++q) {
-        const int64_t rank = (pct[q] * count + 99) / 100;   // nearest rank, 1-based (0 if none)
-        if (rank <= 0) continue;                            // st[0][q] says done, rank 0
-        const unsigned long long rk = static_cast<unsigned long long>(rank);
-        if (excl < rk && rk <= excl + run) {               // exactly one thread
-            unsigned long long cum = excl;
-            int bin = -1;
-#pragma unroll
-            for (int j = 0; j < kRun; ++j) {
-                if (bin < 0) {
-                    if (rk <= cum + c[j]) bin = threadIdx.x * kRun + j;
-                    else cum += c[j];
-                }
-            }
-            SelState st;
-            st.rank = static_cast<int64_t>(rk - cum);
-            st.kmask = 0u;
-            st.kvalue = 0u;
-            st.done = 0;
-            st.pad = 0;
-            if (bin == kCoarseZero) {                 // every key in the bin is |d| = 0
-                st.done = 1;
-            } else if (bin >= kCoarseFirst && bin < kCoarseHigh) {
-                // the bin fixes the exponent and the top 7 mantissa bits
-                st.kmask = 0x7fff0000u;
-                st.kvalue =
-                    (static_cast<uint32_t>((bin - kCoarseFirst) >> 7) + kCoarseWindowLo) << 23 |
-                    (static_cast<uint32_t>((bin - kCoarseFirst) & 0x7f) << 16);
-            }
-            sel->bin[q] = bin;
-            sel->st[0][q] = st;
+        if (rank <= 0) {
+            st = window_state(1u, 1u, 0);                  // done; NaN stays
+        } else if (below < rank && rank <= below + ncq) {
+            st = window_state(sel->win_lo[q], sel->win_hi[q], rank - below);
+        } else {
+            st = window_state(1u, 1u, 0);                  // replaced by the fallback
+            sel->fallback[q] = 1;
+            need = 1;
         }
+        sel->st[0][q] = st;
     }
+    sel->need_fallback = need;
 }
 
-// Pass 2 puts every key in a percentile's coarse bin in that percentile's candidate
-// list, in any order (only the multiset matters); kCandStage keys per list are
-// staged in shared memory first.
-constexpr int kCandStage = 2048;
-
-__device__ __forceinline__ void collect_key(uint32_t key, const uint32_t (&lo)[3],
-                                            const uint32_t (&span)[3], unsigned* s_n,
-                                            uint32_t (*stage)[kCandStage], ExtSelect* sel,
-                                            uint32_t* cand, int64_t cand_stride) {
-#pragma unroll
-    for (int q = 0; q < 3; ++q) {
-        if (key - lo[q] < span[q]) {          // inactive keys (0) are below every range
-            const unsigned pos = atomicAdd(&s_n[q], 1u);
-            if (pos < kCandStage) {
-                stage[q][pos] = key;
-            } else {                  // the stage is full: straight to the global list
-                const unsigned long long g = atomicAdd(&sel->cand_count[q], 1ull);
-                cand[q * cand_stride + static_cast<int64_t>(g)] = key;
-            }
-        }
-    }
-}
-
-// Pass 2 reads the keys as a plain stream (16 bytes per thread and iteration, the
-// whole grid sweeping them front to back; the candidate multiset does not depend on
-// it).  A block stages its candidates in shared memory (a shared atomic per
-// candidate: they are rare) and, at the end, reserves room in each global list with
-// one atomic; what does not fit in the stage goes to the global list at once.
+// Fallback, step 1 (returns at once unless some window missed its rank): the exact
+// coarse histogram of all keys.
+template <bool VEC>
 __global__ void __launch_bounds__(kAuditThreads)
-    audit_ext_collect(const uint32_t* __restrict__ keys, int64_t N, ExtSelect* __restrict__ sel,
-                      uint32_t* __restrict__ cand, int64_t cand_stride) {
-    __shared__ uint32_t stage[3][kCandStage];
-    __shared__ unsigned s_n[3];
-    __shared__ unsigned long long s_base[3];
-    // each percentile's key range; an empty range (span 0) for one already known
-    uint32_t lo[3], span[3];
-    bool need = false;
-#pragma unroll
+    audit_ext_fallback_hist(const float* __restrict__ nw, const float* __restrict__ od,
+                            const uint8_t* __restrict__ mask, int64_t N,
+                            unsigned long long* __restrict__ hist,
+                            const ExtSelect* __restrict__ sel) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    if (sel->need_fallback == 0) return;
+    const int64_t slices = (N + kSlice - 1) / kSlice;
+    coarse_histogram<VEC>(nw, od, mask, N, slices, 1, hist);
+}
+
+// Fallback, step 2: every block finds the coarse bin of each missed rank (block 0
+// stores the selection state), then the keys of those bins replace those lists,
+// with the main pass's blocks, slices and warp ranges.
+template <bool VEC>
+__global__ void __launch_bounds__(kAuditThreads, 3)
+    audit_ext_fallback_collect(const float* __restrict__ nw, const float* __restrict__ od,
+                               const uint8_t* __restrict__ mask, int64_t N,
+                               const unsigned long long* __restrict__ hist,
+                               ExtSelect* __restrict__ sel, uint32_t* __restrict__ cand,
+                               uint32_t* __restrict__ wn) {
+    __shared__ int s_bin[3];
+    __shared__ unsigned long long s_below[3];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    if (sel->need_fallback == 0) return;
+    if (threadIdx.x < 3) {
+        s_bin[threadIdx.x] = -1;
+        s_below[threadIdx.x] = 0ull;
+    }
+    BinScan bs;
+    bs.load(hist);                                   // its barriers order the writes above
     for (int q = 0; q < 3; ++q) {
-        lo[q] = 0u;
-        span[q] = 0u;
-        if (!sel->st[0][q].done) {
-            coarse_bin_keys(sel->bin[q], lo[q], span[q]);
-            need = true;
+        int bin;
+        unsigned long long below;
+        if (sel->fallback[q] && bs.find(static_cast<unsigned long long>(sel->rank[q]), bin, below)) {
+            s_bin[q] = bin;
+            s_below[q] = below;
         }
     }
-    if (!need) return;
-    if (threadIdx.x < 3) s_n[threadIdx.x] = 0u;
     __syncthreads();
-    const int64_t n4 = N / 4;
-    const uint4* k4 = reinterpret_cast<const uint4*>(keys);
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kAuditThreads;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kAuditThreads + threadIdx.x; i < n4;
-         i += stride) {
-        const uint4 v = __ldcs(k4 + i);
-        collect_key(v.x, lo, span, s_n, stage, sel, cand, cand_stride);
-        collect_key(v.y, lo, span, s_n, stage, sel, cand, cand_stride);
-        collect_key(v.z, lo, span, s_n, stage, sel, cand, cand_stride);
-        collect_key(v.w, lo, span, s_n, stage, sel, cand, cand_stride);
-    }
-    if (blockIdx.x == 0 && threadIdx.x < N - n4 * 4)     // the last N mod 4 keys
-        collect_key(keys[n4 * 4 + threadIdx.x], lo, span, s_n, stage, sel, cand, cand_stride);
-    __syncthreads();
-    if (threadIdx.x < 3) {
-        const unsigned n = min(s_n[threadIdx.x], static_cast<unsigned>(kCandStage));
-        s_base[threadIdx.x] = n > 0u ? atomicAdd(&sel->cand_count[threadIdx.x],
-                                                 static_cast<unsigned long long>(n))
-                                     : 0ull;
-    }
-    __syncthreads();
+    __shared__ uint32_t skeys[kAuditV3PerThread][kAuditThreads];
+    const ExtGeom g(N);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t wr = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+    ExtSlice x;
+    x.skeys = skeys;
+    bool redo[3];
 #pragma unroll
     for (int q = 0; q < 3; ++q) {
-        const unsigned n = min(s_n[q], static_cast<unsigned>(kCandStage));
-        for (unsigned i = threadIdx.x; i < n; i += kAuditThreads)
-            cand[q * cand_stride + static_cast<int64_t>(s_base[q]) + i] = stage[q][i];
+        x.lo[q] = 0xffffffffu;                        // an empty window: no key reaches it
+        x.span[q] = 0u;
+        redo[q] = s_bin[q] >= 0;
+        if (redo[q]) {
+            uint32_t lo, hi;
+            coarse_bin_range(s_bin[q], lo, hi);
+            const SelState st = window_state(lo, hi, sel->rank[q] - static_cast<int64_t>(s_below[q]));
+            if (blockIdx.x == 0 && threadIdx.x == 0) {
+                sel->st[0][q] = st;
+                sel->win_lo[q] = lo;
+                sel->win_hi[q] = hi;
+            }
+            x.lo[q] = lo;
+            x.span[q] = hi - lo;
+        }
+    }
+    x.clip_lo = -INFINITY;
+    x.clip_hi = INFINITY;
+    x.cand = cand + wr * g.capw;
+    x.qstride = g.qstride;
+#pragma unroll 1
+    for (int64_t sl = blockIdx.x; sl < g.slices; sl += gridDim.x) {
+        ThreadAcc a;
+        load_and_visit_slice<VEC, true>(nw, od, mask, N, sl * kSlice, 0xffffffffu, a, &x);
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int q = 0; q < 3; ++q)
+            if (redo[q]) wn[q * kWnStride + wr] = x.n[q];
     }
 }
 
 // The select step after radix pass p of percentile q: the digit whose bin holds
 // the rank (an exclusive scan of the 2^bits counts, exact), appended to the known
 // bits.  Run identically by every block of the next pass and by the final step.
-__device__ void sel_step(int q, int p, int bin, const unsigned long long* __restrict__ sel_hist,
+__device__ void sel_step(int q, int p, const unsigned long long* __restrict__ sel_hist,
                          SelState& st) {
     __shared__ unsigned long long warp_sum[kAuditThreads / 32];
     __shared__ uint32_t s_digit;
     __shared__ int64_t s_rank;
     int shift, bits;
-    sel_digit(bin, p, shift, bits);
+    sel_digit(st.vbits, p, shift, bits);
     if (st.done || bits == 0) return;                  // block-uniform
     if (threadIdx.x == 0) {                            // (always overwritten: the counts are exact)
         s_digit = 0u;
         s_rank = 1;
     }
     const int nb = 1 << bits;
-    const int runl = nb / kAuditThreads;                 // 8, or 2 for 9 bits
+    const int runl = nb > kAuditThreads ? nb / kAuditThreads : 1;    // 8, 4, 2 or 1
     const unsigned long long* hq = sel_hist + (static_cast<int64_t>(p) * 3 + q) * kSelBins;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     unsigned long long c[8];
     unsigned long long run = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        c[j] = j < runl ? hq[threadIdx.x * runl + j] : 0ull;
+        const int b = threadIdx.x * runl + j;
+        c[j] = (j < runl && b < nb) ? hq[b] : 0ull;
         run += c[j];
     }
     unsigned long long incl = run;
@@ -978,38 +1225,43 @@ __device__ void sel_step(int q, int p, int bin, const unsigned long long* __rest
     st.kvalue = (st.kvalue & ~dmask) | (s_digit << shift);
     st.rank = s_rank;
     int s2, b2;
-    sel_digit(bin, p + 1, s2, b2);
+    sel_digit(st.vbits, p + 1, s2, b2);
     st.done = (p + 1 >= kSelPasses || b2 == 0) ? 1 : 0;
     __syncthreads();
 }
 
-// Radix pass p over each percentile's candidates (blockIdx.y = percentile): the
+// Radix pass p over each percentile's candidates (blockIdx.y = percentile; warp w
+// of block b reads the range warp w of block b of the main pass filled): the
 // histogram of digit p among the candidates that match the bits known so far.
 // For p > 0 every block first repeats the select step of pass p - 1; block 0
 // stores its outcome.
 template <int P>
 __global__ void __launch_bounds__(kAuditThreads)
     audit_ext_radix(ExtSelect* __restrict__ sel, const uint32_t* __restrict__ cand,
-                    int64_t cand_stride, unsigned long long* __restrict__ sel_hist) {
+                    const uint32_t* __restrict__ wn, int64_t N,
+                    unsigned long long* __restrict__ sel_hist) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
     const int q = blockIdx.y;
-    const int bin = sel->bin[q];
     SelState st = sel->st[P == 0 ? 0 : P - 1][q];
     if (P > 0) {
-        sel_step(q, P - 1, bin, sel_hist, st);
+        sel_step(q, P - 1, sel_hist, st);
         if (blockIdx.x == 0 && threadIdx.x == 0) sel->st[P][q] = st;
     }
     if (st.done) return;                                // block-uniform
     const uint32_t kmask = st.kmask, kvalue = st.kvalue;
     int shift, bits;
-    sel_digit(bin, P, shift, bits);
+    sel_digit(st.vbits, P, shift, bits);
     const uint32_t dmask = (1u << bits) - 1u;
     __shared__ uint32_t h[kSelBins];
     for (int i = threadIdx.x; i < kSelBins; i += kAuditThreads) h[i] = 0u;
     __syncthreads();
-    const int64_t n = static_cast<int64_t>(sel->cand_count[q]);
-    const uint32_t* cq = cand + q * cand_stride;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kAuditThreads + threadIdx.x; i - threadIdx.x < n;
-         i += static_cast<int64_t>(gridDim.x) * kAuditThreads) {
+    const ExtGeom g(N);
+    const int lane = threadIdx.x & 31;
+    const int64_t wr = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+    const int64_t n = wn[q * kWnStride + wr];
+    const uint32_t* cq = cand + q * g.qstride + wr * g.capw;
+    for (int64_t i = lane; i - lane < n; i += 32) {
         const bool in = i < n;
         const uint32_t b = in ? cq[i] - 1u : 0u;
         const bool match = in && (b & kmask) == kvalue;
@@ -1018,7 +1270,7 @@ __global__ void __launch_bounds__(kAuditThreads)
         const unsigned act = __ballot_sync(0xffffffffu, match);
         if (match) {
             const unsigned peers = __match_any_sync(act, digit);
-            if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&h[digit], __popc(peers));
+            if (lane == __ffs(peers) - 1) atomicAdd(&h[digit], __popc(peers));
         }
     }
     __syncthreads();
@@ -1032,10 +1284,11 @@ __global__ void __launch_bounds__(kAuditThreads)
     audit_ext_finish(const ExtSelect* __restrict__ sel,
                      const unsigned long long* __restrict__ sel_hist,
                      rlk_audit_ext_t* __restrict__ result) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int q = 0; q < 3; ++q) {
         SelState st = sel->st[kSelPasses - 1][q];
         if (st.rank <= 0) continue;                      // no active token: NaN stays
-        sel_step(q, kSelPasses - 1, sel->bin[q], sel_hist, st);
+        sel_step(q, kSelPasses - 1, sel_hist, st);
         if (threadIdx.x == 0) {
             const float v = __uint_as_float(st.kvalue);
             if (q == 0) result->p50_abs_dlogp = v;
@@ -1145,17 +1398,20 @@ cudaError_t launch_audit(const float* logp_new, const float* logp_old, const uin
     return cudaLaunchKernelEx(&cfg, audit_pass2, cparts, nparts, result);
 }
 
-// extended audit workspace: partials | coarse histogram | select state | select
-// histograms | |d| keys [N] | candidate lists [3][N] (uint32)
+// extended audit workspace: partials | sample histogram, exact histogram, ticket
+// (cleared by one memset) | select state | select histograms | the warps' list
+// lengths [3][kWnStride] | candidate lists [3][qstride] (uint32)
 struct ExtLayout {
-    size_t coarse_off, sel_off, hist_off, keys_off, cand_off, total;
+    size_t hist_off, ticket_off, sel_off, selhist_off, wn_off, cand_off, total;
     explicit ExtLayout(int64_t N) {
-        coarse_off = align_up(static_cast<size_t>(kExtMaxBlocks) * sizeof(ExtPartial), 256);
-        sel_off = align_up(coarse_off + kCoarseBins * sizeof(unsigned long long), 256);
-        hist_off = align_up(sel_off + sizeof(ExtSelect), 256);
-        keys_off = align_up(hist_off + kSelPasses * 3 * kSelBins * sizeof(unsigned long long), 256);
-        cand_off = align_up(keys_off + static_cast<size_t>(N) * 4, 256);
-        total = align_up(cand_off + 3 * static_cast<size_t>(N) * 4, 256) + 256;
+        const ExtGeom g(N);
+        hist_off = align_up(static_cast<size_t>(kExtMaxBlocks) * sizeof(ExtPartial), 256);
+        ticket_off = hist_off + 2 * kCoarseBins * sizeof(unsigned long long);
+        sel_off = align_up(ticket_off + 16, 256);
+        selhist_off = align_up(sel_off + sizeof(ExtSelect), 256);
+        wn_off = align_up(selhist_off + kSelPasses * 3 * kSelBins * sizeof(unsigned long long), 256);
+        cand_off = align_up(wn_off + 3 * static_cast<size_t>(kWnStride) * 4, 256);
+        total = align_up(cand_off + 3 * static_cast<size_t>(g.qstride) * 4, 256) + 256;
     }
 };
 
@@ -1165,48 +1421,96 @@ cudaError_t launch_audit_ext(const float* logp_new, const float* logp_old, const
                              int64_t N, const int64_t* seq_offsets, int64_t num_seqs, float eps,
                              rlk_audit_ext_t* result, void* workspace, bool vec_ok, int sms,
                              cudaStream_t stream) {
+    (void)sms;
     const ExtLayout lay(N);
+    const ExtGeom geo(N);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     ExtPartial* parts = reinterpret_cast<ExtPartial*>(ws);
-    unsigned long long* coarse = reinterpret_cast<unsigned long long*>(ws + lay.coarse_off);
+    unsigned long long* shist = reinterpret_cast<unsigned long long*>(ws + lay.hist_off);
+    unsigned long long* hist = shist + kCoarseBins;
+    unsigned* ticket = reinterpret_cast<unsigned*>(ws + lay.ticket_off);
     ExtSelect* sel = reinterpret_cast<ExtSelect*>(ws + lay.sel_off);
-    unsigned long long* sel_hist = reinterpret_cast<unsigned long long*>(ws + lay.hist_off);
-    uint32_t* keys = reinterpret_cast<uint32_t*>(ws + lay.keys_off);
+    unsigned long long* sel_hist = reinterpret_cast<unsigned long long*>(ws + lay.selhist_off);
+    uint32_t* wn = reinterpret_cast<uint32_t*>(ws + lay.wn_off);
     uint32_t* cand = reinterpret_cast<uint32_t*>(ws + lay.cand_off);
-    const int64_t cand_stride = N;
     // the clip thresholds of |exp(d) - 1| > eps, rounded to fp32 once
     const double e = static_cast<double>(eps);
     const float clip_hi = static_cast<float>(std::log1p(e));
     const float clip_lo = e < 1.0 ? static_cast<float>(std::log1p(-e)) : -INFINITY;
-    const int64_t slices = static_cast<int64_t>(audit_v3_blocks(N));
-    const unsigned blocks = static_cast<unsigned>(std::min<int64_t>(slices, kExtMaxBlocks));
-    cudaError_t err = cudaMemsetAsync(coarse, 0, kCoarseBins * sizeof(unsigned long long), stream);
+    cudaError_t err = cudaMemsetAsync(ws + lay.hist_off, 0, lay.ticket_off + 16 - lay.hist_off, stream);
     if (err != cudaSuccess) return err;
-    if (blocks > 0) {
-        if (vec_ok)
-            audit_ext_pass1<true><<<blocks, kAuditThreads, 0, stream>>>(
-                logp_new, logp_old, mask, N, clip_lo, clip_hi, parts, keys, coarse);
-        else
-            audit_ext_pass1<false><<<blocks, kAuditThreads, 0, stream>>>(
-                logp_new, logp_old, mask, N, clip_lo, clip_hi, parts, keys, coarse);
+    if (geo.slices == 0) {
+        audit_ext_merge<<<1, kMergeThreads, 0, stream>>>(parts, 0, seq_offsets, num_seqs, result,
+                                                         sel, sel_hist, wn);
+        return cudaGetLastError();
     }
-    audit_ext_merge<<<1, kMergeThreads, 0, stream>>>(parts, static_cast<int64_t>(blocks),
-                                                     seq_offsets, num_seqs, coarse, result, sel,
-                                                     sel_hist);
-    if (blocks > 0) {
-        // the candidate scan: eight blocks per SM at most (the candidate lists do not depend
-        // on the grid)
-        const unsigned cgrid = static_cast<unsigned>(std::max<int64_t>(
-            1, std::min<int64_t>((N / 4 + kAuditThreads - 1) / kAuditThreads,
-                                 8 * static_cast<int64_t>(sms > 0 ? sms : 1))));
-        audit_ext_collect<<<cgrid, kAuditThreads, 0, stream>>>(keys, N, sel, cand, cand_stride);
-        const dim3 rg(blocks, 3);
-        audit_ext_radix<0><<<rg, kAuditThreads, 0, stream>>>(sel, cand, cand_stride, sel_hist);
-        audit_ext_radix<1><<<rg, kAuditThreads, 0, stream>>>(sel, cand, cand_stride, sel_hist);
-        audit_ext_radix<2><<<rg, kAuditThreads, 0, stream>>>(sel, cand, cand_stride, sel_hist);
-        audit_ext_finish<<<1, kAuditThreads, 0, stream>>>(sel, sel_hist, result);
+    const int64_t stride = ext_sample_stride(geo.slices);
+    const unsigned sgrid = static_cast<unsigned>(
+        std::min<int64_t>((geo.slices + stride - 1) / stride, kSampleMaxBlocks));
+    const unsigned blocks = static_cast<unsigned>(geo.blocks);
+    const dim3 tb(kAuditThreads);
+    if (vec_ok)
+        audit_ext_sample<true><<<sgrid, tb, 0, stream>>>(logp_new, logp_old, mask, N, stride, shist,
+                                                         ticket, sel);
+    else
+        audit_ext_sample<false><<<sgrid, tb, 0, stream>>>(logp_new, logp_old, mask, N, stride,
+                                                          shist, ticket, sel);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    // the rest: each launch may begin while the previous one runs, and waits for it
+    // in-kernel (programmatic dependent launch)
+    auto dep = [&](auto kernel, dim3 grid, unsigned threads, auto... args) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(threads);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kernel, args...);
+    };
+#define RLK_TRY(x)                               \
+    do {                                         \
+        const cudaError_t e_ = (x);              \
+        if (e_ != cudaSuccess) return e_;        \
+    } while (0)
+    const ExtSelect* csel = sel;
+    const ExtPartial* cparts = parts;
+    const unsigned long long* chist = hist;
+    const uint32_t* cwn = wn;
+    const uint32_t* ccand = cand;
+    const unsigned long long* csh = sel_hist;
+    const int64_t nparts = geo.blocks;
+    if (vec_ok) {
+        RLK_TRY(dep(audit_ext_main<true>, dim3(blocks), kAuditThreads, logp_new, logp_old, mask, N,
+                    clip_lo, clip_hi, parts, csel, cand, wn));
+    } else {
+        RLK_TRY(dep(audit_ext_main<false>, dim3(blocks), kAuditThreads, logp_new, logp_old, mask, N,
+                    clip_lo, clip_hi, parts, csel, cand, wn));
     }
-    return cudaGetLastError();
+    RLK_TRY(dep(audit_ext_merge, dim3(1), kMergeThreads, cparts, nparts, seq_offsets, num_seqs,
+                result, sel, sel_hist, cwn));
+    if (vec_ok) {
+        RLK_TRY(dep(audit_ext_fallback_hist<true>, dim3(blocks), kAuditThreads, logp_new, logp_old,
+                    mask, N, hist, csel));
+        RLK_TRY(dep(audit_ext_fallback_collect<true>, dim3(blocks), kAuditThreads, logp_new,
+                    logp_old, mask, N, chist, sel, cand, wn));
+    } else {
+        RLK_TRY(dep(audit_ext_fallback_hist<false>, dim3(blocks), kAuditThreads, logp_new, logp_old,
+                    mask, N, hist, csel));
+        RLK_TRY(dep(audit_ext_fallback_collect<false>, dim3(blocks), kAuditThreads, logp_new,
+                    logp_old, mask, N, chist, sel, cand, wn));
+    }
+    const dim3 rgrid(blocks, 3);
+    RLK_TRY(dep(audit_ext_radix<0>, rgrid, kAuditThreads, sel, ccand, cwn, N, sel_hist));
+    RLK_TRY(dep(audit_ext_radix<1>, rgrid, kAuditThreads, sel, ccand, cwn, N, sel_hist));
+    RLK_TRY(dep(audit_ext_radix<2>, rgrid, kAuditThreads, sel, ccand, cwn, N, sel_hist));
+    RLK_TRY(dep(audit_ext_finish, dim3(1), kAuditThreads, csel, csh, result));
+#undef RLK_TRY
+    return cudaSuccess;
 }
 
 }  // namespace rlk

@@ -67,3 +67,67 @@ def test_edge_cases():
     new = torch.full((20000,), 0.125)
     new[::7] = -0.5
     _compare(new, torch.zeros(20000), None, None, 0.3)
+
+
+def _slice_scaled(n, seed, scale_of_slice):
+    """Audit inputs whose |d| in 4096-element slice s is multiplied by scale_of_slice(s)."""
+    new, old, mask = wl.audit_inputs(n, seed)
+    d = new.double() - old.double()
+    s = torch.arange(n) // 4096
+    scale = torch.tensor([scale_of_slice(int(k)) for k in range((n + 4095) // 4096)],
+                         dtype=torch.float64)[s]
+    new = (old.double() + d * scale).float()
+    return new, old, mask
+
+
+def _fallback_flags(new, old, mask, eps):
+    """Which percentiles took the exact fallback: the selection state in the workspace
+    after one call (partials 456 x 80 B, padded to 256 B; two coarse histograms of
+    4099 u64 and a 16-byte ticket, padded to 256 B; then the state, whose fallback
+    flags are three int32 at byte 48)."""
+    d = dev()
+    n = len(new)
+    ws = torch.zeros(rlk.rlk_dlogp_audit_ext_workspace_bytes(n), dtype=torch.uint8, device=d)
+    res = torch.empty(rlk.AUDIT_EXT_RESULT_BYTES, dtype=torch.uint8, device=d)
+    rlk.rlk_dlogp_audit_ext(new.to(d), old.to(d), mask.to(d), None, eps, res, ws)
+    def up(x):
+        return (x + 255) // 256 * 256
+    sel_off = up(up(456 * 80) + 2 * 4099 * 8 + 16)
+    return ws[sel_off + 48: sel_off + 60].cpu().view(torch.int32).tolist()
+
+
+def test_percentiles_where_the_sample_misrepresents_the_batch():
+    # 769 slices: the percentile windows come from every third slice (0, 3, 6, ...).
+    # (a) |d| in the sampled slices is 1e-4 times that of the others: all three ranks lie
+    # outside their windows and the exact fallback selects them.  (b) two unsampled
+    # slices (0.26 % of the tokens) hold |d| 30 times larger: the p99 rank moves out of
+    # its window, the other two stay inside theirs.  (|d| stays below about 2: exp(d)
+    # carries the fp32 rounding of d, |d| 2^-24 relative, into mean ratio0.)
+    n = 769 * 4096 - 1000
+    assert -(-n // 4096) == 769
+    new, old, mask = _slice_scaled(n, 31, lambda k: 1e-4 if k % 3 == 0 else 1.0)
+    _compare(new, old, mask, None, 0.01)
+    assert _fallback_flags(new, old, mask, 0.01) == [1, 1, 1]
+    new, old, mask = _slice_scaled(n, 32, lambda k: 30.0 if k in (1, 385) else 1.0)
+    _compare(new, old, mask, None, 0.01)
+    assert _fallback_flags(new, old, mask, 0.01) == [0, 0, 1]
+    # a representative sample: no fallback
+    new, old, mask = wl.audit_inputs(n, 34)
+    _compare(new, old, mask, None, 0.01)
+    assert _fallback_flags(new, old, mask, 0.01) == [0, 0, 0]
+
+
+def test_windows_open_to_either_side():
+    # Few tokens per sampled slice are active: some windows reach the first or the last
+    # coarse bin.  Also all active tokens equal, and a NaN among them.
+    n = 600 * 4096
+    new, old, mask = wl.audit_inputs(n, 33)
+    mask[:] = 0
+    mask[::4096] = 1
+    mask[5::9999] = 1
+    _compare(new, old, mask, None, 0.2)
+    new2 = old.clone()
+    new2[::7] += 0.5
+    _compare(new2, old, None, None, 0.2)
+    new2[12345] = float("nan")
+    _compare(new2, old, None, None, 0.2)
