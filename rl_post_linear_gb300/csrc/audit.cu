@@ -31,6 +31,7 @@
 #include <cstddef>
 #include <mutex>
 
+#include "ptx.cuh"
 #include "rlk_internal.h"
 
 namespace rlk {
@@ -174,6 +175,22 @@ struct ThreadAcc {
     uint32_t flags = 0;
 };
 
+// a - b as the 64-bit multiply-add a * one + (2^64 - b) (one = 1): the high word is
+// all ones exactly when a < b (unsigned), the low word is a - b mod 2^32.  (This
+// form of the window tests below measured faster than compares and selects.)
+__device__ __forceinline__ uint64_t sub_wide(uint32_t a, uint64_t neg_b, uint32_t one) {
+    uint64_t t;
+    asm("mad.wide.u32 %0, %1, %2, %3;" : "=l"(t) : "r"(a), "r"(one), "l"(neg_b));
+    return t;
+}
+
+// acc + m * k (low 32 bits)
+__device__ __forceinline__ uint32_t mad_lo(uint32_t m, uint32_t k, uint32_t acc) {
+    uint32_t r;
+    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(m), "r"(k), "r"(acc));
+    return r;
+}
+
 // The extended audit's terms of one slice seen by one thread: the sum of |d| and
 // the count of clipped ratios (outputs, per slice); per percentile q the count of
 // active keys below its window (running over the thread's slices).  The keys inside
@@ -183,9 +200,11 @@ struct ThreadAcc {
 struct ExtSlice {
     float sabs = 0.f;
     int clip = 0;
-    int below[3] = {0, 0, 0};
+    uint32_t below[3] = {0u, 0u, 0u};     // keys below window q, inactive elements included
     uint32_t n[3] = {0u, 0u, 0u};
     uint32_t lo[3], span[3];
+    uint64_t neg_lo[3], neg_size[3];      // 2^64 - lo, 2^64 - (span + 1)
+    uint32_t one, neg_one;                // 1 and 2^32 - 1
     float clip_lo, clip_hi;
     uint32_t* cand;
     int64_t qstride;
@@ -307,9 +326,12 @@ __device__ __forceinline__ void visit_slice(const float4 (&x)[kVec], const float
                 ext->skeys[4 * j + e][tid] = key;
 #pragma unroll
                 for (int q = 0; q < 3; ++q) {
-                    const uint32_t u = key - ext->lo[q];
-                    ext->below[q] += (u > 0u - ext->lo[q]) ? 1 : 0;
-                    inw[q] |= (u <= ext->span[q]) ? (1u << (4 * j + e)) : 0u;
+                    // below: key < lo (key 0 too: the inactive are taken off per slice);
+                    // inside: key - lo < span + 1 (key 0 wraps far above)
+                    const uint64_t t = sub_wide(key, ext->neg_lo[q], ext->one);
+                    ext->below[q] = mad_lo(static_cast<uint32_t>(t >> 32), ext->neg_one, ext->below[q]);
+                    const uint64_t v = sub_wide(static_cast<uint32_t>(t), ext->neg_size[q], ext->one);
+                    inw[q] = mad_lo(static_cast<uint32_t>(v >> 32), 0u - (1u << (4 * j + e)), inw[q]);
                 }
             }
         }
@@ -383,11 +405,12 @@ __device__ __forceinline__ void visit_slice(const float4 (&x)[kVec], const float
 template <bool VEC>
 __device__ __forceinline__ void load_slice(const float* nw, const float* od, const uint8_t* mask,
                                            int64_t N, int64_t base, float4 (&x)[kVec],
-                                           float4 (&y)[kVec], uint32_t (&m)[kVec]) {
+                                           float4 (&y)[kVec], uint32_t (&m)[kVec],
+                                           int tid = static_cast<int>(threadIdx.x)) {
     if (VEC && base + kSlice <= N) {
 #pragma unroll
         for (int j = 0; j < kVec; ++j) {
-            const int64_t i0 = base + j * (kAuditThreads * 4) + threadIdx.x * 4;
+            const int64_t i0 = base + j * (kAuditThreads * 4) + tid * 4;
             x[j] = __ldcs(reinterpret_cast<const float4*>(nw + i0));
             y[j] = __ldcs(reinterpret_cast<const float4*>(od + i0));
             m[j] = mask == nullptr ? 0x01010101u
@@ -396,7 +419,7 @@ __device__ __forceinline__ void load_slice(const float* nw, const float* od, con
     } else {
 #pragma unroll
         for (int j = 0; j < kVec; ++j) {
-            const int64_t i0 = base + j * (kAuditThreads * 4) + threadIdx.x * 4;
+            const int64_t i0 = base + j * (kAuditThreads * 4) + tid * 4;
             float xv[4], yv[4];
             uint32_t mv = 0;
 #pragma unroll
@@ -584,9 +607,9 @@ __global__ void __launch_bounds__(kMergeThreads)
 //   sample   every K-th 4096-element slice (K a function of N, 64 to 127
 //            slices in all) is counted into a coarse histogram of |d|: exact
 //            zeros, |d| below 2^-31, 128 bins per octave over [2^-31, 2), |d|
-//            from 2 up (inf and NaN included).  The last block to finish
-//            (an integer ticket) turns it into one window of keys per
-//            percentile: the bins from sample rank r - w to r + w, where r is
+//            from 2 up (inf and NaN included), by one cluster of blocks that
+//            sums its counts in distributed shared memory.  Block 0 turns
+//            them into one window of keys per percentile: the bins from sample rank r - w to r + w, where r is
 //            the percentile's rank in the sample and w six standard
 //            deviations of a sample rank plus 16.
 //   main     the base audit's slices and blocks, plus per thread the sum of
@@ -698,25 +721,40 @@ __device__ __forceinline__ SelState window_state(uint32_t lo, uint32_t hi, int64
     return st;
 }
 
-// A coarse histogram (kCoarseBins u64 counts, read through L2) held by the 256
-// threads of a block, kBinRun consecutive bins each, with the exclusive prefix
-// of each thread's run: find(r) locates the bin of 1-based rank r.
-constexpr int kBinRun = (kCoarseBins + kAuditThreads - 1) / kAuditThreads;   // 17
-
+// A coarse histogram held by the THREADS threads of a block, kRun consecutive bins
+// each, with the exclusive prefix of each thread's run: find(r) locates the bin of
+// 1-based rank r.  Loaded from u64 counts in global memory (through L2) or from
+// u32 counts in shared memory.
+template <int THREADS>
 struct BinScan {
-    unsigned long long c[kBinRun];
+    static constexpr int kRun = (kCoarseBins + THREADS - 1) / THREADS;
+    unsigned long long c[kRun];
     unsigned long long run, excl, total;
 
     __device__ void load(const unsigned long long* hist) {
-        __shared__ unsigned long long warp_sum[kAuditThreads / 32];
+#pragma unroll
+        for (int j = 0; j < kRun; ++j) {
+            const int b = threadIdx.x * kRun + j;
+            c[j] = b < kCoarseBins ? __ldcg(hist + b) : 0ull;
+        }
+        scan();
+    }
+
+    __device__ void load_shared(const uint32_t* hist) {
+#pragma unroll
+        for (int j = 0; j < kRun; ++j) {
+            const int b = threadIdx.x * kRun + j;
+            c[j] = b < kCoarseBins ? hist[b] : 0ull;
+        }
+        scan();
+    }
+
+    __device__ void scan() {
+        __shared__ unsigned long long warp_sum[THREADS / 32];
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
         run = 0;
 #pragma unroll
-        for (int j = 0; j < kBinRun; ++j) {
-            const int b = threadIdx.x * kBinRun + j;
-            c[j] = b < kCoarseBins ? __ldcg(hist + b) : 0ull;
-            run += c[j];
-        }
+        for (int j = 0; j < kRun; ++j) run += c[j];
         unsigned long long incl = run;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -728,7 +766,7 @@ struct BinScan {
         unsigned long long before = 0;
         total = 0;
 #pragma unroll
-        for (int w = 0; w < kAuditThreads / 32; ++w) {
+        for (int w = 0; w < THREADS / 32; ++w) {
             before += w < warp ? warp_sum[w] : 0ull;
             total += warp_sum[w];
         }
@@ -743,9 +781,9 @@ struct BinScan {
         unsigned long long cum = excl;
         bin = -1;
 #pragma unroll
-        for (int j = 0; j < kBinRun; ++j) {
+        for (int j = 0; j < kRun; ++j) {
             if (bin < 0) {
-                if (r <= cum + c[j]) bin = threadIdx.x * kBinRun + j;
+                if (r <= cum + c[j]) bin = threadIdx.x * kRun + j;
                 else cum += c[j];
             }
         }
@@ -790,35 +828,84 @@ __device__ void coarse_histogram(const float* nw, const float* od, const uint8_t
         if (h[i] != 0u) atomicAdd(&hist[i], static_cast<unsigned long long>(h[i]));
 }
 
-// Sample slices: every K-th, about kSampleSlices of them, one block each.
+// Sample slices: every K-th, kSampleSlices to 2 kSampleSlices - 1 of them (all of
+// them below kSampleSlices), read by one cluster of kSampleCtas blocks of
+// kSampleThreads threads: 256 threads to a slice.
 constexpr int64_t kSampleSlices = 64;
-constexpr int64_t kSampleMaxBlocks = 128;
+constexpr int kSampleCtas = 8;
+constexpr int kSampleThreads = 1024;
+constexpr int kSampleWorkers = kSampleCtas * (kSampleThreads / kAuditThreads);   // 32
 
 inline int64_t ext_sample_stride(int64_t slices) {
     return slices > kSampleSlices ? slices / kSampleSlices : 1;
 }
 
-// The sample's histogram; the last block to finish sets the windows and clears the
-// candidate counts.
+// The sample's coarse histogram: per block in shared memory, summed over the cluster
+// through distributed shared memory into block 0, which sets the windows.  On the
+// side the cluster clears the exact histogram of the fallback and the select
+// histograms (nothing reads either before this kernel has finished).
 template <bool VEC>
-__global__ void __launch_bounds__(kAuditThreads)
+__global__ void __launch_bounds__(kSampleThreads)
     audit_ext_sample(const float* __restrict__ nw, const float* __restrict__ od,
                      const uint8_t* __restrict__ mask, int64_t N, int64_t stride,
-                     unsigned long long* __restrict__ shist, unsigned* __restrict__ ticket,
+                     unsigned long long* __restrict__ hist, uint32_t* __restrict__ sel_hist,
                      ExtSelect* __restrict__ sel) {
     asm volatile("griddepcontrol.launch_dependents;");
+    __shared__ uint32_t h[kCoarseBins];       // this block's counts
+    __shared__ uint32_t sum[kCoarseBins];     // block 0: the cluster's counts
+    const uint32_t rank = cluster_ctarank();
+    for (int i = threadIdx.x; i < kCoarseBins; i += kSampleThreads) h[i] = 0u;
+    {
+        const int g = static_cast<int>(rank) * kSampleThreads + threadIdx.x;
+        constexpr int kAll = kSampleCtas * kSampleThreads;
+        for (int i = g; i < kCoarseBins; i += kAll) hist[i] = 0ull;
+        for (int i = g; i < kSelPasses * 3 * kSelBins; i += kAll) sel_hist[i] = 0u;
+    }
+    __syncthreads();
     const int64_t slices = (N + kSlice - 1) / kSlice;
-    coarse_histogram<VEC>(nw, od, mask, N, slices, stride, shist);
-    __shared__ bool s_last;
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) s_last = atomicAdd(ticket, 1u) == gridDim.x - 1;
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    BinScan bs;
-    bs.load(shist);
-    const unsigned long long sa = bs.total;           // active keys in the sample
+    const int tid = threadIdx.x % kAuditThreads;
+    const int worker = static_cast<int>(rank) * (kSampleThreads / kAuditThreads) +
+                       static_cast<int>(threadIdx.x / kAuditThreads);
+    uint32_t n_zero = 0;
+#pragma unroll 1
+    for (int64_t i = worker; i * stride < slices; i += kSampleWorkers) {
+        float4 x[kVec], y[kVec];
+        uint32_t m[kVec];
+        load_slice<VEC>(nw, od, mask, N, i * stride * kSlice, x, y, m, tid);
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+            const float xs[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
+            const float ys[4] = {y[j].x, y[j].y, y[j].z, y[j].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const bool act = ((m[j] >> (8 * e)) & 0xffu) != 0u;
+                const uint32_t bits = __float_as_uint(xs[e] - ys[e]) & 0x7fffffffu;
+                n_zero += (act && bits == 0u) ? 1u : 0u;
+                if (act && bits != 0u) atomicAdd(&h[coarse_bin_nonzero(bits)], 1u);
+            }
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) n_zero += __shfl_down_sync(0xffffffffu, n_zero, off);
+    if ((threadIdx.x & 31) == 0 && n_zero != 0u) atomicAdd(&h[kCoarseZero], n_zero);
+    cluster_sync();                           // every block's counts are complete
+    // block r sums bins r, r + kSampleCtas, ... over the cluster into block 0's `sum`
+    {
+        const uint32_t sum0 = mapa_shared(smem_u32(sum), 0);
+        for (int b = static_cast<int>(rank) * kSampleThreads + threadIdx.x; b < kCoarseBins;
+             b += kSampleCtas * kSampleThreads) {
+            const uint32_t local = smem_u32(&h[b]);
+            uint32_t t = 0u;
+#pragma unroll
+            for (int c = 0; c < kSampleCtas; ++c) t += ld_shared_cluster_u32(mapa_shared(local, c));
+            st_shared_cluster_u32(sum0 + 4u * static_cast<uint32_t>(b), t);
+        }
+    }
+    cluster_sync();                           // block 0 holds the sums; the others may leave
+    if (rank != 0) return;
+    BinScan<kSampleThreads> bs;
+    bs.load_shared(sum);
+    const unsigned long long sa = bs.total;   // active keys in the sample
     // window ends in sample ranks; an end outside [1, sa] opens the window to that side
     __shared__ int s_bin[3][2];
     if (threadIdx.x < 3) {
@@ -871,10 +958,14 @@ __global__ void __launch_bounds__(kAuditThreads, 3)
     const int64_t wr = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
     ExtSlice x;
     x.skeys = skeys;
+    x.one = (blockDim.x >> 30) | 1u;
+    x.neg_one = 0u - x.one;
 #pragma unroll
     for (int q = 0; q < 3; ++q) {
         x.lo[q] = sel->win_lo[q];
         x.span[q] = sel->win_hi[q] - x.lo[q];
+        x.neg_lo[q] = 0ull - x.lo[q];
+        x.neg_size[q] = 0ull - (static_cast<uint64_t>(x.span[q]) + 1ull);
     }
     x.clip_lo = clip_lo;
     x.clip_hi = clip_hi;
@@ -883,6 +974,7 @@ __global__ void __launch_bounds__(kAuditThreads, 3)
     RunAcc r;
     DFloat sabs{0.f, 0.f};
     int clip = 0;
+    int visited = 0;
 #pragma unroll 1
     for (int64_t sl = blockIdx.x; sl < g.slices; sl += gridDim.x) {
         const int64_t base = sl * kSlice;
@@ -891,14 +983,17 @@ __global__ void __launch_bounds__(kAuditThreads, 3)
         r.add_slice(a, base);
         sabs = df_add(sabs, DFloat{x.sabs, 0.f});
         clip += x.clip;
+        ++visited;
     }
     if (lane == 0) {
 #pragma unroll
         for (int q = 0; q < 3; ++q) wn[q * kWnStride + wr] = x.n[q];
     }
     // the block's partial: the base audit's tree, then the same tree for |d|, the clips
-    // and the counts below the windows
-    long long below[3] = {x.below[0], x.below[1], x.below[2]};
+    // and the counts below the windows (the thread's inactive elements, counted below
+    // every window as key 0, taken off)
+    const long long inactive = static_cast<long long>(visited) * kAuditV3PerThread - r.count;
+    long long below[3] = {x.below[0] - inactive, x.below[1] - inactive, x.below[2] - inactive};
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
         DFloat y;
@@ -947,12 +1042,12 @@ __global__ void __launch_bounds__(kAuditThreads, 3)
 }
 
 // One block: the fixed-order merge of the partials into the result; each
-// percentile's rank, checked against its window; clears the select histograms.
+// percentile's rank, checked against its window.
 __global__ void __launch_bounds__(kMergeThreads)
     audit_ext_merge(const ExtPartial* __restrict__ parts, int64_t num_parts,
                     const int64_t* __restrict__ seq_offsets, int64_t num_seqs,
                     rlk_audit_ext_t* __restrict__ result, ExtSelect* __restrict__ sel,
-                    unsigned long long* __restrict__ sel_hist, const uint32_t* __restrict__ wn) {
+                    const uint32_t* __restrict__ wn) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
     Acc a = empty_acc();
@@ -982,7 +1077,6 @@ __global__ void __launch_bounds__(kMergeThreads)
 #pragma unroll
         for (int q = 0; q < 3; ++q) nc[q] += wn[q * kWnStride + k];
     }
-    for (int k = threadIdx.x; k < kSelPasses * 3 * kSelBins; k += kMergeThreads) sel_hist[k] = 0ull;
     a = block_reduce<kMergeThreads>(a);
     __shared__ DFloat s_abs[kMergeThreads / 32];
     __shared__ long long s_clip[kMergeThreads / 32];
@@ -1115,7 +1209,7 @@ __global__ void __launch_bounds__(kAuditThreads, 3)
         s_bin[threadIdx.x] = -1;
         s_below[threadIdx.x] = 0ull;
     }
-    BinScan bs;
+    BinScan<kAuditThreads> bs;
     bs.load(hist);                                   // its barriers order the writes above
     for (int q = 0; q < 3; ++q) {
         int bin;
@@ -1132,6 +1226,8 @@ __global__ void __launch_bounds__(kAuditThreads, 3)
     const int64_t wr = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
     ExtSlice x;
     x.skeys = skeys;
+    x.one = (blockDim.x >> 30) | 1u;
+    x.neg_one = 0u - x.one;
     bool redo[3];
 #pragma unroll
     for (int q = 0; q < 3; ++q) {
@@ -1150,6 +1246,8 @@ __global__ void __launch_bounds__(kAuditThreads, 3)
             x.lo[q] = lo;
             x.span[q] = hi - lo;
         }
+        x.neg_lo[q] = 0ull - x.lo[q];
+        x.neg_size[q] = 0ull - (static_cast<uint64_t>(x.span[q]) + 1ull);
     }
     x.clip_lo = -INFINITY;
     x.clip_hi = INFINITY;
@@ -1170,7 +1268,7 @@ __global__ void __launch_bounds__(kAuditThreads, 3)
 // The select step after radix pass p of percentile q: the digit whose bin holds
 // the rank (an exclusive scan of the 2^bits counts, exact), appended to the known
 // bits.  Run identically by every block of the next pass and by the final step.
-__device__ void sel_step(int q, int p, const unsigned long long* __restrict__ sel_hist,
+__device__ void sel_step(int q, int p, const uint32_t* __restrict__ sel_hist,
                          SelState& st) {
     __shared__ unsigned long long warp_sum[kAuditThreads / 32];
     __shared__ uint32_t s_digit;
@@ -1184,7 +1282,7 @@ __device__ void sel_step(int q, int p, const unsigned long long* __restrict__ se
     }
     const int nb = 1 << bits;
     const int runl = nb > kAuditThreads ? nb / kAuditThreads : 1;    // 8, 4, 2 or 1
-    const unsigned long long* hq = sel_hist + (static_cast<int64_t>(p) * 3 + q) * kSelBins;
+    const uint32_t* hq = sel_hist + (static_cast<int64_t>(p) * 3 + q) * kSelBins;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     unsigned long long c[8];
     unsigned long long run = 0;
@@ -1230,16 +1328,19 @@ __device__ void sel_step(int q, int p, const unsigned long long* __restrict__ se
     __syncthreads();
 }
 
-// Radix pass p over each percentile's candidates (blockIdx.y = percentile; warp w
-// of block b reads the range warp w of block b of the main pass filled): the
-// histogram of digit p among the candidates that match the bits known so far.
-// For p > 0 every block first repeats the select step of pass p - 1; block 0
-// stores its outcome.
+// Radix pass p over each percentile's candidates (blockIdx.y = percentile): block x
+// reads the ranges of main-pass blocks x, x + R, x + 2R, ... (R = gridDim.x, one
+// wave; warp w the ranges of their warps w) and counts digit p of the candidates
+// that match the bits known so far.  For p > 0 every block first repeats the select step of
+// pass p - 1; block 0 stores its outcome.
+constexpr int kRadixBlocks = 152;
+constexpr int kRadixBatch = 8;
+
 template <int P>
 __global__ void __launch_bounds__(kAuditThreads)
     audit_ext_radix(ExtSelect* __restrict__ sel, const uint32_t* __restrict__ cand,
                     const uint32_t* __restrict__ wn, int64_t N,
-                    unsigned long long* __restrict__ sel_hist) {
+                    uint32_t* __restrict__ sel_hist) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
     const int q = blockIdx.y;
@@ -1258,31 +1359,41 @@ __global__ void __launch_bounds__(kAuditThreads)
     __syncthreads();
     const ExtGeom g(N);
     const int lane = threadIdx.x & 31;
-    const int64_t wr = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-    const int64_t n = wn[q * kWnStride + wr];
-    const uint32_t* cq = cand + q * g.qstride + wr * g.capw;
-    for (int64_t i = lane; i - lane < n; i += 32) {
-        const bool in = i < n;
-        const uint32_t b = in ? cq[i] - 1u : 0u;
-        const bool match = in && (b & kmask) == kvalue;
-        const uint32_t digit = (b >> shift) & dmask;
-        // equal digits within the warp add up in one atomic (many equal keys are common)
-        const unsigned act = __ballot_sync(0xffffffffu, match);
-        if (match) {
-            const unsigned peers = __match_any_sync(act, digit);
-            if (lane == __ffs(peers) - 1) atomicAdd(&h[digit], __popc(peers));
+    for (int64_t b = blockIdx.x; b < g.blocks; b += gridDim.x) {
+        const int64_t wr = b * kWarps + (threadIdx.x >> 5);
+        const int64_t n = wn[q * kWnStride + wr];
+        const uint32_t* cq = cand + q * g.qstride + wr * g.capw;
+        // kRadixBatch keys per lane loaded before any is counted, so their loads overlap
+        for (int64_t base = 0; base < n; base += 32 * kRadixBatch) {
+            uint32_t kk[kRadixBatch];
+#pragma unroll
+            for (int u = 0; u < kRadixBatch; ++u) {
+                const int64_t i = base + u * 32 + lane;
+                kk[u] = i < n ? cq[i] : 0u;             // 0: no key (keys start at 1)
+            }
+#pragma unroll
+            for (int u = 0; u < kRadixBatch; ++u) {
+                const uint32_t k = kk[u] - 1u;
+                const bool match = kk[u] != 0u && (k & kmask) == kvalue;
+                const uint32_t digit = (k >> shift) & dmask;
+                // equal digits within the warp add up in one atomic (many equal keys are common)
+                const unsigned act = __ballot_sync(0xffffffffu, match);
+                if (match) {
+                    const unsigned peers = __match_any_sync(act, digit);
+                    if (lane == __ffs(peers) - 1) atomicAdd(&h[digit], __popc(peers));
+                }
+            }
         }
     }
     __syncthreads();
-    unsigned long long* gh = sel_hist + (static_cast<int64_t>(P) * 3 + q) * kSelBins;
+    uint32_t* gh = sel_hist + (static_cast<int64_t>(P) * 3 + q) * kSelBins;
     for (int i = threadIdx.x; i < (1 << bits); i += kAuditThreads)
-        if (h[i] != 0u) atomicAdd(&gh[i], static_cast<unsigned long long>(h[i]));
+        if (h[i] != 0u) atomicAdd(&gh[i], h[i]);
 }
 
 // The last select step; the selected |d| bits become p50 / p90 / p99.
 __global__ void __launch_bounds__(kAuditThreads)
-    audit_ext_finish(const ExtSelect* __restrict__ sel,
-                     const unsigned long long* __restrict__ sel_hist,
+    audit_ext_finish(const ExtSelect* __restrict__ sel, const uint32_t* __restrict__ sel_hist,
                      rlk_audit_ext_t* __restrict__ result) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int q = 0; q < 3; ++q) {
@@ -1398,18 +1509,18 @@ cudaError_t launch_audit(const float* logp_new, const float* logp_old, const uin
     return cudaLaunchKernelEx(&cfg, audit_pass2, cparts, nparts, result);
 }
 
-// extended audit workspace: partials | sample histogram, exact histogram, ticket
-// (cleared by one memset) | select state | select histograms | the warps' list
-// lengths [3][kWnStride] | candidate lists [3][qstride] (uint32)
+// extended audit workspace: partials | the fallback's exact histogram | select
+// state | select histograms | the warps' list lengths [3][kWnStride] | candidate
+// lists [3][qstride] (uint32).  Nothing in it has to start at zero: the sample
+// kernel clears the two histograms.
 struct ExtLayout {
-    size_t hist_off, ticket_off, sel_off, selhist_off, wn_off, cand_off, total;
+    size_t hist_off, sel_off, selhist_off, wn_off, cand_off, total;
     explicit ExtLayout(int64_t N) {
         const ExtGeom g(N);
         hist_off = align_up(static_cast<size_t>(kExtMaxBlocks) * sizeof(ExtPartial), 256);
-        ticket_off = hist_off + 2 * kCoarseBins * sizeof(unsigned long long);
-        sel_off = align_up(ticket_off + 16, 256);
+        sel_off = align_up(hist_off + kCoarseBins * sizeof(unsigned long long), 256);
         selhist_off = align_up(sel_off + sizeof(ExtSelect), 256);
-        wn_off = align_up(selhist_off + kSelPasses * 3 * kSelBins * sizeof(unsigned long long), 256);
+        wn_off = align_up(selhist_off + kSelPasses * 3 * kSelBins * sizeof(uint32_t), 256);
         cand_off = align_up(wn_off + 3 * static_cast<size_t>(kWnStride) * 4, 256);
         total = align_up(cand_off + 3 * static_cast<size_t>(g.qstride) * 4, 256) + 256;
     }
@@ -1426,37 +1537,43 @@ cudaError_t launch_audit_ext(const float* logp_new, const float* logp_old, const
     const ExtGeom geo(N);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     ExtPartial* parts = reinterpret_cast<ExtPartial*>(ws);
-    unsigned long long* shist = reinterpret_cast<unsigned long long*>(ws + lay.hist_off);
-    unsigned long long* hist = shist + kCoarseBins;
-    unsigned* ticket = reinterpret_cast<unsigned*>(ws + lay.ticket_off);
+    unsigned long long* hist = reinterpret_cast<unsigned long long*>(ws + lay.hist_off);
     ExtSelect* sel = reinterpret_cast<ExtSelect*>(ws + lay.sel_off);
-    unsigned long long* sel_hist = reinterpret_cast<unsigned long long*>(ws + lay.selhist_off);
+    uint32_t* sel_hist = reinterpret_cast<uint32_t*>(ws + lay.selhist_off);
     uint32_t* wn = reinterpret_cast<uint32_t*>(ws + lay.wn_off);
     uint32_t* cand = reinterpret_cast<uint32_t*>(ws + lay.cand_off);
     // the clip thresholds of |exp(d) - 1| > eps, rounded to fp32 once
     const double e = static_cast<double>(eps);
     const float clip_hi = static_cast<float>(std::log1p(e));
     const float clip_lo = e < 1.0 ? static_cast<float>(std::log1p(-e)) : -INFINITY;
-    cudaError_t err = cudaMemsetAsync(ws + lay.hist_off, 0, lay.ticket_off + 16 - lay.hist_off, stream);
-    if (err != cudaSuccess) return err;
     if (geo.slices == 0) {
         audit_ext_merge<<<1, kMergeThreads, 0, stream>>>(parts, 0, seq_offsets, num_seqs, result,
-                                                         sel, sel_hist, wn);
+                                                         sel, wn);
         return cudaGetLastError();
     }
     const int64_t stride = ext_sample_stride(geo.slices);
-    const unsigned sgrid = static_cast<unsigned>(
-        std::min<int64_t>((geo.slices + stride - 1) / stride, kSampleMaxBlocks));
     const unsigned blocks = static_cast<unsigned>(geo.blocks);
-    const dim3 tb(kAuditThreads);
-    if (vec_ok)
-        audit_ext_sample<true><<<sgrid, tb, 0, stream>>>(logp_new, logp_old, mask, N, stride, shist,
-                                                         ticket, sel);
-    else
-        audit_ext_sample<false><<<sgrid, tb, 0, stream>>>(logp_new, logp_old, mask, N, stride,
-                                                          shist, ticket, sel);
-    err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
+    {
+        // the sample: one cluster
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(kSampleCtas);
+        cfg.blockDim = dim3(kSampleThreads);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = kSampleCtas;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t err =
+            vec_ok ? cudaLaunchKernelEx(&cfg, audit_ext_sample<true>, logp_new, logp_old, mask, N,
+                                        stride, hist, sel_hist, sel)
+                   : cudaLaunchKernelEx(&cfg, audit_ext_sample<false>, logp_new, logp_old, mask, N,
+                                        stride, hist, sel_hist, sel);
+        if (err != cudaSuccess) return err;
+    }
     // the rest: each launch may begin while the previous one runs, and waits for it
     // in-kernel (programmatic dependent launch)
     auto dep = [&](auto kernel, dim3 grid, unsigned threads, auto... args) {
@@ -1482,7 +1599,7 @@ cudaError_t launch_audit_ext(const float* logp_new, const float* logp_old, const
     const unsigned long long* chist = hist;
     const uint32_t* cwn = wn;
     const uint32_t* ccand = cand;
-    const unsigned long long* csh = sel_hist;
+    const uint32_t* csh = sel_hist;
     const int64_t nparts = geo.blocks;
     if (vec_ok) {
         RLK_TRY(dep(audit_ext_main<true>, dim3(blocks), kAuditThreads, logp_new, logp_old, mask, N,
@@ -1492,7 +1609,7 @@ cudaError_t launch_audit_ext(const float* logp_new, const float* logp_old, const
                     clip_lo, clip_hi, parts, csel, cand, wn));
     }
     RLK_TRY(dep(audit_ext_merge, dim3(1), kMergeThreads, cparts, nparts, seq_offsets, num_seqs,
-                result, sel, sel_hist, cwn));
+                result, sel, cwn));
     if (vec_ok) {
         RLK_TRY(dep(audit_ext_fallback_hist<true>, dim3(blocks), kAuditThreads, logp_new, logp_old,
                     mask, N, hist, csel));
@@ -1504,7 +1621,7 @@ cudaError_t launch_audit_ext(const float* logp_new, const float* logp_old, const
         RLK_TRY(dep(audit_ext_fallback_collect<false>, dim3(blocks), kAuditThreads, logp_new,
                     logp_old, mask, N, chist, sel, cand, wn));
     }
-    const dim3 rgrid(blocks, 3);
+    const dim3 rgrid(static_cast<unsigned>(std::min<int64_t>(geo.blocks, kRadixBlocks)), 3);
     RLK_TRY(dep(audit_ext_radix<0>, rgrid, kAuditThreads, sel, ccand, cwn, N, sel_hist));
     RLK_TRY(dep(audit_ext_radix<1>, rgrid, kAuditThreads, sel, ccand, cwn, N, sel_hist));
     RLK_TRY(dep(audit_ext_radix<2>, rgrid, kAuditThreads, sel, ccand, cwn, N, sel_hist));
