@@ -31,7 +31,6 @@
 #include <cstddef>
 #include <mutex>
 
-#include "ptx.cuh"
 #include "rlk_internal.h"
 
 namespace rlk {
@@ -604,13 +603,13 @@ __global__ void __launch_bounds__(kMergeThreads)
 // base audit's order-preserving keys); it is found among a small candidate set
 // that provably holds it, by an exact radix select with integer histograms.
 //
-//   sample   every K-th 4096-element slice (K a function of N, 64 to 127
-//            slices in all) is counted into a coarse histogram of |d|: exact
+//   sample   every K-th 4096-element slice (K a function of N: 128 to 255
+//            slices in all, every slice of a smaller batch) is counted into a coarse histogram of |d|: exact
 //            zeros, |d| below 2^-31, 128 bins per octave over [2^-31, 2), |d|
-//            from 2 up (inf and NaN included), by one cluster of blocks that
-//            sums its counts in distributed shared memory.  Block 0 turns
-//            them into one window of keys per percentile: the bins from sample rank r - w to r + w, where r is
-//            the percentile's rank in the sample and w six standard
+//            from 2 up (inf and NaN included).  The last block to finish
+//            (an integer ticket) turns it into one window of keys per
+//            percentile: the bins from sample rank r - w to r + w, where r is
+//            the percentile's rank in the sample and w four standard
 //            deviations of a sample rank plus 16.
 //   main     the base audit's slices and blocks, plus per thread the sum of
 //            |d|, the clip count, and per percentile the count of active keys
@@ -740,6 +739,15 @@ struct BinScan {
         scan();
     }
 
+    __device__ void load_u32(const uint32_t* hist) {          // global, through L2
+#pragma unroll
+        for (int j = 0; j < kRun; ++j) {
+            const int b = threadIdx.x * kRun + j;
+            c[j] = b < kCoarseBins ? __ldcg(hist + b) : 0ull;
+        }
+        scan();
+    }
+
     __device__ void load_shared(const uint32_t* hist) {
 #pragma unroll
         for (int j = 0; j < kRun; ++j) {
@@ -828,50 +836,46 @@ __device__ void coarse_histogram(const float* nw, const float* od, const uint8_t
         if (h[i] != 0u) atomicAdd(&hist[i], static_cast<unsigned long long>(h[i]));
 }
 
-// Sample slices: every K-th, kSampleSlices to 2 kSampleSlices - 1 of them (all of
-// them below kSampleSlices), read by one cluster of kSampleCtas blocks of
-// kSampleThreads threads: 256 threads to a slice.
-constexpr int64_t kSampleSlices = 64;
-constexpr int kSampleCtas = 8;
-constexpr int kSampleThreads = 1024;
-constexpr int kSampleWorkers = kSampleCtas * (kSampleThreads / kAuditThreads);   // 32
+// Sample slices: every K-th, kSampleSlices to 2 kSampleSlices - 1 of them (every
+// slice of a batch of fewer than 2 kSampleSlices slices), one block each.
+constexpr int64_t kSampleSlices = 128;
+// Half-width of a window in standard deviations of a sample rank (plus 16 ranks).
+// For a sample that represents the batch a rank leaves its window with probability
+// below 1e-4; the fallback then keeps the result exact.
+constexpr double kWindowSigmas = 4.0;
 
 inline int64_t ext_sample_stride(int64_t slices) {
     return slices > kSampleSlices ? slices / kSampleSlices : 1;
 }
 
-// The sample's coarse histogram: per block in shared memory, summed over the cluster
-// through distributed shared memory into block 0, which sets the windows.  On the
-// side the cluster clears the exact histogram of the fallback and the select
-// histograms (nothing reads either before this kernel has finished).
+// The sample's coarse histogram, per block in shared memory, then added to `shist`
+// (cleared before the launch); the last block to finish (an integer ticket) sets the
+// windows.  On the side the blocks clear the exact histogram of the fallback and the
+// select histograms (nothing reads either before this kernel has finished).
 template <bool VEC>
-__global__ void __launch_bounds__(kSampleThreads)
+__global__ void __launch_bounds__(kAuditThreads)
     audit_ext_sample(const float* __restrict__ nw, const float* __restrict__ od,
                      const uint8_t* __restrict__ mask, int64_t N, int64_t stride,
+                     uint32_t* __restrict__ shist, unsigned* __restrict__ ticket,
                      unsigned long long* __restrict__ hist, uint32_t* __restrict__ sel_hist,
                      ExtSelect* __restrict__ sel) {
     asm volatile("griddepcontrol.launch_dependents;");
-    __shared__ uint32_t h[kCoarseBins];       // this block's counts
-    __shared__ uint32_t sum[kCoarseBins];     // block 0: the cluster's counts
-    const uint32_t rank = cluster_ctarank();
-    for (int i = threadIdx.x; i < kCoarseBins; i += kSampleThreads) h[i] = 0u;
+    __shared__ uint32_t h[kCoarseBins];
+    for (int i = threadIdx.x; i < kCoarseBins; i += kAuditThreads) h[i] = 0u;
     {
-        const int g = static_cast<int>(rank) * kSampleThreads + threadIdx.x;
-        constexpr int kAll = kSampleCtas * kSampleThreads;
-        for (int i = g; i < kCoarseBins; i += kAll) hist[i] = 0ull;
-        for (int i = g; i < kSelPasses * 3 * kSelBins; i += kAll) sel_hist[i] = 0u;
+        const int g = blockIdx.x * kAuditThreads + threadIdx.x;
+        const int all = gridDim.x * kAuditThreads;
+        for (int i = g; i < kCoarseBins; i += all) hist[i] = 0ull;
+        for (int i = g; i < kSelPasses * 3 * kSelBins; i += all) sel_hist[i] = 0u;
     }
     __syncthreads();
     const int64_t slices = (N + kSlice - 1) / kSlice;
-    const int tid = threadIdx.x % kAuditThreads;
-    const int worker = static_cast<int>(rank) * (kSampleThreads / kAuditThreads) +
-                       static_cast<int>(threadIdx.x / kAuditThreads);
     uint32_t n_zero = 0;
 #pragma unroll 1
-    for (int64_t i = worker; i * stride < slices; i += kSampleWorkers) {
+    for (int64_t i = blockIdx.x; i * stride < slices; i += gridDim.x) {
         float4 x[kVec], y[kVec];
         uint32_t m[kVec];
-        load_slice<VEC>(nw, od, mask, N, i * stride * kSlice, x, y, m, tid);
+        load_slice<VEC>(nw, od, mask, N, i * stride * kSlice, x, y, m);
 #pragma unroll
         for (int j = 0; j < kVec; ++j) {
             const float xs[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
@@ -888,23 +892,18 @@ __global__ void __launch_bounds__(kSampleThreads)
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) n_zero += __shfl_down_sync(0xffffffffu, n_zero, off);
     if ((threadIdx.x & 31) == 0 && n_zero != 0u) atomicAdd(&h[kCoarseZero], n_zero);
-    cluster_sync();                           // every block's counts are complete
-    // block r sums bins r, r + kSampleCtas, ... over the cluster into block 0's `sum`
-    {
-        const uint32_t sum0 = mapa_shared(smem_u32(sum), 0);
-        for (int b = static_cast<int>(rank) * kSampleThreads + threadIdx.x; b < kCoarseBins;
-             b += kSampleCtas * kSampleThreads) {
-            const uint32_t local = smem_u32(&h[b]);
-            uint32_t t = 0u;
-#pragma unroll
-            for (int c = 0; c < kSampleCtas; ++c) t += ld_shared_cluster_u32(mapa_shared(local, c));
-            st_shared_cluster_u32(sum0 + 4u * static_cast<uint32_t>(b), t);
-        }
-    }
-    cluster_sync();                           // block 0 holds the sums; the others may leave
-    if (rank != 0) return;
-    BinScan<kSampleThreads> bs;
-    bs.load_shared(sum);
+    __syncthreads();
+    for (int i = threadIdx.x; i < kCoarseBins; i += kAuditThreads)
+        if (h[i] != 0u) atomicAdd(&shist[i], h[i]);
+    __shared__ bool s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    BinScan<kAuditThreads> bs;
+    bs.load_u32(shist);
     const unsigned long long sa = bs.total;   // active keys in the sample
     // window ends in sample ranks; an end outside [1, sa] opens the window to that side
     __shared__ int s_bin[3][2];
@@ -918,8 +917,9 @@ __global__ void __launch_bounds__(kSampleThreads)
         if (sa == 0ull) break;
         const double pf = pct_of(q) / 100.0;
         const long long r = static_cast<long long>((pct_of(q) * sa + 99) / 100);
-        const long long w =
-            static_cast<long long>(ceil(6.0 * sqrt(static_cast<double>(sa) * pf * (1.0 - pf)))) + 16;
+        const long long w = static_cast<long long>(
+                                ceil(kWindowSigmas * sqrt(static_cast<double>(sa) * pf * (1.0 - pf)))) +
+                            16;
         int bin;
         unsigned long long below;
         if (r - w >= 1 && bs.find(static_cast<unsigned long long>(r - w), bin, below))
@@ -1289,7 +1289,7 @@ __device__ void sel_step(int q, int p, const uint32_t* __restrict__ sel_hist,
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const int b = threadIdx.x * runl + j;
-        c[j] = (j < runl && b < nb) ? hq[b] : 0ull;
+        c[j] = (j < runl && b < nb) ? __ldcg(hq + b) : 0ull;
         run += c[j];
     }
     unsigned long long incl = run;
@@ -1509,15 +1509,18 @@ cudaError_t launch_audit(const float* logp_new, const float* logp_old, const uin
     return cudaLaunchKernelEx(&cfg, audit_pass2, cparts, nparts, result);
 }
 
-// extended audit workspace: partials | the fallback's exact histogram | select
-// state | select histograms | the warps' list lengths [3][kWnStride] | candidate
-// lists [3][qstride] (uint32).  Nothing in it has to start at zero: the sample
-// kernel clears the two histograms.
+// extended audit workspace: partials | sample histogram (u32) and ticket (cleared
+// by one memset) | the fallback's exact histogram | select state | select
+// histograms | the warps' list lengths [3][kWnStride] | candidate lists
+// [3][qstride] (uint32).  Nothing else in it has to start at zero: the sample
+// kernel clears the other two histograms.
 struct ExtLayout {
-    size_t hist_off, sel_off, selhist_off, wn_off, cand_off, total;
+    size_t shist_off, ticket_off, hist_off, sel_off, selhist_off, wn_off, cand_off, total;
     explicit ExtLayout(int64_t N) {
         const ExtGeom g(N);
-        hist_off = align_up(static_cast<size_t>(kExtMaxBlocks) * sizeof(ExtPartial), 256);
+        shist_off = align_up(static_cast<size_t>(kExtMaxBlocks) * sizeof(ExtPartial), 256);
+        ticket_off = shist_off + kCoarseBins * sizeof(uint32_t);
+        hist_off = align_up(ticket_off + 16, 256);
         sel_off = align_up(hist_off + kCoarseBins * sizeof(unsigned long long), 256);
         selhist_off = align_up(sel_off + sizeof(ExtSelect), 256);
         wn_off = align_up(selhist_off + kSelPasses * 3 * kSelBins * sizeof(uint32_t), 256);
@@ -1537,6 +1540,8 @@ cudaError_t launch_audit_ext(const float* logp_new, const float* logp_old, const
     const ExtGeom geo(N);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     ExtPartial* parts = reinterpret_cast<ExtPartial*>(ws);
+    uint32_t* shist = reinterpret_cast<uint32_t*>(ws + lay.shist_off);
+    unsigned* ticket = reinterpret_cast<unsigned*>(ws + lay.ticket_off);
     unsigned long long* hist = reinterpret_cast<unsigned long long*>(ws + lay.hist_off);
     ExtSelect* sel = reinterpret_cast<ExtSelect*>(ws + lay.sel_off);
     uint32_t* sel_hist = reinterpret_cast<uint32_t*>(ws + lay.selhist_off);
@@ -1553,27 +1558,17 @@ cudaError_t launch_audit_ext(const float* logp_new, const float* logp_old, const
     }
     const int64_t stride = ext_sample_stride(geo.slices);
     const unsigned blocks = static_cast<unsigned>(geo.blocks);
-    {
-        // the sample: one cluster
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(kSampleCtas);
-        cfg.blockDim = dim3(kSampleThreads);
-        cfg.dynamicSmemBytes = 0;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = kSampleCtas;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        const cudaError_t err =
-            vec_ok ? cudaLaunchKernelEx(&cfg, audit_ext_sample<true>, logp_new, logp_old, mask, N,
-                                        stride, hist, sel_hist, sel)
-                   : cudaLaunchKernelEx(&cfg, audit_ext_sample<false>, logp_new, logp_old, mask, N,
-                                        stride, hist, sel_hist, sel);
-        if (err != cudaSuccess) return err;
-    }
+    cudaError_t err = cudaMemsetAsync(ws + lay.shist_off, 0, lay.ticket_off + 16 - lay.shist_off, stream);
+    if (err != cudaSuccess) return err;
+    const unsigned sgrid = static_cast<unsigned>((geo.slices + stride - 1) / stride);
+    if (vec_ok)
+        audit_ext_sample<true><<<sgrid, kAuditThreads, 0, stream>>>(
+            logp_new, logp_old, mask, N, stride, shist, ticket, hist, sel_hist, sel);
+    else
+        audit_ext_sample<false><<<sgrid, kAuditThreads, 0, stream>>>(
+            logp_new, logp_old, mask, N, stride, shist, ticket, hist, sel_hist, sel);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
     // the rest: each launch may begin while the previous one runs, and waits for it
     // in-kernel (programmatic dependent launch)
     auto dep = [&](auto kernel, dim3 grid, unsigned threads, auto... args) {
@@ -1599,7 +1594,6 @@ cudaError_t launch_audit_ext(const float* logp_new, const float* logp_old, const
     const unsigned long long* chist = hist;
     const uint32_t* cwn = wn;
     const uint32_t* ccand = cand;
-    const uint32_t* csh = sel_hist;
     const int64_t nparts = geo.blocks;
     if (vec_ok) {
         RLK_TRY(dep(audit_ext_main<true>, dim3(blocks), kAuditThreads, logp_new, logp_old, mask, N,
@@ -1625,6 +1619,7 @@ cudaError_t launch_audit_ext(const float* logp_new, const float* logp_old, const
     RLK_TRY(dep(audit_ext_radix<0>, rgrid, kAuditThreads, sel, ccand, cwn, N, sel_hist));
     RLK_TRY(dep(audit_ext_radix<1>, rgrid, kAuditThreads, sel, ccand, cwn, N, sel_hist));
     RLK_TRY(dep(audit_ext_radix<2>, rgrid, kAuditThreads, sel, ccand, cwn, N, sel_hist));
+    const uint32_t* csh = sel_hist;
     RLK_TRY(dep(audit_ext_finish, dim3(1), kAuditThreads, csel, csh, result));
 #undef RLK_TRY
     return cudaSuccess;

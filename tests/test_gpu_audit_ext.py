@@ -82,9 +82,9 @@ def _slice_scaled(n, seed, scale_of_slice):
 
 def _fallback_flags(new, old, mask, eps):
     """Which percentiles took the exact fallback: the selection state in the workspace
-    after one call (partials 456 x 80 B, padded to 256 B; a coarse histogram of 4099
-    u64, padded to 256 B; then the state, whose fallback flags are three int32 at
-    byte 48)."""
+    after one call (partials 456 x 80 B, padded to 256 B; the sample's histogram of
+    4099 u32 and a 16-byte ticket, padded to 256 B; a histogram of 4099 u64, padded to
+    256 B; then the state, whose fallback flags are three int32 at byte 48)."""
     d = dev()
     n = len(new)
     ws = torch.zeros(rlk.rlk_dlogp_audit_ext_workspace_bytes(n), dtype=torch.uint8, device=d)
@@ -92,12 +92,12 @@ def _fallback_flags(new, old, mask, eps):
     rlk.rlk_dlogp_audit_ext(new.to(d), old.to(d), mask.to(d), None, eps, res, ws)
     def up(x):
         return (x + 255) // 256 * 256
-    sel_off = up(up(456 * 80) + 4099 * 8)
+    sel_off = up(up(up(456 * 80) + 4099 * 4 + 16) + 4099 * 8)
     return ws[sel_off + 48: sel_off + 60].cpu().view(torch.int32).tolist()
 
 
 def test_percentiles_where_the_sample_misrepresents_the_batch():
-    # 769 slices: the percentile windows come from every third slice (0, 3, 6, ...).
+    # 769 slices: the percentile windows come from every sixth slice (0, 6, 12, ...).
     # (a) |d| in the sampled slices is 1e-4 times that of the others: all three ranks lie
     # outside their windows and the exact fallback selects them.  (b) two unsampled
     # slices (0.26 % of the tokens) hold |d| 30 times larger: the p99 rank moves out of
