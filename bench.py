@@ -538,9 +538,10 @@ def measure_next_rows(rlk, dev, pk, warmup, steps, state):
     res["audit_ext_2p26"] = {"ms": ms, "gbs": na * 9 / (ms * 1e-3) / 1e9,
                              "frac_of_hbm": na * 9 / (ms * 1e-3) / 1e9 / hbm,
                              "bytes": na * 9,
-                             "note": "algorithmic 9 B/token; pass 1 also writes the 4-byte "
-                                     "|d| keys, which one scan reads back to collect the "
-                                     "percentiles' candidates"}
+                             "note": "algorithmic 9 B/token: the inputs are read once by the "
+                                     "main pass (plus a sample of 128 slices); the keys inside "
+                                     "the percentiles' windows (a few % of the tokens) are "
+                                     "listed and radix-selected"}
     adv = torch.randn(na, device=dev, generator=gen)
     grad = torch.empty(na, dtype=torch.float32, device=dev)
     r_loss = torch.empty(rlk.GRPO_RESULT_BYTES, dtype=torch.uint8, device=dev)

@@ -454,6 +454,8 @@ rlk_status_t rlk_grpo_clip_loss(const float* logp_new, const float* logp_old,
  * p99; ratio0 = exp(dlogp); clipfrac0; approx_kl0; active token count; and the
  * worst token's location.  Over active tokens only.
  *
+ *   N            <= RLK_AUDIT_EXT_MAX_N (RLK_ERR_UNSUPPORTED above: the
+ *                selection counts in 32 bits)
  *   seq_offsets  device int64 [num_seqs + 1] (sequence s holds tokens
  *                [seq_offsets[s], seq_offsets[s+1])), or NULL
  *   clip_eps     >= 0, finite: the ratio0 clip range of clipfrac0
@@ -461,8 +463,17 @@ rlk_status_t rlk_grpo_clip_loss(const float* logp_new, const float* logp_old,
  * The sums follow rlk_dlogp_audit's fixed blocks and trees; the percentiles
  * are exact order statistics selected with integer histograms, so the whole
  * result is bitwise reproducible for a given N.  ratio0 and the clip test
- * are evaluated in fp32.
+ * are evaluated in fp32.  The inputs are read once, plus a fixed sample of
+ * their 4096-element slices that sets each percentile's window of |d|; a
+ * window that misses its rank (a sample unlike the batch) costs two more
+ * reads of the inputs, never a different result.
+ *
+ *   workspace    rlk_dlogp_audit_ext_workspace_bytes(N) bytes (about 12 bytes
+ *                per token: room for the candidate lists), 256-aligned; its
+ *                contents need not be initialised.  Several launches on
+ *                `stream`; calls that share a workspace must not overlap.
  */
+#define RLK_AUDIT_EXT_MAX_N ((int64_t)0xffffffff)
 rlk_status_t rlk_dlogp_audit_ext(const float* logp_new, const float* logp_old,
                                  const uint8_t* active_mask, int64_t N,
                                  const int64_t* seq_offsets, int64_t num_seqs, double clip_eps,

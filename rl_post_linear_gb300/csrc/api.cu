@@ -657,7 +657,8 @@ rlk_status_t rlk_dlogp_audit_ext(const float* logp_new, const float* logp_old,
                                  const int64_t* seq_offsets, int64_t num_seqs, double clip_eps,
                                  rlk_audit_ext_t* result_dev, void* workspace,
                                  size_t workspace_bytes, cudaStream_t stream) {
-    if (N < 0 || N > (int64_t(1) << 40)) return RLK_ERR_INVALID_VALUE;
+    if (N < 0) return RLK_ERR_INVALID_VALUE;
+    if (N > RLK_AUDIT_EXT_MAX_N) return RLK_ERR_UNSUPPORTED;   // 32-bit select counts
     if (result_dev == nullptr) return RLK_ERR_INVALID_VALUE;
     if (N > 0 && (logp_new == nullptr || logp_old == nullptr)) return RLK_ERR_INVALID_VALUE;
     if (!(std::isfinite(clip_eps) && clip_eps >= 0.0)) return RLK_ERR_INVALID_VALUE;

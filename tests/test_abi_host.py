@@ -115,6 +115,15 @@ def test_backward_and_audit_argument_errors(lib):
     assert lib.rlk_dlogp_audit(None, FAKE, None, 10, FAKE, FAKE, 1 << 20, None) == \
         rlk.RLK_ERR_INVALID_VALUE
     assert lib.rlk_dlogp_audit(FAKE, FAKE, None, 10, FAKE, FAKE, 8, None) == rlk.RLK_ERR_WORKSPACE
+    # the extended audit counts its selection in 32 bits: N below 2^32
+    ext = lib.rlk_dlogp_audit_ext
+    assert ext(FAKE, FAKE, None, 1 << 32, None, 0, 0.2, FAKE, FAKE, 1 << 40, None) == \
+        rlk.RLK_ERR_UNSUPPORTED
+    assert ext(FAKE, FAKE, None, -1, None, 0, 0.2, FAKE, FAKE, 1 << 40, None) == \
+        rlk.RLK_ERR_INVALID_VALUE
+    assert ext(FAKE, FAKE, None, 10, None, 0, -0.1, FAKE, FAKE, 1 << 40, None) == \
+        rlk.RLK_ERR_INVALID_VALUE
+    assert ext(FAKE, FAKE, None, 10, None, 0, 0.2, FAKE, FAKE, 8, None) == rlk.RLK_ERR_WORKSPACE
 
 
 def test_binding_refuses_cpu_tensors(lib):
