@@ -266,16 +266,16 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
             }
             uint4* dst = reinterpret_cast<uint4*>(ds + static_cast<size_t>(i) * kLd + col);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
-                                    packed[4 * i + 3]);
+            for (int w = 0; w < 4; ++w)
+                dst[w] = make_uint4(packed[4 * w], packed[4 * w + 1], packed[4 * w + 2],
+                                    packed[4 * w + 3]);
             if constexpr (ENT) {
                 uint4* dlo = reinterpret_cast<uint4*>(ds + static_cast<size_t>(i) * kLd +
                                                       kBwdChunk + col);
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    dlo[i] = make_uint4(packed_lo[4 * i], packed_lo[4 * i + 1],
-                                        packed_lo[4 * i + 2], packed_lo[4 * i + 3]);
+                for (int w = 0; w < 4; ++w)
+                    dlo[w] = make_uint4(packed_lo[4 * w], packed_lo[4 * w + 1],
+                                        packed_lo[4 * w + 2], packed_lo[4 * w + 3]);
             }
         }
     }
