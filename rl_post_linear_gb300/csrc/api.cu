@@ -64,7 +64,8 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 // 2D bf16 tensor map, 128-byte swizzle, zero fill outside the tensor.
 rlk_status_t make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
-                      uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+                      uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                      CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (fn == nullptr) return RLK_ERR_LAUNCH;
     cuuint64_t dims[2] = {inner, outer};
@@ -72,7 +73,7 @@ rlk_status_t make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? RLK_OK : RLK_ERR_LAUNCH;
 }
@@ -135,6 +136,9 @@ static rlk_status_t bwd_chunks(rlk::BwdStepMaps& maps, rlk::BwdStep& st, void* d
         const uint64_t inner = uint64_t(width) + (st.hilo ? uint64_t(rlk::kBwdChunk) : 0);
         RLK_TRY(make_map(&maps.ds_kmajor, ds, inner, N, ld * 2, 64, rlk::kTileM));
         RLK_TRY(make_map(&maps.ds_mnmajor, ds, inner, N, ld * 2, 64, 64));
+        if (st.kl)   // the KL dS epilogue writes its tiles with TMA stores
+            RLK_TRY(make_map(&maps.ds_store, ds, inner, N, ld * 2, 32, 32,
+                             CU_TENSOR_MAP_SWIZZLE_NONE));
         st.ds = ds;
         st.chunk = c;
         for (int role : {rlk::kRoleDs, rlk::kRoleDh, rlk::kRoleDw}) {
@@ -274,11 +278,11 @@ rlk_status_t rlk_linear_kl_bwd(const void* hidden, const void* weight, const voi
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     rlk::BwdStepMaps maps;
     RLK_TRY(make_map(&maps.h_kmajor, hidden, H, N, H * 2, 64, rlk::kTileM));
-    RLK_TRY(make_map(&maps.w_kmajor, weight, H, V, H * 2, 64, rlk::kTileV));
+    RLK_TRY(make_map(&maps.w_kmajor, weight, H, V, H * 2, 64, rlk::kPairBRows));
     RLK_TRY(make_map(&maps.w_mnmajor, weight, H, V, H * 2, 64, 64));
     RLK_TRY(make_map(&maps.h_mnmajor, hidden, H, N, H * 2, 64, 64));
     RLK_TRY(make_map(&maps.hr_kmajor, hidden_ref, H_ref, N, H_ref * 2, 64, rlk::kTileM));
-    RLK_TRY(make_map(&maps.wr_kmajor, weight_ref, H_ref, V, H_ref * 2, 64, rlk::kTileV));
+    RLK_TRY(make_map(&maps.wr_kmajor, weight_ref, H_ref, V, H_ref * 2, 64, rlk::kPairBRows));
     rlk::BwdStep st{};
     st.mask = active_mask;
     st.grad = grad_kl;

@@ -297,15 +297,20 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
 // the per-chunk sorted list).  The dh and dW roles run without target terms.
 
 struct DsKlMaps {
-    CUtensorMap h, w, hr, wr;     // K-major; boxes {64,128} for h / hr, {64,256} for w / wr
+    CUtensorMap h, w, hr, wr;     // K-major; boxes {64,128} (each CTA of a pair loads 128 rows)
+    CUtensorMap ds;               // dS [N, kLd] written by TMA stores, box {32, 32}, no swizzle
 };
 
 struct DsKlPolicy {
     using Maps = DsKlMaps;
     static constexpr bool kPairTiles = true;
     static constexpr bool kKRemap = false;
-    static constexpr bool kCtaPair = false;
+    static constexpr bool kCtaPair = true;    // 256-token units on a CTA pair
     static constexpr int kEpiWarps = 8;       // two column halves per row
+    // Each epilogue warp stages its 32 rows x 32 columns of the hi and lo planes
+    // (2 KiB each) in shared memory and writes them with two TMA stores, so that
+    // the epilogue the MMA waits for issues no per-row global stores.
+    static constexpr int kEpiSmemPerWarp = 4096;
     // dS as hi / lo bf16 planes (columns [0, kBwdChunk) and [kBwdChunk, 2 kBwdChunk) of
     // each row), which the dh and dW GEMMs both consume: the KL gradient has no fp32
     // part that dominates a row, so one bf16 rounding of dS would cost as much
@@ -347,12 +352,12 @@ struct DsKlPolicy {
     __device__ int num_units() const { return num_m * num_n; }
     __device__ int tiles_in_unit(int) const { return 2; }
     __device__ void unit(int u, int& m, int& n) const {
-        grouped_unit(u, num_m, num_n, kRasterTokenRows / kTileM, m, n);
+        grouped_unit(u, num_m, num_n, kRasterTokenRows / kUnitM, m, n);
     }
     __device__ void coords(int u, int, int& a_mn, int& a_k, int& b_mn, int& b_k) const {
         int m, n;
         unit(u, m, n);
-        a_mn = m * kTileM;
+        a_mn = m * kUnitM;
         a_k = 0;
         b_mn = c0 + n * kTileV;
         b_k = 0;
@@ -366,7 +371,7 @@ struct DsKlPolicy {
     __device__ void epi_begin(int u, int row, int, EpiState& st) const {
         int m, n;
         unit(u, m, n);
-        const int t = m * kTileM + row;
+        const int t = m * kUnitM + row;
         st.live = t < N && (mask == nullptr || mask[t] != 0);
         st.lse2 = st.live ? lse[t] * kLog2e : 0.f;
         st.lse2r = st.live ? lse_ref[t] * kLog2e : 0.f;
@@ -375,17 +380,18 @@ struct DsKlPolicy {
         st.gq = (st.live && grad_rev != nullptr) ? __fdiv_rn(grad_rev[t], temp) : 0.f;
     }
 
-    __device__ void epi_pair(int u, int, int row, int half, uint32_t tp, uint32_t tr,
-                             EpiState& st) const {
+    __device__ void epi_pair(const Maps& maps, int u, int, int row, int half, uint32_t tp,
+                             uint32_t tr, EpiState& st, uint8_t* stage) const {
         int m, n;
         unit(u, m, n);
-        const int t = m * kTileM + row;
+        const int t = m * kUnitM + row;
+        const int lane = row & 31;
+        const int t0 = t - lane;                    // the warp's first row
 #pragma unroll 1
         for (int cc = half * (kTileV / 64); cc < (half + 1) * (kTileV / 64); ++cc) {
             uint32_t rp[32], rr[32];
-            tmem_load_32(tp + cc * 32, rp);
-            tmem_load_32(tr + cc * 32, rr);
-            if (t >= N) continue;
+            tmem_load_32x2(tp + cc * 32, rp, tr + cc * 32, rr);
+            // rows past N compute zeros (not live); the TMA store drops them
             const int col = n * kTileV + cc * 32;   // column inside the chunk
             const int vb = c0 + col;
             // the slice's top policy entry, if it dominates the row
@@ -429,14 +435,24 @@ struct DsKlPolicy {
                 dcoef[t] = gdom;
                 atomicOr(dom_flag, 1);   // set by many rows
             }
-            uint4* dst = reinterpret_cast<uint4*>(ds + static_cast<size_t>(t) * kLd + col);
-            uint4* dlo = reinterpret_cast<uint4*>(ds + static_cast<size_t>(t) * kLd + kBwdChunk + col);
+            // the slot is free once the previous slice's stores have read it
+            if (lane == 0) bulk_wait_group_read0();
+            __syncwarp();
+            uint4* shi = reinterpret_cast<uint4*>(stage + lane * 64);
+            uint4* slo = reinterpret_cast<uint4*>(stage + 2048 + lane * 64);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                shi[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
                                     packed[4 * i + 3]);
-                dlo[i] = make_uint4(packed_lo[4 * i], packed_lo[4 * i + 1], packed_lo[4 * i + 2],
+                slo[i] = make_uint4(packed_lo[4 * i], packed_lo[4 * i + 1], packed_lo[4 * i + 2],
                                     packed_lo[4 * i + 3]);
+            }
+            fence_proxy_async_smem();               // visible to the TMA engine
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_2d(&maps.ds, stage, col, t0);
+                tma_store_2d(&maps.ds, stage + 2048, kBwdChunk + col, t0);
+                bulk_commit_group();
             }
         }
     }
@@ -956,22 +972,17 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
         ps.N = N;
         ps.V = V;
         ps.c0 = c0;
-        ps.num_m = (N + kTileM - 1) / kTileM;
+        ps.num_m = (N + kUnitM - 1) / kUnitM;
         ps.num_n = (width + kTileV - 1) / kTileV;
         ps.kblocks = H / 64;
         ps.kblocks_r = st.H_ref / 64;
         ps.k = st.k;
         ps.kr = st.k_ref;
         ps.temp = st.temp;
-        auto kern = gemm_persistent_kernel<DsKlPolicy>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kGemmSmemBytes));
-        if (e != cudaSuccess) return e;
-        const int units = ps.num_m * ps.num_n;
-        const int grid = units < num_sms ? units : num_sms;
-        kern<<<grid, gemm_threads<DsKlPolicy>(), kGemmSmemBytes, stream>>>(
-            DsKlMaps{maps.h_kmajor, maps.w_kmajor, maps.hr_kmajor, maps.wr_kmajor}, ps, err);
-        e = cudaGetLastError();
+        const long long units = static_cast<long long>(ps.num_m) * ps.num_n;
+        const cudaError_t e = launch_persistent<DsKlPolicy>(
+            DsKlMaps{maps.h_kmajor, maps.w_kmajor, maps.hr_kmajor, maps.wr_kmajor, maps.ds_store},
+            ps, units, num_sms, err, stream);
         if (e != cudaSuccess) return e;
         return launch_dom_sort(st.dom, N, V, c0, c0 + width, st.dom_flags + st.chunk, st.tiles,
                                st.sorted_dy, st.sorted_dt, stream);

@@ -159,10 +159,15 @@ __device__ __forceinline__ uint64_t operand_desc_rt(bool mn_major, uint32_t stag
 // different operands (tile_a_map / tile_b_map / tile_k_blocks(u, q)); the
 // epilogue sees both accumulators at once (epi_pair, after the odd tile) and
 // releases the two TMEM buffers together.  Units then hold an even number of
-// tiles, so a pair always occupies buffers 0 and 1.  Pair policies may set
+// tiles, so a pair always occupies buffers 0 and 1.  Paired tiles also run on
+// CTA pairs: each CTA's epilogue warps take its 128 rows of both accumulators and
+// arrive on the leader's barriers.  Pair policies may set
 // kEpiWarps = 8: two warps per TMEM lane quarter, each given half of the
 // tile's columns (epi_begin / epi_pair / epi_end take the half), so that the
-// epilogue, which the MMA waits for, takes half as long.
+// epilogue, which the MMA waits for, takes half as long.  epi_pair also gets the
+// kernel's tensor maps and, for a policy with kEpiSmemPerWarp > 0, this warp's
+// slot of that many bytes of shared memory (after the ring), e.g. to stage a tile
+// for a TMA store; such a warp waits for its bulk stores before the CTA exits.
 // TwoMaps serves the single-role policies.
 struct TwoMaps {
     CUtensorMap a, b;
@@ -176,6 +181,7 @@ struct SingleRole {
     static constexpr bool kKRemap = false;
     static constexpr bool kCtaPair = false;
     static constexpr int kEpiWarps = 4;
+    static constexpr int kEpiSmemPerWarp = 0;
     static constexpr bool kAMn = AMN;
     static constexpr bool kBMn = BMN;
     __device__ static void prefetch(const Maps& m) {
@@ -237,8 +243,9 @@ constexpr int gemm_threads() {
 }
 
 template <class P>
-constexpr uint32_t gemm_smem_bytes() {
-    return RingShape<P::kCtaPair>::smem_bytes;
+__host__ __device__ constexpr uint32_t gemm_smem_bytes() {
+    return RingShape<P::kCtaPair>::smem_bytes +
+           static_cast<uint32_t>(P::kEpiWarps * P::kEpiSmemPerWarp);
 }
 
 template <class P>
@@ -246,7 +253,6 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1)
     gemm_persistent_kernel(const __grid_constant__ typename P::Maps maps, const P p,
                            uint32_t* err) {
     constexpr bool PAIR = P::kCtaPair;
-    static_assert(!(PAIR && P::kPairTiles), "paired-tile policies run on single CTAs");
     using Ring = RingShape<PAIR>;
     constexpr int S = Ring::stages;
     extern __shared__ uint8_t smem_raw[];
@@ -255,6 +261,8 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1)
     uint8_t* a_stages = smem;
     uint8_t* b_stages = smem + S * Ring::a_bytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Ring::stage_bytes);
+    uint8_t* epi_smem = smem + S * Ring::stage_bytes + kBarrierBytes;   // [kEpiWarps] slots
+    static_assert(gemm_smem_bytes<P>() <= 227 * 1024, "shared memory of the launch");
     uint64_t* full = bars;                    // [S] TMA -> MMA (pair: the even CTA's counts both CTAs' bytes)
     uint64_t* empty = bars + S;               // [S] MMA -> TMA
     uint64_t* tmem_full = bars + 2 * S;       // [2] MMA -> epilogue
@@ -465,7 +473,7 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1)
         for (int u = wg; ok && u < units; u += num_wg) {
             typename P::EpiState st;
             if constexpr (P::kPairTiles)
-                p.epi_begin(u, row, half, st);
+                p.epi_begin(u, prow, half, st);
             else
                 p.epi_begin(u, prow, st);
             const int nt = p.tiles_in_unit(u);
@@ -484,13 +492,19 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1)
                 if constexpr (P::kPairTiles) {
                     if ((q & 1) == 0) continue;       // hold the even tile's buffer
                     tc_fence_after();
-                    p.epi_pair(u, q, row, half, taddr_row + (buf ^ 1u) * kBN,
-                               taddr_row + buf * kBN, st);
+                    p.epi_pair(maps, u, q, prow, half, taddr_row + (buf ^ 1u) * kBN,
+                               taddr_row + buf * kBN, st,
+                               epi_smem + (warp - 2) * P::kEpiSmemPerWarp);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) {
-                        mbar_arrive(&tmem_empty[buf ^ 1u]);
-                        mbar_arrive(&tmem_empty[buf]);
+                        if constexpr (PAIR) {
+                            mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty[buf ^ 1u]), 0));
+                            mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty[buf]), 0));
+                        } else {
+                            mbar_arrive(&tmem_empty[buf ^ 1u]);
+                            mbar_arrive(&tmem_empty[buf]);
+                        }
                     }
                 } else {
                     tc_fence_after();
@@ -507,13 +521,17 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1)
             }
             if (!ok) break;
             if constexpr (P::kPairTiles)
-                p.epi_end(u, row, half, st);
+                p.epi_end(u, prow, half, st);
             else
                 p.epi_end(u, prow, st);
         }
         if (!ok && lane == 0) {
             report_error(err, RLK_DEVERR_WAIT_TIMEOUT);
             *abort_flag = 1;
+        }
+        if constexpr (P::kEpiSmemPerWarp > 0) {
+            if (lane == 0) bulk_wait_group0();   // this warp's bulk stores are done
+            __syncwarp();
         }
     }
 

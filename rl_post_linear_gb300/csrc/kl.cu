@@ -20,6 +20,11 @@
 //   (mr, sr, b) = the same for R with weights 2^((R - mr) kr) and values -d
 // and takes the target logit S[t, y_t] from the policy accumulator.  Columns
 // >= V are excluded.  At the end of a unit it writes the chunk's partials.
+// It runs on single CTAs: on CTA pairs it took 7 % fewer cycles but read the
+// two heads' weights from DRAM about 2.5 times as often (54 against 22 GB at
+// N = 8192), which under the power cap cost more than the cycles saved.  (The
+// KL backward's dS GEMM, whose weight traffic does not grow that way, runs on
+// pairs.)
 //
 // Kernel 2 (kl_merge_kernel): one thread per row merges the chunks in
 // ascending order (max, then rescaled sums) and forms KL, reverse KL, both
@@ -47,6 +52,7 @@ struct KlFwdPolicy {
     static constexpr bool kKRemap = false;
     static constexpr bool kCtaPair = false;
     static constexpr int kEpiWarps = 8;       // two column halves per row
+    static constexpr int kEpiSmemPerWarp = 0;
 
     const int64_t* targets;   // nullptr: no selected logp
     // partials per (chunk, column half, row): [num_chunks][2][N]
@@ -111,8 +117,8 @@ struct KlFwdPolicy {
         st.y = (targets != nullptr && t < N) ? targets[t] : -1;
     }
 
-    __device__ void epi_pair(int u, int q, int, int half, uint32_t tp, uint32_t tr,
-                             EpiState& st) const {
+    __device__ void epi_pair(const Maps&, int u, int q, int, int half, uint32_t tp, uint32_t tr,
+                             EpiState& st, uint8_t*) const {
         int m, c;
         unit(u, m, c);
         const int v0 = (c * kFwdTilesPerChunk + (q >> 1)) * kTileV;
@@ -121,8 +127,7 @@ struct KlFwdPolicy {
             const int vb = v0 + cc * 32;
             if (vb >= V) break;                       // same for the whole warp
             uint32_t rp[32], rr[32];
-            tmem_load_32(tp + cc * 32, rp);
-            tmem_load_32(tr + cc * 32, rr);
+            tmem_load_32x2(tp + cc * 32, rp, tr + cc * 32, rr);
             float x[32], xr[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) {

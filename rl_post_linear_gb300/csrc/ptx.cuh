@@ -160,6 +160,36 @@ __device__ __forceinline__ void tmem_load_32(uint32_t taddr, uint32_t (&r)[32]) 
                  : "memory");
 }
 
+// Two 32-column TMEM loads (e.g. the same slice of two accumulators) behind one
+// wait, so that their latencies overlap.
+__device__ __forceinline__ void tmem_load_32x2(uint32_t ta, uint32_t (&a)[32], uint32_t tb,
+                                               uint32_t (&b)[32]) {
+#define RLK_TMEM_LD(R, T)                                                                       \
+    asm volatile(                                                                               \
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "                                               \
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "               \
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];" \
+        : "=r"(R[0]), "=r"(R[1]), "=r"(R[2]), "=r"(R[3]), "=r"(R[4]), "=r"(R[5]), "=r"(R[6]),   \
+          "=r"(R[7]), "=r"(R[8]), "=r"(R[9]), "=r"(R[10]), "=r"(R[11]), "=r"(R[12]),           \
+          "=r"(R[13]), "=r"(R[14]), "=r"(R[15]), "=r"(R[16]), "=r"(R[17]), "=r"(R[18]),        \
+          "=r"(R[19]), "=r"(R[20]), "=r"(R[21]), "=r"(R[22]), "=r"(R[23]), "=r"(R[24]),        \
+          "=r"(R[25]), "=r"(R[26]), "=r"(R[27]), "=r"(R[28]), "=r"(R[29]), "=r"(R[30]),        \
+          "=r"(R[31])                                                                           \
+        : "r"(T))
+    RLK_TMEM_LD(a, ta);
+    RLK_TMEM_LD(b, tb);
+#undef RLK_TMEM_LD
+#define RLK_TMEM_TIE(R)                                                                          \
+    "+r"(R[0]), "+r"(R[1]), "+r"(R[2]), "+r"(R[3]), "+r"(R[4]), "+r"(R[5]), "+r"(R[6]),          \
+        "+r"(R[7]), "+r"(R[8]), "+r"(R[9]), "+r"(R[10]), "+r"(R[11]), "+r"(R[12]), "+r"(R[13]),  \
+        "+r"(R[14]), "+r"(R[15]), "+r"(R[16]), "+r"(R[17]), "+r"(R[18]), "+r"(R[19]),            \
+        "+r"(R[20]), "+r"(R[21]), "+r"(R[22]), "+r"(R[23]), "+r"(R[24]), "+r"(R[25]),            \
+        "+r"(R[26]), "+r"(R[27]), "+r"(R[28]), "+r"(R[29]), "+r"(R[30]), "+r"(R[31])
+    // the wait covers both loads; tying all 64 registers keeps every use behind it
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : RLK_TMEM_TIE(a), RLK_TMEM_TIE(b)::"memory");
+#undef RLK_TMEM_TIE
+}
+
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading
 // and stride byte offsets (all >> 4), descriptor version 1 at bit 46, and
 // the 128-byte swizzle mode (2) in bits 61..63.  Tiles are 1024-byte aligned,
@@ -215,6 +245,29 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t local_addr, uint32_t ra
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
     return r;
+}
+
+// TMA tiled store of a 2-D box from shared memory (completion by bulk group)
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(x), "r"(y), "r"(smem_u32(src))
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// the shared-memory sources of every committed bulk group have been read
+__device__ __forceinline__ void bulk_wait_group_read0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// every committed bulk group has completed (its writes are done)
+__device__ __forceinline__ void bulk_wait_group0() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void cluster_sync() {

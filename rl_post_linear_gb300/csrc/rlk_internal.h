@@ -187,14 +187,15 @@ inline int64_t fwd_num_chunks(int64_t V) {
 // Tensor maps of the backward launches (one role per launch).
 struct BwdStepMaps {
     CUtensorMap h_kmajor;      // hidden [N,H], box {64, 128}: A of the dS recompute
-    CUtensorMap w_kmajor;      // weight [V,H], box {64, 256}: B of the KL dS recompute
+    CUtensorMap w_kmajor;      // weight [V,H], box {64, 128}: B of the KL dS recompute (pair)
     CUtensorMap w_kmajor_pair; // weight [V,H], box {64, 128}: B of the dS recompute (CTA pair)
     CUtensorMap w_mnmajor;     // weight [V,H], box {64, 64}:  B of the dh GEMM
     CUtensorMap h_mnmajor;     // hidden [N,H], box {64, 64}:  B of the dW GEMM
     CUtensorMap ds_kmajor;     // consumed dS [N, width], box {64, 128}: A of the dh GEMM
     CUtensorMap ds_mnmajor;    // consumed dS [N, width], box {64, 64}:  A of the dW GEMM
     CUtensorMap hr_kmajor;     // KL only: reference hidden [N,Hr], box {64, 128}
-    CUtensorMap wr_kmajor;     // KL only: reference weight [V,Hr], box {64, 256}
+    CUtensorMap wr_kmajor;     // KL only: reference weight [V,Hr], box {64, 128} (pair)
+    CUtensorMap ds_store;      // KL only: dS [N, width] written by TMA stores, box {32, 32}
 };
 
 // One launch of the backward: a role (the dS recompute, the dh GEMM or the dW
