@@ -612,6 +612,25 @@ def test_audit_ext_hand_built(oracle_lib):
     assert r["argmax_index"] == w and r["argmax_seq"] == s and r["argmax_pos"] == w - offs[s]
 
 
+def test_audit_ext_ratio_and_clip_closed_forms(oracle_lib):
+    """ratio0 = exp(logp_new - logp_old) and clipfrac0 counts |ratio0 - 1| > eps ("RL-Kernel
+    integration roadmap for vime", Consistency Contract, minimum diagnostics).  With d = ln 2,
+    ln 4, ln 1/2 and 0 the ratios are 2, 4, 1/2 and 1: mean 15/8.  A reversed difference gives
+    15/16, a ratio of exp|d| gives 9/4; eps = 0.75 clips 2 tokens, while a test on |d| clips 1."""
+    o = oracle_lib
+    lnv = np.array([math.log(2.0), math.log(4.0), math.log(0.5), 0.0], np.float32)
+    for new, old in ((lnv, np.zeros(4, np.float32)), (np.zeros(4, np.float32), -lnv)):
+        r = o.dlogp_audit_ext(new, old, None, None, 0.75)
+        assert abs(r["mean_ratio"] - 1.875) < 1e-6
+        assert r["clip_count"] == 2 and r["clipfrac"] == 0.5
+        r = o.dlogp_audit_ext(new, old, None, None, 0.4)
+        assert r["clip_count"] == 3
+    # a masked-out token contributes to neither
+    r = o.dlogp_audit_ext(lnv, np.zeros(4, np.float32), np.array([1, 0, 1, 1], np.uint8), None,
+                          0.75)
+    assert abs(r["mean_ratio"] - 3.5 / 3) < 1e-6 and r["clip_count"] == 1
+
+
 def test_audit_ext_small_counts_and_masked(oracle_lib):
     o = oracle_lib
     # one active token: every percentile is that token
