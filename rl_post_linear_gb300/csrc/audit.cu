@@ -5,9 +5,10 @@
 // max_abs_dlogp is the primary metric, reported with the worst token;
 // approx_kl0 = mean(exp(dlogp) - 1 - dlogp); the active-token count.
 //
-// Pass 1: the elements are cut into 4096-element slices, and block b owns a
-// fixed run of consecutive slices (ceil(slices / 608) of them: a function of N
-// only, so that one wave of blocks covers any N).  For each slice a thread
+// Pass 1: the elements are cut into 4096-element slices, dealt round-robin to
+// G = min(slices, 608) blocks (block b takes slices b, b + G, b + 2G, ...: a
+// function of N only, so that one wave of blocks covers any N and the grid
+// sweeps the inputs front to back together).  For each slice a thread
 // issues all its loads first (4 float4 of each input and 4 mask words,
 // streaming cache hint), then handles its 16 elements without branches:
 // d = new - old in fp32 (a correctly rounded difference), its count, the
