@@ -918,8 +918,9 @@ static cudaError_t launch_dom_sort(const int* dom, int N, int V, int lo, int hi,
 
 template <class P>
 static cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const P& p, int units,
-                               int num_sms, uint32_t* err, cudaStream_t stream) {
-    return launch_persistent(TwoMaps{a, b}, p, units, num_sms, err, stream);
+                               int num_sms, uint32_t* err, cudaStream_t stream,
+                               unsigned pdl = 0) {
+    return launch_persistent(TwoMaps{a, b}, p, units, num_sms, err, stream, pdl);
 }
 
 template <bool ENT>
@@ -1024,8 +1025,10 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
         pd.temp = st.temp;
         pd.terms = !st.kl;
         pd.hilo = st.hilo;
+        // the dW GEMM that follows overlaps this one's last wave (with 6.7 waves of dh
+        // units at N = 8192, a quarter of the CTA pairs would otherwise idle for a unit)
         return launch_gemm(maps.ds_kmajor, maps.w_mnmajor, pd, pd.num_m * pd.num_n, num_sms, err,
-                           stream);
+                           stream, kPdlTrigger);
     }
     DwPolicy pw;
     pw.grad = st.grad;
@@ -1050,8 +1053,10 @@ cudaError_t launch_bwd_step(const BwdStepMaps& maps, const BwdStep& st, int num_
     pw.temp = st.temp;
     pw.terms = !st.kl;
     pw.hilo = st.hilo;
+    // dW reads dS, h and the target lists, all complete before the dh GEMM started, and
+    // writes only dW, which the dh GEMM does not touch
     return launch_gemm(maps.ds_mnmajor, maps.h_mnmajor, pw, pw.num_m * pw.num_n, num_sms, err,
-                       stream);
+                       stream, kPdlOverlap);
 }
 
 // ----------------------------------------------------------------------------- dh merge

@@ -248,10 +248,17 @@ __host__ __device__ constexpr uint32_t gemm_smem_bytes() {
            static_cast<uint32_t>(P::kEpiWarps * P::kEpiSmemPerWarp);
 }
 
+// Programmatic dependent launch between two GEMM launches that share no data:
+// kPdlTrigger lets the next launch start on SMs as this grid's CTAs finish;
+// kPdlOverlap launches a GEMM that does not wait for the previous grid to start,
+// only to end (it reads and writes nothing that grid touches).
+constexpr unsigned kPdlTrigger = 1u;
+constexpr unsigned kPdlOverlap = 2u;
+
 template <class P>
 __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1)
     gemm_persistent_kernel(const __grid_constant__ typename P::Maps maps, const P p,
-                           uint32_t* err) {
+                           uint32_t* err, unsigned pdl) {
     constexpr bool PAIR = P::kCtaPair;
     using Ring = RingShape<PAIR>;
     constexpr int S = Ring::stages;
@@ -310,6 +317,9 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1)
     if constexpr (PAIR) cluster_sync();       // the peer's barriers exist before any remote arrival
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // every CTA is resident: the next launch in the stream may be scheduled onto the
+    // SMs that this grid's CTAs leave
+    if (pdl & kPdlTrigger) asm volatile("griddepcontrol.launch_dependents;");
 
     const int units = p.num_units();
 
@@ -545,13 +555,17 @@ __global__ void __launch_bounds__(64 + 32 * P::kEpiWarps, 1)
         else
             tmem_dealloc(tmem_base, kTmemCols);
     }
+    // a launch that overlapped the previous grid ends only after that grid has, so
+    // that whatever follows in the stream sees both complete
+    if (pdl & kPdlOverlap) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // Launch of a persistent GEMM: one CTA (pair: one cluster of two) per SM (pair: per
 // two SMs) up to the number of units.
 template <class P>
 cudaError_t launch_persistent(const typename P::Maps& maps, const P& p, long long units,
-                              int num_sms, uint32_t* err, cudaStream_t stream) {
+                              int num_sms, uint32_t* err, cudaStream_t stream,
+                              unsigned pdl = 0) {
     auto kern = gemm_persistent_kernel<P>;
     constexpr uint32_t smem = gemm_smem_bytes<P>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -564,14 +578,23 @@ cudaError_t launch_persistent(const typename P::Maps& maps, const P& p, long lon
     cfg.blockDim = dim3(gemm_threads<P>());
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = P::kCtaPair ? 2 : 1;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    unsigned na = 0;
+    if (P::kCtaPair) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 2;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (pdl & kPdlOverlap) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = P::kCtaPair ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, maps, p, err);
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kern, maps, p, err, pdl);
 }
 
 }  // namespace rlk

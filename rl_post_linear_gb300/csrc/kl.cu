@@ -285,7 +285,7 @@ cudaError_t launch_kl_fwd(const CUtensorMap& map_h, const CUtensorMap& map_w,
     const long long units = static_cast<long long>(p.num_m) * p.num_chunks;
     const int grid = static_cast<int>(units < num_sms ? units : num_sms);
     kern<<<grid, gemm_threads<KlFwdPolicy>(), kGemmSmemBytes, stream>>>(
-        KlMaps{map_h, map_w, map_hr, map_wr}, p, err);
+        KlMaps{map_h, map_w, map_hr, map_wr}, p, err, 0u);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     kl_merge_kernel<<<(N + 255) / 256, 256, 0, stream>>>(
