@@ -2,7 +2,7 @@
 
 Each translation unit is compiled by its own nvcc process (in parallel), then
 linked into a shared object next to this file.  The CUDA runtime is linked
-statically, so the library needs only the driver at run time.
+statically, so the library needs only the CUDA driver library at run time.
 """
 from __future__ import annotations
 
