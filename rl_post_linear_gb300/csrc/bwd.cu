@@ -225,10 +225,16 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
             // fp32 error of p, so dom has one writer.
             int ai = 32;                              // no dominant entry in this slice
             float da = 0.f;
+            const bool full = vb + 32 <= V;           // no column of the slice is past V
             if (st.live) {
                 float cm = -INFINITY;
+                if (full) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) cm = (vb + j < V) ? fmaxf(cm, x[j]) : cm;
+                    for (int j = 0; j < 32; ++j) cm = fmaxf(cm, x[j]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) cm = (vb + j < V) ? fmaxf(cm, x[j]) : cm;
+                }
                 const float l2 = fmaf(cm, k, -st.lse2);          // log2 of the slice's top p
                 if (l2 > -0.99f) {
                     int idx = 31;
@@ -246,23 +252,44 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
             }
             uint32_t packed[16];
             uint32_t packed_lo[ENT ? 16 : 1];
+            if (full && yi == 32 && ai == 32) {
+                // the common slice: every column inside V, no target or dominant entry
+                // to patch in (the same arithmetic as below, without the selects)
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float s0 = x[2 * j];
-                const float s1 = x[2 * j + 1];
-                float c0 = st.coef, c1 = st.coef;
-                if constexpr (ENT) {
-                    c0 = fmaf(st.c2, s0, st.coef);
-                    c1 = fmaf(st.c2, s1, st.coef);
+                for (int j = 0; j < 16; ++j) {
+                    const float s0 = x[2 * j];
+                    const float s1 = x[2 * j + 1];
+                    float c0 = st.coef, c1 = st.coef;
+                    if constexpr (ENT) {
+                        c0 = fmaf(st.c2, s0, st.coef);
+                        c1 = fmaf(st.c2, s1, st.coef);
+                    }
+                    const float d0 = st.live ? c0 * ex2_approx(fmaf(s0, k, -st.lse2)) : 0.f;
+                    const float d1 = st.live ? c1 * ex2_approx(fmaf(s1, k, -st.lse2)) : 0.f;
+                    packed[j] = pack_bf16x2(d0, d1);
+                    if constexpr (ENT)
+                        packed_lo[j] = st.lo ? pack_lo_bf16x2(d0, d1, packed[j]) : 0u;
                 }
-                float d0 = (st.live && vb + 2 * j < V)
-                               ? c0 * ex2_approx(fmaf(s0, k, -st.lse2)) : 0.f;
-                float d1 = (st.live && vb + 2 * j + 1 < V)
-                               ? c1 * ex2_approx(fmaf(s1, k, -st.lse2)) : 0.f;
-                d0 = (yi == 2 * j) ? dy : ((ai == 2 * j) ? da : d0);
-                d1 = (yi == 2 * j + 1) ? dy : ((ai == 2 * j + 1) ? da : d1);
-                packed[j] = pack_bf16x2(d0, d1);
-                if constexpr (ENT) packed_lo[j] = st.lo ? pack_lo_bf16x2(d0, d1, packed[j]) : 0u;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float s0 = x[2 * j];
+                    const float s1 = x[2 * j + 1];
+                    float c0 = st.coef, c1 = st.coef;
+                    if constexpr (ENT) {
+                        c0 = fmaf(st.c2, s0, st.coef);
+                        c1 = fmaf(st.c2, s1, st.coef);
+                    }
+                    float d0 = (st.live && vb + 2 * j < V)
+                                   ? c0 * ex2_approx(fmaf(s0, k, -st.lse2)) : 0.f;
+                    float d1 = (st.live && vb + 2 * j + 1 < V)
+                                   ? c1 * ex2_approx(fmaf(s1, k, -st.lse2)) : 0.f;
+                    d0 = (yi == 2 * j) ? dy : ((ai == 2 * j) ? da : d0);
+                    d1 = (yi == 2 * j + 1) ? dy : ((ai == 2 * j + 1) ? da : d1);
+                    packed[j] = pack_bf16x2(d0, d1);
+                    if constexpr (ENT)
+                        packed_lo[j] = st.lo ? pack_lo_bf16x2(d0, d1, packed[j]) : 0u;
+                }
             }
             uint4* dst = reinterpret_cast<uint4*>(ds + static_cast<size_t>(i) * kLd + col);
 #pragma unroll
