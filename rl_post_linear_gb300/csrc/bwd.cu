@@ -423,11 +423,17 @@ struct DsKlPolicy {
             const int vb = c0 + col;
             // the slice's top policy entry, if it dominates the row
             int ai = 32;
+            const bool full = vb + 32 <= V;             // no column of the slice is past V
             if (st.live) {
                 float cm = -INFINITY;
+                if (full) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    cm = (vb + j < V) ? fmaxf(cm, __uint_as_float(rp[j])) : cm;
+                    for (int j = 0; j < 32; ++j) cm = fmaxf(cm, __uint_as_float(rp[j]));
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        cm = (vb + j < V) ? fmaxf(cm, __uint_as_float(rp[j])) : cm;
+                }
                 if (fmaf(cm, k, -st.lse2) > -0.99f) {
                     int idx = 31;
 #pragma unroll
@@ -438,24 +444,46 @@ struct DsKlPolicy {
             }
             uint32_t packed[16], packed_lo[16];
             float gdom = 0.f;                           // the dominant entry's gradient
+            if (full && ai == 32) {
+                // the common slice: every column inside V and no dominant entry (the
+                // same arithmetic as below, without the per-entry selects)
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                float d[2];
+                for (int j = 0; j < 16; ++j) {
+                    float d[2];
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float s = __uint_as_float(rp[2 * j + e]);
-                    const float r = __uint_as_float(rr[2 * j + e]);
-                    const float l2p = fmaf(s, k, -st.lse2);     // log2 p
-                    const float l2q = fmaf(r, kr, -st.lse2r);   // log2 q
-                    const float p = ex2_approx(l2p), q = ex2_approx(l2q);
-                    const float ell = (l2p - l2q) * kLn2;
-                    const float g = fmaf(st.gp * p, ell - st.kl, st.gq * (p - q));
-                    const bool is_dom = ai == 2 * j + e;        // fp32 path, not dS
-                    gdom = is_dom ? g : gdom;
-                    d[e] = (st.live && vb + 2 * j + e < V && !is_dom) ? g : 0.f;
+                    for (int e = 0; e < 2; ++e) {
+                        const float s = __uint_as_float(rp[2 * j + e]);
+                        const float r = __uint_as_float(rr[2 * j + e]);
+                        const float l2p = fmaf(s, k, -st.lse2);     // log2 p
+                        const float l2q = fmaf(r, kr, -st.lse2r);   // log2 q
+                        const float p = ex2_approx(l2p), q = ex2_approx(l2q);
+                        const float ell = (l2p - l2q) * kLn2;
+                        const float g = fmaf(st.gp * p, ell - st.kl, st.gq * (p - q));
+                        d[e] = st.live ? g : 0.f;
+                    }
+                    packed[j] = pack_bf16x2(d[0], d[1]);
+                    packed_lo[j] = pack_lo_bf16x2(d[0], d[1], packed[j]);
                 }
-                packed[j] = pack_bf16x2(d[0], d[1]);
-                packed_lo[j] = pack_lo_bf16x2(d[0], d[1], packed[j]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    float d[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float s = __uint_as_float(rp[2 * j + e]);
+                        const float r = __uint_as_float(rr[2 * j + e]);
+                        const float l2p = fmaf(s, k, -st.lse2);     // log2 p
+                        const float l2q = fmaf(r, kr, -st.lse2r);   // log2 q
+                        const float p = ex2_approx(l2p), q = ex2_approx(l2q);
+                        const float ell = (l2p - l2q) * kLn2;
+                        const float g = fmaf(st.gp * p, ell - st.kl, st.gq * (p - q));
+                        const bool is_dom = ai == 2 * j + e;        // fp32 path, not dS
+                        gdom = is_dom ? g : gdom;
+                        d[e] = (st.live && vb + 2 * j + e < V && !is_dom) ? g : 0.f;
+                    }
+                    packed[j] = pack_bf16x2(d[0], d[1]);
+                    packed_lo[j] = pack_lo_bf16x2(d[0], d[1], packed[j]);
+                }
             }
             if (ai < 32) {
                 dom[t] = vb + ai;
