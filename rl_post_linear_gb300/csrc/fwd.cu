@@ -136,19 +136,20 @@ struct FwdPolicyT : SingleRole<false, false> {   // h [N,H] and W [V,H]: K-major
             for (int j = 1; j < 32; ++j) cm = fmaxf(cm, x[j]);
             const float nm = fmaxf(st.m, cm);
             const float rescale = ex2_approx((st.m - nm) * k);
+            const float nmk = nm * k;                 // each exponent: one fma, x k - m k
             float acc = st.s * rescale;
             if constexpr (ENT) {
                 float aa = st.a * rescale;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    const float e = ex2_approx((x[j] - nm) * k);
+                    const float e = ex2_approx(fmaf(x[j], k, -nmk));
                     acc += e;
                     aa = fmaf(e, x[j], aa);
                 }
                 st.a = aa;
             } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) acc += ex2_approx((x[j] - nm) * k);
+                for (int j = 0; j < 32; ++j) acc += ex2_approx(fmaf(x[j], k, -nmk));
             }
             st.s = acc;
             st.m = nm;

@@ -163,14 +163,17 @@ struct KlFwdPolicy {
         }
         const float nm = fmaxf(st.m, cm), nmr = fmaxf(st.mr, cmr);
         const float sc = ex2_approx((st.m - nm) * k), scr = ex2_approx((st.mr - nmr) * kr);
+        const float nmk = __fmul_rn(nm, k), nmrk = __fmul_rn(nmr, kr);
         float s = st.s * sc, a = st.a * sc, sr = st.sr * scr, b = st.b * scr;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             if (FULL || j < nv) {
-                // two rounded products, so that identical heads give d = 0 exactly
-                const float d = __fmul_rn(x[j], k) - __fmul_rn(xr[j], kr);
-                const float e = ex2_approx((x[j] - nm) * k);
-                const float er = ex2_approx((xr[j] - nmr) * kr);
+                // two rounded products, so that identical heads give d = 0 exactly; the
+                // exponents reuse them (x k - m k)
+                const float xk = __fmul_rn(x[j], k), xrk = __fmul_rn(xr[j], kr);
+                const float d = xk - xrk;
+                const float e = ex2_approx(xk - nmk);
+                const float er = ex2_approx(xrk - nmrk);
                 s += e;
                 a = fmaf(e, d, a);
                 sr += er;
