@@ -229,8 +229,7 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
             if (st.live) {
                 float cm = -INFINITY;
                 if (full) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) cm = fmaxf(cm, x[j]);
+                    cm = fmaxf(cm, max32(x));
                 } else {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) cm = (vb + j < V) ? fmaxf(cm, x[j]) : cm;
@@ -252,9 +251,10 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
             }
             uint32_t packed[16];
             uint32_t packed_lo[ENT ? 16 : 1];
-            if (full && yi == 32 && ai == 32) {
-                // the common slice: every column inside V, no target or dominant entry
-                // to patch in (the same arithmetic as below, without the selects)
+            if (full && yi == 32 && ai == 32 && st.live) {
+                // the common slice: a live row, every column inside V, no target or
+                // dominant entry to patch in (the same arithmetic as below, without the
+                // selects)
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const float s0 = x[2 * j];
@@ -264,8 +264,8 @@ struct DsPolicyT : SingleRole<false, false> {   // h [N,H], W [V,H]: K-major
                         c0 = fmaf(st.c2, s0, st.coef);
                         c1 = fmaf(st.c2, s1, st.coef);
                     }
-                    const float d0 = st.live ? c0 * ex2_approx(fmaf(s0, k, -st.lse2)) : 0.f;
-                    const float d1 = st.live ? c1 * ex2_approx(fmaf(s1, k, -st.lse2)) : 0.f;
+                    const float d0 = c0 * ex2_approx(fmaf(s0, k, -st.lse2));
+                    const float d1 = c1 * ex2_approx(fmaf(s1, k, -st.lse2));
                     packed[j] = pack_bf16x2(d0, d1);
                     if constexpr (ENT)
                         packed_lo[j] = st.lo ? pack_lo_bf16x2(d0, d1, packed[j]) : 0u;
@@ -392,6 +392,7 @@ struct DsKlPolicy {
 
     struct EpiState {
         float lse2, lse2r, kl, gp, gq;
+        float gpl, gpk;            // gp ln 2 and gp KL: g = p (gpl (l2p - l2q) - gpk) + gq (p - q)
         bool live;
     };
 
@@ -405,6 +406,8 @@ struct DsKlPolicy {
         st.kl = (st.live && grad != nullptr) ? kl[t] : 0.f;
         st.gp = (st.live && grad != nullptr) ? __fdiv_rn(grad[t], temp) : 0.f;
         st.gq = (st.live && grad_rev != nullptr) ? __fdiv_rn(grad_rev[t], temp) : 0.f;
+        st.gpl = st.gp * kLn2;
+        st.gpk = st.gp * st.kl;
     }
 
     __device__ void epi_pair(const Maps& maps, int u, int, int row, int half, uint32_t tp,
@@ -427,8 +430,10 @@ struct DsKlPolicy {
             if (st.live) {
                 float cm = -INFINITY;
                 if (full) {
+                    float xp[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) cm = fmaxf(cm, __uint_as_float(rp[j]));
+                    for (int j = 0; j < 32; ++j) xp[j] = __uint_as_float(rp[j]);
+                    cm = fmaxf(cm, max32(xp));
                 } else {
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
@@ -444,9 +449,11 @@ struct DsKlPolicy {
             }
             uint32_t packed[16], packed_lo[16];
             float gdom = 0.f;                           // the dominant entry's gradient
-            if (full && ai == 32) {
-                // the common slice: every column inside V and no dominant entry (the
-                // same arithmetic as below, without the per-entry selects)
+            if (full && ai == 32 && st.live) {
+                // the common slice: a live row, every column inside V and no dominant
+                // entry; the gradient grouped as p (gp ln2 (log2 p - log2 q) - gp KL) +
+                // gq (p - q), two operations fewer an entry than below (identical heads
+                // still give exactly 0)
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     float d[2];
@@ -457,9 +464,8 @@ struct DsKlPolicy {
                         const float l2p = fmaf(s, k, -st.lse2);     // log2 p
                         const float l2q = fmaf(r, kr, -st.lse2r);   // log2 q
                         const float p = ex2_approx(l2p), q = ex2_approx(l2q);
-                        const float ell = (l2p - l2q) * kLn2;
-                        const float g = fmaf(st.gp * p, ell - st.kl, st.gq * (p - q));
-                        d[e] = st.live ? g : 0.f;
+                        const float tt = fmaf(st.gpl, l2p - l2q, -st.gpk);
+                        d[e] = fmaf(p, tt, st.gq * (p - q));
                     }
                     packed[j] = pack_bf16x2(d[0], d[1]);
                     packed_lo[j] = pack_lo_bf16x2(d[0], d[1], packed[j]);

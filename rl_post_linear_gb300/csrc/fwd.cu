@@ -131,9 +131,7 @@ struct FwdPolicyT : SingleRole<false, false> {   // h [N,H] and W [V,H]: K-major
                 st.sy = select32(x, static_cast<int>(dy));
                 st.found = true;
             }
-            float cm = x[0];
-#pragma unroll
-            for (int j = 1; j < 32; ++j) cm = fmaxf(cm, x[j]);
+            const float cm = max32(x);
             const float nm = fmaxf(st.m, cm);
             const float rescale = ex2_approx((st.m - nm) * k);
             const float nmk = nm * k;                 // each exponent: one fma, x k - m k

@@ -154,11 +154,16 @@ struct KlFwdPolicy {
     __device__ __forceinline__ void fold(const float (&x)[32], const float (&xr)[32], int nv,
                                          EpiState& st) const {
         float cm = -INFINITY, cmr = -INFINITY;
+        if constexpr (FULL) {
+            cm = fmaxf(cm, max32(x));
+            cmr = fmaxf(cmr, max32(xr));
+        } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            if (FULL || j < nv) {
-                cm = fmaxf(cm, x[j]);
-                cmr = fmaxf(cmr, xr[j]);
+            for (int j = 0; j < 32; ++j) {
+                if (j < nv) {
+                    cm = fmaxf(cm, x[j]);
+                    cmr = fmaxf(cmr, xr[j]);
+                }
             }
         }
         const float nm = fmaxf(st.m, cm), nmr = fmaxf(st.mr, cmr);
