@@ -415,7 +415,9 @@ def measure_next_rows(rlk, dev, pk, warmup, steps, state):
     """The rows built after the hot path, each timed alone on the Qwen-shaped batch (or at
     N = 2^26 for the per-token fragments), against the roofline that bounds it:
     the vocab-sharded forward (TP = 4 emulated on one GPU: four block launches and the
-    fixed-order merge, checked bitwise against the unsharded logp), the entropy forward and
+    fixed-order merge, checked bitwise against the unsharded logp) and backward (four block
+    backwards and the dh merge), the data-parallel backward of four emulated ranks (fp32 dW
+    partials and their rank-order merge), the entropy forward and
     backward, logp from existing fp32 / bf16 logits [8192, 151936], the extended audit and
     the clipped-ratio loss fragment."""
     from rl_post_linear_gb300 import tp
@@ -454,6 +456,66 @@ def measure_next_rows(rlk, dev, pk, warmup, steps, state):
                                                        logp_ref.view(torch.int32))),
         "launches": len(shards) + 1}
     del partials
+
+    # NEXT-1 backward: TP = 4 emulated (each vocab block's fp32 dh partial and its rows of
+    # dW, then the fixed-order dh merge); the dW rows are bitwise the unsharded ones
+    lse_m = torch.empty_like(logp_ref)
+    rlk.rlk_linear_logp_fwd(hid, wt, y, mask, T, logp_ref, lse_m, ws_f)
+    dh_parts = torch.empty(len(shards), n, h, dtype=torch.float32, device=dev)
+    dw4, dh4 = torch.empty_like(wt), torch.empty_like(hid)
+    ws_s = torch.empty(max(256, max(rlk.rlk_linear_logp_bwd_workspace_bytes(n, h, size)
+                                    for _, size in shards)), dtype=torch.uint8, device=dev)
+
+    def tp_bwd():
+        for r, (start, size) in enumerate(shards):
+            rlk.rlk_linear_logp_bwd_shard(hid, wt[start:start + size], y, mask, g, lse_m, start,
+                                          v, T, dh_parts[r], dw4[start:start + size], ws_s)
+        rlk.rlk_linear_logp_dh_merge(dh_parts, dh4)
+
+    ms = _time_calls(tp_bwd, warmup, steps, stream)
+    rlk.rlk_linear_logp_bwd(hid, wt, y, mask, g, lse_m, T, dh, dw, ws_b)
+    torch.cuda.synchronize()
+    res["tp4_emulated_bwd"] = {
+        "ms": ms, "tflops": bwd_flops / (ms * 1e-3) / 1e12,
+        "frac_of_peak": bwd_flops / (ms * 1e-3) / 1e12 / peak,
+        "dw_bitwise_equal_to_unsharded": bool(torch.equal(dw4.view(torch.int16),
+                                                          dw.view(torch.int16))),
+        "dh_rel_diff_to_unsharded": float((dh4.float() - dh.float()).norm()
+                                          / dh.float().norm())}
+    del dh_parts, dw4, dh4, ws_s
+
+    # Section 8(e): data parallelism over tokens emulated as 4 ranks of N/4 tokens, each an
+    # unrounded fp32 dW partial, then the rank-order merge (reads 4 V H fp32, writes V H bf16)
+    splits = [0, n // 4, n // 2, 3 * n // 4, n]
+    parts = torch.empty(4, v, h, dtype=torch.float32, device=dev)
+    dh_d, dw_d = torch.empty_like(hid), torch.empty_like(wt)
+    ws_d = torch.empty(max(rlk.rlk_linear_logp_bwd_workspace_bytes(splits[r + 1] - splits[r], h, v)
+                           for r in range(4)), dtype=torch.uint8, device=dev)
+
+    def dp_partials():
+        for r in range(4):
+            a, b = splits[r], splits[r + 1]
+            rlk.rlk_linear_logp_bwd_dw_partial(hid[a:b], wt, y[a:b], mask[a:b], g[a:b],
+                                               lse_m[a:b], T, dh_d[a:b], parts[r], ws_d)
+
+    def dp_bwd():
+        dp_partials()
+        rlk.rlk_linear_logp_dw_merge(parts, dw_d)
+
+    ms = _time_calls(dp_bwd, warmup, steps, stream)
+    ms_m = _time_calls(lambda: rlk.rlk_linear_logp_dw_merge(parts, dw_d), warmup, steps, stream)
+    merge_bytes = 4 * v * h * 4 + v * h * 2
+    res["dp4_emulated_bwd"] = {
+        "ms": ms, "tflops": bwd_flops / (ms * 1e-3) / 1e12,
+        "frac_of_peak": bwd_flops / (ms * 1e-3) / 1e12 / peak,
+        "merge_ms": ms_m, "merge_gbs": merge_bytes / (ms_m * 1e-3) / 1e9,
+        "merge_frac_of_hbm": merge_bytes / (ms_m * 1e-3) / 1e9 / hbm,
+        "dw_rel_diff_to_whole_batch": float((dw_d.float() - dw.float()).norm()
+                                            / dw.float().norm()),
+        "note": "4 emulated ranks of N/4 tokens; fp32 partials 4 V H (9.96 GB) merged in rank "
+                "order, rounded once"}
+    del parts, dh_d, dw_d, ws_d
+    torch.cuda.empty_cache()
 
     # NEXT-3: entropy forward and backward
     ent = torch.empty_like(logp_ref)
